@@ -1,0 +1,453 @@
+"""Pins of the CPU oracle against facts that the pages or mathematics fix.
+
+Nothing here calls the CUDA library.  Each test names the fact it checks and
+the kind of mistake it catches.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import qmm_synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ---------------------------------------------------------------------------
+# An independent Python reading of the block layouts (written from the field
+# description, not from the C oracle): used to cross-check unpacking.
+# ---------------------------------------------------------------------------
+
+def py_f16(bits):
+    return np.asarray(bits, dtype=np.uint16).view(np.float16).astype(np.float32)
+
+
+def py_decode_q8_0(row: np.ndarray, K: int):
+    blocks = row.reshape(K // 32, 34)
+    d = py_f16(blocks[:, 0].astype(np.uint16) | (blocks[:, 1].astype(np.uint16) << 8))
+    q = blocks[:, 2:].view(np.int8).astype(np.int64)
+    return d, q
+
+
+def py_decode_q8_k(row: np.ndarray, K: int):
+    blocks = row.reshape(K // 256, 292)
+    d = blocks[:, 0:4].copy().view(np.float32).ravel()
+    q = blocks[:, 4:260].view(np.int8).astype(np.int64)
+    bs = blocks[:, 260:292].copy().view(np.int16).astype(np.int64)
+    return d, q, bs
+
+
+def py_decode_q4_k(row: np.ndarray, K: int):
+    blocks = row.reshape(K // 256, 144)
+    D = py_f16(blocks[:, 0].astype(np.uint16) | (blocks[:, 1].astype(np.uint16) << 8))
+    Dm = py_f16(blocks[:, 2].astype(np.uint16) | (blocks[:, 3].astype(np.uint16) << 8))
+    sc = np.zeros((K // 256, 8), np.int64)
+    mn = np.zeros((K // 256, 8), np.int64)
+    s = blocks[:, 4:16].astype(np.int64)
+    for j in range(8):
+        if j < 4:
+            sc[:, j] = s[:, j] & 63
+            mn[:, j] = s[:, j + 4] & 63
+        else:
+            sc[:, j] = (s[:, j + 4] & 0xF) | ((s[:, j - 4] >> 6) << 4)
+            mn[:, j] = (s[:, j + 4] >> 4) | ((s[:, j] >> 6) << 4)
+    qs = blocks[:, 16:].astype(np.int64)          # [nsb, 128]
+    q = np.zeros((K // 256, 256), np.int64)
+    for c in range(4):
+        q[:, 64 * c: 64 * c + 32] = qs[:, 32 * c: 32 * c + 32] & 0xF
+        q[:, 64 * c + 32: 64 * c + 64] = qs[:, 32 * c: 32 * c + 32] >> 4
+    return D, Dm, sc, mn, q
+
+
+# ---------------------------------------------------------------------------
+# f16 conversion
+# ---------------------------------------------------------------------------
+
+@pytest.mark.slow
+def test_f16_exhaustive_against_compiler_cast(orc):
+    """All 2^32 f32 bit patterns: the oracle's hand-written f32->f16 (RNE with
+    subnormals) equals the compiler's _Float16 conversion."""
+    step = 1 << 28
+    bad = sum(orc.f16_check_range(lo, lo + step) for lo in range(0, 1 << 32, step))
+    assert bad == 0
+
+
+def test_f16_against_numpy(orc):
+    """A second independent reference: numpy's float16 conversion, on random
+    bit patterns and on every half value (f16 -> f32 is exact)."""
+    rng = np.random.default_rng(3)
+    bits = rng.integers(0, 1 << 32, size=1 << 21, dtype=np.uint64).astype(np.uint32)
+    x = bits.view(np.float32)
+    finite = np.isfinite(x)
+    with np.errstate(over="ignore"):
+        ref = x[finite].astype(np.float16).view(np.uint16)
+    got = orc.f32_to_f16_bits(x[finite])
+    assert np.array_equal(got, ref)
+    allh = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    f = orc.f16_bits_to_f32(allh)
+    ref32 = allh.view(np.float16).astype(np.float32)
+    assert (np.isnan(ref32) == np.isnan(f)).all()
+    fin = ~np.isnan(ref32)
+    assert np.array_equal(f[fin].view(np.uint32), ref32[fin].view(np.uint32))
+
+
+# ---------------------------------------------------------------------------
+# Sizes printed on the pages
+# ---------------------------------------------------------------------------
+
+def test_block_bytes_match_page_tensor_sizes(orc):
+    """Per-tensor byte counts printed on the pages fix 34 B per 32 values
+    (Q8_0) and 144 B per 256 values (Q4K)."""
+    g = json.load(open(os.path.join(GOLDEN, "page_sizes.json")))
+    for e in g["tensor_groups"]:
+        if e["type"] not in ("q8_0", "q4_k"):
+            continue
+        N, K = e["shape"]
+        assert e["tensors"] * N * orc.row_bytes(e["type"], K) == e["bytes"], e["what"]
+
+
+def test_file_sizes_close_with_block_bytes(orc):
+    """Whole-file sizes on the pages: every own file = header + 61 F32 norms
+    + its matrices at the type's bytes per value, with ONE header size for all
+    of them; Q8_0 and Q4K bytes come from the oracle, Q5_0 from a per-tensor
+    size, Q4_0 at 18/32; Q6K at 210 B / 256 closes the downloaded Q4_K_M."""
+    g = json.load(open(os.path.join(GOLDEN, "page_sizes.json")))
+    files = {e["what"]: e["bytes"] for e in g["files"]}
+    q5 = next(e for e in g["tensor_groups"] if e["type"] == "q5_0" and e["shape"] == [192, 576])
+    q5_bpv = q5["bytes"] / (q5["tensors"] * 192 * 576)               # 22 / 32
+    q8_bpv = orc.block_bytes("q8_0") / orc.block_values("q8_0")
+    q4k_bpv = orc.block_bytes("q4_k") / orc.block_values("q4_k")
+    lin = qmm_synth.smollm2_linears()[:-1]                            # 210 layer linears
+    emb = qmm_synth.VOCAB * qmm_synth.HIDDEN                          # token_embd (lm_head is tied)
+    norms = g["f32_norm_tensors"]["value"] * qmm_synth.HIDDEN * 4
+    vals = sum(n * k for _, n, k in lin) + emb
+    header = files["own F32 GGUF"] - norms - 4 * vals
+    assert 0 < header < 65536
+    assert header + norms + vals * q8_bpv == files["own Q8_0 GGUF"]
+    assert header + norms + vals * 18 / 32 == files["own Q4_0 GGUF"]
+    down = [(n, k) for name, n, k in lin if "ffn_down" in name]
+    other = vals - sum(n * k for n, k in down)
+    assert header + norms + sum(n * k for n, k in down) * q4k_bpv + other * q5_bpv == \
+        files["own Q4K GGUF (ffn_down Q4K, other matrices Q5_0)"]
+    meta = g["metadata_difference_bytes"]["value"]
+    assert files["own Q8_0 GGUF"] + meta == files["downloaded Q8_0 GGUF"]
+    # downloaded Q4_K_M: token_embd Q8_0; ffn_down 16 Q4K + 14 Q6K; attn_v 16 Q5_0 + 14 Q8_0; rest Q5_0
+    size = header + meta + norms + emb * q8_bpv
+    size += 16 * 576 * 1536 * q4k_bpv + 14 * 576 * 1536 * 210 / 256
+    size += 16 * 192 * 576 * q5_bpv + 14 * 192 * 576 * q8_bpv
+    rest = [(n, k) for name, n, k in lin if not ("ffn_down" in name or "attn_v" in name)]
+    size += sum(n * k for n, k in rest) * q5_bpv
+    assert size == files["downloaded Q4_K_M GGUF"]
+
+
+def test_row_bytes_rejects_ragged_K(orc):
+    """K-quants need K divisible by 256 (the Q4K shape error for 576-wide rows)."""
+    with pytest.raises(ValueError):
+        orc.row_bytes("q4_k", 576)
+    assert orc.row_bytes("q8_0", 576) == 612
+
+
+# ---------------------------------------------------------------------------
+# Q8_0 / Q8K quantization
+# ---------------------------------------------------------------------------
+
+def test_q8_0_scale_rule_and_codes(orc):
+    """Scale d = max|x|/127 (no freedom); the extreme value gets code +-127;
+    every code is the nearest integer to x/d (up to the f32 reciprocal's
+    rounding) and lies in [-127, 127]; an all-zero block has codes 0."""
+    x = np.concatenate([qmm_synth.weights(64, 576), qmm_synth.special_block_rows(576)])
+    q = orc.quantize("q8_0", x)
+    for r in range(x.shape[0]):
+        d16, codes = py_decode_q8_0(q[r], 576)
+        blocks = x[r].reshape(-1, 32).astype(np.float32)
+        amax = np.abs(blocks).max(axis=1)
+        d = amax / np.float32(127.0)
+        assert np.array_equal(d16.astype(np.float16).view(np.uint16), d.astype(np.float16).view(np.uint16))
+        assert np.abs(codes).max() <= 127
+        nz = amax > 0
+        ext = np.abs(codes[nz][np.arange(nz.sum()), np.abs(blocks[nz]).argmax(axis=1)])
+        assert (ext == 127).all()
+        ratio = blocks[nz].astype(np.float64) / d[nz, None].astype(np.float64)
+        assert (np.abs(codes[nz] - ratio) <= 0.5 + 1e-4).all()
+        assert (codes[~nz] == 0).all()
+
+
+def test_q8_0_requantize_is_idempotent(orc):
+    """quantize(dequantize(q)) reproduces q byte for byte: the scale rule has
+    no freedom, so re-quantizing already-quantized weights is a fixed point
+    (the byte-identical own vs downloaded Q8_0 files)."""
+    x = qmm_synth.weights(96, 1536)
+    q = orc.quantize("q8_0", x)
+    w = orc.dequantize("q8_0", q, 1536)
+    assert np.array_equal(orc.quantize("q8_0", w), q)
+
+
+def test_q8_k_fields(orc):
+    """Q8K: f32 d = max|x|/127, int8 codes within +-0.5 of x/d, bsums equal
+    the sums of 16 consecutive codes."""
+    x = np.concatenate([qmm_synth.activations(8, 1536), qmm_synth.special_block_rows(1536)])
+    q = orc.quantize("q8_k", x)
+    for r in range(x.shape[0]):
+        d, codes, bs = py_decode_q8_k(q[r], 1536)
+        blocks = x[r].reshape(-1, 256)
+        assert np.array_equal(d, np.abs(blocks).max(axis=1) / np.float32(127.0))
+        assert np.array_equal(bs, codes.reshape(-1, 16, 16).sum(axis=2))
+        ok = d > 0
+        assert (np.abs(codes[ok] - blocks[ok].astype(np.float64) / d[ok, None]) <= 0.5 + 1e-4).all()
+        assert (codes[~ok] == 0).all()
+
+
+# ---------------------------------------------------------------------------
+# Round-trip bounds
+# ---------------------------------------------------------------------------
+
+def test_round_trip_bounds(orc):
+    """Per element |x - dequant(quant(x))|, with slack 2^-20 amax for the f32
+    reciprocal and products:  Q8_0 <= d/2 + 127|d - f16(d)| + 2^-20 amax;
+    Q8K <= d/2 + 2^-20 amax;  Q4_K interior points <= e_j/2 + 2^-20 (|x| +
+    15 e_j); all Q4_K points <= e_j/2 + 7.97 d + 0.531 dmin + 2^-20 (hi -
+    lo + |x|) in the normal f16 range (|sc d - s| <= d/2 and |f(D) - d| <=
+    2^-11 d give |e - s| <= 0.531 d; the same for the offset); with the f16
+    subnormal spacing the f16 error is max(2^-11 d, 2^-25)."""
+    K = 1536
+    x = np.concatenate([qmm_synth.weights(64, K), qmm_synth.special_block_rows(K)]).astype(np.float32)
+    # Q8_0
+    q = orc.quantize("q8_0", x)
+    w = orc.dequantize("q8_0", q, K)
+    b = x.reshape(-1, 32).astype(np.float64)
+    amax = np.abs(b).max(axis=1, keepdims=True)
+    d = amax / 127.0
+    d16 = np.asarray([py_decode_q8_0(q[r], K)[0] for r in range(x.shape[0])]).reshape(-1, 1).astype(np.float64)
+    bound = d / 2 + 127 * np.abs(d - d16) + 2.0 ** -20 * amax
+    assert (np.abs(b - w.reshape(-1, 32)) <= bound).all()
+    # Q8K
+    q = orc.quantize("q8_k", x)
+    w = orc.dequantize("q8_k", q, K)
+    b = x.reshape(-1, 256).astype(np.float64)
+    amax = np.abs(b).max(axis=1, keepdims=True)
+    assert (np.abs(b - w.reshape(-1, 256)) <= amax / 254.0 + 2.0 ** -20 * amax).all()
+    # Q4_K
+    q = orc.quantize("q4_k", x)
+    w = orc.dequantize("q4_k", q, K).astype(np.float64)
+    for r in range(x.shape[0]):
+        D, Dm, sc, mn, codes = py_decode_q4_k(q[r], K)
+        xs = x[r].reshape(-1, 8, 32).astype(np.float64)
+        ws = w[r].reshape(-1, 8, 32)
+        e = (D[:, None].astype(np.float64) * sc)[:, :, None]
+        o = (Dm[:, None].astype(np.float64) * mn)[:, :, None]
+        lo = np.minimum(0.0, xs.min(axis=2, keepdims=True))
+        hi = xs.max(axis=2, keepdims=True)
+        err = np.abs(xs - ws)
+        interior = (xs + o >= 0) & (xs + o <= 15 * e) & (e > 0)
+        ib = e / 2 + 2.0 ** -20 * (np.abs(xs) + 15 * e)
+        assert (err[interior] <= ib[interior]).all()
+        # super-block scales before f16 rounding; f16 error <= max(2^-11 d, 2^-25)
+        d = ((hi - lo) / 15.0).max(axis=1, keepdims=True) / 63.0
+        dmin = (-lo).max(axis=1, keepdims=True) / 63.0
+        dD = np.maximum(2.0 ** -11 * d, 2.0 ** -25)
+        dDm = np.maximum(2.0 ** -11 * dmin, 2.0 ** -25)
+        allb = e / 2 + 15 * (d / 2 + 63 * dD) + dmin / 2 + 63 * dDm + 2.0 ** -20 * (hi - lo + np.abs(xs))
+        assert (err <= allb).all()
+        assert (sc >= 0).all() and (sc <= 63).all() and (mn >= 0).all() and (mn <= 63).all()
+
+
+def test_q4_k_extreme_subblocks_use_full_scale(orc):
+    """Closed form of the min/max reading: the sub-block with the largest step
+    gets sc = 63 and the one with the largest offset gets m = 63."""
+    x = qmm_synth.weights(32, 2048)
+    q = orc.quantize("q4_k", x)
+    for r in range(32):
+        D, Dm, sc, mn, codes = py_decode_q4_k(q[r], 2048)
+        assert (sc.max(axis=1) == 63).all()
+        assert (mn.max(axis=1) == 63).all()
+
+
+def test_q4_k_layout_decode_matches_python_reader(orc):
+    """The oracle's Q4_K dequantization equals an independent Python reader
+    of the same field layout: w = (f(d) sc) q - f(dmin) m."""
+    K = 1024
+    x = qmm_synth.weights(16, K)
+    q = orc.quantize("q4_k", x)
+    w = orc.dequantize("q4_k", q, K)
+    for r in range(16):
+        D, Dm, sc, mn, codes = py_decode_q4_k(q[r], K)
+        e = (D[:, None] * sc.astype(np.float32)).astype(np.float32)
+        o = (Dm[:, None] * mn.astype(np.float32)).astype(np.float32)
+        ref = (e[:, :, None] * codes.reshape(-1, 8, 32).astype(np.float32)).astype(np.float32) - o[:, :, None]
+        assert np.array_equal(ref.astype(np.float32).ravel(), w[r])
+
+
+# ---------------------------------------------------------------------------
+# Integer block sums: brute force on tiny inputs
+# ---------------------------------------------------------------------------
+
+def _brute_q8_0(wq, xq, M, N, K):
+    out = np.zeros((M, N, K // 32), np.int64)
+    for m in range(M):
+        _, a = py_decode_q8_0(xq[m], K)
+        for n in range(N):
+            _, w = py_decode_q8_0(wq[n], K)
+            for b in range(K // 32):
+                out[m, n, b] = sum(int(w[b, i]) * int(a[b, i]) for i in range(32))
+    return out
+
+
+def _brute_q4_k(wq, xq, M, N, K):
+    out = np.zeros((M, N, K // 256, 2), np.int64)
+    for m in range(M):
+        _, a, _ = py_decode_q8_k(xq[m], K)
+        for n in range(N):
+            _, _, sc, mn, q = py_decode_q4_k(wq[n], K)
+            for s in range(K // 256):
+                ssc = sm = 0
+                for j in range(8):
+                    isum = sum(int(q[s, 32 * j + i]) * int(a[s, 32 * j + i]) for i in range(32))
+                    asum = sum(int(a[s, 32 * j + i]) for i in range(32))
+                    ssc += int(sc[s, j]) * isum
+                    sm += int(mn[s, j]) * asum
+                out[m, n, s] = (ssc, sm)
+    return out
+
+
+@pytest.mark.parametrize("K", [256, 512])
+def test_block_sums_equal_brute_force(orc, K):
+    """Per-block integer sums equal Python-int brute force, including
+    adversarial constant (all +-127) rows."""
+    M, N = 3, 4
+    w = qmm_synth.weights(N, K, seed=11)
+    x = qmm_synth.activations(M, K, seed=12)
+    w[0] = 1.0
+    x[0] = 1.0
+    w[1, ::2] = -5.0
+    x[1] = -2.0
+    wq8, xq8 = orc.quantize("q8_0", w), orc.quantize("q8_0", x)
+    assert np.array_equal(orc.block_sums("q8_0", wq8, xq8, M, N, K), _brute_q8_0(wq8, xq8, M, N, K))
+    wq4, xqk = orc.quantize("q4_k", w), orc.quantize("q8_k", x)
+    assert np.array_equal(orc.block_sums("q4_k", wq4, xqk, M, N, K), _brute_q4_k(wq4, xqk, M, N, K))
+
+
+def test_block_sums_extremes_stay_exact(orc):
+    """All codes +-127 (Q8_0), and a Q4_K ramp whose codes span 0..15: the
+    largest per-block sums are still exact integers."""
+    K = 256
+    w = np.full((2, K), 1.0, np.float32)
+    w[1] = np.linspace(0.0, 1.0, K, dtype=np.float32)
+    x = np.full((2, K), -1.0, np.float32)
+    s = orc.block_sums("q8_0", orc.quantize("q8_0", w), orc.quantize("q8_0", x), 2, 2, K)
+    assert (s[:, 0] == -32 * 127 * 127).all()
+    wq4, xqk = orc.quantize("q4_k", w), orc.quantize("q8_k", x)
+    assert np.array_equal(orc.block_sums("q4_k", wq4, xqk, 2, 2, K), _brute_q4_k(wq4, xqk, 2, 2, K))
+
+
+# ---------------------------------------------------------------------------
+# Matmul forms
+# ---------------------------------------------------------------------------
+
+def test_row_permutation_permutes_blocks(orc):
+    """Blocks run along a row: permuting output rows (the q/k per-head
+    permutation with 9 and 3 heads) permutes the quantized rows byte for byte
+    and changes nothing else."""
+    for n_head, N in ((9, 576), (3, 192)):
+        w = qmm_synth.weights(N, 576, seed=5)
+        perm = np.arange(N).reshape(n_head, 2, N // n_head // 2).transpose(0, 2, 1).reshape(N)
+        assert np.array_equal(orc.quantize("q8_0", w[perm]), orc.quantize("q8_0", w)[perm])
+    w = qmm_synth.weights(576, 1536, seed=5)
+    perm = np.random.default_rng(0).permutation(576)
+    assert np.array_equal(orc.quantize("q4_k", w[perm]), orc.quantize("q4_k", w)[perm])
+
+
+@pytest.mark.parametrize("wtype,K", [("q8_0", 576), ("q4_k", 1536)])
+def test_activation_rows_are_independent(orc, wtype, K):
+    """Activation quantization is per row: row m's result is the same alone
+    and inside a batch of 8 (contrast: per-tensor dynamic quantization)."""
+    wq = orc.quantize(wtype, qmm_synth.weights(64, K))
+    x = qmm_synth.activations(8, K)
+    x[5] *= 50.0
+    yb, _ = orc.matmul(wtype, "int8_act", wq, x)
+    for m in range(8):
+        y1, _ = orc.matmul(wtype, "int8_act", wq, x[m:m + 1])
+        assert np.array_equal(y1[0], yb[m])
+
+
+@pytest.mark.parametrize("wtype,K", [("q8_0", 576), ("q4_k", 1536)])
+def test_one_hot_activation_selects_dequantized_column(orc, wtype, K):
+    """f32_act with x = e_k equals column k of the dequantized weights
+    exactly (the Metal form multiplies f32 activations by dequantized
+    weights)."""
+    wq = orc.quantize(wtype, qmm_synth.weights(48, K))
+    W = orc.dequantize(wtype, wq, K)
+    for k in (0, 31, K // 2 + 3, K - 1):
+        x = np.zeros((1, K), np.float32)
+        x[0, k] = 1.0
+        y, T = orc.matmul(wtype, "f32_act", wq, x)
+        assert np.array_equal(y[0], W[:, k].astype(np.float64))
+        assert np.array_equal(T[0], np.abs(W[:, k]).astype(np.float64))
+
+
+def test_f32_act_equals_dequantized_matmul(orc):
+    """f32_act = x @ dequant(W)^T (the dequantize-all form), here against
+    numpy's float64 matmul of the dequantized weights."""
+    for wtype, K in (("q8_0", 576), ("q4_k", 512)):
+        wq = orc.quantize(wtype, qmm_synth.weights(40, K))
+        x = qmm_synth.activations(3, K)
+        y, T = orc.matmul(wtype, "f32_act", wq, x)
+        W = orc.dequantize(wtype, wq, K).astype(np.float64)
+        ref = x.astype(np.float64) @ W.T
+        assert np.allclose(y, ref, rtol=0, atol=1e-12 * np.abs(x).sum() * np.abs(W).max())
+        assert np.allclose(T, np.abs(x.astype(np.float64)) @ np.abs(W).T, rtol=1e-12)
+
+
+def test_exactly_representable_activations_make_the_forms_agree(orc):
+    """When every activation block is integers with max |x| = 127, d_a = 1
+    and the codes are x itself, so the CPU form equals the Metal form."""
+    K = 576
+    wq = orc.quantize("q8_0", qmm_synth.weights(64, K))
+    r = np.random.default_rng(4)
+    x = r.integers(-127, 128, (4, K)).astype(np.float32)
+    x[:, ::32] = 127.0
+    yi, _ = orc.matmul("q8_0", "int8_act", wq, x)
+    yf, _ = orc.matmul("q8_0", "f32_act", wq, x)
+    assert np.allclose(yi, yf, rtol=1e-13, atol=0)
+
+
+def test_constant_row_closed_form(orc):
+    """A constant row c: Q8_0 codes are all 127 sign(c), the dequantized
+    value is f16(|c|/127) * 127 sign(c)."""
+    for c in (0.75, -3.0, 1e-3):
+        x = np.full((1, 64), c, np.float32)
+        q = orc.quantize("q8_0", x)
+        d, codes = py_decode_q8_0(q[0], 64)
+        assert (codes == 127 * np.sign(c)).all()
+        w = orc.dequantize("q8_0", q, 64)
+        ref = np.float32(np.float16(np.float32(abs(c)) / np.float32(127.0))) * np.float32(127.0) * np.sign(c)
+        assert (w == ref).all()
+
+
+@pytest.mark.parametrize("wtype,K", [("q8_0", 576), ("q4_k", 1536)])
+def test_activation_quantization_error_has_the_predicted_size(orc, wtype, K):
+    """The CPU form differs from the Metal form only by the activation
+    rounding: each code moves x by a near-uniform error of width d_a, so the
+    gap per output has variance sum_k w_k^2 d_a^2 / 12.  A wrong step (e.g.
+    amax/255), a dropped block scale or a wrong block size breaks the ratio."""
+    wq = orc.quantize(wtype, qmm_synth.weights(576, K))
+    x = qmm_synth.activations(4, K)
+    yi, _ = orc.matmul(wtype, "int8_act", wq, x)
+    yf, _ = orc.matmul(wtype, "f32_act", wq, x)
+    W = orc.dequantize(wtype, wq, K).astype(np.float64)
+    bv = 32 if wtype == "q8_0" else 256
+    da = np.abs(x.reshape(4, -1, bv)).max(axis=2) / 127.0
+    var = (W ** 2) @ (np.repeat(da, bv, axis=1) ** 2 / 12.0).T        # [N, M]
+    z = (yi - yf) / np.sqrt(var.T)
+    assert 0.85 < z.std() < 1.15
+    assert abs(z.mean()) < 0.1
+
+
+def test_tolerance_scale_bounds_the_output(orc):
+    """T = sum of |scaled terms| >= |y| for both forms and all outputs."""
+    for wtype, K in (("q8_0", 576), ("q4_k", 1536)):
+        wq = orc.quantize(wtype, qmm_synth.weights(64, K))
+        x = qmm_synth.activations(2, K)
+        for mode in ("int8_act", "f32_act"):
+            y, T = orc.matmul(wtype, mode, wq, x)
+            assert (np.abs(y) <= T * (1 + 1e-12)).all()
