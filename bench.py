@@ -1,0 +1,406 @@
+"""Benchmark of the GGUF block-quantized matmul on GB300.
+
+Workload (one "step"): the L2-defeating decode sweep -- for each weight type
+(Q4_K and Q8_0) eight distinct 28672 x 8192 weight buffers (132 MB and 250 MB
+each, more than the 129 MB L2) rotated call by call, for activation batches
+M in {1, 2, 4, 8} and both QMatMul forms (int8_act: activations quantized per
+row inside the launch; f32_act: f32 activations times in-kernel dequantized
+weights).  128 qmm_matmul calls per step, inputs resident in HBM.
+
+Printed JSON line: value = weight bytes streamed per second (GB/s, whole
+job), roofline of the streaming kernel against the measured HBM copy
+bandwidth, the oracle's throughput on the host cores on a bounded sample, an
+end-to-end figure through the public API with pinned host buffers (x copied in
+and y copied out on every call), SM clocks sampled during the timed region,
+and a per-(type, form, M) breakdown.  A prefill section times the Llama-shaped
+int8_act GEMMs (14336 x 4096, M = 256 and 1024) as TOPS.
+
+--impl reference times the CPU oracle (the only reference there is: the pages
+publish no code) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import qmm_synth  # noqa: E402
+
+METRIC = "decode GEMV weight GB/s (% of HBM peak); prefill int8 GEMM TOPS (% of peak)"
+N_DEC, K_DEC = 28672, 8192
+BUFFERS = 8
+MS = (1, 2, 4, 8)
+TYPES = ("q4_k", "q8_0")
+MODES = ("int8_act", "f32_act")
+WORKLOAD = (f"L2-defeating decode sweep: {BUFFERS} distinct {N_DEC}x{K_DEC} weight buffers per type "
+            f"(Q4_K 132 MB, Q8_0 250 MB each) rotated per call; activations M in {list(MS)} x {K_DEC} N(0,1); "
+            "int8_act and f32_act; 128 qmm_matmul calls per step")
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    cs = os.path.join(ROOT, "gguf_block_quantized_qmatmul_gb300", "csrc")
+    for f in sorted(os.listdir(cs)):
+        h.update(open(os.path.join(cs, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic():
+    """Per-launch DRAM bytes / algorithmic bytes from the committed ncu summary,
+    valid only for the kernel sources it was taken on."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    if d.get("kernel_hash") != kernel_hash():
+        return None
+    return d
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200", "-f", self.path],
+                                         stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        loaded = [s for s in sm if s > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_init():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def allmax(world, v: float) -> float:
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle on a bounded sample (cpu_baseline and --impl reference)
+# ---------------------------------------------------------------------------
+
+def oracle_sample(rows: int, wq_host: dict, xs: dict):
+    """One pass of the step's structure over `rows` weight rows of one buffer
+    per type (instead of 8 full buffers).  Returns (weight bytes, seconds)."""
+    import oracle
+    t0 = time.perf_counter()
+    nbytes = 0
+    for M in MS:
+        for wtype in TYPES:
+            wq = wq_host[wtype][:rows]
+            for mode in MODES:
+                oracle.matmul(wtype, mode, wq, xs[M])
+                nbytes += wq.nbytes
+    return nbytes, time.perf_counter() - t0
+
+
+def host_sample_inputs(rows: int):
+    """The sampled weight rows, quantized by the oracle (the reference arm may
+    not use the CUDA path), and the activations."""
+    import oracle
+    w = qmm_synth.weights(rows, K_DEC, seed=0)
+    wq = {t: oracle.quantize(t, w) for t in TYPES}
+    xs = {M: qmm_synth.activations(M, K_DEC) for M in MS}
+    return wq, xs
+
+
+def run_reference(args):
+    world, rank, _ = int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")), 0
+    if rank != 0:
+        return
+    import oracle
+    rows = args.ref_rows
+    wq, xs = host_sample_inputs(rows)
+    for _ in range(args.warmup):
+        oracle_sample(rows, wq, xs)
+    tot_b, tot_s = 0, 0.0
+    for _ in range(args.steps):
+        b, s = oracle_sample(rows, wq, xs)
+        tot_b += b
+        tot_s += s
+    v = tot_b / tot_s / 1e9
+    sample = f"{rows} of {N_DEC} rows of one buffer per type, all M and both forms, per step"
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_s / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
+            "data": "synthetic", "config": {"workload": WORKLOAD, "sample": sample},
+            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def make_buffers(q, torch, wtype: str, seed0: int):
+    cols = torch.from_numpy(qmm_synth.outlier_columns(K_DEC)).cuda()
+    out = []
+    for b in range(BUFFERS):
+        g = torch.Generator(device="cuda").manual_seed(seed0 + b)
+        w = torch.randn((N_DEC, K_DEC), generator=g, device="cuda") * 0.02
+        w[:, cols] *= 8.0
+        out.append(q.quantize_weights(w, wtype))
+        del w
+    torch.cuda.synchronize()
+    return out
+
+
+def run_ours(args):
+    import torch
+
+    import gguf_block_quantized_qmatmul_gb300 as q
+
+    world, rank, local = dist_init()
+    torch.cuda.set_device(local)
+    hbm_peak, bf16_peak, peak_src = peaks()
+    stream = torch.cuda.current_stream()
+
+    wqs = {t: make_buffers(q, torch, t, seed0=100 * rank + (0 if t == "q4_k" else 50)) for t in TYPES}
+    xs = {M: torch.from_numpy(qmm_synth.activations(M, K_DEC)).cuda() for M in MS}
+    ys = {M: torch.empty((M, N_DEC), dtype=torch.float32, device="cuda") for M in MS}
+    ws_need = max(q.matmul_workspace(t, m, M, N_DEC, K_DEC) for t in TYPES for m in MODES for M in MS)
+    ws = torch.empty(max(ws_need, 16), dtype=torch.uint8, device="cuda")
+    wbytes = {t: wqs[t][0].numel() for t in TYPES}
+
+    calls = [(M, t, mode, b) for M in MS for t in TYPES for mode in MODES for b in range(BUFFERS)]
+
+    def call(M, t, mode, b):
+        q.matmul(wqs[t][b], xs[M], t, mode, N=N_DEC, out=ys[M], workspace=ws)
+
+    def step():
+        for c in calls:
+            call(*c)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    barrier(world)
+
+    # per-call events inside the timed region (all launches go to `stream`)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)] for _ in range(args.steps)]
+    clocks = Clocks(local)
+    clocks.start()
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    barrier(world)
+    start.record(stream)
+    for s in range(args.steps):
+        ev[s][0].record(stream)
+        for i, c in enumerate(calls):
+            call(*c)
+            ev[s][i + 1].record(stream)
+    stop.record(stream)
+    torch.cuda.synchronize()
+    ck = clocks.stop()
+    barrier(world)
+    elapsed_ms = allmax(world, start.elapsed_time(stop))
+    bytes_per_step = sum(wbytes[t] for (_, t, _, _) in calls)
+    value = world * bytes_per_step * args.steps / (elapsed_ms / 1e3) / 1e9
+
+    # per-call durations -> roofline and breakdown
+    per = {}
+    alg_bytes, dur_ms = 0.0, 0.0
+    for s in range(args.steps):
+        for i, (M, t, mode, b) in enumerate(calls):
+            d = ev[s][i].elapsed_time(ev[s][i + 1])
+            ab = wbytes[t] + M * K_DEC * 4 + M * N_DEC * 4
+            alg_bytes += ab
+            dur_ms += d
+            per.setdefault((t, mode, M), []).append((wbytes[t], d))
+    achieved = alg_bytes / (dur_ms / 1e3) / 1e9
+    sweep = {f"{t}/{mode}/M{M}": round(sum(b for b, _ in v) / (sum(d for _, d in v) / 1e3) / 1e9, 1)
+             for (t, mode, M), v in sorted(per.items())}
+    tr = ncu_traffic()
+    launches = len(calls)
+    traffic = None
+    if tr is not None:
+        traffic = tr["dram_bytes_per_alg_byte"] * alg_bytes / (launches * args.steps)
+
+    # end to end through the public API with pinned host buffers
+    xh = {M: xs[M].cpu().pin_memory() for M in MS}
+    yh = {M: torch.empty((M, N_DEC), dtype=torch.float32).pin_memory() for M in MS}
+    xd = {M: torch.empty_like(xs[M]) for M in MS}
+    h2d = sum(xh[M].numel() * 4 for (M, _, _, _) in calls)
+    d2h = sum(yh[M].numel() * 4 for (M, _, _, _) in calls)
+
+    def e2e_step():
+        for (M, t, mode, b) in calls:
+            xd[M].copy_(xh[M], non_blocking=True)
+            q.matmul(wqs[t][b], xd[M], t, mode, N=N_DEC, out=ys[M], workspace=ws)
+            yh[M].copy_(ys[M], non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_s = allmax(world, time.perf_counter() - t0)
+    e2e = world * bytes_per_step * args.steps / e2e_s / 1e9
+
+    # prefill (Llama-shaped, int8_act): TOPS = 2 M N K / time
+    prefill = {}
+    if not args.no_prefill:
+        for t in TYPES:
+            g = torch.Generator(device="cuda").manual_seed(7)
+            w = torch.randn((14336, 4096), generator=g, device="cuda") * 0.02
+            wq = q.quantize_weights(w, t)
+            del w
+            for M in (256, 1024):
+                x = torch.from_numpy(qmm_synth.activations(M, 4096, outlier_channels=4)).cuda()
+                y = torch.empty((M, 14336), dtype=torch.float32, device="cuda")
+                need = q.matmul_workspace(t, "int8_act", M, 14336, 4096)
+                wsp = torch.empty(max(need, 16), dtype=torch.uint8, device="cuda")
+                for _ in range(3):
+                    q.matmul(wq, x, t, "int8_act", N=14336, out=y, workspace=wsp)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                reps = 10
+                e0.record(stream)
+                for _ in range(reps):
+                    q.matmul(wq, x, t, "int8_act", N=14336, out=y, workspace=wsp)
+                e1.record(stream)
+                torch.cuda.synchronize()
+                ms = e0.elapsed_time(e1) / reps
+                tops = 2.0 * M * 14336 * 4096 / (ms / 1e3) / 1e12
+                prefill[f"{t}/int8_act/M{M}/14336x4096"] = {"ms": round(ms, 4), "TOPS": round(tops, 1),
+                                                            "frac_of_bf16_dense_peak": round(tops / bf16_peak, 4)}
+            del wq
+
+    # oracle on the host cores, bounded sample (rank 0, N = 1 only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        import oracle
+        rows = N_DEC
+        wq_h = {t: wqs[t][0][:rows].cpu().numpy() for t in TYPES}
+        xs_h = {M: xs[M].cpu().numpy() for M in MS}
+        b, s = oracle_sample(rows, wq_h, xs_h)
+        cpu = {"value": b / s / 1e9, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
+               "sample": f"{rows} of {N_DEC} rows of one buffer per type, all M and both forms ({s:.1f} s)"}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "s8xs8->s32 (int8_act), f16xf16->f32 (f32_act)",
+                "data": "synthetic",
+                "config": {"workload": WORKLOAD, "l2": "inputs larger than L2 (8 distinct weight buffers per type, "
+                           "each >= 132 MB, rotated per call)", "parallelism": f"replicas x{world}"},
+                "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                             "frac": round(achieved / hbm_peak, 4), "traffic": traffic,
+                             "kernel": "qmm_stream_kernel", "peak_source": f"{peak_src} hbm_gbs",
+                             "alg_bytes": "weights + x f32 + y f32 per launch"},
+                "cpu_baseline": cpu,
+                "e2e": {"value": round(e2e, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                        "d2h_bytes_per_step": d2h},
+                "gpu_launches": launches * args.steps,
+                "clocks": ck, "sweep_GBps": sweep, "prefill": prefill}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--ref-rows", type=int, default=4096)
+    ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

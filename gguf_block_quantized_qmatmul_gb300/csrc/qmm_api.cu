@@ -1,0 +1,220 @@
+// qmm_api.cu -- the C ABI (include/qmm.h): argument checks, planning, launches.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+
+#include "../../include/qmm.h"
+#include "qmm_internal.h"
+
+using namespace qmm;
+
+namespace {
+
+__device__ unsigned g_qmm_err = 0;  // device error word (timeouts of bounded waits)
+
+constexpr int kMaxDev = 64;
+unsigned* g_err_ptr[kMaxDev];
+int g_sm_count[kMaxDev];
+int g_smem_optin[kMaxDev];
+
+// Per-device constants: error-word address, SM count, opt-in shared memory.
+cudaError_t device_info(unsigned** err, int* sms, int* smem) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
+    if (!g_err_ptr[dev]) {
+        void* p = nullptr;
+        if ((e = cudaGetSymbolAddress(&p, g_qmm_err)) != cudaSuccess) return e;
+        int n = 0, s = 0;
+        if ((e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+        if ((e = cudaDeviceGetAttribute(&s, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess) return e;
+        g_sm_count[dev] = n;
+        g_smem_optin[dev] = s;
+        g_err_ptr[dev] = static_cast<unsigned*>(p);
+    }
+    if (err) *err = g_err_ptr[dev];
+    if (sms) *sms = g_sm_count[dev];
+    if (smem) *smem = g_smem_optin[dev];
+    return cudaSuccess;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+bool valid_type(qmm_type t) { return t == QMM_Q8_0 || t == QMM_Q4_K || t == QMM_Q8_K; }
+
+qmm_status check_shape(qmm_type t, int64_t rows, int64_t K) {
+    if (rows < 0 || K < 0) return QMM_ERR_SHAPE;
+    if (rows > INT32_MAX || K > INT32_MAX) return QMM_ERR_SHAPE;
+    const int64_t bv = qmm_block_values(t);
+    if (bv <= 0 || K % bv != 0) return QMM_ERR_SHAPE;
+    return QMM_OK;
+}
+
+size_t round_up_sz(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+size_t workspace_for(const StreamPlan& pl) {
+    if (pl.p.kslices <= 1) return 0;
+    return round_up_sz((size_t)pl.p.kslices * pl.p.M * pl.p.N * 4, 256) + (size_t)pl.p.mchunks * pl.p.ntiles * 4;
+}
+
+qmm_status stream_call(qmm_type wtype, int am, int epi, const void* wq, const float* x, float* y, int32_t* sums,
+                       int64_t M, int64_t N, int64_t K, void* ws, size_t ws_bytes, qmm_stream_t stream) {
+    unsigned* err = nullptr;
+    int sms = 0, smem = 0;
+    if (device_info(&err, &sms, &smem) != cudaSuccess) return QMM_ERR_CUDA;
+    StreamPlan pl;
+    const int wt = wtype == QMM_Q8_0 ? T_Q8_0 : T_Q4_K;
+    if (!plan_stream(wt, am, epi, M, N, K, sms, smem, pl)) return QMM_ERR_SHAPE;
+    pl.p.wq = static_cast<const uint8_t*>(wq);
+    pl.p.x = x;
+    pl.p.y = y;
+    pl.p.sums = sums;
+    pl.p.err = err;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (epi == E_Y && pl.p.kslices > 1) {
+        const size_t need = workspace_for(pl);
+        if (!ws || ws_bytes < need) return QMM_ERR_WORKSPACE;
+        pl.p.partial = static_cast<float*>(ws);
+        const size_t coff = round_up_sz((size_t)pl.p.kslices * pl.p.M * pl.p.N * 4, 256);
+        pl.p.counters = reinterpret_cast<unsigned*>(static_cast<uint8_t*>(ws) + coff);
+        if (cudaMemsetAsync(pl.p.counters, 0, (size_t)pl.p.mchunks * pl.p.ntiles * 4, s) != cudaSuccess)
+            return QMM_ERR_CUDA;
+    }
+    const cudaError_t e = wt == T_Q8_0 ? launch_stream_q8_0(am, epi, pl, smem, s) : launch_stream_q4_k(am, epi, pl, smem, s);
+    return e == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int64_t qmm_block_values(qmm_type t) {
+    switch (t) {
+        case QMM_F32: return 1;
+        case QMM_Q8_0: return 32;
+        case QMM_Q4_K: return 256;
+        case QMM_Q8_K: return 256;
+        default: return 0;
+    }
+}
+
+size_t qmm_block_bytes(qmm_type t) {
+    switch (t) {
+        case QMM_F32: return 4;
+        case QMM_Q8_0: return 34;
+        case QMM_Q4_K: return 144;
+        case QMM_Q8_K: return 292;
+        default: return 0;
+    }
+}
+
+size_t qmm_row_bytes(qmm_type t, int64_t K) {
+    const int64_t bv = qmm_block_values(t);
+    if (bv <= 0 || K < 0 || K % bv != 0) return 0;
+    return (size_t)(K / bv) * qmm_block_bytes(t);
+}
+
+qmm_status qmm_quantize_weights(qmm_type wtype, const float* w, int64_t N, int64_t K, void* wq, qmm_stream_t stream) {
+    if (wtype != QMM_Q8_0 && wtype != QMM_Q4_K) return QMM_ERR_TYPE;
+    qmm_status st = check_shape(wtype, N, K);
+    if (st != QMM_OK) return st;
+    if (N == 0 || K == 0) return QMM_OK;
+    if (!w || !wq) return QMM_ERR_NULL;
+    if (!aligned(w, 16) || !aligned(wq, 16)) return QMM_ERR_ALIGN;
+    const int t = wtype == QMM_Q8_0 ? T_Q8_0 : T_Q4_K;
+    return launch_quantize(t, w, N, K, wq, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
+}
+
+qmm_status qmm_quantize_act(qmm_type atype, const float* x, int64_t M, int64_t K, void* xq, qmm_stream_t stream) {
+    if (atype != QMM_Q8_0 && atype != QMM_Q8_K) return QMM_ERR_TYPE;
+    qmm_status st = check_shape(atype, M, K);
+    if (st != QMM_OK) return st;
+    if (M == 0 || K == 0) return QMM_OK;
+    if (!x || !xq) return QMM_ERR_NULL;
+    if (!aligned(x, 16) || !aligned(xq, 16)) return QMM_ERR_ALIGN;
+    const int t = atype == QMM_Q8_0 ? T_Q8_0 : T_Q8_K;
+    return launch_quantize(t, x, M, K, xq, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
+}
+
+qmm_status qmm_dequantize(qmm_type t, const void* q, int64_t rows, int64_t K, float* out, qmm_stream_t stream) {
+    if (!valid_type(t)) return QMM_ERR_TYPE;
+    qmm_status st = check_shape(t, rows, K);
+    if (st != QMM_OK) return st;
+    if (rows == 0 || K == 0) return QMM_OK;
+    if (!q || !out) return QMM_ERR_NULL;
+    if (!aligned(q, 16) || !aligned(out, 16)) return QMM_ERR_ALIGN;
+    const int tt = t == QMM_Q8_0 ? T_Q8_0 : t == QMM_Q4_K ? T_Q4_K : T_Q8_K;
+    return launch_dequantize(tt, q, rows, K, out, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? QMM_OK
+                                                                                                          : QMM_ERR_CUDA;
+}
+
+size_t qmm_matmul_workspace(qmm_type wtype, qmm_act_mode mode, int64_t M, int64_t N, int64_t K) {
+    if (wtype != QMM_Q8_0 && wtype != QMM_Q4_K) return 0;
+    if (mode != QMM_INT8_ACT && mode != QMM_F32_ACT) return 0;
+    if (check_shape(wtype, N, K) != QMM_OK || M <= 0 || M > INT32_MAX || N == 0 || K == 0) return 0;
+    int sms = 0, smem = 0;
+    if (device_info(nullptr, &sms, &smem) != cudaSuccess) return 0;
+    StreamPlan pl;
+    if (!plan_stream(wtype == QMM_Q8_0 ? T_Q8_0 : T_Q4_K, mode == QMM_INT8_ACT ? A_INT8 : A_F32, E_Y, M, N, K, sms,
+                     smem, pl))
+        return 0;
+    return workspace_for(pl);
+}
+
+qmm_status qmm_matmul(qmm_type wtype, qmm_act_mode mode, const void* wq, const float* x, float* y, int64_t M,
+                      int64_t N, int64_t K, void* workspace, size_t workspace_bytes, qmm_stream_t stream) {
+    if (wtype != QMM_Q8_0 && wtype != QMM_Q4_K) return QMM_ERR_TYPE;
+    if (mode != QMM_INT8_ACT && mode != QMM_F32_ACT) return QMM_ERR_TYPE;
+    qmm_status st = check_shape(wtype, N, K);
+    if (st != QMM_OK) return st;
+    if (M < 0 || M > INT32_MAX) return QMM_ERR_SHAPE;
+    if (M == 0 || N == 0) return QMM_OK;
+    if (K == 0) return QMM_ERR_SHAPE;
+    if (!wq || !x || !y) return QMM_ERR_NULL;
+    if (!aligned(wq, 16) || !aligned(x, 16) || !aligned(y, 4)) return QMM_ERR_ALIGN;
+    if (workspace && !aligned(workspace, 16)) return QMM_ERR_ALIGN;
+    return stream_call(wtype, mode == QMM_INT8_ACT ? A_INT8 : A_F32, E_Y, wq, x, y, nullptr, M, N, K, workspace,
+                       workspace_bytes, stream);
+}
+
+qmm_status qmm_block_sums(qmm_type wtype, const void* wq, const float* x, int64_t M, int64_t N, int64_t K,
+                          int32_t* out, qmm_stream_t stream) {
+    if (wtype != QMM_Q8_0 && wtype != QMM_Q4_K) return QMM_ERR_TYPE;
+    qmm_status st = check_shape(wtype, N, K);
+    if (st != QMM_OK) return st;
+    if (M < 0 || M > INT32_MAX) return QMM_ERR_SHAPE;
+    if (M == 0 || N == 0) return QMM_OK;
+    if (K == 0) return QMM_ERR_SHAPE;
+    if (!wq || !x || !out) return QMM_ERR_NULL;
+    if (!aligned(wq, 16) || !aligned(x, 16) || !aligned(out, 4)) return QMM_ERR_ALIGN;
+    return stream_call(wtype, A_INT8, E_SUMS, wq, x, nullptr, out, M, N, K, nullptr, 0, stream);
+}
+
+qmm_status qmm_last_device_error(void) {
+    unsigned v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_qmm_err, sizeof(v)) != cudaSuccess) return QMM_ERR_CUDA;
+    if (v) {
+        const unsigned zero = 0;
+        if (cudaMemcpyToSymbol(g_qmm_err, &zero, sizeof(zero)) != cudaSuccess) return QMM_ERR_CUDA;
+        return QMM_ERR_TIMEOUT;
+    }
+    return QMM_OK;
+}
+
+const char* qmm_status_string(qmm_status s) {
+    switch (s) {
+        case QMM_OK: return "ok";
+        case QMM_ERR_NULL: return "a required pointer is NULL";
+        case QMM_ERR_SHAPE: return "invalid shape: negative size or K not a multiple of the block size";
+        case QMM_ERR_TYPE: return "type not valid for this call";
+        case QMM_ERR_ALIGN: return "pointer misaligned (16 bytes for blocks, x and workspace; 4 for floats)";
+        case QMM_ERR_WORKSPACE: return "workspace smaller than qmm_matmul_workspace()";
+        case QMM_ERR_CUDA: return "CUDA runtime or launch error";
+        case QMM_ERR_TIMEOUT: return "a device-side wait timed out";
+        default: return "unknown status";
+    }
+}
+
+}  // extern "C"

@@ -1,0 +1,28 @@
+// qmm_internal.h -- launchers shared between the translation units of the library.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "qmm_stream.cuh"
+
+namespace qmm {
+
+cudaError_t launch_quantize(int type, const float* x, long long rows, long long K, void* out, cudaStream_t s);
+cudaError_t launch_dequantize(int type, const void* q, long long rows, long long K, float* out, cudaStream_t s);
+cudaError_t launch_stream_q8_0(int am, int epi, const StreamPlan& plan, int smem_max, cudaStream_t s);
+cudaError_t launch_stream_q4_k(int am, int epi, const StreamPlan& plan, int smem_max, cudaStream_t s);
+
+// Raise a kernel's dynamic shared-memory limit once per device.
+template <typename F>
+inline cudaError_t ensure_smem(F* kernel, int smem_max, unsigned long long& done_mask) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (done_mask & bit) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
+    if (e == cudaSuccess) done_mask |= bit;
+    return e;
+}
+
+}  // namespace qmm

@@ -1,0 +1,620 @@
+// qmm_stream.cuh -- the streaming block-MMA kernel behind qmm_matmul and
+// qmm_block_sums.
+//
+// One persistent CTA per SM.  A producer warp streams the raw GGUF bytes of
+// 16-row weight tiles into a ring of shared-memory stages with 1-D bulk
+// copies (cp.async.bulk, mbarrier completion); eight consumer warps turn each
+// 32-value block (Q8_0) or 32-value sub-block (Q4_K) of 16 rows into one
+// warp-level tensor-core product against 8 (int8) or 4 (f32 pieces) activation
+// rows, and apply the block scales in registers:
+//   int8_act ("同一个 GGUF，CPU 和 Metal 生成的文字不一样" section 出处, the CPU
+//     form): mma.m16n8k32.s8 gives the exact int32 block sums isum; then
+//     Q8_0: y += f(d_w) f(d_a) isum;  Q4_K: S_sc += sc_j isum_j, S_m += m_j
+//     (sum of the sub-block's activation codes), y += d_a (f(d) S_sc -
+//     f(dmin) S_m) per super-block.
+//   f32_act (the Metal form): each activation row is scaled by a power of two
+//     and split into two f16 pieces (x 2^s = hi + lo to 2^-22 relative);
+//     weight codes are exact in f16; mma.m16n8k16.f16 with f32 accumulation
+//     gives sum q x per block; Q8_0: y += f(d) sum(q x); Q4_K: y += e_j sum(q x)
+//     - o_j sum(x) with e_j = f(d) sc_j, o_j = f(dmin) m_j.
+// Activations of the CTA's (row chunk, K slice) are quantized / split into
+// shared memory by the consumer warps while the producer already streams the
+// first weight stages.  When the K dimension is split across CTAs (to fit the
+// activation slice in shared memory), partial sums go to a workspace and the
+// last-arriving CTA of a tile adds them in slice order (deterministic).
+#pragma once
+
+#include "qmm_device.cuh"
+
+namespace qmm {
+
+template <int WT>
+struct Unit;
+template <>
+struct Unit<T_Q8_0> {
+    static constexpr int vals = 32, bytes = 34;
+};
+template <>
+struct Unit<T_Q4_K> {
+    static constexpr int vals = 256, bytes = 144;
+};
+
+// ---------------------------------------------------------------------------
+// activation preparation (consumer warps, 256 threads)
+// ---------------------------------------------------------------------------
+
+template <int WT, int AM>
+__device__ __forceinline__ void prepare_acts(const StreamParams& p, uint8_t* smem, int m0, int k0, int klen, int tid) {
+    const int MR = p.mr;
+    if (AM == A_INT8 && WT == T_Q8_0) {
+        uint8_t* codes = smem + p.off_codes;
+        float* da = reinterpret_cast<float*>(smem + p.off_scale);
+        const int nb = p.slice_units;  // blocks of 32 in the (largest) slice
+        for (int idx = tid; idx < MR * nb; idx += 256) {
+            int r = idx / nb, b = idx - r * nb;
+            int m = m0 + r;
+            uint32_t c[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+            float s = 0.0f;
+            if (m < p.M && b * 32 < klen) {
+                float d;
+                quant_q8_0_32(p.x + (long long)m * p.K + k0 + b * 32, c, d);
+                s = h2f(f2h(d));
+            }
+            uint4* dst = reinterpret_cast<uint4*>(codes + r * p.code_pitch + b * 32);
+            dst[0] = make_uint4(c[0], c[1], c[2], c[3]);
+            dst[1] = make_uint4(c[4], c[5], c[6], c[7]);
+            da[r * p.scale_pitch + b] = s;
+        }
+    } else if (AM == A_INT8 && WT == T_Q4_K) {
+        uint8_t* codes = smem + p.off_codes;
+        float* da = reinterpret_cast<float*>(smem + p.off_scale);
+        int* bs = reinterpret_cast<int*>(smem + p.off_aux);
+        const int nsb = p.slice_units;  // super-blocks of 256
+        for (int idx = tid; idx < MR * nsb; idx += 256) {
+            int r = idx / nsb, sb = idx - r * nsb;
+            int m = m0 + r;
+            uint4* dst = reinterpret_cast<uint4*>(codes + r * p.code_pitch + sb * 256);
+            if (m < p.M && sb * 256 < klen) {
+                const float* src = p.x + (long long)m * p.K + k0 + sb * 256;
+                float d, id;
+                q8_scale(q8k_amax(src), d, id);
+                for (int j = 0; j < 8; ++j) {
+                    uint32_t w[8];
+                    int sum = 0;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        float4 v = __ldg(reinterpret_cast<const float4*>(src + 32 * j) + i);
+                        w[i] = pack4(q8_code(v.x, id), q8_code(v.y, id), q8_code(v.z, id), q8_code(v.w, id));
+                        sum += bsum4(w[i]);
+                    }
+                    dst[2 * j] = make_uint4(w[0], w[1], w[2], w[3]);
+                    dst[2 * j + 1] = make_uint4(w[4], w[5], w[6], w[7]);
+                    bs[r * p.aux_pitch + sb * 8 + j] = sum;
+                }
+                da[r * p.scale_pitch + sb] = d;
+            } else {
+                for (int j = 0; j < 16; ++j) dst[j] = make_uint4(0, 0, 0, 0);
+                for (int j = 0; j < 8; ++j) bs[r * p.aux_pitch + sb * 8 + j] = 0;
+                da[r * p.scale_pitch + sb] = 0.0f;
+            }
+        }
+    } else {
+        // f32_act: per-row power-of-two scale from the slice's max |x|, then
+        // two f16 pieces per value; Q4_K also needs the scaled sum of each 32.
+        __half* pieces = reinterpret_cast<__half*>(smem + p.off_codes);
+        float* rs = reinterpret_cast<float*>(smem + p.off_rs);          // [MR][2]: 2^s, 2^-s
+        float* xs = reinterpret_cast<float*>(smem + p.off_aux);         // [MR][slice/32]
+        const int warp = tid >> 5, lane = tid & 31;
+        for (int r = warp; r < MR; r += 8) {
+            int m = m0 + r;
+            float amax = 0.0f;
+            if (m < p.M) {
+                const float4* src = reinterpret_cast<const float4*>(p.x + (long long)m * p.K + k0);
+                for (int i = lane; i < klen / 4; i += 32) {
+                    float4 v = __ldg(src + i);
+                    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+                }
+            }
+#pragma unroll
+            for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+            if (lane == 0) {
+                int s = 0;
+                if (amax > 0.0f) {
+                    int e = (int)((__float_as_uint(amax) >> 23) & 0xff) - 127;  // amax in [2^e, 2^(e+1))
+                    s = 14 - e;
+                    s = s > 100 ? 100 : (s < -100 ? -100 : s);
+                }
+                rs[2 * r] = ldexpf(1.0f, s);
+                rs[2 * r + 1] = ldexpf(1.0f, -s);
+            }
+        }
+        consumer_sync();
+        const int nch = p.slice_units * Unit<WT>::vals / 32;  // chunks of 32 values
+        for (int idx = tid; idx < MR * nch; idx += 256) {
+            int r = idx / nch, c = idx - r * nch;
+            int m = m0 + r;
+            uint32_t hw[16], lw[16];
+            float sum = 0.0f;
+            if (m < p.M && c * 32 < klen) {
+                const float scale = rs[2 * r];
+                const float4* src = reinterpret_cast<const float4*>(p.x + (long long)m * p.K + k0 + c * 32);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    float4 v4 = __ldg(src + i);
+                    float v[4] = {__fmul_rn(v4.x, scale), __fmul_rn(v4.y, scale), __fmul_rn(v4.z, scale),
+                                  __fmul_rn(v4.w, scale)};
+                    uint32_t hb[4], lb[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        __half h = __float2half_rn(v[k]);
+                        __half l = __float2half_rn(__fsub_rn(v[k], __half2float(h)));
+                        hb[k] = __half_as_ushort(h);
+                        lb[k] = __half_as_ushort(l);
+                        sum = __fadd_rn(sum, v[k]);
+                    }
+                    hw[2 * i] = hb[0] | (hb[1] << 16);
+                    hw[2 * i + 1] = hb[2] | (hb[3] << 16);
+                    lw[2 * i] = lb[0] | (lb[1] << 16);
+                    lw[2 * i + 1] = lb[2] | (lb[3] << 16);
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) hw[i] = lw[i] = 0u;
+            }
+            uint4* dh = reinterpret_cast<uint4*>(pieces + (long long)(2 * r) * p.code_pitch + c * 32);
+            uint4* dl = reinterpret_cast<uint4*>(pieces + (long long)(2 * r + 1) * p.code_pitch + c * 32);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                dh[i] = make_uint4(hw[4 * i], hw[4 * i + 1], hw[4 * i + 2], hw[4 * i + 3]);
+                dl[i] = make_uint4(lw[4 * i], lw[4 * i + 1], lw[4 * i + 2], lw[4 * i + 3]);
+            }
+            if (WT == T_Q4_K) xs[r * p.aux_pitch + c] = sum;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// per-stage compute
+// ---------------------------------------------------------------------------
+
+// acc layout: int8: acc[nt][0..3] = (row g, col 2t), (g, 2t+1), (g+8, 2t), (g+8, 2t+1)
+//             f32 : acc[nt][0..1] = (row g, act row 4nt+t), (g+8, 4nt+t)
+template <int WT, int AM, int NT, int EPI>
+__device__ __forceinline__ void compute_stage(const StreamParams& p, uint8_t* smem, const uint8_t* st, int nunits,
+                                              int ur0, int gu0, int off0, int off1, int warp, int lane,
+                                              float (&acc)[NT][4], int tile, int m0) {
+    const int g = lane >> 2, t = lane & 3;
+    const uint8_t* row0 = st + g * p.row_stride + off0;
+    const uint8_t* row1 = st + (g + 8) * p.row_stride + off1;
+    for (int u = warp; u < nunits; u += kConsumerWarps) {
+        const int ur = ur0 + u;  // unit index inside the K slice
+        if (WT == T_Q8_0) {
+            const uint8_t* b0 = row0 + u * 34;
+            const uint8_t* b1 = row1 + u * 34;
+            const float dw0 = h2f(*reinterpret_cast<const uint16_t*>(b0));
+            const float dw1 = h2f(*reinterpret_cast<const uint16_t*>(b1));
+            uint32_t w0, w1, v0, v1;  // 8 code bytes of rows g and g+8 at block offset 8t
+            lds8_unaligned(b0 + 2 + 8 * t, w0, w1);
+            lds8_unaligned(b1 + 2 + 8 * t, v0, v1);
+            if (AM == A_INT8) {
+                const uint8_t* codes = smem + p.off_codes;
+                const float* da = reinterpret_cast<const float*>(smem + p.off_scale);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    const uint2 bb = *reinterpret_cast<const uint2*>(codes + (nt * 8 + g) * p.code_pitch + ur * 32 + 8 * t);
+                    int d[4];
+                    mma_s8(d, w0, v0, w1, v1, bb.x, bb.y);
+                    if (EPI == E_Y) {
+                        const float da0 = da[(nt * 8 + 2 * t) * p.scale_pitch + ur];
+                        const float da1 = da[(nt * 8 + 2 * t + 1) * p.scale_pitch + ur];
+                        acc[nt][0] = fmaf((float)d[0], dw0 * da0, acc[nt][0]);
+                        acc[nt][1] = fmaf((float)d[1], dw0 * da1, acc[nt][1]);
+                        acc[nt][2] = fmaf((float)d[2], dw1 * da0, acc[nt][2]);
+                        acc[nt][3] = fmaf((float)d[3], dw1 * da1, acc[nt][3]);
+                    } else {
+                        const int n0 = tile * kTileRows + g, n1 = n0 + 8;
+                        const int ma = m0 + nt * 8 + 2 * t, mb = ma + 1;
+                        const long long nbk = p.units, gb = gu0 + u;
+                        if (ma < p.M && n0 < p.N) p.sums[((long long)ma * p.N + n0) * nbk + gb] = d[0];
+                        if (mb < p.M && n0 < p.N) p.sums[((long long)mb * p.N + n0) * nbk + gb] = d[1];
+                        if (ma < p.M && n1 < p.N) p.sums[((long long)ma * p.N + n1) * nbk + gb] = d[2];
+                        if (mb < p.M && n1 < p.N) p.sums[((long long)mb * p.N + n1) * nbk + gb] = d[3];
+                    }
+                }
+            } else {
+                const __half* pieces = reinterpret_cast<const __half*>(smem + p.off_codes);
+                const uint32_t A1a0 = s8x2_to_h2(w0, SEL01), A1a2 = s8x2_to_h2(w0, SEL23);
+                const uint32_t A1a1 = s8x2_to_h2(v0, SEL01), A1a3 = s8x2_to_h2(v0, SEL23);
+                const uint32_t A2a0 = s8x2_to_h2(w1, SEL01), A2a2 = s8x2_to_h2(w1, SEL23);
+                const uint32_t A2a1 = s8x2_to_h2(v1, SEL01), A2a3 = s8x2_to_h2(v1, SEL23);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    const int prow = 2 * (nt * 4 + (g >> 1)) + (g & 1);
+                    const uint4 bb = *reinterpret_cast<const uint4*>(pieces + (long long)prow * p.code_pitch + ur * 32 + 8 * t);
+                    float d[4] = {0.f, 0.f, 0.f, 0.f};
+                    mma_f16(d, A1a0, A1a1, A1a2, A1a3, bb.x, bb.y);
+                    mma_f16(d, A2a0, A2a1, A2a2, A2a3, bb.z, bb.w);
+                    acc[nt][0] = fmaf(dw0, d[0] + d[1], acc[nt][0]);
+                    acc[nt][1] = fmaf(dw1, d[2] + d[3], acc[nt][1]);
+                }
+            }
+        } else {  // Q4_K super-block
+            const uint8_t* s0 = row0 + u * 144;
+            const uint8_t* s1 = row1 + u * 144;
+            const uint32_t hd0 = *reinterpret_cast<const uint32_t*>(s0);
+            const uint32_t hd1 = *reinterpret_cast<const uint32_t*>(s1);
+            const uint32_t W00 = *reinterpret_cast<const uint32_t*>(s0 + 4), W01 = *reinterpret_cast<const uint32_t*>(s0 + 8),
+                           W02 = *reinterpret_cast<const uint32_t*>(s0 + 12);
+            const uint32_t W10 = *reinterpret_cast<const uint32_t*>(s1 + 4), W11 = *reinterpret_cast<const uint32_t*>(s1 + 8),
+                           W12 = *reinterpret_cast<const uint32_t*>(s1 + 12);
+            const float fD0 = h2f(hd0), fDm0 = h2f(hd0 >> 16), fD1 = h2f(hd1), fDm1 = h2f(hd1 >> 16);
+            if (AM == A_INT8) {
+                const uint8_t* codes = smem + p.off_codes;
+                const float* da = reinterpret_cast<const float*>(smem + p.off_scale);
+                const int* bs = reinterpret_cast<const int*>(smem + p.off_aux);
+                int ssc[NT][4], smn[NT][4];
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) ssc[nt][i] = smn[nt][i] = 0;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const uint2 q0 = *reinterpret_cast<const uint2*>(s0 + 16 + 32 * c + 8 * t);
+                    const uint2 q1 = *reinterpret_cast<const uint2*>(s1 + 16 + 32 * c + 8 * t);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int j = 2 * c + h;
+                        const uint32_t a0 = (q0.x >> (4 * h)) & 0x0F0F0F0Fu, a2 = (q0.y >> (4 * h)) & 0x0F0F0F0Fu;
+                        const uint32_t a1 = (q1.x >> (4 * h)) & 0x0F0F0F0Fu, a3 = (q1.y >> (4 * h)) & 0x0F0F0F0Fu;
+                        const int sc0 = q4k_sc(W00, W02, j), mn0 = q4k_mn(W01, W02, j);
+                        const int sc1 = q4k_sc(W10, W12, j), mn1 = q4k_mn(W11, W12, j);
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) {
+                            const uint2 bb = *reinterpret_cast<const uint2*>(codes + (nt * 8 + g) * p.code_pitch + ur * 256 + 32 * j + 8 * t);
+                            int d[4];
+                            mma_s8(d, a0, a1, a2, a3, bb.x, bb.y);
+                            const int bs0 = bs[(nt * 8 + 2 * t) * p.aux_pitch + ur * 8 + j];
+                            const int bs1 = bs[(nt * 8 + 2 * t + 1) * p.aux_pitch + ur * 8 + j];
+                            ssc[nt][0] += sc0 * d[0];
+                            ssc[nt][1] += sc0 * d[1];
+                            ssc[nt][2] += sc1 * d[2];
+                            ssc[nt][3] += sc1 * d[3];
+                            smn[nt][0] += mn0 * bs0;
+                            smn[nt][1] += mn0 * bs1;
+                            smn[nt][2] += mn1 * bs0;
+                            smn[nt][3] += mn1 * bs1;
+                        }
+                    }
+                }
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    if (EPI == E_Y) {
+                        const float da0 = da[(nt * 8 + 2 * t) * p.scale_pitch + ur];
+                        const float da1 = da[(nt * 8 + 2 * t + 1) * p.scale_pitch + ur];
+                        acc[nt][0] += da0 * (fD0 * (float)ssc[nt][0] - fDm0 * (float)smn[nt][0]);
+                        acc[nt][1] += da1 * (fD0 * (float)ssc[nt][1] - fDm0 * (float)smn[nt][1]);
+                        acc[nt][2] += da0 * (fD1 * (float)ssc[nt][2] - fDm1 * (float)smn[nt][2]);
+                        acc[nt][3] += da1 * (fD1 * (float)ssc[nt][3] - fDm1 * (float)smn[nt][3]);
+                    } else {
+                        const int n0 = tile * kTileRows + g, n1 = n0 + 8;
+                        const int ma = m0 + nt * 8 + 2 * t, mb = ma + 1;
+                        const long long nsb = p.units, gs = gu0 + u;
+                        if (ma < p.M && n0 < p.N) { int* o = p.sums + (((long long)ma * p.N + n0) * nsb + gs) * 2; o[0] = ssc[nt][0]; o[1] = smn[nt][0]; }
+                        if (mb < p.M && n0 < p.N) { int* o = p.sums + (((long long)mb * p.N + n0) * nsb + gs) * 2; o[0] = ssc[nt][1]; o[1] = smn[nt][1]; }
+                        if (ma < p.M && n1 < p.N) { int* o = p.sums + (((long long)ma * p.N + n1) * nsb + gs) * 2; o[0] = ssc[nt][2]; o[1] = smn[nt][2]; }
+                        if (mb < p.M && n1 < p.N) { int* o = p.sums + (((long long)mb * p.N + n1) * nsb + gs) * 2; o[0] = ssc[nt][3]; o[1] = smn[nt][3]; }
+                    }
+                }
+            } else {
+                const __half* pieces = reinterpret_cast<const __half*>(smem + p.off_codes);
+                const float* xs = reinterpret_cast<const float*>(smem + p.off_aux);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const uint2 q0 = *reinterpret_cast<const uint2*>(s0 + 16 + 32 * c + 8 * t);
+                    const uint2 q1 = *reinterpret_cast<const uint2*>(s1 + 16 + 32 * c + 8 * t);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int j = 2 * c + h;
+                        const uint32_t n0x = (q0.x >> (4 * h)) & 0x0F0F0F0Fu, n0y = (q0.y >> (4 * h)) & 0x0F0F0F0Fu;
+                        const uint32_t n1x = (q1.x >> (4 * h)) & 0x0F0F0F0Fu, n1y = (q1.y >> (4 * h)) & 0x0F0F0F0Fu;
+                        const uint32_t A1a0 = u4x2_to_h2(n0x, SEL01), A1a2 = u4x2_to_h2(n0x, SEL23);
+                        const uint32_t A1a1 = u4x2_to_h2(n1x, SEL01), A1a3 = u4x2_to_h2(n1x, SEL23);
+                        const uint32_t A2a0 = u4x2_to_h2(n0y, SEL01), A2a2 = u4x2_to_h2(n0y, SEL23);
+                        const uint32_t A2a1 = u4x2_to_h2(n1y, SEL01), A2a3 = u4x2_to_h2(n1y, SEL23);
+                        const float e0 = fD0 * (float)q4k_sc(W00, W02, j), o0 = fDm0 * (float)q4k_mn(W01, W02, j);
+                        const float e1 = fD1 * (float)q4k_sc(W10, W12, j), o1 = fDm1 * (float)q4k_mn(W11, W12, j);
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) {
+                            const int prow = 2 * (nt * 4 + (g >> 1)) + (g & 1);
+                            const uint4 bb = *reinterpret_cast<const uint4*>(pieces + (long long)prow * p.code_pitch + ur * 256 + 32 * j + 8 * t);
+                            float d[4] = {0.f, 0.f, 0.f, 0.f};
+                            mma_f16(d, A1a0, A1a1, A1a2, A1a3, bb.x, bb.y);
+                            mma_f16(d, A2a0, A2a1, A2a2, A2a3, bb.z, bb.w);
+                            const float X = xs[(nt * 4 + t) * p.aux_pitch + ur * 8 + j];
+                            acc[nt][0] += fmaf(e0, d[0] + d[1], -o0 * X);
+                            acc[nt][1] += fmaf(e1, d[2] + d[3], -o1 * X);
+                        }
+                    }
+                }
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// the kernel
+// ---------------------------------------------------------------------------
+
+template <int WT, int AM, int NT, int EPI>
+__global__ void __launch_bounds__(kThreads, 1) qmm_stream_kernel(const StreamParams p) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    constexpr int UB = Unit<WT>::bytes;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int S = p.stages;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem);  // full[S], empty[S]
+    volatile int* flags = reinterpret_cast<volatile int*>(smem + p.off_flags);  // [0] abort, [1] last
+    const int pair = blockIdx.x % p.pairs;
+    const int slice = pair % p.kslices, mc = pair / p.kslices;
+    const int tile0 = blockIdx.x / p.pairs;
+    const int m0 = mc * p.mr;
+    const int su0 = slice * p.slice_units;                                   // first unit of the slice
+    const int sunits = min(p.slice_units, p.units - su0);                    // units in this slice
+    const int nchunks = (sunits + p.ups - 1) / p.ups;
+
+    if (tid == 0) {
+        for (int i = 0; i < S; ++i) {
+            mbar_init(smem_u32(&bars[i]), 1);
+            mbar_init(smem_u32(&bars[S + i]), kConsumerWarps);
+        }
+        flags[0] = 0;
+        flags[1] = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == kConsumerWarps) {
+        // ----------------------------- producer -----------------------------
+        if (lane != 0) return;
+        long long g = 0;
+        bool ok = true;
+        for (int tile = tile0; tile < p.ntiles && ok; tile += p.per_pair) {
+            for (int ch = 0; ch < nchunks && ok; ++ch, ++g) {
+                const int slot = (int)(g % S);
+                if (g >= S) ok = mbar_wait(smem_u32(&bars[S + slot]), (uint32_t)(((g / S) - 1) & 1), flags, p.err);
+                if (!ok) break;
+                const int cu0 = su0 + ch * p.ups;
+                const int cnu = min(p.ups, su0 + sunits - cu0);
+                uint8_t* st = smem + p.off_stage + (long long)slot * kTileRows * p.row_stride;
+                uint32_t tx = 0;
+                // pass 1: tail bytes by plain loads (rows whose 16-byte superset
+                // would run past the end of the weight buffer), and tx bytes
+                for (int r = 0; r < kTileRows; ++r) {
+                    const long long row = (long long)tile * kTileRows + r;
+                    if (row >= p.N) break;
+                    const long long s = row * p.rb + (long long)cu0 * UB;
+                    const long long a = s & ~15ll, e = s + (long long)cnu * UB;
+                    long long b = (e + 15) & ~15ll;
+                    if (b > p.total_bytes) {
+                        b = e & ~15ll;
+                        for (long long q = b; q < e; ++q) st[r * p.row_stride + (q - a)] = p.wq[q];
+                    }
+                    if (b > a) tx += (uint32_t)(b - a);
+                }
+                fence_proxy_async();
+                const uint32_t fb = smem_u32(&bars[slot]);
+                mbar_arrive_tx(fb, tx);
+                for (int r = 0; r < kTileRows; ++r) {
+                    const long long row = (long long)tile * kTileRows + r;
+                    if (row >= p.N) break;
+                    const long long s = row * p.rb + (long long)cu0 * UB;
+                    const long long a = s & ~15ll, e = s + (long long)cnu * UB;
+                    long long b = (e + 15) & ~15ll;
+                    if (b > p.total_bytes) b = e & ~15ll;
+                    if (b > a) bulk_g2s(smem_u32(st + r * p.row_stride), p.wq + a, (uint32_t)(b - a), fb);
+                }
+            }
+        }
+        // wait for the copies still in flight into this block's stages
+        const long long first = g > S ? g - S : 0;
+        for (long long q = first; q < g; ++q) mbar_wait(smem_u32(&bars[q % S]), (uint32_t)((q / S) & 1), flags, p.err);
+        return;
+    }
+
+    // ------------------------------- consumers -------------------------------
+    const int k0 = su0 * Unit<WT>::vals;
+    const int klen = sunits * Unit<WT>::vals;
+    if (EPI == E_Y || true) prepare_acts<WT, AM>(p, smem, m0, k0, klen, tid);
+    consumer_sync();
+
+    float* red = reinterpret_cast<float*>(smem + p.off_red);
+    const float* rs = reinterpret_cast<const float*>(smem + p.off_rs);
+    const int g8 = lane >> 2, t4 = lane & 3;
+    long long g = 0;
+    for (int tile = tile0; tile < p.ntiles; tile += p.per_pair) {
+        float acc[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc[nt][i] = 0.0f;
+        const long long rowA = (long long)tile * kTileRows + g8, rowB = rowA + 8;
+        for (int ch = 0; ch < nchunks; ++ch, ++g) {
+            const int slot = (int)(g % S);
+            const bool ok = mbar_wait(smem_u32(&bars[slot]), (uint32_t)((g / S) & 1), flags, p.err);
+            const int cu0 = su0 + ch * p.ups;
+            const int cnu = min(p.ups, su0 + sunits - cu0);
+            if (ok) {
+                const uint8_t* st = smem + p.off_stage + (long long)slot * kTileRows * p.row_stride;
+                const int off0 = (int)((rowA * p.rb + (long long)cu0 * UB) & 15);
+                const int off1 = (int)((rowB * p.rb + (long long)cu0 * UB) & 15);
+                compute_stage<WT, AM, NT, EPI>(p, smem, st, cnu, cu0 - su0, cu0, off0, off1, warp, lane, acc, tile, m0);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&bars[S + slot]));
+        }
+        if (EPI != E_Y) continue;
+        // ---- cross-warp reduction of the tile: red[warp][16][mr]
+        const int MR = p.mr;
+        float* rw = red + warp * kTileRows * MR;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            if (AM == A_INT8) {
+                rw[g8 * MR + nt * 8 + 2 * t4] = acc[nt][0];
+                rw[g8 * MR + nt * 8 + 2 * t4 + 1] = acc[nt][1];
+                rw[(g8 + 8) * MR + nt * 8 + 2 * t4] = acc[nt][2];
+                rw[(g8 + 8) * MR + nt * 8 + 2 * t4 + 1] = acc[nt][3];
+            } else {
+                rw[g8 * MR + nt * 4 + t4] = acc[nt][0];
+                rw[(g8 + 8) * MR + nt * 4 + t4] = acc[nt][1];
+            }
+        }
+        consumer_sync();
+        const bool aborted = flags[0] != 0;
+        for (int o = tid; o < kTileRows * MR; o += 256) {
+            const int r = o / MR, c = o - r * MR;
+            float v = 0.0f;
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) v += red[(w * kTileRows + r) * MR + c];
+            if (AM == A_F32) v *= rs[2 * c + 1];
+            const long long n = (long long)tile * kTileRows + r;
+            const int m = m0 + c;
+            if (!aborted && n < p.N && m < p.M) {
+                if (p.kslices == 1) p.y[(long long)m * p.N + n] = v;
+                else p.partial[((long long)slice * p.M + m) * p.N + n] = v;
+            }
+        }
+        if (p.kslices > 1) {
+            __threadfence();
+            consumer_sync();
+            if (tid == 0) {
+                const unsigned old = atomicAdd(&p.counters[(long long)mc * p.ntiles + tile], 1u);
+                flags[1] = (old == (unsigned)(p.kslices - 1)) ? 1 : 0;
+            }
+            consumer_sync();
+            if (flags[1] && !aborted) {
+                __threadfence();
+                for (int o = tid; o < kTileRows * MR; o += 256) {
+                    const int r = o / MR, c = o - r * MR;
+                    const long long n = (long long)tile * kTileRows + r;
+                    const int m = m0 + c;
+                    if (n < p.N && m < p.M) {
+                        float v = 0.0f;
+                        for (int s = 0; s < p.kslices; ++s) v += __ldcg(p.partial + ((long long)s * p.M + m) * p.N + n);
+                        p.y[(long long)m * p.N + n] = v;
+                    }
+                }
+            }
+        }
+        consumer_sync();
+    }
+}
+
+// ---------------------------------------------------------------------------
+// host-side planning (shared-memory layout, grid, split of K)
+// ---------------------------------------------------------------------------
+
+struct StreamPlan {
+    StreamParams p;
+    int nt;
+    int grid;
+    size_t smem;
+    size_t workspace;  // bytes of partial sums + counters (0 when K is not split)
+};
+
+inline int round_up(int v, int a) { return (v + a - 1) / a * a; }
+
+// Fills the layout for wtype/mode/epilogue and sizes; returns false if no
+// layout fits in smem_max.
+inline bool plan_stream(int wt, int am, int epi, long long M, long long N, long long K, int sm_count, int smem_max,
+                        StreamPlan& out) {
+    StreamPlan pl{};
+    StreamParams& p = pl.p;
+    const int uv = wt == T_Q8_0 ? 32 : 256, ub = wt == T_Q8_0 ? 34 : 144;
+    int nt;
+    if (am == A_INT8) nt = M <= 8 ? 1 : M <= 16 ? 2 : M <= 32 ? 4 : 8;
+    else nt = M <= 4 ? 1 : M <= 8 ? 2 : M <= 16 ? 4 : 8;
+    if (wt == T_Q4_K && am == A_INT8 && nt > 4) nt = 4;  // register budget of the integer super-block sums
+    const int mr = am == A_INT8 ? 8 * nt : 4 * nt;
+    p.M = (int)M;
+    p.N = (int)N;
+    p.K = (int)K;
+    p.mr = mr;
+    p.mchunks = (int)((M + mr - 1) / mr);
+    p.units = (int)(K / uv);
+    p.rb = (long long)p.units * ub;
+    p.total_bytes = p.rb * N;
+    p.ntiles = (int)((N + kTileRows - 1) / kTileRows);
+    const int ups_max = wt == T_Q8_0 ? 32 : 8;  // 1024 (Q8_0) or 2048 (Q4_K) values per stage
+    const int red_bytes = kConsumerWarps * kTileRows * mr * 4;
+    for (int ks = 1; ks <= p.units; ++ks) {
+        const int su = (p.units + ks - 1) / ks;
+        if ((long long)(ks - 1) * su >= p.units) continue;  // empty last slice
+        const int ups = su < ups_max ? su : ups_max;
+        const int row_stride = round_up(ups * ub + 32, 16) + 16;
+        const int stage_bytes = kTileRows * row_stride;
+        const int kv = su * uv;  // values per slice
+        int codes, scale_pitch = 0, aux_pitch = 0, code_pitch;
+        if (am == A_INT8) {
+            code_pitch = kv + 16;
+            codes = mr * code_pitch;
+            scale_pitch = su;
+            if (wt == T_Q4_K) aux_pitch = su * 8;
+        } else {
+            code_pitch = kv + 8;  // halves
+            codes = mr * 2 * code_pitch * 2;
+            if (wt == T_Q4_K) aux_pitch = kv / 32;
+        }
+        int off = round_up(2 * 8 * 8, 128);  // up to 8 stages x 2 barriers
+        const int off_flags = off;
+        off += 128;
+        const int off_codes = off;
+        off = round_up(off + codes, 128);
+        const int off_scale = off;
+        off = round_up(off + mr * scale_pitch * 4, 128);
+        const int off_aux = off;
+        off = round_up(off + mr * aux_pitch * 4, 128);
+        const int off_rs = off;
+        off = round_up(off + mr * 2 * 4, 128);
+        const int off_red = off;
+        off = round_up(off + red_bytes, 128);
+        const int off_stage = off;
+        int stages = (smem_max - off) / stage_bytes;
+        if (stages > 8) stages = 8;
+        if (stages < 3 && ks < p.units) continue;
+        if (stages < 2) return false;
+        p.kslices = ks;
+        p.slice_units = su;
+        p.ups = ups;
+        p.row_stride = row_stride;
+        p.stages = stages;
+        p.code_pitch = code_pitch;
+        p.scale_pitch = scale_pitch;
+        p.aux_pitch = aux_pitch;
+        p.off_flags = off_flags;
+        p.off_codes = off_codes;
+        p.off_scale = off_scale;
+        p.off_aux = off_aux;
+        p.off_rs = off_rs;
+        p.off_red = off_red;
+        p.off_stage = off_stage;
+        pl.smem = (size_t)off_stage + (size_t)stages * stage_bytes;
+        break;
+    }
+    if (p.kslices == 0) return false;
+    if (epi == E_SUMS) {
+        // sums need no reduction: the workspace is not used
+    }
+    p.pairs = p.kslices * p.mchunks;
+    int per = sm_count / p.pairs;
+    if (per < 1) per = 1;
+    if (per > p.ntiles) per = p.ntiles;
+    p.per_pair = per;
+    pl.grid = p.pairs * per;
+    pl.nt = nt;
+    pl.workspace = (epi == E_Y && p.kslices > 1)
+                       ? (size_t)p.kslices * (size_t)M * (size_t)N * 4 + (size_t)p.mchunks * p.ntiles * 4 + 256
+                       : 0;
+    out = pl;
+    return true;
+}
+
+}  // namespace qmm

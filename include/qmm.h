@@ -1,0 +1,158 @@
+/*
+ * qmm.h -- C ABI of the GB300 (sm_103a) GGUF block-quantized matmul library.
+ *
+ * The operations follow the candle tutorial pages:
+ *  - "同一个 GGUF，CPU 和 Metal 生成的文字不一样", section 出处: QMatMul has a CPU
+ *    form that quantizes every activation row (Q8_0 activations for Q8_0
+ *    weights, Q8K for K-quant weights) and takes integer block dot products,
+ *    and a Metal form that multiplies f32 activations by weight blocks
+ *    dequantized inside the kernel; CANDLE_DEQUANTIZE_ALL is the third form
+ *    (dequantize every weight to f32, then a plain matmul).
+ *  - "自己量化", section 3 (量化): QTensor::quantize(tensor, type) quantizes
+ *    row-major weights along the last dimension and fails with a shape
+ *    error when that dimension is not a multiple of the block size; section
+ *    和下载的 Q8_0 逐字节比: a Q8_0 block's scale is max|x|/127; section
+ *    动脑筋答案: activations are quantized row by row in groups of 32 (Q8_0)
+ *    or 256 (Q8K).
+ *
+ * Conventions for every entry point:
+ *  - Pointers are DEVICE pointers owned by the caller unless stated.  The
+ *    library allocates nothing.  It keeps one 4-byte device error word per
+ *    device (see qmm_last_device_error).
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *    default stream).  Argument errors are returned synchronously, before
+ *    anything is launched.  QMM_ERR_CUDA reports a launch error.
+ *  - Matrices are row-major.  W is [N, K] (N output rows, K input channels,
+ *    the GGUF / Linear convention), x is [M, K], y = x . W^T is [M, N].
+ *    Blocks run along K inside a row; a quantized matrix is N rows of
+ *    K / block_values blocks, each block in the GGUF byte layout:
+ *      Q8_0: { f16 d; int8 q[32]; }                                34 B / 32
+ *      Q4_K: { f16 d; f16 dmin; u8 scales[12]; u8 q[128]; }      144 B / 256
+ *      Q8_K: { f32 d; int8 q[256]; int16 bsums[16]; }             292 B / 256
+ *    (Q4_K: 8 sub-blocks of 32 with 6-bit scale sc_j and min m_j packed in
+ *    `scales`; byte 32c+l of q holds value l of sub-block 2c in its low
+ *    nibble and value l of sub-block 2c+1 in its high nibble.)
+ *  - Alignment: quantized buffers, x and workspace must start on a 16-byte
+ *    boundary, float outputs on a 4-byte boundary (QMM_ERR_ALIGN).
+ *  - M = 0 or N = 0 is a no-op returning QMM_OK.
+ */
+#ifndef QMM_H
+#define QMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* qmm_stream_t;   /* same type as cudaStream_t */
+
+typedef enum {
+    QMM_F32 = 0,    /* plain f32 (only as a dequantization target)          */
+    QMM_Q8_0 = 1,   /* 32 values: f16 scale, int8 codes                      */
+    QMM_Q4_K = 2,   /* 256 values: f16 d/dmin, 6-bit sub-block scales/mins   */
+    QMM_Q8_K = 3    /* 256 values: f32 scale, int8 codes, 16 int16 sums      */
+} qmm_type;
+
+typedef enum {
+    QMM_INT8_ACT = 0,  /* CPU form: activations quantized per row, integer block dots */
+    QMM_F32_ACT = 1    /* Metal form: f32 activations x in-kernel dequantized weights */
+} qmm_act_mode;
+
+typedef enum {
+    QMM_OK = 0,
+    QMM_ERR_NULL = 1,       /* a required pointer is NULL                        */
+    QMM_ERR_SHAPE = 2,      /* negative size, or K not a multiple of the block   */
+    QMM_ERR_TYPE = 3,       /* type not valid for this call / bad pairing        */
+    QMM_ERR_ALIGN = 4,      /* pointer misaligned                                */
+    QMM_ERR_WORKSPACE = 5,  /* workspace smaller than qmm_matmul_workspace()     */
+    QMM_ERR_CUDA = 6,       /* a CUDA runtime call or launch failed              */
+    QMM_ERR_TIMEOUT = 7     /* a device-side wait gave up (reported by qmm_last_device_error) */
+} qmm_status;
+
+/* Values per block: 32 (Q8_0), 256 (Q4_K, Q8_K), 1 (F32); 0 for an unknown type. */
+int64_t qmm_block_values(qmm_type t);
+
+/* Bytes per block: 34, 144, 292; 4 for F32; 0 for an unknown type.
+   ("自己量化" section 大小和误差: the printed file sizes fix 34 B per 32 values
+   for Q8_0 and 144 B per 256 for Q4K.) */
+size_t qmm_block_bytes(qmm_type t);
+
+/* Bytes of one quantized row of K values; 0 when K is not a multiple of the
+   block size (the QTensor::quantize shape error) or K < 0. */
+size_t qmm_row_bytes(qmm_type t, int64_t K);
+
+/* Quantize weights w [N, K] (f32, device) into wq (N * qmm_row_bytes(wtype, K)
+   bytes, device).  wtype: QMM_Q8_0 or QMM_Q4_K ("自己量化" section 3,
+   QTensor::quantize).  Q8_0: per 32 values d = max|x|/127, codes
+   round(x / d) with ties away from zero.  Q4_K: per sub-block of 32 a step
+   (max - min(0, min))/15 and offset -min(0, min), super-block scales
+   d = max step / 63 and dmin = max offset / 63, 6-bit factors and 4-bit
+   codes by rounding (the pages do not give the K-quant algorithm; this is the
+   closed-form min/max reading).  Errors: NULL, SHAPE (K % block), TYPE, ALIGN. */
+qmm_status qmm_quantize_weights(qmm_type wtype, const float* w, int64_t N, int64_t K, void* wq,
+                                qmm_stream_t stream);
+
+/* Quantize activations x [M, K] row by row ("同一个 GGUF…" section 出处,
+   from_float; "自己量化" 动脑筋答案: each row is quantized on its own).
+   atype: QMM_Q8_0 (blocks of 32, f16 scale) or QMM_Q8_K (blocks of 256, f32
+   scale, int16 sums of 16 codes).  Output xq: M * qmm_row_bytes(atype, K)
+   bytes.  qmm_matmul(QMM_INT8_ACT) performs exactly this quantization inside
+   its own launch; this call exports the codes.  Errors as above. */
+qmm_status qmm_quantize_act(qmm_type atype, const float* x, int64_t M, int64_t K, void* xq,
+                            qmm_stream_t stream);
+
+/* Dequantize rows blocks -> out [rows, K] f32 (the CANDLE_DEQUANTIZE_ALL form,
+   "同一个 GGUF…" section 出处).  Q8_0 and Q8_K: f(d) * q; Q4_K:
+   (f(d) * sc_j) * q - f(dmin) * m_j, both products exact in f32, one rounding
+   in the subtraction (bit-exact contract).  t: Q8_0, Q4_K or Q8_K. */
+qmm_status qmm_dequantize(qmm_type t, const void* q, int64_t rows, int64_t K, float* out,
+                          qmm_stream_t stream);
+
+/* Workspace bytes qmm_matmul needs for this shape (0 when none).  The
+   workspace holds split-K partial sums and their arrival counters. */
+size_t qmm_matmul_workspace(qmm_type wtype, qmm_act_mode mode, int64_t M, int64_t N, int64_t K);
+
+/* y [M, N] f32 = x [M, K] f32 . W^T with W given as quantized blocks wq
+   (wtype QMM_Q8_0 or QMM_Q4_K).
+   mode QMM_INT8_ACT ("同一个 GGUF…" section 出处, the CPU form): each row of x
+     is quantized in-kernel to Q8_0 (Q8_0 weights) or Q8_K (Q4_K weights),
+     per-block int32 dot products of codes are formed exactly and combined as
+       Q8_0: y = sum_b f(d_w) f(d_a) isum_b
+       Q4_K: y = sum_s d_a (f(d) S_sc - f(dmin) S_m),
+             S_sc = sum_j sc_j isum_j, S_m = sum_j m_j (sum of the sub-block's codes).
+   mode QMM_F32_ACT (the Metal form): y = sum_k x_k w_k with w the dequantized
+     weights, x kept at f32 accuracy.
+   Floats: |y - exact| <= 1e-5 * (sum of |scaled block terms|) + 1e-6.
+   workspace: device memory of at least qmm_matmul_workspace(...) bytes (may
+   be NULL when that is 0); its contents need no initialisation.
+   Errors: NULL, SHAPE, TYPE, ALIGN, WORKSPACE, CUDA. */
+qmm_status qmm_matmul(qmm_type wtype, qmm_act_mode mode, const void* wq, const float* x, float* y,
+                      int64_t M, int64_t N, int64_t K, void* workspace, size_t workspace_bytes,
+                      qmm_stream_t stream);
+
+/* Test hook: the exact integer block sums of the CPU form, computed by the
+   same kernel, fragment layout and in-kernel activation quantization as
+   qmm_matmul(QMM_INT8_ACT), written out instead of being scaled.
+   x is f32 [M, K].  out (int32, device):
+     Q8_0: [M][N][K/32]          isum of each 32-block;
+     Q4_K: [M][N][K/256][2]      (S_sc, S_m) of each super-block.
+   Bit-exact contract.  Errors as for qmm_matmul (no workspace). */
+qmm_status qmm_block_sums(qmm_type wtype, const void* wq, const float* x, int64_t M, int64_t N, int64_t K,
+                          int32_t* out, qmm_stream_t stream);
+
+/* Reads and clears the current device's error word (synchronizes that
+   device).  QMM_ERR_TIMEOUT if a device-side wait of an earlier launch gave
+   up after its bounded spin (its outputs are then undefined), QMM_OK
+   otherwise, QMM_ERR_CUDA if the read itself failed. */
+qmm_status qmm_last_device_error(void);
+
+/* Static English text for a status code. */
+const char* qmm_status_string(qmm_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QMM_H */

@@ -1,0 +1,103 @@
+"""The C-ABI library builds, loads and exports every declared symbol; host-side
+argument checks (no GPU needed: every call here returns before touching the
+device)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def qmm():
+    from gguf_block_quantized_qmatmul_gb300 import build
+    build.build()
+    import gguf_block_quantized_qmatmul_gb300 as q
+    return q
+
+
+def header_functions():
+    src = open(os.path.join(ROOT, "include", "qmm.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(qmm_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(qmm):
+    lib = ctypes.CDLL(qmm._build.LIB)
+    names = header_functions()
+    assert len(names) >= 11
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(qmm.EXPORTS) == names
+
+
+def test_block_sizes(qmm):
+    assert (qmm.block_values("q8_0"), qmm.block_bytes("q8_0")) == (32, 34)
+    assert (qmm.block_values("q4_k"), qmm.block_bytes("q4_k")) == (256, 144)
+    assert (qmm.block_values("q8_k"), qmm.block_bytes("q8_k")) == (256, 292)
+    assert qmm.row_bytes("q8_0", 576) == 612
+    assert qmm.row_bytes("q4_k", 1536) == 864
+    assert qmm.row_bytes("q4_k", 576) == 0        # the K-quant shape error
+    assert qmm.row_bytes("q8_0", 33) == 0
+    assert qmm.block_bytes(99) == 0
+
+
+def test_row_bytes_agree_with_oracle(qmm, orc):
+    for t in ("q8_0", "q4_k", "q8_k"):
+        for K in (256, 512, 4096, 8192):
+            assert qmm.row_bytes(t, K) == orc.row_bytes(t, K)
+
+
+def _lib(qmm):
+    return qmm._lib()
+
+
+def test_argument_errors_return_before_launch(qmm):
+    L = _lib(qmm)
+    Q8_0, Q4_K, Q8_K, F32 = qmm.QMM_Q8_0, qmm.QMM_Q4_K, qmm.QMM_Q8_K, qmm.QMM_F32
+    # wrong weight / activation types
+    assert L.qmm_quantize_weights(Q8_K, 16, 4, 256, 16, None) == 3
+    assert L.qmm_quantize_weights(F32, 16, 4, 256, 16, None) == 3
+    assert L.qmm_quantize_act(Q4_K, 16, 4, 256, 16, None) == 3
+    assert L.qmm_matmul(Q8_K, 0, 16, 16, 16, 1, 1, 256, None, 0, None) == 3
+    assert L.qmm_matmul(Q8_0, 7, 16, 16, 16, 1, 1, 256, None, 0, None) == 3
+    assert L.qmm_dequantize(F32, 16, 1, 256, 16, None) == 3
+    # K not a multiple of the block: the Q4K shape error on 576-wide rows
+    assert L.qmm_quantize_weights(Q4_K, 16, 576, 576, 16, None) == 2
+    assert L.qmm_matmul(Q4_K, 0, 16, 16, 16, 1, 576, 576, None, 0, None) == 2
+    assert L.qmm_matmul(Q8_0, 0, 16, 16, 16, 1, 1, 100, None, 0, None) == 2
+    assert L.qmm_matmul(Q8_0, 0, 16, 16, 16, -1, 1, 256, None, 0, None) == 2
+    assert L.qmm_block_sums(Q8_0, 16, 16, 1, -3, 256, 16, None) == 2
+    # NULL pointers
+    assert L.qmm_quantize_weights(Q8_0, None, 4, 256, 16, None) == 1
+    assert L.qmm_matmul(Q8_0, 0, None, 16, 16, 1, 1, 256, None, 0, None) == 1
+    assert L.qmm_matmul(Q8_0, 1, 16, 16, None, 1, 1, 256, None, 0, None) == 1
+    assert L.qmm_dequantize(Q8_0, 16, 1, 256, None, None) == 1
+    # misaligned pointers
+    assert L.qmm_matmul(Q8_0, 0, 18, 16, 16, 1, 1, 256, None, 0, None) == 4
+    assert L.qmm_matmul(Q8_0, 0, 16, 20, 16, 1, 1, 256, None, 0, None) == 4
+    assert L.qmm_matmul(Q8_0, 0, 16, 16, 18, 1, 1, 256, None, 0, None) == 4
+    assert L.qmm_quantize_weights(Q4_K, 16, 4, 256, 8, None) == 4
+    # empty problems are no-ops, even with NULL pointers
+    assert L.qmm_matmul(Q8_0, 0, None, None, None, 0, 5, 256, None, 0, None) == 0
+    assert L.qmm_matmul(Q4_K, 1, None, None, None, 3, 0, 256, None, 0, None) == 0
+    assert L.qmm_quantize_act(Q8_K, None, 0, 256, None, None) == 0
+    for s in range(8):
+        assert L.qmm_status_string(s)
+
+
+def test_binding_raises_on_error_status(qmm):
+    with pytest.raises(qmm.QmmError) as e:
+        qmm._check(2, "qmm_matmul")
+    assert e.value.status == 2 and "QMM_ERR_SHAPE" in str(e.value)
+
+
+def test_product_package_never_imports_the_oracle():
+    pkg = os.path.join(ROOT, "gguf_block_quantized_qmatmul_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                txt = open(os.path.join(dirpath, f), encoding="utf-8").read()
+                assert "import oracle" not in txt and "from oracle" not in txt and "qmm_oracle" not in txt, f

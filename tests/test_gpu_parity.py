@@ -1,0 +1,223 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Codes, packed scales, dequantized values and integer block sums: bit-exact.
+Float outputs: |y_gpu - y_oracle| <= 1e-5 * T + 1e-6 per element, with T the
+sum of |scaled block terms| the oracle returns beside y.
+"""
+import numpy as np
+import pytest
+
+import qmm_synth
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def qmm():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from gguf_block_quantized_qmatmul_gb300 import build
+    build.build()
+    import gguf_block_quantized_qmatmul_gb300 as q
+    return q
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def host(t):
+    torch.cuda.synchronize()
+    return t.cpu().numpy()
+
+
+def assert_within_bound(y_gpu, y_orc, T, what=""):
+    err = np.abs(y_gpu.astype(np.float64) - y_orc)
+    bound = 1e-5 * T + 1e-6
+    worst = np.max(err / bound) if err.size else 0.0
+    assert np.all(err <= bound), f"{what}: worst err/bound = {worst:.3g}"
+    return worst
+
+
+def check_device_error(qmm):
+    assert qmm.last_device_error() == 0
+
+
+# ---------------------------------------------------------------------------
+# quantizers and dequantization: bit-exact
+# ---------------------------------------------------------------------------
+
+WEIGHT_CASES = [("q8_0", 576, 576), ("q8_0", 37, 96), ("q8_0", 61, 608), ("q8_0", 5, 8192),
+                ("q4_k", 576, 1536), ("q4_k", 37, 256), ("q4_k", 19, 8192)]
+
+
+@pytest.mark.parametrize("wtype,N,K", WEIGHT_CASES)
+def test_quantize_weights_bit_exact(qmm, orc, wtype, N, K):
+    w = np.concatenate([qmm_synth.weights(N, K, seed=N + K), qmm_synth.special_block_rows(K)])
+    q = host(qmm.quantize_weights(dev(w), wtype))
+    ref = orc.quantize(wtype, w)
+    assert np.array_equal(q, ref)
+    check_device_error(qmm)
+
+
+@pytest.mark.parametrize("atype,M,K", [("q8_0", 8, 576), ("q8_0", 3, 8192), ("q8_k", 8, 1536), ("q8_k", 5, 8192)])
+def test_quantize_act_bit_exact(qmm, orc, atype, M, K):
+    x = np.concatenate([qmm_synth.activations(M, K, outlier_channels=4), qmm_synth.special_block_rows(K)])
+    q = host(qmm.quantize_act(dev(x), atype))
+    assert np.array_equal(q, orc.quantize(atype, x))
+
+
+@pytest.mark.parametrize("t,K", [("q8_0", 576), ("q4_k", 1536), ("q8_k", 1024)])
+def test_dequantize_bit_exact(qmm, orc, t, K):
+    w = np.concatenate([qmm_synth.weights(40, K), qmm_synth.special_block_rows(K)])
+    q = orc.quantize(t, w)
+    out = host(qmm.dequantize(dev(q), t, K))
+    ref = orc.dequantize(t, q, K)
+    assert np.array_equal(out.view(np.uint32), ref.view(np.uint32))
+
+
+# ---------------------------------------------------------------------------
+# integer block sums of the int8_act kernel: bit-exact
+# ---------------------------------------------------------------------------
+
+SUM_CASES = [("q8_0", 1, 33, 576), ("q8_0", 8, 576, 576), ("q8_0", 5, 40, 4096), ("q8_0", 13, 17, 1536),
+             ("q8_0", 37, 24, 96), ("q4_k", 1, 33, 1536), ("q4_k", 8, 64, 2048), ("q4_k", 19, 20, 4096)]
+
+
+@pytest.mark.parametrize("wtype,M,N,K", SUM_CASES)
+def test_block_sums_bit_exact(qmm, orc, wtype, M, N, K):
+    w = qmm_synth.weights(N, K, seed=3)
+    w[0] = 1.0                    # all codes at the extreme
+    x = qmm_synth.activations(M, K, seed=4, outlier_channels=4)
+    x[0] = -1.0
+    wq = orc.quantize(wtype, w)
+    s = host(qmm.block_sums(dev(wq), dev(x), wtype, N=N))
+    xq = orc.quantize("q8_0" if wtype == "q8_0" else "q8_k", x)
+    ref = orc.block_sums(wtype, wq, xq, M, N, K)
+    assert np.array_equal(s, ref)
+    check_device_error(qmm)
+
+
+# ---------------------------------------------------------------------------
+# matmul: both forms against the oracle's bound
+# ---------------------------------------------------------------------------
+
+MATMUL_CASES = [
+    ("q8_0", 1, 576, 576),        # SmolLM2 q/o projection, single-token decode
+    ("q8_0", 1, 192, 576),
+    ("q8_0", 1, 576, 1536),       # ffn_down
+    ("q8_0", 1, 1536, 576),
+    ("q4_k", 1, 576, 1536),       # ffn_down in Q4_K, batches 1, 2, 4, 8
+    ("q4_k", 2, 576, 1536),
+    ("q4_k", 4, 576, 1536),
+    ("q4_k", 8, 576, 1536),
+    ("q8_0", 5, 37, 608),         # ragged tile, odd number of blocks
+    ("q8_0", 8, 100, 8192),       # f32_act splits K here
+    ("q4_k", 8, 100, 8192),
+    ("q8_0", 16, 70, 4096),
+    ("q8_0", 37, 64, 4096),       # prefill, ragged M
+    ("q4_k", 37, 64, 4096),
+    ("q8_0", 64, 33, 1024),
+    ("q4_k", 100, 48, 1024),
+]
+
+
+@pytest.mark.parametrize("mode", ["int8_act", "f32_act"])
+@pytest.mark.parametrize("wtype,M,N,K", MATMUL_CASES)
+def test_matmul_within_bound(qmm, orc, wtype, M, N, K, mode):
+    w = qmm_synth.weights(N, K, seed=N * 7 + K)
+    x = qmm_synth.activations(M, K, seed=M + 11, outlier_channels=4 if M >= 16 else 0)
+    wq = orc.quantize(wtype, w)
+    y = host(qmm.matmul(dev(wq), dev(x), wtype, mode, N=N))
+    y_orc, T = orc.matmul(wtype, mode, wq, x)
+    assert_within_bound(y, y_orc, T, f"{wtype} {mode} M{M} N{N} K{K}")
+    check_device_error(qmm)
+
+
+def test_gap_ordering(qmm, orc):
+    """The CPU form's distance to the dequantized-f32 product is far larger
+    than the Metal form's (the activation-quantization error; the pages put
+    the ratio at about 30 on model logits)."""
+    for wtype, N, K in (("q8_0", 576, 576), ("q4_k", 576, 1536)):
+        wq = orc.quantize(wtype, qmm_synth.weights(N, K))
+        x = qmm_synth.activations(8, K)
+        y_deq, _ = orc.matmul(wtype, "f32_act", wq, x)
+        yi = host(qmm.matmul(dev(wq), dev(x), wtype, "int8_act", N=N)).astype(np.float64)
+        yf = host(qmm.matmul(dev(wq), dev(x), wtype, "f32_act", N=N)).astype(np.float64)
+        gap_cpu = np.abs(yi - y_deq).max()
+        gap_metal = np.abs(yf - y_deq).max()
+        assert gap_cpu >= 30 * gap_metal, (wtype, gap_cpu, gap_metal)
+
+
+def test_batch_rows_are_independent(qmm, orc):
+    """Row m's codes and output do not depend on the other rows of the batch."""
+    K, N = 1536, 96
+    for wtype in ("q8_0", "q4_k"):
+        wq = dev(orc.quantize(wtype, qmm_synth.weights(N, K)))
+        x = qmm_synth.activations(8, K)
+        x[3] *= 40.0
+        yb = host(qmm.matmul(wq, dev(x), wtype, "int8_act", N=N))
+        sb = host(qmm.block_sums(wq, dev(x), wtype, N=N))
+        for m in range(8):
+            y1 = host(qmm.matmul(wq, dev(x[m:m + 1]), wtype, "int8_act", N=N))
+            s1 = host(qmm.block_sums(wq, dev(x[m:m + 1]), wtype, N=N))
+            assert np.array_equal(s1[0], sb[m])
+            assert np.array_equal(y1[0], yb[m])
+
+
+def test_one_hot_f32_act_is_exact(qmm, orc):
+    """x = e_k: the Metal form returns column k of the dequantized weights."""
+    for wtype, K in (("q8_0", 576), ("q4_k", 1536)):
+        wq = orc.quantize(wtype, qmm_synth.weights(64, K))
+        W = orc.dequantize(wtype, wq, K)
+        x = np.zeros((4, K), np.float32)
+        for i, k in enumerate((0, 33, K // 2, K - 1)):
+            x[i, k] = 1.0
+        y = host(qmm.matmul(dev(wq), dev(x), wtype, "f32_act", N=64))
+        for i, k in enumerate((0, 33, K // 2, K - 1)):
+            assert np.array_equal(y[i], W[:, k])
+
+
+def test_error_statuses_on_device(qmm, orc):
+    wq = dev(orc.quantize("q8_0", qmm_synth.weights(100, 8192)))
+    x = dev(qmm_synth.activations(8, 8192))
+    need = qmm.matmul_workspace("q8_0", "f32_act", 8, 100, 8192)
+    assert need > 0
+    small = torch.empty(need - 16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(qmm.QmmError) as e:
+        qmm.matmul(wq, x, "q8_0", "f32_act", N=100, workspace=small)
+    assert e.value.status == 5
+    assert qmm.matmul_workspace("q8_0", "int8_act", 8, 100, 8192) == 0
+    # a workspace reused across calls needs no clearing by the caller
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda").fill_(0xAB)
+    y1 = host(qmm.matmul(wq, x, "q8_0", "f32_act", N=100, workspace=ws))
+    y2 = host(qmm.matmul(wq, x, "q8_0", "f32_act", N=100, workspace=ws))
+    assert np.array_equal(y1, y2)
+    check_device_error(qmm)
+
+
+# ---------------------------------------------------------------------------
+# full-size workloads, in the launch configuration the benchmark times,
+# checked on sampled output rows
+# ---------------------------------------------------------------------------
+
+FULL = [("q4_k", 28672, 8192, 8), ("q8_0", 28672, 8192, 8), ("q8_0", 14336, 4096, 1024),
+        ("q4_k", 4096, 4096, 256), ("q8_0", 49152, 576, 1)]
+
+
+@pytest.mark.parametrize("wtype,N,K,M", FULL)
+def test_full_size_sampled_rows(qmm, orc, wtype, N, K, M):
+    g = torch.Generator(device="cuda").manual_seed(0)
+    w = torch.randn((N, K), generator=g, device="cuda") * 0.02
+    wq = qmm.quantize_weights(w, wtype)
+    del w
+    x_np = qmm_synth.activations(M, K, outlier_channels=4 if M >= 16 else 0)
+    x = dev(x_np)
+    rows = np.unique(np.concatenate([np.arange(16), np.random.default_rng(0).choice(N, 48, replace=False), [N - 1]]))
+    wq_rows = host(wq)[rows]
+    for mode in ("int8_act", "f32_act"):
+        y = host(qmm.matmul(wq, x, wtype, mode, N=N))
+        y_orc, T = orc.matmul(wtype, mode, wq_rows, x_np)
+        assert_within_bound(y[:, rows], y_orc, T, f"{wtype} {mode} N{N} K{K} M{M}")
+    check_device_error(qmm)
