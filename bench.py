@@ -384,6 +384,28 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def run_profile_case(spec: str, launches: int):
+    """A few launches of one configuration, for ncu: spec = wtype:mode:M:N:K."""
+    import torch
+
+    import gguf_block_quantized_qmatmul_gb300 as q
+    wtype, mode, M, N, K = spec.split(":")
+    M, N, K = int(M), int(N), int(K)
+    g = torch.Generator(device="cuda").manual_seed(0)
+    w = torch.randn((N, K), generator=g, device="cuda") * 0.02
+    wq = q.quantize_weights(w, wtype)
+    del w
+    x = torch.from_numpy(qmm_synth.activations(M, K, outlier_channels=4 if M >= 16 else 0)).cuda()
+    y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    need = q.matmul_workspace(wtype, mode, M, N, K)
+    ws = torch.empty(max(need, 16), dtype=torch.uint8, device="cuda")
+    for _ in range(launches):
+        q.matmul(wq, x, wtype, mode, N=N, out=y, workspace=ws)
+    torch.cuda.synchronize()
+    assert q.last_device_error() == 0
+    print(f"profile case {spec}: {launches} launches ok")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -393,7 +415,12 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=4096)
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--profile", default=None, help="wtype:mode:M:N:K -- run a few launches for ncu and exit")
+    ap.add_argument("--launches", type=int, default=4)
     args = ap.parse_args()
+    if args.profile:
+        run_profile_case(args.profile, args.launches)
+        return
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

@@ -82,7 +82,7 @@ qmm_status stream_call(qmm_type wtype, int am, int epi, const void* wq, const fl
         if (cudaMemsetAsync(pl.p.counters, 0, (size_t)pl.p.mchunks * pl.p.ntiles * 4, s) != cudaSuccess)
             return QMM_ERR_CUDA;
     }
-    const cudaError_t e = wt == T_Q8_0 ? launch_stream_q8_0(am, epi, pl, smem, s) : launch_stream_q4_k(am, epi, pl, smem, s);
+    const cudaError_t e = launch_stream(wt, am, epi, pl, smem, s);
     return e == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
 }
 

@@ -151,14 +151,23 @@ __device__ __forceinline__ void fence_proxy_async() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-__device__ __forceinline__ void consumer_sync() {  // the 8 consumer warps only
-    asm volatile("bar.sync 1, 256;" ::: "memory");
+template <int CW>
+__device__ __forceinline__ void consumer_sync() {  // the CW consumer warps only
+    asm volatile("bar.sync 1, %0;" ::"n"(CW * 32) : "memory");
 }
+
+// Shared-memory loads through pointers derived from the kernel's __shared__
+// array (the compiler keeps them in the shared address space and may schedule
+// them freely between the mbarrier waits, which clobber memory).
+__device__ __forceinline__ uint32_t ld32(const uint8_t* p) { return *reinterpret_cast<const uint32_t*>(p); }
+__device__ __forceinline__ uint2 ld64(const uint8_t* p) { return *reinterpret_cast<const uint2*>(p); }
+__device__ __forceinline__ uint4 ld128(const uint8_t* p) { return *reinterpret_cast<const uint4*>(p); }
+__device__ __forceinline__ int dp4a(uint32_t a, uint32_t b, int c) { return __dp4a((int)a, (int)b, c); }
 
 // D = A(16x32 s8) * B(32x8 s8), exact int32, C = 0
 __device__ __forceinline__ void mma_s8(int d[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
                                        uint32_t b1) {
-    asm volatile(
+    asm(
         "mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
         "{%10,%10,%10,%10};"
         : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
@@ -168,7 +177,7 @@ __device__ __forceinline__ void mma_s8(int d[4], uint32_t a0, uint32_t a1, uint3
 // D += A(16x16 f16) * B(16x8 f16), f32 accumulate
 __device__ __forceinline__ void mma_f16(float d[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                         uint32_t b0, uint32_t b1) {
-    asm volatile(
+    asm(
         "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
         "{%0,%1,%2,%3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
@@ -204,9 +213,8 @@ __device__ __forceinline__ void lds8_unaligned(const uint8_t* p, uint32_t& r0, u
 // Streaming block-MMA kernel: plan shared by host and device
 // ---------------------------------------------------------------------------
 
-constexpr int kConsumerWarps = 8;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;  // + one producer warp
-constexpr int kTileRows = 16;                         // weight rows per tile (MMA M)
+constexpr int kTileRows = 16;  // weight rows per tile (the MMA M dimension)
+enum : int { P_MMA = 0, P_DOT = 1 };  // consumer path: warp MMA tiles, or per-thread dp4a
 
 struct StreamParams {
     const uint8_t* wq;
@@ -229,7 +237,8 @@ struct StreamParams {
     int ntiles;
     // shared-memory layout (bytes from the dynamic smem base)
     int off_stage, off_codes, off_scale, off_aux, off_rs, off_red, off_flags;
-    int code_pitch;         // int8_act: bytes per activation row; f32_act: halves per (row, piece)
+    int code_pitch;         // MMA int8_act: bytes per activation row; f32_act: halves per (row, piece);
+                            // DOT: bytes per (row, 16-byte lane piece)
     int scale_pitch;        // entries per activation row in the scale array
     int aux_pitch;          // entries per activation row in the aux array (Q8K sub-block sums, Q4_K x sums)
 };

@@ -1,26 +1,33 @@
-// qmm_stream.cuh -- the streaming block-MMA kernel behind qmm_matmul and
-// qmm_block_sums.
+// qmm_stream.cuh -- the streaming kernel behind qmm_matmul and qmm_block_sums.
 //
 // One persistent CTA per SM.  A producer warp streams the raw GGUF bytes of
 // 16-row weight tiles into a ring of shared-memory stages with 1-D bulk
-// copies (cp.async.bulk, mbarrier completion); eight consumer warps turn each
-// 32-value block (Q8_0) or 32-value sub-block (Q4_K) of 16 rows into one
-// warp-level tensor-core product against 8 (int8) or 4 (f32 pieces) activation
-// rows, and apply the block scales in registers:
-//   int8_act ("同一个 GGUF，CPU 和 Metal 生成的文字不一样" section 出处, the CPU
-//     form): mma.m16n8k32.s8 gives the exact int32 block sums isum; then
-//     Q8_0: y += f(d_w) f(d_a) isum;  Q4_K: S_sc += sc_j isum_j, S_m += m_j
-//     (sum of the sub-block's activation codes), y += d_a (f(d) S_sc -
-//     f(dmin) S_m) per super-block.
-//   f32_act (the Metal form): each activation row is scaled by a power of two
-//     and split into two f16 pieces (x 2^s = hi + lo to 2^-22 relative);
-//     weight codes are exact in f16; mma.m16n8k16.f16 with f32 accumulation
-//     gives sum q x per block; Q8_0: y += f(d) sum(q x); Q4_K: y += e_j sum(q x)
-//     - o_j sum(x) with e_j = f(d) sc_j, o_j = f(dmin) m_j.
-// Activations of the CTA's (row chunk, K slice) are quantized / split into
-// shared memory by the consumer warps while the producer already streams the
-// first weight stages.  When the K dimension is split across CTAs (to fit the
-// activation slice in shared memory), partial sums go to a workspace and the
+// copies (cp.async.bulk, mbarrier completion); CW consumer warps compute on
+// each stage while the next ones are in flight.  Two consumer paths:
+//
+//   P_DOT (int8_act, M <= 8, the decode GEMV): one thread per (weight row,
+//     block): it reads the raw 34-byte Q8_0 block (or a 64-value Q4_K pair of
+//     sub-blocks) and takes dp4a dot products with the quantized activation
+//     rows; the lanes of a row are summed with shuffles at the end of a tile.
+//   P_MMA (everything else): one warp-level tensor-core product per 32-value
+//     block (Q8_0) or sub-block (Q4_K) of 16 rows against 8 activation rows
+//     (int8: mma.m16n8k32.s8, exact int32 block sums) or 4 activation rows
+//     split into two f16 pieces (f32_act: mma.m16n8k16.f16, f32 accumulate).
+//
+// Block arithmetic ("同一个 GGUF，CPU 和 Metal 生成的文字不一样" section 出处):
+//   int8_act (CPU form): per-block exact int32 sums isum of weight codes times
+//     the row-quantized activation codes, then
+//     Q8_0: y += f(d_w) f(d_a) isum;  Q4_K: S_sc = sum_j sc_j isum_j,
+//     S_m = sum_j m_j (sum of sub-block j's activation codes),
+//     y += d_a (f(d) S_sc - f(dmin) S_m).
+//   f32_act (Metal form): each activation row is scaled by a power of two and
+//     split into two f16 pieces (x 2^s = hi + lo to 2^-22 relative); weight
+//     codes are exact in f16; y += f(d) sum(q x) (Q8_0) or e_j sum(q x) -
+//     o_j sum(x) with e_j = f(d) sc_j, o_j = f(dmin) m_j (Q4_K).
+// Activations of the CTA's (row chunk, K slice) are prepared in shared memory
+// by the consumer warps while the producer already streams the first weight
+// stages.  When the K dimension is split across CTAs (to fit the activation
+// slice in shared memory), partial sums go to a workspace and the
 // last-arriving CTA of a tile adds them in slice order (deterministic).
 #pragma once
 
@@ -32,27 +39,37 @@ template <int WT>
 struct Unit;
 template <>
 struct Unit<T_Q8_0> {
-    static constexpr int vals = 32, bytes = 34;
+    static constexpr int vals = 32, bytes = 34, per_stage = 32;
 };
 template <>
 struct Unit<T_Q4_K> {
-    static constexpr int vals = 256, bytes = 144;
+    static constexpr int vals = 256, bytes = 144, per_stage = 8;
 };
 
+// consumer warps per CTA for a kernel variant (host and device agree on it)
+__host__ __device__ constexpr int consumer_warps(int wt, int am, int nt, int path) {
+    return path == P_DOT ? 16 : (wt == T_Q8_0 && nt <= 2 ? 16 : 8);
+}
+// activation rows per CTA chunk
+__host__ __device__ constexpr int chunk_rows(int am, int nt, int path) {
+    return path == P_DOT ? nt : (am == A_INT8 ? 8 * nt : 4 * nt);
+}
+
 // ---------------------------------------------------------------------------
-// activation preparation (consumer warps, 256 threads)
+// activation preparation (consumer warps)
 // ---------------------------------------------------------------------------
 
-template <int WT, int AM>
+template <int WT, int AM, int PATH, int CW>
 __device__ __forceinline__ void prepare_acts(const StreamParams& p, uint8_t* smem, int m0, int k0, int klen, int tid) {
+    constexpr int NTH = CW * 32;
     const int MR = p.mr;
     if (AM == A_INT8 && WT == T_Q8_0) {
         uint8_t* codes = smem + p.off_codes;
         float* da = reinterpret_cast<float*>(smem + p.off_scale);
         const int nb = p.slice_units;  // blocks of 32 in the (largest) slice
-        for (int idx = tid; idx < MR * nb; idx += 256) {
-            int r = idx / nb, b = idx - r * nb;
-            int m = m0 + r;
+        for (int idx = tid; idx < MR * nb; idx += NTH) {
+            const int r = idx / nb, b = idx - r * nb;
+            const int m = m0 + r;
             uint32_t c[8] = {0, 0, 0, 0, 0, 0, 0, 0};
             float s = 0.0f;
             if (m < p.M && b * 32 < klen) {
@@ -60,9 +77,16 @@ __device__ __forceinline__ void prepare_acts(const StreamParams& p, uint8_t* sme
                 quant_q8_0_32(p.x + (long long)m * p.K + k0 + b * 32, c, d);
                 s = h2f(f2h(d));
             }
-            uint4* dst = reinterpret_cast<uint4*>(codes + r * p.code_pitch + b * 32);
-            dst[0] = make_uint4(c[0], c[1], c[2], c[3]);
-            dst[1] = make_uint4(c[4], c[5], c[6], c[7]);
+            uint4 *d0, *d1;
+            if (PATH == P_DOT) {  // two 16-byte halves in separate planes: [r][half][block]
+                d0 = reinterpret_cast<uint4*>(codes + (2 * r) * p.code_pitch + b * 16);
+                d1 = reinterpret_cast<uint4*>(codes + (2 * r + 1) * p.code_pitch + b * 16);
+            } else {
+                d0 = reinterpret_cast<uint4*>(codes + r * p.code_pitch + b * 32);
+                d1 = d0 + 1;
+            }
+            *d0 = make_uint4(c[0], c[1], c[2], c[3]);
+            *d1 = make_uint4(c[4], c[5], c[6], c[7]);
             da[r * p.scale_pitch + b] = s;
         }
     } else if (AM == A_INT8 && WT == T_Q4_K) {
@@ -70,43 +94,48 @@ __device__ __forceinline__ void prepare_acts(const StreamParams& p, uint8_t* sme
         float* da = reinterpret_cast<float*>(smem + p.off_scale);
         int* bs = reinterpret_cast<int*>(smem + p.off_aux);
         const int nsb = p.slice_units;  // super-blocks of 256
-        for (int idx = tid; idx < MR * nsb; idx += 256) {
-            int r = idx / nsb, sb = idx - r * nsb;
-            int m = m0 + r;
-            uint4* dst = reinterpret_cast<uint4*>(codes + r * p.code_pitch + sb * 256);
-            if (m < p.M && sb * 256 < klen) {
-                const float* src = p.x + (long long)m * p.K + k0 + sb * 256;
-                float d, id;
-                q8_scale(q8k_amax(src), d, id);
-                for (int j = 0; j < 8; ++j) {
-                    uint32_t w[8];
-                    int sum = 0;
+        for (int idx = tid; idx < MR * nsb; idx += NTH) {
+            const int r = idx / nsb, sb = idx - r * nsb;
+            const int m = m0 + r;
+            const bool live = m < p.M && sb * 256 < klen;
+            const float* src = p.x + (long long)m * p.K + k0 + sb * 256;
+            float d = 0.0f, id = 0.0f;
+            if (live) q8_scale(q8k_amax(src), d, id);
+            for (int j = 0; j < 8; ++j) {
+                uint32_t w[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+                int sum = 0;
+                if (live) {
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
                         float4 v = __ldg(reinterpret_cast<const float4*>(src + 32 * j) + i);
                         w[i] = pack4(q8_code(v.x, id), q8_code(v.y, id), q8_code(v.z, id), q8_code(v.w, id));
                         sum += bsum4(w[i]);
                     }
-                    dst[2 * j] = make_uint4(w[0], w[1], w[2], w[3]);
-                    dst[2 * j + 1] = make_uint4(w[4], w[5], w[6], w[7]);
-                    bs[r * p.aux_pitch + sb * 8 + j] = sum;
                 }
-                da[r * p.scale_pitch + sb] = d;
-            } else {
-                for (int j = 0; j < 16; ++j) dst[j] = make_uint4(0, 0, 0, 0);
-                for (int j = 0; j < 8; ++j) bs[r * p.aux_pitch + sb * 8 + j] = 0;
-                da[r * p.scale_pitch + sb] = 0.0f;
+                uint4 *d0, *d1;
+                if (PATH == P_DOT) {  // 64-value pairs split in four 16-byte planes: [r][piece][pair]
+                    const int pair = sb * 4 + (j >> 1), h = j & 1;
+                    d0 = reinterpret_cast<uint4*>(codes + (4 * r + 2 * h) * p.code_pitch + pair * 16);
+                    d1 = reinterpret_cast<uint4*>(codes + (4 * r + 2 * h + 1) * p.code_pitch + pair * 16);
+                } else {
+                    d0 = reinterpret_cast<uint4*>(codes + r * p.code_pitch + sb * 256 + 32 * j);
+                    d1 = d0 + 1;
+                }
+                *d0 = make_uint4(w[0], w[1], w[2], w[3]);
+                *d1 = make_uint4(w[4], w[5], w[6], w[7]);
+                bs[r * p.aux_pitch + sb * 8 + j] = sum;
             }
+            da[r * p.scale_pitch + sb] = d;
         }
     } else {
         // f32_act: per-row power-of-two scale from the slice's max |x|, then
         // two f16 pieces per value; Q4_K also needs the scaled sum of each 32.
         __half* pieces = reinterpret_cast<__half*>(smem + p.off_codes);
-        float* rs = reinterpret_cast<float*>(smem + p.off_rs);          // [MR][2]: 2^s, 2^-s
-        float* xs = reinterpret_cast<float*>(smem + p.off_aux);         // [MR][slice/32]
+        float* rs = reinterpret_cast<float*>(smem + p.off_rs);   // [MR][2]: 2^s, 2^-s
+        float* xs = reinterpret_cast<float*>(smem + p.off_aux);  // [MR][slice/32]
         const int warp = tid >> 5, lane = tid & 31;
-        for (int r = warp; r < MR; r += 8) {
-            int m = m0 + r;
+        for (int r = warp; r < MR; r += CW) {
+            const int m = m0 + r;
             float amax = 0.0f;
             if (m < p.M) {
                 const float4* src = reinterpret_cast<const float4*>(p.x + (long long)m * p.K + k0);
@@ -120,7 +149,7 @@ __device__ __forceinline__ void prepare_acts(const StreamParams& p, uint8_t* sme
             if (lane == 0) {
                 int s = 0;
                 if (amax > 0.0f) {
-                    int e = (int)((__float_as_uint(amax) >> 23) & 0xff) - 127;  // amax in [2^e, 2^(e+1))
+                    const int e = (int)((__float_as_uint(amax) >> 23) & 0xff) - 127;  // amax in [2^e, 2^(e+1))
                     s = 14 - e;
                     s = s > 100 ? 100 : (s < -100 ? -100 : s);
                 }
@@ -128,11 +157,11 @@ __device__ __forceinline__ void prepare_acts(const StreamParams& p, uint8_t* sme
                 rs[2 * r + 1] = ldexpf(1.0f, -s);
             }
         }
-        consumer_sync();
+        consumer_sync<CW>();
         const int nch = p.slice_units * Unit<WT>::vals / 32;  // chunks of 32 values
-        for (int idx = tid; idx < MR * nch; idx += 256) {
-            int r = idx / nch, c = idx - r * nch;
-            int m = m0 + r;
+        for (int idx = tid; idx < MR * nch; idx += NTH) {
+            const int r = idx / nch, c = idx - r * nch;
+            const int m = m0 + r;
             uint32_t hw[16], lw[16];
             float sum = 0.0f;
             if (m < p.M && c * 32 < klen) {
@@ -140,14 +169,14 @@ __device__ __forceinline__ void prepare_acts(const StreamParams& p, uint8_t* sme
                 const float4* src = reinterpret_cast<const float4*>(p.x + (long long)m * p.K + k0 + c * 32);
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    float4 v4 = __ldg(src + i);
-                    float v[4] = {__fmul_rn(v4.x, scale), __fmul_rn(v4.y, scale), __fmul_rn(v4.z, scale),
-                                  __fmul_rn(v4.w, scale)};
+                    const float4 v4 = __ldg(src + i);
+                    const float v[4] = {__fmul_rn(v4.x, scale), __fmul_rn(v4.y, scale), __fmul_rn(v4.z, scale),
+                                        __fmul_rn(v4.w, scale)};
                     uint32_t hb[4], lb[4];
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
-                        __half h = __float2half_rn(v[k]);
-                        __half l = __float2half_rn(__fsub_rn(v[k], __half2float(h)));
+                        const __half h = __float2half_rn(v[k]);
+                        const __half l = __float2half_rn(__fsub_rn(v[k], __half2float(h)));
                         hb[k] = __half_as_ushort(h);
                         lb[k] = __half_as_ushort(l);
                         sum = __fadd_rn(sum, v[k]);
@@ -174,19 +203,152 @@ __device__ __forceinline__ void prepare_acts(const StreamParams& p, uint8_t* sme
 }
 
 // ---------------------------------------------------------------------------
-// per-stage compute
+// P_DOT: per-thread dp4a over raw blocks (int8_act, NT = activation rows)
+// ---------------------------------------------------------------------------
+
+// acc[m] of the thread's row; rows r = warp * RPW + lane / LPR
+template <int WT, int NT, int EPI, int CW>
+__device__ __forceinline__ void stage_dot(const StreamParams& p, const uint8_t* smem, const uint8_t* st, int cnu,
+                                          int ur0, int gu0, int off, int warp, int lane, float (&acc)[8], int tile,
+                                          int m0) {
+    constexpr int RPW = 16 / CW, LPR = 32 / RPW;
+    const int r = warp * RPW + lane / LPR, j = lane % LPR;
+    const uint8_t* row = st + r * p.row_stride + off;
+    const uint8_t* codes = smem + p.off_codes;
+    const float* da = reinterpret_cast<const float*>(smem + p.off_scale);
+    const long long n = (long long)tile * kTileRows + r;
+    if (WT == T_Q8_0) {
+        constexpr int UPL = Unit<T_Q8_0>::per_stage / LPR;  // blocks per lane and stage
+#pragma unroll
+        for (int i = 0; i < UPL; ++i) {
+            const int b = j + LPR * i;
+            const bool live = b < cnu;
+            const int bc = live ? b : cnu - 1;
+            // the 34-byte block starts 2-byte aligned: read the 9 covering words
+            const uintptr_t addr = reinterpret_cast<uintptr_t>(row + 34 * bc);
+            const uint8_t* aw = reinterpret_cast<const uint8_t*>(addr & ~uintptr_t(3));
+            const uint32_t sh = (uint32_t)(addr & 2u) * 8u;  // 0 or 16
+            uint32_t w[9];
+#pragma unroll
+            for (int k = 0; k < 9; ++k) w[k] = ld32(aw + 4 * k);
+            const float dw = h2f(sh ? (w[0] >> 16) : w[0]);
+            uint32_t c[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) c[k] = __funnelshift_rc(w[k], w[k + 1], 16u + sh);
+            const int ub = ur0 + bc;
+#pragma unroll
+            for (int m = 0; m < NT; ++m) {
+                const uint4 a0 = ld128(codes + (2 * m) * p.code_pitch + ub * 16);
+                const uint4 a1 = ld128(codes + (2 * m + 1) * p.code_pitch + ub * 16);
+                int s0 = dp4a(c[0], a0.x, 0), s1 = dp4a(c[1], a0.y, 0);
+                s0 = dp4a(c[2], a0.z, s0);
+                s1 = dp4a(c[3], a0.w, s1);
+                s0 = dp4a(c[4], a1.x, s0);
+                s1 = dp4a(c[5], a1.y, s1);
+                s0 = dp4a(c[6], a1.z, s0);
+                s1 = dp4a(c[7], a1.w, s1);
+                const int isum = s0 + s1;
+                if (EPI == E_Y) {
+                    if (live) acc[m] = fmaf((float)isum, dw * da[m * p.scale_pitch + ub], acc[m]);
+                } else if (live && m0 + m < p.M && n < p.N) {
+                    p.sums[((long long)(m0 + m) * p.N + n) * p.units + gu0 + b] = isum;
+                }
+            }
+        }
+    } else {
+        constexpr int UPL = Unit<T_Q4_K>::per_stage * 4 / LPR;  // (super-block, pair) tasks per lane
+#pragma unroll
+        for (int i = 0; i < UPL; ++i) {
+            const int q = j + LPR * i;
+            const int u = q >> 2, c = q & 3;
+            const bool live = u < cnu;
+            const int uc = live ? u : cnu - 1;
+            const uint8_t* sb = row + 144 * uc;
+            const uint4 hw = ld128(sb);  // d, dmin, scales[0..11]
+            const uint4 q0 = ld128(sb + 16 + 32 * c), q1 = ld128(sb + 32 + 32 * c);
+            const int j0 = 2 * c, j1 = 2 * c + 1;
+            // 6-bit scale/min of sub-blocks j0, j1 (j0 < 4 <=> c < 2)
+            int sc0, mn0, sc1, mn1;
+            if (c < 2) {
+                sc0 = (int)((hw.y >> (8 * j0)) & 63u);
+                mn0 = (int)((hw.z >> (8 * j0)) & 63u);
+                sc1 = (int)((hw.y >> (8 * j1)) & 63u);
+                mn1 = (int)((hw.z >> (8 * j1)) & 63u);
+            } else {
+                const int k0 = j0 - 4, k1 = j1 - 4;
+                sc0 = (int)(((hw.w >> (8 * k0)) & 15u) | (((hw.y >> (8 * k0 + 6)) & 3u) << 4));
+                mn0 = (int)(((hw.w >> (8 * k0 + 4)) & 15u) | (((hw.z >> (8 * k0 + 6)) & 3u) << 4));
+                sc1 = (int)(((hw.w >> (8 * k1)) & 15u) | (((hw.y >> (8 * k1 + 6)) & 3u) << 4));
+                mn1 = (int)(((hw.w >> (8 * k1 + 4)) & 15u) | (((hw.z >> (8 * k1 + 6)) & 3u) << 4));
+            }
+            const uint32_t qq[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+            uint32_t lo[8], hi[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                lo[k] = qq[k] & 0x0F0F0F0Fu;
+                hi[k] = (qq[k] >> 4) & 0x0F0F0F0Fu;
+            }
+            const float fD = h2f(hw.x), fDm = h2f(hw.x >> 16);
+            const int pair = (ur0 + uc) * 4 + c;
+            const int* bs = reinterpret_cast<const int*>(smem + p.off_aux);
+#pragma unroll
+            for (int m = 0; m < NT; ++m) {
+                const uint4 a0 = ld128(codes + (4 * m + 0) * p.code_pitch + pair * 16);
+                const uint4 a1 = ld128(codes + (4 * m + 1) * p.code_pitch + pair * 16);
+                const uint4 a2 = ld128(codes + (4 * m + 2) * p.code_pitch + pair * 16);
+                const uint4 a3 = ld128(codes + (4 * m + 3) * p.code_pitch + pair * 16);
+                int s0 = dp4a(lo[0], a0.x, 0), s1 = dp4a(hi[0], a2.x, 0);
+                s0 = dp4a(lo[1], a0.y, s0);
+                s1 = dp4a(hi[1], a2.y, s1);
+                s0 = dp4a(lo[2], a0.z, s0);
+                s1 = dp4a(hi[2], a2.z, s1);
+                s0 = dp4a(lo[3], a0.w, s0);
+                s1 = dp4a(hi[3], a2.w, s1);
+                s0 = dp4a(lo[4], a1.x, s0);
+                s1 = dp4a(hi[4], a3.x, s1);
+                s0 = dp4a(lo[5], a1.y, s0);
+                s1 = dp4a(hi[5], a3.y, s1);
+                s0 = dp4a(lo[6], a1.z, s0);
+                s1 = dp4a(hi[6], a3.z, s1);
+                s0 = dp4a(lo[7], a1.w, s0);
+                s1 = dp4a(hi[7], a3.w, s1);
+                const int2 b2 = *reinterpret_cast<const int2*>(bs + m * p.aux_pitch + (ur0 + uc) * 8 + j0);
+                int ssc = live ? sc0 * s0 + sc1 * s1 : 0;
+                int smn = live ? mn0 * b2.x + mn1 * b2.y : 0;
+                if (EPI == E_Y) {
+                    const float dam = da[m * p.scale_pitch + ur0 + uc];
+                    acc[m] += dam * (fD * (float)ssc - fDm * (float)smn);
+                } else {
+                    // the four pairs of a super-block sit on four consecutive lanes
+                    ssc += __shfl_xor_sync(0xffffffffu, ssc, 1);
+                    smn += __shfl_xor_sync(0xffffffffu, smn, 1);
+                    ssc += __shfl_xor_sync(0xffffffffu, ssc, 2);
+                    smn += __shfl_xor_sync(0xffffffffu, smn, 2);
+                    if (live && c == 0 && m0 + m < p.M && n < p.N) {
+                        int* o = p.sums + (((long long)(m0 + m) * p.N + n) * p.units + gu0 + u) * 2;
+                        o[0] = ssc;
+                        o[1] = smn;
+                    }
+                }
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// P_MMA: warp tensor-core products over 16-row blocks
 // ---------------------------------------------------------------------------
 
 // acc layout: int8: acc[nt][0..3] = (row g, col 2t), (g, 2t+1), (g+8, 2t), (g+8, 2t+1)
 //             f32 : acc[nt][0..1] = (row g, act row 4nt+t), (g+8, 4nt+t)
-template <int WT, int AM, int NT, int EPI>
-__device__ __forceinline__ void compute_stage(const StreamParams& p, uint8_t* smem, const uint8_t* st, int nunits,
-                                              int ur0, int gu0, int off0, int off1, int warp, int lane,
-                                              float (&acc)[NT][4], int tile, int m0) {
+template <int WT, int AM, int NT, int EPI, int CW>
+__device__ __forceinline__ void stage_mma(const StreamParams& p, const uint8_t* smem, const uint8_t* st, int nunits,
+                                          int ur0, int gu0, int off0, int off1, int warp, int lane,
+                                          float (&acc)[NT][4], int tile, int m0) {
     const int g = lane >> 2, t = lane & 3;
     const uint8_t* row0 = st + g * p.row_stride + off0;
     const uint8_t* row1 = st + (g + 8) * p.row_stride + off1;
-    for (int u = warp; u < nunits; u += kConsumerWarps) {
+    for (int u = warp; u < nunits; u += CW) {
         const int ur = ur0 + u;  // unit index inside the K slice
         if (WT == T_Q8_0) {
             const uint8_t* b0 = row0 + u * 34;
@@ -201,7 +363,7 @@ __device__ __forceinline__ void compute_stage(const StreamParams& p, uint8_t* sm
                 const float* da = reinterpret_cast<const float*>(smem + p.off_scale);
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
-                    const uint2 bb = *reinterpret_cast<const uint2*>(codes + (nt * 8 + g) * p.code_pitch + ur * 32 + 8 * t);
+                    const uint2 bb = ld64(codes + (nt * 8 + g) * p.code_pitch + ur * 32 + 8 * t);
                     int d[4];
                     mma_s8(d, w0, v0, w1, v1, bb.x, bb.y);
                     if (EPI == E_Y) {
@@ -222,7 +384,7 @@ __device__ __forceinline__ void compute_stage(const StreamParams& p, uint8_t* sm
                     }
                 }
             } else {
-                const __half* pieces = reinterpret_cast<const __half*>(smem + p.off_codes);
+                const uint8_t* pieces = smem + p.off_codes;
                 const uint32_t A1a0 = s8x2_to_h2(w0, SEL01), A1a2 = s8x2_to_h2(w0, SEL23);
                 const uint32_t A1a1 = s8x2_to_h2(v0, SEL01), A1a3 = s8x2_to_h2(v0, SEL23);
                 const uint32_t A2a0 = s8x2_to_h2(w1, SEL01), A2a2 = s8x2_to_h2(w1, SEL23);
@@ -230,7 +392,7 @@ __device__ __forceinline__ void compute_stage(const StreamParams& p, uint8_t* sm
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
                     const int prow = 2 * (nt * 4 + (g >> 1)) + (g & 1);
-                    const uint4 bb = *reinterpret_cast<const uint4*>(pieces + (long long)prow * p.code_pitch + ur * 32 + 8 * t);
+                    const uint4 bb = ld128(pieces + ((long long)prow * p.code_pitch + ur * 32 + 8 * t) * 2);
                     float d[4] = {0.f, 0.f, 0.f, 0.f};
                     mma_f16(d, A1a0, A1a1, A1a2, A1a3, bb.x, bb.y);
                     mma_f16(d, A2a0, A2a1, A2a2, A2a3, bb.z, bb.w);
@@ -241,13 +403,9 @@ __device__ __forceinline__ void compute_stage(const StreamParams& p, uint8_t* sm
         } else {  // Q4_K super-block
             const uint8_t* s0 = row0 + u * 144;
             const uint8_t* s1 = row1 + u * 144;
-            const uint32_t hd0 = *reinterpret_cast<const uint32_t*>(s0);
-            const uint32_t hd1 = *reinterpret_cast<const uint32_t*>(s1);
-            const uint32_t W00 = *reinterpret_cast<const uint32_t*>(s0 + 4), W01 = *reinterpret_cast<const uint32_t*>(s0 + 8),
-                           W02 = *reinterpret_cast<const uint32_t*>(s0 + 12);
-            const uint32_t W10 = *reinterpret_cast<const uint32_t*>(s1 + 4), W11 = *reinterpret_cast<const uint32_t*>(s1 + 8),
-                           W12 = *reinterpret_cast<const uint32_t*>(s1 + 12);
-            const float fD0 = h2f(hd0), fDm0 = h2f(hd0 >> 16), fD1 = h2f(hd1), fDm1 = h2f(hd1 >> 16);
+            const uint4 h0 = ld128(s0), h1 = ld128(s1);
+            const uint32_t W00 = h0.y, W01 = h0.z, W02 = h0.w, W10 = h1.y, W11 = h1.z, W12 = h1.w;
+            const float fD0 = h2f(h0.x), fDm0 = h2f(h0.x >> 16), fD1 = h2f(h1.x), fDm1 = h2f(h1.x >> 16);
             if (AM == A_INT8) {
                 const uint8_t* codes = smem + p.off_codes;
                 const float* da = reinterpret_cast<const float*>(smem + p.off_scale);
@@ -259,8 +417,8 @@ __device__ __forceinline__ void compute_stage(const StreamParams& p, uint8_t* sm
                     for (int i = 0; i < 4; ++i) ssc[nt][i] = smn[nt][i] = 0;
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
-                    const uint2 q0 = *reinterpret_cast<const uint2*>(s0 + 16 + 32 * c + 8 * t);
-                    const uint2 q1 = *reinterpret_cast<const uint2*>(s1 + 16 + 32 * c + 8 * t);
+                    const uint2 q0 = ld64(s0 + 16 + 32 * c + 8 * t);
+                    const uint2 q1 = ld64(s1 + 16 + 32 * c + 8 * t);
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         const int j = 2 * c + h;
@@ -270,7 +428,7 @@ __device__ __forceinline__ void compute_stage(const StreamParams& p, uint8_t* sm
                         const int sc1 = q4k_sc(W10, W12, j), mn1 = q4k_mn(W11, W12, j);
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt) {
-                            const uint2 bb = *reinterpret_cast<const uint2*>(codes + (nt * 8 + g) * p.code_pitch + ur * 256 + 32 * j + 8 * t);
+                            const uint2 bb = ld64(codes + (nt * 8 + g) * p.code_pitch + ur * 256 + 32 * j + 8 * t);
                             int d[4];
                             mma_s8(d, a0, a1, a2, a3, bb.x, bb.y);
                             const int bs0 = bs[(nt * 8 + 2 * t) * p.aux_pitch + ur * 8 + j];
@@ -306,12 +464,12 @@ __device__ __forceinline__ void compute_stage(const StreamParams& p, uint8_t* sm
                     }
                 }
             } else {
-                const __half* pieces = reinterpret_cast<const __half*>(smem + p.off_codes);
+                const uint8_t* pieces = smem + p.off_codes;
                 const float* xs = reinterpret_cast<const float*>(smem + p.off_aux);
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
-                    const uint2 q0 = *reinterpret_cast<const uint2*>(s0 + 16 + 32 * c + 8 * t);
-                    const uint2 q1 = *reinterpret_cast<const uint2*>(s1 + 16 + 32 * c + 8 * t);
+                    const uint2 q0 = ld64(s0 + 16 + 32 * c + 8 * t);
+                    const uint2 q1 = ld64(s1 + 16 + 32 * c + 8 * t);
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         const int j = 2 * c + h;
@@ -326,7 +484,7 @@ __device__ __forceinline__ void compute_stage(const StreamParams& p, uint8_t* sm
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt) {
                             const int prow = 2 * (nt * 4 + (g >> 1)) + (g & 1);
-                            const uint4 bb = *reinterpret_cast<const uint4*>(pieces + (long long)prow * p.code_pitch + ur * 256 + 32 * j + 8 * t);
+                            const uint4 bb = ld128(pieces + ((long long)prow * p.code_pitch + ur * 256 + 32 * j + 8 * t) * 2);
                             float d[4] = {0.f, 0.f, 0.f, 0.f};
                             mma_f16(d, A1a0, A1a1, A1a2, A1a3, bb.x, bb.y);
                             mma_f16(d, A2a0, A2a1, A2a2, A2a3, bb.z, bb.w);
@@ -345,10 +503,12 @@ __device__ __forceinline__ void compute_stage(const StreamParams& p, uint8_t* sm
 // the kernel
 // ---------------------------------------------------------------------------
 
-template <int WT, int AM, int NT, int EPI>
-__global__ void __launch_bounds__(kThreads, 1) qmm_stream_kernel(const StreamParams p) {
-    extern __shared__ __align__(128) uint8_t smem[];
+template <int WT, int AM, int NT, int EPI, int PATH>
+__global__ void __launch_bounds__((consumer_warps(WT, AM, NT, PATH) + 1) * 32, 1)
+    qmm_stream_kernel(const StreamParams p) {
+    constexpr int CW = consumer_warps(WT, AM, NT, PATH);
     constexpr int UB = Unit<WT>::bytes;
+    extern __shared__ __align__(128) uint8_t smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int S = p.stages;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem);  // full[S], empty[S]
@@ -357,14 +517,14 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_stream_kernel(const StreamPar
     const int slice = pair % p.kslices, mc = pair / p.kslices;
     const int tile0 = blockIdx.x / p.pairs;
     const int m0 = mc * p.mr;
-    const int su0 = slice * p.slice_units;                                   // first unit of the slice
-    const int sunits = min(p.slice_units, p.units - su0);                    // units in this slice
+    const int su0 = slice * p.slice_units;                 // first unit of the slice
+    const int sunits = min(p.slice_units, p.units - su0);  // units in this slice
     const int nchunks = (sunits + p.ups - 1) / p.ups;
 
     if (tid == 0) {
         for (int i = 0; i < S; ++i) {
             mbar_init(smem_u32(&bars[i]), 1);
-            mbar_init(smem_u32(&bars[S + i]), kConsumerWarps);
+            mbar_init(smem_u32(&bars[S + i]), CW);
         }
         flags[0] = 0;
         flags[1] = 0;
@@ -372,71 +532,81 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_stream_kernel(const StreamPar
     }
     __syncthreads();
 
-    if (warp == kConsumerWarps) {
+    if (warp == CW) {
         // ----------------------------- producer -----------------------------
-        if (lane != 0) return;
+        // Lane r (< 16) owns weight row r of the tile: it copies the 16-byte
+        // aligned superset of the row's chunk with one bulk copy (and the
+        // ragged tail at the very end of the buffer with plain loads); lane 0
+        // waits for the slot and posts the stage's byte count.
         long long g = 0;
         bool ok = true;
         for (int tile = tile0; tile < p.ntiles && ok; tile += p.per_pair) {
-            for (int ch = 0; ch < nchunks && ok; ++ch, ++g) {
+            const long long row = (long long)tile * kTileRows + lane;
+            const bool has_row = lane < kTileRows && row < p.N;
+            for (int ch = 0; ch < nchunks; ++ch, ++g) {
                 const int slot = (int)(g % S);
-                if (g >= S) ok = mbar_wait(smem_u32(&bars[S + slot]), (uint32_t)(((g / S) - 1) & 1), flags, p.err);
-                if (!ok) break;
+                if (g >= S) {
+                    int okl = 1;
+                    if (lane == 0) okl = mbar_wait(smem_u32(&bars[S + slot]), (uint32_t)(((g / S) - 1) & 1), flags, p.err);
+                    ok = __shfl_sync(0xffffffffu, okl, 0) != 0;
+                    if (!ok) break;
+                }
                 const int cu0 = su0 + ch * p.ups;
                 const int cnu = min(p.ups, su0 + sunits - cu0);
                 uint8_t* st = smem + p.off_stage + (long long)slot * kTileRows * p.row_stride;
-                uint32_t tx = 0;
-                // pass 1: tail bytes by plain loads (rows whose 16-byte superset
-                // would run past the end of the weight buffer), and tx bytes
-                for (int r = 0; r < kTileRows; ++r) {
-                    const long long row = (long long)tile * kTileRows + r;
-                    if (row >= p.N) break;
-                    const long long s = row * p.rb + (long long)cu0 * UB;
-                    const long long a = s & ~15ll, e = s + (long long)cnu * UB;
+                uint32_t bytes = 0;
+                long long a = 0;
+                if (has_row) {
+                    const long long s0 = row * p.rb + (long long)cu0 * UB;
+                    const long long e = s0 + (long long)cnu * UB;
+                    a = s0 & ~15ll;
                     long long b = (e + 15) & ~15ll;
                     if (b > p.total_bytes) {
                         b = e & ~15ll;
-                        for (long long q = b; q < e; ++q) st[r * p.row_stride + (q - a)] = p.wq[q];
+                        for (long long q = b; q < e; ++q) st[lane * p.row_stride + (q - a)] = p.wq[q];
+                        fence_proxy_async();
                     }
-                    if (b > a) tx += (uint32_t)(b - a);
+                    if (b > a) bytes = (uint32_t)(b - a);
                 }
-                fence_proxy_async();
+                const uint32_t tx = __reduce_add_sync(0xffffffffu, bytes);
                 const uint32_t fb = smem_u32(&bars[slot]);
-                mbar_arrive_tx(fb, tx);
-                for (int r = 0; r < kTileRows; ++r) {
-                    const long long row = (long long)tile * kTileRows + r;
-                    if (row >= p.N) break;
-                    const long long s = row * p.rb + (long long)cu0 * UB;
-                    const long long a = s & ~15ll, e = s + (long long)cnu * UB;
-                    long long b = (e + 15) & ~15ll;
-                    if (b > p.total_bytes) b = e & ~15ll;
-                    if (b > a) bulk_g2s(smem_u32(st + r * p.row_stride), p.wq + a, (uint32_t)(b - a), fb);
-                }
+                if (lane == 0) mbar_arrive_tx(fb, tx);
+                __syncwarp();
+                if (bytes) bulk_g2s(smem_u32(st + lane * p.row_stride), p.wq + a, bytes, fb);
             }
         }
         // wait for the copies still in flight into this block's stages
-        const long long first = g > S ? g - S : 0;
-        for (long long q = first; q < g; ++q) mbar_wait(smem_u32(&bars[q % S]), (uint32_t)((q / S) & 1), flags, p.err);
+        if (lane == 0) {
+            const long long first = g > S ? g - S : 0;
+            for (long long q = first; q < g; ++q) mbar_wait(smem_u32(&bars[q % S]), (uint32_t)((q / S) & 1), flags, p.err);
+        }
         return;
     }
 
     // ------------------------------- consumers -------------------------------
     const int k0 = su0 * Unit<WT>::vals;
     const int klen = sunits * Unit<WT>::vals;
-    if (EPI == E_Y || true) prepare_acts<WT, AM>(p, smem, m0, k0, klen, tid);
-    consumer_sync();
+    prepare_acts<WT, AM, PATH, CW>(p, smem, m0, k0, klen, tid);
+    consumer_sync<CW>();
 
+    constexpr int MR = chunk_rows(AM, NT, PATH);
+    constexpr int NRED = PATH == P_DOT ? 1 : CW;  // partial sums per output in `red`
     float* red = reinterpret_cast<float*>(smem + p.off_red);
     const float* rs = reinterpret_cast<const float*>(smem + p.off_rs);
     const int g8 = lane >> 2, t4 = lane & 3;
+    constexpr int RPW = 16 / CW, LPR = 32 / (RPW > 0 ? RPW : 1);
+    const int dot_row = PATH == P_DOT ? warp * RPW + lane / LPR : 0;
     long long g = 0;
     for (int tile = tile0; tile < p.ntiles; tile += p.per_pair) {
         float acc[NT][4];
+        float dacc[8];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
             for (int i = 0; i < 4; ++i) acc[nt][i] = 0.0f;
-        const long long rowA = (long long)tile * kTileRows + g8, rowB = rowA + 8;
+#pragma unroll
+        for (int m = 0; m < 8; ++m) dacc[m] = 0.0f;
+        const long long rowA = (long long)tile * kTileRows + (PATH == P_DOT ? dot_row : g8), rowB = rowA + 8;
         for (int ch = 0; ch < nchunks; ++ch, ++g) {
             const int slot = (int)(g % S);
             const bool ok = mbar_wait(smem_u32(&bars[slot]), (uint32_t)((g / S) & 1), flags, p.err);
@@ -445,35 +615,48 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_stream_kernel(const StreamPar
             if (ok) {
                 const uint8_t* st = smem + p.off_stage + (long long)slot * kTileRows * p.row_stride;
                 const int off0 = (int)((rowA * p.rb + (long long)cu0 * UB) & 15);
-                const int off1 = (int)((rowB * p.rb + (long long)cu0 * UB) & 15);
-                compute_stage<WT, AM, NT, EPI>(p, smem, st, cnu, cu0 - su0, cu0, off0, off1, warp, lane, acc, tile, m0);
+                if (PATH == P_DOT) {
+                    stage_dot<WT, NT, EPI, CW>(p, smem, st, cnu, cu0 - su0, cu0, off0, warp, lane, dacc, tile, m0);
+                } else {
+                    const int off1 = (int)((rowB * p.rb + (long long)cu0 * UB) & 15);
+                    stage_mma<WT, AM, NT, EPI, CW>(p, smem, st, cnu, cu0 - su0, cu0, off0, off1, warp, lane, acc, tile, m0);
+                }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&bars[S + slot]));
         }
         if (EPI != E_Y) continue;
-        // ---- cross-warp reduction of the tile: red[warp][16][mr]
-        const int MR = p.mr;
-        float* rw = red + warp * kTileRows * MR;
+        // ---- tile epilogue: red[NRED][16][MR], then sum, scale and store
+        if (PATH == P_DOT) {
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            if (AM == A_INT8) {
-                rw[g8 * MR + nt * 8 + 2 * t4] = acc[nt][0];
-                rw[g8 * MR + nt * 8 + 2 * t4 + 1] = acc[nt][1];
-                rw[(g8 + 8) * MR + nt * 8 + 2 * t4] = acc[nt][2];
-                rw[(g8 + 8) * MR + nt * 8 + 2 * t4 + 1] = acc[nt][3];
-            } else {
-                rw[g8 * MR + nt * 4 + t4] = acc[nt][0];
-                rw[(g8 + 8) * MR + nt * 4 + t4] = acc[nt][1];
+            for (int m = 0; m < NT; ++m) {
+                float v = dacc[m];
+#pragma unroll
+                for (int o = LPR / 2; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+                if (lane % LPR == 0) red[dot_row * MR + m] = v;
+            }
+        } else {
+            float* rw = red + warp * kTileRows * MR;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                if (AM == A_INT8) {
+                    rw[g8 * MR + nt * 8 + 2 * t4] = acc[nt][0];
+                    rw[g8 * MR + nt * 8 + 2 * t4 + 1] = acc[nt][1];
+                    rw[(g8 + 8) * MR + nt * 8 + 2 * t4] = acc[nt][2];
+                    rw[(g8 + 8) * MR + nt * 8 + 2 * t4 + 1] = acc[nt][3];
+                } else {
+                    rw[g8 * MR + nt * 4 + t4] = acc[nt][0];
+                    rw[(g8 + 8) * MR + nt * 4 + t4] = acc[nt][1];
+                }
             }
         }
-        consumer_sync();
+        consumer_sync<CW>();
         const bool aborted = flags[0] != 0;
-        for (int o = tid; o < kTileRows * MR; o += 256) {
+        for (int o = tid; o < kTileRows * MR; o += CW * 32) {
             const int r = o / MR, c = o - r * MR;
             float v = 0.0f;
 #pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) v += red[(w * kTileRows + r) * MR + c];
+            for (int w = 0; w < NRED; ++w) v += red[(w * kTileRows + r) * MR + c];
             if (AM == A_F32) v *= rs[2 * c + 1];
             const long long n = (long long)tile * kTileRows + r;
             const int m = m0 + c;
@@ -484,15 +667,15 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_stream_kernel(const StreamPar
         }
         if (p.kslices > 1) {
             __threadfence();
-            consumer_sync();
+            consumer_sync<CW>();
             if (tid == 0) {
                 const unsigned old = atomicAdd(&p.counters[(long long)mc * p.ntiles + tile], 1u);
                 flags[1] = (old == (unsigned)(p.kslices - 1)) ? 1 : 0;
             }
-            consumer_sync();
+            consumer_sync<CW>();
             if (flags[1] && !aborted) {
                 __threadfence();
-                for (int o = tid; o < kTileRows * MR; o += 256) {
+                for (int o = tid; o < kTileRows * MR; o += CW * 32) {
                     const int r = o / MR, c = o - r * MR;
                     const long long n = (long long)tile * kTileRows + r;
                     const int m = m0 + c;
@@ -504,23 +687,29 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_stream_kernel(const StreamPar
                 }
             }
         }
-        consumer_sync();
+        consumer_sync<CW>();
     }
 }
 
 // ---------------------------------------------------------------------------
-// host-side planning (shared-memory layout, grid, split of K)
+// host-side planning (path, shared-memory layout, grid, split of K)
 // ---------------------------------------------------------------------------
 
 struct StreamPlan {
     StreamParams p;
     int nt;
+    int path;
+    int cw;
     int grid;
     size_t smem;
     size_t workspace;  // bytes of partial sums + counters (0 when K is not split)
 };
 
 inline int round_up(int v, int a) { return (v + a - 1) / a * a; }
+
+// largest M served by the per-thread dp4a path (int8_act)
+constexpr int kDotMaxQ8_0 = 8;
+constexpr int kDotMaxQ4_K = 4;
 
 // Fills the layout for wtype/mode/epilogue and sizes; returns false if no
 // layout fits in smem_max.
@@ -529,11 +718,18 @@ inline bool plan_stream(int wt, int am, int epi, long long M, long long N, long 
     StreamPlan pl{};
     StreamParams& p = pl.p;
     const int uv = wt == T_Q8_0 ? 32 : 256, ub = wt == T_Q8_0 ? 34 : 144;
-    int nt;
-    if (am == A_INT8) nt = M <= 8 ? 1 : M <= 16 ? 2 : M <= 32 ? 4 : 8;
-    else nt = M <= 4 ? 1 : M <= 8 ? 2 : M <= 16 ? 4 : 8;
-    if (wt == T_Q4_K && am == A_INT8 && nt > 4) nt = 4;  // register budget of the integer super-block sums
-    const int mr = am == A_INT8 ? 8 * nt : 4 * nt;
+    int nt, path;
+    if (am == A_INT8 && M <= (wt == T_Q8_0 ? kDotMaxQ8_0 : kDotMaxQ4_K)) {
+        path = P_DOT;
+        nt = M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : 8;
+    } else {
+        path = P_MMA;
+        if (am == A_INT8) nt = M <= 8 ? 1 : M <= 16 ? 2 : M <= 32 ? 4 : 8;
+        else nt = M <= 4 ? 1 : M <= 8 ? 2 : M <= 16 ? 4 : 8;
+        if (wt == T_Q4_K && am == A_INT8 && nt > 4) nt = 4;  // register budget of the integer super-block sums
+    }
+    const int cw = consumer_warps(wt, am, nt, path);
+    const int mr = chunk_rows(am, nt, path);
     p.M = (int)M;
     p.N = (int)N;
     p.K = (int)K;
@@ -543,19 +739,29 @@ inline bool plan_stream(int wt, int am, int epi, long long M, long long N, long 
     p.rb = (long long)p.units * ub;
     p.total_bytes = p.rb * N;
     p.ntiles = (int)((N + kTileRows - 1) / kTileRows);
-    const int ups_max = wt == T_Q8_0 ? 32 : 8;  // 1024 (Q8_0) or 2048 (Q4_K) values per stage
-    const int red_bytes = kConsumerWarps * kTileRows * mr * 4;
+    const int ups_max = wt == T_Q8_0 ? Unit<T_Q8_0>::per_stage : Unit<T_Q4_K>::per_stage;
+    const int nred = path == P_DOT ? 1 : cw;
+    const int red_bytes = nred * kTileRows * mr * 4;
     for (int ks = 1; ks <= p.units; ++ks) {
         const int su = (p.units + ks - 1) / ks;
         if ((long long)(ks - 1) * su >= p.units) continue;  // empty last slice
         const int ups = su < ups_max ? su : ups_max;
-        const int row_stride = round_up(ups * ub + 32, 16) + 16;
+        // row pitch in a stage: room for the 16-byte superset; the remainder
+        // mod 128 spreads the rows of one access over the banks
+        const int want = path == P_DOT ? 64 : 16;
+        int row_stride = round_up(ups * ub + 32, 16);
+        row_stride += ((want - row_stride % 128) + 128) % 128;
         const int stage_bytes = kTileRows * row_stride;
         const int kv = su * uv;  // values per slice
         int codes, scale_pitch = 0, aux_pitch = 0, code_pitch;
         if (am == A_INT8) {
-            code_pitch = kv + 16;
-            codes = mr * code_pitch;
+            if (path == P_DOT) {
+                code_pitch = wt == T_Q8_0 ? su * 16 : su * 4 * 16;  // bytes per (row, 16-byte plane)
+                codes = mr * kv;
+            } else {
+                code_pitch = kv + 16;
+                codes = mr * code_pitch;
+            }
             scale_pitch = su;
             if (wt == T_Q4_K) aux_pitch = su * 8;
         } else {
@@ -600,9 +806,6 @@ inline bool plan_stream(int wt, int am, int epi, long long M, long long N, long 
         break;
     }
     if (p.kslices == 0) return false;
-    if (epi == E_SUMS) {
-        // sums need no reduction: the workspace is not used
-    }
     p.pairs = p.kslices * p.mchunks;
     int per = sm_count / p.pairs;
     if (per < 1) per = 1;
@@ -610,6 +813,8 @@ inline bool plan_stream(int wt, int am, int epi, long long M, long long N, long 
     p.per_pair = per;
     pl.grid = p.pairs * per;
     pl.nt = nt;
+    pl.path = path;
+    pl.cw = cw;
     pl.workspace = (epi == E_Y && p.kslices > 1)
                        ? (size_t)p.kslices * (size_t)M * (size_t)N * 4 + (size_t)p.mchunks * p.ntiles * 4 + 256
                        : 0;

@@ -1,23 +1,23 @@
-// qmm_stream_q8_0.cu -- instantiations of the streaming block-MMA kernel for
-// Q8_0 weights (both activation forms, both epilogues) and their launcher.
+// qmm_stream_q8_0_mma.cu -- instantiations of the streaming kernel for
+// Q8_0 weights on the P_MMA consumer path, and their launcher.
 #include "qmm_internal.h"
 
 namespace qmm {
 namespace {
 unsigned long long g_smem_done[2][2][4];
-}
 
 template <int AM, int NT, int EPI>
-static cudaError_t go(const StreamPlan& pl, int smem_max, cudaStream_t s, unsigned long long& done) {
-    auto* k = qmm_stream_kernel<T_Q8_0, AM, NT, EPI>;
+cudaError_t go(const StreamPlan& pl, int smem_max, cudaStream_t s, unsigned long long& done) {
+    auto* k = qmm_stream_kernel<T_Q8_0, AM, NT, EPI, P_MMA>;
     cudaError_t e = ensure_smem(k, smem_max, done);
     if (e != cudaSuccess) return e;
-    k<<<pl.grid, kThreads, pl.smem, s>>>(pl.p);
+    constexpr int threads = (consumer_warps(T_Q8_0, AM, NT, P_MMA) + 1) * 32;
+    k<<<pl.grid, threads, pl.smem, s>>>(pl.p);
     return cudaGetLastError();
 }
 
 template <int AM, int EPI>
-static cudaError_t by_nt(const StreamPlan& pl, int smem_max, cudaStream_t s) {
+cudaError_t by_nt(const StreamPlan& pl, int smem_max, cudaStream_t s) {
     unsigned long long* d = g_smem_done[AM][EPI];
     switch (pl.nt) {
         case 1: return go<AM, 1, EPI>(pl, smem_max, s, d[0]);
@@ -27,8 +27,9 @@ static cudaError_t by_nt(const StreamPlan& pl, int smem_max, cudaStream_t s) {
         default: return cudaErrorInvalidValue;
     }
 }
+}  // namespace
 
-cudaError_t launch_stream_q8_0(int am, int epi, const StreamPlan& pl, int smem_max, cudaStream_t s) {
+cudaError_t launch_stream_q8_0_mma(int am, int epi, const StreamPlan& pl, int smem_max, cudaStream_t s) {
     if (am == A_INT8 && epi == E_Y) return by_nt<A_INT8, E_Y>(pl, smem_max, s);
     if (am == A_INT8 && epi == E_SUMS) return by_nt<A_INT8, E_SUMS>(pl, smem_max, s);
     if (am == A_F32 && epi == E_Y) return by_nt<A_F32, E_Y>(pl, smem_max, s);
