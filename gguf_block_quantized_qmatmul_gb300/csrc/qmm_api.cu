@@ -64,15 +64,25 @@ qmm_status stream_call(qmm_type wtype, int am, int epi, const void* wq, const fl
     unsigned* err = nullptr;
     int sms = 0, smem = 0;
     if (device_info(&err, &sms, &smem) != cudaSuccess) return QMM_ERR_CUDA;
-    StreamPlan pl;
     const int wt = wtype == QMM_Q8_0 ? T_Q8_0 : T_Q4_K;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    GemvPlan gp;
+    if (am == A_INT8 && plan_gemv(wt, M, N, K, sms, smem, gp)) {  // decode: whole-row weight stream
+        gp.p.wq = static_cast<const uint8_t*>(wq);
+        gp.p.x = x;
+        gp.p.y = y;
+        gp.p.sums = sums;
+        gp.p.err = err;
+        const cudaError_t e = wt == T_Q8_0 ? launch_gemv_q8_0(epi, gp, smem, s) : launch_gemv_q4_k(epi, gp, smem, s);
+        return e == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
+    }
+    StreamPlan pl;
     if (!plan_stream(wt, am, epi, M, N, K, sms, smem, pl)) return QMM_ERR_SHAPE;
     pl.p.wq = static_cast<const uint8_t*>(wq);
     pl.p.x = x;
     pl.p.y = y;
     pl.p.sums = sums;
     pl.p.err = err;
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (epi == E_Y && pl.p.kslices > 1) {
         const size_t need = workspace_for(pl);
         if (!ws || ws_bytes < need) return QMM_ERR_WORKSPACE;
@@ -82,7 +92,7 @@ qmm_status stream_call(qmm_type wtype, int am, int epi, const void* wq, const fl
         if (cudaMemsetAsync(pl.p.counters, 0, (size_t)pl.p.mchunks * pl.p.ntiles * 4, s) != cudaSuccess)
             return QMM_ERR_CUDA;
     }
-    const cudaError_t e = launch_stream(wt, am, epi, pl, smem, s);
+    const cudaError_t e = wt == T_Q8_0 ? launch_stream_q8_0(am, epi, pl, smem, s) : launch_stream_q4_k(am, epi, pl, smem, s);
     return e == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
 }
 
@@ -156,6 +166,8 @@ size_t qmm_matmul_workspace(qmm_type wtype, qmm_act_mode mode, int64_t M, int64_
     if (check_shape(wtype, N, K) != QMM_OK || M <= 0 || M > INT32_MAX || N == 0 || K == 0) return 0;
     int sms = 0, smem = 0;
     if (device_info(nullptr, &sms, &smem) != cudaSuccess) return 0;
+    GemvPlan gp;
+    if (mode == QMM_INT8_ACT && plan_gemv(wtype == QMM_Q8_0 ? T_Q8_0 : T_Q4_K, M, N, K, sms, smem, gp)) return 0;
     StreamPlan pl;
     if (!plan_stream(wtype == QMM_Q8_0 ? T_Q8_0 : T_Q4_K, mode == QMM_INT8_ACT ? A_INT8 : A_F32, E_Y, M, N, K, sms,
                      smem, pl))

@@ -214,7 +214,8 @@ __device__ __forceinline__ void lds8_unaligned(const uint8_t* p, uint32_t& r0, u
 // ---------------------------------------------------------------------------
 
 constexpr int kTileRows = 16;  // weight rows per tile (the MMA M dimension)
-enum : int { P_MMA = 0, P_DOT = 1 };  // consumer path: warp MMA tiles, or per-thread dp4a
+
+inline int round_up(int v, int a) { return (v + a - 1) / a * a; }
 
 struct StreamParams {
     const uint8_t* wq;

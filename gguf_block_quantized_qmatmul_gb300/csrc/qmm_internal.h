@@ -3,22 +3,17 @@
 
 #include <cuda_runtime.h>
 
+#include "qmm_gemv.cuh"
 #include "qmm_stream.cuh"
 
 namespace qmm {
 
 cudaError_t launch_quantize(int type, const float* x, long long rows, long long K, void* out, cudaStream_t s);
 cudaError_t launch_dequantize(int type, const void* q, long long rows, long long K, float* out, cudaStream_t s);
-cudaError_t launch_stream_q8_0_mma(int am, int epi, const StreamPlan& plan, int smem_max, cudaStream_t s);
-cudaError_t launch_stream_q8_0_dot(int am, int epi, const StreamPlan& plan, int smem_max, cudaStream_t s);
-cudaError_t launch_stream_q4_k_mma(int am, int epi, const StreamPlan& plan, int smem_max, cudaStream_t s);
-cudaError_t launch_stream_q4_k_dot(int am, int epi, const StreamPlan& plan, int smem_max, cudaStream_t s);
-
-inline cudaError_t launch_stream(int wt, int am, int epi, const StreamPlan& pl, int smem_max, cudaStream_t s) {
-    if (wt == T_Q8_0)
-        return pl.path == P_DOT ? launch_stream_q8_0_dot(am, epi, pl, smem_max, s) : launch_stream_q8_0_mma(am, epi, pl, smem_max, s);
-    return pl.path == P_DOT ? launch_stream_q4_k_dot(am, epi, pl, smem_max, s) : launch_stream_q4_k_mma(am, epi, pl, smem_max, s);
-}
+cudaError_t launch_stream_q8_0(int am, int epi, const StreamPlan& plan, int smem_max, cudaStream_t s);
+cudaError_t launch_stream_q4_k(int am, int epi, const StreamPlan& plan, int smem_max, cudaStream_t s);
+cudaError_t launch_gemv_q8_0(int epi, const GemvPlan& plan, int smem_max, cudaStream_t s);
+cudaError_t launch_gemv_q4_k(int epi, const GemvPlan& plan, int smem_max, cudaStream_t s);
 
 // Raise a kernel's dynamic shared-memory limit once per device.
 template <typename F>

@@ -3,16 +3,11 @@
 // One persistent CTA per SM.  A producer warp streams the raw GGUF bytes of
 // 16-row weight tiles into a ring of shared-memory stages with 1-D bulk
 // copies (cp.async.bulk, mbarrier completion); CW consumer warps compute on
-// each stage while the next ones are in flight.  Two consumer paths:
-//
-//   P_DOT (int8_act, M <= 8, the decode GEMV): one thread per (weight row,
-//     block): it reads the raw 34-byte Q8_0 block (or a 64-value Q4_K pair of
-//     sub-blocks) and takes dp4a dot products with the quantized activation
-//     rows; the lanes of a row are summed with shuffles at the end of a tile.
-//   P_MMA (everything else): one warp-level tensor-core product per 32-value
-//     block (Q8_0) or sub-block (Q4_K) of 16 rows against 8 activation rows
-//     (int8: mma.m16n8k32.s8, exact int32 block sums) or 4 activation rows
-//     split into two f16 pieces (f32_act: mma.m16n8k16.f16, f32 accumulate).
+// each stage while the next ones are in flight: one warp-level tensor-core
+// product per 32-value block (Q8_0) or sub-block (Q4_K) of 16 rows against 8
+// activation rows (int8: mma.m16n8k32.s8, exact int32 block sums) or 4
+// activation rows split into two f16 pieces (f32_act: mma.m16n8k16.f16, f32
+// accumulate).  (Decode int8_act with M <= 8 runs in qmm_gemv.cuh instead.)
 //
 // Block arithmetic ("同一个 GGUF，CPU 和 Metal 生成的文字不一样" section 出处):
 //   int8_act (CPU form): per-block exact int32 sums isum of weight codes times
@@ -47,19 +42,17 @@ struct Unit<T_Q4_K> {
 };
 
 // consumer warps per CTA for a kernel variant (host and device agree on it)
-__host__ __device__ constexpr int consumer_warps(int wt, int am, int nt, int path) {
-    return path == P_DOT ? 16 : (wt == T_Q8_0 && nt <= 2 ? 16 : 8);
+__host__ __device__ constexpr int consumer_warps(int wt, int am, int nt) {
+    return wt == T_Q8_0 && nt <= 2 ? 16 : 8;
 }
 // activation rows per CTA chunk
-__host__ __device__ constexpr int chunk_rows(int am, int nt, int path) {
-    return path == P_DOT ? nt : (am == A_INT8 ? 8 * nt : 4 * nt);
-}
+__host__ __device__ constexpr int chunk_rows(int am, int nt) { return am == A_INT8 ? 8 * nt : 4 * nt; }
 
 // ---------------------------------------------------------------------------
 // activation preparation (consumer warps)
 // ---------------------------------------------------------------------------
 
-template <int WT, int AM, int PATH, int CW>
+template <int WT, int AM, int CW>
 __device__ __forceinline__ void prepare_acts(const StreamParams& p, uint8_t* smem, int m0, int k0, int klen, int tid) {
     constexpr int NTH = CW * 32;
     const int MR = p.mr;
@@ -77,14 +70,8 @@ __device__ __forceinline__ void prepare_acts(const StreamParams& p, uint8_t* sme
                 quant_q8_0_32(p.x + (long long)m * p.K + k0 + b * 32, c, d);
                 s = h2f(f2h(d));
             }
-            uint4 *d0, *d1;
-            if (PATH == P_DOT) {  // two 16-byte halves in separate planes: [r][half][block]
-                d0 = reinterpret_cast<uint4*>(codes + (2 * r) * p.code_pitch + b * 16);
-                d1 = reinterpret_cast<uint4*>(codes + (2 * r + 1) * p.code_pitch + b * 16);
-            } else {
-                d0 = reinterpret_cast<uint4*>(codes + r * p.code_pitch + b * 32);
-                d1 = d0 + 1;
-            }
+            uint4* d0 = reinterpret_cast<uint4*>(codes + r * p.code_pitch + b * 32);
+            uint4* d1 = d0 + 1;
             *d0 = make_uint4(c[0], c[1], c[2], c[3]);
             *d1 = make_uint4(c[4], c[5], c[6], c[7]);
             da[r * p.scale_pitch + b] = s;
@@ -112,15 +99,8 @@ __device__ __forceinline__ void prepare_acts(const StreamParams& p, uint8_t* sme
                         sum += bsum4(w[i]);
                     }
                 }
-                uint4 *d0, *d1;
-                if (PATH == P_DOT) {  // 64-value pairs split in four 16-byte planes: [r][piece][pair]
-                    const int pair = sb * 4 + (j >> 1), h = j & 1;
-                    d0 = reinterpret_cast<uint4*>(codes + (4 * r + 2 * h) * p.code_pitch + pair * 16);
-                    d1 = reinterpret_cast<uint4*>(codes + (4 * r + 2 * h + 1) * p.code_pitch + pair * 16);
-                } else {
-                    d0 = reinterpret_cast<uint4*>(codes + r * p.code_pitch + sb * 256 + 32 * j);
-                    d1 = d0 + 1;
-                }
+                uint4* d0 = reinterpret_cast<uint4*>(codes + r * p.code_pitch + sb * 256 + 32 * j);
+                uint4* d1 = d0 + 1;
                 *d0 = make_uint4(w[0], w[1], w[2], w[3]);
                 *d1 = make_uint4(w[4], w[5], w[6], w[7]);
                 bs[r * p.aux_pitch + sb * 8 + j] = sum;
@@ -203,140 +183,7 @@ __device__ __forceinline__ void prepare_acts(const StreamParams& p, uint8_t* sme
 }
 
 // ---------------------------------------------------------------------------
-// P_DOT: per-thread dp4a over raw blocks (int8_act, NT = activation rows)
-// ---------------------------------------------------------------------------
-
-// acc[m] of the thread's row; rows r = warp * RPW + lane / LPR
-template <int WT, int NT, int EPI, int CW>
-__device__ __forceinline__ void stage_dot(const StreamParams& p, const uint8_t* smem, const uint8_t* st, int cnu,
-                                          int ur0, int gu0, int off, int warp, int lane, float (&acc)[8], int tile,
-                                          int m0) {
-    constexpr int RPW = 16 / CW, LPR = 32 / RPW;
-    const int r = warp * RPW + lane / LPR, j = lane % LPR;
-    const uint8_t* row = st + r * p.row_stride + off;
-    const uint8_t* codes = smem + p.off_codes;
-    const float* da = reinterpret_cast<const float*>(smem + p.off_scale);
-    const long long n = (long long)tile * kTileRows + r;
-    if (WT == T_Q8_0) {
-        constexpr int UPL = Unit<T_Q8_0>::per_stage / LPR;  // blocks per lane and stage
-#pragma unroll
-        for (int i = 0; i < UPL; ++i) {
-            const int b = j + LPR * i;
-            const bool live = b < cnu;
-            const int bc = live ? b : cnu - 1;
-            // the 34-byte block starts 2-byte aligned: read the 9 covering words
-            const uintptr_t addr = reinterpret_cast<uintptr_t>(row + 34 * bc);
-            const uint8_t* aw = reinterpret_cast<const uint8_t*>(addr & ~uintptr_t(3));
-            const uint32_t sh = (uint32_t)(addr & 2u) * 8u;  // 0 or 16
-            uint32_t w[9];
-#pragma unroll
-            for (int k = 0; k < 9; ++k) w[k] = ld32(aw + 4 * k);
-            const float dw = h2f(sh ? (w[0] >> 16) : w[0]);
-            uint32_t c[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) c[k] = __funnelshift_rc(w[k], w[k + 1], 16u + sh);
-            const int ub = ur0 + bc;
-#pragma unroll
-            for (int m = 0; m < NT; ++m) {
-                const uint4 a0 = ld128(codes + (2 * m) * p.code_pitch + ub * 16);
-                const uint4 a1 = ld128(codes + (2 * m + 1) * p.code_pitch + ub * 16);
-                int s0 = dp4a(c[0], a0.x, 0), s1 = dp4a(c[1], a0.y, 0);
-                s0 = dp4a(c[2], a0.z, s0);
-                s1 = dp4a(c[3], a0.w, s1);
-                s0 = dp4a(c[4], a1.x, s0);
-                s1 = dp4a(c[5], a1.y, s1);
-                s0 = dp4a(c[6], a1.z, s0);
-                s1 = dp4a(c[7], a1.w, s1);
-                const int isum = s0 + s1;
-                if (EPI == E_Y) {
-                    if (live) acc[m] = fmaf((float)isum, dw * da[m * p.scale_pitch + ub], acc[m]);
-                } else if (live && m0 + m < p.M && n < p.N) {
-                    p.sums[((long long)(m0 + m) * p.N + n) * p.units + gu0 + b] = isum;
-                }
-            }
-        }
-    } else {
-        constexpr int UPL = Unit<T_Q4_K>::per_stage * 4 / LPR;  // (super-block, pair) tasks per lane
-#pragma unroll
-        for (int i = 0; i < UPL; ++i) {
-            const int q = j + LPR * i;
-            const int u = q >> 2, c = q & 3;
-            const bool live = u < cnu;
-            const int uc = live ? u : cnu - 1;
-            const uint8_t* sb = row + 144 * uc;
-            const uint4 hw = ld128(sb);  // d, dmin, scales[0..11]
-            const uint4 q0 = ld128(sb + 16 + 32 * c), q1 = ld128(sb + 32 + 32 * c);
-            const int j0 = 2 * c, j1 = 2 * c + 1;
-            // 6-bit scale/min of sub-blocks j0, j1 (j0 < 4 <=> c < 2)
-            int sc0, mn0, sc1, mn1;
-            if (c < 2) {
-                sc0 = (int)((hw.y >> (8 * j0)) & 63u);
-                mn0 = (int)((hw.z >> (8 * j0)) & 63u);
-                sc1 = (int)((hw.y >> (8 * j1)) & 63u);
-                mn1 = (int)((hw.z >> (8 * j1)) & 63u);
-            } else {
-                const int k0 = j0 - 4, k1 = j1 - 4;
-                sc0 = (int)(((hw.w >> (8 * k0)) & 15u) | (((hw.y >> (8 * k0 + 6)) & 3u) << 4));
-                mn0 = (int)(((hw.w >> (8 * k0 + 4)) & 15u) | (((hw.z >> (8 * k0 + 6)) & 3u) << 4));
-                sc1 = (int)(((hw.w >> (8 * k1)) & 15u) | (((hw.y >> (8 * k1 + 6)) & 3u) << 4));
-                mn1 = (int)(((hw.w >> (8 * k1 + 4)) & 15u) | (((hw.z >> (8 * k1 + 6)) & 3u) << 4));
-            }
-            const uint32_t qq[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-            uint32_t lo[8], hi[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                lo[k] = qq[k] & 0x0F0F0F0Fu;
-                hi[k] = (qq[k] >> 4) & 0x0F0F0F0Fu;
-            }
-            const float fD = h2f(hw.x), fDm = h2f(hw.x >> 16);
-            const int pair = (ur0 + uc) * 4 + c;
-            const int* bs = reinterpret_cast<const int*>(smem + p.off_aux);
-#pragma unroll
-            for (int m = 0; m < NT; ++m) {
-                const uint4 a0 = ld128(codes + (4 * m + 0) * p.code_pitch + pair * 16);
-                const uint4 a1 = ld128(codes + (4 * m + 1) * p.code_pitch + pair * 16);
-                const uint4 a2 = ld128(codes + (4 * m + 2) * p.code_pitch + pair * 16);
-                const uint4 a3 = ld128(codes + (4 * m + 3) * p.code_pitch + pair * 16);
-                int s0 = dp4a(lo[0], a0.x, 0), s1 = dp4a(hi[0], a2.x, 0);
-                s0 = dp4a(lo[1], a0.y, s0);
-                s1 = dp4a(hi[1], a2.y, s1);
-                s0 = dp4a(lo[2], a0.z, s0);
-                s1 = dp4a(hi[2], a2.z, s1);
-                s0 = dp4a(lo[3], a0.w, s0);
-                s1 = dp4a(hi[3], a2.w, s1);
-                s0 = dp4a(lo[4], a1.x, s0);
-                s1 = dp4a(hi[4], a3.x, s1);
-                s0 = dp4a(lo[5], a1.y, s0);
-                s1 = dp4a(hi[5], a3.y, s1);
-                s0 = dp4a(lo[6], a1.z, s0);
-                s1 = dp4a(hi[6], a3.z, s1);
-                s0 = dp4a(lo[7], a1.w, s0);
-                s1 = dp4a(hi[7], a3.w, s1);
-                const int2 b2 = *reinterpret_cast<const int2*>(bs + m * p.aux_pitch + (ur0 + uc) * 8 + j0);
-                int ssc = live ? sc0 * s0 + sc1 * s1 : 0;
-                int smn = live ? mn0 * b2.x + mn1 * b2.y : 0;
-                if (EPI == E_Y) {
-                    const float dam = da[m * p.scale_pitch + ur0 + uc];
-                    acc[m] += dam * (fD * (float)ssc - fDm * (float)smn);
-                } else {
-                    // the four pairs of a super-block sit on four consecutive lanes
-                    ssc += __shfl_xor_sync(0xffffffffu, ssc, 1);
-                    smn += __shfl_xor_sync(0xffffffffu, smn, 1);
-                    ssc += __shfl_xor_sync(0xffffffffu, ssc, 2);
-                    smn += __shfl_xor_sync(0xffffffffu, smn, 2);
-                    if (live && c == 0 && m0 + m < p.M && n < p.N) {
-                        int* o = p.sums + (((long long)(m0 + m) * p.N + n) * p.units + gu0 + u) * 2;
-                        o[0] = ssc;
-                        o[1] = smn;
-                    }
-                }
-            }
-        }
-    }
-}
-
-// ---------------------------------------------------------------------------
-// P_MMA: warp tensor-core products over 16-row blocks
+// warp tensor-core products over 16-row blocks
 // ---------------------------------------------------------------------------
 
 // acc layout: int8: acc[nt][0..3] = (row g, col 2t), (g, 2t+1), (g+8, 2t), (g+8, 2t+1)
@@ -503,10 +350,10 @@ __device__ __forceinline__ void stage_mma(const StreamParams& p, const uint8_t* 
 // the kernel
 // ---------------------------------------------------------------------------
 
-template <int WT, int AM, int NT, int EPI, int PATH>
-__global__ void __launch_bounds__((consumer_warps(WT, AM, NT, PATH) + 1) * 32, 1)
+template <int WT, int AM, int NT, int EPI>
+__global__ void __launch_bounds__((consumer_warps(WT, AM, NT) + 1) * 32, 1)
     qmm_stream_kernel(const StreamParams p) {
-    constexpr int CW = consumer_warps(WT, AM, NT, PATH);
+    constexpr int CW = consumer_warps(WT, AM, NT);
     constexpr int UB = Unit<WT>::bytes;
     extern __shared__ __align__(128) uint8_t smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -586,27 +433,22 @@ __global__ void __launch_bounds__((consumer_warps(WT, AM, NT, PATH) + 1) * 32, 1
     // ------------------------------- consumers -------------------------------
     const int k0 = su0 * Unit<WT>::vals;
     const int klen = sunits * Unit<WT>::vals;
-    prepare_acts<WT, AM, PATH, CW>(p, smem, m0, k0, klen, tid);
+    prepare_acts<WT, AM, CW>(p, smem, m0, k0, klen, tid);
     consumer_sync<CW>();
 
-    constexpr int MR = chunk_rows(AM, NT, PATH);
-    constexpr int NRED = PATH == P_DOT ? 1 : CW;  // partial sums per output in `red`
+    constexpr int MR = chunk_rows(AM, NT);
+    constexpr int NRED = CW;  // partial sums per output in `red`
     float* red = reinterpret_cast<float*>(smem + p.off_red);
     const float* rs = reinterpret_cast<const float*>(smem + p.off_rs);
     const int g8 = lane >> 2, t4 = lane & 3;
-    constexpr int RPW = 16 / CW, LPR = 32 / (RPW > 0 ? RPW : 1);
-    const int dot_row = PATH == P_DOT ? warp * RPW + lane / LPR : 0;
     long long g = 0;
     for (int tile = tile0; tile < p.ntiles; tile += p.per_pair) {
         float acc[NT][4];
-        float dacc[8];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
             for (int i = 0; i < 4; ++i) acc[nt][i] = 0.0f;
-#pragma unroll
-        for (int m = 0; m < 8; ++m) dacc[m] = 0.0f;
-        const long long rowA = (long long)tile * kTileRows + (PATH == P_DOT ? dot_row : g8), rowB = rowA + 8;
+        const long long rowA = (long long)tile * kTileRows + g8, rowB = rowA + 8;
         for (int ch = 0; ch < nchunks; ++ch, ++g) {
             const int slot = (int)(g % S);
             const bool ok = mbar_wait(smem_u32(&bars[slot]), (uint32_t)((g / S) & 1), flags, p.err);
@@ -615,27 +457,15 @@ __global__ void __launch_bounds__((consumer_warps(WT, AM, NT, PATH) + 1) * 32, 1
             if (ok) {
                 const uint8_t* st = smem + p.off_stage + (long long)slot * kTileRows * p.row_stride;
                 const int off0 = (int)((rowA * p.rb + (long long)cu0 * UB) & 15);
-                if (PATH == P_DOT) {
-                    stage_dot<WT, NT, EPI, CW>(p, smem, st, cnu, cu0 - su0, cu0, off0, warp, lane, dacc, tile, m0);
-                } else {
-                    const int off1 = (int)((rowB * p.rb + (long long)cu0 * UB) & 15);
-                    stage_mma<WT, AM, NT, EPI, CW>(p, smem, st, cnu, cu0 - su0, cu0, off0, off1, warp, lane, acc, tile, m0);
-                }
+                const int off1 = (int)((rowB * p.rb + (long long)cu0 * UB) & 15);
+                stage_mma<WT, AM, NT, EPI, CW>(p, smem, st, cnu, cu0 - su0, cu0, off0, off1, warp, lane, acc, tile, m0);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&bars[S + slot]));
         }
         if (EPI != E_Y) continue;
         // ---- tile epilogue: red[NRED][16][MR], then sum, scale and store
-        if (PATH == P_DOT) {
-#pragma unroll
-            for (int m = 0; m < NT; ++m) {
-                float v = dacc[m];
-#pragma unroll
-                for (int o = LPR / 2; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-                if (lane % LPR == 0) red[dot_row * MR + m] = v;
-            }
-        } else {
+        {
             float* rw = red + warp * kTileRows * MR;
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
@@ -698,18 +528,11 @@ __global__ void __launch_bounds__((consumer_warps(WT, AM, NT, PATH) + 1) * 32, 1
 struct StreamPlan {
     StreamParams p;
     int nt;
-    int path;
     int cw;
     int grid;
     size_t smem;
     size_t workspace;  // bytes of partial sums + counters (0 when K is not split)
 };
-
-inline int round_up(int v, int a) { return (v + a - 1) / a * a; }
-
-// largest M served by the per-thread dp4a path (int8_act)
-constexpr int kDotMaxQ8_0 = 8;
-constexpr int kDotMaxQ4_K = 4;
 
 // Fills the layout for wtype/mode/epilogue and sizes; returns false if no
 // layout fits in smem_max.
@@ -718,18 +541,12 @@ inline bool plan_stream(int wt, int am, int epi, long long M, long long N, long 
     StreamPlan pl{};
     StreamParams& p = pl.p;
     const int uv = wt == T_Q8_0 ? 32 : 256, ub = wt == T_Q8_0 ? 34 : 144;
-    int nt, path;
-    if (am == A_INT8 && M <= (wt == T_Q8_0 ? kDotMaxQ8_0 : kDotMaxQ4_K)) {
-        path = P_DOT;
-        nt = M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : 8;
-    } else {
-        path = P_MMA;
-        if (am == A_INT8) nt = M <= 8 ? 1 : M <= 16 ? 2 : M <= 32 ? 4 : 8;
-        else nt = M <= 4 ? 1 : M <= 8 ? 2 : M <= 16 ? 4 : 8;
-        if (wt == T_Q4_K && am == A_INT8 && nt > 4) nt = 4;  // register budget of the integer super-block sums
-    }
-    const int cw = consumer_warps(wt, am, nt, path);
-    const int mr = chunk_rows(am, nt, path);
+    int nt;
+    if (am == A_INT8) nt = M <= 8 ? 1 : M <= 16 ? 2 : M <= 32 ? 4 : 8;
+    else nt = M <= 4 ? 1 : M <= 8 ? 2 : M <= 16 ? 4 : 8;
+    if (wt == T_Q4_K && am == A_INT8 && nt > 4) nt = 4;  // register budget of the integer super-block sums
+    const int cw = consumer_warps(wt, am, nt);
+    const int mr = chunk_rows(am, nt);
     p.M = (int)M;
     p.N = (int)N;
     p.K = (int)K;
@@ -740,28 +557,22 @@ inline bool plan_stream(int wt, int am, int epi, long long M, long long N, long 
     p.total_bytes = p.rb * N;
     p.ntiles = (int)((N + kTileRows - 1) / kTileRows);
     const int ups_max = wt == T_Q8_0 ? Unit<T_Q8_0>::per_stage : Unit<T_Q4_K>::per_stage;
-    const int nred = path == P_DOT ? 1 : cw;
-    const int red_bytes = nred * kTileRows * mr * 4;
+    const int red_bytes = cw * kTileRows * mr * 4;
     for (int ks = 1; ks <= p.units; ++ks) {
         const int su = (p.units + ks - 1) / ks;
         if ((long long)(ks - 1) * su >= p.units) continue;  // empty last slice
         const int ups = su < ups_max ? su : ups_max;
         // row pitch in a stage: room for the 16-byte superset; the remainder
         // mod 128 spreads the rows of one access over the banks
-        const int want = path == P_DOT ? 64 : 16;
+        const int want = 16;
         int row_stride = round_up(ups * ub + 32, 16);
         row_stride += ((want - row_stride % 128) + 128) % 128;
         const int stage_bytes = kTileRows * row_stride;
         const int kv = su * uv;  // values per slice
         int codes, scale_pitch = 0, aux_pitch = 0, code_pitch;
         if (am == A_INT8) {
-            if (path == P_DOT) {
-                code_pitch = wt == T_Q8_0 ? su * 16 : su * 4 * 16;  // bytes per (row, 16-byte plane)
-                codes = mr * kv;
-            } else {
-                code_pitch = kv + 16;
-                codes = mr * code_pitch;
-            }
+            code_pitch = kv + 16;
+            codes = mr * code_pitch;
             scale_pitch = su;
             if (wt == T_Q4_K) aux_pitch = su * 8;
         } else {
@@ -813,7 +624,6 @@ inline bool plan_stream(int wt, int am, int epi, long long M, long long N, long 
     p.per_pair = per;
     pl.grid = p.pairs * per;
     pl.nt = nt;
-    pl.path = path;
     pl.cw = cw;
     pl.workspace = (epi == E_Y && p.kslices > 1)
                        ? (size_t)p.kslices * (size_t)M * (size_t)N * 4 + (size_t)p.mchunks * p.ntiles * 4 + 256

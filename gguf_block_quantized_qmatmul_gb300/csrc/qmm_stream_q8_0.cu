@@ -1,5 +1,5 @@
-// qmm_stream_q4_k_mma.cu -- instantiations of the streaming kernel for
-// Q4_K weights on the P_MMA consumer path, and their launcher.
+// qmm_stream_q8_0.cu -- instantiations of the streaming kernel for
+// Q8_0 weights (warp MMA tiles), and their launcher.
 #include "qmm_internal.h"
 
 namespace qmm {
@@ -8,10 +8,10 @@ unsigned long long g_smem_done[2][2][4];
 
 template <int AM, int NT, int EPI>
 cudaError_t go(const StreamPlan& pl, int smem_max, cudaStream_t s, unsigned long long& done) {
-    auto* k = qmm_stream_kernel<T_Q4_K, AM, NT, EPI, P_MMA>;
+    auto* k = qmm_stream_kernel<T_Q8_0, AM, NT, EPI>;
     cudaError_t e = ensure_smem(k, smem_max, done);
     if (e != cudaSuccess) return e;
-    constexpr int threads = (consumer_warps(T_Q4_K, AM, NT, P_MMA) + 1) * 32;
+    constexpr int threads = (consumer_warps(T_Q8_0, AM, NT) + 1) * 32;
     k<<<pl.grid, threads, pl.smem, s>>>(pl.p);
     return cudaGetLastError();
 }
@@ -29,7 +29,7 @@ cudaError_t by_nt(const StreamPlan& pl, int smem_max, cudaStream_t s) {
 }
 }  // namespace
 
-cudaError_t launch_stream_q4_k_mma(int am, int epi, const StreamPlan& pl, int smem_max, cudaStream_t s) {
+cudaError_t launch_stream_q8_0(int am, int epi, const StreamPlan& pl, int smem_max, cudaStream_t s) {
     if (am == A_INT8 && epi == E_Y) return by_nt<A_INT8, E_Y>(pl, smem_max, s);
     if (am == A_INT8 && epi == E_SUMS) return by_nt<A_INT8, E_SUMS>(pl, smem_max, s);
     if (am == A_F32 && epi == E_Y) return by_nt<A_F32, E_Y>(pl, smem_max, s);

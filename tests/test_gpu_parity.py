@@ -151,19 +151,24 @@ def test_gap_ordering(qmm, orc):
 
 
 def test_batch_rows_are_independent(qmm, orc):
-    """Row m's codes and output do not depend on the other rows of the batch."""
+    """Row m's codes and integer block sums do not depend on the other rows of
+    the batch (bit-exact); its output agrees within the bound (a batch of 8
+    and a single row may run on different kernel paths, which sum in a
+    different order)."""
     K, N = 1536, 96
     for wtype in ("q8_0", "q4_k"):
-        wq = dev(orc.quantize(wtype, qmm_synth.weights(N, K)))
+        wq_h = orc.quantize(wtype, qmm_synth.weights(N, K))
+        wq = dev(wq_h)
         x = qmm_synth.activations(8, K)
         x[3] *= 40.0
+        _, T = orc.matmul(wtype, "int8_act", wq_h, x)
         yb = host(qmm.matmul(wq, dev(x), wtype, "int8_act", N=N))
         sb = host(qmm.block_sums(wq, dev(x), wtype, N=N))
         for m in range(8):
             y1 = host(qmm.matmul(wq, dev(x[m:m + 1]), wtype, "int8_act", N=N))
             s1 = host(qmm.block_sums(wq, dev(x[m:m + 1]), wtype, N=N))
             assert np.array_equal(s1[0], sb[m])
-            assert np.array_equal(y1[0], yb[m])
+            assert np.all(np.abs(y1[0].astype(np.float64) - yb[m]) <= 1e-5 * T[m] + 1e-6)
 
 
 def test_one_hot_f32_act_is_exact(qmm, orc):
