@@ -31,8 +31,8 @@ STATUS = {0: "QMM_OK", 1: "QMM_ERR_NULL", 2: "QMM_ERR_SHAPE", 3: "QMM_ERR_TYPE",
 
 # every symbol declared in include/qmm.h
 EXPORTS = ["qmm_block_values", "qmm_block_bytes", "qmm_row_bytes", "qmm_quantize_weights", "qmm_quantize_act",
-           "qmm_dequantize", "qmm_matmul_workspace", "qmm_matmul", "qmm_block_sums", "qmm_last_device_error",
-           "qmm_status_string"]
+           "qmm_dequantize", "qmm_matmul_workspace", "qmm_matmul", "qmm_matmul_static_workspace", "qmm_block_sums",
+           "qmm_last_device_error", "qmm_status_string"]
 
 
 class QmmError(RuntimeError):

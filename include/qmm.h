@@ -142,6 +142,28 @@ qmm_status qmm_matmul(qmm_type wtype, qmm_act_mode mode, const void* wq, const f
 qmm_status qmm_block_sums(qmm_type wtype, const void* wq, const float* x, int64_t M, int64_t N, int64_t K,
                           int32_t* out, qmm_stream_t stream);
 
+/* qmm_matmul for callers that cannot allocate device memory.
+   (The pages have no counterpart: this is an addition of this library.)
+   Some callers never call cudaMalloc themselves: a host engine that owns all
+   device allocations and hands a plugin only finished input/output buffers,
+   or a latency-critical loop that must not hit the allocator.  This call
+   computes exactly what qmm_matmul computes, but when the shape needs a
+   workspace it uses one array of QMM_STATIC_WORKSPACE_BYTES that the library
+   keeps in device memory (every GPU that loads the library holds it until
+   the process exits); it calls no cudaMalloc, cudaFree or allocating routine.
+   - Shapes whose workspace (qmm_matmul_workspace) exceeds
+     QMM_STATIC_WORKSPACE_BYTES are refused with QMM_ERR_WORKSPACE before
+     anything is launched.
+   - The first call on a device looks up the array's device address (with
+     that device current); make that first call before any stream capture.
+   - Every call shares the one array and it keeps the last call's contents:
+     the split-K counters are cleared on `stream` by each call, but calls that
+     overlap on the GPU (other streams, other host threads) race on it.
+   Other arguments and errors as qmm_matmul. */
+#define QMM_STATIC_WORKSPACE_BYTES (8u << 20)
+qmm_status qmm_matmul_static_workspace(qmm_type wtype, qmm_act_mode mode, const void* wq, const float* x, float* y,
+                                       int64_t M, int64_t N, int64_t K, qmm_stream_t stream);
+
 /* Reads and clears the current device's error word (synchronizes that
    device).  QMM_ERR_TIMEOUT if a device-side wait of an earlier launch gave
    up after its bounded spin (its outputs are then undefined), QMM_OK
