@@ -67,7 +67,8 @@ qmm_status stream_call(qmm_type wtype, int am, int epi, const void* wq, const fl
     const int wt = wtype == QMM_Q8_0 ? T_Q8_0 : T_Q4_K;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     GemvPlan gp;
-    if (am == A_INT8 && plan_gemv(wt, M, N, K, sms, smem, gp)) {  // decode: whole-row weight stream
+    DmmaPlan dp;
+    if (am == A_INT8 && M <= kGemvMaxM && plan_gemv(wt, M, N, K, sms, smem, gp)) {  // decode: whole-row weight stream
         gp.p.wq = static_cast<const uint8_t*>(wq);
         gp.p.x = x;
         gp.p.y = y;
@@ -75,6 +76,21 @@ qmm_status stream_call(qmm_type wtype, int am, int epi, const void* wq, const fl
         gp.p.err = err;
         const cudaError_t e = wt == T_Q8_0 ? launch_gemv_q8_0(epi, gp, smem, s) : launch_gemv_q4_k(epi, gp, smem, s);
         return e == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
+    }
+    if (M <= kDecodeMaxM && plan_dmma(wt, am, M, N, K, sms, smem, dp)) {  // decode on 8-row tensor-core tiles
+        dp.p.wq = static_cast<const uint8_t*>(wq);
+        dp.p.x = x;
+        dp.p.y = y;
+        dp.p.sums = sums;
+        dp.p.err = err;
+        if (epi == E_Y && dp.p.kslices > 1) {
+            if (!ws || ws_bytes < dp.workspace) return QMM_ERR_WORKSPACE;
+            dp.p.partial = static_cast<float*>(ws);
+            const size_t coff = round_up_sz((size_t)dp.p.kslices * M * N * 4, 256);
+            dp.p.counters = reinterpret_cast<unsigned*>(static_cast<uint8_t*>(ws) + coff);
+            if (cudaMemsetAsync(dp.p.counters, 0, (size_t)dp.p.ngroups * 4, s) != cudaSuccess) return QMM_ERR_CUDA;
+        }
+        return launch_dmma(wt, am, epi, dp, smem, s) == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
     }
     StreamPlan pl;
     if (!plan_stream(wt, am, epi, M, N, K, sms, smem, pl)) return QMM_ERR_SHAPE;
@@ -166,8 +182,12 @@ size_t qmm_matmul_workspace(qmm_type wtype, qmm_act_mode mode, int64_t M, int64_
     if (check_shape(wtype, N, K) != QMM_OK || M <= 0 || M > INT32_MAX || N == 0 || K == 0) return 0;
     int sms = 0, smem = 0;
     if (device_info(nullptr, &sms, &smem) != cudaSuccess) return 0;
+    const int wt = wtype == QMM_Q8_0 ? T_Q8_0 : T_Q4_K;
     GemvPlan gp;
-    if (mode == QMM_INT8_ACT && plan_gemv(wtype == QMM_Q8_0 ? T_Q8_0 : T_Q4_K, M, N, K, sms, smem, gp)) return 0;
+    if (mode == QMM_INT8_ACT && M <= kGemvMaxM && plan_gemv(wt, M, N, K, sms, smem, gp)) return 0;
+    DmmaPlan dp;
+    if (M <= kDecodeMaxM && plan_dmma(wt, mode == QMM_INT8_ACT ? A_INT8 : A_F32, M, N, K, sms, smem, dp))
+        return dp.workspace;
     StreamPlan pl;
     if (!plan_stream(wtype == QMM_Q8_0 ? T_Q8_0 : T_Q4_K, mode == QMM_INT8_ACT ? A_INT8 : A_F32, E_Y, M, N, K, sms,
                      smem, pl))

@@ -3,6 +3,7 @@
 
 #include <cuda_runtime.h>
 
+#include "qmm_dmma.cuh"
 #include "qmm_gemv.cuh"
 #include "qmm_stream.cuh"
 
@@ -14,6 +15,13 @@ cudaError_t launch_stream_q8_0(int am, int epi, const StreamPlan& plan, int smem
 cudaError_t launch_stream_q4_k(int am, int epi, const StreamPlan& plan, int smem_max, cudaStream_t s);
 cudaError_t launch_gemv_q8_0(int epi, const GemvPlan& plan, int smem_max, cudaStream_t s);
 cudaError_t launch_gemv_q4_k(int epi, const GemvPlan& plan, int smem_max, cudaStream_t s);
+cudaError_t launch_dmma(int wt, int am, int epi, const DmmaPlan& plan, int smem_max, cudaStream_t s);
+
+// largest activation batch served by the per-thread dp4a GEMV (int8_act);
+// larger decode batches (and every f32_act decode batch up to 8) use the
+// 8-row-tile tensor-core kernel
+constexpr int kGemvMaxM = 4;
+constexpr int kDecodeMaxM = 8;
 
 // Raise a kernel's dynamic shared-memory limit once per device.
 template <typename F>
