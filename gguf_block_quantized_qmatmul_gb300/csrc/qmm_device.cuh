@@ -216,6 +216,11 @@ __device__ __forceinline__ void lds8_unaligned(const uint8_t* p, uint32_t& r0, u
 constexpr int kTileRows = 16;  // weight rows per tile (the MMA M dimension)
 
 inline int round_up(int v, int a) { return (v + a - 1) / a * a; }
+// smallest pitch >= v (v a multiple of 16) with pitch % 128 == want
+inline int pitch_mod(int v, int want) {
+    v = round_up(v, 16);
+    return v + ((want - v % 128) % 128 + 128) % 128;
+}
 
 struct StreamParams {
     const uint8_t* wq;

@@ -44,7 +44,7 @@ struct DmmaParams {
     int ngroups;      // ceil(N / 8)
     int stages;
     int stage_bytes;
-    int row_pitch;    // bytes between rows in a stage when K is split (per-row copies)
+    int row_pitch;    // bytes between rows in a stage with one copy per row (0: one contiguous copy)
     int off_flags, off_codes, off_scale, off_aux, off_rs, off_red, off_stage;
     int code_pitch;   // int8: bytes per activation row; f32: halves per activation row and piece
 };
@@ -190,7 +190,7 @@ __global__ void __launch_bounds__((kDmmaWarps + 1) * 32, 1) qmm_dmma_kernel(cons
     const int grp0 = blockIdx.x / p.kslices;
     const int su0 = slice * p.slice_units;
     const int sunits = min(p.slice_units, p.units - su0);
-    const bool whole = p.kslices == 1;  // whole rows: one contiguous copy per stage
+    const bool whole = p.row_pitch == 0;  // short rows: one contiguous copy of the 8 rows per stage
     if (tid == 0) {
         for (int i = 0; i < S; ++i) {
             mbar_init(smem_u32(&bars[i]), 1);
@@ -429,12 +429,12 @@ inline bool plan_dmma(int wt, int am, long long M, long long N, long long K, int
         const int kv = su * uv;
         int codes, scale = 0, aux = 0, rsb = 0;
         if (am == A_INT8) {
-            p.code_pitch = kv + 16;
+            p.code_pitch = pitch_mod(kv, 32);  // 8-byte A loads of 4 rows per half-warp: no bank conflict
             codes = (int)M * p.code_pitch;
             scale = (int)M * su * 4;
             if (wt == T_Q4_K) aux = (int)M * su * 8 * 4;
         } else {
-            p.code_pitch = kv + 8;  // halves
+            p.code_pitch = pitch_mod(2 * kv, 64) / 2;  // halves; 16-byte A loads of 2 rows per quarter-warp
             codes = 2 * (int)M * p.code_pitch * 2;
             if (wt == T_Q4_K) aux = (int)M * (kv / 32) * 4;
         }
@@ -454,11 +454,14 @@ inline bool plan_dmma(int wt, int am, long long M, long long N, long long K, int
         off = round_up(off + 2 * kDmmaWarps * 64 * 4, 128);
         p.off_stage = off;
         long long sb;
-        if (ks == 1) {
-            sb = 8 * p.rb + 64;
+        const long long slice_bytes = (long long)su * ub;
+        if (ks == 1 && p.rb < 2048) {
+            sb = 8 * p.rb + 64;  // short rows: one contiguous copy of the whole tile
             p.row_pitch = 0;
         } else {
-            p.row_pitch = round_up(su * ub + 48, 16);
+            // one copy per row; a pitch of 16 mod 128 bytes keeps the 8 rows of a
+            // B fragment load on distinct banks (row bytes are often 0 mod 128)
+            p.row_pitch = pitch_mod((int)slice_bytes + 48, 16);
             sb = 8LL * p.row_pitch;
         }
         sb = (sb + 127) / 128 * 128;
