@@ -83,14 +83,14 @@ qmm_status stream_call(qmm_type wtype, int am, int epi, const void* wq, const fl
         dp.p.y = y;
         dp.p.sums = sums;
         dp.p.err = err;
-        if (epi == E_Y && dp.p.kslices > 1) {
+        const bool split = epi == E_Y && dp.p.kslices > 1;
+        if (split) {
             if (!ws || ws_bytes < dp.workspace) return QMM_ERR_WORKSPACE;
             dp.p.partial = static_cast<float*>(ws);
-            const size_t coff = round_up_sz((size_t)dp.p.kslices * M * N * 4, 256);
-            dp.p.counters = reinterpret_cast<unsigned*>(static_cast<uint8_t*>(ws) + coff);
-            if (cudaMemsetAsync(dp.p.counters, 0, (size_t)dp.p.ngroups * 4, s) != cudaSuccess) return QMM_ERR_CUDA;
         }
-        return launch_dmma(wt, am, epi, dp, smem, s) == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
+        if (launch_dmma(wt, am, epi, dp, smem, s) != cudaSuccess) return QMM_ERR_CUDA;
+        if (split && launch_splitk_reduce(dp.p.partial, M * N, dp.p.kslices, y, s) != cudaSuccess) return QMM_ERR_CUDA;
+        return QMM_OK;
     }
     StreamPlan pl;
     if (!plan_stream(wt, am, epi, M, N, K, sms, smem, pl)) return QMM_ERR_SHAPE;

@@ -8,17 +8,19 @@
 // rows) holds the activations -- for f32_act the 8 activation rows split in
 // two exact f16 pieces (x 2^s = hi + lo), for int8_act the 8 rows of codes --
 // and the B operand (8 columns) holds 8 weight rows.  A weight tile is
-// therefore only 8 rows, so a stage of 8 whole rows (or 8 row slices when K is
-// split) arrives by one or eight large bulk copies.  16 consumer warps split
-// the K range of a stage block by block; per block:
+// therefore only 8 rows: a tile is 8 rows x the CTA's K range, streamed in
+// stages of 8 row chunks of >= 4 KB each (one bulk copy per row; one copy for
+// the whole tile when rows are short).  16 consumer warps split the K range
+// of a stage block by block; per block:
 //   Q8_0: two mma.m16n8k16.f16 (f32_act) or one mma.m16n8k32.s8 (int8_act),
 //         then y += f(d_w) * sum (and f(d_a) for int8_act) in registers;
 //   Q4_K: per 32-value sub-block the same, with e_j = f(d) sc_j and
 //         o_j = f(dmin) m_j: y += e_j sum(q x) - o_j sum(x) (f32_act), or the
 //         exact integer S_sc, S_m of the CPU form (int8_act).
 // Warp partials of a tile are summed in shared memory (one named barrier per
-// stage); a K split across CTAs adds the slices through the workspace in slice
-// order, as the streaming kernel does.
+// tile).  K is split across CTAs only when the activation rows of the whole K
+// range do not fit in shared memory; the slices' partial sums then go to the
+// workspace and a second small kernel adds them in slice order.
 #pragma once
 
 #include "qmm_device.cuh"
@@ -33,14 +35,14 @@ struct DmmaParams {
     const float* x;
     float* y;
     int32_t* sums;
-    float* partial;
-    unsigned* counters;
+    float* partial;   // [kslices][M][N] when K is split (summed by qmm_splitk_reduce_kernel)
     unsigned* err;
     long long total_bytes;
     long long rb;
     int M, N, K;
     int units;        // weight units per row (32-blocks or super-blocks)
     int kslices, slice_units, per_slice;
+    int ups;          // units per stage (K chunk of a tile)
     int ngroups;      // ceil(N / 8)
     int stages;
     int stage_bytes;
@@ -191,13 +193,13 @@ __global__ void __launch_bounds__((kDmmaWarps + 1) * 32, 1) qmm_dmma_kernel(cons
     const int su0 = slice * p.slice_units;
     const int sunits = min(p.slice_units, p.units - su0);
     const bool whole = p.row_pitch == 0;  // short rows: one contiguous copy of the 8 rows per stage
+    const int nch = (sunits + p.ups - 1) / p.ups;
     if (tid == 0) {
         for (int i = 0; i < S; ++i) {
             mbar_init(smem_u32(&bars[i]), 1);
             mbar_init(smem_u32(&bars[S + i]), kDmmaWarps);
         }
         flags[0] = 0;
-        flags[1] = 0;
         fence_mbar_init();
     }
     __syncthreads();
@@ -206,36 +208,40 @@ __global__ void __launch_bounds__((kDmmaWarps + 1) * 32, 1) qmm_dmma_kernel(cons
         // ------------------------------ producer ------------------------------
         long long g = 0;
         bool ok = true;
-        for (int grp = grp0; grp < p.ngroups && ok; grp += p.per_slice, ++g) {
-            const int slot = (int)(g % S);
-            if (g >= S) {
-                int okl = 1;
-                if (lane == 0) okl = mbar_wait(smem_u32(&bars[S + slot]), (uint32_t)(((g / S) - 1) & 1), flags, p.err);
-                ok = __shfl_sync(0xffffffffu, okl, 0) != 0;
-                if (!ok) break;
-            }
-            uint8_t* st = smem + p.off_stage + (long long)slot * p.stage_bytes;
-            long long a = 0, b = 0, e = 0;
-            int dst = 0;
-            const long long row = (long long)grp * 8 + lane;
-            if (whole ? lane == 0 : (lane < 8 && row < p.N)) {
-                const long long s0 = whole ? (long long)grp * 8 * p.rb : row * p.rb + (long long)su0 * UB;
-                e = whole ? min((long long)grp * 8 + 8, (long long)p.N) * p.rb : s0 + (long long)sunits * UB;
-                a = s0 & ~15ll;
-                b = (e + 15) & ~15ll;
-                dst = whole ? 0 : lane * p.row_pitch;
-                if (b > p.total_bytes) {
-                    b = e & ~15ll;
-                    for (long long q = b; q < e; ++q) st[dst + (q - a)] = p.wq[q];
-                    fence_proxy_async();
+        for (int grp = grp0; grp < p.ngroups && ok; grp += p.per_slice) {
+            for (int ch = 0; ch < nch && ok; ++ch, ++g) {
+                const int slot = (int)(g % S);
+                if (g >= S) {
+                    int okl = 1;
+                    if (lane == 0) okl = mbar_wait(smem_u32(&bars[S + slot]), (uint32_t)(((g / S) - 1) & 1), flags, p.err);
+                    ok = __shfl_sync(0xffffffffu, okl, 0) != 0;
+                    if (!ok) break;
                 }
+                const int cu0 = su0 + ch * p.ups;
+                const int cnu = min(p.ups, su0 + sunits - cu0);
+                uint8_t* st = smem + p.off_stage + (long long)slot * p.stage_bytes;
+                long long a = 0, b = 0;
+                int dst = 0;
+                const long long row = (long long)grp * 8 + lane;
+                if (whole ? lane == 0 : (lane < 8 && row < p.N)) {
+                    const long long s0 = whole ? (long long)grp * 8 * p.rb : row * p.rb + (long long)cu0 * UB;
+                    const long long e = whole ? min((long long)grp * 8 + 8, (long long)p.N) * p.rb : s0 + (long long)cnu * UB;
+                    a = s0 & ~15ll;
+                    b = (e + 15) & ~15ll;
+                    dst = whole ? 0 : lane * p.row_pitch;
+                    if (b > p.total_bytes) {
+                        b = e & ~15ll;
+                        for (long long q = b; q < e; ++q) st[dst + (q - a)] = p.wq[q];
+                        fence_proxy_async();
+                    }
+                }
+                const uint32_t bytes = b > a ? (uint32_t)(b - a) : 0u;
+                const uint32_t tx = __reduce_add_sync(0xffffffffu, bytes);
+                const uint32_t fb = smem_u32(&bars[slot]);
+                if (lane == 0) mbar_arrive_tx(fb, tx);
+                __syncwarp();
+                if (bytes) bulk_g2s(smem_u32(st + dst), p.wq + a, bytes, fb);
             }
-            const uint32_t bytes = b > a ? (uint32_t)(b - a) : 0u;
-            const uint32_t tx = __reduce_add_sync(0xffffffffu, bytes);
-            const uint32_t fb = smem_u32(&bars[slot]);
-            if (lane == 0) mbar_arrive_tx(fb, tx);
-            __syncwarp();
-            if (bytes) bulk_g2s(smem_u32(st + dst), p.wq + a, bytes, fb);
         }
         if (lane == 0) {
             const long long first = g > S ? g - S : 0;
@@ -263,138 +269,126 @@ __global__ void __launch_bounds__((kDmmaWarps + 1) * 32, 1) qmm_dmma_kernel(cons
     float* red = reinterpret_cast<float*>(smem + p.off_red);  // [2][16 warps][64]
     const int su = p.slice_units;
     long long g = 0;
-    for (int grp = grp0; grp < p.ngroups; grp += p.per_slice, ++g) {
-        const int slot = (int)(g % S);
-        const bool ok = mbar_wait(smem_u32(&bars[slot]), (uint32_t)((g / S) & 1), flags, p.err);
+    int tcount = 0;
+    for (int grp = grp0; grp < p.ngroups; grp += p.per_slice, ++tcount) {
         float acc0 = 0.0f, acc1 = 0.0f;  // (activation row g8, weight rows 2t4 and 2t4+1)
-        if (ok) {
-            const uint8_t* st = smem + p.off_stage + (long long)slot * p.stage_bytes;
-            // this thread's weight rows of the tile: g8 (B operand) and 2t4, 2t4+1 (scales)
-            auto rowptr = [&](int r) -> const uint8_t* {
-                const long long n = (long long)grp * 8 + r;
-                if (whole) return st + (int)(((long long)grp * 8 * p.rb) & 15) + (long long)r * p.rb;
-                return st + r * p.row_pitch + (int)((n * p.rb + (long long)su0 * UB) & 15);
-            };
-            const uint8_t* rB = rowptr(g8);
-            const uint8_t* rS0 = rowptr(2 * t4);
-            const uint8_t* rS1 = rowptr(2 * t4 + 1);
-            for (int u = warp; u < sunits; u += kDmmaWarps) {
-                if (WT == T_Q8_0) {
-                    uint32_t w0, w1;
-                    lds8_unaligned(rB + 34 * u + 2 + 8 * t4, w0, w1);
-                    const float dw0 = h2f(*reinterpret_cast<const uint16_t*>(rS0 + 34 * u));
-                    const float dw1 = h2f(*reinterpret_cast<const uint16_t*>(rS1 + 34 * u));
-                    if (AM == A_F32) {
-                        const uint4 xh = ld128(reinterpret_cast<const uint8_t*>(hi + ga * p.code_pitch + u * 32 + 8 * t4));
-                        const uint4 xl = ld128(reinterpret_cast<const uint8_t*>(lo + ga * p.code_pitch + u * 32 + 8 * t4));
-                        float d[4] = {0.f, 0.f, 0.f, 0.f};
-                        mma_f16(d, xh.x, xl.x, xh.y, xl.y, s8x2_to_h2(w0, SEL01), s8x2_to_h2(w0, SEL23));
-                        mma_f16(d, xh.z, xl.z, xh.w, xl.w, s8x2_to_h2(w1, SEL01), s8x2_to_h2(w1, SEL23));
-                        acc0 = fmaf(dw0, d[0] + d[2], acc0);
-                        acc1 = fmaf(dw1, d[1] + d[3], acc1);
-                    } else {
-                        const uint2 xa = ld64(codes + ga * p.code_pitch + u * 32 + 8 * t4);
-                        int d[4];
-                        mma_s8(d, xa.x, 0u, xa.y, 0u, w0, w1);
-                        if (EPI == E_Y) {
-                            const float dam = da[ga * su + u];
-                            acc0 = fmaf((float)d[0], dam * dw0, acc0);
-                            acc1 = fmaf((float)d[1], dam * dw1, acc1);
+        for (int ch = 0; ch < nch; ++ch, ++g) {
+            const int slot = (int)(g % S);
+            const bool ok = mbar_wait(smem_u32(&bars[slot]), (uint32_t)((g / S) & 1), flags, p.err);
+            const int cu0 = su0 + ch * p.ups;
+            const int cnu = min(p.ups, su0 + sunits - cu0);
+            if (ok) {
+                const uint8_t* st = smem + p.off_stage + (long long)slot * p.stage_bytes;
+                // rows of this thread in the stage: g8 (B operand), 2t4 and 2t4+1 (scales)
+                auto rowptr = [&](int r) -> const uint8_t* {
+                    const long long n = (long long)grp * 8 + r;
+                    if (whole) return st + (int)(((long long)grp * 8 * p.rb) & 15) + (long long)r * p.rb;
+                    return st + r * p.row_pitch + (int)((n * p.rb + (long long)cu0 * UB) & 15);
+                };
+                const uint8_t* rB = rowptr(g8);
+                const uint8_t* rS0 = rowptr(2 * t4);
+                const uint8_t* rS1 = rowptr(2 * t4 + 1);
+                const int ur0 = cu0 - su0;  // first unit of the chunk inside the slice
+                for (int uu = warp; uu < cnu; uu += kDmmaWarps) {
+                    const int u = ur0 + uu;  // unit index inside the slice (activation side)
+                    if (WT == T_Q8_0) {
+                        uint32_t w0, w1;
+                        lds8_unaligned(rB + 34 * uu + 2 + 8 * t4, w0, w1);
+                        const float dw0 = h2f(*reinterpret_cast<const uint16_t*>(rS0 + 34 * uu));
+                        const float dw1 = h2f(*reinterpret_cast<const uint16_t*>(rS1 + 34 * uu));
+                        if (AM == A_F32) {
+                            const uint4 xh = ld128(reinterpret_cast<const uint8_t*>(hi + ga * p.code_pitch + u * 32 + 8 * t4));
+                            const uint4 xl = ld128(reinterpret_cast<const uint8_t*>(lo + ga * p.code_pitch + u * 32 + 8 * t4));
+                            float d[4] = {0.f, 0.f, 0.f, 0.f};
+                            mma_f16(d, xh.x, xl.x, xh.y, xl.y, s8x2_to_h2(w0, SEL01), s8x2_to_h2(w0, SEL23));
+                            mma_f16(d, xh.z, xl.z, xh.w, xl.w, s8x2_to_h2(w1, SEL01), s8x2_to_h2(w1, SEL23));
+                            acc0 = fmaf(dw0, d[0] + d[2], acc0);
+                            acc1 = fmaf(dw1, d[1] + d[3], acc1);
                         } else {
-                            const long long n0 = (long long)grp * 8 + 2 * t4;
-                            if (g8 < p.M && n0 < p.N) p.sums[((long long)g8 * p.N + n0) * p.units + su0 + u] = d[0];
-                            if (g8 < p.M && n0 + 1 < p.N) p.sums[((long long)g8 * p.N + n0 + 1) * p.units + su0 + u] = d[1];
-                        }
-                    }
-                } else {
-                    const uint8_t* sbB = rB + 144 * u;
-                    const uint4 h0 = ld128(rS0 + 144 * u), h1 = ld128(rS1 + 144 * u);
-                    const float fD0 = h2f(h0.x), fDm0 = h2f(h0.x >> 16), fD1 = h2f(h1.x), fDm1 = h2f(h1.x >> 16);
-                    int ssc0 = 0, smn0 = 0, ssc1 = 0, smn1 = 0;
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const uint2 q = ld64(sbB + 16 + 32 * c + 8 * t4);
-#pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            const int j = 2 * c + h;
-                            const uint32_t nx = (q.x >> (4 * h)) & 0x0F0F0F0Fu, ny = (q.y >> (4 * h)) & 0x0F0F0F0Fu;
-                            int sc0, mn0, sc1, mn1;
-                            q4k_scmin(h0, j, sc0, mn0);
-                            q4k_scmin(h1, j, sc1, mn1);
-                            if (AM == A_F32) {
-                                const int kk = u * 256 + 32 * j + 8 * t4;
-                                const uint4 xh = ld128(reinterpret_cast<const uint8_t*>(hi + ga * p.code_pitch + kk));
-                                const uint4 xl = ld128(reinterpret_cast<const uint8_t*>(lo + ga * p.code_pitch + kk));
-                                float d[4] = {0.f, 0.f, 0.f, 0.f};
-                                mma_f16(d, xh.x, xl.x, xh.y, xl.y, u4x2_to_h2(nx, SEL01), u4x2_to_h2(nx, SEL23));
-                                mma_f16(d, xh.z, xl.z, xh.w, xl.w, u4x2_to_h2(ny, SEL01), u4x2_to_h2(ny, SEL23));
-                                const float X = xs[ga * su * 8 + u * 8 + j];
-                                acc0 += fmaf(fD0 * (float)sc0, d[0] + d[2], -(fDm0 * (float)mn0) * X);
-                                acc1 += fmaf(fD1 * (float)sc1, d[1] + d[3], -(fDm1 * (float)mn1) * X);
+                            const uint2 xa = ld64(codes + ga * p.code_pitch + u * 32 + 8 * t4);
+                            int d[4];
+                            mma_s8(d, xa.x, 0u, xa.y, 0u, w0, w1);
+                            if (EPI == E_Y) {
+                                const float dam = da[ga * su + u];
+                                acc0 = fmaf((float)d[0], dam * dw0, acc0);
+                                acc1 = fmaf((float)d[1], dam * dw1, acc1);
                             } else {
-                                const uint2 xa = ld64(codes + ga * p.code_pitch + u * 256 + 32 * j + 8 * t4);
-                                int d[4];
-                                mma_s8(d, xa.x, 0u, xa.y, 0u, nx, ny);
-                                const int bsj = bsum[ga * su * 8 + u * 8 + j];
-                                ssc0 += sc0 * d[0];
-                                ssc1 += sc1 * d[1];
-                                smn0 += mn0 * bsj;
-                                smn1 += mn1 * bsj;
+                                const long long n0 = (long long)grp * 8 + 2 * t4;
+                                if (g8 < p.M && n0 < p.N) p.sums[((long long)g8 * p.N + n0) * p.units + su0 + u] = d[0];
+                                if (g8 < p.M && n0 + 1 < p.N) p.sums[((long long)g8 * p.N + n0 + 1) * p.units + su0 + u] = d[1];
                             }
                         }
-                    }
-                    if (AM == A_INT8) {
-                        if (EPI == E_Y) {
-                            const float dam = da[ga * su + u];
-                            acc0 += dam * (fD0 * (float)ssc0 - fDm0 * (float)smn0);
-                            acc1 += dam * (fD1 * (float)ssc1 - fDm1 * (float)smn1);
-                        } else {
-                            const long long n0 = (long long)grp * 8 + 2 * t4;
-                            if (g8 < p.M && n0 < p.N) { int* o = p.sums + (((long long)g8 * p.N + n0) * p.units + su0 + u) * 2; o[0] = ssc0; o[1] = smn0; }
-                            if (g8 < p.M && n0 + 1 < p.N) { int* o = p.sums + (((long long)g8 * p.N + n0 + 1) * p.units + su0 + u) * 2; o[0] = ssc1; o[1] = smn1; }
+                    } else {
+                        const uint8_t* sbB = rB + 144 * uu;
+                        const uint4 h0 = ld128(rS0 + 144 * uu), h1 = ld128(rS1 + 144 * uu);
+                        const float fD0 = h2f(h0.x), fDm0 = h2f(h0.x >> 16), fD1 = h2f(h1.x), fDm1 = h2f(h1.x >> 16);
+                        int ssc0 = 0, smn0 = 0, ssc1 = 0, smn1 = 0;
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            const uint2 q = ld64(sbB + 16 + 32 * c + 8 * t4);
+#pragma unroll
+                            for (int h = 0; h < 2; ++h) {
+                                const int j = 2 * c + h;
+                                const uint32_t nx = (q.x >> (4 * h)) & 0x0F0F0F0Fu, ny = (q.y >> (4 * h)) & 0x0F0F0F0Fu;
+                                int sc0, mn0, sc1, mn1;
+                                q4k_scmin(h0, j, sc0, mn0);
+                                q4k_scmin(h1, j, sc1, mn1);
+                                if (AM == A_F32) {
+                                    const int kk = u * 256 + 32 * j + 8 * t4;
+                                    const uint4 xh = ld128(reinterpret_cast<const uint8_t*>(hi + ga * p.code_pitch + kk));
+                                    const uint4 xl = ld128(reinterpret_cast<const uint8_t*>(lo + ga * p.code_pitch + kk));
+                                    float d[4] = {0.f, 0.f, 0.f, 0.f};
+                                    mma_f16(d, xh.x, xl.x, xh.y, xl.y, u4x2_to_h2(nx, SEL01), u4x2_to_h2(nx, SEL23));
+                                    mma_f16(d, xh.z, xl.z, xh.w, xl.w, u4x2_to_h2(ny, SEL01), u4x2_to_h2(ny, SEL23));
+                                    const float X = xs[ga * su * 8 + u * 8 + j];
+                                    acc0 += fmaf(fD0 * (float)sc0, d[0] + d[2], -(fDm0 * (float)mn0) * X);
+                                    acc1 += fmaf(fD1 * (float)sc1, d[1] + d[3], -(fDm1 * (float)mn1) * X);
+                                } else {
+                                    const uint2 xa = ld64(codes + ga * p.code_pitch + u * 256 + 32 * j + 8 * t4);
+                                    int d[4];
+                                    mma_s8(d, xa.x, 0u, xa.y, 0u, nx, ny);
+                                    const int bsj = bsum[ga * su * 8 + u * 8 + j];
+                                    ssc0 += sc0 * d[0];
+                                    ssc1 += sc1 * d[1];
+                                    smn0 += mn0 * bsj;
+                                    smn1 += mn1 * bsj;
+                                }
+                            }
+                        }
+                        if (AM == A_INT8) {
+                            if (EPI == E_Y) {
+                                const float dam = da[ga * su + u];
+                                acc0 += dam * (fD0 * (float)ssc0 - fDm0 * (float)smn0);
+                                acc1 += dam * (fD1 * (float)ssc1 - fDm1 * (float)smn1);
+                            } else {
+                                const long long n0 = (long long)grp * 8 + 2 * t4;
+                                if (g8 < p.M && n0 < p.N) { int* o = p.sums + (((long long)g8 * p.N + n0) * p.units + su0 + u) * 2; o[0] = ssc0; o[1] = smn0; }
+                                if (g8 < p.M && n0 + 1 < p.N) { int* o = p.sums + (((long long)g8 * p.N + n0 + 1) * p.units + su0 + u) * 2; o[0] = ssc1; o[1] = smn1; }
+                            }
                         }
                     }
                 }
             }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&bars[S + slot]));
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&bars[S + slot]));
         if (EPI != E_Y) continue;
         // ---- tile epilogue: 16 warp partials of (activation row, weight row)
-        float* rb2 = red + (int)(g & 1) * kDmmaWarps * 64;
+        float* rb2 = red + (tcount & 1) * kDmmaWarps * 64;
         rb2[warp * 64 + g8 * 8 + 2 * t4] = acc0;
         rb2[warp * 64 + g8 * 8 + 2 * t4 + 1] = acc1;
         consumer_sync<kDmmaWarps>();
-        const bool aborted = flags[0] != 0;
-        float v = 0.0f;
-        int m = 0;
-        long long n = 0;
         if (tid < 64) {
-            m = tid >> 3;
-            n = (long long)grp * 8 + (tid & 7);
+            const int m = tid >> 3;
+            const long long n = (long long)grp * 8 + (tid & 7);
+            float v = 0.0f;
 #pragma unroll
             for (int w = 0; w < kDmmaWarps; ++w) v += rb2[w * 64 + tid];
             if (AM == A_F32) v *= rs[2 * m + 1];
-            if (!aborted && m < p.M && n < p.N) {
+            if (!flags[0] && m < p.M && n < p.N) {
                 if (p.kslices == 1) p.y[(long long)m * p.N + n] = v;
                 else p.partial[((long long)slice * p.M + m) * p.N + n] = v;
             }
-        }
-        if (p.kslices > 1) {
-            __threadfence();
-            consumer_sync<kDmmaWarps>();
-            if (tid == 0) {
-                const unsigned old = atomicAdd(&p.counters[grp], 1u);
-                flags[1] = (old == (unsigned)(p.kslices - 1)) ? 1 : 0;
-            }
-            consumer_sync<kDmmaWarps>();
-            if (flags[1] && !aborted && tid < 64 && m < p.M && n < p.N) {
-                __threadfence();
-                float t = 0.0f;
-                for (int s = 0; s < p.kslices; ++s) t += __ldcg(p.partial + ((long long)s * p.M + m) * p.N + n);
-                p.y[(long long)m * p.N + n] = t;
-            }
-            consumer_sync<kDmmaWarps>();
         }
     }
 }
@@ -454,16 +448,18 @@ inline bool plan_dmma(int wt, int am, long long M, long long N, long long K, int
         off = round_up(off + 2 * kDmmaWarps * 64 * 4, 128);
         p.off_stage = off;
         long long sb;
-        const long long slice_bytes = (long long)su * ub;
-        if (ks == 1 && p.rb < 2048) {
+        // K chunk per stage: ~4 KB per row copy (4096 values of Q8_0, 8192 of Q4_K)
+        const int ups = su < (wt == T_Q8_0 ? 128 : 32) ? su : (wt == T_Q8_0 ? 128 : 32);
+        if (ks == 1 && ups == su && p.rb < 2048) {
             sb = 8 * p.rb + 64;  // short rows: one contiguous copy of the whole tile
             p.row_pitch = 0;
         } else {
             // one copy per row; a pitch of 16 mod 128 bytes keeps the 8 rows of a
             // B fragment load on distinct banks (row bytes are often 0 mod 128)
-            p.row_pitch = pitch_mod((int)slice_bytes + 48, 16);
+            p.row_pitch = pitch_mod(ups * ub + 48, 16);
             sb = 8LL * p.row_pitch;
         }
+        p.ups = ups;
         sb = (sb + 127) / 128 * 128;
         const int stages = sb > 0 ? (int)((smem_max - off) / sb) : 0;
         if (stages < 2) continue;
@@ -480,7 +476,7 @@ inline bool plan_dmma(int wt, int am, long long M, long long N, long long K, int
     if (per > p.ngroups) per = p.ngroups;
     p.per_slice = per;
     pl.grid = per * p.kslices;
-    pl.workspace = p.kslices > 1 ? ((size_t)p.kslices * M * N * 4 + 255) / 256 * 256 + (size_t)p.ngroups * 4 : 0;
+    pl.workspace = p.kslices > 1 ? (size_t)p.kslices * M * N * 4 : 0;
     out = pl;
     return true;
 }

@@ -178,7 +178,21 @@ __global__ void dequant_q4_k_kernel(const uint8_t* __restrict__ q, long long nsu
 
 inline unsigned grid_for(long long n, int block) { return (unsigned)((n + block - 1) / block); }
 
+// y[i] = sum over K slices s = 0..ks-1 of partial[s][i], in slice order.
+__global__ void splitk_reduce_kernel(const float* __restrict__ partial, long long n, int ks, float* __restrict__ y) {
+    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    float v = 0.0f;
+    for (int s = 0; s < ks; ++s) v += __ldg(partial + (long long)s * n + i);
+    y[i] = v;
+}
+
 }  // namespace
+
+cudaError_t launch_splitk_reduce(const float* partial, long long n, int ks, float* y, cudaStream_t s) {
+    splitk_reduce_kernel<<<grid_for(n, 256), 256, 0, s>>>(partial, n, ks, y);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_quantize(int type, const float* x, long long rows, long long K, void* out, cudaStream_t s) {
     const int bs = 128;

@@ -43,7 +43,8 @@ extern "C" qmm_status qmm_matmul_static_workspace(qmm_type wtype, qmm_act_mode m
     void* ws = nullptr;
     const qmm_status st = static_workspace_address(&ws);
     if (st != QMM_OK) return st;
-    // qmm_matmul clears the part of the workspace that must start at zero
-    // (the split-K arrival counters) on `stream` before its launch.
+    // qmm_matmul clears on `stream` the part of the workspace that must start
+    // at zero (the arrival counters of a K split in the prefill kernel) before
+    // its launch; partial sums are overwritten and need no clearing.
     return qmm_matmul(wtype, mode, wq, x, y, M, N, K, ws, (size_t)QMM_STATIC_WORKSPACE_BYTES, stream);
 }

@@ -157,7 +157,8 @@ qmm_status qmm_block_sums(qmm_type wtype, const void* wq, const float* x, int64_
    - The first call on a device looks up the array's device address (with
      that device current); make that first call before any stream capture.
    - Every call shares the one array and it keeps the last call's contents:
-     the split-K counters are cleared on `stream` by each call, but calls that
+     each call clears on `stream` whatever part must start at zero (the
+     arrival counters of a K split in the prefill kernel), but calls that
      overlap on the GPU (other streams, other host threads) race on it.
    Other arguments and errors as qmm_matmul. */
 #define QMM_STATIC_WORKSPACE_BYTES (8u << 20)
