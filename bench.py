@@ -56,22 +56,39 @@ def peaks():
     return 6800.0, 1900.0, "fallback"
 
 
-def kernel_hash() -> str:
+# source files that define each kernel (its traffic figure is void once they change)
+KERNEL_SOURCES = {
+    "qmm_gemv_kernel": ["qmm_gemv.cuh", "qmm_device.cuh"],
+    "qmm_dmma_kernel": ["qmm_dmma.cuh", "qmm_device.cuh"],
+    "qmm_stream_kernel": ["qmm_stream.cuh", "qmm_device.cuh"],
+}
+
+
+def kernel_hash(kernel: str) -> str:
     h = hashlib.sha256()
     cs = os.path.join(ROOT, "gguf_block_quantized_qmatmul_gb300", "csrc")
-    for f in sorted(os.listdir(cs)):
+    for f in KERNEL_SOURCES[kernel]:
         h.update(open(os.path.join(cs, f), "rb").read())
     return h.hexdigest()[:16]
 
 
-def ncu_traffic():
-    """Per-launch DRAM bytes / algorithmic bytes from the committed ncu summary,
-    valid only for the kernel sources it was taken on."""
+def kernel_of(wtype: str, mode: str, M: int) -> str:
+    """The kernel qmm_matmul dispatches to (the library's own rule): int8_act
+    with M <= 4 -> per-thread dp4a GEMV; other M <= 8 -> 8-row tensor-core
+    decode kernel; larger M -> the streaming MMA kernel."""
+    if mode == "int8_act" and M <= 4:
+        return "qmm_gemv_kernel"
+    return "qmm_dmma_kernel" if M <= 8 else "qmm_stream_kernel"
+
+
+def ncu_traffic(kernel: str):
+    """DRAM bytes per algorithmic byte of `kernel` from the committed ncu
+    summary (profiles/traffic.json), or None if the kernel changed since."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
-    d = json.load(open(p))
-    if d.get("kernel_hash") != kernel_hash():
+    d = json.load(open(p)).get(kernel)
+    if not d or d.get("source_hash") != kernel_hash(kernel):
         return None
     return d
 
@@ -227,6 +244,74 @@ def make_buffers(q, torch, wtype: str, seed0: int):
     return out
 
 
+def small_configs(q, torch, stream):
+    """Latency-bound configurations: one Q8_0 GEMV 576x576 (M=1), the Q4_K
+    576x1536 GEMV (M = 1, 2, 4, 8), and the 211-matmul SmolLM2-135M-shaped
+    decode step (all Q8_0, M=1), each in both forms.  The step is timed with
+    the L2 flushed before every step (a 2 x L2 write), eagerly and replayed
+    from a CUDA graph."""
+    out = {}
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def time_calls(fn, reps=200):
+        for _ in range(10):
+            fn()
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        for _ in range(reps):
+            fn()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        return ev0.elapsed_time(ev1) / reps * 1e3  # us
+
+    for wtype, N, K, Ms in (("q8_0", 576, 576, (1,)), ("q4_k", 576, 1536, (1, 2, 4, 8))):
+        wq = q.quantize_weights(torch.from_numpy(qmm_synth.weights(N, K)).cuda(), wtype)
+        for M in Ms:
+            x = torch.from_numpy(qmm_synth.activations(M, K)).cuda()
+            y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+            for mode in MODES:
+                us = time_calls(lambda: q.matmul(wq, x, wtype, mode, N=N, out=y))
+                out[f"{wtype} {N}x{K} M{M} {mode}"] = {"us_per_call": round(us, 2),
+                                                      "weight_GBps": round(wq.numel() / (us * 1e3), 1)}
+    # SmolLM2-135M-shaped decode step: 211 Q8_0 matmuls, M = 1
+    lins = qmm_synth.smollm2_linears()
+    wqs = []
+    for i, (_, N, K) in enumerate(lins):
+        g = torch.Generator(device="cuda").manual_seed(1000 + i)
+        w = torch.randn((N, K), generator=g, device="cuda") * 0.02
+        wqs.append((q.quantize_weights(w, "q8_0"), N, K))
+    step_bytes = sum(w.numel() for w, _, _ in wqs)
+    xs = {K: torch.from_numpy(qmm_synth.activations(1, K)).cuda() for K in (576, 1536)}
+    ys = [torch.empty((1, N), dtype=torch.float32, device="cuda") for _, N, _ in wqs]
+    flush = torch.empty(2 * 129 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+    for mode in MODES:
+        def step():
+            for (w, N, K), y in zip(wqs, ys):
+                q.matmul(w, xs[K], "q8_0", mode, N=N, out=y)
+        step()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
+        torch.cuda.synchronize()
+        res = {}
+        for name, fn in (("eager", step), ("graph", graph.replay)):
+            tot = 0.0
+            reps = 20
+            for _ in range(reps + 3):
+                flush.fill_(1.0)
+                ev0.record(stream)
+                fn()
+                ev1.record(stream)
+                torch.cuda.synchronize()
+                tot += ev0.elapsed_time(ev1)
+            ms = tot / (reps + 3)
+            res[name] = {"ms_per_step": round(ms, 4), "weight_GBps": round(step_bytes / (ms * 1e6), 1)}
+        out[f"smollm2_step_211_matmuls q8_0 M1 {mode} (L2 flushed)"] = res
+    out["smollm2_step_weight_bytes"] = step_bytes
+    return out
+
+
 def run_ours(args):
     import torch
 
@@ -280,24 +365,29 @@ def run_ours(args):
     bytes_per_step = sum(wbytes[t] for (_, t, _, _) in calls)
     value = world * bytes_per_step * args.steps / (elapsed_ms / 1e3) / 1e9
 
-    # per-call durations -> roofline and breakdown
+    # per-call durations -> per-kernel roofline and breakdown
     per = {}
-    alg_bytes, dur_ms = 0.0, 0.0
+    kern = {}  # kernel -> [algorithmic bytes, ms, launches]
     for s in range(args.steps):
         for i, (M, t, mode, b) in enumerate(calls):
             d = ev[s][i].elapsed_time(ev[s][i + 1])
             ab = wbytes[t] + M * K_DEC * 4 + M * N_DEC * 4
-            alg_bytes += ab
-            dur_ms += d
+            k = kern.setdefault(kernel_of(t, mode, M), [0.0, 0.0, 0])
+            k[0] += ab
+            k[1] += d
+            k[2] += 1
             per.setdefault((t, mode, M), []).append((wbytes[t], d))
-    achieved = alg_bytes / (dur_ms / 1e3) / 1e9
     sweep = {f"{t}/{mode}/M{M}": round(sum(b for b, _ in v) / (sum(d for _, d in v) / 1e3) / 1e9, 1)
              for (t, mode, M), v in sorted(per.items())}
-    tr = ncu_traffic()
+    dom = max(kern, key=lambda k: kern[k][1])
+    alg_bytes, dur_ms, nl = kern[dom]
+    achieved = alg_bytes / (dur_ms / 1e3) / 1e9
+    tr = ncu_traffic(dom)
+    traffic = None if tr is None else tr["dram_bytes_per_alg_byte"] * alg_bytes / nl
+    kernels = {k: {"GBps": round(v[0] / (v[1] / 1e3) / 1e9, 1), "frac": round(v[0] / (v[1] / 1e3) / 1e9 / hbm_peak, 4),
+                   "time_share": round(v[1] / sum(x[1] for x in kern.values()), 3), "launches": v[2]}
+               for k, v in kern.items()}
     launches = len(calls)
-    traffic = None
-    if tr is not None:
-        traffic = tr["dram_bytes_per_alg_byte"] * alg_bytes / (launches * args.steps)
 
     # end to end through the public API with pinned host buffers
     xh = {M: xs[M].cpu().pin_memory() for M in MS}
@@ -351,6 +441,8 @@ def run_ours(args):
                                                             "frac_of_bf16_dense_peak": round(tops / bf16_peak, 4)}
             del wq
 
+    small = small_configs(q, torch, stream) if not args.no_small else {}
+
     # oracle on the host cores, bounded sample (rank 0, N = 1 only)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
@@ -371,13 +463,14 @@ def run_ours(args):
                            "each >= 132 MB, rotated per call)", "parallelism": f"replicas x{world}"},
                 "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                              "frac": round(achieved / hbm_peak, 4), "traffic": traffic,
-                             "kernel": "qmm_stream_kernel", "peak_source": f"{peak_src} hbm_gbs",
+                             "kernel": dom, "peak_source": f"{peak_src} hbm_gbs",
                              "alg_bytes": "weights + x f32 + y f32 per launch"},
+                "kernels": kernels,
                 "cpu_baseline": cpu,
                 "e2e": {"value": round(e2e, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                         "d2h_bytes_per_step": d2h},
                 "gpu_launches": launches * args.steps,
-                "clocks": ck, "sweep_GBps": sweep, "prefill": prefill}
+                "clocks": ck, "sweep_GBps": sweep, "prefill": prefill, "small_configs": small}
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
@@ -415,6 +508,7 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=4096)
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-small", action="store_true")
     ap.add_argument("--profile", default=None, help="wtype:mode:M:N:K -- run a few launches for ncu and exit")
     ap.add_argument("--launches", type=int, default=4)
     args = ap.parse_args()
