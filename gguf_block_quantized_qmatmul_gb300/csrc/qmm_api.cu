@@ -92,6 +92,13 @@ qmm_status stream_call(qmm_type wtype, int am, int epi, const void* wq, const fl
         if (split && launch_splitk_reduce(dp.p.partial, M * N, dp.p.kslices, y, s) != cudaSuccess) return QMM_ERR_CUDA;
         return QMM_OK;
     }
+    PrefillPlan fp;
+    if (epi == E_Y && plan_prefill(wt, am, M, N, K, sms, smem, fp)) {  // prefill: f16 tensor-core GEMM
+        fp.p.y = y;
+        fp.p.err = err;
+        if (!ws || ws_bytes < fp.workspace) return QMM_ERR_WORKSPACE;
+        return launch_prefill(am, fp, wq, x, ws, smem, s) == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
+    }
     StreamPlan pl;
     if (!plan_stream(wt, am, epi, M, N, K, sms, smem, pl)) return QMM_ERR_SHAPE;
     pl.p.wq = static_cast<const uint8_t*>(wq);
@@ -188,6 +195,8 @@ size_t qmm_matmul_workspace(qmm_type wtype, qmm_act_mode mode, int64_t M, int64_
     DmmaPlan dp;
     if (M <= kDecodeMaxM && plan_dmma(wt, mode == QMM_INT8_ACT ? A_INT8 : A_F32, M, N, K, sms, smem, dp))
         return dp.workspace;
+    PrefillPlan fp;
+    if (plan_prefill(wt, mode == QMM_INT8_ACT ? A_INT8 : A_F32, M, N, K, sms, smem, fp)) return fp.workspace;
     StreamPlan pl;
     if (!plan_stream(wtype == QMM_Q8_0 ? T_Q8_0 : T_Q4_K, mode == QMM_INT8_ACT ? A_INT8 : A_F32, E_Y, M, N, K, sms,
                      smem, pl))

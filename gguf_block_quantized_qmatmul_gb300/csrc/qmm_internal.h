@@ -5,6 +5,7 @@
 
 #include "qmm_dmma.cuh"
 #include "qmm_gemv.cuh"
+#include "qmm_prefill.cuh"
 #include "qmm_stream.cuh"
 
 namespace qmm {
@@ -17,6 +18,8 @@ cudaError_t launch_stream_q4_k(int am, int epi, const StreamPlan& plan, int smem
 cudaError_t launch_gemv_q8_0(int epi, const GemvPlan& plan, int smem_max, cudaStream_t s);
 cudaError_t launch_gemv_q4_k(int epi, const GemvPlan& plan, int smem_max, cudaStream_t s);
 cudaError_t launch_dmma(int wt, int am, int epi, const DmmaPlan& plan, int smem_max, cudaStream_t s);
+cudaError_t launch_prefill(int am, const PrefillPlan& plan, const void* wq, const float* x, void* ws, int smem_max,
+                           cudaStream_t s);
 
 // largest activation batch served by the per-thread dp4a GEMV (int8_act);
 // larger decode batches (and every f32_act decode batch up to 8) use the

@@ -1,0 +1,345 @@
+// qmm_prefill.cuh -- prefill GEMM (M > 8 activation rows) for Q8_0 weights.
+//
+// Both QMatMul forms ("同一个 GGUF，CPU 和 Metal 生成的文字不一样" section 出处):
+//   int8_act: y = sum_b f(d_w) f(d_a) isum_b, isum_b the exact integer dot of
+//             the 32 weight codes and the row-quantized activation codes;
+//   f32_act:  y = sum_k x_k w_k with w = f(d_w) q dequantized in-kernel.
+//
+// GB300 mapping.  On this part the warp-level f16 MMA runs at ~4x the rate of
+// the warp-level int8 MMA (about 605 vs 152 TFLOP/s measured), and every code
+// (|q| <= 127) is exact in f16, as is every per-block sum (< 2^24 in the f32
+// accumulator), so the integer block sums of the CPU form are taken with
+// mma.m16n8k16.f16 on integer-valued operands: still exact.  A small prologue
+// kernel writes the activation operand once per call into the workspace:
+//   int8_act: f16 codes [M][K] and f32 scales f(d_a) [M][K/32];
+//   f32_act:  each row scaled by a power of two and split into two f16 planes
+//             hi, lo (x 2^s = hi + lo to 2^-22 relative), and 2^-s per row.
+// The GEMM CTA owns a 128 (f32_act: 64) x 128 output tile; a producer warp
+// fetches per K chunk of 256 one 2-D TMA box of raw weight bytes (128 rows x
+// 272 bytes = 8 Q8_0 blocks per row) and 128B-swizzled boxes of the f16
+// activation planes; 8 consumer warps convert the weight codes to f16 in
+// registers (exact), run the MMAs of one 32-value block with a zero
+// accumulator and fold the block sum into the f32 result with the block's
+// scales (f(d_w) f(d_a) or f(d_w)).
+#pragma once
+
+#include <cuda.h>
+
+#include "qmm_device.cuh"
+
+namespace qmm {
+
+constexpr int kPfWarps = 8;            // consumer warps (+1 producer)
+constexpr int kPfBN = 128;             // weight rows per tile
+constexpr int kPfKC = 256;             // K values per stage (8 Q8_0 blocks)
+constexpr int kPfWRow = kPfKC / 32 * 34;  // raw bytes per weight row per stage (272)
+
+struct PrefillParams {
+    float* y;
+    const float* rs;  // f32_act: 2^-s per activation row
+    unsigned* err;
+    int M, N, K;
+    int bm;           // activation rows per tile (128 int8_act, 64 f32_act)
+    int n_mt, n_nt, ntiles;
+    int kchunks;
+    int stages;
+    int stage_bytes;
+    int off_w, off_a, off_a2, off_s;  // offsets inside a stage
+};
+
+// load one TMA box (2-D) into shared memory, completing on an mbarrier
+__device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            dst),
+        "l"(map), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+// byte offset of (row, half index h) in a [rows][64 halves] 128B-swizzled box
+__device__ __forceinline__ int swz128(int row, int h) { return row * 128 + ((((h >> 3) ^ row) & 7) << 4); }
+
+template <int AM>
+__global__ void __launch_bounds__((kPfWarps + 1) * 32, 1)
+    qmm_prefill_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUtensorMap ta,
+                       const __grid_constant__ CUtensorMap ta2, const __grid_constant__ CUtensorMap ts,
+                       const PrefillParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // 1024-byte alignment for the swizzled boxes
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int S = p.stages;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem);  // full[S], empty[S]
+    volatile int* flags = reinterpret_cast<volatile int*>(smem + 256);
+    uint8_t* stage0 = smem + 1024;
+    if (tid == 0) {
+        for (int i = 0; i < S; ++i) {
+            mbar_init(smem_u32(&bars[i]), 1);
+            mbar_init(smem_u32(&bars[S + i]), kPfWarps);
+        }
+        flags[0] = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    const int BM = p.bm;
+
+    if (warp == kPfWarps) {
+        // ------------------------------ producer ------------------------------
+        if (lane != 0) return;
+        long long g = 0;
+        const uint32_t a_box = (uint32_t)BM * 128;  // bytes of one [BM][64 halves] box
+        const uint32_t tx = (uint32_t)kPfBN * kPfWRow + a_box * 4 * (AM == A_F32 ? 2 : 1) +
+                            (AM == A_INT8 ? (uint32_t)BM * 32 : 0u);
+        for (int t = blockIdx.x; t < p.ntiles; t += gridDim.x) {
+            const int m0 = (t % p.n_mt) * BM, n0 = (t / p.n_mt) * kPfBN;
+            bool ok = true;
+            for (int kc = 0; kc < p.kchunks; ++kc, ++g) {
+                const int slot = (int)(g % S);
+                if (g >= S && !mbar_wait(smem_u32(&bars[S + slot]), (uint32_t)(((g / S) - 1) & 1), flags, p.err)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t* st = stage0 + (long long)slot * p.stage_bytes;
+                const uint32_t fb = smem_u32(&bars[slot]);
+                mbar_arrive_tx(fb, tx);
+                tma_2d(smem_u32(st + p.off_w), &tw, kc * (kPfWRow / 2), n0, fb);
+                for (int s = 0; s < 4; ++s) tma_2d(smem_u32(st + p.off_a + s * a_box), &ta, kc * kPfKC + s * 64, m0, fb);
+                if (AM == A_F32)
+                    for (int s = 0; s < 4; ++s) tma_2d(smem_u32(st + p.off_a2 + s * a_box), &ta2, kc * kPfKC + s * 64, m0, fb);
+                else
+                    tma_2d(smem_u32(st + p.off_s), &ts, kc * 8, m0, fb);
+            }
+            if (!ok) break;
+        }
+        const long long first = g > S ? g - S : 0;
+        for (long long q = first; q < g; ++q) mbar_wait(smem_u32(&bars[q % S]), (uint32_t)((q / S) & 1), flags, p.err);
+        return;
+    }
+
+    // ------------------------------ consumers ------------------------------
+    // int8_act: warps 2 (M) x 4 (N), warp tile 64 x 32 (4 m16 x 4 n8)
+    // f32_act : warps 2 (M) x 4 (N), warp tile 32 x 32 (2 m16 x 4 n8)
+    constexpr int MI = AM == A_INT8 ? 4 : 2;
+    const int wm = warp >> 2, wn = warp & 3;
+    const int g8 = lane >> 2, t4 = lane & 3;
+    long long g = 0;
+    for (int t = blockIdx.x; t < p.ntiles; t += gridDim.x) {
+        const int m0 = (t % p.n_mt) * BM, n0 = (t / p.n_mt) * kPfBN;
+        float acc[MI][4][4];
+#pragma unroll
+        for (int i = 0; i < MI; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[i][j][e] = 0.0f;
+        for (int kc = 0; kc < p.kchunks; ++kc, ++g) {
+            const int slot = (int)(g % S);
+            const bool ok = mbar_wait(smem_u32(&bars[slot]), (uint32_t)((g / S) & 1), flags, p.err);
+            if (ok) {
+                const uint8_t* st = stage0 + (long long)slot * p.stage_bytes;
+                const uint8_t* W = st + p.off_w;
+                const uint8_t* A = st + p.off_a;
+                const uint8_t* A2 = st + p.off_a2;
+                const float* SC = reinterpret_cast<const float*>(st + p.off_s);
+#pragma unroll 1
+                for (int b = 0; b < 8; ++b) {
+                    // weight (B) fragments and scales of the warp's 4 n8 tiles
+                    uint32_t bf[4][4];
+                    float dw[4][2];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int nr = wn * 32 + 8 * j;
+                        uint32_t w0, w1;
+                        lds8_unaligned(W + (nr + g8) * kPfWRow + 34 * b + 2 + 8 * t4, w0, w1);
+                        bf[j][0] = s8x2_to_h2(w0, SEL01);
+                        bf[j][1] = s8x2_to_h2(w0, SEL23);
+                        bf[j][2] = s8x2_to_h2(w1, SEL01);
+                        bf[j][3] = s8x2_to_h2(w1, SEL23);
+                        dw[j][0] = h2f(*reinterpret_cast<const uint16_t*>(W + (nr + 2 * t4) * kPfWRow + 34 * b));
+                        dw[j][1] = h2f(*reinterpret_cast<const uint16_t*>(W + (nr + 2 * t4 + 1) * kPfWRow + 34 * b));
+                    }
+                    // activation (A) fragments: 8 halves at K offset 32b + 8t of rows g, g+8
+                    const int hk = b * 32 + 8 * t4;        // half index inside the 256-value chunk
+                    const int box = (hk >> 6) * BM * 128;  // which 64-half box
+#pragma unroll
+                    for (int i = 0; i < MI; ++i) {
+                        const int r0 = wm * (MI * 16) + 16 * i + g8, r1 = r0 + 8;
+                        const uint4 x0 = ld128(A + box + swz128(r0, hk & 63));
+                        const uint4 x1 = ld128(A + box + swz128(r1, hk & 63));
+                        if (AM == A_INT8) {
+                            const float da0 = SC[r0 * 8 + b], da1 = SC[r1 * 8 + b];
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                float d[4] = {0.f, 0.f, 0.f, 0.f};
+                                mma_f16(d, x0.x, x1.x, x0.y, x1.y, bf[j][0], bf[j][1]);
+                                mma_f16(d, x0.z, x1.z, x0.w, x1.w, bf[j][2], bf[j][3]);
+                                acc[i][j][0] = fmaf(d[0], da0 * dw[j][0], acc[i][j][0]);
+                                acc[i][j][1] = fmaf(d[1], da0 * dw[j][1], acc[i][j][1]);
+                                acc[i][j][2] = fmaf(d[2], da1 * dw[j][0], acc[i][j][2]);
+                                acc[i][j][3] = fmaf(d[3], da1 * dw[j][1], acc[i][j][3]);
+                            }
+                        } else {
+                            const uint4 l0 = ld128(A2 + box + swz128(r0, hk & 63));
+                            const uint4 l1 = ld128(A2 + box + swz128(r1, hk & 63));
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                float d[4] = {0.f, 0.f, 0.f, 0.f};
+                                mma_f16(d, l0.x, l1.x, l0.y, l1.y, bf[j][0], bf[j][1]);
+                                mma_f16(d, l0.z, l1.z, l0.w, l1.w, bf[j][2], bf[j][3]);
+                                mma_f16(d, x0.x, x1.x, x0.y, x1.y, bf[j][0], bf[j][1]);
+                                mma_f16(d, x0.z, x1.z, x0.w, x1.w, bf[j][2], bf[j][3]);
+                                acc[i][j][0] = fmaf(d[0], dw[j][0], acc[i][j][0]);
+                                acc[i][j][1] = fmaf(d[1], dw[j][1], acc[i][j][1]);
+                                acc[i][j][2] = fmaf(d[2], dw[j][0], acc[i][j][2]);
+                                acc[i][j][3] = fmaf(d[3], dw[j][1], acc[i][j][3]);
+                            }
+                        }
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&bars[S + slot]));
+        }
+        if (flags[0]) continue;
+        // store: thread owns (row g, cols 2t, 2t+1) and (row g+8, ...) of each m16 x n8 tile
+#pragma unroll
+        for (int i = 0; i < MI; ++i) {
+            const int ra = m0 + wm * (MI * 16) + 16 * i + g8, rb = ra + 8;
+            const float sa = (AM == A_F32 && ra < p.M) ? __ldg(p.rs + ra) : 1.0f;
+            const float sb = (AM == A_F32 && rb < p.M) ? __ldg(p.rs + rb) : 1.0f;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int c = n0 + wn * 32 + 8 * j + 2 * t4;
+                if (ra < p.M) {
+                    if (c < p.N) p.y[(long long)ra * p.N + c] = acc[i][j][0] * sa;
+                    if (c + 1 < p.N) p.y[(long long)ra * p.N + c + 1] = acc[i][j][1] * sa;
+                }
+                if (rb < p.M) {
+                    if (c < p.N) p.y[(long long)rb * p.N + c] = acc[i][j][2] * sb;
+                    if (c + 1 < p.N) p.y[(long long)rb * p.N + c + 1] = acc[i][j][3] * sb;
+                }
+            }
+        }
+    }
+}
+
+// activation prologue: the A operand of the prefill GEMM, written to the workspace
+template <int AM>
+__global__ void prefill_act_kernel(const float* __restrict__ x, int M, int K, __half* __restrict__ a,
+                                   __half* __restrict__ a2, float* __restrict__ sc) {
+    if (AM == A_INT8) {
+        // one thread per (row, 32-block): Q8_0 codes as f16, scale f(d)
+        const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+        const long long nb = K / 32;
+        if (i >= (long long)M * nb) return;
+        const long long r = i / nb, b = i - r * nb;
+        uint32_t c[8];
+        float d;
+        quant_q8_0_32(x + r * K + b * 32, c, d);
+        uint32_t h[16];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            h[2 * k] = s8x2_to_h2(c[k], SEL01);
+            h[2 * k + 1] = s8x2_to_h2(c[k], SEL23);
+        }
+        uint4* dst = reinterpret_cast<uint4*>(a + r * K + b * 32);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) dst[k] = make_uint4(h[4 * k], h[4 * k + 1], h[4 * k + 2], h[4 * k + 3]);
+        sc[r * nb + b] = h2f(f2h(d));
+    } else {
+        // one CTA per row: power-of-two scale from max |x|, then two f16 planes
+        const int r = blockIdx.x;
+        __shared__ float red[32];
+        __shared__ float s_scale;
+        float amax = 0.0f;
+        const float4* src = reinterpret_cast<const float4*>(x + (long long)r * K);
+        for (int i = threadIdx.x; i < K / 4; i += blockDim.x) {
+            const float4 v = __ldg(src + i);
+            amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            float m = 0.0f;
+            for (int w = 0; w < (int)(blockDim.x >> 5); ++w) m = fmaxf(m, red[w]);
+            int s = 0;
+            if (m > 0.0f) {
+                const int e = (int)((__float_as_uint(m) >> 23) & 0xff) - 127;
+                s = 14 - e;
+                s = s > 100 ? 100 : (s < -100 ? -100 : s);
+            }
+            s_scale = ldexpf(1.0f, s);
+            sc[r] = ldexpf(1.0f, -s);
+        }
+        __syncthreads();
+        const float scale = s_scale;
+        for (int i = threadIdx.x; i < K / 4; i += blockDim.x) {
+            const float4 v4 = __ldg(src + i);
+            const float v[4] = {__fmul_rn(v4.x, scale), __fmul_rn(v4.y, scale), __fmul_rn(v4.z, scale),
+                                __fmul_rn(v4.w, scale)};
+            __half hh[4], ll[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                hh[k] = __float2half_rn(v[k]);
+                ll[k] = __float2half_rn(__fsub_rn(v[k], __half2float(hh[k])));
+            }
+            reinterpret_cast<uint2*>(a + (long long)r * K)[i] =
+                make_uint2(__half_as_ushort(hh[0]) | ((uint32_t)__half_as_ushort(hh[1]) << 16),
+                           __half_as_ushort(hh[2]) | ((uint32_t)__half_as_ushort(hh[3]) << 16));
+            reinterpret_cast<uint2*>(a2 + (long long)r * K)[i] =
+                make_uint2(__half_as_ushort(ll[0]) | ((uint32_t)__half_as_ushort(ll[1]) << 16),
+                           __half_as_ushort(ll[2]) | ((uint32_t)__half_as_ushort(ll[3]) << 16));
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// host-side planning
+// ---------------------------------------------------------------------------
+
+struct PrefillPlan {
+    PrefillParams p;
+    int grid;
+    size_t smem;
+    size_t workspace;  // bytes of the activation operand
+    size_t ws_a, ws_a2, ws_s;  // offsets in the workspace
+};
+
+inline bool plan_prefill(int wt, int am, long long M, long long N, long long K, int sm_count, int smem_max,
+                         PrefillPlan& out) {
+    if (wt != T_Q8_0 || K % kPfKC != 0 || M < 9) return false;
+    PrefillPlan pl{};
+    PrefillParams& p = pl.p;
+    p.M = (int)M;
+    p.N = (int)N;
+    p.K = (int)K;
+    p.bm = am == A_INT8 ? 128 : 64;
+    p.n_mt = (int)((M + p.bm - 1) / p.bm);
+    p.n_nt = (int)((N + kPfBN - 1) / kPfBN);
+    p.ntiles = p.n_mt * p.n_nt;
+    p.kchunks = (int)(K / kPfKC);
+    const int a_box = p.bm * 128;
+    p.off_w = 0;
+    p.off_a = round_up(kPfBN * kPfWRow, 1024);
+    p.off_a2 = p.off_a + 4 * a_box;
+    p.off_s = p.off_a2 + (am == A_F32 ? 4 * a_box : 0);
+    p.stage_bytes = round_up(p.off_s + (am == A_INT8 ? p.bm * 32 : 0), 1024);
+    const int base = 1024 + 1024;  // alignment slack + barriers
+    const int stages = (smem_max - base) / p.stage_bytes;
+    if (stages < 2) return false;
+    p.stages = stages > 4 ? 4 : stages;
+    pl.smem = (size_t)base + (size_t)p.stages * p.stage_bytes;
+    pl.grid = p.ntiles < sm_count ? p.ntiles : sm_count;
+    // workspace: activation planes (16-byte aligned pieces)
+    pl.ws_a = 0;
+    pl.ws_a2 = (size_t)M * K * 2;
+    pl.ws_s = pl.ws_a2 + (am == A_F32 ? (size_t)M * K * 2 : 0);
+    pl.workspace = pl.ws_s + (am == A_INT8 ? (size_t)M * (K / 32) * 4 : (size_t)M * 4);
+    pl.workspace = (pl.workspace + 255) / 256 * 256;
+    out = pl;
+    return true;
+}
+
+}  // namespace qmm
