@@ -184,6 +184,23 @@ __device__ __forceinline__ void mma_f16(float d[4], uint32_t a0, uint32_t a1, ui
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// Packed f32x2 arithmetic (two lanes per instruction).
+__device__ __forceinline__ unsigned long long f2pack(float lo, float hi) {
+    return (unsigned long long)__float_as_uint(lo) | ((unsigned long long)__float_as_uint(hi) << 32);
+}
+__device__ __forceinline__ unsigned long long mul2(unsigned long long a, unsigned long long b) {
+    unsigned long long d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigned long long b, unsigned long long c) {
+    unsigned long long d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ float f2lo(unsigned long long v) { return __uint_as_float((uint32_t)v); }
+__device__ __forceinline__ float f2hi(unsigned long long v) { return __uint_as_float((uint32_t)(v >> 32)); }
+
 // Two signed bytes (byte lanes lo, lo+1 of w) -> exact f16x2 via 1024 + (q + 128) - 1152.
 __device__ __forceinline__ uint32_t s8x2_to_h2(uint32_t w, uint32_t sel) {
     uint32_t h = __byte_perm(w ^ 0x80808080u, 0x64646464u, sel);

@@ -122,16 +122,16 @@ __global__ void __launch_bounds__((kPfWarps + 1) * 32, 1)
     constexpr int MI = AM == A_INT8 ? 4 : 2;
     const int wm = warp >> 2, wn = warp & 3;
     const int g8 = lane >> 2, t4 = lane & 3;
+    const int rp = ((g8 & 1) << 2) | (g8 >> 1);  // tile row of MMA row g (a permutation of 0..7)
     long long g = 0;
     for (int t = blockIdx.x; t < p.ntiles; t += gridDim.x) {
         const int m0 = (t % p.n_mt) * BM, n0 = (t / p.n_mt) * kPfBN;
-        float acc[MI][4][4];
+        // acc[i][j][0] = (row g, cols 2t, 2t+1), acc[i][j][1] = (row g+8, ...): packed f32 pairs
+        unsigned long long acc[MI][4][2];
 #pragma unroll
         for (int i = 0; i < MI; ++i)
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) acc[i][j][e] = 0.0f;
+            for (int j = 0; j < 4; ++j) acc[i][j][0] = acc[i][j][1] = 0ull;
         for (int kc = 0; kc < p.kchunks; ++kc, ++g) {
             const int slot = (int)(g % S);
             const bool ok = mbar_wait(smem_u32(&bars[slot]), (uint32_t)((g / S) & 1), flags, p.err);
@@ -145,7 +145,7 @@ __global__ void __launch_bounds__((kPfWarps + 1) * 32, 1)
                 for (int b = 0; b < 8; ++b) {
                     // weight (B) fragments and scales of the warp's 4 n8 tiles
                     uint32_t bf[4][4];
-                    float dw[4][2];
+                    unsigned long long dw[4];  // (f(d_w) of col 2t, of col 2t+1)
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         const int nr = wn * 32 + 8 * j;
@@ -155,28 +155,29 @@ __global__ void __launch_bounds__((kPfWarps + 1) * 32, 1)
                         bf[j][1] = s8x2_to_h2(w0, SEL23);
                         bf[j][2] = s8x2_to_h2(w1, SEL01);
                         bf[j][3] = s8x2_to_h2(w1, SEL23);
-                        dw[j][0] = h2f(*reinterpret_cast<const uint16_t*>(W + (nr + 2 * t4) * kPfWRow + 34 * b));
-                        dw[j][1] = h2f(*reinterpret_cast<const uint16_t*>(W + (nr + 2 * t4 + 1) * kPfWRow + 34 * b));
+                        dw[j] = f2pack(h2f(*reinterpret_cast<const uint16_t*>(W + (nr + 2 * t4) * kPfWRow + 34 * b)),
+                                       h2f(*reinterpret_cast<const uint16_t*>(W + (nr + 2 * t4 + 1) * kPfWRow + 34 * b)));
                     }
                     // activation (A) fragments: 8 halves at K offset 32b + 8t of rows g, g+8
                     const int hk = b * 32 + 8 * t4;        // half index inside the 256-value chunk
                     const int box = (hk >> 6) * BM * 128;  // which 64-half box
 #pragma unroll
                     for (int i = 0; i < MI; ++i) {
-                        const int r0 = wm * (MI * 16) + 16 * i + g8, r1 = r0 + 8;
+                        // MMA row g holds tile row rperm(g): the rows a quarter-warp reads are 4 apart,
+                        // so their 128B-swizzled chunks do not share banks
+                        const int r0 = wm * (MI * 16) + 16 * i + rp, r1 = r0 + 8;
                         const uint4 x0 = ld128(A + box + swz128(r0, hk & 63));
                         const uint4 x1 = ld128(A + box + swz128(r1, hk & 63));
                         if (AM == A_INT8) {
                             const float da0 = SC[r0 * 8 + b], da1 = SC[r1 * 8 + b];
+                            const unsigned long long a0 = f2pack(da0, da0), a1 = f2pack(da1, da1);
 #pragma unroll
                             for (int j = 0; j < 4; ++j) {
                                 float d[4] = {0.f, 0.f, 0.f, 0.f};
                                 mma_f16(d, x0.x, x1.x, x0.y, x1.y, bf[j][0], bf[j][1]);
                                 mma_f16(d, x0.z, x1.z, x0.w, x1.w, bf[j][2], bf[j][3]);
-                                acc[i][j][0] = fmaf(d[0], da0 * dw[j][0], acc[i][j][0]);
-                                acc[i][j][1] = fmaf(d[1], da0 * dw[j][1], acc[i][j][1]);
-                                acc[i][j][2] = fmaf(d[2], da1 * dw[j][0], acc[i][j][2]);
-                                acc[i][j][3] = fmaf(d[3], da1 * dw[j][1], acc[i][j][3]);
+                                acc[i][j][0] = fma2(f2pack(d[0], d[1]), mul2(a0, dw[j]), acc[i][j][0]);
+                                acc[i][j][1] = fma2(f2pack(d[2], d[3]), mul2(a1, dw[j]), acc[i][j][1]);
                             }
                         } else {
                             const uint4 l0 = ld128(A2 + box + swz128(r0, hk & 63));
@@ -188,10 +189,8 @@ __global__ void __launch_bounds__((kPfWarps + 1) * 32, 1)
                                 mma_f16(d, l0.z, l1.z, l0.w, l1.w, bf[j][2], bf[j][3]);
                                 mma_f16(d, x0.x, x1.x, x0.y, x1.y, bf[j][0], bf[j][1]);
                                 mma_f16(d, x0.z, x1.z, x0.w, x1.w, bf[j][2], bf[j][3]);
-                                acc[i][j][0] = fmaf(d[0], dw[j][0], acc[i][j][0]);
-                                acc[i][j][1] = fmaf(d[1], dw[j][1], acc[i][j][1]);
-                                acc[i][j][2] = fmaf(d[2], dw[j][0], acc[i][j][2]);
-                                acc[i][j][3] = fmaf(d[3], dw[j][1], acc[i][j][3]);
+                                acc[i][j][0] = fma2(f2pack(d[0], d[1]), dw[j], acc[i][j][0]);
+                                acc[i][j][1] = fma2(f2pack(d[2], d[3]), dw[j], acc[i][j][1]);
                             }
                         }
                     }
@@ -204,19 +203,19 @@ __global__ void __launch_bounds__((kPfWarps + 1) * 32, 1)
         // store: thread owns (row g, cols 2t, 2t+1) and (row g+8, ...) of each m16 x n8 tile
 #pragma unroll
         for (int i = 0; i < MI; ++i) {
-            const int ra = m0 + wm * (MI * 16) + 16 * i + g8, rb = ra + 8;
+            const int ra = m0 + wm * (MI * 16) + 16 * i + rp, rb = ra + 8;
             const float sa = (AM == A_F32 && ra < p.M) ? __ldg(p.rs + ra) : 1.0f;
             const float sb = (AM == A_F32 && rb < p.M) ? __ldg(p.rs + rb) : 1.0f;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const int c = n0 + wn * 32 + 8 * j + 2 * t4;
                 if (ra < p.M) {
-                    if (c < p.N) p.y[(long long)ra * p.N + c] = acc[i][j][0] * sa;
-                    if (c + 1 < p.N) p.y[(long long)ra * p.N + c + 1] = acc[i][j][1] * sa;
+                    if (c < p.N) p.y[(long long)ra * p.N + c] = f2lo(acc[i][j][0]) * sa;
+                    if (c + 1 < p.N) p.y[(long long)ra * p.N + c + 1] = f2hi(acc[i][j][0]) * sa;
                 }
                 if (rb < p.M) {
-                    if (c < p.N) p.y[(long long)rb * p.N + c] = acc[i][j][2] * sb;
-                    if (c + 1 < p.N) p.y[(long long)rb * p.N + c + 1] = acc[i][j][3] * sb;
+                    if (c < p.N) p.y[(long long)rb * p.N + c] = f2lo(acc[i][j][1]) * sb;
+                    if (c + 1 < p.N) p.y[(long long)rb * p.N + c + 1] = f2hi(acc[i][j][1]) * sb;
                 }
             }
         }
