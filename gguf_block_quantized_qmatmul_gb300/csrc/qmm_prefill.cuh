@@ -20,7 +20,8 @@
 // activation planes; 8 consumer warps convert the weight codes to f16 in
 // registers (exact), run the MMAs of one 32-value block with a zero
 // accumulator and fold the block sum into the f32 result with the block's
-// scales (f(d_w) f(d_a) or f(d_w)).
+// scales (f(d_w) f(d_a) or f(d_w)).  (Packed f32x2 arithmetic and a 2x unroll
+// of the block loop were measured slower on this kernel and are not used.)
 #pragma once
 
 #include <cuda.h>
@@ -170,14 +171,14 @@ __global__ void __launch_bounds__((kPfWarps + 1) * 32, 1)
                         const uint4 x1 = ld128(A + box + swz128(r1, hk & 63));
                         if (AM == A_INT8) {
                             const float da0 = SC[r0 * 8 + b], da1 = SC[r1 * 8 + b];
-                            const unsigned long long a0 = f2pack(da0, da0), a1 = f2pack(da1, da1);
 #pragma unroll
                             for (int j = 0; j < 4; ++j) {
                                 float d[4] = {0.f, 0.f, 0.f, 0.f};
                                 mma_f16(d, x0.x, x1.x, x0.y, x1.y, bf[j][0], bf[j][1]);
                                 mma_f16(d, x0.z, x1.z, x0.w, x1.w, bf[j][2], bf[j][3]);
-                                acc[i][j][0] = fma2(f2pack(d[0], d[1]), mul2(a0, dw[j]), acc[i][j][0]);
-                                acc[i][j][1] = fma2(f2pack(d[2], d[3]), mul2(a1, dw[j]), acc[i][j][1]);
+                                const float w0 = f2lo(dw[j]), w1 = f2hi(dw[j]);
+                                acc[i][j][0] = f2pack(fmaf(d[0], da0 * w0, f2lo(acc[i][j][0])), fmaf(d[1], da0 * w1, f2hi(acc[i][j][0])));
+                                acc[i][j][1] = f2pack(fmaf(d[2], da1 * w0, f2lo(acc[i][j][1])), fmaf(d[3], da1 * w1, f2hi(acc[i][j][1])));
                             }
                         } else {
                             const uint4 l0 = ld128(A2 + box + swz128(r0, hk & 63));
@@ -189,8 +190,9 @@ __global__ void __launch_bounds__((kPfWarps + 1) * 32, 1)
                                 mma_f16(d, l0.z, l1.z, l0.w, l1.w, bf[j][2], bf[j][3]);
                                 mma_f16(d, x0.x, x1.x, x0.y, x1.y, bf[j][0], bf[j][1]);
                                 mma_f16(d, x0.z, x1.z, x0.w, x1.w, bf[j][2], bf[j][3]);
-                                acc[i][j][0] = fma2(f2pack(d[0], d[1]), dw[j], acc[i][j][0]);
-                                acc[i][j][1] = fma2(f2pack(d[2], d[3]), dw[j], acc[i][j][1]);
+                                const float w0 = f2lo(dw[j]), w1 = f2hi(dw[j]);
+                                acc[i][j][0] = f2pack(fmaf(d[0], w0, f2lo(acc[i][j][0])), fmaf(d[1], w1, f2hi(acc[i][j][0])));
+                                acc[i][j][1] = f2pack(fmaf(d[2], w0, f2lo(acc[i][j][1])), fmaf(d[3], w1, f2hi(acc[i][j][1])));
                             }
                         }
                     }
