@@ -77,7 +77,7 @@ qmm_status stream_call(qmm_type wtype, int am, int epi, const void* wq, const fl
         const cudaError_t e = wt == T_Q8_0 ? launch_gemv_q8_0(epi, gp, smem, s) : launch_gemv_q4_k(epi, gp, smem, s);
         return e == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
     }
-    if (M <= kDecodeMaxM && plan_dmma(wt, am, M, N, K, sms, smem, dp)) {  // decode on 8-row tensor-core tiles
+    if (M <= kDecodeMaxM && plan_dmma(wt, am, M, N, K, sms, smem, dp)) {  // decode on 16-row tensor-core tiles
         dp.p.wq = static_cast<const uint8_t*>(wq);
         dp.p.x = x;
         dp.p.y = y;

@@ -184,6 +184,14 @@ __device__ __forceinline__ void mma_f16(float d[4], uint32_t a0, uint32_t a1, ui
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// D += A(16x8 f16) * B(8x8 f16), f32 accumulate
+__device__ __forceinline__ void mma_f16_k8(float d[4], uint32_t a0, uint32_t a1, uint32_t b0) {
+    asm(
+        "mma.sync.aligned.m16n8k8.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5}, {%6}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(b0));
+}
+
 // Packed f32x2 arithmetic (two lanes per instruction).
 __device__ __forceinline__ unsigned long long f2pack(float lo, float hi) {
     return (unsigned long long)__float_as_uint(lo) | ((unsigned long long)__float_as_uint(hi) << 32);
@@ -200,6 +208,30 @@ __device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigne
 }
 __device__ __forceinline__ float f2lo(unsigned long long v) { return __uint_as_float((uint32_t)v); }
 __device__ __forceinline__ float f2hi(unsigned long long v) { return __uint_as_float((uint32_t)(v >> 32)); }
+
+// The 16 six-bit factors of a Q4_K header as packed bytes: sc0..3, sc4..7,
+// m0..3, m4..7 (header words W0, W1, W2 = scales bytes 0-3, 4-7, 8-11).
+__device__ __forceinline__ void q4k_unpack4(uint32_t W0, uint32_t W1, uint32_t W2, uint32_t& sc03, uint32_t& sc47,
+                                            uint32_t& mn03, uint32_t& mn47) {
+    sc03 = W0 & 0x3F3F3F3Fu;
+    mn03 = W1 & 0x3F3F3F3Fu;
+    sc47 = (W2 & 0x0F0F0F0Fu) | ((W0 >> 2) & 0x30303030u);
+    mn47 = ((W2 >> 4) & 0x0F0F0F0Fu) | ((W1 >> 2) & 0x30303030u);
+}
+// byte j (0..3) of w as f16x2 (v, v), exact: (1024 + v) - 1024
+__device__ __forceinline__ uint32_t byte_h2(uint32_t w, int j) {
+    const uint32_t sel = (uint32_t)(j | 0x40 | (j << 8) | 0x4000);  // bytes j, 0x64, j, 0x64
+    uint32_t h = __byte_perm(w, 0x64646464u, sel);
+    __half2 r = __hsub2(*reinterpret_cast<__half2*>(&h), __half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400)));
+    return *reinterpret_cast<uint32_t*>(&r);
+}
+// two nibble codes (bytes lo, lo+1 of w, values 0..15) times the f16x2 factor
+// sc2 = (sc, sc), exact: (1024 + n) * sc - 1024 * sc with one rounding (n sc <= 945)
+__device__ __forceinline__ uint32_t u4x2_scaled(uint32_t w, uint32_t sel, uint32_t sc2, uint32_t negsc2) {
+    uint32_t h = __byte_perm(w, 0x64646464u, sel);
+    __half2 r = __hfma2(*reinterpret_cast<__half2*>(&h), *reinterpret_cast<__half2*>(&sc2), *reinterpret_cast<__half2*>(&negsc2));
+    return *reinterpret_cast<uint32_t*>(&r);
+}
 
 // Two signed bytes (byte lanes lo, lo+1 of w) -> exact f16x2 via 1024 + (q + 128) - 1152.
 __device__ __forceinline__ uint32_t s8x2_to_h2(uint32_t w, uint32_t sel) {

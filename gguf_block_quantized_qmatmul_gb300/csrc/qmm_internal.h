@@ -23,7 +23,7 @@ cudaError_t launch_prefill(int am, const PrefillPlan& plan, const void* wq, cons
 
 // largest activation batch served by the per-thread dp4a GEMV (int8_act);
 // larger decode batches (and every f32_act decode batch up to 8) use the
-// 8-row-tile tensor-core kernel
+// 16-row-tile tensor-core kernel
 constexpr int kGemvMaxM = 4;
 constexpr int kDecodeMaxM = 8;
 
