@@ -77,16 +77,20 @@ qmm_status stream_call(qmm_type wtype, int am, int epi, const void* wq, const fl
         const cudaError_t e = wt == T_Q8_0 ? launch_gemv_q8_0(epi, gp, smem, s) : launch_gemv_q4_k(epi, gp, smem, s);
         return e == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
     }
-    if (M <= kDecodeMaxM && plan_dmma(wt, am, M, N, K, sms, smem, dp)) {  // decode on 16-row tensor-core tiles
+    if (M <= kDecodeMaxM && plan_dmma(wt, am, M, N, K, sms, smem, dp, epi == E_Y)) {  // decode on 16-row tensor-core tiles
         dp.p.wq = static_cast<const uint8_t*>(wq);
         dp.p.x = x;
         dp.p.y = y;
         dp.p.sums = sums;
         dp.p.err = err;
         const bool split = epi == E_Y && dp.p.kslices > 1;
-        if (split) {
+        if (split || dp.ext_bytes) {
             if (!ws || ws_bytes < dp.workspace) return QMM_ERR_WORKSPACE;
-            dp.p.partial = static_cast<float*>(ws);
+            if (split) dp.p.partial = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + dp.ext_bytes);
+        }
+        if (dp.ext_bytes) {  // activations prepared once, fetched by every CTA
+            dp.p.ext = static_cast<const uint8_t*>(ws);
+            if (launch_dmma_prep(wt, am, dp, ws, s) != cudaSuccess) return QMM_ERR_CUDA;
         }
         if (launch_dmma(wt, am, epi, dp, smem, s) != cudaSuccess) return QMM_ERR_CUDA;
         if (split && launch_splitk_reduce(dp.p.partial, M * N, dp.p.kslices, y, s) != cudaSuccess) return QMM_ERR_CUDA;

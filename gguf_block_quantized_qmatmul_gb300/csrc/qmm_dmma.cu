@@ -11,8 +11,23 @@ cudaError_t go(const DmmaPlan& pl, int smem_max, cudaStream_t s) {
     auto* k = qmm_dmma_kernel<WT, AM, NB, EPI>;
     cudaError_t e = ensure_smem(k, smem_max, g_smem_done[WT == T_Q8_0 ? 0 : 1][AM][NB - 1][EPI]);
     if (e != cudaSuccess) return e;
-    k<<<pl.grid, (kDmmaWarps + 1) * 32, pl.smem, s>>>(pl.p);
-    return cudaGetLastError();
+    if (!pl.p.ext) {
+        k<<<pl.grid, kDmmaThreads, pl.smem, s>>>(pl.p);
+        return cudaGetLastError();
+    }
+    // after the preparing kernel: programmatic dependent launch, so that the
+    // weight stream starts while the activations are being prepared
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)pl.grid);
+    cfg.blockDim = dim3(kDmmaThreads);
+    cfg.dynamicSmemBytes = pl.smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k, pl.p);
 }
 
 template <int WT>
@@ -23,7 +38,23 @@ cudaError_t go_type(int am, int epi, const DmmaPlan& pl, int smem_max, cudaStrea
     }
     return epi == E_Y ? go<WT, A_INT8, 1, E_Y>(pl, smem_max, s) : go<WT, A_INT8, 1, E_SUMS>(pl, smem_max, s);
 }
+template <int WT, int AM>
+cudaError_t prep(const DmmaPlan& pl, void* ext, cudaStream_t s) {
+    const DmmaParams& p = pl.p;
+    long long blocks;
+    if (AM == A_F32) blocks = p.M;                                            // a block per row
+    else if (WT == T_Q8_0) blocks = ((long long)p.M * p.units + kPrepThreads - 1) / kPrepThreads;  // a thread per 32-block
+    else blocks = ((long long)p.M * p.units + kPrepThreads / 32 - 1) / (kPrepThreads / 32);       // a warp per super-block
+    if (blocks > 1024) blocks = 1024;
+    dmma_prep_kernel<WT, AM><<<(unsigned)blocks, kPrepThreads, 0, s>>>(p, static_cast<uint8_t*>(ext));
+    return cudaGetLastError();
+}
 }  // namespace
+
+cudaError_t launch_dmma_prep(int wt, int am, const DmmaPlan& pl, void* ext, cudaStream_t s) {
+    if (wt == T_Q8_0) return am == A_F32 ? prep<T_Q8_0, A_F32>(pl, ext, s) : prep<T_Q8_0, A_INT8>(pl, ext, s);
+    return am == A_F32 ? prep<T_Q4_K, A_F32>(pl, ext, s) : prep<T_Q4_K, A_INT8>(pl, ext, s);
+}
 
 cudaError_t launch_dmma(int wt, int am, int epi, const DmmaPlan& pl, int smem_max, cudaStream_t s) {
     return wt == T_Q8_0 ? go_type<T_Q8_0>(am, epi, pl, smem_max, s) : go_type<T_Q4_K>(am, epi, pl, smem_max, s);

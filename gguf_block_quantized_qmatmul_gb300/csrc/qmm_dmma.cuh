@@ -7,29 +7,35 @@
 // weights dequantized in-kernel).
 //
 // The MMA's A operand holds 16 weight rows, its B operand the activations:
-//   int8_act: B column c = activation row c (M <= 8); mma.m16n8k32.s8 takes
-//     the raw Q8_0 codes, or the Q4_K nibbles (0..15), as A with no conversion.
-//     Q8_0: y += f(d_w) f(d_a) isum per block.  Q4_K: S_sc accumulates
-//     sc_j * isum_j exactly in int32; S_m = sum_j m_j bsum_j comes from one
+//   int8_act: B column c = activation row c (M <= 8); mma.m16n8k32 takes the
+//     raw Q8_0 codes, or the Q4_K nibbles (low as 0..15, high as 16 n), as A
+//     with no conversion.  Q8_0: y += f(d_w) f(d_a) isum per block.  Q4_K: S_sc
+//     accumulates sc_j * isum_j exactly in int32; S_m = sum_j m_j bsum_j is one
 //     f16 MMA per super-block over the 16 sums of 16 activation codes (every
 //     product and partial sum is an integer below 2^24, so it is exact).
-//   f32_act: every activation row is scaled by a power of two and split into
-//     two exact f16 pieces, x 2^s = hi + lo; B column 2r holds hi of row r and
+//   f32_act: each weight unit (Q8_0 block, Q4_K super-block) of each
+//     activation row is scaled by its own power of two 2^s and split into two
+//     exact f16 pieces, x 2^s = hi + lo; B column 2r holds hi of row r and
 //     column 2r+1 its lo (a second column set serves rows 4..7).  Weight codes
-//     become exact f16: Q8_0 q; Q4_K sc_j * q (<= 945) with the 6-bit factor
-//     folded into the conversion, so the 16 MMAs of a super-block chain in
-//     one accumulator and are scaled once by f(d).  The min term
-//     f(dmin) sum_j m_j X_j (X_j = sum of the sub-block's x) is one
-//     mma.m16n8k8 per super-block with X_j / 32 in two f16 pieces.
+//     become exact f16: Q8_0 q; Q4_K sc_j * q (<= 945), the 6-bit factor
+//     folded into the conversion, so the 16 MMAs of a super-block chain in one
+//     accumulator.  The min term f(dmin) sum_j m_j X_j (X_j = the sub-block's
+//     sum of x 2^s) is one mma.m16n8k8 per super-block with X_j / 32 in two f16
+//     pieces.  2^-s is applied with the unit's weight scale.
 // The MMA k order is a fixed permutation of each 32-value group: thread t4
-// of a quad owns values 4t4..4t4+3 and 16+4t4..16+4t4+3 of the group, read
-// as two 4-byte words; the f32 activation planes are stored in the matching
+// of a quad owns values 4t4..4t4+3 and 16+4t4..16+4t4+3 of the group, read as
+// two 4-byte words; the f32 activation planes are stored in the matching
 // order.  Weight tiles stream through a shared-memory ring as one bulk copy
-// per row and K chunk (~4.3 KB), into rows at a pitch of 16 mod 128 bytes so
-// that the word loads of 8 rows x 4 threads hit 32 distinct banks.  K is
-// split across CTAs only when the activation rows of the whole K range do not
-// fit in shared memory; the slices' partial sums then go to the workspace and
-// a second small kernel adds them in slice order.
+// per row and K chunk (~4 KB: one SM's bulk-copy engine pays a fixed cost per
+// contiguous segment), into rows at a pitch of 16 mod 128 bytes so that the
+// word loads of 8 rows x 4 threads hit 32 distinct banks.
+// Activations are prepared in the layout the MMAs read: inside the kernel
+// for small weight matrices (one launch), or once per call by
+// dmma_prep_kernel for large ones, whose output every CTA fetches with a few
+// bulk copies after its first weight stages are in flight (programmatic
+// dependent launch).  K is split across CTAs only when the activation rows of
+// the whole K range do not fit in shared memory; the slices' partial sums then
+// go to the workspace and a second small kernel adds them in slice order.
 #pragma once
 
 #include "qmm_device.cuh"
@@ -57,8 +63,14 @@ struct DmmaParams {
     int stages;
     int stage_bytes;
     int row_pitch;    // bytes between rows in a stage with one copy per row (0: one contiguous copy)
-    int off_flags, off_act, off_scale, off_aux, off_rs, off_red, off_stage;
+    int off_flags, off_act, off_scale, off_aux, off_red, off_stage;
     int act_pitch;    // int8: bytes per activation row; f32: halves per (row, piece) plane
+    int sstride;      // activation scales per unit: 8 (int8), 4 * column sets (f32)
+    // Activations prepared once by dmma_prep_kernel (null: every CTA prepares
+    // its own slice).  Byte offsets in ext: codes (int8 [M][K]) or f16 planes
+    // ([2M][K] in MMA k order), scales [unit][sstride], aux [unit][...].
+    const uint8_t* ext;
+    long long ext_codes, ext_scale, ext_aux;
 };
 
 // position p (0..31) of a 32-value group in the MMA k order -> value index
@@ -67,190 +79,246 @@ __host__ __device__ constexpr int dmma_kperm(int p) {
 }
 
 // ---------------------------------------------------------------------------
-// activation preparation (consumer warps, once per CTA)
+// activation preparation: per-unit work items, shared by the in-kernel path
+// (shared memory, one K slice) and dmma_prep_kernel (global memory, all K)
 // ---------------------------------------------------------------------------
-template <int WT, int AM>
-__device__ __forceinline__ void dmma_prepare(const DmmaParams& p, uint8_t* smem, int k0, int klen, int tid) {
-    constexpr int NTH = kDmmaWarps * 32;
-    const int su = p.slice_units;
-    if (AM == A_INT8 && WT == T_Q8_0) {
-        uint8_t* codes = smem + p.off_act;
-        float* da = reinterpret_cast<float*>(smem + p.off_scale);  // [unit][8 rows]
-        for (int idx = tid; idx < p.M * su; idx += NTH) {
-            const int r = idx / su, b = idx - r * su;
-            uint32_t c[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-            float s = 0.0f;
-            if (b * 32 < klen) {
-                float d;
-                quant_q8_0_32(p.x + (long long)r * p.K + k0 + b * 32, c, d);
-                s = h2f(f2h(d));
-            }
-            uint4* d0 = reinterpret_cast<uint4*>(codes + r * p.act_pitch + b * 32);
-            d0[0] = make_uint4(c[0], c[1], c[2], c[3]);
-            d0[1] = make_uint4(c[4], c[5], c[6], c[7]);
-            da[b * 8 + r] = s;
-        }
-    } else if (AM == A_INT8 && WT == T_Q4_K) {
-        uint8_t* codes = smem + p.off_act;
-        float* da = reinterpret_cast<float*>(smem + p.off_scale);       // [super-block][8 rows]
-        uint32_t* bs = reinterpret_cast<uint32_t*>(smem + p.off_aux);   // [super-block][pair][8 rows] f16x2
-        for (int idx = tid; idx < p.M * su; idx += NTH) {
-            const int r = idx / su, sb = idx - r * su;
-            const bool live = sb * 256 < klen;
-            const float* src = p.x + (long long)r * p.K + k0 + sb * 256;
-            float d = 0.0f, id = 0.0f;
-            if (live) q8_scale(q8k_amax(src), d, id);
-            for (int q = 0; q < 8; ++q) {  // 32 values: two sums of 16
-                uint32_t w[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-                int s0 = 0, s1 = 0;
-                if (live) {
+struct ActDst {
+    uint8_t* act;     // int8 codes [M][pitch] bytes, or f16 planes [2M][pitch] halves
+    long long pitch;
+    float* scale;     // [unit][sstride]
+    int sstride;
+    uint8_t* aux;     // int8 Q4_K: [unit][8 pairs][8 rows] f16x2 sums of 16 codes; f32 Q4_K: [unit][16 planes][8] X halves
+};
+
+// int8 Q8_0, one thread: the 32-block b of row r (src: its 32 floats)
+__device__ __forceinline__ void prep_i8_q8_0(const float* src, int r, int b, const ActDst& o) {
+    uint32_t c[8];
+    float d;
+    quant_q8_0_32(src, c, d);
+    uint4* dst = reinterpret_cast<uint4*>(o.act + r * o.pitch + b * 32);
+    dst[0] = make_uint4(c[0], c[1], c[2], c[3]);
+    dst[1] = make_uint4(c[4], c[5], c[6], c[7]);
+    o.scale[b * 8 + r] = h2f(f2h(d));
+}
+
+// int8 Q8K, one warp: super-block sb of row r (src: its 256 floats); lane l
+// quantizes values 8l..8l+7
+__device__ __forceinline__ void prep_i8_q8k(const float* src, int r, int sb, int lane, const ActDst& o) {
+    const float4 v0 = __ldg(reinterpret_cast<const float4*>(src) + 2 * lane);
+    const float4 v1 = __ldg(reinterpret_cast<const float4*>(src) + 2 * lane + 1);
+    float amax = fmaxf(fmaxf(fmaxf(fabsf(v0.x), fabsf(v0.y)), fmaxf(fabsf(v0.z), fabsf(v0.w))),
+                       fmaxf(fmaxf(fabsf(v1.x), fabsf(v1.y)), fmaxf(fabsf(v1.z), fabsf(v1.w))));
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const float4 v = __ldg(reinterpret_cast<const float4*>(src + 32 * q) + i);
-                        w[i] = pack4(q8_code(v.x, id), q8_code(v.y, id), q8_code(v.z, id), q8_code(v.w, id));
-                        if (i < 4) s0 += bsum4(w[i]);
-                        else s1 += bsum4(w[i]);
-                    }
-                }
-                uint4* d0 = reinterpret_cast<uint4*>(codes + r * p.act_pitch + sb * 256 + 32 * q);
-                d0[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                d0[1] = make_uint4(w[4], w[5], w[6], w[7]);
-                // |sum of 16 codes| <= 2032: exact in f16
-                bs[(sb * 8 + q) * 8 + r] = f2h((float)s0) | (f2h((float)s1) << 16);
-            }
-            da[sb * 8 + r] = d;
+    for (int m = 16; m; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
+    float d, id;
+    q8_scale(amax, d, id);
+    const uint32_t w0 = pack4(q8_code(v0.x, id), q8_code(v0.y, id), q8_code(v0.z, id), q8_code(v0.w, id));
+    const uint32_t w1 = pack4(q8_code(v1.x, id), q8_code(v1.y, id), q8_code(v1.z, id), q8_code(v1.w, id));
+    *reinterpret_cast<uint2*>(o.act + r * o.pitch + sb * 256 + 8 * lane) = make_uint2(w0, w1);
+    const int s8 = bsum4(w0) + bsum4(w1);
+    const int s16 = s8 + __shfl_xor_sync(0xffffffffu, s8, 1);   // sum of 16 codes (lanes 2i, 2i+1)
+    const int s16n = __shfl_down_sync(0xffffffffu, s16, 2);      // the next sum of 16
+    // |sum of 16 codes| <= 2032: exact in f16
+    if ((lane & 3) == 0)
+        reinterpret_cast<uint32_t*>(o.aux)[(sb * 8 + (lane >> 2)) * 8 + r] = f2h((float)s16) | (f2h((float)s16n) << 16);
+    if (lane == 0) o.scale[sb * 8 + r] = d;
+}
+
+// f32: one lane's 8 values of a 32-group (positions 8t..8t+7 of the MMA k
+// order: values 4t..4t+3 and 16+4t..16+4t+3), scaled by 2^s and split in two
+// f16 pieces; returns the sum of the 8 scaled values
+__device__ __forceinline__ float prep_f32_lane(const float4 a, const float4 b, float scale, __half* hi, __half* lo) {
+    const float v[8] = {__fmul_rn(a.x, scale), __fmul_rn(a.z, scale), __fmul_rn(a.y, scale), __fmul_rn(a.w, scale),
+                        __fmul_rn(b.x, scale), __fmul_rn(b.z, scale), __fmul_rn(b.y, scale), __fmul_rn(b.w, scale)};
+    uint32_t hw[4], lw[4];
+    float sum = 0.0f;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint32_t hb[2], lb[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const float f = v[2 * q + e];
+            const __half h = __float2half_rn(f);
+            hb[e] = __half_as_ushort(h);
+            lb[e] = __half_as_ushort(__float2half_rn(__fsub_rn(f, __half2float(h))));
+            sum = __fadd_rn(sum, f);
+        }
+        hw[q] = hb[0] | (hb[1] << 16);
+        lw[q] = lb[0] | (lb[1] << 16);
+    }
+    *reinterpret_cast<uint4*>(hi) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+    *reinterpret_cast<uint4*>(lo) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+    return sum;
+}
+
+// s of the power-of-two scale 2^s for a unit with largest magnitude amax:
+// amax 2^s lies in [2^14, 2^15)
+__device__ __forceinline__ int unit_shift(float amax) {
+    if (!(amax > 0.0f)) return 0;
+    const int e = (int)((__float_as_uint(amax) >> 23) & 0xff) - 127;
+    const int s = 14 - e;
+    return s > 100 ? 100 : (s < -100 ? -100 : s);
+}
+
+__device__ __forceinline__ float lane_amax(const float4 a, const float4 b) {
+    return fmaxf(fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(a.z), fabsf(a.w))),
+                 fmaxf(fmaxf(fabsf(b.x), fabsf(b.y)), fmaxf(fabsf(b.z), fabsf(b.w))));
+}
+
+// f32 Q8_0, one warp: the 8 blocks g0..g0+7 of row r (src: row start, block
+// index relative to it); lanes 4i..4i+3 take block g0+i
+__device__ __forceinline__ void prep_f32_q8_0(const float* src, int r, int g0, int nblocks, int lane, const ActDst& o) {
+    const int b = g0 + (lane >> 2), t = lane & 3;
+    const bool live = b < nblocks;
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f), c = a;
+    if (live) {
+        a = __ldg(reinterpret_cast<const float4*>(src + b * 32 + 4 * t));
+        c = __ldg(reinterpret_cast<const float4*>(src + b * 32 + 16 + 4 * t));
+    }
+    float amax = lane_amax(a, c);
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    const int s = unit_shift(amax);
+    if (!live) return;
+    __half* pl = reinterpret_cast<__half*>(o.act);
+    prep_f32_lane(a, c, ldexpf(1.0f, s), pl + (2 * r) * o.pitch + b * 32 + 8 * t, pl + (2 * r + 1) * o.pitch + b * 32 + 8 * t);
+    if (t == 0) o.scale[b * o.sstride + r] = ldexpf(1.0f, -s);
+}
+
+// f32 Q4_K, one warp: super-block sb of row r (src: its 256 floats); lanes
+// 4c..4c+3 take 32-group c (sub-block c)
+__device__ __forceinline__ void prep_f32_q4_k(const float* src, int r, int sb, int lane, const ActDst& o) {
+    const int c = lane >> 2, t = lane & 3;
+    const float4 a = __ldg(reinterpret_cast<const float4*>(src + c * 32 + 4 * t));
+    const float4 b = __ldg(reinterpret_cast<const float4*>(src + c * 32 + 16 + 4 * t));
+    float amax = lane_amax(a, b);
+#pragma unroll
+    for (int m = 16; m; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
+    const int s = unit_shift(amax);
+    __half* pl = reinterpret_cast<__half*>(o.act);
+    const long long k = (long long)sb * 256 + c * 32 + 8 * t;
+    float sum = prep_f32_lane(a, b, ldexpf(1.0f, s), pl + (2 * r) * o.pitch + k, pl + (2 * r + 1) * o.pitch + k);
+    sum = __fadd_rn(sum, __shfl_xor_sync(0xffffffffu, sum, 1));
+    sum = __fadd_rn(sum, __shfl_xor_sync(0xffffffffu, sum, 2));
+    if (t == 0) {
+        // X_c / 32 (|.| < 2^15) in two f16 pieces
+        const float xq = __fmul_rn(sum, 0.03125f);
+        const __half h = __float2half_rn(xq);
+        const __half l = __float2half_rn(__fsub_rn(xq, __half2float(h)));
+        uint16_t* xs = reinterpret_cast<uint16_t*>(o.aux);
+        xs[(sb * 16 + 2 * r) * 8 + c] = __half_as_ushort(h);
+        xs[(sb * 16 + 2 * r + 1) * 8 + c] = __half_as_ushort(l);
+    }
+    if (lane == 0) o.scale[sb * o.sstride + r] = ldexpf(1.0f, -s);
+}
+
+// Items are per thread for int8 Q8_0 and per warp otherwise.
+template <int WT, int AM>
+__host__ __device__ constexpr bool prep_per_warp() { return !(AM == A_INT8 && WT == T_Q8_0); }
+
+// The work items of rows 0..M-1 over units u0..u0+nu-1 of x, written at unit
+// index 0 of `o`; item indices first, first+step, ...
+template <int WT, int AM>
+__device__ __forceinline__ void prep_items(const float* x, int M, int K, int u0, int nu, const ActDst& o,
+                                           long long first, long long step, int lane) {
+    constexpr int UV = Unit<WT>::vals;
+    const long long k0 = (long long)u0 * UV;
+    if (AM == A_INT8 && WT == T_Q8_0) {
+        for (long long i = first; i < (long long)M * nu; i += step) {
+            const int r = (int)(i / nu), b = (int)(i - (long long)r * nu);
+            prep_i8_q8_0(x + (long long)r * K + k0 + b * 32, r, b, o);
+        }
+    } else if (AM == A_INT8) {
+        for (long long i = first; i < (long long)M * nu; i += step) {
+            const int r = (int)(i / nu), sb = (int)(i - (long long)r * nu);
+            prep_i8_q8k(x + (long long)r * K + k0 + sb * 256, r, sb, lane, o);
+        }
+    } else if (WT == T_Q8_0) {
+        const int ng = (nu + 7) / 8;
+        for (long long i = first; i < (long long)M * ng; i += step) {
+            const int r = (int)(i / ng), gi = (int)(i - (long long)r * ng);
+            prep_f32_q8_0(x + (long long)r * K + k0, r, 8 * gi, nu, lane, o);
         }
     } else {
-        // f32_act: per-row power-of-two scale; planes 2r (hi) and 2r+1 (lo) in MMA k order
-        __half* pl = reinterpret_cast<__half*>(smem + p.off_act);
-        float* rs = reinterpret_cast<float*>(smem + p.off_rs);               // [8][2]: 2^s, 2^-s
-        uint16_t* xs = reinterpret_cast<uint16_t*>(smem + p.off_aux);        // Q4_K: [sb][16 planes][8 sub-blocks]
-        const int warp = tid >> 5, lane = tid & 31;
-        if (warp < p.M) {
-            const int r = warp;
-            float amax = 0.0f;
-            const float4* src = reinterpret_cast<const float4*>(p.x + (long long)r * p.K + k0);
-            for (int i = lane; i < klen / 4; i += 32) {
-                const float4 v = __ldg(src + i);
-                amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
-            }
-#pragma unroll
-            for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-            if (lane == 0) {
-                int s = 0;
-                if (amax > 0.0f) {
-                    const int e = (int)((__float_as_uint(amax) >> 23) & 0xff) - 127;
-                    s = 14 - e;
-                    s = s > 100 ? 100 : (s < -100 ? -100 : s);
-                }
-                rs[2 * r] = ldexpf(1.0f, s);
-                rs[2 * r + 1] = ldexpf(1.0f, -s);
-            }
-        }
-        consumer_sync<kDmmaWarps>();
-        const int nch = su * Unit<WT>::vals / 32;
-        for (int idx = tid; idx < p.M * nch; idx += NTH) {
-            const int r = idx / nch, c = idx - r * nch;
-            float v[32];
-            float sum = 0.0f;
-            if (c * 32 < klen) {
-                const float scale = rs[2 * r];
-                const float4* src = reinterpret_cast<const float4*>(p.x + (long long)r * p.K + k0 + c * 32);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float4 v4 = __ldg(src + i);
-                    v[4 * i] = __fmul_rn(v4.x, scale);
-                    v[4 * i + 1] = __fmul_rn(v4.y, scale);
-                    v[4 * i + 2] = __fmul_rn(v4.z, scale);
-                    v[4 * i + 3] = __fmul_rn(v4.w, scale);
-                }
-#pragma unroll
-                for (int i = 0; i < 32; ++i) sum = __fadd_rn(sum, v[i]);
-            } else {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] = 0.0f;
-            }
-            uint32_t hw[16], lw[16];
-#pragma unroll
-            for (int q = 0; q < 16; ++q) {
-                uint32_t hb[2], lb[2];
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const float f = v[dmma_kperm(2 * q + e)];
-                    const __half h = __float2half_rn(f);
-                    hb[e] = __half_as_ushort(h);
-                    lb[e] = __half_as_ushort(__float2half_rn(__fsub_rn(f, __half2float(h))));
-                }
-                hw[q] = hb[0] | (hb[1] << 16);
-                lw[q] = lb[0] | (lb[1] << 16);
-            }
-            uint4* dh = reinterpret_cast<uint4*>(pl + (long long)(2 * r) * p.act_pitch + c * 32);
-            uint4* dl = reinterpret_cast<uint4*>(pl + (long long)(2 * r + 1) * p.act_pitch + c * 32);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                dh[i] = make_uint4(hw[4 * i], hw[4 * i + 1], hw[4 * i + 2], hw[4 * i + 3]);
-                dl[i] = make_uint4(lw[4 * i], lw[4 * i + 1], lw[4 * i + 2], lw[4 * i + 3]);
-            }
-            if (WT == T_Q4_K) {
-                // X_j / 32 (|.| < 2^15) in two f16 pieces
-                const float xq = __fmul_rn(sum, 0.03125f);
-                const __half h = __float2half_rn(xq);
-                const __half l = __float2half_rn(__fsub_rn(xq, __half2float(h)));
-                const int sb = c >> 3, j = c & 7;
-                xs[(sb * 16 + 2 * r) * 8 + j] = __half_as_ushort(h);
-                xs[(sb * 16 + 2 * r + 1) * 8 + j] = __half_as_ushort(l);
-            }
+        for (long long i = first; i < (long long)M * nu; i += step) {
+            const int r = (int)(i / nu), sb = (int)(i - (long long)r * nu);
+            prep_f32_q4_k(x + (long long)r * K + k0 + sb * 256, r, sb, lane, o);
         }
     }
+}
+
+constexpr int kPrepThreads = 1024;
+
+// Once per call, for large weight matrices: the whole K range into ext.
+template <int WT, int AM>
+__global__ void __launch_bounds__(kPrepThreads) dmma_prep_kernel(const DmmaParams p, uint8_t* ext) {
+    grid_dep_launch();  // the decode grid may start streaming weights now
+    ActDst o;
+    o.act = ext + p.ext_codes;
+    o.pitch = p.K;
+    o.scale = reinterpret_cast<float*>(ext + p.ext_scale);
+    o.sstride = p.sstride;
+    o.aux = ext + p.ext_aux;
+    const long long tid = (long long)blockIdx.x * kPrepThreads + threadIdx.x;
+    if (prep_per_warp<WT, AM>())
+        prep_items<WT, AM>(p.x, p.M, p.K, 0, p.units, o, tid >> 5, (long long)gridDim.x * (kPrepThreads / 32), threadIdx.x & 31);
+    else
+        prep_items<WT, AM>(p.x, p.M, p.K, 0, p.units, o, tid, (long long)gridDim.x * kPrepThreads, threadIdx.x & 31);
 }
 
 // ---------------------------------------------------------------------------
 // weight-side helpers
 // ---------------------------------------------------------------------------
 
-// The thread's code words of a Q8_0 block at `blk` (2-byte aligned in shared
-// memory): bytes 4t..4t+3 (lo) and 16+4t..16+4t+3 (hi) of the 32 codes, and
-// the same one byte further on (lo1, hi1).
-__device__ __forceinline__ void q8_0_words(const uint8_t* blk, int t, uint32_t& lo, uint32_t& hi, uint32_t& lo1,
-                                           uint32_t& hi1) {
-    const uintptr_t a = reinterpret_cast<uintptr_t>(blk + 2);
-    const uint32_t* w = reinterpret_cast<const uint32_t*>(a & ~uintptr_t(3));
-    const uint32_t sh = (uint32_t)(a & 3u) * 8u;
-    const uint32_t w0 = w[t], w1 = w[t + 1], w4 = w[t + 4], w5 = w[t + 5];
-    lo = __funnelshift_r(w0, w1, sh);
-    hi = __funnelshift_r(w4, w5, sh);
-    lo1 = __funnelshift_r(w0, w1, sh + 8);
-    hi1 = __funnelshift_r(w4, w5, sh + 8);
-}
-
 __device__ __forceinline__ uint32_t h2_sub(uint32_t a, uint32_t b) {
     __half2 r = __hsub2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
     return *reinterpret_cast<uint32_t*>(&r);
 }
-__device__ __forceinline__ uint32_t h2_mul(uint32_t a, uint32_t b) {
-    __half2 r = __hmul2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
-    return *reinterpret_cast<uint32_t*>(&r);
+__device__ __forceinline__ __half2 u2h(uint32_t v) { return *reinterpret_cast<__half2*>(&v); }
+__device__ __forceinline__ uint32_t h2u(__half2 v) { return *reinterpret_cast<uint32_t*>(&v); }
+
+// One lop3 each: (a & b) | c and (a & b) ^ c.  Callers pass b and c in
+// registers (see opaque()): with two immediate operands the compiler splits
+// the expression into two logic instructions.
+__device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
 }
-__device__ __forceinline__ uint32_t h2_fma(uint32_t a, uint32_t b, uint32_t c) {
-    __half2 r = __hfma2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b), *reinterpret_cast<__half2*>(&c));
-    return *reinterpret_cast<uint32_t*>(&r);
+__device__ __forceinline__ uint32_t and_xor(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
 }
-__device__ __forceinline__ uint32_t h2_lo2(uint32_t a) { return __byte_perm(a, 0, 0x1010); }
-__device__ __forceinline__ uint32_t h2_hi2(uint32_t a) { return __byte_perm(a, 0, 0x3232); }
+// a constant the compiler keeps in a register instead of folding it
+__device__ __forceinline__ uint32_t opaque(uint32_t v) {
+    asm volatile("" : "+r"(v));
+    return v;
+}
 
 // signed bytes 0 and 2 of w -> exact f16x2: 0x64 | (b ^ 0x80) is 1152 + b
-__device__ __forceinline__ uint32_t s8_02_h2(uint32_t w) { return h2_sub((w & 0x00FF00FFu) ^ 0x64806480u, 0x64806480u); }
+__device__ __forceinline__ uint32_t s8_02_h2(uint32_t w, uint32_t m00ff, uint32_t k6480) {
+    return h2_sub(and_xor(w, m00ff, k6480), 0x64806480u);
+}
 
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
+// Warps: kDmmaWarps consumers, one producer (bulk copies), one reducer that
+// sums the consumers' tile partials (so that consumers never wait for each
+// other at the end of a tile).
+constexpr int kDmmaThreads = (kDmmaWarps + 2) * 32;
+
 template <int WT, int AM, int NB, int EPI>
-__global__ void __launch_bounds__((kDmmaWarps + 1) * 32, 1) qmm_dmma_kernel(const DmmaParams p) {
+__global__ void __launch_bounds__(kDmmaThreads, 1) qmm_dmma_kernel(const DmmaParams p) {
     constexpr int UB = Unit<WT>::bytes;
     extern __shared__ __align__(128) uint8_t smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int S = p.stages;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem);  // full[S], empty[S], red full, red empty, activations
+    uint64_t* rfull = bars + 2 * S;
+    uint64_t* rempty = bars + 2 * S + 1;
+    uint64_t* abar = bars + 2 * S + 2;
     volatile int* flags = reinterpret_cast<volatile int*>(smem + p.off_flags);
     const int slice = blockIdx.x % p.kslices;
     const int grp0 = blockIdx.x / p.kslices;
@@ -258,23 +326,61 @@ __global__ void __launch_bounds__((kDmmaWarps + 1) * 32, 1) qmm_dmma_kernel(cons
     const int sunits = min(p.slice_units, p.units - su0);
     const bool whole = p.row_pitch == 0;  // short rows: one contiguous copy of the 16 rows per stage
     const int nch = (sunits + p.ups - 1) / p.ups;
+    float* red = reinterpret_cast<float*>(smem + p.off_red);  // [16 warps][16 weight rows][8 activation rows]
     if (tid == 0) {
         for (int i = 0; i < S; ++i) {
             mbar_init(smem_u32(&bars[i]), 1);
             mbar_init(smem_u32(&bars[S + i]), kDmmaWarps);
         }
+        mbar_init(smem_u32(rfull), kDmmaWarps * 32);
+        mbar_init(smem_u32(rempty), 32);
+        mbar_init(smem_u32(abar), 1);
         flags[0] = 0;
         fence_mbar_init();
     }
     __syncthreads();
+    grid_dep_launch();  // a K-split reduction launched after this grid may be scheduled
 
     if (warp == kDmmaWarps) {
         // ------------------------------ producer ------------------------------
+        // Prepared activations: wait for the preparing grid, then fetch this
+        // CTA's K slice with one copy per row (int8) or (row, piece) plane
+        // (f32), one for the scales and one for the aux sums.
+        auto fetch_act = [&]() {
+            grid_dep_wait();
+            const int k0 = su0 * Unit<WT>::vals, klen = sunits * Unit<WT>::vals;
+            const int nrow = AM == A_INT8 ? p.M : 2 * p.M;
+            const int vb = AM == A_INT8 ? 1 : 2;  // bytes per activation value
+            long long src = 0;
+            uint32_t dst = 0, bytes = 0;
+            if (lane < nrow) {
+                src = p.ext_codes + ((long long)lane * p.K + k0) * vb;
+                dst = p.off_act + lane * p.act_pitch * vb;
+                bytes = (uint32_t)(klen * vb);
+            } else if (lane == nrow) {
+                src = p.ext_scale + (long long)su0 * p.sstride * 4;
+                dst = p.off_scale;
+                bytes = (uint32_t)(sunits * p.sstride * 4);
+            } else if (lane == nrow + 1 && WT == T_Q4_K) {
+                src = p.ext_aux + (long long)su0 * 256;
+                dst = p.off_aux;
+                bytes = (uint32_t)sunits * 256u;
+            }
+            const uint32_t tx = __reduce_add_sync(0xffffffffu, bytes);
+            if (lane == 0) mbar_arrive_tx(smem_u32(abar), tx);
+            __syncwarp();
+            if (bytes) bulk_g2s(smem_u32(smem + dst), p.ext + src, bytes, smem_u32(abar));
+        };
+        bool act_done = p.ext == nullptr;
         long long g = 0;
         bool ok = true;
         for (int grp = grp0; grp < p.ntiles && ok; grp += p.per_slice) {
             for (int ch = 0; ch < nch && ok; ++ch, ++g) {
                 const int slot = (int)(g % S);
+                if (g == S && !act_done) {  // the first stages are in flight: now the activations
+                    fetch_act();
+                    act_done = true;
+                }
                 if (g >= S) {
                     int okl = 1;
                     if (lane == 0) okl = mbar_wait(smem_u32(&bars[S + slot]), (uint32_t)(((g / S) - 1) & 1), flags, p.err);
@@ -308,44 +414,85 @@ __global__ void __launch_bounds__((kDmmaWarps + 1) * 32, 1) qmm_dmma_kernel(cons
                 if (bytes) bulk_g2s(smem_u32(st + dst), p.wq + a, bytes, fb);
             }
         }
+        if (!act_done) fetch_act();
         if (lane == 0) {
             const long long first = g > S ? g - S : 0;
             for (long long q = first; q < g; ++q) mbar_wait(smem_u32(&bars[q % S]), (uint32_t)((q / S) & 1), flags, p.err);
+            if (p.ext) mbar_wait(smem_u32(abar), 0u, flags, p.err);
+        }
+        return;
+    }
+    if (warp == kDmmaWarps + 1) {
+        // ------------------------------ reducer ------------------------------
+        if (EPI != E_Y) return;
+        int tc = 0;
+        for (int grp = grp0; grp < p.ntiles; grp += p.per_slice, ++tc) {
+            if (!mbar_wait(smem_u32(rfull), (uint32_t)(tc & 1), flags, p.err)) break;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int o = lane + 32 * i;
+                const int m = o & 7;
+                const long long n = (long long)grp * kDmmaRows + (o >> 3);
+                float v = 0.0f;
+#pragma unroll
+                for (int w = 0; w < kDmmaWarps; ++w) v += red[w * 128 + o];
+                if (!flags[0] && m < p.M && n < p.N) {
+                    if (p.kslices == 1) p.y[(long long)m * p.N + n] = v;
+                    else p.partial[((long long)slice * p.M + m) * p.N + n] = v;
+                }
+            }
+            __syncwarp();
+            mbar_arrive(smem_u32(rempty));
         }
         return;
     }
 
     // ------------------------------ consumers ------------------------------
-    const int k0 = su0 * Unit<WT>::vals;
-    const int klen = sunits * Unit<WT>::vals;
-    dmma_prepare<WT, AM>(p, smem, k0, klen, tid);
-    consumer_sync<kDmmaWarps>();
+    if (p.ext) {
+        mbar_wait(smem_u32(abar), 0u, flags, p.err);
+    } else {
+        ActDst o;
+        o.act = smem + p.off_act;
+        o.pitch = p.act_pitch;
+        o.scale = reinterpret_cast<float*>(smem + p.off_scale);
+        o.sstride = p.sstride;
+        o.aux = smem + p.off_aux;
+        if (prep_per_warp<WT, AM>())
+            prep_items<WT, AM>(p.x, p.M, p.K, su0, sunits, o, warp, kDmmaWarps, lane);
+        else
+            prep_items<WT, AM>(p.x, p.M, p.K, su0, sunits, o, tid, kDmmaWarps * 32, lane);
+        consumer_sync<kDmmaWarps>();
+    }
 
     const int g8 = lane >> 2, t4 = lane & 3;
     const uint8_t* act = smem + p.off_act;
-    const float* da = reinterpret_cast<const float*>(smem + p.off_scale);
+    const float* asc = reinterpret_cast<const float*>(smem + p.off_scale);
     const uint32_t* aux = reinterpret_cast<const uint32_t*>(smem + p.off_aux);
-    const float* rs = reinterpret_cast<const float*>(smem + p.off_rs);
-    float* red = reinterpret_cast<float*>(smem + p.off_red);  // [16 warps][16 weight rows][8 activation rows]
-    // B-operand column of this thread: activation row (int8) or (row, piece) plane (f32), per column set
-    bool bval[NB];
-    const uint8_t* bcol[NB];
+    // B-operand column of this thread: activation row (int8) or (row, piece)
+    // plane (f32), per column set.  Columns past the batch read a valid row;
+    // their outputs are never written.
+    int bc[NB];
 #pragma unroll
     for (int s = 0; s < NB; ++s) {
-        if (AM == A_INT8) {
-            bval[s] = g8 < p.M;
-            bcol[s] = act + (bval[s] ? g8 : 0) * p.act_pitch;
-        } else {
+        if (AM == A_INT8) bc[s] = g8 < p.M ? g8 : g8 % p.M;
+        else {
             const int pl = 8 * s + g8;
-            bval[s] = (pl >> 1) < p.M;
-            bcol[s] = act + (long long)(bval[s] ? pl : 0) * p.act_pitch * 2;
+            bc[s] = (pl >> 1) < p.M ? pl : pl % (2 * p.M);
         }
     }
+    // f32: this thread's output activation row of column set s is t4 + 4 s
+    // (its scale index); rows past the batch read row 0's
+    int ar[NB];
+#pragma unroll
+    for (int s = 0; s < NB; ++s) ar[s] = t4 + 4 * s < p.M ? t4 + 4 * s : 0;
     // Q4_K min-term A fragments: bytes of the packed 6-bit mins as f16 pairs
     const uint32_t sel_m2 = (uint32_t)((2 * (t4 & 1)) | 0x40 | ((2 * (t4 & 1) + 1) << 8) | 0x4000);  // m_{2t}, m_{2t+1}
     const uint32_t sel_m1 = (uint32_t)(t4 | 0x40 | (t4 << 8) | 0x4000);                                   // m_t, m_t
+    const uint32_t kM00FF = opaque(0x00FF00FFu), k6480 = opaque(0x64806480u);
+    const uint32_t kM000F = opaque(0x000F000Fu), kM00F0 = opaque(0x00F000F0u), k6400 = opaque(0x64006400u);
     long long g = 0;
-    for (int grp = grp0; grp < p.ntiles; grp += p.per_slice) {
+    int tc = 0;
+    for (int grp = grp0; grp < p.ntiles; grp += p.per_slice, ++tc) {
         float acc[NB][2][2];
 #pragma unroll
         for (int s = 0; s < NB; ++s) acc[s][0][0] = acc[s][0][1] = acc[s][1][0] = acc[s][1][1] = 0.0f;
@@ -354,7 +501,7 @@ __global__ void __launch_bounds__((kDmmaWarps + 1) * 32, 1) qmm_dmma_kernel(cons
             const bool ok = mbar_wait(smem_u32(&bars[slot]), (uint32_t)((g / S) & 1), flags, p.err);
             const int cu0 = su0 + ch * p.ups;
             const int cnu = min(p.ups, su0 + sunits - cu0);
-            if (ok) {
+            if (ok && warp < cnu) {
                 const uint8_t* st = smem + p.off_stage + (long long)slot * p.stage_bytes;
                 auto rowptr = [&](int r) -> const uint8_t* {
                     const long long n = (long long)grp * kDmmaRows + r;
@@ -362,46 +509,62 @@ __global__ void __launch_bounds__((kDmmaWarps + 1) * 32, 1) qmm_dmma_kernel(cons
                     return st + r * p.row_pitch + (int)((n * p.rb + (long long)cu0 * UB) & 15);
                 };
                 const uint8_t* r0p = rowptr(g8);
-                const uint8_t* r1p = rowptr(g8 + 8);
-                const int ur0 = cu0 - su0;  // first unit of the chunk inside the slice
-#pragma unroll 1
-                for (int uu = warp; uu < cnu; uu += kDmmaWarps) {
-                    const int u = ur0 + uu;  // unit index inside the slice (activation side)
-                    if (WT == T_Q8_0) {
-                        const uint8_t* b0p = r0p + 34 * uu;
-                        const uint8_t* b1p = r1p + 34 * uu;
-                        const float dw0 = h2f(*reinterpret_cast<const uint16_t*>(b0p));
-                        const float dw1 = h2f(*reinterpret_cast<const uint16_t*>(b1p));
-                        uint32_t lo0, hi0, lo0s, hi0s, lo1, hi1, lo1s, hi1s;
-                        q8_0_words(b0p, t4, lo0, hi0, lo0s, hi0s);
-                        q8_0_words(b1p, t4, lo1, hi1, lo1s, hi1s);
+                const int dr = (int)(rowptr(g8 + 8) - r0p);  // row g8+8 relative to row g8 (a multiple of 16)
+                const int u0 = cu0 - su0 + warp;              // first unit of this warp (slice-relative)
+                if (WT == T_Q8_0) {
+                    // The warp's blocks are 16 apart (544 bytes): their code bytes share one 4-byte alignment.
+                    const uint8_t* q0 = r0p + 34 * warp;
+                    const uintptr_t a = reinterpret_cast<uintptr_t>(q0 + 2);
+                    const uint32_t sh = (uint32_t)(a & 3u) * 8u;
+                    const uint32_t* w0p = reinterpret_cast<const uint32_t*>(a & ~uintptr_t(3)) + t4;
+                    const uint16_t* s0p = reinterpret_cast<const uint16_t*>(q0);
+                    const uint8_t* xp[NB];
+#pragma unroll
+                    for (int s = 0; s < NB; ++s)
+                        xp[s] = AM == A_F32 ? act + (long long)bc[s] * p.act_pitch * 2 + (u0 * 32 + 8 * t4) * 2
+                                            : act + bc[s] * p.act_pitch + u0 * 32 + 4 * t4;
+                    const float* sp = AM == A_F32 ? asc + u0 * p.sstride : asc + u0 * 8 + 2 * t4;
+                    int u = u0;
+#pragma unroll 2
+                    for (int uu = warp; uu < cnu; uu += kDmmaWarps, u += kDmmaWarps) {
+                        const uint32_t* w1p = reinterpret_cast<const uint32_t*>(reinterpret_cast<const uint8_t*>(w0p) + dr);
+                        const uint32_t x0 = w0p[0], x1 = w0p[1], x4 = w0p[4], x5 = w0p[5];
+                        const uint32_t y0 = w1p[0], y1 = w1p[1], y4 = w1p[4], y5 = w1p[5];
+                        const float dw0 = h2f(s0p[0]);
+                        const float dw1 = h2f(*reinterpret_cast<const uint16_t*>(reinterpret_cast<const uint8_t*>(s0p) + dr));
+                        const uint32_t lo0 = __funnelshift_r(x0, x1, sh), hi0 = __funnelshift_r(x4, x5, sh);
+                        const uint32_t lo1 = __funnelshift_r(y0, y1, sh), hi1 = __funnelshift_r(y4, y5, sh);
                         if (AM == A_F32) {
-                            const uint32_t a0 = s8_02_h2(lo0), a1 = s8_02_h2(lo1), a2 = s8_02_h2(lo0s), a3 = s8_02_h2(lo1s);
-                            const uint32_t c0 = s8_02_h2(hi0), c1 = s8_02_h2(hi1), c2 = s8_02_h2(hi0s), c3 = s8_02_h2(hi1s);
+                            const uint32_t lo0s = __funnelshift_r(x0, x1, sh + 8), hi0s = __funnelshift_r(x4, x5, sh + 8);
+                            const uint32_t lo1s = __funnelshift_r(y0, y1, sh + 8), hi1s = __funnelshift_r(y4, y5, sh + 8);
+                            const uint32_t a0 = s8_02_h2(lo0, kM00FF, k6480), a1 = s8_02_h2(lo1, kM00FF, k6480);
+                            const uint32_t a2 = s8_02_h2(lo0s, kM00FF, k6480), a3 = s8_02_h2(lo1s, kM00FF, k6480);
+                            const uint32_t c0 = s8_02_h2(hi0, kM00FF, k6480), c1 = s8_02_h2(hi1, kM00FF, k6480);
+                            const uint32_t c2 = s8_02_h2(hi0s, kM00FF, k6480), c3 = s8_02_h2(hi1s, kM00FF, k6480);
 #pragma unroll
                             for (int s = 0; s < NB; ++s) {
-                                uint4 xv = make_uint4(0u, 0u, 0u, 0u);
-                                if (bval[s]) xv = ld128(bcol[s] + (u * 32 + 8 * t4) * 2);
-                                float d[4] = {0.f, 0.f, 0.f, 0.f};
-                                mma_f16(d, a0, a1, a2, a3, xv.x, xv.y);
+                                const uint4 xv = ld128(xp[s]);
+                                const float io = sp[ar[s]];  // 2^-s of (activation row, block)
+                                float d[4];
+                                mma_f16_z(d, a0, a1, a2, a3, xv.x, xv.y);
                                 mma_f16(d, c0, c1, c2, c3, xv.z, xv.w);
-                                acc[s][0][0] = fmaf(dw0, d[0] + d[1], acc[s][0][0]);
-                                acc[s][1][0] = fmaf(dw1, d[2] + d[3], acc[s][1][0]);
+                                acc[s][0][0] = fmaf(dw0 * io, d[0] + d[1], acc[s][0][0]);
+                                acc[s][1][0] = fmaf(dw1 * io, d[2] + d[3], acc[s][1][0]);
+                                xp[s] += kDmmaWarps * 32 * 2;
                             }
+                            sp += kDmmaWarps * p.sstride;
                         } else {
-                            uint32_t b0 = 0u, b1 = 0u;
-                            if (bval[0]) {
-                                b0 = ld32(bcol[0] + u * 32 + 4 * t4);
-                                b1 = ld32(bcol[0] + u * 32 + 16 + 4 * t4);
-                            }
+                            const uint32_t b0 = ld32(xp[0]), b1 = ld32(xp[0] + 16);
+                            xp[0] += kDmmaWarps * 32;
                             int d[4];
                             mma_s8(d, lo0, lo1, hi0, hi1, b0, b1);
                             if (EPI == E_Y) {
-                                const float2 dap = *reinterpret_cast<const float2*>(da + u * 8 + 2 * t4);
-                                acc[0][0][0] = fmaf((float)d[0], dw0 * dap.x, acc[0][0][0]);
-                                acc[0][0][1] = fmaf((float)d[1], dw0 * dap.y, acc[0][0][1]);
-                                acc[0][1][0] = fmaf((float)d[2], dw1 * dap.x, acc[0][1][0]);
-                                acc[0][1][1] = fmaf((float)d[3], dw1 * dap.y, acc[0][1][1]);
+                                const float2 dv = *reinterpret_cast<const float2*>(sp);
+                                acc[0][0][0] = fmaf((float)d[0], dw0 * dv.x, acc[0][0][0]);
+                                acc[0][0][1] = fmaf((float)d[1], dw0 * dv.y, acc[0][0][1]);
+                                acc[0][1][0] = fmaf((float)d[2], dw1 * dv.x, acc[0][1][0]);
+                                acc[0][1][1] = fmaf((float)d[3], dw1 * dv.y, acc[0][1][1]);
+                                sp += kDmmaWarps * 8;
                             } else {
 #pragma unroll
                                 for (int i = 0; i < 4; ++i) {
@@ -411,50 +574,56 @@ __global__ void __launch_bounds__((kDmmaWarps + 1) * 32, 1) qmm_dmma_kernel(cons
                                 }
                             }
                         }
-                    } else {
-                        const uint8_t* s0p = r0p + 144 * uu;
-                        const uint8_t* s1p = r1p + 144 * uu;
-                        const uint4 h0 = ld128(s0p), h1 = ld128(s1p);
+                        w0p += kDmmaWarps * 34 / 4;
+                        s0p += kDmmaWarps * 34 / 2;
+                    }
+                } else {
+                    const uint8_t* h0p = r0p + 144 * warp;
+                    int u = u0;
+#pragma unroll 1
+                    for (int uu = warp; uu < cnu; uu += kDmmaWarps, u += kDmmaWarps, h0p += kDmmaWarps * 144) {
+                        const uint8_t* h1p = h0p + dr;
+                        const uint4 h0 = ld128(h0p), h1 = ld128(h1p);
                         uint32_t sc03[2], sc47[2], mn03[2], mn47[2];
                         q4k_unpack4(h0.y, h0.z, h0.w, sc03[0], sc47[0], mn03[0], mn47[0]);
                         q4k_unpack4(h1.y, h1.z, h1.w, sc03[1], sc47[1], mn03[1], mn47[1]);
                         if (AM == A_F32) {
                             float d[NB][4];
 #pragma unroll
-                            for (int s = 0; s < NB; ++s) d[s][0] = d[s][1] = d[s][2] = d[s][3] = 0.0f;
-#pragma unroll
                             for (int c = 0; c < 4; ++c) {
-                                // per row: (sc_{2c}, sc_{2c+1}/16) and (-1024 sc_{2c}, -64 sc_{2c+1})
+                                // per row: P = (sc_{2c}, sc_{2c+1}/16), Q = (-1024 sc_{2c}, -64 sc_{2c+1})
                                 const uint32_t sel = (uint32_t)((2 * (c & 1)) | 0x40 | ((2 * (c & 1) + 1) << 8) | 0x5000);
-                                uint32_t P[2], Q[2];
+                                __half2 P[2], Q[2];
 #pragma unroll
                                 for (int r = 0; r < 2; ++r) {
-                                    P[r] = h2_sub(__byte_perm(c < 2 ? sc03[r] : sc47[r], 0x00005464u, sel), 0x54006400u);
-                                    Q[r] = h2_mul(P[r], 0xE400E400u);
+                                    P[r] = __hsub2(u2h(__byte_perm(c < 2 ? sc03[r] : sc47[r], 0x00005464u, sel)), u2h(0x54006400u));
+                                    Q[r] = __hmul2(P[r], u2h(0xE400E400u));
                                 }
-                                const uint32_t qa0 = ld32(s0p + 16 + 32 * c + 4 * t4), qb0 = ld32(s0p + 32 + 32 * c + 4 * t4);
-                                const uint32_t qa1 = ld32(s1p + 16 + 32 * c + 4 * t4), qb1 = ld32(s1p + 32 + 32 * c + 4 * t4);
+                                const uint32_t qa0 = ld32(h0p + 16 + 32 * c + 4 * t4), qb0 = ld32(h0p + 32 + 32 * c + 4 * t4);
+                                const uint32_t qa1 = ld32(h1p + 16 + 32 * c + 4 * t4), qb1 = ld32(h1p + 32 + 32 * c + 4 * t4);
                                 const uint32_t qa0s = qa0 >> 8, qb0s = qb0 >> 8, qa1s = qa1 >> 8, qb1s = qb1 >> 8;
 #pragma unroll
                                 for (int h = 0; h < 2; ++h) {
                                     // low nibbles (sub-block 2c): 1024 + n; high nibbles (2c+1): 1024 + 16 n
-                                    const uint32_t mk = h ? 0x00F000F0u : 0x000F000Fu;
-                                    const uint32_t S0 = h ? h2_hi2(P[0]) : h2_lo2(P[0]), N0 = h ? h2_hi2(Q[0]) : h2_lo2(Q[0]);
-                                    const uint32_t S1 = h ? h2_hi2(P[1]) : h2_lo2(P[1]), N1 = h ? h2_hi2(Q[1]) : h2_lo2(Q[1]);
-                                    const uint32_t a0 = h2_fma((qa0 & mk) | 0x64006400u, S0, N0);
-                                    const uint32_t a1 = h2_fma((qa1 & mk) | 0x64006400u, S1, N1);
-                                    const uint32_t a2 = h2_fma((qa0s & mk) | 0x64006400u, S0, N0);
-                                    const uint32_t a3 = h2_fma((qa1s & mk) | 0x64006400u, S1, N1);
-                                    const uint32_t c0 = h2_fma((qb0 & mk) | 0x64006400u, S0, N0);
-                                    const uint32_t c1 = h2_fma((qb1 & mk) | 0x64006400u, S1, N1);
-                                    const uint32_t c2 = h2_fma((qb0s & mk) | 0x64006400u, S0, N0);
-                                    const uint32_t c3 = h2_fma((qb1s & mk) | 0x64006400u, S1, N1);
+                                    const uint32_t mk = h ? kM00F0 : kM000F;
+                                    const __half2 S0 = h ? __high2half2(P[0]) : __low2half2(P[0]);
+                                    const __half2 N0 = h ? __high2half2(Q[0]) : __low2half2(Q[0]);
+                                    const __half2 S1 = h ? __high2half2(P[1]) : __low2half2(P[1]);
+                                    const __half2 N1 = h ? __high2half2(Q[1]) : __low2half2(Q[1]);
+                                    const uint32_t a0 = h2u(__hfma2(u2h(and_or(qa0, mk, k6400)), S0, N0));
+                                    const uint32_t a1 = h2u(__hfma2(u2h(and_or(qa1, mk, k6400)), S1, N1));
+                                    const uint32_t a2 = h2u(__hfma2(u2h(and_or(qa0s, mk, k6400)), S0, N0));
+                                    const uint32_t a3 = h2u(__hfma2(u2h(and_or(qa1s, mk, k6400)), S1, N1));
+                                    const uint32_t c0 = h2u(__hfma2(u2h(and_or(qb0, mk, k6400)), S0, N0));
+                                    const uint32_t c1 = h2u(__hfma2(u2h(and_or(qb1, mk, k6400)), S1, N1));
+                                    const uint32_t c2 = h2u(__hfma2(u2h(and_or(qb0s, mk, k6400)), S0, N0));
+                                    const uint32_t c3 = h2u(__hfma2(u2h(and_or(qb1s, mk, k6400)), S1, N1));
                                     const int j = 2 * c + h;
 #pragma unroll
                                     for (int s = 0; s < NB; ++s) {
-                                        uint4 xv = make_uint4(0u, 0u, 0u, 0u);
-                                        if (bval[s]) xv = ld128(bcol[s] + ((u * 8 + j) * 32 + 8 * t4) * 2);
-                                        mma_f16(d[s], a0, a1, a2, a3, xv.x, xv.y);
+                                        const uint4 xv = ld128(act + (long long)bc[s] * p.act_pitch * 2 + ((u * 8 + j) * 32 + 8 * t4) * 2);
+                                        if (j == 0) mma_f16_z(d[s], a0, a1, a2, a3, xv.x, xv.y);
+                                        else mma_f16(d[s], a0, a1, a2, a3, xv.x, xv.y);
                                         mma_f16(d[s], c0, c1, c2, c3, xv.z, xv.w);
                                     }
                                 }
@@ -466,59 +635,54 @@ __global__ void __launch_bounds__((kDmmaWarps + 1) * 32, 1) qmm_dmma_kernel(cons
                             const float fM0 = 32.0f * h2f(h0.x >> 16), fM1 = 32.0f * h2f(h1.x >> 16);
 #pragma unroll
                             for (int s = 0; s < NB; ++s) {
-                                uint32_t xb = 0u;
-                                if (bval[s]) xb = aux[(u * 16 + 8 * s + g8) * 4 + t4];
-                                float dm[4] = {0.f, 0.f, 0.f, 0.f};
-                                mma_f16_k8(dm, ma0, ma1, xb);
-                                acc[s][0][0] += fD0 * (d[s][0] + d[s][1]) - fM0 * (dm[0] + dm[1]);
-                                acc[s][1][0] += fD1 * (d[s][2] + d[s][3]) - fM1 * (dm[2] + dm[3]);
+                                float dm[4];
+                                mma_f16_k8(dm, ma0, ma1, aux[(u * 16 + bc[s]) * 4 + t4]);
+                                const float io = asc[u * p.sstride + ar[s]];  // 2^-s of (activation row, super-block)
+                                acc[s][0][0] = fmaf(io, fD0 * (d[s][0] + d[s][1]) - fM0 * (dm[0] + dm[1]), acc[s][0][0]);
+                                acc[s][1][0] = fmaf(io, fD1 * (d[s][2] + d[s][3]) - fM1 * (dm[2] + dm[3]), acc[s][1][0]);
                             }
                         } else {
-                            int ssc[4] = {0, 0, 0, 0};
+                            // S_sc: low nibbles as they are, high nibbles as 16 n (their sums are then
+                            // multiples of 16 and are divided back exactly at the end)
+                            int sl[4] = {0, 0, 0, 0}, shi[4] = {0, 0, 0, 0};
+                            const uint8_t* xb = act + bc[0] * p.act_pitch + u * 256 + 4 * t4;
 #pragma unroll
                             for (int c = 0; c < 4; ++c) {
-                                const uint32_t qa0 = ld32(s0p + 16 + 32 * c + 4 * t4), qb0 = ld32(s0p + 32 + 32 * c + 4 * t4);
-                                const uint32_t qa1 = ld32(s1p + 16 + 32 * c + 4 * t4), qb1 = ld32(s1p + 32 + 32 * c + 4 * t4);
+                                const uint32_t qa0 = ld32(h0p + 16 + 32 * c + 4 * t4), qb0 = ld32(h0p + 32 + 32 * c + 4 * t4);
+                                const uint32_t qa1 = ld32(h1p + 16 + 32 * c + 4 * t4), qb1 = ld32(h1p + 32 + 32 * c + 4 * t4);
 #pragma unroll
                                 for (int h = 0; h < 2; ++h) {
                                     const int j = 2 * c + h;
-                                    const uint32_t sh = 4u * h;
-                                    uint32_t b0 = 0u, b1 = 0u;
-                                    if (bval[0]) {
-                                        b0 = ld32(bcol[0] + u * 256 + 32 * j + 4 * t4);
-                                        b1 = ld32(bcol[0] + u * 256 + 32 * j + 16 + 4 * t4);
-                                    }
+                                    const uint32_t mk = h ? 0xF0F0F0F0u : 0x0F0F0F0Fu;
                                     int dj[4];
-                                    mma_s8(dj, (qa0 >> sh) & 0x0F0F0F0Fu, (qa1 >> sh) & 0x0F0F0F0Fu, (qb0 >> sh) & 0x0F0F0F0Fu,
-                                           (qb1 >> sh) & 0x0F0F0F0Fu, b0, b1);
+                                    mma_u8s8(dj, qa0 & mk, qa1 & mk, qb0 & mk, qb1 & mk, ld32(xb + 32 * j), ld32(xb + 32 * j + 16));
                                     const uint32_t selj = 0x4440u | (uint32_t)(j & 3);
                                     const int sc0 = (int)__byte_perm(j < 4 ? sc03[0] : sc47[0], 0, selj);
                                     const int sc1 = (int)__byte_perm(j < 4 ? sc03[1] : sc47[1], 0, selj);
-                                    ssc[0] += sc0 * dj[0];
-                                    ssc[1] += sc0 * dj[1];
-                                    ssc[2] += sc1 * dj[2];
-                                    ssc[3] += sc1 * dj[3];
+                                    int* t = h ? shi : sl;
+                                    t[0] += sc0 * dj[0];
+                                    t[1] += sc0 * dj[1];
+                                    t[2] += sc1 * dj[2];
+                                    t[3] += sc1 * dj[3];
                                 }
                             }
+                            int ssc[4];
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) ssc[i] = sl[i] + (shi[i] >> 4);
                             // S_m = sum_j m_j (sum of the sub-block's 32 codes), as 16 slots of sums of 16
                             const uint32_t ma0 = h2_sub(__byte_perm(mn03[0], 0x64646464u, sel_m1), 0x64006400u);
                             const uint32_t ma1 = h2_sub(__byte_perm(mn03[1], 0x64646464u, sel_m1), 0x64006400u);
                             const uint32_t ma2 = h2_sub(__byte_perm(mn47[0], 0x64646464u, sel_m1), 0x64006400u);
                             const uint32_t ma3 = h2_sub(__byte_perm(mn47[1], 0x64646464u, sel_m1), 0x64006400u);
-                            uint32_t xb0 = 0u, xb1 = 0u;
-                            if (bval[0]) {
-                                xb0 = aux[(u * 8 + t4) * 8 + g8];
-                                xb1 = aux[(u * 8 + t4 + 4) * 8 + g8];
-                            }
-                            float sm[4] = {0.f, 0.f, 0.f, 0.f};
-                            mma_f16(sm, ma0, ma1, ma2, ma3, xb0, xb1);
+                            float sm[4];
+                            mma_f16_z(sm, ma0, ma1, ma2, ma3, aux[(u * 8 + t4) * 8 + bc[0]], aux[(u * 8 + t4 + 4) * 8 + bc[0]]);
                             if (EPI == E_Y) {
-                                const float2 dap = *reinterpret_cast<const float2*>(da + u * 8 + 2 * t4);
+                                const float2 dv = *reinterpret_cast<const float2*>(asc + u * 8 + 2 * t4);
                                 const float fD0 = h2f(h0.x), fD1 = h2f(h1.x), fM0 = h2f(h0.x >> 16), fM1 = h2f(h1.x >> 16);
-                                acc[0][0][0] = fmaf(dap.x, fD0 * (float)ssc[0] - fM0 * sm[0], acc[0][0][0]);
-                                acc[0][0][1] = fmaf(dap.y, fD0 * (float)ssc[1] - fM0 * sm[1], acc[0][0][1]);
-                                acc[0][1][0] = fmaf(dap.x, fD1 * (float)ssc[2] - fM1 * sm[2], acc[0][1][0]);
-                                acc[0][1][1] = fmaf(dap.y, fD1 * (float)ssc[3] - fM1 * sm[3], acc[0][1][1]);
+                                acc[0][0][0] = fmaf(dv.x, fD0 * (float)ssc[0] - fM0 * sm[0], acc[0][0][0]);
+                                acc[0][0][1] = fmaf(dv.y, fD0 * (float)ssc[1] - fM0 * sm[1], acc[0][0][1]);
+                                acc[0][1][0] = fmaf(dv.x, fD1 * (float)ssc[2] - fM1 * sm[2], acc[0][1][0]);
+                                acc[0][1][1] = fmaf(dv.y, fD1 * (float)ssc[3] - fM1 * sm[3], acc[0][1][1]);
                             } else {
 #pragma unroll
                                 for (int i = 0; i < 4; ++i) {
@@ -539,31 +703,21 @@ __global__ void __launch_bounds__((kDmmaWarps + 1) * 32, 1) qmm_dmma_kernel(cons
             if (lane == 0) mbar_arrive(smem_u32(&bars[S + slot]));
         }
         if (EPI != E_Y) continue;
-        // ---- tile epilogue: 16 warp partials of (weight row, activation row)
+        // ---- tile partials of (weight row, activation row) to the reducer;
+        // its buffer is free once the reducer has read the previous tile
+        if (tc >= 1) mbar_wait(smem_u32(rempty), (uint32_t)((tc - 1) & 1), flags, p.err);
+        float* rb = red + warp * 128;
         if (AM == A_F32) {
 #pragma unroll
             for (int s = 0; s < NB; ++s) {
-                red[warp * 128 + g8 * 8 + t4 + 4 * s] = acc[s][0][0];
-                red[warp * 128 + (g8 + 8) * 8 + t4 + 4 * s] = acc[s][1][0];
+                rb[g8 * 8 + t4 + 4 * s] = acc[s][0][0];
+                rb[(g8 + 8) * 8 + t4 + 4 * s] = acc[s][1][0];
             }
         } else {
-            *reinterpret_cast<float2*>(red + warp * 128 + g8 * 8 + 2 * t4) = make_float2(acc[0][0][0], acc[0][0][1]);
-            *reinterpret_cast<float2*>(red + warp * 128 + (g8 + 8) * 8 + 2 * t4) = make_float2(acc[0][1][0], acc[0][1][1]);
+            *reinterpret_cast<float2*>(rb + g8 * 8 + 2 * t4) = make_float2(acc[0][0][0], acc[0][0][1]);
+            *reinterpret_cast<float2*>(rb + (g8 + 8) * 8 + 2 * t4) = make_float2(acc[0][1][0], acc[0][1][1]);
         }
-        consumer_sync<kDmmaWarps>();
-        if (tid < 128) {
-            const int m = tid & 7;
-            const long long n = (long long)grp * kDmmaRows + (tid >> 3);
-            float v = 0.0f;
-#pragma unroll
-            for (int w = 0; w < kDmmaWarps; ++w) v += red[w * 128 + tid];
-            if (AM == A_F32) v *= rs[2 * m + 1];
-            if (!flags[0] && m < p.M && n < p.N) {
-                if (p.kslices == 1) p.y[(long long)m * p.N + n] = v;
-                else p.partial[((long long)slice * p.M + m) * p.N + n] = v;
-            }
-        }
-        consumer_sync<kDmmaWarps>();
+        mbar_arrive(smem_u32(rfull));
     }
 }
 
@@ -576,30 +730,38 @@ struct DmmaPlan {
     int nb;   // B column sets (2 for f32_act with M > 4)
     int grid;
     size_t smem;
-    size_t workspace;
+    size_t workspace;  // ext_bytes + split-K partial sums
+    size_t ext_bytes;  // prepared activations (0: prepared inside the decode kernel)
 };
+
+// Weight matrices at least this large prepare the activations once per call
+// (a second, small launch); smaller ones, bound by launch latency, prepare
+// them inside the single decode launch.
+constexpr long long kDmmaExtMinBytes = 32ll << 20;
 
 // Shared-memory layout for K split in `ks` slices and `ups` units per stage;
 // false when fewer than two stages fit.
-inline bool dmma_layout(int wt, int am, long long M, int ks, int ups, int smem_max, DmmaPlan& pl) {
+inline bool dmma_layout(int wt, int am, long long M, int nb, int ks, int ups, int smem_max, DmmaPlan& pl) {
     DmmaParams& p = pl.p;
     const int uv = wt == T_Q8_0 ? 32 : 256, ub = wt == T_Q8_0 ? 34 : 144;
     const int su = (p.units + ks - 1) / ks;
     if ((long long)(ks - 1) * su >= p.units) return false;
     if (ups > su) ups = su;
     const int kv = su * uv;
-    int act, scale = 0, aux = 0;
+    int act, aux = 0;
     if (am == A_INT8) {
         p.act_pitch = pitch_mod(kv, 16);  // 4-byte B loads of 8 rows x 4 threads: 32 banks
         act = (int)M * p.act_pitch;
-        scale = su * 8 * 4;
+        p.sstride = 8;
         if (wt == T_Q4_K) aux = su * 8 * 8 * 4;
     } else {
         p.act_pitch = pitch_mod(2 * kv, 64) / 2;  // 16-byte B loads of 2 planes per quarter-warp
         act = 2 * (int)M * p.act_pitch * 2;
+        p.sstride = 4 * nb;
         if (wt == T_Q4_K) aux = su * 16 * 8 * 2;
     }
-    int off = 256;
+    const int scale = su * p.sstride * 4;
+    int off = 256;  // mbarriers: 2 per stage (<= 8 stages), 2 for the reducer, 1 for the activations
     p.off_flags = off;
     off += 128;
     p.off_act = off;
@@ -608,8 +770,6 @@ inline bool dmma_layout(int wt, int am, long long M, int ks, int ups, int smem_m
     off = round_up(off + scale, 128);
     p.off_aux = off;
     off = round_up(off + aux, 128);
-    p.off_rs = off;
-    off = round_up(off + 64, 128);
     p.off_red = off;
     off = round_up(off + kDmmaWarps * 128 * 4, 128);
     p.off_stage = off;
@@ -618,7 +778,9 @@ inline bool dmma_layout(int wt, int am, long long M, int ks, int ups, int smem_m
         sb = 16 * p.rb + 64;  // short rows: one contiguous copy of the whole tile
         p.row_pitch = 0;
     } else {
-        p.row_pitch = pitch_mod(ups * ub + 48, 16);
+        // Q8_0 word loads reach 18 bytes past the chunk (2-byte offset
+        // rounding and the 9th word); a copy starts up to 15 bytes early
+        p.row_pitch = pitch_mod(ups * ub + (wt == T_Q8_0 ? 32 : 0), 16);
         sb = 16LL * p.row_pitch;
     }
     sb = (sb + 127) / 128 * 128;
@@ -634,7 +796,7 @@ inline bool dmma_layout(int wt, int am, long long M, int ks, int ups, int smem_m
 }
 
 inline bool plan_dmma(int wt, int am, long long M, long long N, long long K, int sm_count, int smem_max,
-                      DmmaPlan& out) {
+                      DmmaPlan& out, bool ext_ok = true) {
     if (M < 1 || M > 8) return false;
     DmmaPlan pl{};
     DmmaParams& p = pl.p;
@@ -647,20 +809,49 @@ inline bool plan_dmma(int wt, int am, long long M, long long N, long long K, int
     p.total_bytes = p.rb * N;
     p.ntiles = (int)((N + kDmmaRows - 1) / kDmmaRows);
     pl.nb = (am == A_F32 && M > 4) ? 2 : 1;
-    // K chunk per stage: ~3.3-4.6 KB per row copy (one SM's bulk-copy rate
-    // caps smaller copies); smaller chunks only when nothing else fits
-    const int big[3] = {wt == T_Q8_0 ? 128 : 32, wt == T_Q8_0 ? 112 : 28, wt == T_Q8_0 ? 96 : 24};
+    // K chunk per stage.  One SM's bulk-copy engine caps row copies below
+    // ~3 KB, so the first tier takes the fewest K slices that fit a chunk of
+    // >= 96 Q8_0 blocks (32 super-blocks, or the whole slice when shorter),
+    // chunks that divide the slice first (the 16 warps of a stage stay busy);
+    // the second tier allows smaller chunks.
+    const int cq[5] = {128, 112, 96, 80, 64}, ck[2] = {32, 16};
+    const int* cand = wt == T_Q8_0 ? cq : ck;
+    const int nbig = wt == T_Q8_0 ? 3 : 1, ncand = wt == T_Q8_0 ? 5 : 2;
     bool found = false;
-    for (int ks = 1; ks <= 16 && !found; ++ks)
-        for (int i = 0; i < 3 && !found; ++i) found = dmma_layout(wt, am, M, ks, big[i], smem_max, pl);
-    for (int ks = 1; ks <= 16 && !found; ++ks) found = dmma_layout(wt, am, M, ks, wt == T_Q8_0 ? 32 : 8, smem_max, pl);
+    for (int ks = 1; ks <= 16 && !found; ++ks) {
+        const int su = (p.units + ks - 1) / ks;
+        for (int pass = 0; pass < 2 && !found; ++pass)
+            for (int i = 0; i < nbig && !found; ++i) {
+                const int u = cand[i] < su ? cand[i] : su;
+                if ((su % u == 0) == (pass == 0)) found = dmma_layout(wt, am, M, pl.nb, ks, u, smem_max, pl);
+            }
+    }
+    for (int ks = 1; ks <= 16 && !found; ++ks) {
+        const int su = (p.units + ks - 1) / ks;
+        for (int i = nbig; i < ncand && !found; ++i) {
+            const int u = cand[i] < su ? cand[i] : su;
+            if (su % u == 0) found = dmma_layout(wt, am, M, pl.nb, ks, u, smem_max, pl);
+        }
+    }
+    for (int ks = 1; ks <= 16 && !found; ++ks) found = dmma_layout(wt, am, M, pl.nb, ks, wt == T_Q8_0 ? 32 : 8, smem_max, pl);
     if (!found) return false;
     int per = sm_count / p.kslices;
     if (per < 1) per = 1;
     if (per > p.ntiles) per = p.ntiles;
     p.per_slice = per;
     pl.grid = per * p.kslices;
-    pl.workspace = p.kslices > 1 ? (size_t)p.kslices * M * N * 4 : 0;
+    pl.ext_bytes = 0;
+    if (ext_ok && p.total_bytes >= kDmmaExtMinBytes) {
+        auto r256 = [](long long v) { return (v + 255) / 256 * 256; };
+        p.ext_codes = 0;
+        long long off = r256(am == A_INT8 ? M * K : 2 * M * K * 2);
+        p.ext_scale = off;
+        off = r256(off + (long long)p.units * p.sstride * 4);
+        p.ext_aux = off;
+        if (wt == T_Q4_K) off = r256(off + (long long)p.units * 256);
+        pl.ext_bytes = (size_t)off;
+    }
+    pl.workspace = pl.ext_bytes + (p.kslices > 1 ? (size_t)p.kslices * M * N * 4 : 0);
     out = pl;
     return true;
 }

@@ -180,18 +180,28 @@ inline unsigned grid_for(long long n, int block) { return (unsigned)((n + block 
 
 // y[i] = sum over K slices s = 0..ks-1 of partial[s][i], in slice order.
 __global__ void splitk_reduce_kernel(const float* __restrict__ partial, long long n, int ks, float* __restrict__ y) {
+    grid_dep_wait();  // launched while the split kernel runs: wait for its partial sums
     const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= n) return;
     float v = 0.0f;
-    for (int s = 0; s < ks; ++s) v += __ldg(partial + (long long)s * n + i);
+    for (int s = 0; s < ks; ++s) v += partial[(long long)s * n + i];
     y[i] = v;
 }
 
 }  // namespace
 
 cudaError_t launch_splitk_reduce(const float* partial, long long n, int ks, float* y, cudaStream_t s) {
-    splitk_reduce_kernel<<<grid_for(n, 256), 256, 0, s>>>(partial, n, ks, y);
-    return cudaGetLastError();
+    // programmatic dependent launch: scheduled while the split kernel still runs
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid_for(n, 256));
+    cfg.blockDim = dim3(256);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, splitk_reduce_kernel, partial, n, ks, y);
 }
 
 cudaError_t launch_quantize(int type, const float* x, long long rows, long long K, void* out, cudaStream_t s) {
