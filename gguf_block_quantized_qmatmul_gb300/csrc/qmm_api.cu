@@ -68,7 +68,7 @@ qmm_status stream_call(qmm_type wtype, int am, int epi, const void* wq, const fl
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     GemvPlan gp;
     DmmaPlan dp;
-    if (am == A_INT8 && M <= kGemvMaxM && plan_gemv(wt, M, N, K, sms, smem, gp)) {  // decode: whole-row weight stream
+    if (am == A_INT8 && wt == T_Q8_0 && M <= kGemvMaxM && plan_gemv(wt, M, N, K, sms, smem, gp)) {  // decode: whole-row weight stream
         gp.p.wq = static_cast<const uint8_t*>(wq);
         gp.p.x = x;
         gp.p.y = y;
@@ -195,7 +195,7 @@ size_t qmm_matmul_workspace(qmm_type wtype, qmm_act_mode mode, int64_t M, int64_
     if (device_info(nullptr, &sms, &smem) != cudaSuccess) return 0;
     const int wt = wtype == QMM_Q8_0 ? T_Q8_0 : T_Q4_K;
     GemvPlan gp;
-    if (mode == QMM_INT8_ACT && M <= kGemvMaxM && plan_gemv(wt, M, N, K, sms, smem, gp)) return 0;
+    if (mode == QMM_INT8_ACT && wt == T_Q8_0 && M <= kGemvMaxM && plan_gemv(wt, M, N, K, sms, smem, gp)) return 0;
     DmmaPlan dp;
     if (M <= kDecodeMaxM && plan_dmma(wt, mode == QMM_INT8_ACT ? A_INT8 : A_F32, M, N, K, sms, smem, dp))
         return dp.workspace;

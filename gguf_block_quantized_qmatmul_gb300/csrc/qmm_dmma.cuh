@@ -739,9 +739,13 @@ struct DmmaPlan {
 // them inside the single decode launch.
 constexpr long long kDmmaExtMinBytes = 32ll << 20;
 
+// The planner first looks for a chunk size that leaves this many stages.
+constexpr int kDmmaPreferStages = 2;
+
 // Shared-memory layout for K split in `ks` slices and `ups` units per stage;
 // false when fewer than two stages fit.
-inline bool dmma_layout(int wt, int am, long long M, int nb, int ks, int ups, int smem_max, DmmaPlan& pl) {
+inline bool dmma_layout(int wt, int am, long long M, int nb, int ks, int ups, int smem_max, DmmaPlan& pl,
+                        int min_stages = 2) {
     DmmaParams& p = pl.p;
     const int uv = wt == T_Q8_0 ? 32 : 256, ub = wt == T_Q8_0 ? 34 : 144;
     const int su = (p.units + ks - 1) / ks;
@@ -785,7 +789,7 @@ inline bool dmma_layout(int wt, int am, long long M, int nb, int ks, int ups, in
     }
     sb = (sb + 127) / 128 * 128;
     const long long stages = (smem_max - off) / sb;
-    if (stages < 2) return false;
+    if (stages < min_stages) return false;
     p.kslices = ks;
     p.slice_units = su;
     p.ups = ups;
@@ -811,21 +815,24 @@ inline bool plan_dmma(int wt, int am, long long M, long long N, long long K, int
     pl.nb = (am == A_F32 && M > 4) ? 2 : 1;
     // K chunk per stage.  One SM's bulk-copy engine caps row copies below
     // ~3 KB, so the first tier takes the fewest K slices that fit a chunk of
-    // >= 96 Q8_0 blocks (32 super-blocks, or the whole slice when shorter),
+    // >= 96 Q8_0 blocks (32 super-blocks; a shorter K as one chunk, unsplit),
     // chunks that divide the slice first (the 16 warps of a stage stay busy);
-    // the second tier allows smaller chunks.
+    // the second tier allows smaller chunks, again with the fewest slices.
     const int cq[5] = {128, 112, 96, 80, 64}, ck[2] = {32, 16};
     const int* cand = wt == T_Q8_0 ? cq : ck;
     const int nbig = wt == T_Q8_0 ? 3 : 1, ncand = wt == T_Q8_0 ? 5 : 2;
+    const int minbig = cand[nbig - 1];
     bool found = false;
-    for (int ks = 1; ks <= 16 && !found; ++ks) {
-        const int su = (p.units + ks - 1) / ks;
-        for (int pass = 0; pass < 2 && !found; ++pass)
-            for (int i = 0; i < nbig && !found; ++i) {
-                const int u = cand[i] < su ? cand[i] : su;
-                if ((su % u == 0) == (pass == 0)) found = dmma_layout(wt, am, M, pl.nb, ks, u, smem_max, pl);
-            }
-    }
+    for (int minst = kDmmaPreferStages; minst >= 2 && !found; --minst)
+        for (int ks = 1; ks <= 16 && !found; ++ks) {
+            const int su = (p.units + ks - 1) / ks;
+            if (ks > 1 && 3 * su < 2 * minbig) break;  // slices too short for a full chunk
+            for (int pass = 0; pass < 2 && !found; ++pass)
+                for (int i = 0; i < nbig && !found; ++i) {
+                    const int u = cand[i] < su ? cand[i] : su;
+                    if ((su % u == 0) == (pass == 0)) found = dmma_layout(wt, am, M, pl.nb, ks, u, smem_max, pl, minst);
+                }
+        }
     for (int ks = 1; ks <= 16 && !found; ++ks) {
         const int su = (p.units + ks - 1) / ks;
         for (int i = nbig; i < ncand && !found; ++i) {
@@ -833,7 +840,6 @@ inline bool plan_dmma(int wt, int am, long long M, long long N, long long K, int
             if (su % u == 0) found = dmma_layout(wt, am, M, pl.nb, ks, u, smem_max, pl);
         }
     }
-    for (int ks = 1; ks <= 16 && !found; ++ks) found = dmma_layout(wt, am, M, pl.nb, ks, wt == T_Q8_0 ? 32 : 8, smem_max, pl);
     if (!found) return false;
     int per = sm_count / p.kslices;
     if (per < 1) per = 1;

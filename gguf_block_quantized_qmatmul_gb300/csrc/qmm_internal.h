@@ -22,10 +22,10 @@ cudaError_t launch_dmma_prep(int wt, int am, const DmmaPlan& plan, void* ext, cu
 cudaError_t launch_prefill(int am, const PrefillPlan& plan, const void* wq, const float* x, void* ws, int smem_max,
                            cudaStream_t s);
 
-// largest activation batch served by the per-thread dp4a GEMV (int8_act);
-// larger decode batches (and every f32_act decode batch up to 8) use the
-// 16-row-tile tensor-core kernel
-constexpr int kGemvMaxM = 4;
+// largest activation batch served by the per-thread dp4a GEMV (int8_act,
+// Q8_0 weights only); larger decode batches, Q4_K weights and every f32_act
+// decode batch up to 8 use the 16-row-tile tensor-core kernel
+constexpr int kGemvMaxM = 1;
 constexpr int kDecodeMaxM = 8;
 
 // Raise a kernel's dynamic shared-memory limit once per device.
