@@ -31,7 +31,8 @@ STATUS = {0: "QMM_OK", 1: "QMM_ERR_NULL", 2: "QMM_ERR_SHAPE", 3: "QMM_ERR_TYPE",
 
 # every symbol declared in include/qmm.h
 EXPORTS = ["qmm_block_values", "qmm_block_bytes", "qmm_row_bytes", "qmm_quantize_weights", "qmm_quantize_act",
-           "qmm_dequantize", "qmm_matmul_workspace", "qmm_matmul", "qmm_matmul_static_workspace", "qmm_block_sums",
+           "qmm_dequantize", "qmm_matmul_workspace", "qmm_matmul_launches", "qmm_matmul", "qmm_matmul_static_workspace",
+           "qmm_block_sums",
            "qmm_last_device_error", "qmm_status_string"]
 
 
@@ -55,6 +56,7 @@ def _load() -> ctypes.CDLL:
     lib.qmm_quantize_act.argtypes, lib.qmm_quantize_act.restype = [i32, p, i64, i64, p, p], i32
     lib.qmm_dequantize.argtypes, lib.qmm_dequantize.restype = [i32, p, i64, i64, p, p], i32
     lib.qmm_matmul_workspace.argtypes, lib.qmm_matmul_workspace.restype = [i32, i32, i64, i64, i64], sz
+    lib.qmm_matmul_launches.argtypes, lib.qmm_matmul_launches.restype = [i32, i32, i64, i64, i64], i32
     lib.qmm_matmul.argtypes, lib.qmm_matmul.restype = [i32, i32, p, p, p, i64, i64, i64, p, sz, p], i32
     lib.qmm_block_sums.argtypes, lib.qmm_block_sums.restype = [i32, p, p, i64, i64, i64, p, p], i32
     lib.qmm_last_device_error.argtypes, lib.qmm_last_device_error.restype = [], i32
@@ -134,6 +136,11 @@ def dequantize(q: torch.Tensor, t, K: int, out: torch.Tensor | None = None, stre
 
 def matmul_workspace(wtype, mode, M: int, N: int, K: int) -> int:
     return int(_lib().qmm_matmul_workspace(_t(wtype), _m(mode), M, N, K))
+
+
+def matmul_launches(wtype, mode, M: int, N: int, K: int) -> int:
+    """Kernel launches of one matmul call for this shape (a diagnostic)."""
+    return int(_lib().qmm_matmul_launches(_t(wtype), _m(mode), M, N, K))
 
 
 def matmul(wq: torch.Tensor, x: torch.Tensor, wtype, mode, N: int | None = None, out: torch.Tensor | None = None,

@@ -19,7 +19,7 @@ int g_sm_count[kMaxDev];
 int g_smem_optin[kMaxDev];
 
 // Per-device constants: error-word address, SM count, opt-in shared memory.
-cudaError_t device_info(unsigned** err, int* sms, int* smem) {
+cudaError_t device_info(unsigned** err, int* sms, int* smem, int* device = nullptr) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -37,6 +37,7 @@ cudaError_t device_info(unsigned** err, int* sms, int* smem) {
     if (err) *err = g_err_ptr[dev];
     if (sms) *sms = g_sm_count[dev];
     if (smem) *smem = g_smem_optin[dev];
+    if (device) *device = dev;
     return cudaSuccess;
 }
 
@@ -59,16 +60,77 @@ size_t workspace_for(const StreamPlan& pl) {
     return round_up_sz((size_t)pl.p.kslices * pl.p.M * pl.p.N * 4, 256) + (size_t)pl.p.mchunks * pl.p.ntiles * 4;
 }
 
+// The kernel a matmul call dispatches to and its plan.  Planning searches
+// chunk sizes and K splits, so decisions are cached per host thread by
+// (device, type, form, epilogue, M, N, K).
+enum Kind { KIND_NONE, KIND_GEMV, KIND_DMMA, KIND_PREFILL, KIND_STREAM };
+struct Dispatch {
+    Kind kind = KIND_NONE;
+    GemvPlan gp;
+    DmmaPlan dp;
+    PrefillPlan fp;
+    StreamPlan sp;
+    size_t workspace = 0;
+    int launches = 0;
+};
+
+void plan_dispatch(int wt, int am, int epi, long long M, long long N, long long K, int sms, int smem, Dispatch& d) {
+    d = Dispatch();
+    if (am == A_INT8 && wt == T_Q8_0 && M <= kGemvMaxM && plan_gemv(wt, M, N, K, sms, smem, d.gp)) {  // decode: whole-row weight stream
+        d.kind = KIND_GEMV;
+        d.launches = 1;
+    } else if (M <= kDecodeMaxM && plan_dmma(wt, am, M, N, K, sms, smem, d.dp, epi == E_Y)) {  // decode on 16-row tensor-core tiles
+        d.kind = KIND_DMMA;
+        d.workspace = d.dp.workspace;
+        d.launches = 1 + (d.dp.ext_bytes ? 1 : 0) + (epi == E_Y && d.dp.p.kslices > 1 ? 1 : 0);
+    } else if (epi == E_Y && plan_prefill(wt, am, M, N, K, sms, smem, d.fp)) {  // prefill: f16 tensor-core GEMM
+        d.kind = KIND_PREFILL;
+        d.workspace = d.fp.workspace;
+        d.launches = 2;  // activation operand, GEMM
+    } else if (plan_stream(wt, am, epi, M, N, K, sms, smem, d.sp)) {
+        d.kind = KIND_STREAM;
+        d.workspace = epi == E_Y ? workspace_for(d.sp) : 0;
+        d.launches = 1;
+    }
+}
+
+struct CachedDispatch {
+    bool used = false;
+    int dev = -1, wt = 0, am = 0, epi = 0;
+    long long M = 0, N = 0, K = 0;
+    Dispatch d;
+};
+constexpr int kPlanCache = 16;
+thread_local CachedDispatch t_plans[kPlanCache];
+thread_local int t_plan_next = 0;
+
+const Dispatch& get_dispatch(int dev, int wt, int am, int epi, long long M, long long N, long long K, int sms, int smem) {
+    for (const CachedDispatch& c : t_plans)
+        if (c.used && c.dev == dev && c.wt == wt && c.am == am && c.epi == epi && c.M == M && c.N == N && c.K == K) return c.d;
+    CachedDispatch& c = t_plans[t_plan_next];
+    t_plan_next = (t_plan_next + 1) % kPlanCache;
+    c.used = true;
+    c.dev = dev;
+    c.wt = wt;
+    c.am = am;
+    c.epi = epi;
+    c.M = M;
+    c.N = N;
+    c.K = K;
+    plan_dispatch(wt, am, epi, M, N, K, sms, smem, c.d);
+    return c.d;
+}
+
 qmm_status stream_call(qmm_type wtype, int am, int epi, const void* wq, const float* x, float* y, int32_t* sums,
                        int64_t M, int64_t N, int64_t K, void* ws, size_t ws_bytes, qmm_stream_t stream) {
     unsigned* err = nullptr;
-    int sms = 0, smem = 0;
-    if (device_info(&err, &sms, &smem) != cudaSuccess) return QMM_ERR_CUDA;
+    int sms = 0, smem = 0, dev = 0;
+    if (device_info(&err, &sms, &smem, &dev) != cudaSuccess) return QMM_ERR_CUDA;
     const int wt = wtype == QMM_Q8_0 ? T_Q8_0 : T_Q4_K;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    GemvPlan gp;
-    DmmaPlan dp;
-    if (am == A_INT8 && wt == T_Q8_0 && M <= kGemvMaxM && plan_gemv(wt, M, N, K, sms, smem, gp)) {  // decode: whole-row weight stream
+    const Dispatch& d = get_dispatch(dev, wt, am, epi, M, N, K, sms, smem);
+    if (d.kind == KIND_GEMV) {
+        GemvPlan gp = d.gp;
         gp.p.wq = static_cast<const uint8_t*>(wq);
         gp.p.x = x;
         gp.p.y = y;
@@ -77,7 +139,8 @@ qmm_status stream_call(qmm_type wtype, int am, int epi, const void* wq, const fl
         const cudaError_t e = wt == T_Q8_0 ? launch_gemv_q8_0(epi, gp, smem, s) : launch_gemv_q4_k(epi, gp, smem, s);
         return e == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
     }
-    if (M <= kDecodeMaxM && plan_dmma(wt, am, M, N, K, sms, smem, dp, epi == E_Y)) {  // decode on 16-row tensor-core tiles
+    if (d.kind == KIND_DMMA) {
+        DmmaPlan dp = d.dp;
         dp.p.wq = static_cast<const uint8_t*>(wq);
         dp.p.x = x;
         dp.p.y = y;
@@ -96,15 +159,15 @@ qmm_status stream_call(qmm_type wtype, int am, int epi, const void* wq, const fl
         if (split && launch_splitk_reduce(dp.p.partial, M * N, dp.p.kslices, y, s) != cudaSuccess) return QMM_ERR_CUDA;
         return QMM_OK;
     }
-    PrefillPlan fp;
-    if (epi == E_Y && plan_prefill(wt, am, M, N, K, sms, smem, fp)) {  // prefill: f16 tensor-core GEMM
+    if (d.kind == KIND_PREFILL) {
+        PrefillPlan fp = d.fp;
         fp.p.y = y;
         fp.p.err = err;
         if (!ws || ws_bytes < fp.workspace) return QMM_ERR_WORKSPACE;
         return launch_prefill(am, fp, wq, x, ws, smem, s) == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
     }
-    StreamPlan pl;
-    if (!plan_stream(wt, am, epi, M, N, K, sms, smem, pl)) return QMM_ERR_SHAPE;
+    if (d.kind != KIND_STREAM) return QMM_ERR_SHAPE;
+    StreamPlan pl = d.sp;
     pl.p.wq = static_cast<const uint8_t*>(wq);
     pl.p.x = x;
     pl.p.y = y;
@@ -187,25 +250,40 @@ qmm_status qmm_dequantize(qmm_type t, const void* q, int64_t rows, int64_t K, fl
                                                                                                           : QMM_ERR_CUDA;
 }
 
+}  // extern "C"
+
+namespace {
+// The dispatch of qmm_matmul for a shape, without launching anything:
+// workspace bytes and the number of kernel launches (0 launches: invalid).
+void dispatch_info(qmm_type wtype, qmm_act_mode mode, int64_t M, int64_t N, int64_t K, size_t* ws, int* launches) {
+    *ws = 0;
+    *launches = 0;
+    if (wtype != QMM_Q8_0 && wtype != QMM_Q4_K) return;
+    if (mode != QMM_INT8_ACT && mode != QMM_F32_ACT) return;
+    if (check_shape(wtype, N, K) != QMM_OK || M <= 0 || M > INT32_MAX || N == 0 || K == 0) return;
+    int sms = 0, smem = 0, dev = 0;
+    if (device_info(nullptr, &sms, &smem, &dev) != cudaSuccess) return;
+    const Dispatch& d = get_dispatch(dev, wtype == QMM_Q8_0 ? T_Q8_0 : T_Q4_K, mode == QMM_INT8_ACT ? A_INT8 : A_F32, E_Y,
+                                     M, N, K, sms, smem);
+    *ws = d.workspace;
+    *launches = d.launches;
+}
+}  // namespace
+
+extern "C" {
+
 size_t qmm_matmul_workspace(qmm_type wtype, qmm_act_mode mode, int64_t M, int64_t N, int64_t K) {
-    if (wtype != QMM_Q8_0 && wtype != QMM_Q4_K) return 0;
-    if (mode != QMM_INT8_ACT && mode != QMM_F32_ACT) return 0;
-    if (check_shape(wtype, N, K) != QMM_OK || M <= 0 || M > INT32_MAX || N == 0 || K == 0) return 0;
-    int sms = 0, smem = 0;
-    if (device_info(nullptr, &sms, &smem) != cudaSuccess) return 0;
-    const int wt = wtype == QMM_Q8_0 ? T_Q8_0 : T_Q4_K;
-    GemvPlan gp;
-    if (mode == QMM_INT8_ACT && wt == T_Q8_0 && M <= kGemvMaxM && plan_gemv(wt, M, N, K, sms, smem, gp)) return 0;
-    DmmaPlan dp;
-    if (M <= kDecodeMaxM && plan_dmma(wt, mode == QMM_INT8_ACT ? A_INT8 : A_F32, M, N, K, sms, smem, dp))
-        return dp.workspace;
-    PrefillPlan fp;
-    if (plan_prefill(wt, mode == QMM_INT8_ACT ? A_INT8 : A_F32, M, N, K, sms, smem, fp)) return fp.workspace;
-    StreamPlan pl;
-    if (!plan_stream(wtype == QMM_Q8_0 ? T_Q8_0 : T_Q4_K, mode == QMM_INT8_ACT ? A_INT8 : A_F32, E_Y, M, N, K, sms,
-                     smem, pl))
-        return 0;
-    return workspace_for(pl);
+    size_t ws;
+    int n;
+    dispatch_info(wtype, mode, M, N, K, &ws, &n);
+    return ws;
+}
+
+int qmm_matmul_launches(qmm_type wtype, qmm_act_mode mode, int64_t M, int64_t N, int64_t K) {
+    size_t ws;
+    int n;
+    dispatch_info(wtype, mode, M, N, K, &ws, &n);
+    return n;
 }
 
 qmm_status qmm_matmul(qmm_type wtype, qmm_act_mode mode, const void* wq, const float* x, float* y, int64_t M,

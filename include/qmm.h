@@ -111,8 +111,17 @@ qmm_status qmm_dequantize(qmm_type t, const void* q, int64_t rows, int64_t K, fl
                           qmm_stream_t stream);
 
 /* Workspace bytes qmm_matmul needs for this shape (0 when none).  The
-   workspace holds split-K partial sums and their arrival counters. */
+   workspace holds activations prepared once per call for large decode
+   weight matrices, split-K partial sums and their arrival counters, and the
+   prefill GEMM's activation operand. */
 size_t qmm_matmul_workspace(qmm_type wtype, qmm_act_mode mode, int64_t M, int64_t N, int64_t K);
+
+/* Number of kernel launches one qmm_matmul call makes for this shape on the
+   current device (decode: an activation-preparing kernel for large weight
+   matrices, the decode kernel, a K-split reduction; prefill: the activation
+   operand and the GEMM).  0 for an invalid shape or type.  Launches nothing.
+   (A diagnostic of this library; the pages have no counterpart.) */
+int qmm_matmul_launches(qmm_type wtype, qmm_act_mode mode, int64_t M, int64_t N, int64_t K);
 
 /* y [M, N] f32 = x [M, K] f32 . W^T with W given as quantized blocks wq
    (wtype QMM_Q8_0 or QMM_Q4_K).

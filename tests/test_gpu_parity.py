@@ -184,6 +184,18 @@ def test_one_hot_f32_act_is_exact(qmm, orc):
             assert np.array_equal(y[i], W[:, k])
 
 
+def test_launch_counts(qmm):
+    """qmm_matmul_launches mirrors the dispatch (decode: optional activation
+    preparation + decode kernel + optional K-split reduction)."""
+    assert qmm.matmul_launches("q8_0", "int8_act", 1, 100, 8192) == 1     # per-thread GEMV
+    assert qmm.matmul_launches("q8_0", "f32_act", 1, 100, 8192) == 1      # small: prepared in-kernel
+    assert qmm.matmul_launches("q8_0", "f32_act", 1, 28672, 8192) == 2    # large: preparing kernel first
+    assert qmm.matmul_launches("q4_k", "int8_act", 8, 28672, 8192) == 2
+    assert qmm.matmul_launches("q8_0", "f32_act", 8, 28672, 8192) == 3    # K split: reduction after
+    assert qmm.matmul_launches("q8_0", "int8_act", 256, 4096, 4096) == 2  # prefill: operand + GEMM
+    assert qmm.matmul_launches("q8_0", "int8_act", 1, 100, 100) == 0      # K not a multiple of 32
+
+
 def test_error_statuses_on_device(qmm, orc):
     wq = dev(orc.quantize("q8_0", qmm_synth.weights(100, 8192)))
     x = dev(qmm_synth.activations(8, 8192))
