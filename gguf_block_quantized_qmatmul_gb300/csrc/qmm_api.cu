@@ -63,11 +63,12 @@ size_t workspace_for(const StreamPlan& pl) {
 // The kernel a matmul call dispatches to and its plan.  Planning searches
 // chunk sizes and K splits, so decisions are cached per host thread by
 // (device, type, form, epilogue, M, N, K).
-enum Kind { KIND_NONE, KIND_GEMV, KIND_DMMA, KIND_PREFILL, KIND_STREAM };
+enum Kind { KIND_NONE, KIND_GEMV, KIND_DMMA, KIND_TC, KIND_PREFILL, KIND_STREAM };
 struct Dispatch {
     Kind kind = KIND_NONE;
     GemvPlan gp;
     DmmaPlan dp;
+    TcPlan tp;
     PrefillPlan fp;
     StreamPlan sp;
     size_t workspace = 0;
@@ -83,7 +84,11 @@ void plan_dispatch(int wt, int am, int epi, long long M, long long N, long long 
         d.kind = KIND_DMMA;
         d.workspace = d.dp.workspace;
         d.launches = 1 + (d.dp.ext_bytes ? 1 : 0) + (epi == E_Y && d.dp.p.kslices > 1 ? 1 : 0);
-    } else if (epi == E_Y && plan_prefill(wt, am, M, N, K, sms, smem, d.fp)) {  // prefill: f16 tensor-core GEMM
+    } else if (epi == E_Y && plan_tc(wt, am, M, N, K, sms, smem, d.tp)) {  // prefill: tcgen05 GEMM
+        d.kind = KIND_TC;
+        d.workspace = d.tp.workspace;
+        d.launches = 2;  // operand preparation, GEMM
+    } else if (epi == E_Y && plan_prefill(wt, am, M, N, K, sms, smem, d.fp)) {  // prefill: warp-MMA GEMM
         d.kind = KIND_PREFILL;
         d.workspace = d.fp.workspace;
         d.launches = 2;  // activation operand, GEMM
@@ -158,6 +163,10 @@ qmm_status stream_call(qmm_type wtype, int am, int epi, const void* wq, const fl
         if (launch_dmma(wt, am, epi, dp, smem, s) != cudaSuccess) return QMM_ERR_CUDA;
         if (split && launch_splitk_reduce(dp.p.partial, M * N, dp.p.kslices, y, s) != cudaSuccess) return QMM_ERR_CUDA;
         return QMM_OK;
+    }
+    if (d.kind == KIND_TC) {
+        if (!ws || ws_bytes < d.tp.workspace) return QMM_ERR_WORKSPACE;
+        return launch_tc(wt, am, d.tp, wq, x, ws, y, smem, s) == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
     }
     if (d.kind == KIND_PREFILL) {
         PrefillPlan fp = d.fp;

@@ -7,6 +7,7 @@ namespace qmm {
 namespace {
 
 unsigned long long g_smem_done[2];
+unsigned long long g_tc_smem_done[2];
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -32,7 +33,58 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, unsigned
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+template <int WT, int AM>
+cudaError_t tc_go(const TcPlan& pl, const void* wq, const float* x, void* ws, float* y, int smem_max, cudaStream_t s) {
+    const TcParams& p0 = pl.p;
+    uint8_t* wsb = static_cast<uint8_t*>(ws);
+    __half* ahi = reinterpret_cast<__half*>(wsb + pl.ws_ahi);
+    __half* alo = reinterpret_cast<__half*>(wsb + pl.ws_alo);
+    float* ais = reinterpret_cast<float*>(wsb + pl.ws_ais);
+    float* wis = reinterpret_cast<float*>(wsb + pl.ws_wis);
+    // 1. operand preparation: activation pieces, row scales of both operands
+    const unsigned pblocks = (unsigned)(p0.M + (p0.N + kTcPrepThreads / 32 - 1) / (kTcPrepThreads / 32));
+    tc_prep_kernel<WT, AM><<<pblocks, kTcPrepThreads, 0, s>>>(x, static_cast<const uint8_t*>(wq), p0.M, p0.N, p0.K, ahi,
+                                                              alo, ais, wis);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    // 2. tensor maps: raw weight rows as uint16, activation pieces (128-byte swizzle)
+    CUtensorMap tw, tah, tal;
+    const unsigned long long rb = (unsigned long long)p0.K / (WT == T_Q8_0 ? 32 : 256) * (WT == T_Q8_0 ? 34 : 144);
+    if (!make_map(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT16, wq, rb / 2, p0.N, rb, p0.raw_row / 2, kTcBN, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_map(&tah, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, ahi, p0.K, p0.M, (unsigned long long)p0.K * 2, kTcBK, kTcBM,
+                  CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&tal, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, alo, p0.K, p0.M, (unsigned long long)p0.K * 2, kTcBK, kTcBM,
+                  CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    TcParams p = p0;
+    p.y = y;
+    p.ais = ais;
+    p.wis = wis;
+    // 3. the GEMM, a programmatic dependent of the preparation
+    auto* k = qmm_tc_kernel<WT>;
+    e = ensure_smem(k, smem_max, g_tc_smem_done[WT == T_Q8_0 ? 0 : 1]);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)pl.grid);
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = pl.smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k, tw, tah, tal, p);
+}
+
 }  // namespace
+
+cudaError_t launch_tc(int wt, int am, const TcPlan& plan, const void* wq, const float* x, void* ws, float* y, int smem_max,
+                      cudaStream_t s) {
+    if (wt == T_Q8_0) return am == A_INT8 ? tc_go<T_Q8_0, A_INT8>(plan, wq, x, ws, y, smem_max, s)
+                                          : tc_go<T_Q8_0, A_F32>(plan, wq, x, ws, y, smem_max, s);
+    return am == A_INT8 ? tc_go<T_Q4_K, A_INT8>(plan, wq, x, ws, y, smem_max, s) : tc_go<T_Q4_K, A_F32>(plan, wq, x, ws, y, smem_max, s);
+}
 
 cudaError_t launch_prefill(int am, const PrefillPlan& pl, const void* wq, const float* x, void* ws, int smem_max,
                            cudaStream_t s) {

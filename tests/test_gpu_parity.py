@@ -120,6 +120,8 @@ MATMUL_CASES = [
     ("q4_k", 37, 64, 4096),
     ("q8_0", 64, 33, 1024),
     ("q4_k", 100, 48, 1024),
+    ("q8_0", 300, 260, 2048),     # prefill tiles: 3 x 3 with ragged edges in both
+    ("q4_k", 200, 300, 1024),
 ]
 
 
@@ -132,6 +134,21 @@ def test_matmul_within_bound(qmm, orc, wtype, M, N, K, mode):
     y = host(qmm.matmul(dev(wq), dev(x), wtype, mode, N=N))
     y_orc, T = orc.matmul(wtype, mode, wq, x)
     assert_within_bound(y, y_orc, T, f"{wtype} {mode} M{M} N{N} K{K}")
+    check_device_error(qmm)
+
+
+@pytest.mark.parametrize("mode", ["int8_act", "f32_act"])
+@pytest.mark.parametrize("wtype,K", [("q8_0", 1024), ("q4_k", 1024)])
+def test_prefill_special_rows(qmm, orc, wtype, K, mode):
+    """Prefill (M > 8) with the adversarial rows in both operands: zeros,
+    constants, one-hot, ties, magnitudes from 1e-9 to 3e3 (each operand row is
+    scaled by its own power of two before the f16 split)."""
+    w = np.concatenate([qmm_synth.weights(100, K, seed=5), qmm_synth.special_block_rows(K)])
+    x = np.concatenate([qmm_synth.activations(20, K, seed=6, outlier_channels=4), qmm_synth.special_block_rows(K)])
+    wq = orc.quantize(wtype, w)
+    y = host(qmm.matmul(dev(wq), dev(x), wtype, mode, N=w.shape[0]))
+    y_orc, T = orc.matmul(wtype, mode, wq, x)
+    assert_within_bound(y, y_orc, T, f"{wtype} {mode} special rows")
     check_device_error(qmm)
 
 
