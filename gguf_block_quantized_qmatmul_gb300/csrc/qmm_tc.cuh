@@ -16,17 +16,25 @@
 // hi.hi + hi.lo + lo.hi (the dropped lo.lo is below 2^-22 relative), all into
 // one f32 accumulator, and the epilogue multiplies by 2^-(s_row + s_col).
 //
-// One persistent CTA per SM, 128 x 128 output tiles, 14 warps:
+// One persistent CTA per SM, 128 x 128 output tiles (128 weight rows x 128
+// activation rows), 14 warps:
 //   producer  TMA: raw weight rows (2-D box, 128 rows x 272 B = 8 Q8_0 blocks,
 //             or 144 B = 1 Q4_K super-block, per 256 K) and the activation
 //             pieces (128 rows x 64 f16, 128-byte swizzle, per 64 K);
-//   MMA       one thread issues tcgen05.mma (M 128, N 128, K 16; 12 per 64 K)
-//             into one of two TMEM accumulators (2 x 128 columns), commits to
-//             mbarriers that free the stage or hand the tile to the epilogue;
 //   converter 8 warps dequantize the raw weight bytes of each 64-K stage into
-//             the two f16 pieces, written in the 128-byte-swizzled K-major
-//             layout the MMA descriptors address;
-//   epilogue  4 warps, one TMEM lane quarter each, tcgen05.ld -> scale -> y.
+//             the two f16 pieces and write them straight into tensor memory
+//             (tcgen05.st): the weights are the MMA's A operand, read from
+//             TMEM, so the three passes re-read only the activation pieces
+//             from shared memory (shared-memory bandwidth, which the operand
+//             reads and the converters' traffic share, bounded an earlier
+//             layout with both operands in shared memory);
+//   MMA       one thread issues tcgen05.mma (M 128 weight rows, N 128
+//             activation rows, K 16; 12 per 64 K) into one of two TMEM
+//             accumulators, commits to mbarriers that free the stage or hand
+//             the tile to the epilogue;
+//   epilogue  4 warps, one TMEM lane quarter (32 weight rows) each:
+//             tcgen05.ld, scale, y stores coalesced along N.
+// TMEM: 2 accumulators x 128 columns + 4 stages x 64 columns of weight pieces.
 #pragma once
 
 #include <cuda.h>
@@ -40,13 +48,16 @@ constexpr int kTcBM = 128;   // activation rows per tile (MMA M)
 constexpr int kTcBN = 128;   // weight rows per tile (MMA N)
 constexpr int kTcBK = 64;    // K per MMA stage
 constexpr int kTcRK = 256;   // K per raw weight stage
-constexpr int kTcMS = 2;     // MMA stages
+constexpr int kTcMS = 4;     // MMA stages
 constexpr int kTcRS = 2;     // raw weight stages
 constexpr int kTcConvWarps = 8;
 constexpr int kTcEpiWarps = 4;
 constexpr int kTcThreads = (2 + kTcEpiWarps + kTcConvWarps) * 32;
-constexpr int kTcStageBytes = 4 * kTcBM * kTcBK * 2;  // A hi, A lo, B hi, B lo: 64 KB
-constexpr int kTcTmemCols = 256;
+constexpr int kTcPiece = kTcBM * kTcBK * 2;      // one activation piece of a stage: 16 KB
+constexpr int kTcStageBytes = 2 * kTcPiece;      // activation hi, lo: 32 KB
+constexpr int kTcTmemCols = 512;                 // 2 x 128 accumulator columns + 4 x 64 weight-piece columns
+constexpr int kTcWCol0 = 2 * kTcBN;              // first TMEM column of the weight pieces
+constexpr int kTcWCols = kTcBK;                  // columns per stage: hi (32) + lo (32), two f16 per column
 
 struct TcParams {
     float* y;
@@ -68,11 +79,20 @@ __device__ __forceinline__ uint64_t tc_sdesc(uint32_t addr) {
 // instruction descriptor: f32 accumulator, f16 A and B, both K-major, N = 128, M = 128
 constexpr uint32_t kTcIdesc = (1u << 4) | ((uint32_t)(kTcBN >> 3) << 17) | ((uint32_t)(kTcBM >> 4) << 24);
 
-__device__ __forceinline__ void tc_mma(uint32_t tmem, uint64_t da, uint64_t db, uint32_t accumulate) {
+// D (TMEM) += A (TMEM, 128 lanes x 16 f16) x B (shared memory)^T
+__device__ __forceinline__ void tc_mma(uint32_t tmem, uint32_t ta, uint64_t db, uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem),
-        "l"(da), "l"(db), "r"(kTcIdesc), "r"(accumulate)
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem),
+        "r"(ta), "l"(db), "r"(kTcIdesc), "r"(accumulate)
+        : "memory");
+}
+// 16 32-bit columns of this warp's TMEM lane quarter from registers
+__device__ __forceinline__ void tc_st16(uint32_t taddr, const uint32_t v[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+        "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
         : "memory");
 }
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
@@ -101,36 +121,26 @@ __device__ __forceinline__ void tc_ld32(uint32_t taddr, float v[32]) {
 __device__ __forceinline__ int tc_chunk(int r, int c) { return r * 128 + (((c ^ r) & 7) << 4); }
 
 // ---------------------------------------------------------------------------
-// weight conversion: one thread, 32 values of one weight row, scaled by 2^s,
-// as hi and lo f16 pieces into chunks 4j..4j+3 of row n of the B tiles
+// weight conversion: one thread, the 32 values of one weight row that one
+// Q8_0 block or one Q4_K sub-block holds, scaled by 2^s, as 16 words of hi
+// and 16 words of lo f16 pairs (k order natural)
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void tc_store_row32(uint8_t* bhi, uint8_t* blo, int n, int j, const uint32_t h[16],
-                                               const uint32_t l[16]) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int off = tc_chunk(n, 4 * j + i);
-        *reinterpret_cast<uint4*>(bhi + off) = make_uint4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
-        *reinterpret_cast<uint4*>(blo + off) = make_uint4(l[4 * i], l[4 * i + 1], l[4 * i + 2], l[4 * i + 3]);
-    }
-}
 
 // Q8_0 block at blk (2-byte aligned): w = ds q with ds = f(d) 2^s as f16
 // (exact while it is a normal f16); hi = f16(ds q) by one hmul2, lo = ds q - hi
 // by one hfma2 (exact: at most 8 significant bits remain)
-__device__ __forceinline__ void tc_conv_q8_0(const uint8_t* blk, float wsc, uint8_t* bhi, uint8_t* blo, int n, int j) {
+__device__ __forceinline__ void tc_conv_q8_0(const uint8_t* blk, float wsc, uint32_t h[16], uint32_t l[16]) {
     const float ds = h2f(*reinterpret_cast<const uint16_t*>(blk)) * wsc;
     const __half2 ds2 = __half2half2(__float2half_rn(ds));
     const uintptr_t a = reinterpret_cast<uintptr_t>(blk + 2);
     const uint32_t* w = reinterpret_cast<const uint32_t*>(a & ~uintptr_t(3));
     const uint32_t sh = (uint32_t)(a & 3u) * 8u;
-    uint32_t h[16], l[16];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const uint32_t word = __funnelshift_r(w[i], w[i + 1], sh) ^ 0x80808080u;  // codes 4i..4i+3, biased by 128
 #pragma unroll
         for (int p = 0; p < 2; ++p) {
-            const uint32_t sel = p ? 0x4342u : 0x4140u;  // bytes (2p, 2p+1) under 0x64: 1152 + q
-            uint32_t qb = __byte_perm(word, 0x64646464u, sel);
+            uint32_t qb = __byte_perm(word, 0x64646464u, p ? 0x4342u : 0x4140u);  // bytes (2p, 2p+1) under 0x64: 1152 + q
             const __half2 q = __hsub2(*reinterpret_cast<__half2*>(&qb), __half2half2(__ushort_as_half(0x6480)));
             const __half2 hi = __hmul2(q, ds2);
             const __half2 lo = __hfma2(q, ds2, __hneg2(hi));
@@ -138,14 +148,12 @@ __device__ __forceinline__ void tc_conv_q8_0(const uint8_t* blk, float wsc, uint
             l[2 * i + p] = *reinterpret_cast<const uint32_t*>(&lo);
         }
     }
-    tc_store_row32(bhi, blo, n, j, h, l);
 }
 
-// Q4_K sub-block jj of the super-block at sbk (16-byte aligned): w 2^s =
+// Q4_K sub-block 2 sub + j of the super-block at sbk (16-byte aligned): w 2^s =
 // fma(e 2^s, q, -o 2^s) in f32 (one rounding, as the dequantization contract),
 // split as f16(v) + f16(v - f16(v))
-__device__ __forceinline__ void tc_conv_q4_k(const uint8_t* sbk, int sub, int j, float wsc, uint8_t* bhi, uint8_t* blo,
-                                             int n) {
+__device__ __forceinline__ void tc_conv_q4_k(const uint8_t* sbk, int sub, int j, float wsc, uint32_t h[16], uint32_t l[16]) {
     const uint4 hd = *reinterpret_cast<const uint4*>(sbk);
     const int jj = 2 * sub + j;
     const float es = h2f(hd.x) * (float)q4k_sc(hd.y, hd.w, jj) * wsc;
@@ -153,7 +161,6 @@ __device__ __forceinline__ void tc_conv_q4_k(const uint8_t* sbk, int sub, int j,
     const uint4 q0 = *reinterpret_cast<const uint4*>(sbk + 16 + 32 * sub);
     const uint4 q1 = *reinterpret_cast<const uint4*>(sbk + 16 + 32 * sub + 16);
     const uint32_t qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-    uint32_t h[16], l[16];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const uint32_t nb = (qw[i] >> (4 * j)) & 0x0F0F0F0Fu;  // values 4i..4i+3 of the sub-block
@@ -168,7 +175,6 @@ __device__ __forceinline__ void tc_conv_q4_k(const uint8_t* sbk, int sub, int j,
             l[2 * i + p] = *reinterpret_cast<const uint32_t*>(&lo);
         }
     }
-    tc_store_row32(bhi, blo, n, j, h, l);
 }
 
 // ---------------------------------------------------------------------------
@@ -182,23 +188,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint8_t* sm = smraw + ((1024 - (smem_u32(smraw) & 1023)) & 1023);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + p.off_bar);
-    uint64_t* a_full = bars;                 // [kTcMS] activation pieces landed (TMA)
-    uint64_t* b_full = bars + 2;             // [kTcMS] weight pieces written (converters)
-    uint64_t* m_empty = bars + 4;            // [kTcMS] stage consumed by the MMAs (commit)
-    uint64_t* r_full = bars + 6;             // [kTcRS] raw weight rows landed (TMA)
-    uint64_t* r_empty = bars + 8;            // [kTcRS] raw stage converted
-    uint64_t* acc_full = bars + 10;          // [2] accumulator complete (commit)
-    uint64_t* acc_empty = bars + 12;         // [2] accumulator read (epilogue)
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + p.off_bar + 128);
-    volatile int* flags = reinterpret_cast<volatile int*>(sm + p.off_bar + 192);
+    uint64_t* x_full = bars;                            // [kTcMS] activation pieces landed (TMA)
+    uint64_t* w_full = bars + kTcMS;                    // [kTcMS] weight pieces in TMEM (converter warps)
+    uint64_t* m_empty = bars + 2 * kTcMS;               // [kTcMS] stage consumed by the MMAs (commit)
+    uint64_t* r_full = bars + 3 * kTcMS;                // [kTcRS] raw weight rows landed (TMA)
+    uint64_t* r_empty = bars + 3 * kTcMS + kTcRS;       // [kTcRS] raw stage converted
+    uint64_t* acc_full = bars + 3 * kTcMS + 2 * kTcRS;  // [2] accumulator complete (commit)
+    uint64_t* acc_empty = acc_full + 2;                 // [2] accumulator read (epilogue)
+    static_assert((3 * kTcMS + 2 * kTcRS + 4) * 8 <= 256, "mbarriers overlap the TMEM slot");
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + p.off_bar + 256);
+    volatile int* flags = reinterpret_cast<volatile int*>(sm + p.off_bar + 320);
     const int kt_n = p.K / kTcBK;
     if (tid == 0) {
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(smem_u32(&a_full[i]), 1);
-            mbar_init(smem_u32(&b_full[i]), kTcConvWarps * 32);
+        for (int i = 0; i < kTcMS; ++i) {
+            mbar_init(smem_u32(&x_full[i]), 1);
+            mbar_init(smem_u32(&w_full[i]), kTcConvWarps);
             mbar_init(smem_u32(&m_empty[i]), 1);
+        }
+        for (int i = 0; i < kTcRS; ++i) {
             mbar_init(smem_u32(&r_full[i]), 1);
-            mbar_init(smem_u32(&r_empty[i]), kTcConvWarps * 32);
+            mbar_init(smem_u32(&r_empty[i]), kTcConvWarps);
+        }
+        for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&acc_full[i]), 1);
             mbar_init(smem_u32(&acc_empty[i]), kTcEpiWarps * 32);
         }
@@ -217,8 +228,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t tmem = *tslot;
     grid_dep_wait();  // the operand-preparing grid has completed
 
-    auto stage = [&](int s) { return sm + s * kTcStageBytes; };  // A hi | A lo | B hi | B lo, 16 KB each
+    auto stage = [&](int s) { return sm + s * kTcStageBytes; };  // activation hi | lo, 16 KB each
     auto raw = [&](int s) { return sm + p.off_raw + s * p.raw_stage; };
+    // tile t: weight rows (t / mtiles) * 128.., activation rows (t % mtiles) * 128..
 
     if (warp == 0) {
         // ------------------------------ producer ------------------------------
@@ -226,27 +238,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             long long g = 0, rg = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x) {
-                const int m0 = (tile % p.mtiles) * kTcBM, n0 = (tile / p.mtiles) * kTcBN;
+                const int m0 = (tile % p.mtiles) * kTcBN, n0 = (tile / p.mtiles) * kTcBM;
                 for (int kt = 0; kt < kt_n && ok; ++kt, ++g) {
                     if ((kt & 3) == 0) {
                         const int rs = (int)(rg % kTcRS);
                         if (rg >= kTcRS) ok = mbar_wait(smem_u32(&r_empty[rs]), (uint32_t)(((rg / kTcRS) - 1) & 1), flags, p.err);
                         if (!ok) break;
-                        mbar_arrive_tx(smem_u32(&r_full[rs]), (uint32_t)(kTcBN * p.raw_row));
+                        mbar_arrive_tx(smem_u32(&r_full[rs]), (uint32_t)(kTcBM * p.raw_row));
                         tma_2d(smem_u32(raw(rs)), &tw, (kt >> 2) * (p.raw_row / 2), n0, smem_u32(&r_full[rs]));
                         ++rg;
                     }
                     const int s = (int)(g % kTcMS);
                     if (g >= kTcMS) ok = mbar_wait(smem_u32(&m_empty[s]), (uint32_t)(((g / kTcMS) - 1) & 1), flags, p.err);
                     if (!ok) break;
-                    mbar_arrive_tx(smem_u32(&a_full[s]), (uint32_t)(2 * kTcBM * kTcBK * 2));
-                    tma_2d(smem_u32(stage(s)), &tah, kt * kTcBK, m0, smem_u32(&a_full[s]));
-                    tma_2d(smem_u32(stage(s) + kTcBM * kTcBK * 2), &tal, kt * kTcBK, m0, smem_u32(&a_full[s]));
+                    mbar_arrive_tx(smem_u32(&x_full[s]), (uint32_t)kTcStageBytes);
+                    tma_2d(smem_u32(stage(s)), &tah, kt * kTcBK, m0, smem_u32(&x_full[s]));
+                    tma_2d(smem_u32(stage(s) + kTcPiece), &tal, kt * kTcBK, m0, smem_u32(&x_full[s]));
                 }
             }
             // let every copy this thread issued land before the CTA can exit
             for (long long q = (g > kTcMS ? g - kTcMS : 0); q < g; ++q)
-                mbar_wait(smem_u32(&a_full[q % kTcMS]), (uint32_t)((q / kTcMS) & 1), flags, p.err);
+                mbar_wait(smem_u32(&x_full[q % kTcMS]), (uint32_t)((q / kTcMS) & 1), flags, p.err);
             for (long long q = (rg > kTcRS ? rg - kTcRS : 0); q < rg; ++q)
                 mbar_wait(smem_u32(&r_full[q % kTcRS]), (uint32_t)((q / kTcRS) & 1), flags, p.err);
         }
@@ -265,17 +277,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 for (int kt = 0; kt < kt_n; ++kt, ++g) {
                     const int s = (int)(g % kTcMS);
                     const uint32_t ph = (uint32_t)((g / kTcMS) & 1);
-                    ok = mbar_wait(smem_u32(&a_full[s]), ph, flags, p.err) && mbar_wait(smem_u32(&b_full[s]), ph, flags, p.err);
+                    ok = mbar_wait(smem_u32(&x_full[s]), ph, flags, p.err) && mbar_wait(smem_u32(&w_full[s]), ph, flags, p.err);
                     if (!ok) break;
                     tc_fence_after();
-                    const uint32_t base = smem_u32(stage(s));
-                    const uint32_t ahi = base, alo = base + 16384, bhi = base + 32768, blo = base + 49152;
+                    const uint32_t xhi = smem_u32(stage(s)), xlo = xhi + kTcPiece;
+                    const uint32_t whi = tmem + (uint32_t)(kTcWCol0 + s * kTcWCols), wlo = whi + kTcBK / 2;
 #pragma unroll
                     for (int pass = 0; pass < 3; ++pass) {
-                        const uint32_t aa = pass == 2 ? alo : ahi, bb = pass == 1 ? blo : bhi;
+                        // w_hi x_hi, w_hi x_lo, w_lo x_hi
+                        const uint32_t wa = pass == 2 ? wlo : whi, xb = pass == 1 ? xlo : xhi;
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
-                            tc_mma(dt, tc_sdesc(aa + 32 * kk), tc_sdesc(bb + 32 * kk), (kt | pass | kk) != 0 ? 1u : 0u);
+                        for (int kk = 0; kk < kTcBK / 16; ++kk)
+                            tc_mma(dt, wa + 8 * kk, tc_sdesc(xb + 32 * kk), (kt | pass | kk) != 0 ? 1u : 0u);
                     }
                     tc_commit(smem_u32(&m_empty[s]));
                 }
@@ -287,35 +300,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
     } else if (warp < 2 + kTcEpiWarps) {
         // ------------------------------ epilogue ------------------------------
-        const int q = warp & 3;  // TMEM lane quarter this warp may access
-        const int r = 32 * q + lane;
+        const int q = warp & 3;  // TMEM lane quarter: weight rows 32q..32q+31 of the tile
         int tc = 0;
         for (int tile = blockIdx.x; tile < p.tiles; tile += gridDim.x, ++tc) {
             const int ab = tc & 1;
             if (!mbar_wait(smem_u32(&acc_full[ab]), (uint32_t)((tc >> 1) & 1), flags, p.err)) break;
             tc_fence_after();
-            const int m0 = (tile % p.mtiles) * kTcBM, n0 = (tile / p.mtiles) * kTcBN;
-            const int m = m0 + r;
-            const float as = m < p.M ? __ldg(p.ais + m) : 0.0f;
-            float* yr = p.y + (long long)m * p.N;
+            const int m0 = (tile % p.mtiles) * kTcBN, n0 = (tile / p.mtiles) * kTcBM;
+            const int n = n0 + 32 * q + lane;
+            const float wsn = n < p.N ? __ldg(p.wis + n) : 0.0f;
 #pragma unroll 1
             for (int c = 0; c < kTcBN / 32; ++c) {
                 float v[32];
                 tc_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(ab * kTcBN + 32 * c), v);
-                const int nb = n0 + 32 * c;
-                if (m < p.M && !flags[0]) {
-                    if ((p.N & 3) == 0 && nb + 32 <= p.N) {
+                const int mb = m0 + 32 * c;
+                if (n < p.N && !flags[0]) {
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            const float4 ws = __ldg(reinterpret_cast<const float4*>(p.wis + nb) + i);
-                            *reinterpret_cast<float4*>(yr + nb + 4 * i) =
-                                make_float4(v[4 * i] * as * ws.x, v[4 * i + 1] * as * ws.y, v[4 * i + 2] * as * ws.z,
-                                            v[4 * i + 3] * as * ws.w);
-                        }
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            if (nb + j < p.N) yr[nb + j] = v[j] * as * __ldg(p.wis + nb + j);
+                    for (int i = 0; i < 32; ++i) {
+                        const int m = mb + i;
+                        if (m < p.M) p.y[(long long)m * p.N + n] = v[i] * wsn * __ldg(p.ais + m);
                     }
                 }
             }
@@ -324,12 +327,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
     } else {
         // ------------------------------ converters ------------------------------
-        const int ct = tid - (2 + kTcEpiWarps) * 32;  // 0..255
-        const int n = ct & (kTcBN - 1), j = ct >> 7;  // weight row of the tile, half of the 64-K stage
+        // warp cw: TMEM lane quarter cw & 3 (weight rows 32 (cw & 3) + lane), values
+        // 32 j..32 j+31 of each 64-K stage with j = cw >> 2
+        const int cw = warp - (2 + kTcEpiWarps);
+        const int q = warp & 3, j = cw >> 2;
+        const int n = 32 * q + lane;
         long long g = 0, rg = 0;
         bool ok = true;
         for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x) {
-            const int n0 = (tile / p.mtiles) * kTcBN;
+            const int n0 = (tile / p.mtiles) * kTcBM;
             const float wsc = n0 + n < p.N ? __frcp_rn(__ldg(p.wis + n0 + n)) : 1.0f;  // 2^s (exact)
             for (int kt = 0; kt < kt_n && ok; ++kt, ++g) {
                 const int sub = kt & 3;
@@ -338,14 +344,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const int s = (int)(g % kTcMS);
                 if (ok && g >= kTcMS) ok = mbar_wait(smem_u32(&m_empty[s]), (uint32_t)(((g / kTcMS) - 1) & 1), flags, p.err);
                 if (!ok) break;
-                uint8_t* st = stage(s);
+                tc_fence_after();
                 const uint8_t* rrow = raw(rs) + n * p.raw_row;
-                if (WT == T_Q8_0) tc_conv_q8_0(rrow + (2 * sub + j) * 34, wsc, st + 32768, st + 49152, n, j);
-                else tc_conv_q4_k(rrow, sub, j, wsc, st + 32768, st + 49152, n);
-                fence_proxy_async();  // generic-proxy writes -> visible to the tensor core
-                mbar_arrive(smem_u32(&b_full[s]));
+                uint32_t h[16], l[16];
+                if (WT == T_Q8_0) tc_conv_q8_0(rrow + (2 * sub + j) * 34, wsc, h, l);
+                else tc_conv_q4_k(rrow, sub, j, wsc, h, l);
+                const uint32_t col = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(kTcWCol0 + s * kTcWCols + 16 * j);
+                tc_st16(col, h);
+                tc_st16(col + kTcBK / 2, l);
+                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&w_full[s]));  // one arrival per converter warp
                 if (sub == 3) {
-                    mbar_arrive(smem_u32(&r_empty[rs]));
+                    if (lane == 0) mbar_arrive(smem_u32(&r_empty[rs]));
                     ++rg;
                 }
             }
@@ -494,9 +506,9 @@ inline bool plan_tc(int wt, int am, long long M, long long N, long long K, int s
     p.tiles = p.mtiles * p.ntiles;
     p.raw_row = wt == T_Q8_0 ? kTcRK / 32 * 34 : 144;
     p.raw_stage = round_up(kTcBN * p.raw_row + 64, 1024);  // Q8_0 word loads reach 4 bytes past a row
-    p.off_raw = kTcMS * kTcStageBytes;
+    p.off_raw = kTcMS * kTcStageBytes;  // activation pieces; weight pieces live in TMEM
     p.off_bar = p.off_raw + kTcRS * p.raw_stage;
-    pl.smem = (size_t)p.off_bar + 256 + 1024;  // barriers, TMEM slot, flags; alignment slack
+    pl.smem = (size_t)p.off_bar + 512 + 1024;  // barriers, TMEM slot, flags; alignment slack
     if ((long long)pl.smem > smem_max) return false;
     pl.grid = p.tiles < sm_count ? p.tiles : sm_count;
     auto r256 = [](size_t v) { return (v + 255) / 256 * 256; };
