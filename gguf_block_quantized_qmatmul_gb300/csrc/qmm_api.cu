@@ -166,7 +166,9 @@ qmm_status stream_call(qmm_type wtype, int am, int epi, const void* wq, const fl
     }
     if (d.kind == KIND_TC) {
         if (!ws || ws_bytes < d.tp.workspace) return QMM_ERR_WORKSPACE;
-        return launch_tc(wt, am, d.tp, wq, x, ws, y, smem, s) == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
+        TcPlan tp = d.tp;
+        tp.p.err = err;
+        return launch_tc(wt, am, tp, wq, x, ws, y, smem, s) == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
     }
     if (d.kind == KIND_PREFILL) {
         PrefillPlan fp = d.fp;

@@ -41,23 +41,27 @@ cudaError_t tc_go(const TcPlan& pl, const void* wq, const float* x, void* ws, fl
     __half* alo = reinterpret_cast<__half*>(wsb + pl.ws_alo);
     float* ais = reinterpret_cast<float*>(wsb + pl.ws_ais);
     float* wis = reinterpret_cast<float*>(wsb + pl.ws_wis);
-    // 1. operand preparation: activation pieces, row scales of both operands
+    float* part = p0.ks > 1 ? reinterpret_cast<float*>(wsb + pl.ws_part) : nullptr;
+    unsigned* cnt = p0.ks > 1 ? reinterpret_cast<unsigned*>(wsb + pl.ws_cnt) : nullptr;
+    // 1. operand preparation: activation pieces, row scales of both operands, split-K counters
     const unsigned pblocks = (unsigned)(p0.M + (p0.N + kTcPrepThreads / 32 - 1) / (kTcPrepThreads / 32));
     tc_prep_kernel<WT, AM><<<pblocks, kTcPrepThreads, 0, s>>>(x, static_cast<const uint8_t*>(wq), p0.M, p0.N, p0.K, ahi,
-                                                              alo, ais, wis);
+                                                              alo, ais, wis, cnt, p0.ks > 1 ? p0.tiles : 0);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    // 2. tensor maps: raw weight rows as uint16, activation pieces (128-byte swizzle)
+    // 2. tensor maps: raw weight rows as uint16; activation pieces, 32 K x bx rows, 64-byte swizzle
     CUtensorMap tw, tah, tal;
     const unsigned long long rb = (unsigned long long)p0.K / (WT == T_Q8_0 ? 32 : 256) * (WT == T_Q8_0 ? 34 : 144);
-    if (!make_map(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT16, wq, rb / 2, p0.N, rb, p0.raw_row / 2, kTcBN, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !make_map(&tah, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, ahi, p0.K, p0.M, (unsigned long long)p0.K * 2, kTcBK, kTcBM,
-                  CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&tal, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, alo, p0.K, p0.M, (unsigned long long)p0.K * 2, kTcBK, kTcBM,
-                  CU_TENSOR_MAP_SWIZZLE_128B))
+    if (!make_map(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT16, wq, rb / 2, p0.N, rb, p0.raw_row / 2, kTcBW, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_map(&tah, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, ahi, p0.K, p0.M, (unsigned long long)p0.K * 2, kTcBK, p0.bx,
+                  CU_TENSOR_MAP_SWIZZLE_64B) ||
+        !make_map(&tal, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, alo, p0.K, p0.M, (unsigned long long)p0.K * 2, kTcBK, p0.bx,
+                  CU_TENSOR_MAP_SWIZZLE_64B))
         return cudaErrorInvalidValue;
     TcParams p = p0;
     p.y = y;
+    p.part = part;
+    p.cnt = cnt;
     p.ais = ais;
     p.wis = wis;
     // 3. the GEMM, a programmatic dependent of the preparation

@@ -16,25 +16,29 @@
 // hi.hi + hi.lo + lo.hi (the dropped lo.lo is below 2^-22 relative), all into
 // one f32 accumulator, and the epilogue multiplies by 2^-(s_row + s_col).
 //
-// One persistent CTA per SM, 128 x 128 output tiles (128 weight rows x 128
-// activation rows), 14 warps:
+// One persistent CTA per SM over work units: an output tile of 128 weight
+// rows x bx activation rows (bx <= 256, a multiple of 16, the MMA's N) and
+// one of ks slices of K.  18 warps:
 //   producer  TMA: raw weight rows (2-D box, 128 rows x 272 B = 8 Q8_0 blocks,
-//             or 144 B = 1 Q4_K super-block, per 256 K) and the activation
-//             pieces (128 rows x 64 f16, 128-byte swizzle, per 64 K);
-//   converter 8 warps dequantize the raw weight bytes of each 64-K stage into
-//             the two f16 pieces and write them straight into tensor memory
-//             (tcgen05.st): the weights are the MMA's A operand, read from
-//             TMEM, so the three passes re-read only the activation pieces
-//             from shared memory (shared-memory bandwidth, which the operand
-//             reads and the converters' traffic share, bounded an earlier
-//             layout with both operands in shared memory);
-//   MMA       one thread issues tcgen05.mma (M 128 weight rows, N 128
-//             activation rows, K 16; 12 per 64 K) into one of two TMEM
-//             accumulators, commits to mbarriers that free the stage or hand
-//             the tile to the epilogue;
-//   epilogue  4 warps, one TMEM lane quarter (32 weight rows) each:
-//             tcgen05.ld, scale, y stores coalesced along N.
-// TMEM: 2 accumulators x 128 columns + 4 stages x 64 columns of weight pieces.
+//             or 144 B = 1 Q4_K super-block, per 256 K; up to six stages in
+//             flight) and the activation pieces (bx rows x 32 f16, 64-byte
+//             swizzle, hi and lo, per 32 K);
+//   MMA       one thread: per 32-K stage six tcgen05.mma (M 128, N bx, K 16:
+//             hi.hi, hi.lo, lo.hi, two K steps each) with the weights as the A
+//             operand in tensor memory and the activation piece from shared
+//             memory; it tests the next stage's barrier before issuing the
+//             current one, so a ready stage costs no stall;
+//   epilogue  8 warps, a TMEM lane quarter (32 weight rows) and half of the
+//             accumulator columns each: tcgen05.ld, scale, y stores coalesced
+//             along N; with K split, unscaled partial tiles in the workspace,
+//             and the unit that completes a tile sums its ks partials in
+//             slice order (deterministic) and writes y;
+//   converter 8 warps in two groups (even and odd stages): each thread one
+//             weight row's 32 values of a stage, read from the raw stage with
+//             conflict-free 16-byte loads, dequantized, split into hi and lo,
+//             written straight into tensor memory (tcgen05.st).
+// TMEM: accumulators (two of 128 columns when bx <= 128, else one of 256) and
+// four stages x 32 columns of weight pieces at column 256.
 #pragma once
 
 #include <cuda.h>
@@ -44,47 +48,56 @@
 
 namespace qmm {
 
-constexpr int kTcBM = 128;   // activation rows per tile (MMA M)
-constexpr int kTcBN = 128;   // weight rows per tile (MMA N)
-constexpr int kTcBK = 64;    // K per MMA stage
-constexpr int kTcRK = 256;   // K per raw weight stage
-constexpr int kTcMS = 4;     // MMA stages
-constexpr int kTcRS = 2;     // raw weight stages
+constexpr int kTcBW = 128;      // weight rows per tile (MMA M, the TMEM lanes)
+constexpr int kTcBXMax = 256;   // activation rows per tile, at most (MMA N)
+constexpr int kTcBK = 32;       // K per stage
+constexpr int kTcRK = 256;      // K per raw weight stage
+constexpr int kTcSub = kTcRK / kTcBK;  // stages per raw stage
+constexpr int kTcS = 4;         // stages: activation pieces in shared memory, weight pieces in TMEM
+constexpr int kTcRSMax = 6;     // raw weight stages, at most
 constexpr int kTcConvWarps = 8;
-constexpr int kTcEpiWarps = 4;
+constexpr int kTcEpiWarps = 8;
 constexpr int kTcThreads = (2 + kTcEpiWarps + kTcConvWarps) * 32;
-constexpr int kTcPiece = kTcBM * kTcBK * 2;      // one activation piece of a stage: 16 KB
-constexpr int kTcStageBytes = 2 * kTcPiece;      // activation hi, lo: 32 KB
-constexpr int kTcTmemCols = 512;                 // 2 x 128 accumulator columns + 4 x 64 weight-piece columns
-constexpr int kTcWCol0 = 2 * kTcBN;              // first TMEM column of the weight pieces
-constexpr int kTcWCols = kTcBK;                  // columns per stage: hi (32) + lo (32), two f16 per column
+constexpr int kTcTmemCols = 512;
+constexpr int kTcWCol0 = 256;   // weight pieces: stage s at 256 + 32 s (hi 16 columns, lo 16 columns)
+constexpr int kTcMaxSplit = 16;
 
 struct TcParams {
     float* y;
+    float* part;        // partial tiles [ks][M][N] when K is split
+    unsigned* cnt;      // per-tile arrival counters when K is split (zeroed by the preparation launch)
     const float* ais;   // 2^-s per activation row
     const float* wis;   // 2^-s per weight row
     unsigned* err;
     int M, N, K;
+    int bx;             // activation rows per tile (MMA N)
+    int nacc;           // accumulators: 2 when bx <= 128
     int mtiles, ntiles, tiles;
+    int ks, units;      // K slices; work units = tiles x ks
+    int nrs;            // raw stages in K
     int raw_row;        // raw bytes per weight row per raw stage (272 Q8_0, 144 Q4_K)
     int raw_stage;      // bytes per raw stage (128 rows, rounded to 1 KB)
+    int nraw;           // raw stages in shared memory
+    int piece;          // bytes of one activation piece (bx rows x 64 B)
     int off_raw, off_bar;
 };
 
-// shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row atoms 1 KB apart
+// shared-memory matrix descriptor: K-major, 64-byte swizzle, 8-row atoms 512 B apart
 __device__ __forceinline__ uint64_t tc_sdesc(uint32_t addr) {
-    return (uint64_t)((addr >> 4) & 0x3FFF) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) |
-           ((uint64_t)2 << 61);
+    return (uint64_t)((addr >> 4) & 0x3FFF) | ((uint64_t)1 << 16) | ((uint64_t)(512 >> 4) << 32) | ((uint64_t)1 << 46) |
+           ((uint64_t)4 << 61);
 }
-// instruction descriptor: f32 accumulator, f16 A and B, both K-major, N = 128, M = 128
-constexpr uint32_t kTcIdesc = (1u << 4) | ((uint32_t)(kTcBN >> 3) << 17) | ((uint32_t)(kTcBM >> 4) << 24);
+// instruction descriptor: f32 accumulator, f16 A and B, both K-major, M = 128, N = bx
+__device__ __forceinline__ uint32_t tc_idesc(int bx) {
+    return (1u << 4) | ((uint32_t)(bx >> 3) << 17) | ((uint32_t)(kTcBW >> 4) << 24);
+}
 
 // D (TMEM) += A (TMEM, 128 lanes x 16 f16) x B (shared memory)^T
-__device__ __forceinline__ void tc_mma(uint32_t tmem, uint32_t ta, uint64_t db, uint32_t accumulate) {
+__device__ __forceinline__ void tc_mma(uint32_t tmem, uint32_t ta, uint64_t db, uint32_t idesc, uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem),
-        "r"(ta), "l"(db), "r"(kTcIdesc), "r"(accumulate)
+        "r"(ta), "l"(db), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 // 16 32-bit columns of this warp's TMEM lane quarter from registers
@@ -100,25 +113,26 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
 }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-
-// 32 f32 columns of this warp's TMEM lane quarter
-__device__ __forceinline__ void tc_ld32(uint32_t taddr, float v[32]) {
-    uint32_t r[32];
+// non-blocking test of an mbarrier phase; the result is consumed later
+__device__ __forceinline__ uint32_t mbar_test(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
-          "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+        "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok;
 }
 
-// byte offset of the 16-byte chunk c (8 halves) of row r in a [128][64] f16 tile, 128-byte swizzle
-__device__ __forceinline__ int tc_chunk(int r, int c) { return r * 128 + (((c ^ r) & 7) << 4); }
+// 16 f32 columns of this warp's TMEM lane quarter (the wait is separate)
+__device__ __forceinline__ void tc_ld16(uint32_t taddr, uint32_t r[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // ---------------------------------------------------------------------------
 // weight conversion: one thread, the 32 values of one weight row that one
@@ -126,44 +140,59 @@ __device__ __forceinline__ int tc_chunk(int r, int c) { return r * 128 + (((c ^ 
 // and 16 words of lo f16 pairs (k order natural)
 // ---------------------------------------------------------------------------
 
-// Q8_0 block at blk (2-byte aligned): w = ds q with ds = f(d) 2^s as f16
-// (exact while it is a normal f16); hi = f16(ds q) by one hmul2, lo = ds q - hi
-// by one hfma2 (exact: at most 8 significant bits remain)
-__device__ __forceinline__ void tc_conv_q8_0(const uint8_t* blk, float wsc, uint32_t h[16], uint32_t l[16]) {
-    const float ds = h2f(*reinterpret_cast<const uint16_t*>(blk)) * wsc;
-    const __half2 ds2 = __half2half2(__float2half_rn(ds));
-    const uintptr_t a = reinterpret_cast<uintptr_t>(blk + 2);
-    const uint32_t* w = reinterpret_cast<const uint32_t*>(a & ~uintptr_t(3));
-    const uint32_t sh = (uint32_t)(a & 3u) * 8u;
+// hi = f16(ds q) by one hmul2, lo = ds q - hi by one hfma2 (exact: at most 8
+// significant bits remain), for the byte pair (2p, 2p+1) of a word of codes
+__device__ __forceinline__ void tc_q8_pair(uint32_t word, int p, __half2 ds2, uint32_t& h, uint32_t& l) {
+    uint32_t qb = __byte_perm(word, 0x64646464u, p ? 0x4342u : 0x4140u);  // bytes under 0x64: 1152 + q
+    const __half2 q = __hsub2(*reinterpret_cast<__half2*>(&qb), __half2half2(__ushort_as_half(0x6480)));
+    const __half2 hi = __hmul2(q, ds2);
+    const __half2 lo = __hfma2(q, ds2, __hneg2(hi));
+    h = *reinterpret_cast<const uint32_t*>(&hi);
+    l = *reinterpret_cast<const uint32_t*>(&lo);
+}
+
+// Q8_0 block J (0..7) of a 272-byte raw row at row (16-byte aligned): w 2^s =
+// ds q with ds = f(d) 2^s as f16 (exact while it is a normal f16).  The block
+// sits at byte 34 J; three 16-byte loads cover it (rows 272 B apart make a
+// quarter warp's 16-byte loads hit 32 distinct banks).
+template <int J>
+__device__ __forceinline__ void tc_conv_q8_0(const uint8_t* row, float wsc, uint32_t h[16], uint32_t l[16]) {
+    constexpr int A = (34 * J) & ~15;  // first 16-byte chunk
+    constexpr int O = 34 * J - A;      // byte offset of d in the chunk (even, < 16)
+    const uint4 c0 = *reinterpret_cast<const uint4*>(row + A);
+    const uint4 c1 = *reinterpret_cast<const uint4*>(row + A + 16);
+    const uint4 c2 = *reinterpret_cast<const uint4*>(row + A + 32);
+    const uint32_t w[12] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w, c2.x, c2.y, c2.z, c2.w};
+    const uint32_t dbits = (w[O / 4] >> (8 * (O % 4))) & 0xFFFFu;
+    const __half2 ds2 = __half2half2(__float2half_rn(h2f(dbits) * wsc));
+    constexpr int QW = (O + 2) / 4, QS = 8 * ((O + 2) % 4);  // codes: word QW onward, shifted by QS bits
+    static_assert(QW + 8 + (QS != 0 ? 1 : 0) <= 12, "the three chunks hold the block");
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        const uint32_t word = __funnelshift_r(w[i], w[i + 1], sh) ^ 0x80808080u;  // codes 4i..4i+3, biased by 128
-#pragma unroll
-        for (int p = 0; p < 2; ++p) {
-            uint32_t qb = __byte_perm(word, 0x64646464u, p ? 0x4342u : 0x4140u);  // bytes (2p, 2p+1) under 0x64: 1152 + q
-            const __half2 q = __hsub2(*reinterpret_cast<__half2*>(&qb), __half2half2(__ushort_as_half(0x6480)));
-            const __half2 hi = __hmul2(q, ds2);
-            const __half2 lo = __hfma2(q, ds2, __hneg2(hi));
-            h[2 * i + p] = *reinterpret_cast<const uint32_t*>(&hi);
-            l[2 * i + p] = *reinterpret_cast<const uint32_t*>(&lo);
-        }
+        uint32_t word;
+        if constexpr (QS != 0) word = __funnelshift_r(w[QW + i], w[QW + i + 1], QS);
+        else word = w[QW + i];
+        word ^= 0x80808080u;  // codes biased by 128
+        tc_q8_pair(word, 0, ds2, h[2 * i], l[2 * i]);
+        tc_q8_pair(word, 1, ds2, h[2 * i + 1], l[2 * i + 1]);
     }
 }
 
-// Q4_K sub-block 2 sub + j of the super-block at sbk (16-byte aligned): w 2^s =
+// Q4_K sub-block J (0..7) of the super-block at sbk (16-byte aligned): w 2^s =
 // fma(e 2^s, q, -o 2^s) in f32 (one rounding, as the dequantization contract),
 // split as f16(v) + f16(v - f16(v))
-__device__ __forceinline__ void tc_conv_q4_k(const uint8_t* sbk, int sub, int j, float wsc, uint32_t h[16], uint32_t l[16]) {
+template <int J>
+__device__ __forceinline__ void tc_conv_q4_k(const uint8_t* sbk, float wsc, uint32_t h[16], uint32_t l[16]) {
+    constexpr int C = J >> 1, NIB = J & 1;  // byte 32 C + i holds sub-block 2 C (low nibble) and 2 C + 1 (high)
     const uint4 hd = *reinterpret_cast<const uint4*>(sbk);
-    const int jj = 2 * sub + j;
-    const float es = h2f(hd.x) * (float)q4k_sc(hd.y, hd.w, jj) * wsc;
-    const float os = h2f(hd.x >> 16) * (float)q4k_mn(hd.z, hd.w, jj) * wsc;
-    const uint4 q0 = *reinterpret_cast<const uint4*>(sbk + 16 + 32 * sub);
-    const uint4 q1 = *reinterpret_cast<const uint4*>(sbk + 16 + 32 * sub + 16);
+    const float es = h2f(hd.x) * (float)q4k_sc(hd.y, hd.w, J) * wsc;
+    const float os = h2f(hd.x >> 16) * (float)q4k_mn(hd.z, hd.w, J) * wsc;
+    const uint4 q0 = *reinterpret_cast<const uint4*>(sbk + 16 + 32 * C);
+    const uint4 q1 = *reinterpret_cast<const uint4*>(sbk + 16 + 32 * C + 16);
     const uint32_t qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        const uint32_t nb = (qw[i] >> (4 * j)) & 0x0F0F0F0Fu;  // values 4i..4i+3 of the sub-block
+        const uint32_t nb = (qw[i] >> (4 * NIB)) & 0x0F0F0F0Fu;  // values 4i..4i+3 of the sub-block
 #pragma unroll
         for (int p = 0; p < 2; ++p) {
             const float v0 = fmaf(es, (float)((nb >> (16 * p)) & 0xFu), -os);
@@ -173,6 +202,101 @@ __device__ __forceinline__ void tc_conv_q4_k(const uint8_t* sbk, int sub, int j,
             const __half2 lo = __floats2half2_rn(v0 - hf.x, v1 - hf.y);
             h[2 * i + p] = *reinterpret_cast<const uint32_t*>(&hi);
             l[2 * i + p] = *reinterpret_cast<const uint32_t*>(&lo);
+        }
+    }
+}
+
+// K slice `split` of ks: raw stages [r0, r1)
+__device__ __forceinline__ void tc_slice(const TcParams& p, int split, int& r0, int& r1) {
+    r0 = split * p.nrs / p.ks;
+    r1 = (split + 1) * p.nrs / p.ks;
+}
+
+// one converter warp's share of a raw stage: stages G, G + 2, G + 4, G + 6 of
+// the eight it feeds (G = the warp's group); g0 = the global index of the
+// raw stage's first stage
+template <int WT, int G>
+__device__ __forceinline__ bool tc_convert_raw(const uint8_t* rrow, float wsc, long long g0, uint32_t tq, uint32_t tmem,
+                                               uint64_t* full, uint64_t* empty, volatile int* flags, unsigned* err,
+                                               int lane) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int j = 2 * u + G;
+        const long long g = g0 + j;
+        const int s = (int)(g % kTcS);
+        if (g >= kTcS && !mbar_wait(smem_u32(&empty[s]), (uint32_t)(((g / kTcS) - 1) & 1), flags, err)) return false;
+        tc_fence_after();
+        uint32_t h[16], l[16];
+        if (WT == T_Q8_0) {
+            if (u == 0) tc_conv_q8_0<G>(rrow, wsc, h, l);
+            else if (u == 1) tc_conv_q8_0<G + 2>(rrow, wsc, h, l);
+            else if (u == 2) tc_conv_q8_0<G + 4>(rrow, wsc, h, l);
+            else tc_conv_q8_0<G + 6>(rrow, wsc, h, l);
+        } else {
+            if (u == 0) tc_conv_q4_k<G>(rrow, wsc, h, l);
+            else if (u == 1) tc_conv_q4_k<G + 2>(rrow, wsc, h, l);
+            else if (u == 2) tc_conv_q4_k<G + 4>(rrow, wsc, h, l);
+            else tc_conv_q4_k<G + 6>(rrow, wsc, h, l);
+        }
+        const uint32_t col = tmem + tq + (uint32_t)(kTcWCol0 + 32 * s);
+        tc_st16(col, h);
+        tc_st16(col + 16, l);
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&full[s]));  // one of the group's four converter arrivals
+    }
+    return true;
+}
+
+// split-K fix-up of one tile by the 256 epilogue threads: thread t takes
+// columns n0 + (t & 31) + 32 e (e < 4) and rows m0 + (t >> 5) + 8 j; per
+// batch of four rows it loads up to four slices' sixteen values at once (64
+// independent loads) and adds them in slice order, so the sum is the same
+// on every run
+__device__ __forceinline__ void tc_fixup(const TcParams& p, int t, int m0, int n0) {
+    const int cl = t & 31, rg = t >> 5;
+    const size_t slice = (size_t)p.M * p.N;
+    float ws4[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const int ne = n0 + cl + 32 * e;
+        ws4[e] = ne < p.N ? __ldg(p.wis + ne) : 0.0f;
+    }
+    for (int j0 = 0; j0 < p.bx / 8; j0 += 4) {
+        float acc[16];
+        uint32_t okm = 0;  // element 4 u + e is in the tile and in y
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int mr = rg + 8 * (j0 + u), m = m0 + mr, ne = n0 + cl + 32 * e;  // rows of this tile only
+                if (mr < p.bx && m < p.M && ne < p.N) okm |= 1u << (4 * u + e);
+                acc[4 * u + e] = 0.0f;
+            }
+        const float* base = p.part + (size_t)(m0 + rg + 8 * j0) * p.N + n0 + cl;
+        for (int s0 = 0; s0 < p.ks; s0 += 2) {
+            float v[2][16];
+#pragma unroll
+            for (int sp = 0; sp < 2; ++sp)
+#pragma unroll
+                for (int el = 0; el < 16; ++el)
+                    v[sp][el] = s0 + sp < p.ks && ((okm >> el) & 1u)
+                                    ? __ldcg(base + (s0 + sp) * slice + (size_t)(8 * (el >> 2)) * p.N + 32 * (el & 3))
+                                    : 0.0f;
+#pragma unroll
+            for (int sp = 0; sp < 2; ++sp)
+#pragma unroll
+                for (int el = 0; el < 16; ++el) acc[el] += v[sp][el];
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int mr = rg + 8 * (j0 + u), m = m0 + mr;
+            if (mr >= p.bx || m >= p.M) continue;
+            const float am = __ldg(p.ais + m);
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if ((okm >> (4 * u + e)) & 1u) p.y[(size_t)m * p.N + n0 + cl + 32 * e] = acc[4 * u + e] * ws4[e] * am;
         }
     }
 }
@@ -188,32 +312,34 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint8_t* sm = smraw + ((1024 - (smem_u32(smraw) & 1023)) & 1023);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + p.off_bar);
-    uint64_t* x_full = bars;                            // [kTcMS] activation pieces landed (TMA)
-    uint64_t* w_full = bars + kTcMS;                    // [kTcMS] weight pieces in TMEM (converter warps)
-    uint64_t* m_empty = bars + 2 * kTcMS;               // [kTcMS] stage consumed by the MMAs (commit)
-    uint64_t* r_full = bars + 3 * kTcMS;                // [kTcRS] raw weight rows landed (TMA)
-    uint64_t* r_empty = bars + 3 * kTcMS + kTcRS;       // [kTcRS] raw stage converted
-    uint64_t* acc_full = bars + 3 * kTcMS + 2 * kTcRS;  // [2] accumulator complete (commit)
-    uint64_t* acc_empty = acc_full + 2;                 // [2] accumulator read (epilogue)
-    static_assert((3 * kTcMS + 2 * kTcRS + 4) * 8 <= 256, "mbarriers overlap the TMEM slot");
+    uint64_t* full = bars;                          // [kTcS] activation pieces landed and weight pieces in TMEM
+    uint64_t* empty = full + kTcS;                  // [kTcS] stage consumed by the MMAs (commit)
+    uint64_t* r_full = empty + kTcS;                // [kTcRSMax] raw weight rows landed (TMA)
+    uint64_t* r_empty = r_full + kTcRSMax;          // [kTcRSMax] raw stage converted
+    uint64_t* acc_full = r_empty + kTcRSMax;        // [2] accumulator complete (commit)
+    uint64_t* acc_empty = acc_full + 2;             // [2] accumulator read (epilogue)
+    uint64_t* epi_done = acc_empty + 2;             // partial tile stored (epilogue warps)
+    uint64_t* fix_ready = epi_done + 1;             // arrival counted, fixflag set
+    static_assert((2 * kTcS + 2 * kTcRSMax + 6) * 8 <= 256, "mbarriers overlap the TMEM slot");
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + p.off_bar + 256);
-    volatile int* flags = reinterpret_cast<volatile int*>(sm + p.off_bar + 320);
-    const int kt_n = p.K / kTcBK;
+    volatile int* flags = reinterpret_cast<volatile int*>(sm + p.off_bar + 320);  // [0] abort, [1] fix-up owner
     if (tid == 0) {
-        for (int i = 0; i < kTcMS; ++i) {
-            mbar_init(smem_u32(&x_full[i]), 1);
-            mbar_init(smem_u32(&w_full[i]), kTcConvWarps);
-            mbar_init(smem_u32(&m_empty[i]), 1);
+        for (int i = 0; i < kTcS; ++i) {
+            mbar_init(smem_u32(&full[i]), 1 + kTcConvWarps / 2);
+            mbar_init(smem_u32(&empty[i]), 1);
         }
-        for (int i = 0; i < kTcRS; ++i) {
+        for (int i = 0; i < kTcRSMax; ++i) {
             mbar_init(smem_u32(&r_full[i]), 1);
             mbar_init(smem_u32(&r_empty[i]), kTcConvWarps);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&acc_full[i]), 1);
-            mbar_init(smem_u32(&acc_empty[i]), kTcEpiWarps * 32);
+            mbar_init(smem_u32(&acc_empty[i]), kTcEpiWarps);
         }
+        mbar_init(smem_u32(epi_done), kTcEpiWarps);
+        mbar_init(smem_u32(fix_ready), 1);
         flags[0] = 0;
+        flags[1] = 0;
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -228,138 +354,201 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t tmem = *tslot;
     grid_dep_wait();  // the operand-preparing grid has completed
 
-    auto stage = [&](int s) { return sm + s * kTcStageBytes; };  // activation hi | lo, 16 KB each
+    auto stage = [&](int s) { return sm + s * 2 * p.piece; };  // activation hi | lo
     auto raw = [&](int s) { return sm + p.off_raw + s * p.raw_stage; };
-    // tile t: weight rows (t / mtiles) * 128.., activation rows (t % mtiles) * 128..
+    // unit u: tile u % tiles (weight rows (tile / mtiles) * 128.., activation
+    // rows (tile % mtiles) * bx..), K slice u / tiles
 
     if (warp == 0) {
         // ------------------------------ producer ------------------------------
         if (lane == 0) {
-            long long g = 0, rg = 0;
+            long long g = 0;            // stages issued
+            long long ri = 0;           // raw stages issued
+            int iu = blockIdx.x, ir = 0, ir1 = 0;  // raw-issue cursor: unit, raw stage, end
+            if (iu < p.units) tc_slice(p, iu / p.tiles, ir, ir1);
             bool ok = true;
-            for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x) {
-                const int m0 = (tile % p.mtiles) * kTcBN, n0 = (tile / p.mtiles) * kTcBM;
-                for (int kt = 0; kt < kt_n && ok; ++kt, ++g) {
-                    if ((kt & 3) == 0) {
-                        const int rs = (int)(rg % kTcRS);
-                        if (rg >= kTcRS) ok = mbar_wait(smem_u32(&r_empty[rs]), (uint32_t)(((rg / kTcRS) - 1) & 1), flags, p.err);
+            long long rc = 0;           // raw stages whose activation stages are issued
+            for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
+                const int tile = u % p.tiles;
+                const int m0 = (tile % p.mtiles) * p.bx;
+                int r0, r1;
+                tc_slice(p, u / p.tiles, r0, r1);
+                for (int r = r0; r < r1 && ok; ++r, ++rc) {
+                    // raw weight rows up to nraw - 1 raw stages ahead, across units
+                    while (ok && iu < p.units && ri <= rc + p.nraw - 1) {
+                        const int rs = (int)(ri % p.nraw);
+                        if (ri >= p.nraw) ok = mbar_wait(smem_u32(&r_empty[rs]), (uint32_t)(((ri / p.nraw) - 1) & 1), flags, p.err);
                         if (!ok) break;
-                        mbar_arrive_tx(smem_u32(&r_full[rs]), (uint32_t)(kTcBM * p.raw_row));
-                        tma_2d(smem_u32(raw(rs)), &tw, (kt >> 2) * (p.raw_row / 2), n0, smem_u32(&r_full[rs]));
-                        ++rg;
+                        const int n0 = ((iu % p.tiles) / p.mtiles) * kTcBW;
+                        mbar_arrive_tx(smem_u32(&r_full[rs]), (uint32_t)(kTcBW * p.raw_row));
+                        tma_2d(smem_u32(raw(rs)), &tw, ir * (p.raw_row / 2), n0, smem_u32(&r_full[rs]));
+                        ++ri;
+                        if (++ir >= ir1) {
+                            iu += gridDim.x;
+                            if (iu < p.units) tc_slice(p, iu / p.tiles, ir, ir1);
+                        }
                     }
-                    const int s = (int)(g % kTcMS);
-                    if (g >= kTcMS) ok = mbar_wait(smem_u32(&m_empty[s]), (uint32_t)(((g / kTcMS) - 1) & 1), flags, p.err);
-                    if (!ok) break;
-                    mbar_arrive_tx(smem_u32(&x_full[s]), (uint32_t)kTcStageBytes);
-                    tma_2d(smem_u32(stage(s)), &tah, kt * kTcBK, m0, smem_u32(&x_full[s]));
-                    tma_2d(smem_u32(stage(s) + kTcPiece), &tal, kt * kTcBK, m0, smem_u32(&x_full[s]));
+                    for (int j = 0; j < kTcSub && ok; ++j, ++g) {
+                        const int s = (int)(g % kTcS);
+                        if (g >= kTcS) ok = mbar_wait(smem_u32(&empty[s]), (uint32_t)(((g / kTcS) - 1) & 1), flags, p.err);
+                        if (!ok) break;
+                        const int kx = (r * kTcSub + j) * kTcBK;
+                        mbar_arrive_tx(smem_u32(&full[s]), (uint32_t)(2 * p.piece));
+                        tma_2d(smem_u32(stage(s)), &tah, kx, m0, smem_u32(&full[s]));
+                        tma_2d(smem_u32(stage(s) + p.piece), &tal, kx, m0, smem_u32(&full[s]));
+                    }
                 }
             }
             // let every copy this thread issued land before the CTA can exit
-            for (long long q = (g > kTcMS ? g - kTcMS : 0); q < g; ++q)
-                mbar_wait(smem_u32(&x_full[q % kTcMS]), (uint32_t)((q / kTcMS) & 1), flags, p.err);
-            for (long long q = (rg > kTcRS ? rg - kTcRS : 0); q < rg; ++q)
-                mbar_wait(smem_u32(&r_full[q % kTcRS]), (uint32_t)((q / kTcRS) & 1), flags, p.err);
+            for (long long q = (g > kTcS ? g - kTcS : 0); q < g; ++q)
+                mbar_wait(smem_u32(&full[q % kTcS]), (uint32_t)((q / kTcS) & 1), flags, p.err);
+            for (long long q = (ri > p.nraw ? ri - p.nraw : 0); q < ri; ++q)
+                mbar_wait(smem_u32(&r_full[q % p.nraw]), (uint32_t)((q / p.nraw) & 1), flags, p.err);
         }
     } else if (warp == 1) {
         // ------------------------------ MMA issuer ------------------------------
         if (lane == 0) {
+            const uint32_t idesc = tc_idesc(p.bx);
             long long g = 0;
-            int tc = 0;
+            int uc = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x, ++tc) {
-                const int ab = tc & 1;
-                if (tc >= 2) ok = mbar_wait(smem_u32(&acc_empty[ab]), (uint32_t)(((tc >> 1) - 1) & 1), flags, p.err);
+            uint32_t ready = 0;  // the next stage's barrier, tested ahead
+            for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x, ++uc) {
+                const int ab = p.nacc == 2 ? (uc & 1) : 0;
+                const int use = p.nacc == 2 ? (uc >> 1) : uc;
+                if (use > 0) ok = mbar_wait(smem_u32(&acc_empty[ab]), (uint32_t)((use - 1) & 1), flags, p.err);
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t dt = tmem + (uint32_t)(ab * kTcBN);
-                for (int kt = 0; kt < kt_n; ++kt, ++g) {
-                    const int s = (int)(g % kTcMS);
-                    const uint32_t ph = (uint32_t)((g / kTcMS) & 1);
-                    ok = mbar_wait(smem_u32(&x_full[s]), ph, flags, p.err) && mbar_wait(smem_u32(&w_full[s]), ph, flags, p.err);
+                const uint32_t dt = tmem + (uint32_t)(ab * 128);
+                int r0, r1;
+                tc_slice(p, u / p.tiles, r0, r1);
+                const int nst = (r1 - r0) * kTcSub;
+                for (int i = 0; i < nst; ++i, ++g) {
+                    const int s = (int)(g % kTcS);
+                    const uint32_t nxt = mbar_test(smem_u32(&full[(g + 1) % kTcS]), (uint32_t)(((g + 1) / kTcS) & 1));
+                    if (!ready) ok = mbar_wait(smem_u32(&full[s]), (uint32_t)((g / kTcS) & 1), flags, p.err);
                     if (!ok) break;
                     tc_fence_after();
-                    const uint32_t xhi = smem_u32(stage(s)), xlo = xhi + kTcPiece;
-                    const uint32_t whi = tmem + (uint32_t)(kTcWCol0 + s * kTcWCols), wlo = whi + kTcBK / 2;
+                    const uint32_t xhi = smem_u32(stage(s)), xlo = xhi + (uint32_t)p.piece;
+                    const uint32_t whi = tmem + (uint32_t)(kTcWCol0 + 32 * s), wlo = whi + 16;
 #pragma unroll
                     for (int pass = 0; pass < 3; ++pass) {
                         // w_hi x_hi, w_hi x_lo, w_lo x_hi
                         const uint32_t wa = pass == 2 ? wlo : whi, xb = pass == 1 ? xlo : xhi;
 #pragma unroll
                         for (int kk = 0; kk < kTcBK / 16; ++kk)
-                            tc_mma(dt, wa + 8 * kk, tc_sdesc(xb + 32 * kk), (kt | pass | kk) != 0 ? 1u : 0u);
+                            tc_mma(dt, wa + 8 * kk, tc_sdesc(xb + 32 * kk), idesc, (i | pass | kk) != 0 ? 1u : 0u);
                     }
-                    tc_commit(smem_u32(&m_empty[s]));
+                    tc_commit(smem_u32(&empty[s]));
+                    ready = nxt;
                 }
                 if (!ok) break;
                 tc_commit(smem_u32(&acc_full[ab]));
             }
             // the last commits must land before TMEM is released
-            if (g > 0) mbar_wait(smem_u32(&m_empty[(g - 1) % kTcMS]), (uint32_t)(((g - 1) / kTcMS) & 1), flags, p.err);
+            if (g > 0) mbar_wait(smem_u32(&empty[(g - 1) % kTcS]), (uint32_t)(((g - 1) / kTcS) & 1), flags, p.err);
         }
     } else if (warp < 2 + kTcEpiWarps) {
         // ------------------------------ epilogue ------------------------------
-        const int q = warp & 3;  // TMEM lane quarter: weight rows 32q..32q+31 of the tile
-        int tc = 0;
-        for (int tile = blockIdx.x; tile < p.tiles; tile += gridDim.x, ++tc) {
-            const int ab = tc & 1;
-            if (!mbar_wait(smem_u32(&acc_full[ab]), (uint32_t)((tc >> 1) & 1), flags, p.err)) break;
-            tc_fence_after();
-            const int m0 = (tile % p.mtiles) * kTcBN, n0 = (tile / p.mtiles) * kTcBM;
+        const int ew = warp - 2;
+        const int q = warp & 3;        // TMEM lane quarter: weight rows 32q..32q+31 of the tile
+        const int half = ew >> 2;      // accumulator columns: 16-column chunks half, half + 2, ...
+        const uint32_t tq = (uint32_t)(32 * q) << 16;
+        const int nch = p.bx / 16;
+        int uc = 0, fix = 0;
+        for (int u = blockIdx.x; u < p.units; u += gridDim.x, ++uc) {
+            const int ab = p.nacc == 2 ? (uc & 1) : 0;
+            const int use = p.nacc == 2 ? (uc >> 1) : uc;
+            const int tile = u % p.tiles, split = u / p.tiles;
+            const int m0 = (tile % p.mtiles) * p.bx, n0 = (tile / p.mtiles) * kTcBW;
             const int n = n0 + 32 * q + lane;
-            const float wsn = n < p.N ? __ldg(p.wis + n) : 0.0f;
-#pragma unroll 1
-            for (int c = 0; c < kTcBN / 32; ++c) {
-                float v[32];
-                tc_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(ab * kTcBN + 32 * c), v);
-                const int mb = m0 + 32 * c;
-                if (n < p.N && !flags[0]) {
+            const bool nok = n < p.N;
+            // the scales first: their loads complete while the accumulator fills; the
+            // warp's activation-row scales (rows 16 c + i, c = half + 2 k) go to its own
+            // 128-float area of shared memory
+            const float wsn = nok && p.ks == 1 ? __ldg(p.wis + n) : 0.0f;
+            float* asc = reinterpret_cast<float*>(sm + p.off_bar + 512) + ew * (kTcBXMax / 2);
+            if (p.ks == 1) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int m = mb + i;
-                        if (m < p.M) p.y[(long long)m * p.N + n] = v[i] * wsn * __ldg(p.ais + m);
-                    }
+                for (int k = 0; k < kTcBXMax / 64; ++k) {
+                    const int j = 32 * k + lane;                  // 0..127: chunk half + 2 (j >> 4), row j & 15
+                    const int mr = 16 * (half + 2 * (j >> 4)) + (j & 15), m = m0 + mr;
+                    asc[j] = mr < p.bx && m < p.M ? __ldg(p.ais + m) : 0.0f;
                 }
             }
+            if (!mbar_wait(smem_u32(&acc_full[ab]), (uint32_t)(use & 1), flags, p.err)) break;
+            tc_fence_after();
+            __syncwarp();
+            float* dst = p.ks == 1 ? p.y : p.part + (size_t)split * p.M * p.N;
+            const uint32_t acol = tmem + tq + (uint32_t)(ab * 128);
+            uint32_t r[16];
+            if (half < nch) tc_ld16(acol + 16 * half, r);
+            for (int c = half, k = 0; c < nch; c += 2, ++k) {
+                tc_wait_ld();
+                float v[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+                if (c + 2 < nch) tc_ld16(acol + 16 * (c + 2), r);  // the next chunk's load overlaps the stores
+                const int mb = m0 + 16 * c;
+                if (nok && !flags[0]) {
+                    float* yr = dst + (size_t)mb * p.N + n;
+                    const float* ak = asc + 16 * k;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        if (mb + i < p.M) yr[(size_t)i * p.N] = p.ks == 1 ? v[i] * wsn * ak[i] : v[i];
+                }
+            }
+            __syncwarp();  // the scale area is rewritten for the next unit
             tc_fence_before();
-            mbar_arrive(smem_u32(&acc_empty[ab]));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&acc_empty[ab]));
+            if (p.ks > 1) {
+                // the unit that completes the tile sums its ks partials in slice order
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(epi_done));
+                if (ew == 0 && lane == 0) {
+                    int owner = 0;
+                    if (mbar_wait(smem_u32(epi_done), (uint32_t)(fix & 1), flags, p.err)) {
+                        __threadfence();
+                        owner = atomicAdd(p.cnt + tile, 1u) == (unsigned)(p.ks - 1);
+                    }
+                    flags[1] = owner;
+                    mbar_arrive(smem_u32(fix_ready));
+                }
+                if (!mbar_wait(smem_u32(fix_ready), (uint32_t)(fix & 1), flags, p.err)) break;
+                ++fix;
+                if (flags[1]) {
+                    __threadfence();
+                    tc_fixup(p, ew * 32 + lane, m0, n0);
+                }
+            }
         }
     } else {
         // ------------------------------ converters ------------------------------
-        // warp cw: TMEM lane quarter cw & 3 (weight rows 32 (cw & 3) + lane), values
-        // 32 j..32 j+31 of each 64-K stage with j = cw >> 2
+        // warp cw: TMEM lane quarter cw & 3 (weight rows 32 (cw & 3) + lane), the
+        // stages of parity cw >> 2 of every raw stage
         const int cw = warp - (2 + kTcEpiWarps);
-        const int q = warp & 3, j = cw >> 2;
-        const int n = 32 * q + lane;
-        long long g = 0, rg = 0;
+        const int q = warp & 3, grp = cw >> 2;
+        const int nrow = 32 * q + lane;
+        const uint32_t tq = (uint32_t)(32 * q) << 16;
+        long long g0 = 0, rg = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x) {
-            const int n0 = (tile / p.mtiles) * kTcBM;
-            const float wsc = n0 + n < p.N ? __frcp_rn(__ldg(p.wis + n0 + n)) : 1.0f;  // 2^s (exact)
-            for (int kt = 0; kt < kt_n && ok; ++kt, ++g) {
-                const int sub = kt & 3;
-                const int rs = (int)(rg % kTcRS);
-                if (sub == 0) ok = mbar_wait(smem_u32(&r_full[rs]), (uint32_t)((rg / kTcRS) & 1), flags, p.err);
-                const int s = (int)(g % kTcMS);
-                if (ok && g >= kTcMS) ok = mbar_wait(smem_u32(&m_empty[s]), (uint32_t)(((g / kTcMS) - 1) & 1), flags, p.err);
+        for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
+            const int tile = u % p.tiles;
+            const int n0 = (tile / p.mtiles) * kTcBW;
+            const float wsc = n0 + nrow < p.N ? __frcp_rn(__ldg(p.wis + n0 + nrow)) : 1.0f;  // 2^s (exact)
+            int r0, r1;
+            tc_slice(p, u / p.tiles, r0, r1);
+            for (int r = r0; r < r1 && ok; ++r, ++rg, g0 += kTcSub) {
+                const int rs = (int)(rg % p.nraw);
+                ok = mbar_wait(smem_u32(&r_full[rs]), (uint32_t)((rg / p.nraw) & 1), flags, p.err);
                 if (!ok) break;
-                tc_fence_after();
-                const uint8_t* rrow = raw(rs) + n * p.raw_row;
-                uint32_t h[16], l[16];
-                if (WT == T_Q8_0) tc_conv_q8_0(rrow + (2 * sub + j) * 34, wsc, h, l);
-                else tc_conv_q4_k(rrow, sub, j, wsc, h, l);
-                const uint32_t col = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(kTcWCol0 + s * kTcWCols + 16 * j);
-                tc_st16(col, h);
-                tc_st16(col + kTcBK / 2, l);
-                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-                tc_fence_before();
+                const uint8_t* rrow = raw(rs) + nrow * p.raw_row;
+                ok = grp == 0 ? tc_convert_raw<WT, 0>(rrow, wsc, g0, tq, tmem, full, empty, flags, p.err, lane)
+                              : tc_convert_raw<WT, 1>(rrow, wsc, g0, tq, tmem, full, empty, flags, p.err, lane);
                 __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&w_full[s]));  // one arrival per converter warp
-                if (sub == 3) {
-                    if (lane == 0) mbar_arrive(smem_u32(&r_empty[rs]));
-                    ++rg;
-                }
+                if (lane == 0) mbar_arrive(smem_u32(&r_empty[rs]));
             }
         }
     }
@@ -388,21 +577,16 @@ __device__ __forceinline__ float tc_row_iscale(float amax) {
     return ldexpf(1.0f, -s);
 }
 
-__device__ __forceinline__ void tc_split_store(float v0, float v1, __half* hi, __half* lo) {
-    const __half2 h = __floats2half2_rn(v0, v1);
-    const float2 hf = __half22float2(h);
-    *reinterpret_cast<__half2*>(hi) = h;
-    *reinterpret_cast<__half2*>(lo) = __floats2half2_rn(v0 - hf.x, v1 - hf.y);
-}
-
 // blocks [0, M): activation rows; blocks [M, M + ceil(N / 8)): 8 weight rows each (a warp per row)
 template <int WT, int AM>
 __global__ void __launch_bounds__(kTcPrepThreads) tc_prep_kernel(const float* __restrict__ x, const uint8_t* __restrict__ wq,
                                                                  int M, int N, int K, __half* ahi, __half* alo,
-                                                                 float* ais, float* wis) {
+                                                                 float* ais, float* wis, unsigned* cnt, int ncnt) {
     grid_dep_launch();
     __shared__ float red[kTcPrepThreads / 32];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (blockIdx.x == 0)
+        for (int i = tid; i < ncnt; i += kTcPrepThreads) cnt[i] = 0u;  // split-K arrival counters
     if ((int)blockIdx.x < M) {
         const int m = blockIdx.x;
         const float* xr = x + (long long)m * K;
@@ -424,43 +608,56 @@ __global__ void __launch_bounds__(kTcPrepThreads) tc_prep_kernel(const float* __
         if (tid == 0) ais[m] = is;
         __half* hr = ahi + (long long)m * K;
         __half* lr = alo + (long long)m * K;
-        if (AM == A_F32) {
-            for (int i = tid; i < K / 2; i += kTcPrepThreads) {
-                const float2 v = __ldg(reinterpret_cast<const float2*>(xr) + i);
-                tc_split_store(__fmul_rn(v.x, sc), __fmul_rn(v.y, sc), hr + 2 * i, lr + 2 * i);
+        // thread t: values 16 g .. 16 g + 15 with g = t + 256 i (a Q8_0 block is two
+        // neighbouring threads, a Q8K block sixteen); 32-byte stores of both pieces
+        const int ng = K / 16;
+        for (int g0 = 0; g0 < ng; g0 += kTcPrepThreads) {
+            const int g = g0 + tid;
+            const bool on = g < ng;
+            float v[16];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float4 t = on ? __ldg(reinterpret_cast<const float4*>(xr + 16 * g) + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+                v[4 * i] = t.x;
+                v[4 * i + 1] = t.y;
+                v[4 * i + 2] = t.z;
+                v[4 * i + 3] = t.w;
             }
-        } else if (WT == T_Q8_0) {
-            for (int b = tid; b < K / 32; b += kTcPrepThreads) {
-                uint32_t c[8];
-                float d;
-                quant_q8_0_32(xr + b * 32, c, d);
-                const float ds = h2f(f2h(d)) * sc;  // f(d_a) 2^s: exact
+            if (AM == A_F32) {
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
+                for (int i = 0; i < 16; ++i) v[i] = __fmul_rn(v[i], sc);
+            } else {
+                float bm = 0.0f;
 #pragma unroll
-                    for (int e = 0; e < 4; e += 2) {
-                        const float q0 = (float)(int8_t)(c[i] >> (8 * e)), q1 = (float)(int8_t)(c[i] >> (8 * e + 8));
-                        tc_split_store(ds * q0, ds * q1, hr + b * 32 + 4 * i + e, lr + b * 32 + 4 * i + e);
-                    }
-            }
-        } else {
-            // Q8K: a warp per super-block, lane l values 8l..8l+7
-            for (int sb = warp; sb < K / 256; sb += kTcPrepThreads / 32) {
-                const float* src = xr + sb * 256 + 8 * lane;
-                const float4 v0 = __ldg(reinterpret_cast<const float4*>(src));
-                const float4 v1 = __ldg(reinterpret_cast<const float4*>(src) + 1);
-                float bm = fmaxf(fmaxf(fmaxf(fabsf(v0.x), fabsf(v0.y)), fmaxf(fabsf(v0.z), fabsf(v0.w))),
-                                 fmaxf(fmaxf(fabsf(v1.x), fabsf(v1.y)), fmaxf(fabsf(v1.z), fabsf(v1.w))));
-#pragma unroll
-                for (int o = 16; o; o >>= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, o));
+                for (int i = 0; i < 16; ++i) bm = fmaxf(bm, fabsf(v[i]));
+                bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 1));  // Q8_0: the block's other half
+                if (WT != T_Q8_0) {                                      // Q8K: sixteen threads
+                    bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 2));
+                    bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
+                    bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 8));
+                }
                 float d, id;
                 q8_scale(bm, d, id);
-                const float vv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-                const long long k = (long long)sb * 256 + 8 * lane;
+                const float ds = (WT == T_Q8_0 ? h2f(f2h(d)) : d) * sc;  // f(d_a) 2^s (Q8_0 keeps d as f16)
 #pragma unroll
-                for (int e = 0; e < 8; e += 2)
-                    tc_split_store(__fmul_rn(d * (float)q8_code(vv[e], id), sc), __fmul_rn(d * (float)q8_code(vv[e + 1], id), sc),
-                                   hr + k + e, lr + k + e);
+                for (int i = 0; i < 16; ++i) v[i] = WT == T_Q8_0 ? ds * (float)q8_code(v[i], id) : __fmul_rn(d * (float)q8_code(v[i], id), sc);
+            }
+            if (on) {
+                uint32_t hw[8], lw[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const __half2 h = __floats2half2_rn(v[2 * i], v[2 * i + 1]);
+                    const float2 hf = __half22float2(h);
+                    const __half2 l = __floats2half2_rn(v[2 * i] - hf.x, v[2 * i + 1] - hf.y);
+                    hw[i] = *reinterpret_cast<const uint32_t*>(&h);
+                    lw[i] = *reinterpret_cast<const uint32_t*>(&l);
+                }
+                uint4* ho = reinterpret_cast<uint4*>(hr + 16 * g);
+                uint4* lo = reinterpret_cast<uint4*>(lr + 16 * g);
+                ho[0] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                ho[1] = make_uint4(hw[4], hw[5], hw[6], hw[7]);
+                lo[0] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                lo[1] = make_uint4(lw[4], lw[5], lw[6], lw[7]);
             }
         }
     } else {
@@ -491,32 +688,83 @@ struct TcPlan {
     TcParams p;
     int grid;
     size_t smem;
-    size_t ws_ahi, ws_alo, ws_ais, ws_wis, workspace;
+    size_t ws_ahi, ws_alo, ws_ais, ws_wis, ws_part, ws_cnt, workspace;
 };
 
+// Modelled SM cycles of one work unit of `nr` raw stages: the MMA time of a
+// stage (six M 128 x N bx x K 16 MMAs, 128 cycles at N 256) with a floor for
+// the issuing thread (about 560 cycles a stage below N ~ 192); the
+// accumulator hand-off (the epilogue's drain when there is one accumulator);
+// with K split, the unit's share of the fix-up (ks + 1 partial-tile
+// transfers through L2 at ~100 B a cycle, done once per tile).
+inline double tc_unit_cycles(int bx, int nacc, int ks, int nr) {
+    const double stage = bx * 3.0 > 560.0 ? bx * 3.0 : 560.0;
+    double c = nr * kTcSub * stage + (nacc == 1 ? 2000.0 : 300.0);
+    if (ks > 1) c += (ks + 1) * bx * 5.12 / ks;
+    return c;
+}
+
 inline bool plan_tc(int wt, int am, long long M, long long N, long long K, int sm_count, int smem_max, TcPlan& out) {
-    if (K % kTcRK != 0 || M < 9 || K > (1 << 26)) return false;
+    if (K % kTcRK != 0 || M < 9 || K > (1 << 26) || M > (1 << 24) || N > (1 << 24)) return false;
     TcPlan pl{};
     TcParams& p = pl.p;
     p.M = (int)M;
     p.N = (int)N;
     p.K = (int)K;
-    p.mtiles = (int)((M + kTcBM - 1) / kTcBM);
-    p.ntiles = (int)((N + kTcBN - 1) / kTcBN);
+    p.mtiles = (int)((M + kTcBXMax - 1) / kTcBXMax);
+    p.bx = round_up((int)((M + p.mtiles - 1) / p.mtiles), 16);
+    p.nacc = p.bx <= 128 ? 2 : 1;
+    p.ntiles = (int)((N + kTcBW - 1) / kTcBW);
     p.tiles = p.mtiles * p.ntiles;
+    p.nrs = (int)(K / kTcRK);
     p.raw_row = wt == T_Q8_0 ? kTcRK / 32 * 34 : 144;
-    p.raw_stage = round_up(kTcBN * p.raw_row + 64, 1024);  // Q8_0 word loads reach 4 bytes past a row
-    p.off_raw = kTcMS * kTcStageBytes;  // activation pieces; weight pieces live in TMEM
-    p.off_bar = p.off_raw + kTcRS * p.raw_stage;
-    pl.smem = (size_t)p.off_bar + 512 + 1024;  // barriers, TMEM slot, flags; alignment slack
-    if ((long long)pl.smem > smem_max) return false;
-    pl.grid = p.tiles < sm_count ? p.tiles : sm_count;
+    p.raw_stage = round_up(kTcBW * p.raw_row, 1024);
+    p.piece = p.bx * 64;
+    p.off_raw = kTcS * 2 * p.piece;  // activation pieces; weight pieces live in TMEM
+    const int fixed = 512 + kTcEpiWarps * kTcBXMax / 2 * 4 + 1024;  // barriers, TMEM slot, flags; epilogue scales; alignment slack
+    p.nraw = (smem_max - p.off_raw - fixed) / p.raw_stage;
+    if (p.nraw > kTcRSMax) p.nraw = kTcRSMax;
+    if (p.nraw < 2) return false;
+    p.off_bar = p.off_raw + p.nraw * p.raw_stage;
+    pl.smem = (size_t)p.off_bar + fixed;
+    // K slices: the smallest ks whose modelled makespan (units dealt round-robin
+    // to one CTA per SM) is within 2 % of the best
+    double best = 0.0;
+    int best_ks = 1;
+    const int kmax = p.nrs < kTcMaxSplit ? p.nrs : kTcMaxSplit;
+    double cost[kTcMaxSplit + 1] = {};
+    for (int ks = 1; ks <= kmax; ++ks) {
+        const long long units = (long long)p.tiles * ks;
+        const int grid = units < sm_count ? (int)units : sm_count;
+        double worst = 0.0;
+        for (int c = 0; c < grid; ++c) {
+            double t = 0.0;
+            for (long long u = c; u < units; u += grid) {
+                const int split = (int)(u / p.tiles);
+                const int nr = (split + 1) * p.nrs / ks - split * p.nrs / ks;
+                t += tc_unit_cycles(p.bx, p.nacc, ks, nr);
+            }
+            if (t > worst) worst = t;
+        }
+        cost[ks] = worst;
+        if (ks == 1 || worst < best) best = worst;
+    }
+    for (int ks = 1; ks <= kmax; ++ks)
+        if (cost[ks] <= best * 1.02) {
+            best_ks = ks;
+            break;
+        }
+    p.ks = best_ks;
+    p.units = p.tiles * p.ks;
+    pl.grid = p.units < sm_count ? p.units : sm_count;
     auto r256 = [](size_t v) { return (v + 255) / 256 * 256; };
     pl.ws_ahi = 0;
     pl.ws_alo = r256((size_t)M * K * 2);
     pl.ws_ais = pl.ws_alo + r256((size_t)M * K * 2);
     pl.ws_wis = pl.ws_ais + r256((size_t)M * 4);
-    pl.workspace = pl.ws_wis + r256((size_t)N * 4);
+    pl.ws_part = pl.ws_wis + r256((size_t)N * 4);
+    pl.ws_cnt = pl.ws_part + (p.ks > 1 ? r256((size_t)p.ks * M * N * 4) : 0);
+    pl.workspace = pl.ws_cnt + (p.ks > 1 ? r256((size_t)p.tiles * 4) : 0);
     (void)am;
     out = pl;
     return true;

@@ -122,6 +122,9 @@ MATMUL_CASES = [
     ("q4_k", 100, 48, 1024),
     ("q8_0", 300, 260, 2048),     # prefill tiles: 3 x 3 with ragged edges in both
     ("q4_k", 200, 300, 1024),
+    ("q8_0", 256, 384, 2048),     # 256-row activation tiles, one accumulator
+    ("q4_k", 520, 130, 1024),     # three activation tiles of 176 rows, ragged weight tile
+    ("q4_k", 9, 1000, 512),       # smallest prefill M (16-row activation tile)
 ]
 
 
@@ -149,6 +152,19 @@ def test_prefill_special_rows(qmm, orc, wtype, K, mode):
     y = host(qmm.matmul(dev(wq), dev(x), wtype, mode, N=w.shape[0]))
     y_orc, T = orc.matmul(wtype, mode, wq, x)
     assert_within_bound(y, y_orc, T, f"{wtype} {mode} special rows")
+    check_device_error(qmm)
+
+
+@pytest.mark.parametrize("wtype,M,N,K", [("q8_0", 64, 300, 4096), ("q4_k", 256, 200, 2048)])
+def test_prefill_split_k_is_deterministic(qmm, orc, wtype, M, N, K):
+    """Few output tiles split K across CTAs; the tile's last unit sums the
+    partial tiles in slice order, so repeated calls agree bit for bit."""
+    w = qmm_synth.weights(N, K, seed=3)
+    x = dev(qmm_synth.activations(M, K, seed=4, outlier_channels=4))
+    wq = dev(orc.quantize(wtype, w))
+    for mode in ("int8_act", "f32_act"):
+        ys = [host(qmm.matmul(wq, x, wtype, mode, N=N)) for _ in range(3)]
+        assert np.array_equal(ys[0], ys[1]) and np.array_equal(ys[0], ys[2])
     check_device_error(qmm)
 
 
@@ -237,7 +253,8 @@ def test_error_statuses_on_device(qmm, orc):
 # ---------------------------------------------------------------------------
 
 FULL = [("q4_k", 28672, 8192, 8), ("q8_0", 28672, 8192, 8), ("q8_0", 14336, 4096, 1024),
-        ("q4_k", 4096, 4096, 256), ("q8_0", 49152, 576, 1)]
+        ("q4_k", 14336, 4096, 1024), ("q8_0", 14336, 4096, 256), ("q4_k", 4096, 4096, 256),
+        ("q8_0", 4096, 4096, 16), ("q8_0", 49152, 576, 1)]
 
 
 @pytest.mark.parametrize("wtype,N,K,M", FULL)
