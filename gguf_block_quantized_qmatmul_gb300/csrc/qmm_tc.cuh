@@ -691,16 +691,16 @@ struct TcPlan {
     size_t ws_ahi, ws_alo, ws_ais, ws_wis, ws_part, ws_cnt, workspace;
 };
 
-// Modelled SM cycles of one work unit of `nr` raw stages: the MMA time of a
-// stage (six M 128 x N bx x K 16 MMAs, 128 cycles at N 256) with a floor for
-// the issuing thread (about 560 cycles a stage below N ~ 192); the
-// accumulator hand-off (the epilogue's drain when there is one accumulator);
-// with K split, the unit's share of the fix-up (ks + 1 partial-tile
-// transfers through L2 at ~100 B a cycle, done once per tile).
-inline double tc_unit_cycles(int bx, int nacc, int ks, int nr) {
-    const double stage = bx * 3.0 > 560.0 ? bx * 3.0 : 560.0;
-    double c = nr * kTcSub * stage + (nacc == 1 ? 2000.0 : 300.0);
-    if (ks > 1) c += (ks + 1) * bx * 5.12 / ks;
+// Modelled SM cycles of one work unit of `nr` raw stages (fitted to GB300
+// timings): a stage costs six M 128 x N bx x K 16 MMAs at ~3.5 cycles per
+// activation row, with a floor of ~560 cycles for the issuing thread at small
+// N; a unit adds its accumulator hand-off (the epilogue's drain of a single
+// accumulator stalls the MMAs); a split tile's last unit also sums the ks
+// partial tiles, at ~24 B a cycle through L2.
+inline double tc_unit_cycles(int bx, int nacc, int ks, int nr, bool last) {
+    const double stage = bx * 3.5 > 560.0 ? bx * 3.5 : 560.0;
+    double c = nr * kTcSub * stage + (nacc == 1 ? 6000.0 : 1500.0);
+    if (ks > 1 && last) c += ks * bx * (kTcBW * 4.0 / 24.0);
     return c;
 }
 
@@ -742,7 +742,7 @@ inline bool plan_tc(int wt, int am, long long M, long long N, long long K, int s
             for (long long u = c; u < units; u += grid) {
                 const int split = (int)(u / p.tiles);
                 const int nr = (split + 1) * p.nrs / ks - split * p.nrs / ks;
-                t += tc_unit_cycles(p.bx, p.nacc, ks, nr);
+                t += tc_unit_cycles(p.bx, p.nacc, ks, nr, split == ks - 1);
             }
             if (t > worst) worst = t;
         }
