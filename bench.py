@@ -13,7 +13,7 @@ bandwidth, the oracle's throughput on the host cores on a bounded sample, an
 end-to-end figure through the public API with pinned host buffers (x copied in
 and y copied out on every call), SM clocks sampled during the timed region,
 and a per-(type, form, M) breakdown.  A prefill section times the Llama-shaped
-int8_act GEMMs (4096 x 4096 and 14336 x 4096 weights, M = 16, 37, 64, 256,
+GEMMs in both forms (4096 x 4096 and 14336 x 4096 weights, M = 16, 37, 64, 256,
 1024) as TOPS, with the tensor work of the three f16 passes against the
 measured bf16 peak.
 
@@ -416,7 +416,7 @@ def run_ours(args):
     e2e_s = allmax(world, time.perf_counter() - t0)
     e2e = world * bytes_per_step * args.steps / e2e_s / 1e9
 
-    # prefill (Llama-shaped, int8_act): TOPS = 2 M N K / time. The tensor cores run
+    # prefill (Llama-shaped, both forms): TOPS = 2 M N K / time. The tensor cores run
     # three f16 passes (hi.hi, hi.lo, lo.hi) of that product, so the tensor work is
     # 3 x 2 M N K; its rate is compared with the measured dense bf16 peak (f16 runs
     # at the bf16 rate).
@@ -428,23 +428,23 @@ def run_ours(args):
                 w = torch.randn((N, 4096), generator=g, device="cuda") * 0.02
                 wq = q.quantize_weights(w, t)
                 del w
-                for M in (16, 37, 64, 256, 1024):
+                for M, mode in [(m, f) for f in ("int8_act", "f32_act") for m in (16, 37, 64, 256, 1024)]:
                     x = torch.from_numpy(qmm_synth.activations(M, 4096, outlier_channels=4)).cuda()
                     y = torch.empty((M, N), dtype=torch.float32, device="cuda")
-                    need = q.matmul_workspace(t, "int8_act", M, N, 4096)
+                    need = q.matmul_workspace(t, mode, M, N, 4096)
                     wsp = torch.empty(max(need, 16), dtype=torch.uint8, device="cuda")
                     for _ in range(3):
-                        q.matmul(wq, x, t, "int8_act", N=N, out=y, workspace=wsp)
+                        q.matmul(wq, x, t, mode, N=N, out=y, workspace=wsp)
                     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                     reps = 10
                     e0.record(stream)
                     for _ in range(reps):
-                        q.matmul(wq, x, t, "int8_act", N=N, out=y, workspace=wsp)
+                        q.matmul(wq, x, t, mode, N=N, out=y, workspace=wsp)
                     e1.record(stream)
                     torch.cuda.synchronize()
                     ms = e0.elapsed_time(e1) / reps
                     tops = 2.0 * M * N * 4096 / (ms / 1e3) / 1e12
-                    prefill[f"{t}/int8_act/M{M}/{N}x4096"] = {
+                    prefill[f"{t}/{mode}/M{M}/{N}x4096"] = {
                         "ms": round(ms, 4), "TOPS": round(tops, 1),
                         "tensor_TFLOPs": round(3 * tops, 1),
                         "tensor_frac_of_bf16_peak": round(3 * tops / bf16_peak, 4),

@@ -26,7 +26,8 @@
  *  codes, 16 int16 sums of 16 codes) follow the public GGUF layout.
  *
  * Readings where the pages are silent (listed with the others in the design
- * notes): rounding of codes is round-half-away-from-zero (C roundf); codes of
+ * notes): Q4_0 and Q5_0 use the public GGUF block layouts and the signed-max
+ * quantizer written below; rounding of codes is round-half-away-from-zero (C roundf); codes of
  * Q8_0/Q8K use the f32 scale d and the reciprocal 1/d; Q8K is symmetric
  * (+-127); Q4_K uses the closed-form min/max quantizer written below; the
  * dequantized Q4_K weight is (f(d)*sc)*q - f(dmin)*m with each product exact
@@ -53,7 +54,7 @@
 #endif
 
 /* type ids used only inside the oracle and its Python wrapper */
-enum { ORC_Q8_0 = 1, ORC_Q4_K = 2, ORC_Q8_K = 3 };
+enum { ORC_Q8_0 = 1, ORC_Q4_K = 2, ORC_Q8_K = 3, ORC_Q4_0 = 4, ORC_Q5_0 = 5 };
 
 /* bytes of one block and values per block (page [p3] sizes; GGUF layout) */
 #define ORC_Q8_0_VALS 32
@@ -61,6 +62,8 @@ enum { ORC_Q8_0 = 1, ORC_Q4_K = 2, ORC_Q8_K = 3 };
 #define ORC_QK_VALS 256
 #define ORC_Q4_K_BYTES 144
 #define ORC_Q8_K_BYTES 292
+#define ORC_Q4_0_BYTES 18   /* page [p3] file sizes: Q4_0 18 B per 32 values */
+#define ORC_Q5_0_BYTES 22   /* Q5_0 22 B per 32 values */
 
 /* ------------------------------------------------------------------ */
 /* IEEE-754 binary16 <-> binary32, written from the format definition  */
@@ -158,11 +161,18 @@ int64_t orc_f16_check_range(uint64_t lo, uint64_t hi) {
 /* ------------------------------------------------------------------ */
 
 int64_t orc_block_values(int t) {
-    return t == ORC_Q8_0 ? ORC_Q8_0_VALS : (t == ORC_Q4_K || t == ORC_Q8_K) ? ORC_QK_VALS : 0;
+    return (t == ORC_Q8_0 || t == ORC_Q4_0 || t == ORC_Q5_0) ? 32 : (t == ORC_Q4_K || t == ORC_Q8_K) ? ORC_QK_VALS : 0;
 }
 
 int64_t orc_block_bytes(int t) {
-    return t == ORC_Q8_0 ? ORC_Q8_0_BYTES : t == ORC_Q4_K ? ORC_Q4_K_BYTES : t == ORC_Q8_K ? ORC_Q8_K_BYTES : 0;
+    switch (t) {
+        case ORC_Q8_0: return ORC_Q8_0_BYTES;
+        case ORC_Q4_K: return ORC_Q4_K_BYTES;
+        case ORC_Q8_K: return ORC_Q8_K_BYTES;
+        case ORC_Q4_0: return ORC_Q4_0_BYTES;
+        case ORC_Q5_0: return ORC_Q5_0_BYTES;
+        default: return 0;
+    }
 }
 
 static void put_u16(uint8_t* p, uint16_t v) { p[0] = (uint8_t)(v & 0xff); p[1] = (uint8_t)(v >> 8); }
@@ -228,6 +238,80 @@ void orc_quantize_q8_k(const float* x, int64_t rows, int64_t K, uint8_t* out) {
     for (int64_t r = 0; r < rows; ++r)
         for (int64_t b = 0; b < nb; ++b)
             q8_k_block(x + r * K + b * 256, out + (r * nb + b) * ORC_Q8_K_BYTES);
+}
+
+/* ------------------------------------------------------------------ */
+/* Q4_0 / Q5_0: 32 values, f16 d, 4- or 5-bit codes with an offset      */
+/* ([p1] 出处: these weights pair with Q8_0 activations; [p3] 大小和误差: */
+/* 18 and 22 bytes per 32 values).  The pages give neither the layout   */
+/* nor the quantizer.  Layout (public GGUF): bytes 0-1 f16 d; Q5_0 then  */
+/* 4 bytes whose little-endian word holds bit 4 of code i at bit i;     */
+/* then 16 bytes, byte j = code j (low nibble) | code j + 16 (high).    */
+/* Quantizer (a reading): with off = 8 (Q4_0) or 16 (Q5_0), the value  */
+/* m of largest magnitude (the first on ties, sign kept) gives          */
+/* d = m / -off, so m maps to code 0 and the signed grid -off..off-1 is */
+/* used in full; code = roundf(x * (1/d)) + off, clamped to             */
+/* [0, 2 off - 1]; the weight is f(d) * (code - off).                   */
+/* ------------------------------------------------------------------ */
+
+static void x_0_block(const float* x, int off, uint8_t* out) {
+    float amax = 0.0f, m = 0.0f;
+    for (int i = 0; i < 32; ++i) {
+        float a = fabsf(x[i]);
+        if (a > amax) { amax = a; m = x[i]; }
+    }
+    float d = m / (float)(-off);
+    float id = d != 0.0f ? 1.0f / d : 0.0f;
+    put_u16(out, orc_f32_to_f16(d));
+    int c[32];
+    for (int i = 0; i < 32; ++i) {
+        float r = roundf(x[i] * id) + (float)off;
+        if (r < 0.0f) r = 0.0f;
+        if (r > (float)(2 * off - 1)) r = (float)(2 * off - 1);
+        c[i] = (int)r;
+    }
+    uint8_t* qs = out + 2;
+    if (off == 16) {
+        uint32_t h = 0;
+        for (int i = 0; i < 32; ++i) h |= (uint32_t)((c[i] >> 4) & 1) << i;
+        out[2] = (uint8_t)(h & 0xff);
+        out[3] = (uint8_t)((h >> 8) & 0xff);
+        out[4] = (uint8_t)((h >> 16) & 0xff);
+        out[5] = (uint8_t)(h >> 24);
+        qs = out + 6;
+    }
+    for (int j = 0; j < 16; ++j) qs[j] = (uint8_t)((c[j] & 15) | ((c[j + 16] & 15) << 4));
+}
+
+static void quantize_x_0(const float* x, int64_t rows, int64_t K, int off, int bytes, uint8_t* out) {
+    int64_t nb = K / 32;
+    #pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t b = 0; b < nb; ++b) x_0_block(x + r * K + b * 32, off, out + (r * nb + b) * bytes);
+}
+
+void orc_quantize_q4_0(const float* x, int64_t rows, int64_t K, uint8_t* out) { quantize_x_0(x, rows, K, 8, ORC_Q4_0_BYTES, out); }
+void orc_quantize_q5_0(const float* x, int64_t rows, int64_t K, uint8_t* out) { quantize_x_0(x, rows, K, 16, ORC_Q5_0_BYTES, out); }
+
+/* signed codes (code - off) of a Q4_0 / Q5_0 block */
+static void x_0_codes(int t, const uint8_t* blk, int c[32]) {
+    const int off = t == ORC_Q5_0 ? 16 : 8;
+    const uint8_t* qs = blk + (t == ORC_Q5_0 ? 6 : 2);
+    uint32_t h = 0;
+    if (t == ORC_Q5_0) h = (uint32_t)blk[2] | ((uint32_t)blk[3] << 8) | ((uint32_t)blk[4] << 16) | ((uint32_t)blk[5] << 24);
+    for (int j = 0; j < 16; ++j) {
+        c[j] = ((qs[j] & 15) | (int)(((h >> j) & 1) << 4)) - off;
+        c[j + 16] = ((qs[j] >> 4) | (int)(((h >> (j + 16)) & 1) << 4)) - off;
+    }
+}
+
+/* signed codes of any 32-value weight block (Q8_0, Q4_0, Q5_0) */
+static void b32_codes(int t, const uint8_t* blk, int c[32]) {
+    if (t == ORC_Q8_0) {
+        for (int i = 0; i < 32; ++i) c[i] = (int8_t)blk[2 + i];
+    } else {
+        x_0_codes(t, blk, c);
+    }
 }
 
 /* ------------------------------------------------------------------ */
@@ -334,6 +418,15 @@ static void dequant_row(int t, const uint8_t* q, int64_t K, float* out) {
             float d = orc_f16_to_f32(get_u16(blk));
             for (int i = 0; i < 32; ++i) out[b * 32 + i] = d * (float)(int8_t)blk[2 + i];
         }
+    } else if (t == ORC_Q4_0 || t == ORC_Q5_0) {
+        const int64_t bytes = orc_block_bytes(t);
+        for (int64_t b = 0; b < K / 32; ++b) {
+            const uint8_t* blk = q + b * bytes;
+            float d = orc_f16_to_f32(get_u16(blk));
+            int c[32];
+            x_0_codes(t, blk, c);
+            for (int i = 0; i < 32; ++i) out[b * 32 + i] = d * (float)c[i];  /* exact: 11 x 5 bits */
+        }
     } else if (t == ORC_Q8_K) {
         for (int64_t b = 0; b < K / 256; ++b) {
             const uint8_t* blk = q + b * ORC_Q8_K_BYTES;
@@ -374,12 +467,15 @@ void orc_dequantize(int t, const uint8_t* q, int64_t rows, int64_t K, float* out
 /*                out[m][n][s][1] = S_m  = sum_j m_j * (bsum_2j+bsum_2j+1)*/
 /* ------------------------------------------------------------------ */
 
-static void sums_q8_0(const uint8_t* wrow, const uint8_t* arow, int64_t nb, int32_t* out) {
+/* any 32-value weight block (Q8_0, Q4_0, Q5_0) against Q8_0 activations */
+static void sums_b32(int t, const uint8_t* wrow, const uint8_t* arow, int64_t nb, int32_t* out) {
+    const int64_t wb = orc_block_bytes(t);
     for (int64_t b = 0; b < nb; ++b) {
-        const uint8_t* w = wrow + b * ORC_Q8_0_BYTES;
         const uint8_t* a = arow + b * ORC_Q8_0_BYTES;
+        int c[32];
+        b32_codes(t, wrow + b * wb, c);
         int32_t s = 0;
-        for (int i = 0; i < 32; ++i) s += (int32_t)(int8_t)w[2 + i] * (int32_t)(int8_t)a[2 + i];
+        for (int i = 0; i < 32; ++i) s += (int32_t)c[i] * (int32_t)(int8_t)a[2 + i];
         out[b] = s;
     }
 }
@@ -409,12 +505,12 @@ static void sums_q4_k(const uint8_t* wrow, const uint8_t* arow, int64_t nsb, int
    Q8_0 weights, Q8K for Q4_K weights).  out: int32 [M][N][nb] (Q8_0) or
    [M][N][nsb][2] (Q4_K). */
 void orc_block_sums(int wtype, const uint8_t* wq, const uint8_t* xq, int64_t M, int64_t N, int64_t K, int32_t* out) {
-    if (wtype == ORC_Q8_0) {
-        int64_t nb = K / 32, rb = nb * ORC_Q8_0_BYTES;
+    if (wtype != ORC_Q4_K) {
+        int64_t nb = K / 32, rbw = nb * orc_block_bytes(wtype), rba = nb * ORC_Q8_0_BYTES;
         #pragma omp parallel for schedule(static) collapse(2)
         for (int64_t m = 0; m < M; ++m)
             for (int64_t n = 0; n < N; ++n)
-                sums_q8_0(wq + n * rb, xq + m * rb, nb, out + (m * N + n) * nb);
+                sums_b32(wtype, wq + n * rbw, xq + m * rba, nb, out + (m * N + n) * nb);
     } else {
         int64_t nsb = K / 256, rbw = nsb * ORC_Q4_K_BYTES, rba = nsb * ORC_Q8_K_BYTES;
         #pragma omp parallel for schedule(static) collapse(2)
@@ -433,22 +529,21 @@ void orc_block_sums(int wtype, const uint8_t* wq, const uint8_t* xq, int64_t M, 
    integer block sums, then y = sum over blocks of scale products x sums. */
 void orc_matmul_int8_act(int wtype, const uint8_t* wq, const float* x, int64_t M, int64_t N, int64_t K,
                          double* y, double* T) {
-    if (wtype == ORC_Q8_0) {
-        int64_t nb = K / 32, rb = nb * ORC_Q8_0_BYTES;
-        uint8_t* xq = (uint8_t*)malloc((size_t)(M * rb));
+    if (wtype != ORC_Q4_K) {  /* Q8_0, Q4_0, Q5_0 weights with Q8_0 activations */
+        int64_t nb = K / 32, wb = orc_block_bytes(wtype), rbw = nb * wb, rba = nb * ORC_Q8_0_BYTES;
+        uint8_t* xq = (uint8_t*)malloc((size_t)(M * rba));
         orc_quantize_q8_0(x, M, K, xq);
         #pragma omp parallel for schedule(dynamic, 16) collapse(2)
         for (int64_t m = 0; m < M; ++m)
             for (int64_t n = 0; n < N; ++n) {
-                const uint8_t* w = wq + n * rb;
-                const uint8_t* a = xq + m * rb;
+                const uint8_t* w = wq + n * rbw;
+                const uint8_t* a = xq + m * rba;
                 double acc = 0.0, t = 0.0;
                 for (int64_t b = 0; b < nb; ++b) {
-                    int32_t s = 0;
-                    for (int i = 0; i < 32; ++i)
-                        s += (int32_t)(int8_t)w[b * 34 + 2 + i] * (int32_t)(int8_t)a[b * 34 + 2 + i];
-                    double term = (double)orc_f16_to_f32(get_u16(w + b * 34)) *
-                                  (double)orc_f16_to_f32(get_u16(a + b * 34)) * (double)s;
+                    int32_t s;
+                    sums_b32(wtype, w + b * wb, a + b * ORC_Q8_0_BYTES, 1, &s);
+                    double term = (double)orc_f16_to_f32(get_u16(w + b * wb)) *
+                                  (double)orc_f16_to_f32(get_u16(a + b * ORC_Q8_0_BYTES)) * (double)s;
                     acc += term;
                     t += fabs(term);
                 }

@@ -98,11 +98,9 @@ def test_f16_against_numpy(orc):
 
 def test_block_bytes_match_page_tensor_sizes(orc):
     """Per-tensor byte counts printed on the pages fix 34 B per 32 values
-    (Q8_0) and 144 B per 256 values (Q4K)."""
+    (Q8_0), 144 B per 256 values (Q4K) and 22 B per 32 values (Q5_0)."""
     g = json.load(open(os.path.join(GOLDEN, "page_sizes.json")))
     for e in g["tensor_groups"]:
-        if e["type"] not in ("q8_0", "q4_k"):
-            continue
         N, K = e["shape"]
         assert e["tensors"] * N * orc.row_bytes(e["type"], K) == e["bytes"], e["what"]
 
@@ -110,12 +108,11 @@ def test_block_bytes_match_page_tensor_sizes(orc):
 def test_file_sizes_close_with_block_bytes(orc):
     """Whole-file sizes on the pages: every own file = header + 61 F32 norms
     + its matrices at the type's bytes per value, with ONE header size for all
-    of them; Q8_0 and Q4K bytes come from the oracle, Q5_0 from a per-tensor
-    size, Q4_0 at 18/32; Q6K at 210 B / 256 closes the downloaded Q4_K_M."""
+    of them; Q8_0, Q4K, Q5_0 and Q4_0 bytes per value come from the oracle;
+    Q6K at 210 B / 256 closes the downloaded Q4_K_M."""
     g = json.load(open(os.path.join(GOLDEN, "page_sizes.json")))
     files = {e["what"]: e["bytes"] for e in g["files"]}
-    q5 = next(e for e in g["tensor_groups"] if e["type"] == "q5_0" and e["shape"] == [192, 576])
-    q5_bpv = q5["bytes"] / (q5["tensors"] * 192 * 576)               # 22 / 32
+    q5_bpv = orc.block_bytes("q5_0") / orc.block_values("q5_0")     # 22 / 32
     q8_bpv = orc.block_bytes("q8_0") / orc.block_values("q8_0")
     q4k_bpv = orc.block_bytes("q4_k") / orc.block_values("q4_k")
     lin = qmm_synth.smollm2_linears()[:-1]                            # 210 layer linears
@@ -125,7 +122,7 @@ def test_file_sizes_close_with_block_bytes(orc):
     header = files["own F32 GGUF"] - norms - 4 * vals
     assert 0 < header < 65536
     assert header + norms + vals * q8_bpv == files["own Q8_0 GGUF"]
-    assert header + norms + vals * 18 / 32 == files["own Q4_0 GGUF"]
+    assert header + norms + vals * orc.block_bytes("q4_0") / orc.block_values("q4_0") == files["own Q4_0 GGUF"]
     down = [(n, k) for name, n, k in lin if "ffn_down" in name]
     other = vals - sum(n * k for n, k in down)
     assert header + norms + sum(n * k for n, k in down) * q4k_bpv + other * q5_bpv == \
@@ -357,7 +354,7 @@ def test_row_permutation_permutes_blocks(orc):
     assert np.array_equal(orc.quantize("q4_k", w[perm]), orc.quantize("q4_k", w)[perm])
 
 
-@pytest.mark.parametrize("wtype,K", [("q8_0", 576), ("q4_k", 1536)])
+@pytest.mark.parametrize("wtype,K", [("q8_0", 576), ("q4_k", 1536), ("q4_0", 576), ("q5_0", 576)])
 def test_activation_rows_are_independent(orc, wtype, K):
     """Activation quantization is per row: row m's result is the same alone
     and inside a batch of 8 (contrast: per-tensor dynamic quantization)."""
@@ -370,7 +367,7 @@ def test_activation_rows_are_independent(orc, wtype, K):
         assert np.array_equal(y1[0], yb[m])
 
 
-@pytest.mark.parametrize("wtype,K", [("q8_0", 576), ("q4_k", 1536)])
+@pytest.mark.parametrize("wtype,K", [("q8_0", 576), ("q4_k", 1536), ("q4_0", 576), ("q5_0", 576)])
 def test_one_hot_activation_selects_dequantized_column(orc, wtype, K):
     """f32_act with x = e_k equals column k of the dequantized weights
     exactly (the Metal form multiplies f32 activations by dequantized
@@ -388,7 +385,7 @@ def test_one_hot_activation_selects_dequantized_column(orc, wtype, K):
 def test_f32_act_equals_dequantized_matmul(orc):
     """f32_act = x @ dequant(W)^T (the dequantize-all form), here against
     numpy's float64 matmul of the dequantized weights."""
-    for wtype, K in (("q8_0", 576), ("q4_k", 512)):
+    for wtype, K in (("q8_0", 576), ("q4_k", 512), ("q4_0", 576), ("q5_0", 576)):
         wq = orc.quantize(wtype, qmm_synth.weights(40, K))
         x = qmm_synth.activations(3, K)
         y, T = orc.matmul(wtype, "f32_act", wq, x)
@@ -424,7 +421,7 @@ def test_constant_row_closed_form(orc):
         assert (w == ref).all()
 
 
-@pytest.mark.parametrize("wtype,K", [("q8_0", 576), ("q4_k", 1536)])
+@pytest.mark.parametrize("wtype,K", [("q8_0", 576), ("q4_k", 1536), ("q5_0", 576)])
 def test_activation_quantization_error_has_the_predicted_size(orc, wtype, K):
     """The CPU form differs from the Metal form only by the activation
     rounding: each code moves x by a near-uniform error of width d_a, so the
@@ -435,7 +432,7 @@ def test_activation_quantization_error_has_the_predicted_size(orc, wtype, K):
     yi, _ = orc.matmul(wtype, "int8_act", wq, x)
     yf, _ = orc.matmul(wtype, "f32_act", wq, x)
     W = orc.dequantize(wtype, wq, K).astype(np.float64)
-    bv = 32 if wtype == "q8_0" else 256
+    bv = 256 if wtype == "q4_k" else 32
     da = np.abs(x.reshape(4, -1, bv)).max(axis=2) / 127.0
     var = (W ** 2) @ (np.repeat(da, bv, axis=1) ** 2 / 12.0).T        # [N, M]
     z = (yi - yf) / np.sqrt(var.T)
@@ -445,9 +442,121 @@ def test_activation_quantization_error_has_the_predicted_size(orc, wtype, K):
 
 def test_tolerance_scale_bounds_the_output(orc):
     """T = sum of |scaled terms| >= |y| for both forms and all outputs."""
-    for wtype, K in (("q8_0", 576), ("q4_k", 1536)):
+    for wtype, K in (("q8_0", 576), ("q4_k", 1536), ("q4_0", 576), ("q5_0", 576)):
         wq = orc.quantize(wtype, qmm_synth.weights(64, K))
         x = qmm_synth.activations(2, K)
         for mode in ("int8_act", "f32_act"):
             y, T = orc.matmul(wtype, mode, wq, x)
             assert (np.abs(y) <= T * (1 + 1e-12)).all()
+
+
+# ---------------------------------------------------------------------------
+# Q4_0 / Q5_0 (weights paired with Q8_0 activations; the pages fix their
+# sizes, 18 and 22 bytes per 32 values, not the quantizer: the signed-max
+# reading is pinned here by its closed forms and error bounds)
+# ---------------------------------------------------------------------------
+
+X0 = [("q4_0", 8), ("q5_0", 16)]
+
+
+def _x0_scale_codes(orc, t, q, K):
+    """f(d) from the block's first two bytes and the signed codes
+    dequantized / f(d) (integers when f(d) != 0)."""
+    rows = q.shape[0]
+    bb = orc.block_bytes(t)
+    blk = q.reshape(rows, K // 32, bb)
+    fd = py_f16(blk[:, :, 0].astype(np.uint16) | (blk[:, :, 1].astype(np.uint16) << 8)).astype(np.float64)
+    w = orc.dequantize(t, q, K).reshape(rows, K // 32, 32).astype(np.float64)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        c = np.where(fd[:, :, None] != 0, w / fd[:, :, None], 0.0)
+    return fd, c, w
+
+
+@pytest.mark.parametrize("t,off", X0)
+def test_x0_scale_rule_and_codes(orc, t, off):
+    """The value of largest magnitude m sets d = m / -off and gets code -off;
+    every code is an integer in [-off, off - 1] within 1/2 of x/d (the top
+    code off - 1 also takes x/d in (off - 1, off]); an all-zero block
+    dequantizes to zeros."""
+    K = 576
+    x = np.concatenate([qmm_synth.weights(64, K), qmm_synth.special_block_rows(K)]).astype(np.float32)
+    q = orc.quantize(t, x)
+    fd, c, w = _x0_scale_codes(orc, t, q, K)
+    b = x.reshape(x.shape[0], -1, 32)
+    amax = np.abs(b).max(axis=2)
+    m = np.take_along_axis(b, np.abs(b).argmax(axis=2)[:, :, None], axis=2)[:, :, 0]
+    d = (m / np.float32(-off)).astype(np.float32)
+    assert np.array_equal(fd, py_f16(d.astype(np.float16).view(np.uint16)).astype(np.float64))
+    nz = fd != 0
+    assert np.array_equal(c[nz], np.round(c[nz]))
+    assert (c[nz] >= -off).all() and (c[nz] <= off - 1).all()
+    cext = np.take_along_axis(c, np.abs(b).argmax(axis=2)[:, :, None], axis=2)[:, :, 0]
+    assert (cext[nz] == -off).all()
+    with np.errstate(divide="ignore", invalid="ignore"):
+        ratio = b.astype(np.float64) / d[:, :, None].astype(np.float64)
+    inner = nz[:, :, None] & (ratio <= off - 1)
+    assert (np.abs(c - ratio)[inner] <= 0.5 + 1e-4).all()
+    assert (np.abs(c - ratio)[nz[:, :, None] & ~(ratio <= off - 1)] <= 1.0 + 1e-4).all()
+    assert (w[amax == 0] == 0).all()
+
+
+@pytest.mark.parametrize("t,off", X0)
+def test_x0_round_trip_bound(orc, t, off):
+    """|x - dequant(quant(x))| <= |d| + off |d - f16(d)| + 2^-20 amax per
+    element (|d|/2 except for the top code), d = m / -off."""
+    K = 1536
+    x = np.concatenate([qmm_synth.weights(64, K), qmm_synth.special_block_rows(K)]).astype(np.float32)
+    q = orc.quantize(t, x)
+    fd, c, w = _x0_scale_codes(orc, t, q, K)
+    b = x.reshape(x.shape[0], -1, 32).astype(np.float64)
+    amax = np.abs(b).max(axis=2, keepdims=True)
+    m = np.take_along_axis(b, np.abs(b).argmax(axis=2)[:, :, None], axis=2)
+    d = m / -off
+    bound = np.abs(d) + off * np.abs(d - fd[:, :, None]) + 2.0 ** -20 * amax
+    assert (np.abs(b - w) <= bound).all()
+
+
+@pytest.mark.parametrize("t,off", X0)
+def test_x0_requantize_is_idempotent(orc, t, off):
+    """Re-quantizing dequantized weights reproduces the bytes: the code -off
+    element has the unique largest magnitude, so d is recovered exactly when
+    f16(d) is a normal number (all blocks here)."""
+    x = qmm_synth.weights(96, 1536)
+    q = orc.quantize(t, x)
+    fd, _, _ = _x0_scale_codes(orc, t, q, 1536)
+    assert (np.abs(fd) >= 2.0 ** -14).all()
+    assert np.array_equal(orc.quantize(t, orc.dequantize(t, q, 1536)), q)
+
+
+@pytest.mark.parametrize("t,off", X0)
+def test_x0_constant_row_closed_form(orc, t, off):
+    """A constant row c: every code is -off and the dequantized value is
+    -off f16(c / -off) (= c up to the f16 rounding of d)."""
+    for cval in (0.75, -3.0, 1e-3):
+        x = np.full((1, 64), cval, np.float32)
+        q = orc.quantize(t, x)
+        fd, c, w = _x0_scale_codes(orc, t, q, 64)
+        assert (c == -off).all()
+        ref = np.float32(np.float16(np.float32(cval) / np.float32(-off))) * np.float32(-off)
+        assert (w.astype(np.float32) == ref).all()
+
+
+@pytest.mark.parametrize("t,off", X0)
+@pytest.mark.parametrize("K", [64, 576])
+def test_x0_block_sums_equal_brute_force(orc, t, off, K):
+    """Per-block integer sums with Q8_0 activations equal Python-int brute
+    force over the signed weight codes (dequantized / f(d)) and the
+    activation codes, including all-(-off) and all-(off - 1) rows."""
+    M, N = 3, 4
+    w = qmm_synth.weights(N, K, seed=21)
+    x = qmm_synth.activations(M, K, seed=22)
+    w[0] = 1.0                                 # all codes -off
+    w[1, ::2], w[1, 1::2] = -1.0, 1.0          # codes off (clamped to off - 1) and -off
+    x[0] = -1.0
+    wq, xq = orc.quantize(t, w), orc.quantize("q8_0", x)
+    fd, c, _ = _x0_scale_codes(orc, t, wq, K)
+    ci = np.round(c).astype(np.int64)
+    assert ci.min() == -off and ci.max() == off - 1
+    a = np.stack([py_decode_q8_0(xq[m], K)[1] for m in range(M)]).astype(np.int64).reshape(M, K // 32, 32)
+    ref = np.einsum("nbi,mbi->mnb", ci, a)
+    assert np.array_equal(orc.block_sums(t, wq, xq, M, N, K), ref.astype(np.int32))
