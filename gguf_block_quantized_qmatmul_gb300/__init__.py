@@ -7,7 +7,7 @@ is no CPU fallback: the first call raises ImportError when the library is
 missing.
 
 Entry points mirror the C ABI names:
-  quantize_weights(w, wtype)      Q8_0 / Q4_K blocks of f32 weights [N, K]
+  quantize_weights(w, wtype)      Q8_0 / Q4_K / Q4_0 / Q5_0 blocks of f32 weights [N, K]
   quantize_act(x, atype)          Q8_0 / Q8_K blocks of f32 activations [M, K]
   dequantize(q, t, K)             f32 [rows, K]
   matmul(wq, x, wtype, mode)      y = x . W^T, mode "int8_act" or "f32_act"
@@ -22,9 +22,9 @@ import torch
 
 from . import build as _build
 
-QMM_F32, QMM_Q8_0, QMM_Q4_K, QMM_Q8_K = 0, 1, 2, 3
+QMM_F32, QMM_Q8_0, QMM_Q4_K, QMM_Q8_K, QMM_Q4_0, QMM_Q5_0 = 0, 1, 2, 3, 4, 5
 QMM_INT8_ACT, QMM_F32_ACT = 0, 1
-TYPES = {"f32": QMM_F32, "q8_0": QMM_Q8_0, "q4_k": QMM_Q4_K, "q8_k": QMM_Q8_K}
+TYPES = {"f32": QMM_F32, "q8_0": QMM_Q8_0, "q4_k": QMM_Q4_K, "q8_k": QMM_Q8_K, "q4_0": QMM_Q4_0, "q5_0": QMM_Q5_0}
 MODES = {"int8_act": QMM_INT8_ACT, "f32_act": QMM_F32_ACT}
 STATUS = {0: "QMM_OK", 1: "QMM_ERR_NULL", 2: "QMM_ERR_SHAPE", 3: "QMM_ERR_TYPE", 4: "QMM_ERR_ALIGN",
           5: "QMM_ERR_WORKSPACE", 6: "QMM_ERR_CUDA", 7: "QMM_ERR_TIMEOUT"}
@@ -163,7 +163,7 @@ def block_sums(wq: torch.Tensor, x: torch.Tensor, wtype, N: int | None = None, s
     M, K = x.shape
     if N is None:
         N = wq.numel() // row_bytes(wtype, K)
-    if _t(wtype) == QMM_Q8_0:
+    if _t(wtype) != QMM_Q4_K:  # 32-value blocks (Q8_0, Q4_0, Q5_0)
         out = torch.empty((M, N, K // 32), dtype=torch.int32, device=x.device)
     else:
         out = torch.empty((M, N, K // 256, 2), dtype=torch.int32, device=x.device)

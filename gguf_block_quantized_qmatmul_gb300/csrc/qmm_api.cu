@@ -43,7 +43,21 @@ cudaError_t device_info(unsigned** err, int* sms, int* smem, int* device = nullp
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
-bool valid_type(qmm_type t) { return t == QMM_Q8_0 || t == QMM_Q4_K || t == QMM_Q8_K; }
+bool valid_type(qmm_type t) {
+    return t == QMM_Q8_0 || t == QMM_Q4_K || t == QMM_Q8_K || t == QMM_Q4_0 || t == QMM_Q5_0;
+}
+// weight types: Q8_0, Q4_0, Q5_0 (with Q8_0 activations) and Q4_K (with Q8K)
+bool weight_type(qmm_type t) { return t == QMM_Q8_0 || t == QMM_Q4_K || t == QMM_Q4_0 || t == QMM_Q5_0; }
+int internal_type(qmm_type t) {
+    switch (t) {
+        case QMM_Q8_0: return T_Q8_0;
+        case QMM_Q4_K: return T_Q4_K;
+        case QMM_Q8_K: return T_Q8_K;
+        case QMM_Q4_0: return T_Q4_0;
+        case QMM_Q5_0: return T_Q5_0;
+        default: return T_F32;
+    }
+}
 
 qmm_status check_shape(qmm_type t, int64_t rows, int64_t K) {
     if (rows < 0 || K < 0) return QMM_ERR_SHAPE;
@@ -77,6 +91,14 @@ struct Dispatch {
 
 void plan_dispatch(int wt, int am, int epi, long long M, long long N, long long K, int sms, int smem, Dispatch& d) {
     d = Dispatch();
+    if (wt == T_Q4_0 || wt == T_Q5_0) {  // every shape on the streaming kernel
+        if (plan_stream(wt, am, epi, M, N, K, sms, smem, d.sp)) {
+            d.kind = KIND_STREAM;
+            d.workspace = epi == E_Y ? workspace_for(d.sp) : 0;
+            d.launches = 1;
+        }
+        return;
+    }
     if (am == A_INT8 && wt == T_Q8_0 && M <= kGemvMaxM && plan_gemv(wt, M, N, K, sms, smem, d.gp)) {  // decode: whole-row weight stream
         d.kind = KIND_GEMV;
         d.launches = 1;
@@ -131,7 +153,7 @@ qmm_status stream_call(qmm_type wtype, int am, int epi, const void* wq, const fl
     unsigned* err = nullptr;
     int sms = 0, smem = 0, dev = 0;
     if (device_info(&err, &sms, &smem, &dev) != cudaSuccess) return QMM_ERR_CUDA;
-    const int wt = wtype == QMM_Q8_0 ? T_Q8_0 : T_Q4_K;
+    const int wt = internal_type(wtype);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const Dispatch& d = get_dispatch(dev, wt, am, epi, M, N, K, sms, smem);
     if (d.kind == KIND_GEMV) {
@@ -193,7 +215,10 @@ qmm_status stream_call(qmm_type wtype, int am, int epi, const void* wq, const fl
         if (cudaMemsetAsync(pl.p.counters, 0, (size_t)pl.p.mchunks * pl.p.ntiles * 4, s) != cudaSuccess)
             return QMM_ERR_CUDA;
     }
-    const cudaError_t e = wt == T_Q8_0 ? launch_stream_q8_0(am, epi, pl, smem, s) : launch_stream_q4_k(am, epi, pl, smem, s);
+    const cudaError_t e = wt == T_Q8_0   ? launch_stream_q8_0(am, epi, pl, smem, s)
+                          : wt == T_Q4_K ? launch_stream_q4_k(am, epi, pl, smem, s)
+                          : wt == T_Q4_0 ? launch_stream_q4_0(am, epi, pl, smem, s)
+                                         : launch_stream_q5_0(am, epi, pl, smem, s);
     return e == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
 }
 
@@ -207,6 +232,8 @@ int64_t qmm_block_values(qmm_type t) {
         case QMM_Q8_0: return 32;
         case QMM_Q4_K: return 256;
         case QMM_Q8_K: return 256;
+        case QMM_Q4_0: return 32;
+        case QMM_Q5_0: return 32;
         default: return 0;
     }
 }
@@ -217,6 +244,8 @@ size_t qmm_block_bytes(qmm_type t) {
         case QMM_Q8_0: return 34;
         case QMM_Q4_K: return 144;
         case QMM_Q8_K: return 292;
+        case QMM_Q4_0: return 18;
+        case QMM_Q5_0: return 22;
         default: return 0;
     }
 }
@@ -228,13 +257,13 @@ size_t qmm_row_bytes(qmm_type t, int64_t K) {
 }
 
 qmm_status qmm_quantize_weights(qmm_type wtype, const float* w, int64_t N, int64_t K, void* wq, qmm_stream_t stream) {
-    if (wtype != QMM_Q8_0 && wtype != QMM_Q4_K) return QMM_ERR_TYPE;
+    if (!weight_type(wtype)) return QMM_ERR_TYPE;
     qmm_status st = check_shape(wtype, N, K);
     if (st != QMM_OK) return st;
     if (N == 0 || K == 0) return QMM_OK;
     if (!w || !wq) return QMM_ERR_NULL;
     if (!aligned(w, 16) || !aligned(wq, 16)) return QMM_ERR_ALIGN;
-    const int t = wtype == QMM_Q8_0 ? T_Q8_0 : T_Q4_K;
+    const int t = internal_type(wtype);
     return launch_quantize(t, w, N, K, wq, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
 }
 
@@ -256,7 +285,7 @@ qmm_status qmm_dequantize(qmm_type t, const void* q, int64_t rows, int64_t K, fl
     if (rows == 0 || K == 0) return QMM_OK;
     if (!q || !out) return QMM_ERR_NULL;
     if (!aligned(q, 16) || !aligned(out, 16)) return QMM_ERR_ALIGN;
-    const int tt = t == QMM_Q8_0 ? T_Q8_0 : t == QMM_Q4_K ? T_Q4_K : T_Q8_K;
+    const int tt = internal_type(t);
     return launch_dequantize(tt, q, rows, K, out, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? QMM_OK
                                                                                                           : QMM_ERR_CUDA;
 }
@@ -269,12 +298,12 @@ namespace {
 void dispatch_info(qmm_type wtype, qmm_act_mode mode, int64_t M, int64_t N, int64_t K, size_t* ws, int* launches) {
     *ws = 0;
     *launches = 0;
-    if (wtype != QMM_Q8_0 && wtype != QMM_Q4_K) return;
+    if (!weight_type(wtype)) return;
     if (mode != QMM_INT8_ACT && mode != QMM_F32_ACT) return;
     if (check_shape(wtype, N, K) != QMM_OK || M <= 0 || M > INT32_MAX || N == 0 || K == 0) return;
     int sms = 0, smem = 0, dev = 0;
     if (device_info(nullptr, &sms, &smem, &dev) != cudaSuccess) return;
-    const Dispatch& d = get_dispatch(dev, wtype == QMM_Q8_0 ? T_Q8_0 : T_Q4_K, mode == QMM_INT8_ACT ? A_INT8 : A_F32, E_Y,
+    const Dispatch& d = get_dispatch(dev, internal_type(wtype), mode == QMM_INT8_ACT ? A_INT8 : A_F32, E_Y,
                                      M, N, K, sms, smem);
     *ws = d.workspace;
     *launches = d.launches;
@@ -299,7 +328,7 @@ int qmm_matmul_launches(qmm_type wtype, qmm_act_mode mode, int64_t M, int64_t N,
 
 qmm_status qmm_matmul(qmm_type wtype, qmm_act_mode mode, const void* wq, const float* x, float* y, int64_t M,
                       int64_t N, int64_t K, void* workspace, size_t workspace_bytes, qmm_stream_t stream) {
-    if (wtype != QMM_Q8_0 && wtype != QMM_Q4_K) return QMM_ERR_TYPE;
+    if (!weight_type(wtype)) return QMM_ERR_TYPE;
     if (mode != QMM_INT8_ACT && mode != QMM_F32_ACT) return QMM_ERR_TYPE;
     qmm_status st = check_shape(wtype, N, K);
     if (st != QMM_OK) return st;
@@ -315,7 +344,7 @@ qmm_status qmm_matmul(qmm_type wtype, qmm_act_mode mode, const void* wq, const f
 
 qmm_status qmm_block_sums(qmm_type wtype, const void* wq, const float* x, int64_t M, int64_t N, int64_t K,
                           int32_t* out, qmm_stream_t stream) {
-    if (wtype != QMM_Q8_0 && wtype != QMM_Q4_K) return QMM_ERR_TYPE;
+    if (!weight_type(wtype)) return QMM_ERR_TYPE;
     qmm_status st = check_shape(wtype, N, K);
     if (st != QMM_OK) return st;
     if (M < 0 || M > INT32_MAX) return QMM_ERR_SHAPE;

@@ -13,7 +13,9 @@
 
 namespace qmm {
 
-enum : int { T_F32 = 0, T_Q8_0 = 1, T_Q4_K = 2, T_Q8_K = 3 };
+enum : int { T_F32 = 0, T_Q8_0 = 1, T_Q4_K = 2, T_Q8_K = 3, T_Q4_0 = 4, T_Q5_0 = 5 };
+// weight types of 32-value blocks with one f16 scale and signed codes (paired with Q8_0 activations)
+__host__ __device__ constexpr bool is_b32(int wt) { return wt == T_Q8_0 || wt == T_Q4_0 || wt == T_Q5_0; }
 enum : int { A_INT8 = 0, A_F32 = 1 };
 enum : int { E_Y = 0, E_SUMS = 1 };
 

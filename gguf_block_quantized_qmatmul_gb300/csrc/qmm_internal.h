@@ -16,6 +16,8 @@ cudaError_t launch_dequantize(int type, const void* q, long long rows, long long
 cudaError_t launch_splitk_reduce(const float* partial, long long n, int ks, float* y, cudaStream_t s);
 cudaError_t launch_stream_q8_0(int am, int epi, const StreamPlan& plan, int smem_max, cudaStream_t s);
 cudaError_t launch_stream_q4_k(int am, int epi, const StreamPlan& plan, int smem_max, cudaStream_t s);
+cudaError_t launch_stream_q4_0(int am, int epi, const StreamPlan& plan, int smem_max, cudaStream_t s);
+cudaError_t launch_stream_q5_0(int am, int epi, const StreamPlan& plan, int smem_max, cudaStream_t s);
 cudaError_t launch_gemv_q8_0(int epi, const GemvPlan& plan, int smem_max, cudaStream_t s);
 cudaError_t launch_gemv_q4_k(int epi, const GemvPlan& plan, int smem_max, cudaStream_t s);
 cudaError_t launch_dmma(int wt, int am, int epi, const DmmaPlan& plan, int smem_max, cudaStream_t s);

@@ -1,5 +1,5 @@
-// qmm_quant.cu -- quantize (Q8_0, Q4_K weights; Q8_0, Q8_K activations) and
-// dequantize kernels.
+// qmm_quant.cu -- quantize (Q8_0, Q4_K, Q4_0, Q5_0 weights; Q8_0, Q8_K
+// activations) and dequantize kernels.
 //
 // "自己量化" section 3 (QTensor::quantize) and section 和下载的 Q8_0 逐字节比
 // (Q8_0 scale max|x|/127); "同一个 GGUF，CPU 和 Metal 生成的文字不一样" section
@@ -126,6 +126,90 @@ __global__ void quant_q4_k_kernel(const float* __restrict__ x, long long nblocks
     for (int k = 0; k < 9; ++k) o[k] = make_uint4(words[4 * k], words[4 * k + 1], words[4 * k + 2], words[4 * k + 3]);
 }
 
+// Q4_0 / Q5_0 (OFF = 8 / 16; weights paired with Q8_0 activations, 18 / 22
+// bytes per 32 values): the value m of largest magnitude (the first on ties,
+// sign kept) sets d = m / -OFF; codes roundf(x (1/d)) + OFF clamped to
+// [0, 2 OFF - 1].  Block: f16 d; (Q5_0) a little-endian word whose bit i is
+// bit 4 of code i; 16 bytes, byte j = code j | code j + 16 << 4.
+template <int OFF>
+__global__ void quant_x_0_kernel(const float* __restrict__ x, long long nblocks, long long nb_row, long long K,
+                                 uint8_t* __restrict__ out) {
+    constexpr int BYTES = OFF == 16 ? 22 : 18;
+    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= nblocks) return;
+    const long long r = i / nb_row, b = i - r * nb_row;
+    const float4* src = reinterpret_cast<const float4*>(x + r * K + b * 32);
+    float v[32];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const float4 t = __ldg(src + k);
+        v[4 * k] = t.x;
+        v[4 * k + 1] = t.y;
+        v[4 * k + 2] = t.z;
+        v[4 * k + 3] = t.w;
+    }
+    float amax = 0.0f, m = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+        const float a = fabsf(v[k]);
+        if (a > amax) {
+            amax = a;
+            m = v[k];
+        }
+    }
+    const float d = __fdiv_rn(m, (float)(-OFF));
+    const float id = d != 0.0f ? __fdiv_rn(1.0f, d) : 0.0f;
+    int c[32];
+#pragma unroll
+    for (int k = 0; k < 32; ++k)
+        c[k] = (int)fminf(fmaxf(__fadd_rn(roundf(__fmul_rn(v[k], id)), (float)OFF), 0.0f), (float)(2 * OFF - 1));
+    uint16_t* o = reinterpret_cast<uint16_t*>(out + i * BYTES);  // 2-byte aligned block
+    o[0] = (uint16_t)f2h(d);
+    int q0 = 1;
+    if (OFF == 16) {
+        uint32_t h = 0;
+#pragma unroll
+        for (int k = 0; k < 32; ++k) h |= (uint32_t)((c[k] >> 4) & 1) << k;
+        o[1] = (uint16_t)(h & 0xffffu);
+        o[2] = (uint16_t)(h >> 16);
+        q0 = 3;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const uint32_t b0 = (uint32_t)((c[2 * j] & 15) | ((c[2 * j + 16] & 15) << 4));
+        const uint32_t b1 = (uint32_t)((c[2 * j + 1] & 15) | ((c[2 * j + 17] & 15) << 4));
+        o[q0 + j] = (uint16_t)(b0 | (b1 << 8));
+    }
+}
+
+template <int OFF>
+__global__ void dequant_x_0_kernel(const uint8_t* __restrict__ q, long long nblocks, float* __restrict__ out) {
+    constexpr int BYTES = OFF == 16 ? 22 : 18;
+    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= nblocks) return;
+    const uint16_t* blk = reinterpret_cast<const uint16_t*>(q + i * BYTES);
+    const float d = h2f(blk[0]);
+    const uint32_t h = OFF == 16 ? (uint32_t)blk[1] | ((uint32_t)blk[2] << 16) : 0u;
+    const int q0 = OFF == 16 ? 3 : 1;
+    float v[32];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const uint32_t pair = blk[q0 + j];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int l = 2 * j + e;
+            const uint32_t byte = (pair >> (8 * e)) & 0xffu;
+            const int lo = (int)((byte & 15u) | (((h >> l) & 1u) << 4)) - OFF;
+            const int hi = (int)((byte >> 4) | (((h >> (l + 16)) & 1u) << 4)) - OFF;
+            v[l] = d * (float)lo;         // exact: 11 x 5 bits
+            v[l + 16] = d * (float)hi;
+        }
+    }
+    float4* o = reinterpret_cast<float4*>(out + i * 32);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) o[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+}
+
 __global__ void dequant_q8_0_kernel(const uint8_t* __restrict__ q, long long nblocks, float* __restrict__ out) {
     const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= nblocks) return;
@@ -215,6 +299,10 @@ cudaError_t launch_quantize(int type, const float* x, long long rows, long long 
     } else if (type == T_Q4_K) {
         const long long nb = K / 256, n = rows * nb;
         quant_q4_k_kernel<<<grid_for(n, bs), bs, 0, s>>>(x, n, nb, K, static_cast<uint8_t*>(out));
+    } else if (type == T_Q4_0 || type == T_Q5_0) {
+        const long long nb = K / 32, n = rows * nb;
+        if (type == T_Q4_0) quant_x_0_kernel<8><<<grid_for(n, bs), bs, 0, s>>>(x, n, nb, K, static_cast<uint8_t*>(out));
+        else quant_x_0_kernel<16><<<grid_for(n, bs), bs, 0, s>>>(x, n, nb, K, static_cast<uint8_t*>(out));
     } else {
         return cudaErrorInvalidValue;
     }
@@ -228,6 +316,8 @@ cudaError_t launch_dequantize(int type, const void* q, long long rows, long long
     if (type == T_Q8_0) dequant_q8_0_kernel<<<grid_for(n, bs), bs, 0, s>>>(qb, n, out);
     else if (type == T_Q8_K) dequant_q8_k_kernel<<<grid_for(n, bs), bs, 0, s>>>(qb, n, out);
     else if (type == T_Q4_K) dequant_q4_k_kernel<<<grid_for(n, bs), bs, 0, s>>>(qb, n, out);
+    else if (type == T_Q4_0) dequant_x_0_kernel<8><<<grid_for(n, bs), bs, 0, s>>>(qb, n, out);
+    else if (type == T_Q5_0) dequant_x_0_kernel<16><<<grid_for(n, bs), bs, 0, s>>>(qb, n, out);
     else return cudaErrorInvalidValue;
     return cudaGetLastError();
 }

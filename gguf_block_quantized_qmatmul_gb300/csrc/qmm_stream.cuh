@@ -40,10 +40,52 @@ template <>
 struct Unit<T_Q4_K> {
     static constexpr int vals = 256, bytes = 144, per_stage = 8;
 };
+template <>
+struct Unit<T_Q4_0> {
+    static constexpr int vals = 32, bytes = 18, per_stage = 32;
+};
+template <>
+struct Unit<T_Q5_0> {
+    static constexpr int vals = 32, bytes = 22, per_stage = 32;
+};
+__host__ __device__ constexpr int unit_vals(int wt) { return wt == T_Q4_K ? 256 : 32; }
+__host__ __device__ constexpr int unit_bytes(int wt) {
+    return wt == T_Q4_K ? 144 : wt == T_Q4_0 ? 18 : wt == T_Q5_0 ? 22 : 34;
+}
+
+// Signed codes of values 8t..8t+7 of a 32-value weight block (2-byte
+// aligned in shared memory): w0 holds values 8t..8t+3, w1 8t+4..8t+7, one
+// byte each.  Q8_0: the int8 codes; Q4_0 / Q5_0: the 4-bit field (low nibble
+// of byte j for value j, high nibble for value j + 16) plus, for Q5_0, bit 4
+// from the block's 32-bit word of fifth bits, minus the offset 8 / 16.
+template <int WT>
+__device__ __forceinline__ void b32_codes8(const uint8_t* blk, int t, uint32_t& w0, uint32_t& w1) {
+    if (WT == T_Q8_0) {
+        lds8_unaligned(blk + 2 + 8 * t, w0, w1);
+    } else {
+        constexpr int QS = WT == T_Q5_0 ? 6 : 2;
+        uint32_t x0, x1;
+        lds8_unaligned(blk + QS + 8 * (t & 1), x0, x1);
+        const uint32_t sh = 4u * (uint32_t)(t >> 1);
+        uint32_t l0 = (x0 >> sh) & 0x0F0F0F0Fu, l1 = (x1 >> sh) & 0x0F0F0F0Fu;
+        if (WT == T_Q5_0) {
+            const uint16_t* hw = reinterpret_cast<const uint16_t*>(blk + 2);
+            const uint32_t hb = (((uint32_t)hw[0] | ((uint32_t)hw[1] << 16)) >> (8 * t)) & 0xFFu;
+            // bits 0..3 of hb to bit 4 of bytes 0..3 (the shifted copies do not overlap)
+            l0 |= (((hb & 0xFu) * 0x00204081u) & 0x01010101u) << 4;
+            l1 |= ((((hb >> 4) & 0xFu) * 0x00204081u) & 0x01010101u) << 4;
+            w0 = __vsub4(l0, 0x10101010u);
+            w1 = __vsub4(l1, 0x10101010u);
+        } else {
+            w0 = __vsub4(l0, 0x08080808u);
+            w1 = __vsub4(l1, 0x08080808u);
+        }
+    }
+}
 
 // consumer warps per CTA for a kernel variant (host and device agree on it)
 __host__ __device__ constexpr int consumer_warps(int wt, int am, int nt) {
-    return wt == T_Q8_0 && nt <= 2 ? 16 : 8;
+    return is_b32(wt) && nt <= 2 ? 16 : 8;
 }
 // activation rows per CTA chunk
 __host__ __device__ constexpr int chunk_rows(int am, int nt) { return am == A_INT8 ? 8 * nt : 4 * nt; }
@@ -56,7 +98,7 @@ template <int WT, int AM, int CW>
 __device__ __forceinline__ void prepare_acts(const StreamParams& p, uint8_t* smem, int m0, int k0, int klen, int tid) {
     constexpr int NTH = CW * 32;
     const int MR = p.mr;
-    if (AM == A_INT8 && WT == T_Q8_0) {
+    if (AM == A_INT8 && is_b32(WT)) {  // Q8_0 activations
         uint8_t* codes = smem + p.off_codes;
         float* da = reinterpret_cast<float*>(smem + p.off_scale);
         const int nb = p.slice_units;  // blocks of 32 in the (largest) slice
@@ -197,14 +239,14 @@ __device__ __forceinline__ void stage_mma(const StreamParams& p, const uint8_t* 
     const uint8_t* row1 = st + (g + 8) * p.row_stride + off1;
     for (int u = warp; u < nunits; u += CW) {
         const int ur = ur0 + u;  // unit index inside the K slice
-        if (WT == T_Q8_0) {
-            const uint8_t* b0 = row0 + u * 34;
-            const uint8_t* b1 = row1 + u * 34;
+        if (is_b32(WT)) {
+            const uint8_t* b0 = row0 + u * Unit<WT>::bytes;
+            const uint8_t* b1 = row1 + u * Unit<WT>::bytes;
             const float dw0 = h2f(*reinterpret_cast<const uint16_t*>(b0));
             const float dw1 = h2f(*reinterpret_cast<const uint16_t*>(b1));
-            uint32_t w0, w1, v0, v1;  // 8 code bytes of rows g and g+8 at block offset 8t
-            lds8_unaligned(b0 + 2 + 8 * t, w0, w1);
-            lds8_unaligned(b1 + 2 + 8 * t, v0, v1);
+            uint32_t w0, w1, v0, v1;  // 8 signed codes of rows g and g+8: values 8t..8t+7
+            b32_codes8<WT>(b0, t, w0, w1);
+            b32_codes8<WT>(b1, t, v0, v1);
             if (AM == A_INT8) {
                 const uint8_t* codes = smem + p.off_codes;
                 const float* da = reinterpret_cast<const float*>(smem + p.off_scale);
@@ -540,7 +582,7 @@ inline bool plan_stream(int wt, int am, int epi, long long M, long long N, long 
                         StreamPlan& out) {
     StreamPlan pl{};
     StreamParams& p = pl.p;
-    const int uv = wt == T_Q8_0 ? 32 : 256, ub = wt == T_Q8_0 ? 34 : 144;
+    const int uv = unit_vals(wt), ub = unit_bytes(wt);
     int nt;
     if (am == A_INT8) nt = M <= 8 ? 1 : M <= 16 ? 2 : M <= 32 ? 4 : 8;
     else nt = M <= 4 ? 1 : M <= 8 ? 2 : M <= 16 ? 4 : 8;
@@ -556,7 +598,7 @@ inline bool plan_stream(int wt, int am, int epi, long long M, long long N, long 
     p.rb = (long long)p.units * ub;
     p.total_bytes = p.rb * N;
     p.ntiles = (int)((N + kTileRows - 1) / kTileRows);
-    const int ups_max = wt == T_Q8_0 ? Unit<T_Q8_0>::per_stage : Unit<T_Q4_K>::per_stage;
+    const int ups_max = wt == T_Q4_K ? Unit<T_Q4_K>::per_stage : Unit<T_Q8_0>::per_stage;
     const int red_bytes = cw * kTileRows * mr * 4;
     for (int ks = 1; ks <= p.units; ++ks) {
         const int su = (p.units + ks - 1) / ks;

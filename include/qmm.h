@@ -52,7 +52,9 @@ typedef enum {
     QMM_F32 = 0,    /* plain f32 (only as a dequantization target)          */
     QMM_Q8_0 = 1,   /* 32 values: f16 scale, int8 codes                      */
     QMM_Q4_K = 2,   /* 256 values: f16 d/dmin, 6-bit sub-block scales/mins   */
-    QMM_Q8_K = 3    /* 256 values: f32 scale, int8 codes, 16 int16 sums      */
+    QMM_Q8_K = 3,   /* 256 values: f32 scale, int8 codes, 16 int16 sums      */
+    QMM_Q4_0 = 4,   /* 32 values: f16 scale, 4-bit codes offset by 8 (18 B)  */
+    QMM_Q5_0 = 5    /* 32 values: f16 scale, 5-bit codes offset by 16 (22 B) */
 } qmm_type;
 
 typedef enum {
@@ -71,12 +73,15 @@ typedef enum {
     QMM_ERR_TIMEOUT = 7     /* a device-side wait gave up (reported by qmm_last_device_error) */
 } qmm_status;
 
-/* Values per block: 32 (Q8_0), 256 (Q4_K, Q8_K), 1 (F32); 0 for an unknown type. */
+/* Values per block: 32 (Q8_0, Q4_0, Q5_0), 256 (Q4_K, Q8_K), 1 (F32); 0 for an
+   unknown type. */
 int64_t qmm_block_values(qmm_type t);
 
-/* Bytes per block: 34, 144, 292; 4 for F32; 0 for an unknown type.
-   ("自己量化" section 大小和误差: the printed file sizes fix 34 B per 32 values
-   for Q8_0 and 144 B per 256 for Q4K.) */
+/* Bytes per block: 34 (Q8_0), 144 (Q4_K), 292 (Q8_K), 18 (Q4_0), 22 (Q5_0);
+   4 for F32; 0 for an unknown type.  ("自己量化" section 大小和误差 and the
+   byte listings of section 和下载的 Q8_0 逐字节比: the printed sizes fix 34 B
+   per 32 values for Q8_0, 144 B per 256 for Q4K, 22 B per 32 for Q5_0 and
+   18 B per 32 for Q4_0.) */
 size_t qmm_block_bytes(qmm_type t);
 
 /* Bytes of one quantized row of K values; 0 when K is not a multiple of the
@@ -84,13 +89,19 @@ size_t qmm_block_bytes(qmm_type t);
 size_t qmm_row_bytes(qmm_type t, int64_t K);
 
 /* Quantize weights w [N, K] (f32, device) into wq (N * qmm_row_bytes(wtype, K)
-   bytes, device).  wtype: QMM_Q8_0 or QMM_Q4_K ("自己量化" section 3,
-   QTensor::quantize).  Q8_0: per 32 values d = max|x|/127, codes
+   bytes, device).  wtype: QMM_Q8_0, QMM_Q4_K, QMM_Q4_0 or QMM_Q5_0 ("自己量化"
+   section 3, QTensor::quantize).  Q8_0: per 32 values d = max|x|/127, codes
    round(x / d) with ties away from zero.  Q4_K: per sub-block of 32 a step
    (max - min(0, min))/15 and offset -min(0, min), super-block scales
    d = max step / 63 and dmin = max offset / 63, 6-bit factors and 4-bit
    codes by rounding (the pages do not give the K-quant algorithm; this is the
-   closed-form min/max reading).  Errors: NULL, SHAPE (K % block), TYPE, ALIGN. */
+   closed-form min/max reading).  Q4_0 / Q5_0 (off = 8 / 16; the pages give
+   only their sizes): the value m of largest magnitude (the first on ties,
+   sign kept) sets d = m / -off, codes round(x / d) + off clamped to
+   [0, 2 off - 1]; block = f16 d, (Q5_0) a little-endian 32-bit word whose
+   bit i is bit 4 of code i, then 16 bytes with code j in the low nibble of
+   byte j and code j + 16 in its high nibble (the public GGUF layout); the
+   weight is f(d) (code - off).  Errors: NULL, SHAPE (K % block), TYPE, ALIGN. */
 qmm_status qmm_quantize_weights(qmm_type wtype, const float* w, int64_t N, int64_t K, void* wq,
                                 qmm_stream_t stream);
 
@@ -106,7 +117,8 @@ qmm_status qmm_quantize_act(qmm_type atype, const float* x, int64_t M, int64_t K
 /* Dequantize rows blocks -> out [rows, K] f32 (the CANDLE_DEQUANTIZE_ALL form,
    "同一个 GGUF…" section 出处).  Q8_0 and Q8_K: f(d) * q; Q4_K:
    (f(d) * sc_j) * q - f(dmin) * m_j, both products exact in f32, one rounding
-   in the subtraction (bit-exact contract).  t: Q8_0, Q4_K or Q8_K. */
+   in the subtraction; Q4_0 / Q5_0: f(d) (code - off), exact (bit-exact
+   contract).  t: Q8_0, Q4_K, Q8_K, Q4_0 or Q5_0. */
 qmm_status qmm_dequantize(qmm_type t, const void* q, int64_t rows, int64_t K, float* out,
                           qmm_stream_t stream);
 
@@ -124,11 +136,12 @@ size_t qmm_matmul_workspace(qmm_type wtype, qmm_act_mode mode, int64_t M, int64_
 int qmm_matmul_launches(qmm_type wtype, qmm_act_mode mode, int64_t M, int64_t N, int64_t K);
 
 /* y [M, N] f32 = x [M, K] f32 . W^T with W given as quantized blocks wq
-   (wtype QMM_Q8_0 or QMM_Q4_K).
+   (wtype QMM_Q8_0, QMM_Q4_K, QMM_Q4_0 or QMM_Q5_0).
    mode QMM_INT8_ACT ("同一个 GGUF…" section 出处, the CPU form): each row of x
-     is quantized in-kernel to Q8_0 (Q8_0 weights) or Q8_K (Q4_K weights),
-     per-block int32 dot products of codes are formed exactly and combined as
-       Q8_0: y = sum_b f(d_w) f(d_a) isum_b
+     is quantized in-kernel to Q8_0 (Q8_0, Q4_0 and Q5_0 weights) or Q8_K
+     (Q4_K weights), per-block int32 dot products of signed codes are formed
+     exactly and combined as
+       Q8_0, Q4_0, Q5_0: y = sum_b f(d_w) f(d_a) isum_b
        Q4_K: y = sum_s d_a (f(d) S_sc - f(dmin) S_m),
              S_sc = sum_j sc_j isum_j, S_m = sum_j m_j (sum of the sub-block's codes).
    mode QMM_F32_ACT (the Metal form): y = sum_k x_k w_k with w the dequantized
@@ -145,7 +158,7 @@ qmm_status qmm_matmul(qmm_type wtype, qmm_act_mode mode, const void* wq, const f
    same kernel, fragment layout and in-kernel activation quantization as
    qmm_matmul(QMM_INT8_ACT), written out instead of being scaled.
    x is f32 [M, K].  out (int32, device):
-     Q8_0: [M][N][K/32]          isum of each 32-block;
+     Q8_0, Q4_0, Q5_0: [M][N][K/32]  isum of each 32-block (signed codes);
      Q4_K: [M][N][K/256][2]      (S_sc, S_m) of each super-block.
    Bit-exact contract.  Errors as for qmm_matmul (no workspace). */
 qmm_status qmm_block_sums(qmm_type wtype, const void* wq, const float* x, int64_t M, int64_t N, int64_t K,

@@ -49,7 +49,8 @@ def check_device_error(qmm):
 # ---------------------------------------------------------------------------
 
 WEIGHT_CASES = [("q8_0", 576, 576), ("q8_0", 37, 96), ("q8_0", 61, 608), ("q8_0", 5, 8192),
-                ("q4_k", 576, 1536), ("q4_k", 37, 256), ("q4_k", 19, 8192)]
+                ("q4_k", 576, 1536), ("q4_k", 37, 256), ("q4_k", 19, 8192),
+                ("q4_0", 576, 576), ("q4_0", 37, 96), ("q5_0", 576, 576), ("q5_0", 1536, 576), ("q5_0", 7, 8192)]
 
 
 @pytest.mark.parametrize("wtype,N,K", WEIGHT_CASES)
@@ -68,7 +69,7 @@ def test_quantize_act_bit_exact(qmm, orc, atype, M, K):
     assert np.array_equal(q, orc.quantize(atype, x))
 
 
-@pytest.mark.parametrize("t,K", [("q8_0", 576), ("q4_k", 1536), ("q8_k", 1024)])
+@pytest.mark.parametrize("t,K", [("q8_0", 576), ("q4_k", 1536), ("q8_k", 1024), ("q4_0", 576), ("q5_0", 576)])
 def test_dequantize_bit_exact(qmm, orc, t, K):
     w = np.concatenate([qmm_synth.weights(40, K), qmm_synth.special_block_rows(K)])
     q = orc.quantize(t, w)
@@ -82,7 +83,9 @@ def test_dequantize_bit_exact(qmm, orc, t, K):
 # ---------------------------------------------------------------------------
 
 SUM_CASES = [("q8_0", 1, 33, 576), ("q8_0", 8, 576, 576), ("q8_0", 5, 40, 4096), ("q8_0", 13, 17, 1536),
-             ("q8_0", 37, 24, 96), ("q4_k", 1, 33, 1536), ("q4_k", 8, 64, 2048), ("q4_k", 19, 20, 4096)]
+             ("q8_0", 37, 24, 96), ("q4_k", 1, 33, 1536), ("q4_k", 8, 64, 2048), ("q4_k", 19, 20, 4096),
+             ("q4_0", 1, 33, 576), ("q4_0", 13, 40, 1536), ("q5_0", 1, 192, 576), ("q5_0", 8, 33, 576),
+             ("q5_0", 37, 24, 4096)]
 
 
 @pytest.mark.parametrize("wtype,M,N,K", SUM_CASES)
@@ -93,7 +96,7 @@ def test_block_sums_bit_exact(qmm, orc, wtype, M, N, K):
     x[0] = -1.0
     wq = orc.quantize(wtype, w)
     s = host(qmm.block_sums(dev(wq), dev(x), wtype, N=N))
-    xq = orc.quantize("q8_0" if wtype == "q8_0" else "q8_k", x)
+    xq = orc.quantize("q8_k" if wtype == "q4_k" else "q8_0", x)
     ref = orc.block_sums(wtype, wq, xq, M, N, K)
     assert np.array_equal(s, ref)
     check_device_error(qmm)
@@ -125,6 +128,14 @@ MATMUL_CASES = [
     ("q8_0", 256, 384, 2048),     # 256-row activation tiles, one accumulator
     ("q4_k", 520, 130, 1024),     # three activation tiles of 176 rows, ragged weight tile
     ("q4_k", 9, 1000, 512),       # smallest prefill M (16-row activation tile)
+    ("q5_0", 1, 576, 576),        # SmolLM2 Q5_0 projections (K = 576 rules out K-quants)
+    ("q5_0", 1, 1536, 576),
+    ("q5_0", 4, 192, 576),
+    ("q5_0", 8, 576, 1536),
+    ("q5_0", 37, 300, 576),       # prefill, ragged
+    ("q4_0", 1, 576, 576),
+    ("q4_0", 2, 100, 8192),       # K split across CTAs
+    ("q4_0", 64, 130, 1024),
 ]
 
 
@@ -227,6 +238,8 @@ def test_launch_counts(qmm):
     assert qmm.matmul_launches("q8_0", "f32_act", 8, 28672, 8192) == 3    # K split: reduction after
     assert qmm.matmul_launches("q8_0", "int8_act", 256, 4096, 4096) == 2  # prefill: operand + GEMM
     assert qmm.matmul_launches("q8_0", "int8_act", 1, 100, 100) == 0      # K not a multiple of 32
+    assert qmm.matmul_launches("q5_0", "int8_act", 1, 576, 576) == 1      # Q4_0 / Q5_0: the streaming kernel
+    assert qmm.matmul_launches("q4_0", "f32_act", 64, 4096, 4096) == 1
 
 
 def test_error_statuses_on_device(qmm, orc):
