@@ -91,8 +91,12 @@ struct Dispatch {
 
 void plan_dispatch(int wt, int am, int epi, long long M, long long N, long long K, int sms, int smem, Dispatch& d) {
     d = Dispatch();
-    if (wt == T_Q4_0 || wt == T_Q5_0) {  // every shape on the streaming kernel
-        if (plan_stream(wt, am, epi, M, N, K, sms, smem, d.sp)) {
+    if (wt == T_Q4_0 || wt == T_Q5_0) {  // prefill on the tcgen05 GEMM where K allows, else the streaming kernel
+        if (epi == E_Y && M > kDecodeMaxM && plan_tc(wt, am, M, N, K, sms, smem, d.tp)) {
+            d.kind = KIND_TC;
+            d.workspace = d.tp.workspace;
+            d.launches = 2;  // operand preparation, GEMM
+        } else if (plan_stream(wt, am, epi, M, N, K, sms, smem, d.sp)) {
             d.kind = KIND_STREAM;
             d.workspace = epi == E_Y ? workspace_for(d.sp) : 0;
             d.launches = 1;

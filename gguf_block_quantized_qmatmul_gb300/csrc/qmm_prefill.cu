@@ -7,7 +7,7 @@ namespace qmm {
 namespace {
 
 unsigned long long g_smem_done[2];
-unsigned long long g_tc_smem_done[2];
+unsigned long long g_tc_smem_done[4];
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -51,7 +51,8 @@ cudaError_t tc_go(const TcPlan& pl, const void* wq, const float* x, void* ws, fl
     if (e != cudaSuccess) return e;
     // 2. tensor maps: raw weight rows as uint16; activation pieces, 32 K x bx rows, 64-byte swizzle
     CUtensorMap tw, tah, tal;
-    const unsigned long long rb = (unsigned long long)p0.K / (WT == T_Q8_0 ? 32 : 256) * (WT == T_Q8_0 ? 34 : 144);
+    const unsigned long long rb = WT == T_Q4_K ? (unsigned long long)p0.K / 256 * 144
+                                               : (unsigned long long)p0.K / 32 * (WT == T_Q8_0 ? 34 : WT == T_Q5_0 ? 22 : 18);
     if (!make_map(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT16, wq, rb / 2, p0.N, rb, p0.raw_row / 2, kTcBW, CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !make_map(&tah, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, ahi, p0.K, p0.M, (unsigned long long)p0.K * 2, kTcBK, p0.bx,
                   CU_TENSOR_MAP_SWIZZLE_64B) ||
@@ -66,7 +67,7 @@ cudaError_t tc_go(const TcPlan& pl, const void* wq, const float* x, void* ws, fl
     p.wis = wis;
     // 3. the GEMM, a programmatic dependent of the preparation
     auto* k = qmm_tc_kernel<WT>;
-    e = ensure_smem(k, smem_max, g_tc_smem_done[WT == T_Q8_0 ? 0 : 1]);
+    e = ensure_smem(k, smem_max, g_tc_smem_done[WT == T_Q8_0 ? 0 : WT == T_Q4_K ? 1 : WT == T_Q4_0 ? 2 : 3]);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)pl.grid);
@@ -87,6 +88,10 @@ cudaError_t launch_tc(int wt, int am, const TcPlan& plan, const void* wq, const 
                       cudaStream_t s) {
     if (wt == T_Q8_0) return am == A_INT8 ? tc_go<T_Q8_0, A_INT8>(plan, wq, x, ws, y, smem_max, s)
                                           : tc_go<T_Q8_0, A_F32>(plan, wq, x, ws, y, smem_max, s);
+    if (wt == T_Q4_0) return am == A_INT8 ? tc_go<T_Q4_0, A_INT8>(plan, wq, x, ws, y, smem_max, s)
+                                          : tc_go<T_Q4_0, A_F32>(plan, wq, x, ws, y, smem_max, s);
+    if (wt == T_Q5_0) return am == A_INT8 ? tc_go<T_Q5_0, A_INT8>(plan, wq, x, ws, y, smem_max, s)
+                                          : tc_go<T_Q5_0, A_F32>(plan, wq, x, ws, y, smem_max, s);
     return am == A_INT8 ? tc_go<T_Q4_K, A_INT8>(plan, wq, x, ws, y, smem_max, s) : tc_go<T_Q4_K, A_F32>(plan, wq, x, ws, y, smem_max, s);
 }
 

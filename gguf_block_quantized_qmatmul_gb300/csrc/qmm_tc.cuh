@@ -206,6 +206,59 @@ __device__ __forceinline__ void tc_conv_q4_k(const uint8_t* sbk, float wsc, uint
     }
 }
 
+// Q4_0 / Q5_0 block J (0..7) of a raw row (144 / 176 bytes, 16-byte
+// aligned): w 2^s = ds (code - off) with ds = f(d) 2^s as f16; the 4-bit
+// fields (code j in the low nibble of byte j, code j + 16 in its high
+// nibble) plus, for Q5_0, bit 4 from the block's word of fifth bits, biased
+// to code - off + 128 and converted as the Q8_0 codes are.
+template <int WT, int J>
+__device__ __forceinline__ void tc_conv_x_0(const uint8_t* row, float wsc, uint32_t h[16], uint32_t l[16]) {
+    constexpr int BB = WT == T_Q5_0 ? 22 : 18;    // bytes per block
+    constexpr int QS = WT == T_Q5_0 ? 6 : 2;      // offset of the 16 nibble bytes
+    constexpr int A = (BB * J) & ~15, O = BB * J - A;
+    constexpr int NC = (O + BB + 15) / 16;        // 16-byte chunks covering the block
+    uint32_t w[12];
+#pragma unroll
+    for (int c = 0; c < 3; ++c) {
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (c < NC) v = *reinterpret_cast<const uint4*>(row + A + 16 * c);
+        w[4 * c] = v.x;
+        w[4 * c + 1] = v.y;
+        w[4 * c + 2] = v.z;
+        w[4 * c + 3] = v.w;
+    }
+    const uint32_t dbits = (w[O / 4] >> (8 * (O % 4))) & 0xFFFFu;
+    const __half2 ds2 = __half2half2(__float2half_rn(h2f(dbits) * wsc));
+    constexpr int QW = (O + QS) / 4, QSH = 8 * ((O + QS) % 4);
+    static_assert(QW + 4 + (QSH != 0 ? 1 : 0) <= 12, "the chunks hold the block");
+    uint32_t q[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        if constexpr (QSH != 0) q[i] = __funnelshift_r(w[QW + i], w[QW + i + 1], QSH);
+        else q[i] = w[QW + i];
+    }
+    uint32_t hb = 0;
+    if constexpr (WT == T_Q5_0) {
+        constexpr int HW = (O + 2) / 4, HSH = 8 * ((O + 2) % 4);
+        if constexpr (HSH != 0) hb = __funnelshift_r(w[HW], w[HW + 1], HSH);
+        else hb = w[HW];
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        // values 4k..4k+3: low nibbles of word k (k < 4) or high nibbles of word k - 4
+        uint32_t word = k < 4 ? (q[k & 3] & 0x0F0F0F0Fu) : ((q[k & 3] >> 4) & 0x0F0F0F0Fu);
+        if constexpr (WT == T_Q5_0) {
+            // bits 4k..4k+3 of the fifth-bit word to bit 4 of the four bytes (no overlapping copies)
+            word |= ((((hb >> (4 * k)) & 0xFu) * 0x00204081u) & 0x01010101u) << 4;
+            word += 0x70707070u;  // code - 16 + 128
+        } else {
+            word += 0x78787878u;  // code - 8 + 128
+        }
+        tc_q8_pair(word, 0, ds2, h[2 * k], l[2 * k]);
+        tc_q8_pair(word, 1, ds2, h[2 * k + 1], l[2 * k + 1]);
+    }
+}
+
 // K slice `split` of ks: raw stages [r0, r1)
 __device__ __forceinline__ void tc_slice(const TcParams& p, int split, int& r0, int& r1) {
     r0 = split * p.nrs / p.ks;
@@ -232,6 +285,11 @@ __device__ __forceinline__ bool tc_convert_raw(const uint8_t* rrow, float wsc, l
             else if (u == 1) tc_conv_q8_0<G + 2>(rrow, wsc, h, l);
             else if (u == 2) tc_conv_q8_0<G + 4>(rrow, wsc, h, l);
             else tc_conv_q8_0<G + 6>(rrow, wsc, h, l);
+        } else if (WT == T_Q4_0 || WT == T_Q5_0) {
+            if (u == 0) tc_conv_x_0<WT, G>(rrow, wsc, h, l);
+            else if (u == 1) tc_conv_x_0<WT, G + 2>(rrow, wsc, h, l);
+            else if (u == 2) tc_conv_x_0<WT, G + 4>(rrow, wsc, h, l);
+            else tc_conv_x_0<WT, G + 6>(rrow, wsc, h, l);
         } else {
             if (u == 0) tc_conv_q4_k<G>(rrow, wsc, h, l);
             else if (u == 1) tc_conv_q4_k<G + 2>(rrow, wsc, h, l);
@@ -631,16 +689,16 @@ __global__ void __launch_bounds__(kTcPrepThreads) tc_prep_kernel(const float* __
 #pragma unroll
                 for (int i = 0; i < 16; ++i) bm = fmaxf(bm, fabsf(v[i]));
                 bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 1));  // Q8_0: the block's other half
-                if (WT != T_Q8_0) {                                      // Q8K: sixteen threads
+                if (!is_b32(WT)) {                                       // Q8K: sixteen threads
                     bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 2));
                     bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
                     bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 8));
                 }
                 float d, id;
                 q8_scale(bm, d, id);
-                const float ds = (WT == T_Q8_0 ? h2f(f2h(d)) : d) * sc;  // f(d_a) 2^s (Q8_0 keeps d as f16)
+                const float ds = (is_b32(WT) ? h2f(f2h(d)) : d) * sc;  // f(d_a) 2^s (Q8_0 keeps d as f16)
 #pragma unroll
-                for (int i = 0; i < 16; ++i) v[i] = WT == T_Q8_0 ? ds * (float)q8_code(v[i], id) : __fmul_rn(d * (float)q8_code(v[i], id), sc);
+                for (int i = 0; i < 16; ++i) v[i] = is_b32(WT) ? ds * (float)q8_code(v[i], id) : __fmul_rn(d * (float)q8_code(v[i], id), sc);
             }
             if (on) {
                 uint32_t hw[8], lw[8];
@@ -665,9 +723,12 @@ __global__ void __launch_bounds__(kTcPrepThreads) tc_prep_kernel(const float* __
         const long long n = (long long)(blockIdx.x - M) * (kTcPrepThreads / 32) + warp;
         if (n >= N) return;
         float bmax = 0.0f;
-        if (WT == T_Q8_0) {
-            const uint8_t* row = wq + n * (long long)(K / 32) * 34;
-            for (int b = lane; b < K / 32; b += 32) bmax = fmaxf(bmax, fabsf(h2f(*reinterpret_cast<const uint16_t*>(row + b * 34))) * 127.0f);
+        if (is_b32(WT)) {
+            // |w| <= |f(d)| times the largest |code|: 127 (Q8_0), 8 (Q4_0), 16 (Q5_0)
+            constexpr int BB = WT == T_Q8_0 ? 34 : WT == T_Q5_0 ? 22 : 18;
+            constexpr float CM = WT == T_Q8_0 ? 127.0f : WT == T_Q5_0 ? 16.0f : 8.0f;
+            const uint8_t* row = wq + n * (long long)(K / 32) * BB;
+            for (int b = lane; b < K / 32; b += 32) bmax = fmaxf(bmax, fabsf(h2f(*reinterpret_cast<const uint16_t*>(row + b * BB))) * CM);
         } else {
             const uint8_t* row = wq + n * (long long)(K / 256) * 144;
             for (int b = lane; b < K / 256; b += 32) {
@@ -717,7 +778,7 @@ inline bool plan_tc(int wt, int am, long long M, long long N, long long K, int s
     p.ntiles = (int)((N + kTcBW - 1) / kTcBW);
     p.tiles = p.mtiles * p.ntiles;
     p.nrs = (int)(K / kTcRK);
-    p.raw_row = wt == T_Q8_0 ? kTcRK / 32 * 34 : 144;
+    p.raw_row = wt == T_Q8_0 ? kTcRK / 32 * 34 : wt == T_Q5_0 ? kTcRK / 32 * 22 : 144;  // Q4_K, Q4_0: 144
     p.raw_stage = round_up(kTcBW * p.raw_row, 1024);
     p.piece = p.bx * 64;
     p.off_raw = kTcS * 2 * p.piece;  // activation pieces; weight pieces live in TMEM

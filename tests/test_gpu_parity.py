@@ -135,7 +135,9 @@ MATMUL_CASES = [
     ("q5_0", 37, 300, 576),       # prefill, ragged
     ("q4_0", 1, 576, 576),
     ("q4_0", 2, 100, 8192),       # K split across CTAs
-    ("q4_0", 64, 130, 1024),
+    ("q4_0", 64, 130, 1024),      # prefill on tcgen05 (K % 256 = 0)
+    ("q5_0", 256, 200, 1536),
+    ("q4_0", 300, 260, 2048),
 ]
 
 
@@ -152,7 +154,7 @@ def test_matmul_within_bound(qmm, orc, wtype, M, N, K, mode):
 
 
 @pytest.mark.parametrize("mode", ["int8_act", "f32_act"])
-@pytest.mark.parametrize("wtype,K", [("q8_0", 1024), ("q4_k", 1024)])
+@pytest.mark.parametrize("wtype,K", [("q8_0", 1024), ("q4_k", 1024), ("q4_0", 1024), ("q5_0", 1024)])
 def test_prefill_special_rows(qmm, orc, wtype, K, mode):
     """Prefill (M > 8) with the adversarial rows in both operands: zeros,
     constants, one-hot, ties, magnitudes from 1e-9 to 3e3 (each operand row is
@@ -239,7 +241,8 @@ def test_launch_counts(qmm):
     assert qmm.matmul_launches("q8_0", "int8_act", 256, 4096, 4096) == 2  # prefill: operand + GEMM
     assert qmm.matmul_launches("q8_0", "int8_act", 1, 100, 100) == 0      # K not a multiple of 32
     assert qmm.matmul_launches("q5_0", "int8_act", 1, 576, 576) == 1      # Q4_0 / Q5_0: the streaming kernel
-    assert qmm.matmul_launches("q4_0", "f32_act", 64, 4096, 4096) == 1
+    assert qmm.matmul_launches("q4_0", "f32_act", 64, 4096, 4096) == 2     # prefill, K % 256 = 0: tcgen05
+    assert qmm.matmul_launches("q5_0", "int8_act", 64, 576, 576) == 1     # K = 576: the streaming kernel
 
 
 def test_error_statuses_on_device(qmm, orc):
@@ -267,7 +270,7 @@ def test_error_statuses_on_device(qmm, orc):
 
 FULL = [("q4_k", 28672, 8192, 8), ("q8_0", 28672, 8192, 8), ("q8_0", 14336, 4096, 1024),
         ("q4_k", 14336, 4096, 1024), ("q8_0", 14336, 4096, 256), ("q4_k", 4096, 4096, 256),
-        ("q8_0", 4096, 4096, 16), ("q8_0", 49152, 576, 1)]
+        ("q8_0", 4096, 4096, 16), ("q8_0", 49152, 576, 1), ("q5_0", 14336, 4096, 256), ("q5_0", 49152, 576, 1)]
 
 
 @pytest.mark.parametrize("wtype,N,K,M", FULL)
