@@ -149,13 +149,19 @@ class Clocks:
                 "samples": len(sm)}
 
 
-def dist_init():
+def dist_init(backend: str | None = None):
+    """Rank, world and local rank from the launcher's environment; one
+    process group when world > 1 (NCCL on GPUs; gloo when asked or when no
+    GPU is present, as in the CPU tests of this multi-rank plumbing)."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
+        import torch
         import torch.distributed as dist
-        dist.init_process_group("nccl")
+        if backend is None:
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
     return world, rank, local
 
 
@@ -166,11 +172,13 @@ def barrier(world):
 
 
 def allmax(world, v: float) -> float:
+    """The largest v over the ranks (the job's time is its slowest rank's)."""
     if world == 1:
         return v
     import torch
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
