@@ -138,6 +138,8 @@ MATMUL_CASES = [
     ("q4_0", 64, 130, 1024),      # prefill on tcgen05 (K % 256 = 0)
     ("q5_0", 256, 200, 1536),
     ("q4_0", 300, 260, 2048),
+    ("q4_k", 8, 40, 65536),       # long rows: activations split over K, 256 raw stages
+    ("q8_0", 24, 24, 65536),
 ]
 
 
@@ -287,4 +289,30 @@ def test_full_size_sampled_rows(qmm, orc, wtype, N, K, M):
         y = host(qmm.matmul(wq, x, wtype, mode, N=N))
         y_orc, T = orc.matmul(wtype, mode, wq_rows, x_np)
         assert_within_bound(y[:, rows], y_orc, T, f"{wtype} {mode} N{N} K{K} M{M}")
+    check_device_error(qmm)
+
+
+@pytest.mark.parametrize("M", [1, 16])
+def test_weights_beyond_2gb_use_64_bit_offsets(qmm, orc, M):
+    """A Q8_0 weight buffer of 262144 x 8192 (2.28 GB > 2^31 bytes): decode and
+    prefill outputs for rows near the end of the buffer match the oracle, so
+    no byte offset wraps in 32 bits."""
+    N, K = 262144, 8192
+    g = torch.Generator(device="cuda").manual_seed(1)
+    wq = torch.empty((N, qmm.row_bytes("q8_0", K)), dtype=torch.uint8, device="cuda")
+    for r0 in range(0, N, 32768):  # quantize in slices (8 GB of f32 weights at once is not needed)
+        w = torch.randn((32768, K), generator=g, device="cuda") * 0.02
+        wq[r0:r0 + 32768] = qmm.quantize_weights(w, "q8_0")
+        del w
+    assert wq.numel() > 2 ** 31
+    x_np = qmm_synth.activations(M, K, outlier_channels=4 if M >= 16 else 0)
+    rows = np.unique(np.concatenate([np.arange(4), np.random.default_rng(3).choice(N, 12, replace=False),
+                                     np.arange(N - 20, N)]))
+    wq_rows = wq[torch.from_numpy(rows).cuda()].cpu().numpy()
+    for mode in ("int8_act", "f32_act"):
+        y = host(qmm.matmul(wq, dev(x_np), "q8_0", mode, N=N))
+        y_orc, T = orc.matmul("q8_0", mode, wq_rows, x_np)
+        assert_within_bound(y[:, rows], y_orc, T, f"q8_0 {mode} N{N} K{K} M{M}")
+    del wq
+    torch.cuda.empty_cache()
     check_device_error(qmm)
