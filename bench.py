@@ -259,8 +259,8 @@ def small_configs(q, torch, stream):
     """Latency-bound configurations: one Q8_0 GEMV 576x576 (M=1), the Q4_K
     576x1536 GEMV (M = 1, 2, 4, 8), and the 211-matmul SmolLM2-135M-shaped
     decode step (all Q8_0, M=1), each in both forms.  The step is timed with
-    the L2 flushed before every step (a 2 x L2 write), eagerly and replayed
-    from a CUDA graph."""
+    the L2 flushed before every step (a 2 x L2 write): eagerly and replayed
+    from a CUDA graph (211 launches), and as one qmm_matmul_batch call."""
     out = {}
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
 
@@ -319,6 +319,27 @@ def small_configs(q, torch, stream):
             ms = tot / (reps + 3)
             res[name] = {"ms_per_step": round(ms, 4), "weight_GBps": round(step_bytes / (ms * 1e6), 1)}
         out[f"smollm2_step_211_matmuls q8_0 M1 {mode} (L2 flushed)"] = res
+        # the same step as one qmm_matmul_batch call (one launch for all 211 items),
+        # its descriptor table built once; called directly and replayed from a graph
+        batch = q.MatmulBatch([(w, xs[K], y) for (w, N, K), y in zip(wqs, ys)], "q8_0", mode)
+        batch.run()
+        torch.cuda.synchronize()
+        bgraph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(bgraph):
+            batch.run()
+        torch.cuda.synchronize()
+        for name, fn in (("batched", batch.run), ("batched_graph", bgraph.replay)):
+            tot = 0.0
+            reps = 20
+            for _ in range(reps + 3):
+                flush.fill_(1.0)
+                ev0.record(stream)
+                fn()
+                ev1.record(stream)
+                torch.cuda.synchronize()
+                tot += ev0.elapsed_time(ev1)
+            ms = tot / (reps + 3)
+            res[name] = {"ms_per_step": round(ms, 4), "weight_GBps": round(step_bytes / (ms * 1e6), 1), "launches": 1}
     out["smollm2_step_weight_bytes"] = step_bytes
     return out
 

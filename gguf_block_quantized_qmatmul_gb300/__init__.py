@@ -12,6 +12,7 @@ Entry points mirror the C ABI names:
   dequantize(q, t, K)             f32 [rows, K]
   matmul(wq, x, wtype, mode)      y = x . W^T, mode "int8_act" or "f32_act"
   block_sums(wq, x, wtype)        exact per-block integer sums of the int8_act form
+  matmul_batch(items, wtype, mode)  many independent small matmuls in one launch
 """
 from __future__ import annotations
 
@@ -32,7 +33,7 @@ STATUS = {0: "QMM_OK", 1: "QMM_ERR_NULL", 2: "QMM_ERR_SHAPE", 3: "QMM_ERR_TYPE",
 # every symbol declared in include/qmm.h
 EXPORTS = ["qmm_block_values", "qmm_block_bytes", "qmm_row_bytes", "qmm_quantize_weights", "qmm_quantize_act",
            "qmm_dequantize", "qmm_matmul_workspace", "qmm_matmul_launches", "qmm_matmul", "qmm_matmul_static_workspace",
-           "qmm_block_sums",
+           "qmm_block_sums", "qmm_matmul_batch",
            "qmm_last_device_error", "qmm_status_string"]
 
 
@@ -59,6 +60,7 @@ def _load() -> ctypes.CDLL:
     lib.qmm_matmul_launches.argtypes, lib.qmm_matmul_launches.restype = [i32, i32, i64, i64, i64], i32
     lib.qmm_matmul.argtypes, lib.qmm_matmul.restype = [i32, i32, p, p, p, i64, i64, i64, p, sz, p], i32
     lib.qmm_block_sums.argtypes, lib.qmm_block_sums.restype = [i32, p, p, i64, i64, i64, p, p], i32
+    lib.qmm_matmul_batch.argtypes, lib.qmm_matmul_batch.restype = [i32, i32, p, i64, p], i32
     lib.qmm_last_device_error.argtypes, lib.qmm_last_device_error.restype = [], i32
     lib.qmm_status_string.argtypes, lib.qmm_status_string.restype = [i32], ctypes.c_char_p
     return lib
@@ -169,6 +171,38 @@ def block_sums(wq: torch.Tensor, x: torch.Tensor, wtype, N: int | None = None, s
         out = torch.empty((M, N, K // 256, 2), dtype=torch.int32, device=x.device)
     _check(_lib().qmm_block_sums(_t(wtype), _ptr(wq), _ptr(x), M, N, K, _ptr(out), _stream(stream)), "qmm_block_sums")
     return out
+
+
+class MatmulDesc(ctypes.Structure):
+    """qmm_matmul_desc: one item of qmm_matmul_batch."""
+    _fields_ = [("wq", ctypes.c_void_p), ("x", ctypes.c_void_p), ("y", ctypes.c_void_p),
+                ("M", ctypes.c_int64), ("N", ctypes.c_int64), ("K", ctypes.c_int64)]
+
+
+class MatmulBatch:
+    """A descriptor table for qmm_matmul_batch, built once: items are (wq, x,
+    y) device tensors, y [M, N] receiving x . W^T.  run() launches it (one
+    launch per 256 items; the table travels in the launch parameters)."""
+
+    def __init__(self, items, wtype, mode):
+        self.items = list(items)  # keeps the tensors alive
+        self.wtype, self.mode = _t(wtype), _m(mode)
+        self.descs = (MatmulDesc * max(len(self.items), 1))()
+        for i, (wq, x, y) in enumerate(self.items):
+            M, K = x.shape
+            self.descs[i] = MatmulDesc(_ptr(wq), _ptr(x), _ptr(y), M, y.shape[1], K)
+        self.ptr = ctypes.cast(self.descs, ctypes.c_void_p)
+
+    def run(self, stream=None):
+        _check(_lib().qmm_matmul_batch(self.wtype, self.mode, self.ptr, len(self.items), _stream(stream)),
+               "qmm_matmul_batch")
+
+
+def matmul_batch(items, wtype, mode, stream=None):
+    """One-off qmm_matmul_batch over (wq, x, y) items; returns the ys."""
+    b = MatmulBatch(items, wtype, mode)
+    b.run(stream)
+    return [y for _, _, y in b.items]
 
 
 def last_device_error() -> int:

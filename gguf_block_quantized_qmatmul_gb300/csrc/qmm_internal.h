@@ -27,6 +27,23 @@ cudaError_t launch_tc(int wt, int am, const TcPlan& plan, const void* wq, const 
 cudaError_t launch_prefill(int am, const PrefillPlan& plan, const void* wq, const float* x, void* ws, int smem_max,
                            cudaStream_t s);
 
+// many independent small matmuls in one launch (qmm_batch.cu)
+constexpr int kBatchMax = 256;  // items per launch (the launch parameters carry the table)
+struct BatchItem {
+    const uint8_t* wq;
+    const float* x;
+    float* y;
+    long long byte0;  // the item's first weight byte in the launch's byte order
+    int M, N, K, pad;
+};
+struct BatchParams {
+    BatchItem it[kBatchMax];
+    long long total;  // weight bytes of all items
+    int count;
+    int max_mk;       // the largest M x K (shared-memory activation codes)
+};
+cudaError_t launch_batch(int wt, int am, const BatchParams& p, int max_m, int sm_count, cudaStream_t s);
+
 // largest activation batch served by the per-thread dp4a GEMV (int8_act,
 // Q8_0 weights only); larger decode batches, Q4_K weights and every f32_act
 // decode batch up to 8 use the 16-row-tile tensor-core kernel

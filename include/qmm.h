@@ -164,6 +164,35 @@ qmm_status qmm_matmul(qmm_type wtype, qmm_act_mode mode, const void* wq, const f
 qmm_status qmm_block_sums(qmm_type wtype, const void* wq, const float* x, int64_t M, int64_t N, int64_t K,
                           int32_t* out, qmm_stream_t stream);
 
+/* One item of qmm_matmul_batch: y [M, N] = x [M, K] . W^T (all device memory). */
+typedef struct {
+    const void* wq;   /* weight blocks, N * qmm_row_bytes(wtype, K) bytes, 16-byte aligned */
+    const float* x;   /* activations [M, K] f32, 16-byte aligned                         */
+    float* y;         /* output [M, N] f32, 4-byte aligned                                */
+    int64_t M, N, K;
+} qmm_matmul_desc;
+
+#define QMM_BATCH_MAX_M 8        /* activation rows per item, at most          */
+#define QMM_BATCH_MAX_MK 16384   /* M * K per item, at most                     */
+
+/* Many independent small matmuls in one launch (per 256 items): the linears
+   of a decode step (q, k, v, o, gate, up, down and the output head), which
+   issued one by one are bound by launch latency rather than by their weight
+   bytes.  Each item computes exactly what qmm_matmul(wtype, mode, ...) computes
+   for it ("同一个 GGUF…" section 出处: int8_act quantizes each activation row
+   to Q8_0 and forms exact int32 block dots; f32_act multiplies f32
+   activations by the dequantized weights in f32), within the same bound.
+   wtype: QMM_Q8_0, QMM_Q4_0 or QMM_Q5_0 (32-value blocks; one type and one
+   form for the whole batch).  items: host array of `count` descriptors, read
+   during the call (the launch carries a copy), so the call can be captured
+   in a CUDA graph.  Items with M = 0 or N = 0 are skipped.  Items may share
+   x; their y must not overlap.  Needs no workspace.
+   Errors: TYPE; SHAPE (negative sizes, K % 32, M > QMM_BATCH_MAX_M or
+   M * K > QMM_BATCH_MAX_MK); NULL; ALIGN; CUDA.  Nothing is launched when
+   any item is invalid. */
+qmm_status qmm_matmul_batch(qmm_type wtype, qmm_act_mode mode, const qmm_matmul_desc* items, int64_t count,
+                            qmm_stream_t stream);
+
 /* qmm_matmul for callers that cannot allocate device memory.
    (The pages have no counterpart: this is an addition of this library.)
    Some callers never call cudaMalloc themselves: a host engine that owns all

@@ -93,6 +93,27 @@ def test_argument_errors_return_before_launch(qmm):
         assert L.qmm_status_string(s)
 
 
+def test_batch_argument_errors_return_before_launch(qmm):
+    L = _lib(qmm)
+    D = qmm.MatmulDesc
+    ok = D(16, 16, 16, 1, 8, 64)
+
+    def call(wtype, mode, items):
+        arr = (D * max(len(items), 1))(*items)
+        return L.qmm_matmul_batch(wtype, mode, ctypes.cast(arr, ctypes.c_void_p), len(items), None)
+
+    assert call(qmm.QMM_Q4_K, 0, [ok]) == 3                  # 32-value block types only
+    assert call(qmm.QMM_Q8_0, 5, [ok]) == 3
+    assert call(qmm.QMM_Q8_0, 0, [ok, D(16, 16, 16, 9, 8, 64)]) == 2      # M > QMM_BATCH_MAX_M
+    assert call(qmm.QMM_Q8_0, 0, [ok, D(16, 16, 16, 2, 8, 16384)]) == 2   # M * K > QMM_BATCH_MAX_MK
+    assert call(qmm.QMM_Q5_0, 1, [D(16, 16, 16, 1, 8, 100)]) == 2         # K % 32
+    assert call(qmm.QMM_Q4_0, 0, [D(None, 16, 16, 1, 8, 64)]) == 1
+    assert call(qmm.QMM_Q8_0, 0, [D(18, 16, 16, 1, 8, 64)]) == 4
+    assert call(qmm.QMM_Q8_0, 0, [D(None, None, None, 0, 8, 64)]) == 0   # empty items are skipped
+    assert L.qmm_matmul_batch(qmm.QMM_Q8_0, 0, None, 0, None) == 0
+    assert L.qmm_matmul_batch(qmm.QMM_Q8_0, 0, None, 3, None) == 1
+
+
 def test_binding_raises_on_error_status(qmm):
     with pytest.raises(qmm.QmmError) as e:
         qmm._check(2, "qmm_matmul")

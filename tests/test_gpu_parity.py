@@ -316,3 +316,48 @@ def test_weights_beyond_2gb_use_64_bit_offsets(qmm, orc, M):
     del wq
     torch.cuda.empty_cache()
     check_device_error(qmm)
+
+
+@pytest.mark.parametrize("wtype", ["q8_0", "q4_0", "q5_0"])
+@pytest.mark.parametrize("mode", ["int8_act", "f32_act"])
+def test_matmul_batch_items_within_bound(qmm, orc, wtype, mode):
+    """qmm_matmul_batch: items of different N, K and M (<= 8), some sharing
+    one x, each within the bound of its own oracle product."""
+    shapes = [(1, 576, 576), (1, 192, 576), (1, 1536, 576), (1, 576, 1536), (4, 100, 2048), (8, 33, 64),
+              (2, 4097, 256), (3, 1, 32), (1, 576, 576)]
+    items, ref = [], []
+    xs = {}
+    for i, (M, N, K) in enumerate(shapes):
+        w = qmm_synth.weights(N, K, seed=40 + i)
+        wq = orc.quantize(wtype, w)
+        if (M, K) not in xs:                 # items with the same (M, K) share x
+            xs[(M, K)] = qmm_synth.activations(M, K, seed=60 + i)
+        x = xs[(M, K)]
+        items.append((dev(wq), dev(x), torch.full((M, N), float("nan"), device="cuda")))
+        ref.append(orc.matmul(wtype, mode, wq, x))
+    qmm.matmul_batch(items, wtype, mode)
+    for (wq, x, y), (y_orc, T), s in zip(items, ref, shapes):
+        assert_within_bound(host(y), y_orc, T, f"batch {wtype} {mode} {s}")
+    check_device_error(qmm)
+
+
+def test_matmul_batch_smollm2_step_matches_single_calls(qmm, orc):
+    """The 211 linears of the SmolLM2-135M-shaped decode step in one batch
+    (two launches of <= 256 items would also do): every output equals the
+    single-call result within the bound, checked against the oracle on a few
+    items, and the batch writes every row."""
+    lins = qmm_synth.smollm2_linears()
+    xs = {K: dev(qmm_synth.activations(1, K, seed=K)) for K in (576, 1536)}
+    items = []
+    for i, (_, N, K) in enumerate(lins):
+        g = torch.Generator(device="cuda").manual_seed(1000 + i)
+        w = torch.randn((N, K), generator=g, device="cuda") * 0.02
+        items.append((qmm.quantize_weights(w, "q8_0"), xs[K], torch.full((1, N), float("nan"), device="cuda")))
+    for mode in ("int8_act", "f32_act"):
+        qmm.matmul_batch(items, "q8_0", mode)
+        for i in (0, 1, 6, 100, len(items) - 1):
+            wq, x, y = items[i]
+            y_orc, T = orc.matmul("q8_0", mode, host(wq), host(x))
+            assert_within_bound(host(y), y_orc, T, f"smollm2 item {i} {mode}")
+        assert all(bool(torch.isfinite(y).all()) for _, _, y in items)
+    check_device_error(qmm)
