@@ -518,10 +518,27 @@ def run_ours(args):
 
 
 def run_profile_case(spec: str, launches: int):
-    """A few launches of one configuration, for ncu: spec = wtype:mode:M:N:K."""
+    """A few launches of one configuration, for ncu: spec = wtype:mode:M:N:K, or
+    smollm2_batch:wtype:mode for the 211-item SmolLM2-135M decode step as one
+    qmm_matmul_batch call (M = 1)."""
     import torch
 
     import gguf_block_quantized_qmatmul_gb300 as q
+    if spec.startswith("smollm2_batch:"):
+        _, wtype, mode = spec.split(":")
+        wqs = []
+        for i, (_, N, K) in enumerate(qmm_synth.smollm2_linears()):
+            g = torch.Generator(device="cuda").manual_seed(1000 + i)
+            wqs.append((q.quantize_weights(torch.randn((N, K), generator=g, device="cuda") * 0.02, wtype), N, K))
+        xs = {K: torch.from_numpy(qmm_synth.activations(1, K)).cuda() for K in (576, 1536)}
+        ys = [torch.empty((1, N), dtype=torch.float32, device="cuda") for _, N, _ in wqs]
+        batch = q.MatmulBatch([(w, xs[K], y) for (w, N, K), y in zip(wqs, ys)], wtype, mode)
+        for _ in range(launches):
+            batch.run()
+        torch.cuda.synchronize()
+        assert q.last_device_error() == 0
+        print(f"profile case {spec}: {launches} launches ok")
+        return
     wtype, mode, M, N, K = spec.split(":")
     M, N, K = int(M), int(N), int(K)
     g = torch.Generator(device="cuda").manual_seed(0)
@@ -549,7 +566,7 @@ def main():
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-small", action="store_true")
-    ap.add_argument("--profile", default=None, help="wtype:mode:M:N:K -- run a few launches for ncu and exit")
+    ap.add_argument("--profile", default=None, help="wtype:mode:M:N:K or smollm2_batch:wtype:mode -- run a few launches for ncu and exit")
     ap.add_argument("--launches", type=int, default=4)
     args = ap.parse_args()
     if args.profile:

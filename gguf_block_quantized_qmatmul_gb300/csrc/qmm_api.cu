@@ -376,6 +376,7 @@ qmm_status qmm_matmul_batch(qmm_type wtype, qmm_act_mode mode, const qmm_matmul_
         p.count = 0;
         p.total = 0;
         p.max_mk = 0;
+        p.err = err;
         int max_m = 1;
         for (; i < count && p.count < kBatchMax; ++i) {
             const qmm_matmul_desc& d = items[i];
@@ -387,14 +388,14 @@ qmm_status qmm_matmul_batch(qmm_type wtype, qmm_act_mode mode, const qmm_matmul_
             it.M = (int)d.M;
             it.N = (int)d.N;
             it.K = (int)d.K;
-            it.pad = 0;
+            it.lpr = it.bpl = it.tr = 0;
             it.byte0 = p.total;
             p.total += d.N * (d.K / 32) * bb;
             if (d.M * d.K > p.max_mk) p.max_mk = (int)(d.M * d.K);
             if (d.M > max_m) max_m = (int)d.M;
         }
         if (p.count == 0) break;
-        if (launch_batch(wt, mode == QMM_INT8_ACT ? A_INT8 : A_F32, p, max_m, sms, s) != cudaSuccess) return QMM_ERR_CUDA;
+        if (launch_batch(wt, mode == QMM_INT8_ACT ? A_INT8 : A_F32, p, max_m, sms, smem, s) != cudaSuccess) return QMM_ERR_CUDA;
     }
     return QMM_OK;
 }
