@@ -259,8 +259,10 @@ def small_configs(q, torch, stream):
     """Latency-bound configurations: one Q8_0 GEMV 576x576 (M=1), the Q4_K
     576x1536 GEMV (M = 1, 2, 4, 8), and the 211-matmul SmolLM2-135M-shaped
     decode step (all Q8_0, M=1), each in both forms.  The step is timed with
-    the L2 flushed before every step (a 2 x L2 write): eagerly and replayed
-    from a CUDA graph (211 launches), and as one qmm_matmul_batch call."""
+    the L2 flushed before every step (a 2 x L2 buffer written, then read back
+    so that no dirty line of it is written back inside the timed step):
+    eagerly and replayed from a CUDA graph (211 launches), and as one
+    qmm_matmul_batch call."""
     out = {}
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
 
@@ -295,6 +297,14 @@ def small_configs(q, torch, stream):
     xs = {K: torch.from_numpy(qmm_synth.activations(1, K)).cuda() for K in (576, 1536)}
     ys = [torch.empty((1, N), dtype=torch.float32, device="cuda") for _, N, _ in wqs]
     flush = torch.empty(2 * 129 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+    sink = torch.empty(1, dtype=torch.float32, device="cuda")
+
+    def flush_l2():
+        # write a 2 x L2 buffer, then read it back: L2 then holds clean lines of the
+        # flush buffer, so the timed step pays no write-back of the flush's dirty lines
+        flush.fill_(1.0)
+        sink.copy_(flush.sum().reshape(1))
+
     for mode in MODES:
         def step():
             for (w, N, K), y in zip(wqs, ys):
@@ -310,7 +320,7 @@ def small_configs(q, torch, stream):
             tot = 0.0
             reps = 20
             for _ in range(reps + 3):
-                flush.fill_(1.0)
+                flush_l2()
                 ev0.record(stream)
                 fn()
                 ev1.record(stream)
@@ -332,7 +342,7 @@ def small_configs(q, torch, stream):
             tot = 0.0
             reps = 20
             for _ in range(reps + 3):
-                flush.fill_(1.0)
+                flush_l2()
                 ev0.record(stream)
                 fn()
                 ev1.record(stream)
@@ -342,6 +352,44 @@ def small_configs(q, torch, stream):
             res[name] = {"ms_per_step": round(ms, 4), "weight_GBps": round(step_bytes / (ms * 1e6), 1), "launches": 1}
     out["smollm2_step_weight_bytes"] = step_bytes
     return out
+
+
+def dequant_all_case(q, torch, stream, wq, t, N, K, Ms=(16, 256, 1024)):
+    """The dequantize-all serving form as a comparison point: the weights
+    dequantized once (the library's dequantize kernel, timed on its own) and
+    kept as dense f32 or bf16, then one cuBLAS GEMM per call (f32 with TF32
+    off, or bf16 operands with f32 accumulation).  TOPS = 2 M N K / time."""
+    res = {}
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def timed(fn, reps=10):
+        fn()
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        for _ in range(reps):
+            fn()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        return ev0.elapsed_time(ev1) / reps
+
+    w32 = torch.empty((N, K), dtype=torch.float32, device="cuda")
+    res["dequantize_ms"] = round(timed(lambda: q.dequantize(wq, t, K, out=w32)), 4)
+    w16 = w32.to(torch.bfloat16)
+    tf32 = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = False
+    try:
+        for M in Ms:
+            x = torch.from_numpy(qmm_synth.activations(M, K, outlier_channels=4)).cuda()
+            x16 = x.to(torch.bfloat16)
+            y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+            y16 = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+            ms32 = timed(lambda: torch.matmul(x, w32.t(), out=y))
+            ms16 = timed(lambda: torch.matmul(x16, w16.t(), out=y16))
+            res[f"M{M}"] = {"f32_gemm_ms": round(ms32, 4), "f32_gemm_TOPS": round(2.0 * M * N * K / ms32 / 1e9, 1),
+                            "bf16_gemm_ms": round(ms16, 4), "bf16_gemm_TOPS": round(2.0 * M * N * K / ms16 / 1e9, 1)}
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = tf32
+    return res
 
 
 def run_ours(args):
@@ -450,6 +498,7 @@ def run_ours(args):
     # 3 x 2 M N K; its rate is compared with the measured dense bf16 peak (f16 runs
     # at the bf16 rate).
     prefill = {}
+    dequant_all = {}
     if not args.no_prefill:
         for t in TYPES:
             for N in (4096, 14336):
@@ -478,6 +527,8 @@ def run_ours(args):
                         "tensor_TFLOPs": round(3 * tops, 1),
                         "tensor_frac_of_bf16_peak": round(3 * tops / bf16_peak, 4),
                         "weight_GBps": round(wq.numel() / (ms / 1e3) / 1e9, 1)}
+                if t == "q8_0":
+                    dequant_all[f"{N}x4096"] = dequant_all_case(q, torch, stream, wq, t, N, 4096)
                 del wq
 
     small = small_configs(q, torch, stream) if not args.no_small else {}
@@ -506,6 +557,7 @@ def run_ours(args):
                              "alg_bytes": "weights + x f32 + y f32 per call; a call's duration includes its "
                                           "activation-preparing launch"},
                 "kernels": kernels,
+                "dequantize_all": dequant_all,
                 "cpu_baseline": cpu,
                 "e2e": {"value": round(e2e, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                         "d2h_bytes_per_step": d2h},

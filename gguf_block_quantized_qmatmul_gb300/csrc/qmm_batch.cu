@@ -11,12 +11,16 @@
 //
 // The weight bytes of all items are one virtual stream; CTA c (one per SM)
 // takes the rows whose first byte falls in its 1/G share of it, item by item
-// (a "segment": consecutive rows of one item, contiguous bytes).  A producer
-// lane streams each segment in stages of whole rows with one 1-D bulk copy
-// per stage into a ring of shared-memory slots; 16 consumer warps quantize the
-// item's activation rows into shared memory (int8_act; f32_act copies them)
-// when a segment starts, then take the stage's rows, a warp per row and two
-// rows at once (lanes over blocks), and reduce each row with shuffles.
+// (a "piece": consecutive rows of one item, contiguous bytes).  A producer
+// lane streams each piece in stages of whole rows, one 1-D bulk copy per
+// stage, into a ring of shared-memory slots (the copy engine pays a fixed cost
+// per contiguous segment, so stages are large).  16 consumer warps stage the
+// item's activation rows in shared memory when a piece starts (int8_act
+// quantizes them; f32_act copies them), then take each stage's rows in lane
+// groups: lpr lanes per group, two rows per group sharing the activation
+// loads, lane gl taking blocks gl, gl + lpr, ...; the group sums its lanes
+// with a shuffle tree.  lpr, the blocks per lane and the rows per stage are
+// planned per K on the host.
 #include <algorithm>
 
 #include "qmm_internal.h"

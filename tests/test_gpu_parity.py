@@ -232,6 +232,26 @@ def test_one_hot_f32_act_is_exact(qmm, orc):
             assert np.array_equal(y[i], W[:, k])
 
 
+@pytest.mark.parametrize("wtype,M,N,K", [("q8_0", 64, 300, 4096), ("q4_k", 37, 256, 2048), ("q5_0", 16, 96, 576)])
+def test_dequantize_all_form_matches_f32_act(qmm, orc, wtype, M, N, K):
+    """The dequantize-all serving form (the weights dequantized once by the
+    library, then a dense f32 GEMM with TF32 off) has the f32_act definition:
+    it lies within the same bound of the oracle's f32_act output."""
+    w = qmm_synth.weights(N, K, seed=N + 3 * K)
+    x = qmm_synth.activations(M, K, seed=M + 5, outlier_channels=4)
+    wq = orc.quantize(wtype, w)
+    W = qmm.dequantize(dev(wq), wtype, K)
+    assert np.array_equal(host(W), orc.dequantize(wtype, wq, K))
+    tf32 = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = False
+    try:
+        y = host(torch.matmul(dev(x), W.t()))
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = tf32
+    y_orc, T = orc.matmul(wtype, "f32_act", wq, x)
+    assert_within_bound(y, y_orc, T, f"dequantize-all {wtype} M{M} N{N} K{K}")
+
+
 def test_launch_counts(qmm):
     """qmm_matmul_launches mirrors the dispatch (decode: optional activation
     preparation + decode kernel + optional K-split reduction)."""
