@@ -9,9 +9,9 @@ code with it: the arithmetic lives in ``qmm_oracle.c`` (plain C, compiled with
 和下载的 Q8_0 逐字节比 and 大小和误差).  This module only marshals numpy arrays.
 
 Parity status: every function is pinned by ``tests/test_oracle_pins.py`` except
-the Q4_K, Q4_0 and Q5_0 quantizers' choice of codes, which is "parity unpinned"
-beyond their round-trip error bounds and closed forms (the pages give neither
-the algorithms nor the Q4_0/Q5_0 layouts, only their sizes).
+the Q4_K, Q4_0, Q5_0 and Q6_K quantizers' choice of codes, which is "parity
+unpinned" beyond their round-trip error bounds and closed forms (the pages give
+neither the algorithms nor the Q4_0/Q5_0/Q6_K layouts, only their sizes).
 """
 from __future__ import annotations
 
@@ -22,8 +22,8 @@ import threading
 
 import numpy as np
 
-Q8_0, Q4_K, Q8_K, Q4_0, Q5_0 = 1, 2, 3, 4, 5
-NAMES = {"q8_0": Q8_0, "q4_k": Q4_K, "q8_k": Q8_K, "q4_0": Q4_0, "q5_0": Q5_0}
+Q8_0, Q4_K, Q8_K, Q4_0, Q5_0, Q6_K = 1, 2, 3, 4, 5, 6
+NAMES = {"q8_0": Q8_0, "q4_k": Q4_K, "q8_k": Q8_K, "q4_0": Q4_0, "q5_0": Q5_0, "q6_k": Q6_K}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "qmm_oracle.c")
@@ -64,7 +64,7 @@ def _load():
             lib.orc_block_bytes.argtypes = [ctypes.c_int]
             lib.orc_block_bytes.restype = i64
             for f in ("orc_quantize_q8_0", "orc_quantize_q8_k", "orc_quantize_q4_k", "orc_quantize_q4_0",
-                      "orc_quantize_q5_0"):
+                      "orc_quantize_q5_0", "orc_quantize_q6_k"):
                 getattr(lib, f).argtypes = [p, i64, i64, p]
             lib.orc_dequantize.argtypes = [ctypes.c_int, p, i64, i64, p]
             lib.orc_block_sums.argtypes = [ctypes.c_int, p, p, i64, i64, i64, p]
@@ -133,7 +133,7 @@ def quantize(t, x) -> np.ndarray:
     rows, K = x.shape
     out = np.empty((rows, row_bytes(t, K)), dtype=np.uint8)
     fn = {Q8_0: "orc_quantize_q8_0", Q8_K: "orc_quantize_q8_k", Q4_K: "orc_quantize_q4_k",
-          Q4_0: "orc_quantize_q4_0", Q5_0: "orc_quantize_q5_0"}[_t(t)]
+          Q4_0: "orc_quantize_q4_0", Q5_0: "orc_quantize_q5_0", Q6_K: "orc_quantize_q6_k"}[_t(t)]
     getattr(_load(), fn)(_ptr(x), rows, K, _ptr(out))
     return out
 
@@ -148,13 +148,16 @@ def dequantize(t, q, K: int) -> np.ndarray:
 
 def block_sums(wtype, wq, xq, M: int, N: int, K: int) -> np.ndarray:
     """Exact per-block integer sums.  Q8_0, Q4_0, Q5_0 (with Q8_0 activations):
-    int32 [M, N, K/32]; Q4_K: int32 [M, N, K/256, 2] holding (S_sc, S_m)."""
+    int32 [M, N, K/32]; Q4_K: int32 [M, N, K/256, 2] holding (S_sc, S_m);
+    Q6_K: int32 [M, N, K/256] holding S = sum_j sc_j isum_j."""
     wq = np.ascontiguousarray(wq, dtype=np.uint8)
     xq = np.ascontiguousarray(xq, dtype=np.uint8)
-    if _t(wtype) != Q4_K:
-        out = np.empty((M, N, K // 32), dtype=np.int32)
-    else:
+    if _t(wtype) == Q4_K:
         out = np.empty((M, N, K // 256, 2), dtype=np.int32)
+    elif _t(wtype) == Q6_K:
+        out = np.empty((M, N, K // 256), dtype=np.int32)
+    else:
+        out = np.empty((M, N, K // 32), dtype=np.int32)
     _load().orc_block_sums(_t(wtype), _ptr(wq), _ptr(xq), M, N, K, _ptr(out))
     return out
 
@@ -163,7 +166,7 @@ def matmul(wtype, mode: str, wq, x):
     """y [M, N] (float64) and the tolerance scale T [M, N] (sum of |terms|).
 
     mode "int8_act": activations quantized per row (Q8_0 for Q8_0, Q4_0 and
-    Q5_0 weights; Q8K for Q4_K), integer
+    Q5_0 weights; Q8K for Q4_K and Q6_K), integer
     block sums, float combine.  mode "f32_act": f32 activations times the
     dequantized weights (equal by definition to the dequantize-all form)."""
     x = _f32(x)

@@ -26,8 +26,8 @@
  *  codes, 16 int16 sums of 16 codes) follow the public GGUF layout.
  *
  * Readings where the pages are silent (listed with the others in the design
- * notes): Q4_0 and Q5_0 use the public GGUF block layouts and the signed-max
- * quantizer written below; rounding of codes is round-half-away-from-zero (C roundf); codes of
+ * notes): Q4_0, Q5_0 and Q6_K use the public GGUF block layouts and the
+ * signed-max quantizers written below; rounding of codes is round-half-away-from-zero (C roundf); codes of
  * Q8_0/Q8K use the f32 scale d and the reciprocal 1/d; Q8K is symmetric
  * (+-127); Q4_K uses the closed-form min/max quantizer written below; the
  * dequantized Q4_K weight is (f(d)*sc)*q - f(dmin)*m with each product exact
@@ -41,9 +41,10 @@
  * against facts fixed by the pages or by mathematics (sizes, scale rule,
  * exhaustive f16 conversion, brute-force integer sums, round-trip bounds,
  * closed forms, row-permutation and batch invariance, the activation-
- * quantization error scale).  The Q4_K quantizer's code choice itself has no
- * external pin ("parity unpinned" beyond the round-trip bound and the
- * oracle-vs-GPU bit-exact comparison): the pages do not give the algorithm.
+ * quantization error scale).  The code choices of the Q4_K, Q4_0, Q5_0 and
+ * Q6_K quantizers themselves have no external pin ("parity unpinned" beyond
+ * the round-trip bounds, closed forms and the oracle-vs-GPU bit-exact
+ * comparison): the pages give neither the algorithms nor these layouts.
  */
 #include <math.h>
 #include <stdint.h>
@@ -54,7 +55,7 @@
 #endif
 
 /* type ids used only inside the oracle and its Python wrapper */
-enum { ORC_Q8_0 = 1, ORC_Q4_K = 2, ORC_Q8_K = 3, ORC_Q4_0 = 4, ORC_Q5_0 = 5 };
+enum { ORC_Q8_0 = 1, ORC_Q4_K = 2, ORC_Q8_K = 3, ORC_Q4_0 = 4, ORC_Q5_0 = 5, ORC_Q6_K = 6 };
 
 /* bytes of one block and values per block (page [p3] sizes; GGUF layout) */
 #define ORC_Q8_0_VALS 32
@@ -64,6 +65,7 @@ enum { ORC_Q8_0 = 1, ORC_Q4_K = 2, ORC_Q8_K = 3, ORC_Q4_0 = 4, ORC_Q5_0 = 5 };
 #define ORC_Q8_K_BYTES 292
 #define ORC_Q4_0_BYTES 18   /* page [p3] file sizes: Q4_0 18 B per 32 values */
 #define ORC_Q5_0_BYTES 22   /* Q5_0 22 B per 32 values */
+#define ORC_Q6_K_BYTES 210  /* the downloaded Q4_K_M file closes with Q6K at 210 B per 256 values */
 
 /* ------------------------------------------------------------------ */
 /* IEEE-754 binary16 <-> binary32, written from the format definition  */
@@ -161,7 +163,8 @@ int64_t orc_f16_check_range(uint64_t lo, uint64_t hi) {
 /* ------------------------------------------------------------------ */
 
 int64_t orc_block_values(int t) {
-    return (t == ORC_Q8_0 || t == ORC_Q4_0 || t == ORC_Q5_0) ? 32 : (t == ORC_Q4_K || t == ORC_Q8_K) ? ORC_QK_VALS : 0;
+    return (t == ORC_Q8_0 || t == ORC_Q4_0 || t == ORC_Q5_0) ? 32
+           : (t == ORC_Q4_K || t == ORC_Q8_K || t == ORC_Q6_K) ? ORC_QK_VALS : 0;
 }
 
 int64_t orc_block_bytes(int t) {
@@ -171,6 +174,7 @@ int64_t orc_block_bytes(int t) {
         case ORC_Q8_K: return ORC_Q8_K_BYTES;
         case ORC_Q4_0: return ORC_Q4_0_BYTES;
         case ORC_Q5_0: return ORC_Q5_0_BYTES;
+        case ORC_Q6_K: return ORC_Q6_K_BYTES;
         default: return 0;
     }
 }
@@ -407,6 +411,79 @@ static void q4_k_codes(const uint8_t* blk, uint8_t q[256]) {
         }
 }
 
+
+/* ------------------------------------------------------------------ */
+/* Q6_K: 256 values = 16 groups of 16, signed 6-bit codes.               */
+/*   bytes 0-127 ql (low 4 bits), 128-191 qh (high 2 bits), 192-207 the */
+/*   16 int8 group scales, 208-209 f16 d (the public GGUF field order).  */
+/*   Value i: half h = i / 128, w = i % 128, quarter q = w / 32,          */
+/*   l = w % 32.  Its low 4 bits are nibble q / 2 (0 low, 1 high) of ql  */
+/*   byte 64h + 32 (q % 2) + l; its high 2 bits are bits 2q, 2q+1 of qh  */
+/*   byte 32h + l; the code is those 6 bits minus 32.  Group j = i / 16  */
+/*   has the scale sc_j.  The weight is (f(d) sc_j) code, exact in f32   */
+/*   (an 11-bit by 7-bit product times at most 2^5).                     */
+/* Quantizer (a reading, the same signed-max rule as Q4_0 / Q5_0 per     */
+/* group): m_j, the group's value of largest magnitude (the first on     */
+/* ties, sign kept), gives s_j = m_j / -32; d = max_j |s_j| / 127;        */
+/* sc_j = roundf(s_j / d) clamped to [-127, 127] (0 when d = 0); with    */
+/* e_j = f(D) sc_j, code = roundf(x / e_j) clamped to [-32, 31] (0 when  */
+/* e_j = 0).                                                            */
+/* ------------------------------------------------------------------ */
+
+static int q6_k_index_ql(int i) { int h = i / 128, w = i % 128; return 64 * h + 32 * ((w / 32) % 2) + w % 32; }
+static int q6_k_shift_ql(int i) { return 4 * ((i % 128) / 64); }
+static int q6_k_index_qh(int i) { int h = i / 128, w = i % 128; return 128 + 32 * h + w % 32; }
+static int q6_k_shift_qh(int i) { return 2 * ((i % 128) / 32); }
+
+static void q6_k_block(const float* x, uint8_t* out) {
+    float s[16];
+    for (int j = 0; j < 16; ++j) {
+        float amax = 0.0f, m = 0.0f;
+        for (int i = 0; i < 16; ++i) {
+            float a = fabsf(x[16 * j + i]);
+            if (a > amax) { amax = a; m = x[16 * j + i]; }
+        }
+        s[j] = m / -32.0f;
+    }
+    float smax = 0.0f;
+    for (int j = 0; j < 16; ++j) if (fabsf(s[j]) > smax) smax = fabsf(s[j]);
+    float d = smax / 127.0f;
+    int sc[16];
+    for (int j = 0; j < 16; ++j) sc[j] = d > 0.0f ? (int)clampf(roundf(s[j] / d), -127.0f, 127.0f) : 0;
+    uint16_t D = orc_f32_to_f16(d);
+    float fD = orc_f16_to_f32(D);
+    memset(out, 0, ORC_Q6_K_BYTES);
+    for (int j = 0; j < 16; ++j) {
+        out[192 + j] = (uint8_t)(int8_t)sc[j];
+        float e = fD * (float)sc[j];
+        for (int i = 16 * j; i < 16 * j + 16; ++i) {
+            int c = e != 0.0f ? (int)clampf(roundf(x[i] / e), -32.0f, 31.0f) : 0;
+            int u = c + 32;  /* 0..63 */
+            out[q6_k_index_ql(i)] |= (uint8_t)((u & 15) << q6_k_shift_ql(i));
+            out[q6_k_index_qh(i)] |= (uint8_t)((u >> 4) << q6_k_shift_qh(i));
+        }
+    }
+    put_u16(out + 208, D);
+}
+
+void orc_quantize_q6_k(const float* x, int64_t rows, int64_t K, uint8_t* out) {
+    int64_t nb = K / 256;
+    #pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t b = 0; b < nb; ++b)
+            q6_k_block(x + r * K + b * 256, out + (r * nb + b) * ORC_Q6_K_BYTES);
+}
+
+/* the 256 signed codes and the 16 group scales of a Q6_K super-block */
+static void q6_k_codes(const uint8_t* blk, int c[256], int sc[16]) {
+    for (int i = 0; i < 256; ++i) {
+        int lo = (blk[q6_k_index_ql(i)] >> q6_k_shift_ql(i)) & 15;
+        int hi = (blk[q6_k_index_qh(i)] >> q6_k_shift_qh(i)) & 3;
+        c[i] = (lo | (hi << 4)) - 32;
+    }
+    for (int j = 0; j < 16; ++j) sc[j] = (int8_t)blk[192 + j];
+}
+
 /* ------------------------------------------------------------------ */
 /* Dequantize ([p1] CANDLE_DEQUANTIZE_ALL form)                          */
 /* ------------------------------------------------------------------ */
@@ -432,6 +509,17 @@ static void dequant_row(int t, const uint8_t* q, int64_t K, float* out) {
             const uint8_t* blk = q + b * ORC_Q8_K_BYTES;
             float d = get_f32(blk);
             for (int i = 0; i < 256; ++i) out[b * 256 + i] = d * (float)(int8_t)blk[4 + i];
+        }
+    } else if (t == ORC_Q6_K) {
+        for (int64_t b = 0; b < K / 256; ++b) {
+            const uint8_t* blk = q + b * ORC_Q6_K_BYTES;
+            float fD = orc_f16_to_f32(get_u16(blk + 208));
+            int c[256], sc[16];
+            q6_k_codes(blk, c, sc);
+            for (int i = 0; i < 256; ++i) {
+                float e = fD * (float)sc[i / 16];     /* exact: 11 x 7 bits */
+                out[b * 256 + i] = e * (float)c[i];   /* exact: |c| <= 2^5 */
+            }
         }
     } else if (t == ORC_Q4_K) {
         for (int64_t b = 0; b < K / 256; ++b) {
@@ -501,16 +589,39 @@ static void sums_q4_k(const uint8_t* wrow, const uint8_t* arow, int64_t nsb, int
     }
 }
 
+/* Q6_K x Q8K: S = sum_j sc_j * sum_{i in group j} code_i * a_i (int32) */
+static void sums_q6_k(const uint8_t* wrow, const uint8_t* arow, int64_t nsb, int32_t* out) {
+    for (int64_t s = 0; s < nsb; ++s) {
+        const uint8_t* w = wrow + s * ORC_Q6_K_BYTES;
+        const uint8_t* a = arow + s * ORC_Q8_K_BYTES;
+        int c[256], sc[16];
+        q6_k_codes(w, c, sc);
+        int32_t S = 0;
+        for (int j = 0; j < 16; ++j) {
+            int32_t isum = 0;
+            for (int i = 16 * j; i < 16 * j + 16; ++i) isum += (int32_t)c[i] * (int32_t)(int8_t)a[4 + i];
+            S += sc[j] * isum;
+        }
+        out[s] = S;
+    }
+}
+
 /* wq: N rows of weight blocks; xq: M rows of activation blocks (Q8_0 for
-   Q8_0 weights, Q8K for Q4_K weights).  out: int32 [M][N][nb] (Q8_0) or
-   [M][N][nsb][2] (Q4_K). */
+   Q8_0 / Q4_0 / Q5_0 weights, Q8K for Q4_K and Q6_K weights).  out: int32
+   [M][N][nb] (32-value blocks), [M][N][nsb][2] (Q4_K) or [M][N][nsb] (Q6_K). */
 void orc_block_sums(int wtype, const uint8_t* wq, const uint8_t* xq, int64_t M, int64_t N, int64_t K, int32_t* out) {
-    if (wtype != ORC_Q4_K) {
+    if (wtype != ORC_Q4_K && wtype != ORC_Q6_K) {
         int64_t nb = K / 32, rbw = nb * orc_block_bytes(wtype), rba = nb * ORC_Q8_0_BYTES;
         #pragma omp parallel for schedule(static) collapse(2)
         for (int64_t m = 0; m < M; ++m)
             for (int64_t n = 0; n < N; ++n)
                 sums_b32(wtype, wq + n * rbw, xq + m * rba, nb, out + (m * N + n) * nb);
+    } else if (wtype == ORC_Q6_K) {
+        int64_t nsb = K / 256, rbw = nsb * ORC_Q6_K_BYTES, rba = nsb * ORC_Q8_K_BYTES;
+        #pragma omp parallel for schedule(static) collapse(2)
+        for (int64_t m = 0; m < M; ++m)
+            for (int64_t n = 0; n < N; ++n)
+                sums_q6_k(wq + n * rbw, xq + m * rba, nsb, out + (m * N + n) * nsb);
     } else {
         int64_t nsb = K / 256, rbw = nsb * ORC_Q4_K_BYTES, rba = nsb * ORC_Q8_K_BYTES;
         #pragma omp parallel for schedule(static) collapse(2)
@@ -529,7 +640,28 @@ void orc_block_sums(int wtype, const uint8_t* wq, const uint8_t* xq, int64_t M, 
    integer block sums, then y = sum over blocks of scale products x sums. */
 void orc_matmul_int8_act(int wtype, const uint8_t* wq, const float* x, int64_t M, int64_t N, int64_t K,
                          double* y, double* T) {
-    if (wtype != ORC_Q4_K) {  /* Q8_0, Q4_0, Q5_0 weights with Q8_0 activations */
+    if (wtype == ORC_Q6_K) {  /* Q6_K weights with Q8K activations */
+        int64_t nsb = K / 256, rbw = nsb * ORC_Q6_K_BYTES, rba = nsb * ORC_Q8_K_BYTES;
+        uint8_t* xq = (uint8_t*)malloc((size_t)(M * rba));
+        orc_quantize_q8_k(x, M, K, xq);
+        #pragma omp parallel for schedule(dynamic, 16) collapse(2)
+        for (int64_t m = 0; m < M; ++m)
+            for (int64_t n = 0; n < N; ++n) {
+                double acc = 0.0, t = 0.0;
+                for (int64_t s = 0; s < nsb; ++s) {
+                    const uint8_t* w = wq + n * rbw + s * ORC_Q6_K_BYTES;
+                    const uint8_t* a = xq + m * rba + s * ORC_Q8_K_BYTES;
+                    int32_t S;
+                    sums_q6_k(w, a, 1, &S);
+                    double term = (double)get_f32(a) * (double)orc_f16_to_f32(get_u16(w + 208)) * (double)S;
+                    acc += term;
+                    t += fabs(term);
+                }
+                y[m * N + n] = acc;
+                T[m * N + n] = t;
+            }
+        free(xq);
+    } else if (wtype != ORC_Q4_K) {  /* Q8_0, Q4_0, Q5_0 weights with Q8_0 activations */
         int64_t nb = K / 32, wb = orc_block_bytes(wtype), rbw = nb * wb, rba = nb * ORC_Q8_0_BYTES;
         uint8_t* xq = (uint8_t*)malloc((size_t)(M * rba));
         orc_quantize_q8_0(x, M, K, xq);

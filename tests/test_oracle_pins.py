@@ -60,6 +60,26 @@ def py_decode_q4_k(row: np.ndarray, K: int):
     return D, Dm, sc, mn, q
 
 
+def py_decode_q6_k(row: np.ndarray, K: int):
+    """Q6_K super-block: ql[128] (low 4 bits), qh[64] (high 2 bits), 16 int8
+    group scales, f16 d.  Value i: half h = i // 128, w = i % 128, quarter
+    q = w // 32, l = w % 32; low bits = nibble q // 2 of ql[64h + 32 (q % 2)
+    + l], high bits = bits 2q..2q+1 of qh[32h + l]; code = 6 bits - 32."""
+    blocks = row.reshape(K // 256, 210)
+    ql = blocks[:, 0:128].astype(np.int64)
+    qh = blocks[:, 128:192].astype(np.int64)
+    sc = blocks[:, 192:208].view(np.int8).astype(np.int64)
+    D = py_f16(blocks[:, 208].astype(np.uint16) | (blocks[:, 209].astype(np.uint16) << 8))
+    q = np.zeros((K // 256, 256), np.int64)
+    for i in range(256):
+        h, w = divmod(i, 128)
+        qq, l = divmod(w, 32)
+        lo = (ql[:, 64 * h + 32 * (qq % 2) + l] >> (4 * (qq // 2))) & 15
+        hi = (qh[:, 32 * h + l] >> (2 * qq)) & 3
+        q[:, i] = (lo | (hi << 4)) - 32
+    return D, sc, q
+
+
 # ---------------------------------------------------------------------------
 # f16 conversion
 # ---------------------------------------------------------------------------
@@ -354,7 +374,7 @@ def test_row_permutation_permutes_blocks(orc):
     assert np.array_equal(orc.quantize("q4_k", w[perm]), orc.quantize("q4_k", w)[perm])
 
 
-@pytest.mark.parametrize("wtype,K", [("q8_0", 576), ("q4_k", 1536), ("q4_0", 576), ("q5_0", 576)])
+@pytest.mark.parametrize("wtype,K", [("q8_0", 576), ("q4_k", 1536), ("q4_0", 576), ("q5_0", 576), ("q6_k", 1536)])
 def test_activation_rows_are_independent(orc, wtype, K):
     """Activation quantization is per row: row m's result is the same alone
     and inside a batch of 8 (contrast: per-tensor dynamic quantization)."""
@@ -367,7 +387,7 @@ def test_activation_rows_are_independent(orc, wtype, K):
         assert np.array_equal(y1[0], yb[m])
 
 
-@pytest.mark.parametrize("wtype,K", [("q8_0", 576), ("q4_k", 1536), ("q4_0", 576), ("q5_0", 576)])
+@pytest.mark.parametrize("wtype,K", [("q8_0", 576), ("q4_k", 1536), ("q4_0", 576), ("q5_0", 576), ("q6_k", 1536)])
 def test_one_hot_activation_selects_dequantized_column(orc, wtype, K):
     """f32_act with x = e_k equals column k of the dequantized weights
     exactly (the Metal form multiplies f32 activations by dequantized
@@ -385,7 +405,7 @@ def test_one_hot_activation_selects_dequantized_column(orc, wtype, K):
 def test_f32_act_equals_dequantized_matmul(orc):
     """f32_act = x @ dequant(W)^T (the dequantize-all form), here against
     numpy's float64 matmul of the dequantized weights."""
-    for wtype, K in (("q8_0", 576), ("q4_k", 512), ("q4_0", 576), ("q5_0", 576)):
+    for wtype, K in (("q8_0", 576), ("q4_k", 512), ("q4_0", 576), ("q5_0", 576), ("q6_k", 512)):
         wq = orc.quantize(wtype, qmm_synth.weights(40, K))
         x = qmm_synth.activations(3, K)
         y, T = orc.matmul(wtype, "f32_act", wq, x)
@@ -421,7 +441,7 @@ def test_constant_row_closed_form(orc):
         assert (w == ref).all()
 
 
-@pytest.mark.parametrize("wtype,K", [("q8_0", 576), ("q4_k", 1536), ("q5_0", 576)])
+@pytest.mark.parametrize("wtype,K", [("q8_0", 576), ("q4_k", 1536), ("q5_0", 576), ("q6_k", 1536)])
 def test_activation_quantization_error_has_the_predicted_size(orc, wtype, K):
     """The CPU form differs from the Metal form only by the activation
     rounding: each code moves x by a near-uniform error of width d_a, so the
@@ -432,7 +452,7 @@ def test_activation_quantization_error_has_the_predicted_size(orc, wtype, K):
     yi, _ = orc.matmul(wtype, "int8_act", wq, x)
     yf, _ = orc.matmul(wtype, "f32_act", wq, x)
     W = orc.dequantize(wtype, wq, K).astype(np.float64)
-    bv = 256 if wtype == "q4_k" else 32
+    bv = 256 if wtype in ("q4_k", "q6_k") else 32
     da = np.abs(x.reshape(4, -1, bv)).max(axis=2) / 127.0
     var = (W ** 2) @ (np.repeat(da, bv, axis=1) ** 2 / 12.0).T        # [N, M]
     z = (yi - yf) / np.sqrt(var.T)
@@ -442,12 +462,128 @@ def test_activation_quantization_error_has_the_predicted_size(orc, wtype, K):
 
 def test_tolerance_scale_bounds_the_output(orc):
     """T = sum of |scaled terms| >= |y| for both forms and all outputs."""
-    for wtype, K in (("q8_0", 576), ("q4_k", 1536), ("q4_0", 576), ("q5_0", 576)):
+    for wtype, K in (("q8_0", 576), ("q4_k", 1536), ("q4_0", 576), ("q5_0", 576), ("q6_k", 1536)):
         wq = orc.quantize(wtype, qmm_synth.weights(64, K))
         x = qmm_synth.activations(2, K)
         for mode in ("int8_act", "f32_act"):
             y, T = orc.matmul(wtype, mode, wq, x)
             assert (np.abs(y) <= T * (1 + 1e-12)).all()
+
+
+# ---------------------------------------------------------------------------
+# Q6_K (weights paired with Q8K activations; the pages fix 210 bytes per 256
+# values, not the quantizer or the layout: the signed-max reading per group of
+# 16 is pinned here by its closed forms and bounds, the layout by the reader)
+# ---------------------------------------------------------------------------
+
+def test_q6_k_bytes_close_the_downloaded_file(orc):
+    """210 B per 256 values: the size with which the downloaded Q4_K_M closes."""
+    assert orc.block_bytes("q6_k") == 210 and orc.block_values("q6_k") == 256
+    with pytest.raises(ValueError):
+        orc.row_bytes("q6_k", 576)
+
+
+def test_q6_k_layout_decode_matches_python_reader(orc):
+    """The oracle's Q6_K dequantization equals the Python reader of the field
+    layout: w = (f(d) sc_j) code, exact in f32."""
+    K = 1024
+    x = qmm_synth.weights(16, K, seed=21)
+    x[3, :16] = np.linspace(-1.0, 1.0, 16, dtype=np.float32)  # one group through zero: codes -32 .. 31
+    q = orc.quantize("q6_k", x)
+    w = orc.dequantize("q6_k", q, K)
+    for r in range(16):
+        D, sc, codes = py_decode_q6_k(q[r], K)
+        assert (codes >= -32).all() and (codes <= 31).all()
+        e = (D[:, None].astype(np.float64) * sc)                      # [nsb, 16]
+        ref = np.repeat(e, 16, axis=1) * codes
+        assert np.array_equal(ref.ravel().astype(np.float32), w[r])
+    _, _, codes = py_decode_q6_k(q[3], K)
+    assert codes[0, :16].min() == -32 and codes[0, :16].max() == 31
+
+
+def test_q6_k_scale_rule_closed_form(orc):
+    """Signed-max reading: the group holding the super-block's largest |x|
+    gets sc = -127 sign(m) (s_j = m / -32 is the largest step), and that
+    element's code is -32; every |sc| <= 127."""
+    K = 2048
+    x = qmm_synth.weights(24, K, seed=22)
+    q = orc.quantize("q6_k", x)
+    for r in range(24):
+        D, sc, codes = py_decode_q6_k(q[r], K)
+        xs = x[r].reshape(-1, 256)
+        for s in range(K // 256):
+            i = int(np.argmax(np.abs(xs[s])))
+            j = i // 16
+            assert sc[s, j] == -127 * np.sign(xs[s, i])
+            assert codes[s, i] == -32
+        assert (np.abs(sc) <= 127).all()
+
+
+def test_q6_k_round_trip_bound(orc):
+    """Per element, with s_j = m_j / -32, d = max|s_j| / 127 and e_j = f(D) sc_j:
+    points inside the grid err <= |e_j| / 2 (+ 2^-20 |x|); every point err <=
+    32 |s_j - e_j| + |e_j|, and |s_j - e_j| <= d / 2 + 127 |d - f(D)|."""
+    K = 1536
+    x = qmm_synth.weights(32, K, seed=23)
+    q = orc.quantize("q6_k", x)
+    w = orc.dequantize("q6_k", q, K).astype(np.float64)
+    for r in range(32):
+        D, sc, codes = py_decode_q6_k(q[r], K)
+        xs = x[r].reshape(-1, 16, 16).astype(np.float64)
+        ws = w[r].reshape(-1, 16, 16)
+        e = np.abs(D[:, None].astype(np.float64) * sc)[:, :, None]
+        err = np.abs(xs - ws)
+        inside = (np.abs(xs) <= 31.5 * e) & (e > 0)
+        assert (err[inside] <= (e / 2 + 2.0 ** -20 * np.abs(xs))[inside]).all()
+        d = np.abs(xs).max(axis=(1, 2), keepdims=True) / 32.0 / 127.0
+        dD = np.maximum(2.0 ** -11 * d, 2.0 ** -25)
+        allb = 32 * (d / 2 + 127 * dD) + e + 2.0 ** -20 * np.abs(xs).max(axis=2, keepdims=True)
+        assert (err <= allb).all()
+
+
+def _brute_q6_k(wq, xq, M, N, K):
+    out = np.zeros((M, N, K // 256), np.int64)
+    for m in range(M):
+        _, a, _ = py_decode_q8_k(xq[m], K)
+        for n in range(N):
+            _, sc, q = py_decode_q6_k(wq[n], K)
+            for s in range(K // 256):
+                out[m, n, s] = sum(int(sc[s, j]) * sum(int(q[s, i]) * int(a[s, i]) for i in range(16 * j, 16 * j + 16))
+                                   for j in range(16))
+    return out
+
+
+@pytest.mark.parametrize("K", [256, 512])
+def test_q6_k_block_sums_equal_brute_force(orc, K):
+    """S = sum_j sc_j sum_{i in group j} code_i a_i equals Python-int brute
+    force, with constant and alternating-sign rows among the inputs."""
+    M, N = 3, 4
+    w = qmm_synth.weights(N, K, seed=24)
+    x = qmm_synth.activations(M, K, seed=25)
+    w[0] = 1.0
+    x[0] = -1.0
+    w[1, ::2] = -5.0
+    wq, xq = orc.quantize("q6_k", w), orc.quantize("q8_k", x)
+    assert np.array_equal(orc.block_sums("q6_k", wq, xq, M, N, K), _brute_q6_k(wq, xq, M, N, K))
+
+
+def test_q6_k_int8_act_is_the_dequantized_dot(orc):
+    """The CPU form equals the float64 dot of the dequantized weights and the
+    dequantized Q8K activation rows: a dropped scale, a wrong group index or
+    a wrong activation offset in the integer path breaks it."""
+    K = 768
+    wq = orc.quantize("q6_k", qmm_synth.weights(40, K, seed=26))
+    x = qmm_synth.activations(3, K, seed=27)
+    y, T = orc.matmul("q6_k", "int8_act", wq, x)
+    W = orc.dequantize("q6_k", wq, K).astype(np.float64)  # exact in f32
+    xq = orc.quantize("q8_k", x)
+    Xq = np.zeros((3, K))
+    for m in range(3):  # d_a q_a exactly, in float64 (it need not fit in f32)
+        d, q, _ = py_decode_q8_k(xq[m], K)
+        Xq[m] = (d[:, None].astype(np.float64) * q).ravel()
+    ref = Xq @ W.T
+    assert np.allclose(y, ref, rtol=0, atol=1e-12 * (np.abs(Xq) @ np.abs(W).T).max())
+    assert (np.abs(y) <= T * (1 + 1e-12)).all()
 
 
 # ---------------------------------------------------------------------------
