@@ -10,8 +10,8 @@ weights).  128 qmm_matmul calls per step, inputs resident in HBM.
 Printed JSON line: value = weight bytes streamed per second (GB/s, whole
 job), roofline of the streaming kernel against the measured HBM copy
 bandwidth, the oracle's throughput on the host cores on a bounded sample, an
-end-to-end figure through the public API with pinned host buffers (x copied in
-and y copied out on every call), SM clocks sampled during the timed region,
+end-to-end figure through the public API with pinned host buffers (each step
+copies its activation batches in and all 128 outputs out), SM clocks sampled during the timed region,
 and a per-(type, form, M) breakdown.  A prefill section times the Llama-shaped
 GEMMs in both forms (4096 x 4096 and 14336 x 4096 weights, M = 16, 37, 64, 256,
 1024) as TOPS, with the tensor work of the three f16 passes against the
@@ -469,18 +469,27 @@ def run_ours(args):
                for k, v in kern.items()}
     launches = sum(q.matmul_launches(t, mode, M, N_DEC, K_DEC) for (M, t, mode, _) in calls)
 
-    # end to end through the public API with pinned host buffers
+    # end to end through the public API with pinned host buffers: each step copies its
+    # activation batches in (one copy per M), runs the 128 calls, each into its own
+    # slice of one output buffer, and reads all 128 outputs back with one copy
     xh = {M: xs[M].cpu().pin_memory() for M in MS}
-    yh = {M: torch.empty((M, N_DEC), dtype=torch.float32).pin_memory() for M in MS}
     xd = {M: torch.empty_like(xs[M]) for M in MS}
-    h2d = sum(xh[M].numel() * 4 for (M, _, _, _) in calls)
-    d2h = sum(yh[M].numel() * 4 for (M, _, _, _) in calls)
+    offs, o = [], 0
+    for (M, _, _, _) in calls:
+        offs.append(o)
+        o += M * N_DEC
+    y_all = torch.empty(o, dtype=torch.float32, device="cuda")
+    y_host = torch.empty(o, dtype=torch.float32).pin_memory()
+    y_views = [y_all[a:a + M * N_DEC].view(M, N_DEC) for a, (M, _, _, _) in zip(offs, calls)]
+    h2d = sum(xh[M].numel() * 4 for M in MS)
+    d2h = y_host.numel() * 4
 
     def e2e_step():
-        for (M, t, mode, b) in calls:
+        for M in MS:
             xd[M].copy_(xh[M], non_blocking=True)
-            q.matmul(wqs[t][b], xd[M], t, mode, N=N_DEC, out=ys[M], workspace=ws)
-            yh[M].copy_(ys[M], non_blocking=True)
+        for (M, t, mode, b), yv in zip(calls, y_views):
+            q.matmul(wqs[t][b], xd[M], t, mode, N=N_DEC, out=yv, workspace=ws)
+        y_host.copy_(y_all, non_blocking=True)
 
     for _ in range(max(1, args.warmup)):
         e2e_step()

@@ -7,7 +7,7 @@ is no CPU fallback: the first call raises ImportError when the library is
 missing.
 
 Entry points mirror the C ABI names:
-  quantize_weights(w, wtype)      Q8_0 / Q4_K / Q4_0 / Q5_0 blocks of f32 weights [N, K]
+  quantize_weights(w, wtype)      Q8_0 / Q4_K / Q4_0 / Q5_0 / Q6_K blocks of f32 weights [N, K]
   quantize_act(x, atype)          Q8_0 / Q8_K blocks of f32 activations [M, K]
   dequantize(q, t, K)             f32 [rows, K]
   matmul(wq, x, wtype, mode)      y = x . W^T, mode "int8_act" or "f32_act"
@@ -23,9 +23,10 @@ import torch
 
 from . import build as _build
 
-QMM_F32, QMM_Q8_0, QMM_Q4_K, QMM_Q8_K, QMM_Q4_0, QMM_Q5_0 = 0, 1, 2, 3, 4, 5
+QMM_F32, QMM_Q8_0, QMM_Q4_K, QMM_Q8_K, QMM_Q4_0, QMM_Q5_0, QMM_Q6_K = 0, 1, 2, 3, 4, 5, 6
 QMM_INT8_ACT, QMM_F32_ACT = 0, 1
-TYPES = {"f32": QMM_F32, "q8_0": QMM_Q8_0, "q4_k": QMM_Q4_K, "q8_k": QMM_Q8_K, "q4_0": QMM_Q4_0, "q5_0": QMM_Q5_0}
+TYPES = {"f32": QMM_F32, "q8_0": QMM_Q8_0, "q4_k": QMM_Q4_K, "q8_k": QMM_Q8_K, "q4_0": QMM_Q4_0, "q5_0": QMM_Q5_0,
+         "q6_k": QMM_Q6_K}
 MODES = {"int8_act": QMM_INT8_ACT, "f32_act": QMM_F32_ACT}
 STATUS = {0: "QMM_OK", 1: "QMM_ERR_NULL", 2: "QMM_ERR_SHAPE", 3: "QMM_ERR_TYPE", 4: "QMM_ERR_ALIGN",
           5: "QMM_ERR_WORKSPACE", 6: "QMM_ERR_CUDA", 7: "QMM_ERR_TIMEOUT"}
@@ -152,9 +153,10 @@ def matmul(wq: torch.Tensor, x: torch.Tensor, wtype, mode, N: int | None = None,
         N = wq.numel() // row_bytes(wtype, K)
     if out is None:
         out = torch.empty((M, N), dtype=torch.float32, device=x.device)
-    need = matmul_workspace(wtype, mode, M, N, K)
-    if need and workspace is None:
-        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    if workspace is None:  # a caller's workspace is checked by the library (QMM_ERR_WORKSPACE)
+        need = matmul_workspace(wtype, mode, M, N, K)
+        if need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(_lib().qmm_matmul(_t(wtype), _m(mode), _ptr(wq), _ptr(x), _ptr(out), M, N, K, _ptr(workspace), ws_bytes,
                           _stream(stream)), "qmm_matmul")
@@ -165,10 +167,12 @@ def block_sums(wq: torch.Tensor, x: torch.Tensor, wtype, N: int | None = None, s
     M, K = x.shape
     if N is None:
         N = wq.numel() // row_bytes(wtype, K)
-    if _t(wtype) != QMM_Q4_K:  # 32-value blocks (Q8_0, Q4_0, Q5_0)
-        out = torch.empty((M, N, K // 32), dtype=torch.int32, device=x.device)
-    else:
+    if _t(wtype) == QMM_Q4_K:  # (S_sc, S_m) per super-block
         out = torch.empty((M, N, K // 256, 2), dtype=torch.int32, device=x.device)
+    elif _t(wtype) == QMM_Q6_K:  # S per super-block
+        out = torch.empty((M, N, K // 256), dtype=torch.int32, device=x.device)
+    else:  # 32-value blocks (Q8_0, Q4_0, Q5_0)
+        out = torch.empty((M, N, K // 32), dtype=torch.int32, device=x.device)
     _check(_lib().qmm_block_sums(_t(wtype), _ptr(wq), _ptr(x), M, N, K, _ptr(out), _stream(stream)), "qmm_block_sums")
     return out
 

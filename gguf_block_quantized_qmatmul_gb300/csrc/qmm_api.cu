@@ -44,10 +44,12 @@ cudaError_t device_info(unsigned** err, int* sms, int* smem, int* device = nullp
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 bool valid_type(qmm_type t) {
-    return t == QMM_Q8_0 || t == QMM_Q4_K || t == QMM_Q8_K || t == QMM_Q4_0 || t == QMM_Q5_0;
+    return t == QMM_Q8_0 || t == QMM_Q4_K || t == QMM_Q8_K || t == QMM_Q4_0 || t == QMM_Q5_0 || t == QMM_Q6_K;
 }
-// weight types: Q8_0, Q4_0, Q5_0 (with Q8_0 activations) and Q4_K (with Q8K)
-bool weight_type(qmm_type t) { return t == QMM_Q8_0 || t == QMM_Q4_K || t == QMM_Q4_0 || t == QMM_Q5_0; }
+// weight types: Q8_0, Q4_0, Q5_0 (with Q8_0 activations); Q4_K, Q6_K (with Q8K)
+bool weight_type(qmm_type t) {
+    return t == QMM_Q8_0 || t == QMM_Q4_K || t == QMM_Q4_0 || t == QMM_Q5_0 || t == QMM_Q6_K;
+}
 int internal_type(qmm_type t) {
     switch (t) {
         case QMM_Q8_0: return T_Q8_0;
@@ -55,6 +57,7 @@ int internal_type(qmm_type t) {
         case QMM_Q8_K: return T_Q8_K;
         case QMM_Q4_0: return T_Q4_0;
         case QMM_Q5_0: return T_Q5_0;
+        case QMM_Q6_K: return T_Q6_K;
         default: return T_F32;
     }
 }
@@ -91,8 +94,10 @@ struct Dispatch {
 
 void plan_dispatch(int wt, int am, int epi, long long M, long long N, long long K, int sms, int smem, Dispatch& d) {
     d = Dispatch();
-    if (wt == T_Q4_0 || wt == T_Q5_0) {  // prefill on the tcgen05 GEMM where K allows, else the streaming kernel
-        if (epi == E_Y && M > kDecodeMaxM && plan_tc(wt, am, M, N, K, sms, smem, d.tp)) {
+    if (wt == T_Q4_0 || wt == T_Q5_0 || wt == T_Q6_K) {
+        // Q4_0 / Q5_0: prefill on the tcgen05 GEMM where K allows; everything else
+        // (and every Q6_K call) on the streaming kernel
+        if (wt != T_Q6_K && epi == E_Y && M > kDecodeMaxM && plan_tc(wt, am, M, N, K, sms, smem, d.tp)) {
             d.kind = KIND_TC;
             d.workspace = d.tp.workspace;
             d.launches = 2;  // operand preparation, GEMM
@@ -222,7 +227,8 @@ qmm_status stream_call(qmm_type wtype, int am, int epi, const void* wq, const fl
     const cudaError_t e = wt == T_Q8_0   ? launch_stream_q8_0(am, epi, pl, smem, s)
                           : wt == T_Q4_K ? launch_stream_q4_k(am, epi, pl, smem, s)
                           : wt == T_Q4_0 ? launch_stream_q4_0(am, epi, pl, smem, s)
-                                         : launch_stream_q5_0(am, epi, pl, smem, s);
+                          : wt == T_Q5_0 ? launch_stream_q5_0(am, epi, pl, smem, s)
+                                         : launch_stream_q6_k(am, epi, pl, smem, s);
     return e == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
 }
 
@@ -238,6 +244,7 @@ int64_t qmm_block_values(qmm_type t) {
         case QMM_Q8_K: return 256;
         case QMM_Q4_0: return 32;
         case QMM_Q5_0: return 32;
+        case QMM_Q6_K: return 256;
         default: return 0;
     }
 }
@@ -250,6 +257,7 @@ size_t qmm_block_bytes(qmm_type t) {
         case QMM_Q8_K: return 292;
         case QMM_Q4_0: return 18;
         case QMM_Q5_0: return 22;
+        case QMM_Q6_K: return 210;
         default: return 0;
     }
 }

@@ -13,7 +13,7 @@
 
 namespace qmm {
 
-enum : int { T_F32 = 0, T_Q8_0 = 1, T_Q4_K = 2, T_Q8_K = 3, T_Q4_0 = 4, T_Q5_0 = 5 };
+enum : int { T_F32 = 0, T_Q8_0 = 1, T_Q4_K = 2, T_Q8_K = 3, T_Q4_0 = 4, T_Q5_0 = 5, T_Q6_K = 6 };
 // weight types of 32-value blocks with one f16 scale and signed codes (paired with Q8_0 activations)
 __host__ __device__ constexpr bool is_b32(int wt) { return wt == T_Q8_0 || wt == T_Q4_0 || wt == T_Q5_0; }
 enum : int { A_INT8 = 0, A_F32 = 1 };
@@ -181,6 +181,14 @@ __device__ __forceinline__ void mma_s8(int d[4], uint32_t a0, uint32_t a1, uint3
         "{%10,%10,%10,%10};"
         : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "r"(0));
+}
+
+// D = A(16x16 s8) * B(16x8 s8), exact int32, C = 0.  Fragments: a0 row g, a1
+// row g + 8, k = 4t..4t+3; b0 k = 4t..4t+3, column g (g = lane / 4, t = lane % 4).
+__device__ __forceinline__ void mma_s8_k16(int d[4], uint32_t a0, uint32_t a1, uint32_t b0) {
+    asm("mma.sync.aligned.m16n8k16.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%5}, {%6}, {%7,%7,%7,%7};"
+        : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
+        : "r"(a0), "r"(a1), "r"(b0), "r"(0));
 }
 
 // D = A(16x32 u8) * B(32x8 s8), exact int32, C = 0

@@ -18,6 +18,7 @@ cudaError_t launch_stream_q8_0(int am, int epi, const StreamPlan& plan, int smem
 cudaError_t launch_stream_q4_k(int am, int epi, const StreamPlan& plan, int smem_max, cudaStream_t s);
 cudaError_t launch_stream_q4_0(int am, int epi, const StreamPlan& plan, int smem_max, cudaStream_t s);
 cudaError_t launch_stream_q5_0(int am, int epi, const StreamPlan& plan, int smem_max, cudaStream_t s);
+cudaError_t launch_stream_q6_k(int am, int epi, const StreamPlan& plan, int smem_max, cudaStream_t s);
 cudaError_t launch_gemv_q8_0(int epi, const GemvPlan& plan, int smem_max, cudaStream_t s);
 cudaError_t launch_gemv_q4_k(int epi, const GemvPlan& plan, int smem_max, cudaStream_t s);
 cudaError_t launch_dmma(int wt, int am, int epi, const DmmaPlan& plan, int smem_max, cudaStream_t s);

@@ -1,4 +1,4 @@
-// qmm_quant.cu -- quantize (Q8_0, Q4_K, Q4_0, Q5_0 weights; Q8_0, Q8_K
+// qmm_quant.cu -- quantize (Q8_0, Q4_K, Q4_0, Q5_0, Q6_K weights; Q8_0, Q8_K
 // activations) and dequantize kernels.
 //
 // "自己量化" section 3 (QTensor::quantize) and section 和下载的 Q8_0 逐字节比
@@ -260,6 +260,86 @@ __global__ void dequant_q4_k_kernel(const uint8_t* __restrict__ q, long long nsu
     }
 }
 
+// Q6_K (paired with Q8K activations; 210 bytes per 256 values): ql[128]
+// holds the codes' low 4 bits, qh[64] their high 2 bits, then 16 int8 group
+// scales and the f16 d.  Value i: half h = i / 128, w = i % 128, quarter
+// q = w / 32, l = w % 32; low bits in nibble q / 2 of ql[64h + 32 (q % 2) + l],
+// high bits in bits 2q..2q+1 of qh[32h + l]; stored code = code + 32.
+// Quantizer (a reading, the signed-max rule per group of 16): the group's
+// value m_j of largest magnitude (the first on ties) gives s_j = m_j / -32;
+// d = max |s_j| / 127; sc_j = roundf(s_j / d) in [-127, 127]; with
+// e_j = f(D) sc_j, code = roundf(x / e_j) in [-32, 31] (0 where e_j = 0).
+__device__ __forceinline__ int q6k_ql_byte(int i) { return 64 * (i >> 7) + 32 * ((i >> 5) & 1) + (i & 31); }
+__device__ __forceinline__ int q6k_ql_shift(int i) { return 4 * ((i >> 6) & 1); }
+__device__ __forceinline__ int q6k_qh_byte(int i) { return 128 + 32 * (i >> 7) + (i & 31); }
+__device__ __forceinline__ int q6k_qh_shift(int i) { return 2 * ((i >> 5) & 3); }
+
+__global__ void quant_q6_k_kernel(const float* __restrict__ x, long long nblocks, long long nb_row, long long K,
+                                  uint8_t* __restrict__ out) {
+    const long long blk = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (blk >= nblocks) return;
+    const long long r = blk / nb_row, b = blk - r * nb_row;
+    const float* src = x + r * K + b * 256;
+    float s[16];
+    float smax = 0.0f;
+    for (int j = 0; j < 16; ++j) {
+        float amax = 0.0f, m = 0.0f;
+        for (int i = 0; i < 16; ++i) {
+            const float v = __ldg(src + 16 * j + i);
+            if (fabsf(v) > amax) amax = fabsf(v), m = v;
+        }
+        s[j] = __fdiv_rn(m, -32.0f);
+        if (fabsf(s[j]) > smax) smax = fabsf(s[j]);
+    }
+    const float d = __fdiv_rn(smax, 127.0f);
+    const uint32_t D = f2h(d);
+    const float fD = h2f(D);
+    uint32_t w[53];  // the block as 16-bit pairs: bytes 0..209 (and one pad half)
+    for (int k = 0; k < 53; ++k) w[k] = 0u;
+    for (int j = 0; j < 16; ++j) {
+        const int sc = d > 0.0f ? (int)fminf(fmaxf(roundf(__fdiv_rn(s[j], d)), -127.0f), 127.0f) : 0;
+        w[(192 + j) >> 2] |= ((uint32_t)sc & 0xFFu) << (8 * ((192 + j) & 3));
+        const float e = __fmul_rn(fD, (float)sc);
+        for (int i = 16 * j; i < 16 * j + 16; ++i) {
+            const int c = e != 0.0f ? (int)fminf(fmaxf(roundf(__fdiv_rn(__ldg(src + i), e)), -32.0f), 31.0f) : 0;
+            const uint32_t u = (uint32_t)(c + 32);
+            const int bl = q6k_ql_byte(i), bh = q6k_qh_byte(i);
+            w[bl >> 2] |= (u & 15u) << (8 * (bl & 3) + q6k_ql_shift(i));
+            w[bh >> 2] |= (u >> 4) << (8 * (bh & 3) + q6k_qh_shift(i));
+        }
+    }
+    w[52] |= D;  // bytes 208, 209
+    uint16_t* o = reinterpret_cast<uint16_t*>(out + blk * 210);  // 2-byte aligned block
+    for (int k = 0; k < 105; ++k) o[k] = (uint16_t)(w[k >> 1] >> (16 * (k & 1)));
+}
+
+// one thread per 32 values (a quarter of a half: one ql nibble plane, one qh bit pair)
+__global__ void dequant_q6_k_kernel(const uint8_t* __restrict__ q, long long nchunks, float* __restrict__ out) {
+    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= nchunks) return;
+    const long long b = i >> 3;
+    const int c = (int)(i & 7), h = c >> 2, qq = c & 3;
+    const uint8_t* blk = q + b * 210;
+    const float fD = h2f((uint32_t)blk[208] | ((uint32_t)blk[209] << 8));
+    const float e0 = __fmul_rn(fD, (float)(int8_t)blk[192 + 8 * h + 2 * qq]);
+    const float e1 = __fmul_rn(fD, (float)(int8_t)blk[192 + 8 * h + 2 * qq + 1]);
+    const uint8_t* ql = blk + 64 * h + 32 * (qq & 1);
+    const uint8_t* qh = blk + 128 + 32 * h;
+    const int sl = 4 * (qq >> 1), shh = 2 * qq;
+    float4* dst = reinterpret_cast<float4*>(out + i * 32);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        float v[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const int l = 4 * k + t;
+            const int code = (int)(((ql[l] >> sl) & 15) | (((qh[l] >> shh) & 3) << 4)) - 32;
+            v[t] = __fmul_rn(l < 16 ? e0 : e1, (float)code);
+        }
+        dst[k] = make_float4(v[0], v[1], v[2], v[3]);
+    }
+}
+
 inline unsigned grid_for(long long n, int block) { return (unsigned)((n + block - 1) / block); }
 
 // y[i] = sum over K slices s = 0..ks-1 of partial[s][i], in slice order.
@@ -299,6 +379,9 @@ cudaError_t launch_quantize(int type, const float* x, long long rows, long long 
     } else if (type == T_Q4_K) {
         const long long nb = K / 256, n = rows * nb;
         quant_q4_k_kernel<<<grid_for(n, bs), bs, 0, s>>>(x, n, nb, K, static_cast<uint8_t*>(out));
+    } else if (type == T_Q6_K) {
+        const long long nb = K / 256, n = rows * nb;
+        quant_q6_k_kernel<<<grid_for(n, bs), bs, 0, s>>>(x, n, nb, K, static_cast<uint8_t*>(out));
     } else if (type == T_Q4_0 || type == T_Q5_0) {
         const long long nb = K / 32, n = rows * nb;
         if (type == T_Q4_0) quant_x_0_kernel<8><<<grid_for(n, bs), bs, 0, s>>>(x, n, nb, K, static_cast<uint8_t*>(out));
@@ -316,6 +399,7 @@ cudaError_t launch_dequantize(int type, const void* q, long long rows, long long
     if (type == T_Q8_0) dequant_q8_0_kernel<<<grid_for(n, bs), bs, 0, s>>>(qb, n, out);
     else if (type == T_Q8_K) dequant_q8_k_kernel<<<grid_for(n, bs), bs, 0, s>>>(qb, n, out);
     else if (type == T_Q4_K) dequant_q4_k_kernel<<<grid_for(n, bs), bs, 0, s>>>(qb, n, out);
+    else if (type == T_Q6_K) dequant_q6_k_kernel<<<grid_for(n, bs), bs, 0, s>>>(qb, n, out);
     else if (type == T_Q4_0) dequant_x_0_kernel<8><<<grid_for(n, bs), bs, 0, s>>>(qb, n, out);
     else if (type == T_Q5_0) dequant_x_0_kernel<16><<<grid_for(n, bs), bs, 0, s>>>(qb, n, out);
     else return cudaErrorInvalidValue;

@@ -4,7 +4,8 @@
 // 16-row weight tiles into a ring of shared-memory stages with 1-D bulk
 // copies (cp.async.bulk, mbarrier completion); CW consumer warps compute on
 // each stage while the next ones are in flight: one warp-level tensor-core
-// product per 32-value block (Q8_0) or sub-block (Q4_K) of 16 rows against 8
+// product per 32-value block (Q8_0, Q4_0, Q5_0), sub-block of 32 (Q4_K) or
+// group of 16 (Q6_K, one k16 MMA) of 16 rows against 8
 // activation rows (int8: mma.m16n8k32.s8, exact int32 block sums) or 4
 // activation rows split into two f16 pieces (f32_act: mma.m16n8k16.f16, f32
 // accumulate).  (Decode int8_act with M <= 8 runs in qmm_gemv.cuh instead.)
@@ -14,7 +15,8 @@
 //     the row-quantized activation codes, then
 //     Q8_0: y += f(d_w) f(d_a) isum;  Q4_K: S_sc = sum_j sc_j isum_j,
 //     S_m = sum_j m_j (sum of sub-block j's activation codes),
-//     y += d_a (f(d) S_sc - f(dmin) S_m).
+//     y += d_a (f(d) S_sc - f(dmin) S_m);  Q6_K: S = sum_j sc_j isum_j over its
+//     16 groups of 16 (signed 6-bit codes), y += d_a f(d) S.
 //   f32_act (Metal form): each activation row is scaled by a power of two and
 //     split into two f16 pieces (x 2^s = hi + lo to 2^-22 relative); weight
 //     codes are exact in f16; y += f(d) sum(q x) (Q8_0) or e_j sum(q x) -
@@ -48,10 +50,16 @@ template <>
 struct Unit<T_Q5_0> {
     static constexpr int vals = 32, bytes = 22, per_stage = 32;
 };
-__host__ __device__ constexpr int unit_vals(int wt) { return wt == T_Q4_K ? 256 : 32; }
+template <>
+struct Unit<T_Q6_K> {
+    static constexpr int vals = 256, bytes = 210, per_stage = 8;
+};
+__host__ __device__ constexpr int unit_vals(int wt) { return wt == T_Q4_K || wt == T_Q6_K ? 256 : 32; }
 __host__ __device__ constexpr int unit_bytes(int wt) {
-    return wt == T_Q4_K ? 144 : wt == T_Q4_0 ? 18 : wt == T_Q5_0 ? 22 : 34;
+    return wt == T_Q4_K ? 144 : wt == T_Q6_K ? 210 : wt == T_Q4_0 ? 18 : wt == T_Q5_0 ? 22 : 34;
 }
+// super-block weight types (paired with Q8K activations)
+__host__ __device__ constexpr bool is_sb(int wt) { return wt == T_Q4_K || wt == T_Q6_K; }
 
 // Signed codes of values 8t..8t+7 of a 32-value weight block (2-byte
 // aligned in shared memory): w0 holds values 8t..8t+3, w1 8t+4..8t+7, one
@@ -118,7 +126,7 @@ __device__ __forceinline__ void prepare_acts(const StreamParams& p, uint8_t* sme
             *d1 = make_uint4(c[4], c[5], c[6], c[7]);
             da[r * p.scale_pitch + b] = s;
         }
-    } else if (AM == A_INT8 && WT == T_Q4_K) {
+    } else if (AM == A_INT8 && is_sb(WT)) {  // Q8K activations (Q4_K also needs the sums of each 32)
         uint8_t* codes = smem + p.off_codes;
         float* da = reinterpret_cast<float*>(smem + p.off_scale);
         int* bs = reinterpret_cast<int*>(smem + p.off_aux);
@@ -145,7 +153,7 @@ __device__ __forceinline__ void prepare_acts(const StreamParams& p, uint8_t* sme
                 uint4* d1 = d0 + 1;
                 *d0 = make_uint4(w[0], w[1], w[2], w[3]);
                 *d1 = make_uint4(w[4], w[5], w[6], w[7]);
-                bs[r * p.aux_pitch + sb * 8 + j] = sum;
+                if (WT == T_Q4_K) bs[r * p.aux_pitch + sb * 8 + j] = sum;
             }
             da[r * p.scale_pitch + sb] = d;
         }
@@ -287,6 +295,94 @@ __device__ __forceinline__ void stage_mma(const StreamParams& p, const uint8_t* 
                     mma_f16(d, A2a0, A2a1, A2a2, A2a3, bb.z, bb.w);
                     acc[nt][0] = fmaf(dw0, d[0] + d[1], acc[nt][0]);
                     acc[nt][1] = fmaf(dw1, d[2] + d[3], acc[nt][1]);
+                }
+            }
+        } else if (WT == T_Q6_K) {
+            // Q6_K super-block: 16 groups of 16 values, one k16 MMA each.  Group
+            // j = 8h + 2q + s holds values 128h + 32q + 16s + l (l < 16); thread t
+            // takes l = 4t..4t+3: one ql word (nibble plane q / 2) and one qh
+            // word (bit pair q) per row.  Blocks are 2-byte aligned: words are
+            // read from the rounded-down start and realigned by a funnel shift.
+            const int o0 = (int)(row0 - smem) + u * 210, o1 = (int)(row1 - smem) + u * 210;
+            const uint8_t* a0p = smem + (o0 & ~3);
+            const uint8_t* a1p = smem + (o1 & ~3);
+            const uint32_t sh0 = (uint32_t)(o0 & 2) * 8u, sh1 = (uint32_t)(o1 & 2) * 8u;
+            auto w0 = [&](int off) { return __funnelshift_r(ld32(a0p + off), ld32(a0p + off + 4), sh0); };
+            auto w1 = [&](int off) { return __funnelshift_r(ld32(a1p + off), ld32(a1p + off + 4), sh1); };
+            const float fD0 = h2f(*reinterpret_cast<const uint16_t*>(smem + o0 + 208));
+            const float fD1 = h2f(*reinterpret_cast<const uint16_t*>(smem + o1 + 208));
+            const int8_t* sc0p = reinterpret_cast<const int8_t*>(smem + o0 + 192);
+            const int8_t* sc1p = reinterpret_cast<const int8_t*>(smem + o1 + 192);
+            int ssc[NT][4];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) ssc[nt][i] = 0;
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int sg = 0; sg < 2; ++sg) {
+                    const int lo = 16 * sg + 4 * t;  // l of this thread's first value
+                    const uint32_t L00 = w0(64 * h + lo), L01 = w0(64 * h + 32 + lo), H0 = w0(128 + 32 * h + lo);
+                    const uint32_t L10 = w1(64 * h + lo), L11 = w1(64 * h + 32 + lo), H1 = w1(128 + 32 * h + lo);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int j = 8 * h + 2 * q + sg;
+                        const int vb = 128 * h + 32 * q + lo;  // value index of this thread's first value
+                        const uint32_t n0 = ((q & 1 ? L01 : L00) >> (4 * (q >> 1))) & 0x0F0F0F0Fu;
+                        const uint32_t n1 = ((q & 1 ? L11 : L10) >> (4 * (q >> 1))) & 0x0F0F0F0Fu;
+                        const uint32_t c0 = __vsub4(n0 | (((H0 >> (2 * q)) & 0x03030303u) << 4), 0x20202020u);
+                        const uint32_t c1 = __vsub4(n1 | (((H1 >> (2 * q)) & 0x03030303u) << 4), 0x20202020u);
+                        if (AM == A_INT8) {
+                            const uint8_t* codes = smem + p.off_codes;
+                            const int s0 = sc0p[j], s1 = sc1p[j];
+#pragma unroll
+                            for (int nt = 0; nt < NT; ++nt) {
+                                const uint32_t bb = ld32(codes + (nt * 8 + g) * p.code_pitch + ur * 256 + vb);
+                                int d[4];
+                                mma_s8_k16(d, c0, c1, bb);
+                                ssc[nt][0] += s0 * d[0];
+                                ssc[nt][1] += s0 * d[1];
+                                ssc[nt][2] += s1 * d[2];
+                                ssc[nt][3] += s1 * d[3];
+                            }
+                        } else {
+                            const uint8_t* pieces = smem + p.off_codes;
+                            const uint32_t a0 = s8x2_to_h2(c0, SEL01), a2 = s8x2_to_h2(c0, SEL23);
+                            const uint32_t a1 = s8x2_to_h2(c1, SEL01), a3 = s8x2_to_h2(c1, SEL23);
+                            const float e0 = __fmul_rn(fD0, (float)sc0p[j]), e1 = __fmul_rn(fD1, (float)sc1p[j]);
+#pragma unroll
+                            for (int nt = 0; nt < NT; ++nt) {
+                                const int prow = 2 * (nt * 4 + (g >> 1)) + (g & 1);
+                                const uint2 bb = ld64(pieces + ((long long)prow * p.code_pitch + ur * 256 + vb) * 2);
+                                float d[4] = {0.f, 0.f, 0.f, 0.f};
+                                mma_f16(d, a0, a1, a2, a3, bb.x, bb.y);
+                                acc[nt][0] = fmaf(e0, d[0] + d[1], acc[nt][0]);
+                                acc[nt][1] = fmaf(e1, d[2] + d[3], acc[nt][1]);
+                            }
+                        }
+                    }
+                }
+            if (AM == A_INT8) {
+                const float* da = reinterpret_cast<const float*>(smem + p.off_scale);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    if (EPI == E_Y) {
+                        const float da0 = da[(nt * 8 + 2 * t) * p.scale_pitch + ur];
+                        const float da1 = da[(nt * 8 + 2 * t + 1) * p.scale_pitch + ur];
+                        acc[nt][0] += da0 * (fD0 * (float)ssc[nt][0]);
+                        acc[nt][1] += da1 * (fD0 * (float)ssc[nt][1]);
+                        acc[nt][2] += da0 * (fD1 * (float)ssc[nt][2]);
+                        acc[nt][3] += da1 * (fD1 * (float)ssc[nt][3]);
+                    } else {
+                        const int n0 = tile * kTileRows + g, n1 = n0 + 8;
+                        const int ma = m0 + nt * 8 + 2 * t, mb = ma + 1;
+                        const long long nsb = p.units, gs = gu0 + u;
+                        if (ma < p.M && n0 < p.N) p.sums[((long long)ma * p.N + n0) * nsb + gs] = ssc[nt][0];
+                        if (mb < p.M && n0 < p.N) p.sums[((long long)mb * p.N + n0) * nsb + gs] = ssc[nt][1];
+                        if (ma < p.M && n1 < p.N) p.sums[((long long)ma * p.N + n1) * nsb + gs] = ssc[nt][2];
+                        if (mb < p.M && n1 < p.N) p.sums[((long long)mb * p.N + n1) * nsb + gs] = ssc[nt][3];
+                    }
                 }
             }
         } else {  // Q4_K super-block
@@ -586,7 +682,7 @@ inline bool plan_stream(int wt, int am, int epi, long long M, long long N, long 
     int nt;
     if (am == A_INT8) nt = M <= 8 ? 1 : M <= 16 ? 2 : M <= 32 ? 4 : 8;
     else nt = M <= 4 ? 1 : M <= 8 ? 2 : M <= 16 ? 4 : 8;
-    if (wt == T_Q4_K && am == A_INT8 && nt > 4) nt = 4;  // register budget of the integer super-block sums
+    if (is_sb(wt) && am == A_INT8 && nt > 4) nt = 4;  // register budget of the integer super-block sums
     const int cw = consumer_warps(wt, am, nt);
     const int mr = chunk_rows(am, nt);
     p.M = (int)M;
@@ -598,7 +694,7 @@ inline bool plan_stream(int wt, int am, int epi, long long M, long long N, long 
     p.rb = (long long)p.units * ub;
     p.total_bytes = p.rb * N;
     p.ntiles = (int)((N + kTileRows - 1) / kTileRows);
-    const int ups_max = wt == T_Q4_K ? Unit<T_Q4_K>::per_stage : Unit<T_Q8_0>::per_stage;
+    const int ups_max = is_sb(wt) ? Unit<T_Q4_K>::per_stage : Unit<T_Q8_0>::per_stage;
     const int red_bytes = cw * kTileRows * mr * 4;
     for (int ks = 1; ks <= p.units; ++ks) {
         const int su = (p.units + ks - 1) / ks;
@@ -616,7 +712,7 @@ inline bool plan_stream(int wt, int am, int epi, long long M, long long N, long 
             code_pitch = kv + 16;
             codes = mr * code_pitch;
             scale_pitch = su;
-            if (wt == T_Q4_K) aux_pitch = su * 8;
+            if (wt == T_Q4_K) aux_pitch = su * 8;  // sums of each 32 activation codes (Q6_K needs none)
         } else {
             code_pitch = kv + 8;  // halves
             codes = mr * 2 * code_pitch * 2;

@@ -54,7 +54,8 @@ typedef enum {
     QMM_Q4_K = 2,   /* 256 values: f16 d/dmin, 6-bit sub-block scales/mins   */
     QMM_Q8_K = 3,   /* 256 values: f32 scale, int8 codes, 16 int16 sums      */
     QMM_Q4_0 = 4,   /* 32 values: f16 scale, 4-bit codes offset by 8 (18 B)  */
-    QMM_Q5_0 = 5    /* 32 values: f16 scale, 5-bit codes offset by 16 (22 B) */
+    QMM_Q5_0 = 5,   /* 32 values: f16 scale, 5-bit codes offset by 16 (22 B) */
+    QMM_Q6_K = 6    /* 256 values: 6-bit codes offset by 32, 16 int8 group scales, f16 d (210 B) */
 } qmm_type;
 
 typedef enum {
@@ -73,15 +74,16 @@ typedef enum {
     QMM_ERR_TIMEOUT = 7     /* a device-side wait gave up (reported by qmm_last_device_error) */
 } qmm_status;
 
-/* Values per block: 32 (Q8_0, Q4_0, Q5_0), 256 (Q4_K, Q8_K), 1 (F32); 0 for an
-   unknown type. */
+/* Values per block: 32 (Q8_0, Q4_0, Q5_0), 256 (Q4_K, Q8_K, Q6_K), 1 (F32); 0
+   for an unknown type. */
 int64_t qmm_block_values(qmm_type t);
 
-/* Bytes per block: 34 (Q8_0), 144 (Q4_K), 292 (Q8_K), 18 (Q4_0), 22 (Q5_0);
-   4 for F32; 0 for an unknown type.  ("自己量化" section 大小和误差 and the
-   byte listings of section 和下载的 Q8_0 逐字节比: the printed sizes fix 34 B
-   per 32 values for Q8_0, 144 B per 256 for Q4K, 22 B per 32 for Q5_0 and
-   18 B per 32 for Q4_0.) */
+/* Bytes per block: 34 (Q8_0), 144 (Q4_K), 292 (Q8_K), 18 (Q4_0), 22 (Q5_0),
+   210 (Q6_K); 4 for F32; 0 for an unknown type.  ("自己量化" section 大小和误差
+   and the byte listings of section 和下载的 Q8_0 逐字节比: the printed sizes fix
+   34 B per 32 values for Q8_0, 144 B per 256 for Q4K, 22 B per 32 for Q5_0,
+   18 B per 32 for Q4_0, and the downloaded Q4_K_M closes with 210 B per 256
+   for Q6K.) */
 size_t qmm_block_bytes(qmm_type t);
 
 /* Bytes of one quantized row of K values; 0 when K is not a multiple of the
@@ -89,7 +91,7 @@ size_t qmm_block_bytes(qmm_type t);
 size_t qmm_row_bytes(qmm_type t, int64_t K);
 
 /* Quantize weights w [N, K] (f32, device) into wq (N * qmm_row_bytes(wtype, K)
-   bytes, device).  wtype: QMM_Q8_0, QMM_Q4_K, QMM_Q4_0 or QMM_Q5_0 ("自己量化"
+   bytes, device).  wtype: QMM_Q8_0, QMM_Q4_K, QMM_Q4_0, QMM_Q5_0 or QMM_Q6_K ("自己量化"
    section 3, QTensor::quantize).  Q8_0: per 32 values d = max|x|/127, codes
    round(x / d) with ties away from zero.  Q4_K: per sub-block of 32 a step
    (max - min(0, min))/15 and offset -min(0, min), super-block scales
@@ -101,7 +103,14 @@ size_t qmm_row_bytes(qmm_type t, int64_t K);
    [0, 2 off - 1]; block = f16 d, (Q5_0) a little-endian 32-bit word whose
    bit i is bit 4 of code i, then 16 bytes with code j in the low nibble of
    byte j and code j + 16 in its high nibble (the public GGUF layout); the
-   weight is f(d) (code - off).  Errors: NULL, SHAPE (K % block), TYPE, ALIGN. */
+   weight is f(d) (code - off).  Q6_K (the pages give only its size): per
+   group of 16 the value m_j of largest magnitude (the first on ties, sign
+   kept) gives s_j = m_j / -32; d = max |s_j| / 127; int8 group scales
+   sc_j = round(s_j / d); codes round(x / (f(d) sc_j)) in [-32, 31], stored
+   +32 as 4 low bits (ql[128]) and 2 high bits (qh[64]): value i = 128h +
+   32q + l has its low bits in nibble q/2 of ql[64h + 32 (q % 2) + l] and its
+   high bits in bits 2q..2q+1 of qh[32h + l]; then the 16 scales and f16 d
+   (the public GGUF layout).  Errors: NULL, SHAPE (K % block), TYPE, ALIGN. */
 qmm_status qmm_quantize_weights(qmm_type wtype, const float* w, int64_t N, int64_t K, void* wq,
                                 qmm_stream_t stream);
 
@@ -117,8 +126,9 @@ qmm_status qmm_quantize_act(qmm_type atype, const float* x, int64_t M, int64_t K
 /* Dequantize rows blocks -> out [rows, K] f32 (the CANDLE_DEQUANTIZE_ALL form,
    "同一个 GGUF…" section 出处).  Q8_0 and Q8_K: f(d) * q; Q4_K:
    (f(d) * sc_j) * q - f(dmin) * m_j, both products exact in f32, one rounding
-   in the subtraction; Q4_0 / Q5_0: f(d) (code - off), exact (bit-exact
-   contract).  t: Q8_0, Q4_K, Q8_K, Q4_0 or Q5_0. */
+   in the subtraction; Q4_0 / Q5_0: f(d) (code - off), exact; Q6_K:
+   (f(d) sc_j) code, exact (bit-exact contract).  t: Q8_0, Q4_K, Q8_K, Q4_0,
+   Q5_0 or Q6_K. */
 qmm_status qmm_dequantize(qmm_type t, const void* q, int64_t rows, int64_t K, float* out,
                           qmm_stream_t stream);
 
@@ -136,14 +146,15 @@ size_t qmm_matmul_workspace(qmm_type wtype, qmm_act_mode mode, int64_t M, int64_
 int qmm_matmul_launches(qmm_type wtype, qmm_act_mode mode, int64_t M, int64_t N, int64_t K);
 
 /* y [M, N] f32 = x [M, K] f32 . W^T with W given as quantized blocks wq
-   (wtype QMM_Q8_0, QMM_Q4_K, QMM_Q4_0 or QMM_Q5_0).
+   (wtype QMM_Q8_0, QMM_Q4_K, QMM_Q4_0, QMM_Q5_0 or QMM_Q6_K).
    mode QMM_INT8_ACT ("同一个 GGUF…" section 出处, the CPU form): each row of x
      is quantized in-kernel to Q8_0 (Q8_0, Q4_0 and Q5_0 weights) or Q8_K
-     (Q4_K weights), per-block int32 dot products of signed codes are formed
-     exactly and combined as
+     (Q4_K and Q6_K weights), per-block int32 dot products of signed codes are
+     formed exactly and combined as
        Q8_0, Q4_0, Q5_0: y = sum_b f(d_w) f(d_a) isum_b
        Q4_K: y = sum_s d_a (f(d) S_sc - f(dmin) S_m),
-             S_sc = sum_j sc_j isum_j, S_m = sum_j m_j (sum of the sub-block's codes).
+             S_sc = sum_j sc_j isum_j, S_m = sum_j m_j (sum of the sub-block's codes)
+       Q6_K: y = sum_s d_a f(d) S, S = sum_j sc_j isum_j over the 16 groups of 16.
    mode QMM_F32_ACT (the Metal form): y = sum_k x_k w_k with w the dequantized
      weights, x kept at f32 accuracy.
    Floats: |y - exact| <= 1e-5 * (sum of |scaled block terms|) + 1e-6.
@@ -159,7 +170,8 @@ qmm_status qmm_matmul(qmm_type wtype, qmm_act_mode mode, const void* wq, const f
    qmm_matmul(QMM_INT8_ACT), written out instead of being scaled.
    x is f32 [M, K].  out (int32, device):
      Q8_0, Q4_0, Q5_0: [M][N][K/32]  isum of each 32-block (signed codes);
-     Q4_K: [M][N][K/256][2]      (S_sc, S_m) of each super-block.
+     Q4_K: [M][N][K/256][2]      (S_sc, S_m) of each super-block;
+     Q6_K: [M][N][K/256]         S of each super-block.
    Bit-exact contract.  Errors as for qmm_matmul (no workspace). */
 qmm_status qmm_block_sums(qmm_type wtype, const void* wq, const float* x, int64_t M, int64_t N, int64_t K,
                           int32_t* out, qmm_stream_t stream);

@@ -39,6 +39,9 @@ def test_block_sizes(qmm):
     assert (qmm.block_values("q8_k"), qmm.block_bytes("q8_k")) == (256, 292)
     assert (qmm.block_values("q4_0"), qmm.block_bytes("q4_0")) == (32, 18)
     assert (qmm.block_values("q5_0"), qmm.block_bytes("q5_0")) == (32, 22)
+    assert (qmm.block_values("q6_k"), qmm.block_bytes("q6_k")) == (256, 210)
+    assert qmm.row_bytes("q6_k", 1536) == 1260    # half of the downloaded file's ffn_down
+    assert qmm.row_bytes("q6_k", 576) == 0        # a K-quant: K % 256
     assert qmm.row_bytes("q5_0", 576) == 396      # the 576-wide SmolLM2 matrices take Q5_0
     assert qmm.row_bytes("q8_0", 576) == 612
     assert qmm.row_bytes("q4_k", 1536) == 864
@@ -48,7 +51,7 @@ def test_block_sizes(qmm):
 
 
 def test_row_bytes_agree_with_oracle(qmm, orc):
-    for t in ("q8_0", "q4_k", "q8_k", "q4_0", "q5_0"):
+    for t in ("q8_0", "q4_k", "q8_k", "q4_0", "q5_0", "q6_k"):
         for K in (256, 512, 4096, 8192):
             assert qmm.row_bytes(t, K) == orc.row_bytes(t, K)
 
@@ -65,6 +68,8 @@ def test_argument_errors_return_before_launch(qmm):
     assert L.qmm_quantize_weights(F32, 16, 4, 256, 16, None) == 3
     assert L.qmm_quantize_act(Q4_K, 16, 4, 256, 16, None) == 3
     assert L.qmm_quantize_act(qmm.QMM_Q5_0, 16, 4, 256, 16, None) == 3   # Q5_0 weights take Q8_0 activations
+    assert L.qmm_quantize_act(qmm.QMM_Q6_K, 16, 4, 256, 16, None) == 3   # Q6_K weights take Q8K activations
+    assert L.qmm_matmul(qmm.QMM_Q6_K, 0, 16, 16, 16, 1, 1, 576, None, 0, None) == 2   # K % 256
     assert L.qmm_matmul(qmm.QMM_Q4_0, 0, 16, 16, 16, 1, 1, 100, None, 0, None) == 2
     assert L.qmm_matmul(Q8_K, 0, 16, 16, 16, 1, 1, 256, None, 0, None) == 3
     assert L.qmm_matmul(Q8_0, 7, 16, 16, 16, 1, 1, 256, None, 0, None) == 3
@@ -103,6 +108,7 @@ def test_batch_argument_errors_return_before_launch(qmm):
         return L.qmm_matmul_batch(wtype, mode, ctypes.cast(arr, ctypes.c_void_p), len(items), None)
 
     assert call(qmm.QMM_Q4_K, 0, [ok]) == 3                  # 32-value block types only
+    assert call(qmm.QMM_Q6_K, 0, [ok]) == 3
     assert call(qmm.QMM_Q8_0, 5, [ok]) == 3
     assert call(qmm.QMM_Q8_0, 0, [ok, D(16, 16, 16, 9, 8, 64)]) == 2      # M > QMM_BATCH_MAX_M
     assert call(qmm.QMM_Q8_0, 0, [ok, D(16, 16, 16, 2, 8, 16384)]) == 2   # M * K > QMM_BATCH_MAX_MK

@@ -50,7 +50,8 @@ def check_device_error(qmm):
 
 WEIGHT_CASES = [("q8_0", 576, 576), ("q8_0", 37, 96), ("q8_0", 61, 608), ("q8_0", 5, 8192),
                 ("q4_k", 576, 1536), ("q4_k", 37, 256), ("q4_k", 19, 8192),
-                ("q4_0", 576, 576), ("q4_0", 37, 96), ("q5_0", 576, 576), ("q5_0", 1536, 576), ("q5_0", 7, 8192)]
+                ("q4_0", 576, 576), ("q4_0", 37, 96), ("q5_0", 576, 576), ("q5_0", 1536, 576), ("q5_0", 7, 8192),
+                ("q6_k", 576, 1536), ("q6_k", 37, 256), ("q6_k", 19, 8192)]
 
 
 @pytest.mark.parametrize("wtype,N,K", WEIGHT_CASES)
@@ -69,7 +70,8 @@ def test_quantize_act_bit_exact(qmm, orc, atype, M, K):
     assert np.array_equal(q, orc.quantize(atype, x))
 
 
-@pytest.mark.parametrize("t,K", [("q8_0", 576), ("q4_k", 1536), ("q8_k", 1024), ("q4_0", 576), ("q5_0", 576)])
+@pytest.mark.parametrize("t,K", [("q8_0", 576), ("q4_k", 1536), ("q8_k", 1024), ("q4_0", 576), ("q5_0", 576),
+                                 ("q6_k", 1536)])
 def test_dequantize_bit_exact(qmm, orc, t, K):
     w = np.concatenate([qmm_synth.weights(40, K), qmm_synth.special_block_rows(K)])
     q = orc.quantize(t, w)
@@ -85,7 +87,7 @@ def test_dequantize_bit_exact(qmm, orc, t, K):
 SUM_CASES = [("q8_0", 1, 33, 576), ("q8_0", 8, 576, 576), ("q8_0", 5, 40, 4096), ("q8_0", 13, 17, 1536),
              ("q8_0", 37, 24, 96), ("q4_k", 1, 33, 1536), ("q4_k", 8, 64, 2048), ("q4_k", 19, 20, 4096),
              ("q4_0", 1, 33, 576), ("q4_0", 13, 40, 1536), ("q5_0", 1, 192, 576), ("q5_0", 8, 33, 576),
-             ("q5_0", 37, 24, 4096)]
+             ("q5_0", 37, 24, 4096), ("q6_k", 1, 33, 1536), ("q6_k", 8, 64, 2048), ("q6_k", 19, 20, 4096)]
 
 
 @pytest.mark.parametrize("wtype,M,N,K", SUM_CASES)
@@ -96,7 +98,7 @@ def test_block_sums_bit_exact(qmm, orc, wtype, M, N, K):
     x[0] = -1.0
     wq = orc.quantize(wtype, w)
     s = host(qmm.block_sums(dev(wq), dev(x), wtype, N=N))
-    xq = orc.quantize("q8_k" if wtype == "q4_k" else "q8_0", x)
+    xq = orc.quantize("q8_k" if wtype in ("q4_k", "q6_k") else "q8_0", x)
     ref = orc.block_sums(wtype, wq, xq, M, N, K)
     assert np.array_equal(s, ref)
     check_device_error(qmm)
@@ -138,6 +140,12 @@ MATMUL_CASES = [
     ("q4_0", 64, 130, 1024),      # prefill on tcgen05 (K % 256 = 0)
     ("q5_0", 256, 200, 1536),
     ("q4_0", 300, 260, 2048),
+    ("q6_k", 1, 576, 1536),       # the downloaded file's Q6K ffn_down, decode batches 1 and 8
+    ("q6_k", 8, 576, 1536),
+    ("q6_k", 3, 37, 8192),        # ragged tile, long rows
+    ("q6_k", 2, 100, 8192),
+    ("q6_k", 37, 64, 4096),       # prefill, ragged M
+    ("q6_k", 200, 130, 1024),
     ("q4_k", 8, 40, 65536),       # long rows: activations split over K, 256 raw stages
     ("q8_0", 24, 24, 65536),
 ]
@@ -221,7 +229,7 @@ def test_batch_rows_are_independent(qmm, orc):
 
 def test_one_hot_f32_act_is_exact(qmm, orc):
     """x = e_k: the Metal form returns column k of the dequantized weights."""
-    for wtype, K in (("q8_0", 576), ("q4_k", 1536)):
+    for wtype, K in (("q8_0", 576), ("q4_k", 1536), ("q6_k", 1536)):
         wq = orc.quantize(wtype, qmm_synth.weights(64, K))
         W = orc.dequantize(wtype, wq, K)
         x = np.zeros((4, K), np.float32)
@@ -232,7 +240,8 @@ def test_one_hot_f32_act_is_exact(qmm, orc):
             assert np.array_equal(y[i], W[:, k])
 
 
-@pytest.mark.parametrize("wtype,M,N,K", [("q8_0", 64, 300, 4096), ("q4_k", 37, 256, 2048), ("q5_0", 16, 96, 576)])
+@pytest.mark.parametrize("wtype,M,N,K", [("q8_0", 64, 300, 4096), ("q4_k", 37, 256, 2048), ("q5_0", 16, 96, 576),
+                                         ("q6_k", 8, 100, 1536)])
 def test_dequantize_all_form_matches_f32_act(qmm, orc, wtype, M, N, K):
     """The dequantize-all serving form (the weights dequantized once by the
     library, then a dense f32 GEMM with TF32 off) has the f32_act definition:
@@ -265,6 +274,8 @@ def test_launch_counts(qmm):
     assert qmm.matmul_launches("q5_0", "int8_act", 1, 576, 576) == 1      # Q4_0 / Q5_0: the streaming kernel
     assert qmm.matmul_launches("q4_0", "f32_act", 64, 4096, 4096) == 2     # prefill, K % 256 = 0: tcgen05
     assert qmm.matmul_launches("q5_0", "int8_act", 64, 576, 576) == 1     # K = 576: the streaming kernel
+    assert qmm.matmul_launches("q6_k", "int8_act", 1, 576, 1536) == 1     # Q6_K: the streaming kernel
+    assert qmm.matmul_launches("q6_k", "f32_act", 256, 4096, 4096) == 1
 
 
 def test_error_statuses_on_device(qmm, orc):
