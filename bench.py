@@ -255,6 +255,37 @@ def make_buffers(q, torch, wtype: str, seed0: int):
     return out
 
 
+def next_types(q, torch, stream, K=K_DEC, N=N_DEC, Ms=(1, 8), reps=10):
+    """The weight types beyond the headline pair (Q4_0, Q5_0, Q6_K) on the
+    decode shape, both forms: weight GB/s over reps calls rotating two buffers
+    of each type (each buffer larger than half of L2; the pair exceeds it)."""
+    out = {}
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for t in ("q4_0", "q5_0", "q6_k"):
+        bufs = []
+        for b in range(2):
+            g = torch.Generator(device="cuda").manual_seed(500 + b)
+            bufs.append(q.quantize_weights(torch.randn((N, K), generator=g, device="cuda") * 0.02, t))
+        for M in Ms:
+            x = torch.from_numpy(qmm_synth.activations(M, K)).cuda()
+            y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+            for mode in MODES:
+                ws = torch.empty(max(q.matmul_workspace(t, mode, M, N, K), 16), dtype=torch.uint8, device="cuda")
+                for i in range(4):
+                    q.matmul(bufs[i % 2], x, t, mode, N=N, out=y, workspace=ws)
+                torch.cuda.synchronize()
+                ev0.record(stream)
+                for i in range(reps):
+                    q.matmul(bufs[i % 2], x, t, mode, N=N, out=y, workspace=ws)
+                ev1.record(stream)
+                torch.cuda.synchronize()
+                us = ev0.elapsed_time(ev1) / reps * 1e3
+                out[f"{t}/{mode}/M{M}/{N}x{K}"] = {"us_per_call": round(us, 1),
+                                                   "weight_GBps": round(bufs[0].numel() / (us * 1e3), 1)}
+        del bufs
+    return out
+
+
 def small_configs(q, torch, stream):
     """Latency-bound configurations: one Q8_0 GEMV 576x576 (M=1), the Q4_K
     576x1536 GEMV (M = 1, 2, 4, 8), and the 211-matmul SmolLM2-135M-shaped
@@ -541,6 +572,7 @@ def run_ours(args):
                 del wq
 
     small = small_configs(q, torch, stream) if not args.no_small else {}
+    nxt = next_types(q, torch, stream) if not args.no_small else {}
 
     # oracle on the host cores, bounded sample (rank 0, N = 1 only)
     cpu = None
@@ -571,7 +603,7 @@ def run_ours(args):
                 "e2e": {"value": round(e2e, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                         "d2h_bytes_per_step": d2h},
                 "gpu_launches": launches * args.steps,
-                "clocks": ck, "sweep_GBps": sweep, "prefill": prefill, "small_configs": small}
+                "clocks": ck, "sweep_GBps": sweep, "prefill": prefill, "small_configs": small, "next_types": nxt}
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

@@ -694,65 +694,76 @@ inline bool plan_stream(int wt, int am, int epi, long long M, long long N, long 
     p.rb = (long long)p.units * ub;
     p.total_bytes = p.rb * N;
     p.ntiles = (int)((N + kTileRows - 1) / kTileRows);
-    const int ups_max = is_sb(wt) ? Unit<T_Q4_K>::per_stage : Unit<T_Q8_0>::per_stage;
+    // Units per stage: a row's chunk is one bulk copy, and the copy engine pays a
+    // fixed cost per segment, so chunks are as long as three stages allow.  An
+    // unsplit K comes first (a K split adds partial sums and a reduction): the
+    // first K split, in increasing order, with a candidate chunk that leaves
+    // three stages wins; the largest such chunk is taken.
+    const int cand_b32[4] = {128, 96, 64, 32}, cand_sb[3] = {16, 12, 8};
+    const int* cand = is_sb(wt) ? cand_sb : cand_b32;
+    const int ncand = is_sb(wt) ? 3 : 4;
     const int red_bytes = cw * kTileRows * mr * 4;
-    for (int ks = 1; ks <= p.units; ++ks) {
+    for (int ks = 1; ks <= p.units && p.kslices == 0; ++ks) {
         const int su = (p.units + ks - 1) / ks;
         if ((long long)(ks - 1) * su >= p.units) continue;  // empty last slice
-        const int ups = su < ups_max ? su : ups_max;
-        // row pitch in a stage: room for the 16-byte superset; the remainder
-        // mod 128 spreads the rows of one access over the banks
-        const int want = 16;
-        int row_stride = round_up(ups * ub + 32, 16);
-        row_stride += ((want - row_stride % 128) + 128) % 128;
-        const int stage_bytes = kTileRows * row_stride;
-        const int kv = su * uv;  // values per slice
-        int codes, scale_pitch = 0, aux_pitch = 0, code_pitch;
-        if (am == A_INT8) {
-            code_pitch = kv + 16;
-            codes = mr * code_pitch;
-            scale_pitch = su;
-            if (wt == T_Q4_K) aux_pitch = su * 8;  // sums of each 32 activation codes (Q6_K needs none)
-        } else {
-            code_pitch = kv + 8;  // halves
-            codes = mr * 2 * code_pitch * 2;
-            if (wt == T_Q4_K) aux_pitch = kv / 32;
+        int prev = 0;
+        for (int ci = 0; ci < ncand && p.kslices == 0; ++ci) {
+            const int ups = su < cand[ci] ? su : cand[ci];
+            if (ups == prev) continue;
+            prev = ups;
+            // row pitch in a stage: room for the 16-byte superset; the remainder
+            // mod 128 spreads the rows of one access over the banks
+            const int want = 16;
+            int row_stride = round_up(ups * ub + 32, 16);
+            row_stride += ((want - row_stride % 128) + 128) % 128;
+            const int stage_bytes = kTileRows * row_stride;
+            const int kv = su * uv;  // values per slice
+            int codes, scale_pitch = 0, aux_pitch = 0, code_pitch;
+            if (am == A_INT8) {
+                code_pitch = kv + 16;
+                codes = mr * code_pitch;
+                scale_pitch = su;
+                if (wt == T_Q4_K) aux_pitch = su * 8;  // sums of each 32 activation codes (Q6_K needs none)
+            } else {
+                code_pitch = kv + 8;  // halves
+                codes = mr * 2 * code_pitch * 2;
+                if (wt == T_Q4_K) aux_pitch = kv / 32;
+            }
+            int off = round_up(2 * 8 * 8, 128);  // up to 8 stages x 2 barriers
+            const int off_flags = off;
+            off += 128;
+            const int off_codes = off;
+            off = round_up(off + codes, 128);
+            const int off_scale = off;
+            off = round_up(off + mr * scale_pitch * 4, 128);
+            const int off_aux = off;
+            off = round_up(off + mr * aux_pitch * 4, 128);
+            const int off_rs = off;
+            off = round_up(off + mr * 2 * 4, 128);
+            const int off_red = off;
+            off = round_up(off + red_bytes, 128);
+            const int off_stage = off;
+            int stages = (smem_max - off) / stage_bytes;
+            if (stages > 8) stages = 8;
+            if (stages < 3 && !(ks == p.units && ci == ncand - 1)) continue;  // a shorter chunk, else a split
+            if (stages < 2) return false;
+            p.kslices = ks;
+            p.slice_units = su;
+            p.ups = ups;
+            p.row_stride = row_stride;
+            p.stages = stages;
+            p.code_pitch = code_pitch;
+            p.scale_pitch = scale_pitch;
+            p.aux_pitch = aux_pitch;
+            p.off_flags = off_flags;
+            p.off_codes = off_codes;
+            p.off_scale = off_scale;
+            p.off_aux = off_aux;
+            p.off_rs = off_rs;
+            p.off_red = off_red;
+            p.off_stage = off_stage;
+            pl.smem = (size_t)off_stage + (size_t)stages * stage_bytes;
         }
-        int off = round_up(2 * 8 * 8, 128);  // up to 8 stages x 2 barriers
-        const int off_flags = off;
-        off += 128;
-        const int off_codes = off;
-        off = round_up(off + codes, 128);
-        const int off_scale = off;
-        off = round_up(off + mr * scale_pitch * 4, 128);
-        const int off_aux = off;
-        off = round_up(off + mr * aux_pitch * 4, 128);
-        const int off_rs = off;
-        off = round_up(off + mr * 2 * 4, 128);
-        const int off_red = off;
-        off = round_up(off + red_bytes, 128);
-        const int off_stage = off;
-        int stages = (smem_max - off) / stage_bytes;
-        if (stages > 8) stages = 8;
-        if (stages < 3 && ks < p.units) continue;
-        if (stages < 2) return false;
-        p.kslices = ks;
-        p.slice_units = su;
-        p.ups = ups;
-        p.row_stride = row_stride;
-        p.stages = stages;
-        p.code_pitch = code_pitch;
-        p.scale_pitch = scale_pitch;
-        p.aux_pitch = aux_pitch;
-        p.off_flags = off_flags;
-        p.off_codes = off_codes;
-        p.off_scale = off_scale;
-        p.off_aux = off_aux;
-        p.off_rs = off_rs;
-        p.off_red = off_red;
-        p.off_stage = off_stage;
-        pl.smem = (size_t)off_stage + (size_t)stages * stage_bytes;
-        break;
     }
     if (p.kslices == 0) return false;
     p.pairs = p.kslices * p.mchunks;
