@@ -301,7 +301,7 @@ def test_error_statuses_on_device(qmm, orc):
 # checked on sampled output rows
 # ---------------------------------------------------------------------------
 
-FULL = [("q4_k", 28672, 8192, 8), ("q8_0", 28672, 8192, 8), ("q8_0", 14336, 4096, 1024),
+FULL = [("q4_k", 28672, 8192, 8), ("q8_0", 28672, 8192, 8), ("q6_k", 28672, 8192, 8), ("q8_0", 14336, 4096, 1024),
         ("q4_k", 14336, 4096, 1024), ("q8_0", 14336, 4096, 256), ("q4_k", 4096, 4096, 256),
         ("q8_0", 4096, 4096, 16), ("q8_0", 49152, 576, 1), ("q5_0", 14336, 4096, 256), ("q5_0", 49152, 576, 1)]
 
@@ -369,6 +369,32 @@ def test_matmul_batch_items_within_bound(qmm, orc, wtype, mode):
     qmm.matmul_batch(items, wtype, mode)
     for (wq, x, y), (y_orc, T), s in zip(items, ref, shapes):
         assert_within_bound(host(y), y_orc, T, f"batch {wtype} {mode} {s}")
+    check_device_error(qmm)
+
+
+@pytest.mark.parametrize("mode", ["int8_act", "f32_act"])
+def test_matmul_batch_many_items_empty_items_and_largest_rows(qmm, orc, mode):
+    """More items than one launch takes (300: two launches of <= 256), empty
+    items (M = 0 or N = 0) among them, and items at the largest M x K
+    (8 x 2048 and 1 x 16384, where f32_act fits only two ring slots)."""
+    shapes = []
+    for i in range(300):
+        shapes.append([(1, 3 + i % 7, 32 * (1 + i % 5)), (0, 8, 64), (2, 0, 64)][0 if i % 50 else 1 + (i // 50) % 2])
+    shapes[17] = (8, 40, 2048)
+    shapes[260] = (1, 50, 16384)
+    items, ref = [], []
+    for i, (M, N, K) in enumerate(shapes):
+        w = qmm_synth.weights(max(N, 1), K, seed=300 + i)[:N]
+        x = qmm_synth.activations(M, K, seed=700 + i) if M else np.zeros((0, K), np.float32)
+        wq = orc.quantize("q8_0", w) if N else np.zeros((0, K // 32 * 34), np.uint8)
+        y = torch.full((M, N), float("nan"), device="cuda")
+        items.append((dev(wq) if N else torch.empty(16, dtype=torch.uint8, device="cuda"),
+                      dev(x) if M else torch.empty((0, K), device="cuda"), y))
+        ref.append(orc.matmul("q8_0", mode, wq, x) if M and N else None)
+    qmm.matmul_batch(items, "q8_0", mode)
+    for (_, _, y), r, sh in zip(items, ref, shapes):
+        if r is not None:
+            assert_within_bound(host(y), r[0], r[1], f"batch item {sh}")
     check_device_error(qmm)
 
 
