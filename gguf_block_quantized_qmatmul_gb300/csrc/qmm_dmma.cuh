@@ -214,7 +214,7 @@ __device__ __forceinline__ void prep_f32_q4_k(const float* src, int r, int sb, i
 
 // Items are per thread for int8 Q8_0 and per warp otherwise.
 template <int WT, int AM>
-__host__ __device__ constexpr bool prep_per_warp() { return !(AM == A_INT8 && WT == T_Q8_0); }
+__host__ __device__ constexpr bool prep_per_warp() { return !(AM == A_INT8 && is_b32(WT)); }
 
 // The work items of rows 0..M-1 over units u0..u0+nu-1 of x, written at unit
 // index 0 of `o`; item indices first, first+step, ...
@@ -223,7 +223,7 @@ __device__ __forceinline__ void prep_items(const float* x, int M, int K, int u0,
                                            long long first, long long step, int lane) {
     constexpr int UV = Unit<WT>::vals;
     const long long k0 = (long long)u0 * UV;
-    if (AM == A_INT8 && WT == T_Q8_0) {
+    if (AM == A_INT8 && is_b32(WT)) {  // Q8_0 activations (Q8_0, Q4_0, Q5_0 weights)
         for (long long i = first; i < (long long)M * nu; i += step) {
             const int r = (int)(i / nu), b = (int)(i - (long long)r * nu);
             prep_i8_q8_0(x + (long long)r * K + k0 + b * 32, r, b, o);
@@ -233,7 +233,7 @@ __device__ __forceinline__ void prep_items(const float* x, int M, int K, int u0,
             const int r = (int)(i / nu), sb = (int)(i - (long long)r * nu);
             prep_i8_q8k(x + (long long)r * K + k0 + sb * 256, r, sb, lane, o);
         }
-    } else if (WT == T_Q8_0) {
+    } else if (is_b32(WT)) {
         const int ng = (nu + 7) / 8;
         for (long long i = first; i < (long long)M * ng; i += step) {
             const int r = (int)(i / ng), gi = (int)(i - (long long)r * ng);
@@ -511,12 +511,17 @@ __global__ void __launch_bounds__(kDmmaThreads, 1) qmm_dmma_kernel(const DmmaPar
                 const uint8_t* r0p = rowptr(g8);
                 const int dr = (int)(rowptr(g8 + 8) - r0p);  // row g8+8 relative to row g8 (a multiple of 16)
                 const int u0 = cu0 - su0 + warp;              // first unit of this warp (slice-relative)
-                if (WT == T_Q8_0) {
-                    // The warp's blocks are 16 apart (544 bytes): their code bytes share one 4-byte alignment.
-                    const uint8_t* q0 = r0p + 34 * warp;
-                    const uintptr_t a = reinterpret_cast<uintptr_t>(q0 + 2);
+                if (is_b32(WT)) {
+                    // The warp's blocks are 16 apart (16 x 34, 18 or 22 bytes, a multiple of
+                    // 4): their payload bytes share one 4-byte alignment.
+                    constexpr int QOFF = WT == T_Q5_0 ? 6 : 2;  // codes (Q8_0) or nibble bytes after d (and qh)
+                    const uint8_t* q0 = r0p + UB * warp;
+                    const uintptr_t a = reinterpret_cast<uintptr_t>(q0 + QOFF);
                     const uint32_t sh = (uint32_t)(a & 3u) * 8u;
                     const uint32_t* w0p = reinterpret_cast<const uint32_t*>(a & ~uintptr_t(3)) + t4;
+                    const uintptr_t ah = reinterpret_cast<uintptr_t>(q0 + 2);  // Q5_0: the word of fifth bits
+                    const uint32_t shh = (uint32_t)(ah & 3u) * 8u;
+                    const uint32_t* h0p = reinterpret_cast<const uint32_t*>(ah & ~uintptr_t(3));
                     const uint16_t* s0p = reinterpret_cast<const uint16_t*>(q0);
                     const uint8_t* xp[NB];
 #pragma unroll
@@ -528,15 +533,34 @@ __global__ void __launch_bounds__(kDmmaThreads, 1) qmm_dmma_kernel(const DmmaPar
 #pragma unroll 2
                     for (int uu = warp; uu < cnu; uu += kDmmaWarps, u += kDmmaWarps) {
                         const uint32_t* w1p = reinterpret_cast<const uint32_t*>(reinterpret_cast<const uint8_t*>(w0p) + dr);
-                        const uint32_t x0 = w0p[0], x1 = w0p[1], x4 = w0p[4], x5 = w0p[5];
-                        const uint32_t y0 = w1p[0], y1 = w1p[1], y4 = w1p[4], y5 = w1p[5];
                         const float dw0 = h2f(s0p[0]);
                         const float dw1 = h2f(*reinterpret_cast<const uint16_t*>(reinterpret_cast<const uint8_t*>(s0p) + dr));
-                        const uint32_t lo0 = __funnelshift_r(x0, x1, sh), hi0 = __funnelshift_r(x4, x5, sh);
-                        const uint32_t lo1 = __funnelshift_r(y0, y1, sh), hi1 = __funnelshift_r(y4, y5, sh);
+                        // signed codes of values 4 t4 .. 4 t4 + 3 (lo) and 16 + 4 t4 .. (hi), rows g8 and g8 + 8
+                        uint32_t lo0, hi0, lo1, hi1;
+                        if (WT == T_Q8_0) {
+                            lo0 = __funnelshift_r(w0p[0], w0p[1], sh), hi0 = __funnelshift_r(w0p[4], w0p[5], sh);
+                            lo1 = __funnelshift_r(w1p[0], w1p[1], sh), hi1 = __funnelshift_r(w1p[4], w1p[5], sh);
+                        } else {
+                            // nibble bytes 4 t4 .. 4 t4 + 3 hold both: values 4 t4 + i in the low
+                            // nibbles, 16 + 4 t4 + i in the high nibbles
+                            const uint32_t n0 = __funnelshift_r(w0p[0], w0p[1], sh), n1 = __funnelshift_r(w1p[0], w1p[1], sh);
+                            uint32_t l0 = n0 & 0x0F0F0F0Fu, h0 = (n0 >> 4) & 0x0F0F0F0Fu;
+                            uint32_t l1 = n1 & 0x0F0F0F0Fu, h1 = (n1 >> 4) & 0x0F0F0F0Fu;
+                            if (WT == T_Q5_0) {
+                                const uint32_t* h1p = reinterpret_cast<const uint32_t*>(reinterpret_cast<const uint8_t*>(h0p) + dr);
+                                const uint32_t f0 = __funnelshift_r(h0p[0], h0p[1], shh), f1 = __funnelshift_r(h1p[0], h1p[1], shh);
+                                // bit i of the word is bit 4 of code i: four bits to bit 4 of four bytes
+                                l0 |= ((((f0 >> (4 * t4)) & 0xFu) * 0x00204081u) & 0x01010101u) << 4;
+                                h0 |= ((((f0 >> (16 + 4 * t4)) & 0xFu) * 0x00204081u) & 0x01010101u) << 4;
+                                l1 |= ((((f1 >> (4 * t4)) & 0xFu) * 0x00204081u) & 0x01010101u) << 4;
+                                h1 |= ((((f1 >> (16 + 4 * t4)) & 0xFu) * 0x00204081u) & 0x01010101u) << 4;
+                            }
+                            constexpr uint32_t OFF = WT == T_Q5_0 ? 0x10101010u : 0x08080808u;
+                            lo0 = __vsub4(l0, OFF), hi0 = __vsub4(h0, OFF), lo1 = __vsub4(l1, OFF), hi1 = __vsub4(h1, OFF);
+                        }
                         if (AM == A_F32) {
-                            const uint32_t lo0s = __funnelshift_r(x0, x1, sh + 8), hi0s = __funnelshift_r(x4, x5, sh + 8);
-                            const uint32_t lo1s = __funnelshift_r(y0, y1, sh + 8), hi1s = __funnelshift_r(y4, y5, sh + 8);
+                            const uint32_t lo0s = lo0 >> 8, hi0s = hi0 >> 8;  // codes 1 and 3 in bytes 0 and 2
+                            const uint32_t lo1s = lo1 >> 8, hi1s = hi1 >> 8;
                             const uint32_t a0 = s8_02_h2(lo0, kM00FF, k6480), a1 = s8_02_h2(lo1, kM00FF, k6480);
                             const uint32_t a2 = s8_02_h2(lo0s, kM00FF, k6480), a3 = s8_02_h2(lo1s, kM00FF, k6480);
                             const uint32_t c0 = s8_02_h2(hi0, kM00FF, k6480), c1 = s8_02_h2(hi1, kM00FF, k6480);
@@ -574,8 +598,9 @@ __global__ void __launch_bounds__(kDmmaThreads, 1) qmm_dmma_kernel(const DmmaPar
                                 }
                             }
                         }
-                        w0p += kDmmaWarps * 34 / 4;
-                        s0p += kDmmaWarps * 34 / 2;
+                        w0p += kDmmaWarps * UB / 4;
+                        h0p += kDmmaWarps * UB / 4;
+                        s0p += kDmmaWarps * UB / 2;
                     }
                 } else {
                     const uint8_t* h0p = r0p + 144 * warp;
@@ -747,7 +772,7 @@ constexpr int kDmmaPreferStages = 2;
 inline bool dmma_layout(int wt, int am, long long M, int nb, int ks, int ups, int smem_max, DmmaPlan& pl,
                         int min_stages = 2) {
     DmmaParams& p = pl.p;
-    const int uv = wt == T_Q8_0 ? 32 : 256, ub = wt == T_Q8_0 ? 34 : 144;
+    const int uv = is_b32(wt) ? 32 : 256, ub = unit_bytes(wt);
     const int su = (p.units + ks - 1) / ks;
     if ((long long)(ks - 1) * su >= p.units) return false;
     if (ups > su) ups = su;
@@ -784,7 +809,7 @@ inline bool dmma_layout(int wt, int am, long long M, int nb, int ks, int ups, in
     } else {
         // Q8_0 word loads reach 18 bytes past the chunk (2-byte offset
         // rounding and the 9th word); a copy starts up to 15 bytes early
-        p.row_pitch = pitch_mod(ups * ub + (wt == T_Q8_0 ? 32 : 0), 16);
+        p.row_pitch = pitch_mod(ups * ub + (is_b32(wt) ? 32 : 0), 16);
         sb = 16LL * p.row_pitch;
     }
     sb = (sb + 127) / 128 * 128;
@@ -804,7 +829,7 @@ inline bool plan_dmma(int wt, int am, long long M, long long N, long long K, int
     if (M < 1 || M > 8) return false;
     DmmaPlan pl{};
     DmmaParams& p = pl.p;
-    const int uv = wt == T_Q8_0 ? 32 : 256, ub = wt == T_Q8_0 ? 34 : 144;
+    const int uv = is_b32(wt) ? 32 : 256, ub = unit_bytes(wt);
     p.M = (int)M;
     p.N = (int)N;
     p.K = (int)K;
@@ -818,9 +843,11 @@ inline bool plan_dmma(int wt, int am, long long M, long long N, long long K, int
     // >= 96 Q8_0 blocks (32 super-blocks; a shorter K as one chunk, unsplit),
     // chunks that divide the slice first (the 16 warps of a stage stay busy);
     // the second tier allows smaller chunks, again with the fewest slices.
-    const int cq[5] = {128, 112, 96, 80, 64}, ck[2] = {32, 16};
-    const int* cand = wt == T_Q8_0 ? cq : ck;
-    const int nbig = wt == T_Q8_0 ? 3 : 1, ncand = wt == T_Q8_0 ? 5 : 2;
+    // (Q4_0 and Q5_0 blocks are shorter: their chunks hold more blocks for about the same bytes)
+    const int cq[5] = {128, 112, 96, 80, 64}, c4[5] = {256, 224, 192, 160, 128}, c5[5] = {256, 192, 128, 96, 64},
+              ck[2] = {32, 16};
+    const int* cand = wt == T_Q8_0 ? cq : wt == T_Q4_0 ? c4 : wt == T_Q5_0 ? c5 : ck;
+    const int nbig = is_b32(wt) ? 3 : 1, ncand = is_b32(wt) ? 5 : 2;
     const int minbig = cand[nbig - 1];
     bool found = false;
     for (int minst = kDmmaPreferStages; minst >= 2 && !found; --minst)

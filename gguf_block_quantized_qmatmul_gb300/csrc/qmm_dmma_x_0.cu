@@ -1,0 +1,48 @@
+// qmm_dmma_x_0.cu -- instantiations of the decode MMA kernel (16-row weight
+// tiles) for Q4_0 and Q5_0 weights, and their launcher.  The kernel unpacks
+// their nibbles (and Q5_0's fifth bits) into the same signed-code fragments
+// as Q8_0; activations are prepared as for Q8_0.
+#include "qmm_internal.h"
+
+namespace qmm {
+namespace {
+unsigned long long g_smem_done[2][2][2][2];  // [Q4_0, Q5_0][form][column sets - 1][epilogue]
+
+template <int WT, int AM, int NB, int EPI>
+cudaError_t go(const DmmaPlan& pl, int smem_max, cudaStream_t s) {
+    auto* k = qmm_dmma_kernel<WT, AM, NB, EPI>;
+    cudaError_t e = ensure_smem(k, smem_max, g_smem_done[WT == T_Q4_0 ? 0 : 1][AM][NB - 1][EPI]);
+    if (e != cudaSuccess) return e;
+    if (!pl.p.ext) {
+        k<<<pl.grid, kDmmaThreads, pl.smem, s>>>(pl.p);
+        return cudaGetLastError();
+    }
+    // after the preparing kernel: programmatic dependent launch
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)pl.grid);
+    cfg.blockDim = dim3(kDmmaThreads);
+    cfg.dynamicSmemBytes = pl.smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k, pl.p);
+}
+
+template <int WT>
+cudaError_t go_type(int am, int epi, const DmmaPlan& pl, int smem_max, cudaStream_t s) {
+    if (am == A_F32) {
+        if (epi != E_Y) return cudaErrorInvalidValue;
+        return pl.nb == 2 ? go<WT, A_F32, 2, E_Y>(pl, smem_max, s) : go<WT, A_F32, 1, E_Y>(pl, smem_max, s);
+    }
+    return epi == E_Y ? go<WT, A_INT8, 1, E_Y>(pl, smem_max, s) : go<WT, A_INT8, 1, E_SUMS>(pl, smem_max, s);
+}
+}  // namespace
+
+cudaError_t launch_dmma_x_0(int wt, int am, int epi, const DmmaPlan& pl, int smem_max, cudaStream_t s) {
+    return wt == T_Q4_0 ? go_type<T_Q4_0>(am, epi, pl, smem_max, s) : go_type<T_Q5_0>(am, epi, pl, smem_max, s);
+}
+
+}  // namespace qmm
