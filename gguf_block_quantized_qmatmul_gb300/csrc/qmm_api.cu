@@ -97,7 +97,7 @@ void plan_dispatch(int wt, int am, int epi, long long M, long long N, long long 
     if (wt == T_Q4_0 || wt == T_Q5_0 || wt == T_Q6_K) {
         // Q4_0 / Q5_0: decode on 16-row tensor-core tiles, prefill on the tcgen05 GEMM
         // where K allows; everything else (and every Q6_K call) on the streaming kernel
-        if (wt != T_Q6_K && M <= kDecodeMaxM && plan_dmma(wt, am, M, N, K, sms, smem, d.dp, epi == E_Y)) {
+        if (wt != T_Q6_K && M <= kDmmaMaxM && plan_dmma(wt, am, M, N, K, sms, smem, d.dp, epi == E_Y)) {
             d.kind = KIND_DMMA;
             d.workspace = d.dp.workspace;
             d.launches = 1 + (d.dp.ext_bytes ? 1 : 0) + (epi == E_Y && d.dp.p.kslices > 1 ? 1 : 0);
@@ -115,7 +115,7 @@ void plan_dispatch(int wt, int am, int epi, long long M, long long N, long long 
     if (am == A_INT8 && wt == T_Q8_0 && M <= kGemvMaxM && plan_gemv(wt, M, N, K, sms, smem, d.gp)) {  // decode: whole-row weight stream
         d.kind = KIND_GEMV;
         d.launches = 1;
-    } else if (M <= kDecodeMaxM && plan_dmma(wt, am, M, N, K, sms, smem, d.dp, epi == E_Y)) {  // decode on 16-row tensor-core tiles
+    } else if (M <= kDmmaMaxM && plan_dmma(wt, am, M, N, K, sms, smem, d.dp, epi == E_Y)) {  // decode and small prefill on 16-row warp-MMA tiles
         d.kind = KIND_DMMA;
         d.workspace = d.dp.workspace;
         d.launches = 1 + (d.dp.ext_bytes ? 1 : 0) + (epi == E_Y && d.dp.p.kslices > 1 ? 1 : 0);

@@ -4,12 +4,12 @@
 
 namespace qmm {
 namespace {
-unsigned long long g_smem_done[2][2][2][2];  // [Q8_0, Q4_K][form][column sets - 1][epilogue]
+unsigned long long g_smem_done[2][2][4][2];  // [Q8_0, Q4_K][form][column sets 1, 2, 4][epilogue]
 
 template <int WT, int AM, int NB, int EPI>
 cudaError_t go(const DmmaPlan& pl, int smem_max, cudaStream_t s) {
     auto* k = qmm_dmma_kernel<WT, AM, NB, EPI>;
-    cudaError_t e = ensure_smem(k, smem_max, g_smem_done[WT == T_Q8_0 ? 0 : 1][AM][NB - 1][EPI]);
+    cudaError_t e = ensure_smem(k, smem_max, g_smem_done[WT == T_Q8_0 ? 0 : 1][AM][NB == 4 ? 2 : NB - 1][EPI]);
     if (e != cudaSuccess) return e;
     if (!pl.p.ext) {
         k<<<pl.grid, kDmmaThreads, pl.smem, s>>>(pl.p);
@@ -34,8 +34,12 @@ template <int WT>
 cudaError_t go_type(int am, int epi, const DmmaPlan& pl, int smem_max, cudaStream_t s) {
     if (am == A_F32) {
         if (epi != E_Y) return cudaErrorInvalidValue;
-        return pl.nb == 2 ? go<WT, A_F32, 2, E_Y>(pl, smem_max, s) : go<WT, A_F32, 1, E_Y>(pl, smem_max, s);
+        return pl.nb == 4   ? go<WT, A_F32, 4, E_Y>(pl, smem_max, s)
+               : pl.nb == 2 ? go<WT, A_F32, 2, E_Y>(pl, smem_max, s)
+                            : go<WT, A_F32, 1, E_Y>(pl, smem_max, s);
     }
+    if (pl.nb == 2)
+        return epi == E_Y ? go<WT, A_INT8, 2, E_Y>(pl, smem_max, s) : go<WT, A_INT8, 2, E_SUMS>(pl, smem_max, s);
     return epi == E_Y ? go<WT, A_INT8, 1, E_Y>(pl, smem_max, s) : go<WT, A_INT8, 1, E_SUMS>(pl, smem_max, s);
 }
 template <int WT, int AM>

@@ -45,6 +45,7 @@ namespace qmm {
 
 constexpr int kDmmaWarps = 16;
 constexpr int kDmmaRows = 16;  // weight rows per tile
+constexpr int kDmmaMaxM = 16;  // activation rows: two int8 column sets, four f32 ones
 
 struct DmmaParams {
     const uint8_t* wq;
@@ -65,7 +66,9 @@ struct DmmaParams {
     int row_pitch;    // bytes between rows in a stage with one copy per row (0: one contiguous copy)
     int off_flags, off_act, off_scale, off_aux, off_red, off_stage;
     int act_pitch;    // int8: bytes per activation row; f32: halves per (row, piece) plane
-    int sstride;      // activation scales per unit: 8 (int8), 4 * column sets (f32)
+    int sstride;      // activation scales per unit: 8 * column sets (int8; also the rows of the Q4_K sums), 4 * column sets (f32)
+    int xplanes;      // f32 Q4_K: activation planes per unit in the sums of 32 (16, or 8 * column sets when more)
+    int aux_unit;     // bytes of the Q4_K aux layout per unit
     // Activations prepared once by dmma_prep_kernel (null: every CTA prepares
     // its own slice).  Byte offsets in ext: codes (int8 [M][K]) or f16 planes
     // ([2M][K] in MMA k order), scales [unit][sstride], aux [unit][...].
@@ -87,7 +90,8 @@ struct ActDst {
     long long pitch;
     float* scale;     // [unit][sstride]
     int sstride;
-    uint8_t* aux;     // int8 Q4_K: [unit][8 pairs][8 rows] f16x2 sums of 16 codes; f32 Q4_K: [unit][16 planes][8] X halves
+    uint8_t* aux;     // int8 Q4_K: [unit][8 pairs][sstride rows] f16x2 sums of 16 codes; f32 Q4_K: [unit][xplanes][8] X halves
+    int xplanes;
 };
 
 // int8 Q8_0, one thread: the 32-block b of row r (src: its 32 floats)
@@ -98,7 +102,7 @@ __device__ __forceinline__ void prep_i8_q8_0(const float* src, int r, int b, con
     uint4* dst = reinterpret_cast<uint4*>(o.act + r * o.pitch + b * 32);
     dst[0] = make_uint4(c[0], c[1], c[2], c[3]);
     dst[1] = make_uint4(c[4], c[5], c[6], c[7]);
-    o.scale[b * 8 + r] = h2f(f2h(d));
+    o.scale[b * o.sstride + r] = h2f(f2h(d));
 }
 
 // int8 Q8K, one warp: super-block sb of row r (src: its 256 floats); lane l
@@ -120,8 +124,8 @@ __device__ __forceinline__ void prep_i8_q8k(const float* src, int r, int sb, int
     const int s16n = __shfl_down_sync(0xffffffffu, s16, 2);      // the next sum of 16
     // |sum of 16 codes| <= 2032: exact in f16
     if ((lane & 3) == 0)
-        reinterpret_cast<uint32_t*>(o.aux)[(sb * 8 + (lane >> 2)) * 8 + r] = f2h((float)s16) | (f2h((float)s16n) << 16);
-    if (lane == 0) o.scale[sb * 8 + r] = d;
+        reinterpret_cast<uint32_t*>(o.aux)[(sb * 8 + (lane >> 2)) * o.sstride + r] = f2h((float)s16) | (f2h((float)s16n) << 16);
+    if (lane == 0) o.scale[sb * o.sstride + r] = d;
 }
 
 // f32: one lane's 8 values of a 32-group (positions 8t..8t+7 of the MMA k
@@ -206,8 +210,8 @@ __device__ __forceinline__ void prep_f32_q4_k(const float* src, int r, int sb, i
         const __half h = __float2half_rn(xq);
         const __half l = __float2half_rn(__fsub_rn(xq, __half2float(h)));
         uint16_t* xs = reinterpret_cast<uint16_t*>(o.aux);
-        xs[(sb * 16 + 2 * r) * 8 + c] = __half_as_ushort(h);
-        xs[(sb * 16 + 2 * r + 1) * 8 + c] = __half_as_ushort(l);
+        xs[(sb * o.xplanes + 2 * r) * 8 + c] = __half_as_ushort(h);
+        xs[(sb * o.xplanes + 2 * r + 1) * 8 + c] = __half_as_ushort(l);
     }
     if (lane == 0) o.scale[sb * o.sstride + r] = ldexpf(1.0f, -s);
 }
@@ -259,6 +263,7 @@ __global__ void __launch_bounds__(kPrepThreads) dmma_prep_kernel(const DmmaParam
     o.scale = reinterpret_cast<float*>(ext + p.ext_scale);
     o.sstride = p.sstride;
     o.aux = ext + p.ext_aux;
+    o.xplanes = p.xplanes;
     const long long tid = (long long)blockIdx.x * kPrepThreads + threadIdx.x;
     if (prep_per_warp<WT, AM>())
         prep_items<WT, AM>(p.x, p.M, p.K, 0, p.units, o, tid >> 5, (long long)gridDim.x * (kPrepThreads / 32), threadIdx.x & 31);
@@ -309,9 +314,16 @@ __device__ __forceinline__ uint32_t s8_02_h2(uint32_t w, uint32_t m00ff, uint32_
 // other at the end of a tile).
 constexpr int kDmmaThreads = (kDmmaWarps + 2) * 32;
 
+// activation rows a tile's partial sums hold per weight row: 8 per int8 column
+// set, 4 per f32 column set (hi and lo pieces of 4 rows), 8 at least
+__host__ __device__ constexpr int dmma_red_cols(int am, int nb) {
+    return (am == A_INT8 ? 8 * nb : 4 * nb) > 8 ? (am == A_INT8 ? 8 * nb : 4 * nb) : 8;
+}
+
 template <int WT, int AM, int NB, int EPI>
 __global__ void __launch_bounds__(kDmmaThreads, 1) qmm_dmma_kernel(const DmmaParams p) {
     constexpr int UB = Unit<WT>::bytes;
+    constexpr int RW = dmma_red_cols(AM, NB);  // activation rows per weight row in the reduction buffer
     extern __shared__ __align__(128) uint8_t smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int S = p.stages;
@@ -349,27 +361,36 @@ __global__ void __launch_bounds__(kDmmaThreads, 1) qmm_dmma_kernel(const DmmaPar
         auto fetch_act = [&]() {
             grid_dep_wait();
             const int k0 = su0 * Unit<WT>::vals, klen = sunits * Unit<WT>::vals;
-            const int nrow = AM == A_INT8 ? p.M : 2 * p.M;
+            const int nrow = AM == A_INT8 ? p.M : 2 * p.M;  // up to 32
             const int vb = AM == A_INT8 ? 1 : 2;  // bytes per activation value
-            long long src = 0;
-            uint32_t dst = 0, bytes = 0;
-            if (lane < nrow) {
-                src = p.ext_codes + ((long long)lane * p.K + k0) * vb;
-                dst = p.off_act + lane * p.act_pitch * vb;
-                bytes = (uint32_t)(klen * vb);
-            } else if (lane == nrow) {
-                src = p.ext_scale + (long long)su0 * p.sstride * 4;
-                dst = p.off_scale;
-                bytes = (uint32_t)(sunits * p.sstride * 4);
-            } else if (lane == nrow + 1 && WT == T_Q4_K) {
-                src = p.ext_aux + (long long)su0 * 256;
-                dst = p.off_aux;
-                bytes = (uint32_t)sunits * 256u;
-            }
-            const uint32_t tx = __reduce_add_sync(0xffffffffu, bytes);
+            // copies: the nrow rows (or row pieces), the scales, the Q4_K aux sums;
+            // lane l takes copies l and l + 32
+            auto item = [&](int i, long long& src, uint32_t& dst, uint32_t& bytes) {
+                src = 0, dst = 0, bytes = 0;
+                if (i < nrow) {
+                    src = p.ext_codes + ((long long)i * p.K + k0) * vb;
+                    dst = p.off_act + i * p.act_pitch * vb;
+                    bytes = (uint32_t)(klen * vb);
+                } else if (i == nrow) {
+                    src = p.ext_scale + (long long)su0 * p.sstride * 4;
+                    dst = p.off_scale;
+                    bytes = (uint32_t)(sunits * p.sstride * 4);
+                } else if (i == nrow + 1 && WT == T_Q4_K) {
+                    src = p.ext_aux + (long long)su0 * p.aux_unit;
+                    dst = p.off_aux;
+                    bytes = (uint32_t)sunits * (uint32_t)p.aux_unit;
+                }
+            };
+            long long src[2];
+            uint32_t dst[2], bytes[2];
+            item(lane, src[0], dst[0], bytes[0]);
+            item(lane + 32, src[1], dst[1], bytes[1]);
+            const uint32_t tx = __reduce_add_sync(0xffffffffu, bytes[0] + bytes[1]);
             if (lane == 0) mbar_arrive_tx(smem_u32(abar), tx);
             __syncwarp();
-            if (bytes) bulk_g2s(smem_u32(smem + dst), p.ext + src, bytes, smem_u32(abar));
+#pragma unroll
+            for (int c = 0; c < 2; ++c)
+                if (bytes[c]) bulk_g2s(smem_u32(smem + dst[c]), p.ext + src[c], bytes[c], smem_u32(abar));
         };
         bool act_done = p.ext == nullptr;
         long long g = 0;
@@ -429,13 +450,13 @@ __global__ void __launch_bounds__(kDmmaThreads, 1) qmm_dmma_kernel(const DmmaPar
         for (int grp = grp0; grp < p.ntiles; grp += p.per_slice, ++tc) {
             if (!mbar_wait(smem_u32(rfull), (uint32_t)(tc & 1), flags, p.err)) break;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
+            for (int i = 0; i < kDmmaRows * RW / 32; ++i) {
                 const int o = lane + 32 * i;
-                const int m = o & 7;
-                const long long n = (long long)grp * kDmmaRows + (o >> 3);
+                const int m = o % RW;
+                const long long n = (long long)grp * kDmmaRows + o / RW;
                 float v = 0.0f;
 #pragma unroll
-                for (int w = 0; w < kDmmaWarps; ++w) v += red[w * 128 + o];
+                for (int w = 0; w < kDmmaWarps; ++w) v += red[w * kDmmaRows * RW + o];
                 if (!flags[0] && m < p.M && n < p.N) {
                     if (p.kslices == 1) p.y[(long long)m * p.N + n] = v;
                     else p.partial[((long long)slice * p.M + m) * p.N + n] = v;
@@ -457,6 +478,7 @@ __global__ void __launch_bounds__(kDmmaThreads, 1) qmm_dmma_kernel(const DmmaPar
         o.scale = reinterpret_cast<float*>(smem + p.off_scale);
         o.sstride = p.sstride;
         o.aux = smem + p.off_aux;
+        o.xplanes = p.xplanes;
         if (prep_per_warp<WT, AM>())
             prep_items<WT, AM>(p.x, p.M, p.K, su0, sunits, o, warp, kDmmaWarps, lane);
         else
@@ -474,7 +496,10 @@ __global__ void __launch_bounds__(kDmmaThreads, 1) qmm_dmma_kernel(const DmmaPar
     int bc[NB];
 #pragma unroll
     for (int s = 0; s < NB; ++s) {
-        if (AM == A_INT8) bc[s] = g8 < p.M ? g8 : g8 % p.M;
+        if (AM == A_INT8) {
+            const int r = 8 * s + g8;
+            bc[s] = r < p.M ? r : r % p.M;
+        }
         else {
             const int pl = 8 * s + g8;
             bc[s] = (pl >> 1) < p.M ? pl : pl % (2 * p.M);
@@ -528,7 +553,7 @@ __global__ void __launch_bounds__(kDmmaThreads, 1) qmm_dmma_kernel(const DmmaPar
                     for (int s = 0; s < NB; ++s)
                         xp[s] = AM == A_F32 ? act + (long long)bc[s] * p.act_pitch * 2 + (u0 * 32 + 8 * t4) * 2
                                             : act + bc[s] * p.act_pitch + u0 * 32 + 4 * t4;
-                    const float* sp = AM == A_F32 ? asc + u0 * p.sstride : asc + u0 * 8 + 2 * t4;
+                    const float* sp = AM == A_F32 ? asc + u0 * p.sstride : asc + u0 * p.sstride + 2 * t4;
                     int u = u0;
 #pragma unroll 2
                     for (int uu = warp; uu < cnu; uu += kDmmaWarps, u += kDmmaWarps) {
@@ -578,25 +603,28 @@ __global__ void __launch_bounds__(kDmmaThreads, 1) qmm_dmma_kernel(const DmmaPar
                             }
                             sp += kDmmaWarps * p.sstride;
                         } else {
-                            const uint32_t b0 = ld32(xp[0]), b1 = ld32(xp[0] + 16);
-                            xp[0] += kDmmaWarps * 32;
+#pragma unroll
+                            for (int s = 0; s < NB; ++s) {
+                            const uint32_t b0 = ld32(xp[s]), b1 = ld32(xp[s] + 16);
+                            xp[s] += kDmmaWarps * 32;
                             int d[4];
                             mma_s8(d, lo0, lo1, hi0, hi1, b0, b1);
                             if (EPI == E_Y) {
-                                const float2 dv = *reinterpret_cast<const float2*>(sp);
-                                acc[0][0][0] = fmaf((float)d[0], dw0 * dv.x, acc[0][0][0]);
-                                acc[0][0][1] = fmaf((float)d[1], dw0 * dv.y, acc[0][0][1]);
-                                acc[0][1][0] = fmaf((float)d[2], dw1 * dv.x, acc[0][1][0]);
-                                acc[0][1][1] = fmaf((float)d[3], dw1 * dv.y, acc[0][1][1]);
-                                sp += kDmmaWarps * 8;
+                                const float2 dv = *reinterpret_cast<const float2*>(sp + 8 * s);
+                                acc[s][0][0] = fmaf((float)d[0], dw0 * dv.x, acc[s][0][0]);
+                                acc[s][0][1] = fmaf((float)d[1], dw0 * dv.y, acc[s][0][1]);
+                                acc[s][1][0] = fmaf((float)d[2], dw1 * dv.x, acc[s][1][0]);
+                                acc[s][1][1] = fmaf((float)d[3], dw1 * dv.y, acc[s][1][1]);
                             } else {
 #pragma unroll
                                 for (int i = 0; i < 4; ++i) {
-                                    const int m = 2 * t4 + (i & 1);
+                                    const int m = 8 * s + 2 * t4 + (i & 1);
                                     const long long n = (long long)grp * kDmmaRows + g8 + 8 * (i >> 1);
                                     if (m < p.M && n < p.N) p.sums[((long long)m * p.N + n) * p.units + su0 + u] = d[i];
                                 }
                             }
+                            }
+                            if (EPI == E_Y) sp += kDmmaWarps * p.sstride;
                         }
                         w0p += kDmmaWarps * UB / 4;
                         h0p += kDmmaWarps * UB / 4;
@@ -661,16 +689,23 @@ __global__ void __launch_bounds__(kDmmaThreads, 1) qmm_dmma_kernel(const DmmaPar
 #pragma unroll
                             for (int s = 0; s < NB; ++s) {
                                 float dm[4];
-                                mma_f16_k8(dm, ma0, ma1, aux[(u * 16 + bc[s]) * 4 + t4]);
+                                mma_f16_k8(dm, ma0, ma1, aux[(u * p.xplanes + bc[s]) * 4 + t4]);
                                 const float io = asc[u * p.sstride + ar[s]];  // 2^-s of (activation row, super-block)
                                 acc[s][0][0] = fmaf(io, fD0 * (d[s][0] + d[s][1]) - fM0 * (dm[0] + dm[1]), acc[s][0][0]);
                                 acc[s][1][0] = fmaf(io, fD1 * (d[s][2] + d[s][3]) - fM1 * (dm[2] + dm[3]), acc[s][1][0]);
                             }
                         } else {
                             // S_sc: low nibbles as they are, high nibbles as 16 n (their sums are then
-                            // multiples of 16 and are divided back exactly at the end)
-                            int sl[4] = {0, 0, 0, 0}, shi[4] = {0, 0, 0, 0};
-                            const uint8_t* xb = act + bc[0] * p.act_pitch + u * 256 + 4 * t4;
+                            // multiples of 16 and are divided back exactly at the end); one set of
+                            // sums per column set (8 activation rows each)
+                            int sl[NB][4], shi[NB][4];
+                            const uint8_t* xb[NB];
+#pragma unroll
+                            for (int s = 0; s < NB; ++s) {
+                                xb[s] = act + bc[s] * p.act_pitch + u * 256 + 4 * t4;
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) sl[s][i] = shi[s][i] = 0;
+                            }
 #pragma unroll
                             for (int c = 0; c < 4; ++c) {
                                 const uint32_t qa0 = ld32(h0p + 16 + 32 * c + 4 * t4), qb0 = ld32(h0p + 32 + 32 * c + 4 * t4);
@@ -679,44 +714,52 @@ __global__ void __launch_bounds__(kDmmaThreads, 1) qmm_dmma_kernel(const DmmaPar
                                 for (int h = 0; h < 2; ++h) {
                                     const int j = 2 * c + h;
                                     const uint32_t mk = h ? 0xF0F0F0F0u : 0x0F0F0F0Fu;
-                                    int dj[4];
-                                    mma_u8s8(dj, qa0 & mk, qa1 & mk, qb0 & mk, qb1 & mk, ld32(xb + 32 * j), ld32(xb + 32 * j + 16));
                                     const uint32_t selj = 0x4440u | (uint32_t)(j & 3);
                                     const int sc0 = (int)__byte_perm(j < 4 ? sc03[0] : sc47[0], 0, selj);
                                     const int sc1 = (int)__byte_perm(j < 4 ? sc03[1] : sc47[1], 0, selj);
-                                    int* t = h ? shi : sl;
-                                    t[0] += sc0 * dj[0];
-                                    t[1] += sc0 * dj[1];
-                                    t[2] += sc1 * dj[2];
-                                    t[3] += sc1 * dj[3];
+#pragma unroll
+                                    for (int s = 0; s < NB; ++s) {
+                                        int dj[4];
+                                        mma_u8s8(dj, qa0 & mk, qa1 & mk, qb0 & mk, qb1 & mk, ld32(xb[s] + 32 * j),
+                                                 ld32(xb[s] + 32 * j + 16));
+                                        int* t = h ? shi[s] : sl[s];
+                                        t[0] += sc0 * dj[0];
+                                        t[1] += sc0 * dj[1];
+                                        t[2] += sc1 * dj[2];
+                                        t[3] += sc1 * dj[3];
+                                    }
                                 }
                             }
-                            int ssc[4];
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) ssc[i] = sl[i] + (shi[i] >> 4);
                             // S_m = sum_j m_j (sum of the sub-block's 32 codes), as 16 slots of sums of 16
                             const uint32_t ma0 = h2_sub(__byte_perm(mn03[0], 0x64646464u, sel_m1), 0x64006400u);
                             const uint32_t ma1 = h2_sub(__byte_perm(mn03[1], 0x64646464u, sel_m1), 0x64006400u);
                             const uint32_t ma2 = h2_sub(__byte_perm(mn47[0], 0x64646464u, sel_m1), 0x64006400u);
                             const uint32_t ma3 = h2_sub(__byte_perm(mn47[1], 0x64646464u, sel_m1), 0x64006400u);
-                            float sm[4];
-                            mma_f16_z(sm, ma0, ma1, ma2, ma3, aux[(u * 8 + t4) * 8 + bc[0]], aux[(u * 8 + t4 + 4) * 8 + bc[0]]);
-                            if (EPI == E_Y) {
-                                const float2 dv = *reinterpret_cast<const float2*>(asc + u * 8 + 2 * t4);
-                                const float fD0 = h2f(h0.x), fD1 = h2f(h1.x), fM0 = h2f(h0.x >> 16), fM1 = h2f(h1.x >> 16);
-                                acc[0][0][0] = fmaf(dv.x, fD0 * (float)ssc[0] - fM0 * sm[0], acc[0][0][0]);
-                                acc[0][0][1] = fmaf(dv.y, fD0 * (float)ssc[1] - fM0 * sm[1], acc[0][0][1]);
-                                acc[0][1][0] = fmaf(dv.x, fD1 * (float)ssc[2] - fM1 * sm[2], acc[0][1][0]);
-                                acc[0][1][1] = fmaf(dv.y, fD1 * (float)ssc[3] - fM1 * sm[3], acc[0][1][1]);
-                            } else {
 #pragma unroll
-                                for (int i = 0; i < 4; ++i) {
-                                    const int m = 2 * t4 + (i & 1);
-                                    const long long n = (long long)grp * kDmmaRows + g8 + 8 * (i >> 1);
-                                    if (m < p.M && n < p.N) {
-                                        int* o = p.sums + (((long long)m * p.N + n) * p.units + su0 + u) * 2;
-                                        o[0] = ssc[i];
-                                        o[1] = (int)sm[i];
+                            for (int s = 0; s < NB; ++s) {
+                                int ssc[4];
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) ssc[i] = sl[s][i] + (shi[s][i] >> 4);
+                                float sm[4];
+                                mma_f16_z(sm, ma0, ma1, ma2, ma3, aux[(u * 8 + t4) * p.sstride + bc[s]],
+                                          aux[(u * 8 + t4 + 4) * p.sstride + bc[s]]);
+                                if (EPI == E_Y) {
+                                    const float2 dv = *reinterpret_cast<const float2*>(asc + u * p.sstride + 8 * s + 2 * t4);
+                                    const float fD0 = h2f(h0.x), fD1 = h2f(h1.x), fM0 = h2f(h0.x >> 16), fM1 = h2f(h1.x >> 16);
+                                    acc[s][0][0] = fmaf(dv.x, fD0 * (float)ssc[0] - fM0 * sm[0], acc[s][0][0]);
+                                    acc[s][0][1] = fmaf(dv.y, fD0 * (float)ssc[1] - fM0 * sm[1], acc[s][0][1]);
+                                    acc[s][1][0] = fmaf(dv.x, fD1 * (float)ssc[2] - fM1 * sm[2], acc[s][1][0]);
+                                    acc[s][1][1] = fmaf(dv.y, fD1 * (float)ssc[3] - fM1 * sm[3], acc[s][1][1]);
+                                } else {
+#pragma unroll
+                                    for (int i = 0; i < 4; ++i) {
+                                        const int m = 8 * s + 2 * t4 + (i & 1);
+                                        const long long n = (long long)grp * kDmmaRows + g8 + 8 * (i >> 1);
+                                        if (m < p.M && n < p.N) {
+                                            int* o = p.sums + (((long long)m * p.N + n) * p.units + su0 + u) * 2;
+                                            o[0] = ssc[i];
+                                            o[1] = (int)sm[i];
+                                        }
                                     }
                                 }
                             }
@@ -731,16 +774,19 @@ __global__ void __launch_bounds__(kDmmaThreads, 1) qmm_dmma_kernel(const DmmaPar
         // ---- tile partials of (weight row, activation row) to the reducer;
         // its buffer is free once the reducer has read the previous tile
         if (tc >= 1) mbar_wait(smem_u32(rempty), (uint32_t)((tc - 1) & 1), flags, p.err);
-        float* rb = red + warp * 128;
+        float* rb = red + warp * kDmmaRows * RW;
         if (AM == A_F32) {
 #pragma unroll
             for (int s = 0; s < NB; ++s) {
-                rb[g8 * 8 + t4 + 4 * s] = acc[s][0][0];
-                rb[(g8 + 8) * 8 + t4 + 4 * s] = acc[s][1][0];
+                rb[g8 * RW + t4 + 4 * s] = acc[s][0][0];
+                rb[(g8 + 8) * RW + t4 + 4 * s] = acc[s][1][0];
             }
         } else {
-            *reinterpret_cast<float2*>(rb + g8 * 8 + 2 * t4) = make_float2(acc[0][0][0], acc[0][0][1]);
-            *reinterpret_cast<float2*>(rb + (g8 + 8) * 8 + 2 * t4) = make_float2(acc[0][1][0], acc[0][1][1]);
+#pragma unroll
+            for (int s = 0; s < NB; ++s) {
+                *reinterpret_cast<float2*>(rb + g8 * RW + 8 * s + 2 * t4) = make_float2(acc[s][0][0], acc[s][0][1]);
+                *reinterpret_cast<float2*>(rb + (g8 + 8) * RW + 8 * s + 2 * t4) = make_float2(acc[s][1][0], acc[s][1][1]);
+            }
         }
         mbar_arrive(smem_u32(rfull));
     }
@@ -752,7 +798,7 @@ __global__ void __launch_bounds__(kDmmaThreads, 1) qmm_dmma_kernel(const DmmaPar
 
 struct DmmaPlan {
     DmmaParams p;
-    int nb;   // B column sets (2 for f32_act with M > 4)
+    int nb;   // B column sets: int8 1 (M <= 8) or 2; f32 1 (M <= 4), 2 (M <= 8) or 4
     int grid;
     size_t smem;
     size_t workspace;  // ext_bytes + split-K partial sums
@@ -781,13 +827,17 @@ inline bool dmma_layout(int wt, int am, long long M, int nb, int ks, int ups, in
     if (am == A_INT8) {
         p.act_pitch = pitch_mod(kv, 16);  // 4-byte B loads of 8 rows x 4 threads: 32 banks
         act = (int)M * p.act_pitch;
-        p.sstride = 8;
-        if (wt == T_Q4_K) aux = su * 8 * 8 * 4;
+        p.sstride = 8 * nb;
+        p.xplanes = 0;
+        p.aux_unit = 8 * p.sstride * 4;  // Q4_K: [8 pairs of sums of 16][rows] f16x2
+        if (wt == T_Q4_K) aux = su * p.aux_unit;
     } else {
         p.act_pitch = pitch_mod(2 * kv, 64) / 2;  // 16-byte B loads of 2 planes per quarter-warp
         act = 2 * (int)M * p.act_pitch * 2;
         p.sstride = 4 * nb;
-        if (wt == T_Q4_K) aux = su * 16 * 8 * 2;
+        p.xplanes = 8 * nb > 16 ? 8 * nb : 16;
+        p.aux_unit = p.xplanes * 8 * 2;  // Q4_K: [planes][8 sums of 32] halves
+        if (wt == T_Q4_K) aux = su * p.aux_unit;
     }
     const int scale = su * p.sstride * 4;
     int off = 256;  // mbarriers: 2 per stage (<= 8 stages), 2 for the reducer, 1 for the activations
@@ -800,7 +850,7 @@ inline bool dmma_layout(int wt, int am, long long M, int nb, int ks, int ups, in
     p.off_aux = off;
     off = round_up(off + aux, 128);
     p.off_red = off;
-    off = round_up(off + kDmmaWarps * 128 * 4, 128);
+    off = round_up(off + kDmmaWarps * kDmmaRows * dmma_red_cols(am, nb) * 4, 128);
     p.off_stage = off;
     long long sb;
     if (ks == 1 && ups == su && 16 * p.rb <= 36864) {
@@ -826,7 +876,7 @@ inline bool dmma_layout(int wt, int am, long long M, int nb, int ks, int ups, in
 
 inline bool plan_dmma(int wt, int am, long long M, long long N, long long K, int sm_count, int smem_max,
                       DmmaPlan& out, bool ext_ok = true) {
-    if (M < 1 || M > 8) return false;
+    if (M < 1 || M > kDmmaMaxM) return false;
     DmmaPlan pl{};
     DmmaParams& p = pl.p;
     const int uv = is_b32(wt) ? 32 : 256, ub = unit_bytes(wt);
@@ -837,7 +887,8 @@ inline bool plan_dmma(int wt, int am, long long M, long long N, long long K, int
     p.rb = (long long)p.units * ub;
     p.total_bytes = p.rb * N;
     p.ntiles = (int)((N + kDmmaRows - 1) / kDmmaRows);
-    pl.nb = (am == A_F32 && M > 4) ? 2 : 1;
+    // B column sets: 8 activation rows each (int8), or 4 rows of two pieces (f32)
+    pl.nb = am == A_INT8 ? (M > 8 ? 2 : 1) : (M > 8 ? 4 : M > 4 ? 2 : 1);
     // K chunk per stage.  One SM's bulk-copy engine caps row copies below
     // ~3 KB, so the first tier takes the fewest K slices that fit a chunk of
     // >= 96 Q8_0 blocks (32 super-blocks; a shorter K as one chunk, unsplit),
@@ -881,7 +932,7 @@ inline bool plan_dmma(int wt, int am, long long M, long long N, long long K, int
         p.ext_scale = off;
         off = r256(off + (long long)p.units * p.sstride * 4);
         p.ext_aux = off;
-        if (wt == T_Q4_K) off = r256(off + (long long)p.units * 256);
+        if (wt == T_Q4_K) off = r256(off + (long long)p.units * p.aux_unit);
         pl.ext_bytes = (size_t)off;
     }
     pl.workspace = pl.ext_bytes + (p.kslices > 1 ? (size_t)p.kslices * M * N * 4 : 0);
