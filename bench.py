@@ -63,6 +63,7 @@ KERNEL_SOURCES = {
     "qmm_gemv_kernel": ["qmm_gemv.cuh", "qmm_device.cuh"],
     "qmm_dmma_kernel": ["qmm_dmma.cuh", "qmm_device.cuh"],
     "qmm_stream_kernel": ["qmm_stream.cuh", "qmm_device.cuh"],
+    "qmm_tc_kernel": ["qmm_tc.cuh", "qmm_device.cuh"],
 }
 
 
@@ -77,11 +78,11 @@ def kernel_hash(kernel: str) -> str:
 def kernel_of(wtype: str, mode: str, M: int) -> str:
     """The streaming kernel qmm_matmul dispatches to for a decode shape (the
     library's own rule): Q8_0 int8_act with M = 1 -> per-thread dp4a GEMV;
-    other M <= 8 -> 16-row tensor-core decode kernel (after an activation-
+    other M <= 16 -> 16-row tensor-core decode kernel (after an activation-
     preparing kernel for large weight matrices); larger M -> the GEMMs."""
     if mode == "int8_act" and wtype == "q8_0" and M <= 1:
         return "qmm_gemv_kernel"
-    return "qmm_dmma_kernel" if M <= 8 else "qmm_stream_kernel"
+    return "qmm_dmma_kernel" if M <= 16 else "qmm_tc_kernel"
 
 
 def ncu_traffic(kernel: str):
