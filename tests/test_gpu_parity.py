@@ -87,7 +87,8 @@ def test_dequantize_bit_exact(qmm, orc, t, K):
 SUM_CASES = [("q8_0", 1, 33, 576), ("q8_0", 8, 576, 576), ("q8_0", 5, 40, 4096), ("q8_0", 13, 17, 1536),
              ("q8_0", 37, 24, 96), ("q4_k", 1, 33, 1536), ("q4_k", 8, 64, 2048), ("q4_k", 19, 20, 4096),
              ("q4_0", 1, 33, 576), ("q4_0", 13, 40, 1536), ("q5_0", 1, 192, 576), ("q5_0", 8, 33, 576),
-             ("q5_0", 37, 24, 4096), ("q6_k", 1, 33, 1536), ("q6_k", 8, 64, 2048), ("q6_k", 19, 20, 4096)]
+             ("q5_0", 37, 24, 4096), ("q6_k", 1, 33, 1536), ("q6_k", 8, 64, 2048), ("q6_k", 19, 20, 4096),
+             ("q4_k", 16, 40, 2048), ("q4_0", 12, 50, 1536), ("q8_0", 16, 33, 4096)]
 
 
 @pytest.mark.parametrize("wtype,M,N,K", SUM_CASES)
@@ -140,6 +141,11 @@ MATMUL_CASES = [
     ("q4_0", 64, 130, 1024),      # prefill on tcgen05 (K % 256 = 0)
     ("q5_0", 256, 200, 1536),
     ("q4_0", 300, 260, 2048),
+    ("q4_k", 13, 300, 4096),      # 9..16 rows on the warp-MMA kernel: f32 four column sets, K split
+    ("q8_0", 12, 2050, 8192),     # ragged tile, activations prepared in the kernel
+    ("q4_0", 16, 600, 4096),
+    ("q5_0", 11, 333, 1536),
+    ("q8_0", 16, 4100, 8192),     # 35.6 MB of weights: activations prepared once, then the decode kernel
     ("q6_k", 1, 576, 1536),       # the downloaded file's Q6K ffn_down, decode batches 1 and 8
     ("q6_k", 8, 576, 1536),
     ("q6_k", 3, 37, 8192),        # ragged tile, long rows
