@@ -95,9 +95,9 @@ struct Dispatch {
 void plan_dispatch(int wt, int am, int epi, long long M, long long N, long long K, int sms, int smem, Dispatch& d) {
     d = Dispatch();
     if (wt == T_Q4_0 || wt == T_Q5_0 || wt == T_Q6_K) {
-        // Q4_0 / Q5_0: decode on 16-row tensor-core tiles, prefill on the tcgen05 GEMM
-        // where K allows; everything else (and every Q6_K call) on the streaming kernel
-        if (wt != T_Q6_K && M <= kDmmaMaxM && plan_dmma(wt, am, M, N, K, sms, smem, d.dp, epi == E_Y)) {
+        // up to 16 rows on 16-row warp-MMA tiles; Q4_0 / Q5_0 prefill on the tcgen05 GEMM
+        // where K allows; everything else (Q6_K prefill among it) on the streaming kernel
+        if (M <= kDmmaMaxM && plan_dmma(wt, am, M, N, K, sms, smem, d.dp, epi == E_Y)) {
             d.kind = KIND_DMMA;
             d.workspace = d.dp.workspace;
             d.launches = 1 + (d.dp.ext_bytes ? 1 : 0) + (epi == E_Y && d.dp.p.kslices > 1 ? 1 : 0);

@@ -58,11 +58,13 @@ cudaError_t prep(const DmmaPlan& pl, void* ext, cudaStream_t s) {
 cudaError_t launch_dmma_prep(int wt, int am, const DmmaPlan& pl, void* ext, cudaStream_t s) {
     // Q4_0 and Q5_0 weights take Q8_0 activations: the same preparation as Q8_0
     if (is_b32(wt)) return am == A_F32 ? prep<T_Q8_0, A_F32>(pl, ext, s) : prep<T_Q8_0, A_INT8>(pl, ext, s);
+    if (wt == T_Q6_K) return am == A_F32 ? prep<T_Q6_K, A_F32>(pl, ext, s) : prep<T_Q6_K, A_INT8>(pl, ext, s);
     return am == A_F32 ? prep<T_Q4_K, A_F32>(pl, ext, s) : prep<T_Q4_K, A_INT8>(pl, ext, s);
 }
 
 cudaError_t launch_dmma(int wt, int am, int epi, const DmmaPlan& pl, int smem_max, cudaStream_t s) {
     if (wt == T_Q4_0 || wt == T_Q5_0) return launch_dmma_x_0(wt, am, epi, pl, smem_max, s);
+    if (wt == T_Q6_K) return launch_dmma_q6_k(am, epi, pl, smem_max, s);
     return wt == T_Q8_0 ? go_type<T_Q8_0>(am, epi, pl, smem_max, s) : go_type<T_Q4_K>(am, epi, pl, smem_max, s);
 }
 

@@ -107,6 +107,7 @@ __device__ __forceinline__ void prep_i8_q8_0(const float* src, int r, int b, con
 
 // int8 Q8K, one warp: super-block sb of row r (src: its 256 floats); lane l
 // quantizes values 8l..8l+7
+template <bool AUX>  // AUX: also the sums of 16 codes (Q4_K's min term; Q6_K has none)
 __device__ __forceinline__ void prep_i8_q8k(const float* src, int r, int sb, int lane, const ActDst& o) {
     const float4 v0 = __ldg(reinterpret_cast<const float4*>(src) + 2 * lane);
     const float4 v1 = __ldg(reinterpret_cast<const float4*>(src) + 2 * lane + 1);
@@ -123,7 +124,7 @@ __device__ __forceinline__ void prep_i8_q8k(const float* src, int r, int sb, int
     const int s16 = s8 + __shfl_xor_sync(0xffffffffu, s8, 1);   // sum of 16 codes (lanes 2i, 2i+1)
     const int s16n = __shfl_down_sync(0xffffffffu, s16, 2);      // the next sum of 16
     // |sum of 16 codes| <= 2032: exact in f16
-    if ((lane & 3) == 0)
+    if (AUX && (lane & 3) == 0)
         reinterpret_cast<uint32_t*>(o.aux)[(sb * 8 + (lane >> 2)) * o.sstride + r] = f2h((float)s16) | (f2h((float)s16n) << 16);
     if (lane == 0) o.scale[sb * o.sstride + r] = d;
 }
@@ -191,6 +192,7 @@ __device__ __forceinline__ void prep_f32_q8_0(const float* src, int r, int g0, i
 
 // f32 Q4_K, one warp: super-block sb of row r (src: its 256 floats); lanes
 // 4c..4c+3 take 32-group c (sub-block c)
+template <bool AUX>  // AUX: also the scaled sums of each 32 (Q4_K's min term; Q6_K has none)
 __device__ __forceinline__ void prep_f32_q4_k(const float* src, int r, int sb, int lane, const ActDst& o) {
     const int c = lane >> 2, t = lane & 3;
     const float4 a = __ldg(reinterpret_cast<const float4*>(src + c * 32 + 4 * t));
@@ -204,7 +206,7 @@ __device__ __forceinline__ void prep_f32_q4_k(const float* src, int r, int sb, i
     float sum = prep_f32_lane(a, b, ldexpf(1.0f, s), pl + (2 * r) * o.pitch + k, pl + (2 * r + 1) * o.pitch + k);
     sum = __fadd_rn(sum, __shfl_xor_sync(0xffffffffu, sum, 1));
     sum = __fadd_rn(sum, __shfl_xor_sync(0xffffffffu, sum, 2));
-    if (t == 0) {
+    if (AUX && t == 0) {
         // X_c / 32 (|.| < 2^15) in two f16 pieces
         const float xq = __fmul_rn(sum, 0.03125f);
         const __half h = __float2half_rn(xq);
@@ -235,7 +237,7 @@ __device__ __forceinline__ void prep_items(const float* x, int M, int K, int u0,
     } else if (AM == A_INT8) {
         for (long long i = first; i < (long long)M * nu; i += step) {
             const int r = (int)(i / nu), sb = (int)(i - (long long)r * nu);
-            prep_i8_q8k(x + (long long)r * K + k0 + sb * 256, r, sb, lane, o);
+            prep_i8_q8k<WT == T_Q4_K>(x + (long long)r * K + k0 + sb * 256, r, sb, lane, o);
         }
     } else if (is_b32(WT)) {
         const int ng = (nu + 7) / 8;
@@ -246,7 +248,7 @@ __device__ __forceinline__ void prep_items(const float* x, int M, int K, int u0,
     } else {
         for (long long i = first; i < (long long)M * nu; i += step) {
             const int r = (int)(i / nu), sb = (int)(i - (long long)r * nu);
-            prep_f32_q4_k(x + (long long)r * K + k0 + sb * 256, r, sb, lane, o);
+            prep_f32_q4_k<WT == T_Q4_K>(x + (long long)r * K + k0 + sb * 256, r, sb, lane, o);
         }
     }
 }
@@ -630,6 +632,99 @@ __global__ void __launch_bounds__(kDmmaThreads, 1) qmm_dmma_kernel(const DmmaPar
                         h0p += kDmmaWarps * UB / 4;
                         s0p += kDmmaWarps * UB / 2;
                     }
+                } else if (WT == T_Q6_K) {
+                    // Q6_K super-blocks (210 bytes; a warp's blocks are 16 x 210 bytes apart, a
+                    // multiple of 4, so they share one alignment): 16 groups of 16 values, one k16
+                    // MMA each.  Group j = 8h + 2q + sg holds values 128h + 32q + 16sg + l (l < 16);
+                    // thread t4 takes l = 4t4..4t4+3 from one ql word (nibble plane q / 2) and one
+                    // qh word (bit pair q) per row, read as aligned words and realigned.
+                    const int o0 = (int)(r0p - smem) + 210 * warp;
+                    const uint32_t sh = (uint32_t)(o0 & 2) * 8u;
+                    const uint8_t* a0p = smem + (o0 & ~3);
+                    int u = u0;
+#pragma unroll 1
+                    for (int uu = warp; uu < cnu; uu += kDmmaWarps, u += kDmmaWarps, a0p += kDmmaWarps * 210) {
+                        const uint8_t* a1p = a0p + dr;
+                        const uint8_t* b0p = a0p + (sh >> 3);  // the block of row g8; row g8 + 8 at + dr
+                        const float fD0 = h2f(*reinterpret_cast<const uint16_t*>(b0p + 208));
+                        const float fD1 = h2f(*reinterpret_cast<const uint16_t*>(b0p + dr + 208));
+                        const int8_t* sc0p = reinterpret_cast<const int8_t*>(b0p + 192);
+                        const int8_t* sc1p = reinterpret_cast<const int8_t*>(b0p + dr + 192);
+                        int ssc[NB][4];
+                        float tf[NB][2];
+#pragma unroll
+                        for (int s = 0; s < NB; ++s) {
+                            ssc[s][0] = ssc[s][1] = ssc[s][2] = ssc[s][3] = 0;
+                            tf[s][0] = tf[s][1] = 0.0f;
+                        }
+#pragma unroll
+                        for (int h = 0; h < 2; ++h)
+#pragma unroll
+                            for (int sg = 0; sg < 2; ++sg) {
+                                const int lo = 16 * sg + 4 * t4;
+                                auto w0 = [&](int off) { return __funnelshift_r(ld32(a0p + off), ld32(a0p + off + 4), sh); };
+                                auto w1 = [&](int off) { return __funnelshift_r(ld32(a1p + off), ld32(a1p + off + 4), sh); };
+                                const uint32_t L00 = w0(64 * h + lo), L01 = w0(64 * h + 32 + lo), H0 = w0(128 + 32 * h + lo);
+                                const uint32_t L10 = w1(64 * h + lo), L11 = w1(64 * h + 32 + lo), H1 = w1(128 + 32 * h + lo);
+#pragma unroll
+                                for (int q = 0; q < 4; ++q) {
+                                    const int j = 8 * h + 2 * q + sg;
+                                    const uint32_t n0 = ((q & 1 ? L01 : L00) >> (4 * (q >> 1))) & 0x0F0F0F0Fu;
+                                    const uint32_t n1 = ((q & 1 ? L11 : L10) >> (4 * (q >> 1))) & 0x0F0F0F0Fu;
+                                    const uint32_t c0 = __vsub4(n0 | (((H0 >> (2 * q)) & 0x03030303u) << 4), 0x20202020u);
+                                    const uint32_t c1 = __vsub4(n1 | (((H1 >> (2 * q)) & 0x03030303u) << 4), 0x20202020u);
+                                    if (AM == A_INT8) {
+                                        const int vb = 128 * h + 32 * q + lo;  // this thread's first value
+                                        const int s0 = sc0p[j], s1 = sc1p[j];
+#pragma unroll
+                                        for (int s = 0; s < NB; ++s) {
+                                            int d[4];
+                                            mma_s8_k16(d, c0, c1, ld32(act + bc[s] * p.act_pitch + u * 256 + vb));
+                                            ssc[s][0] += s0 * d[0];
+                                            ssc[s][1] += s0 * d[1];
+                                            ssc[s][2] += s1 * d[2];
+                                            ssc[s][3] += s1 * d[3];
+                                        }
+                                    } else {
+                                        // the planes hold each quad of a 32-group as values 0, 2, 1, 3:
+                                        // codes 0 and 2 go with the first pair, 1 and 3 with the second
+                                        const uint32_t a0 = s8_02_h2(c0, kM00FF, k6480), a1 = s8_02_h2(c1, kM00FF, k6480);
+                                        const uint32_t a2 = s8_02_h2(c0 >> 8, kM00FF, k6480), a3 = s8_02_h2(c1 >> 8, kM00FF, k6480);
+                                        const float e0 = __fmul_rn(fD0, (float)sc0p[j]), e1 = __fmul_rn(fD1, (float)sc1p[j]);
+#pragma unroll
+                                        for (int s = 0; s < NB; ++s) {
+                                            const uint2 xv = ld64(act + ((long long)bc[s] * p.act_pitch + u * 256 + 32 * (4 * h + q) +
+                                                                         8 * t4 + 4 * sg) * 2);
+                                            float d[4];
+                                            mma_f16_z(d, a0, a1, a2, a3, xv.x, xv.y);
+                                            tf[s][0] = fmaf(e0, d[0] + d[1], tf[s][0]);
+                                            tf[s][1] = fmaf(e1, d[2] + d[3], tf[s][1]);
+                                        }
+                                    }
+                                }
+                            }
+#pragma unroll
+                        for (int s = 0; s < NB; ++s) {
+                            if (AM == A_F32) {
+                                const float io = asc[u * p.sstride + ar[s]];  // 2^-s of (activation row, super-block)
+                                acc[s][0][0] = fmaf(io, tf[s][0], acc[s][0][0]);
+                                acc[s][1][0] = fmaf(io, tf[s][1], acc[s][1][0]);
+                            } else if (EPI == E_Y) {
+                                const float2 dv = *reinterpret_cast<const float2*>(asc + u * p.sstride + 8 * s + 2 * t4);
+                                acc[s][0][0] = fmaf(dv.x, fD0 * (float)ssc[s][0], acc[s][0][0]);
+                                acc[s][0][1] = fmaf(dv.y, fD0 * (float)ssc[s][1], acc[s][0][1]);
+                                acc[s][1][0] = fmaf(dv.x, fD1 * (float)ssc[s][2], acc[s][1][0]);
+                                acc[s][1][1] = fmaf(dv.y, fD1 * (float)ssc[s][3], acc[s][1][1]);
+                            } else {
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) {
+                                    const int m = 8 * s + 2 * t4 + (i & 1);
+                                    const long long n = (long long)grp * kDmmaRows + g8 + 8 * (i >> 1);
+                                    if (m < p.M && n < p.N) p.sums[((long long)m * p.N + n) * p.units + su0 + u] = ssc[s][i];
+                                }
+                            }
+                        }
+                    }
                 } else {
                     const uint8_t* h0p = r0p + 144 * warp;
                     int u = u0;
@@ -859,7 +954,7 @@ inline bool dmma_layout(int wt, int am, long long M, int nb, int ks, int ups, in
     } else {
         // Q8_0 word loads reach 18 bytes past the chunk (2-byte offset
         // rounding and the 9th word); a copy starts up to 15 bytes early
-        p.row_pitch = pitch_mod(ups * ub + (is_b32(wt) ? 32 : 0), 16);
+        p.row_pitch = pitch_mod(ups * ub + (is_b32(wt) || wt == T_Q6_K ? 32 : 0), 16);
         sb = 16LL * p.row_pitch;
     }
     sb = (sb + 127) / 128 * 128;

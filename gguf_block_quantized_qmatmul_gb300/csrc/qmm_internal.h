@@ -23,6 +23,7 @@ cudaError_t launch_gemv_q8_0(int epi, const GemvPlan& plan, int smem_max, cudaSt
 cudaError_t launch_gemv_q4_k(int epi, const GemvPlan& plan, int smem_max, cudaStream_t s);
 cudaError_t launch_dmma(int wt, int am, int epi, const DmmaPlan& plan, int smem_max, cudaStream_t s);
 cudaError_t launch_dmma_x_0(int wt, int am, int epi, const DmmaPlan& plan, int smem_max, cudaStream_t s);
+cudaError_t launch_dmma_q6_k(int am, int epi, const DmmaPlan& plan, int smem_max, cudaStream_t s);
 cudaError_t launch_dmma_prep(int wt, int am, const DmmaPlan& plan, void* ext, cudaStream_t s);
 cudaError_t launch_tc(int wt, int am, const TcPlan& plan, const void* wq, const float* x, void* ws, float* y, int smem_max,
                       cudaStream_t s);

@@ -281,7 +281,7 @@ def test_launch_counts(qmm):
     assert qmm.matmul_launches("q4_0", "f32_act", 8, 28672, 8192) == 3    # large: preparing kernel, K split
     assert qmm.matmul_launches("q4_0", "f32_act", 64, 4096, 4096) == 2     # prefill, K % 256 = 0: tcgen05
     assert qmm.matmul_launches("q5_0", "int8_act", 64, 576, 576) == 1     # K = 576: the streaming kernel
-    assert qmm.matmul_launches("q6_k", "int8_act", 1, 576, 1536) == 1     # Q6_K: the streaming kernel
+    assert qmm.matmul_launches("q6_k", "int8_act", 1, 576, 1536) == 1     # Q6_K decode: the MMA kernel
     assert qmm.matmul_launches("q6_k", "f32_act", 256, 4096, 4096) == 1
 
 
