@@ -78,7 +78,14 @@ __device__ __forceinline__ float load_block(const uint8_t* s, int o, uint32_t c[
 }
 
 __device__ __forceinline__ unsigned long long pack2(uint32_t lo, uint32_t hi) {
-    return ((unsigned long long)hi << 32) | lo;
+    unsigned long long d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "r"(lo), "r"(hi));
+    return d;
+}
+__device__ __forceinline__ float2 unpack2(unsigned long long v) {
+    uint32_t lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=r"(lo), "=r"(hi) : "l"(v));
+    return make_float2(__uint_as_float(lo), __uint_as_float(hi));
 }
 __device__ __forceinline__ unsigned long long add2(unsigned long long a, unsigned long long b) {
     unsigned long long d;
@@ -148,7 +155,8 @@ __device__ __forceinline__ void block_dot(const uint8_t* s, const int (&wo)[R], 
 #pragma unroll
             for (int h = 0; h < R; ++h) {
                 const unsigned long long s2 = add2(s01[h], s23[h]);
-                const float t = fmaf(dw[h], __uint_as_float((uint32_t)s2) + __uint_as_float((uint32_t)(s2 >> 32)), acc[h][m]);
+                const float2 sv = unpack2(s2);
+                const float t = fmaf(dw[h], sv.x + sv.y, acc[h][m]);
                 acc[h][m] = v[h] ? t : acc[h][m];
             }
         }
