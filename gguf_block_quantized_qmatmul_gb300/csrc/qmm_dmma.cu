@@ -11,23 +11,9 @@ cudaError_t go(const DmmaPlan& pl, int smem_max, cudaStream_t s) {
     auto* k = qmm_dmma_kernel<WT, AM, NB, EPI>;
     cudaError_t e = ensure_smem(k, smem_max, g_smem_done[WT == T_Q8_0 ? 0 : 1][AM][NB == 4 ? 2 : NB - 1][EPI]);
     if (e != cudaSuccess) return e;
-    if (!pl.p.ext) {
-        k<<<pl.grid, kDmmaThreads, pl.smem, s>>>(pl.p);
-        return cudaGetLastError();
-    }
-    // after the preparing kernel: programmatic dependent launch, so that the
-    // weight stream starts while the activations are being prepared
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)pl.grid);
-    cfg.blockDim = dim3(kDmmaThreads);
-    cfg.dynamicSmemBytes = pl.smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k, pl.p);
+    // programmatic dependent launch: the first weight stages stream while the
+    // previous grid (the preparing kernel, or the last call) finishes
+    return launch_pdl(k, (unsigned)pl.grid, kDmmaThreads, pl.smem, s, pl.p);
 }
 
 template <int WT>
@@ -50,8 +36,10 @@ cudaError_t prep(const DmmaPlan& pl, void* ext, cudaStream_t s) {
     else if (WT == T_Q8_0) blocks = ((long long)p.M * p.units + kPrepThreads - 1) / kPrepThreads;  // a thread per 32-block
     else blocks = ((long long)p.M * p.units + kPrepThreads / 32 - 1) / (kPrepThreads / 32);       // a warp per super-block
     if (blocks > 1024) blocks = 1024;
-    dmma_prep_kernel<WT, AM><<<(unsigned)blocks, kPrepThreads, 0, s>>>(p, static_cast<uint8_t*>(ext));
-    return cudaGetLastError();
+    // programmatic dependent launch: scheduled while the previous grid in the
+    // stream (normally the last call's decode grid) still runs; the kernel
+    // waits for that grid before it reads x or writes ext
+    return launch_pdl(dmma_prep_kernel<WT, AM>, (unsigned)blocks, kPrepThreads, 0, s, p, static_cast<uint8_t*>(ext));
 }
 }  // namespace
 

@@ -258,7 +258,10 @@ constexpr int kPrepThreads = 1024;
 // Once per call, for large weight matrices: the whole K range into ext.
 template <int WT, int AM>
 __global__ void __launch_bounds__(kPrepThreads) dmma_prep_kernel(const DmmaParams p, uint8_t* ext) {
-    grid_dep_launch();  // the decode grid may start streaming weights now
+    // The decode grid may launch now and stream its first weight stages; it
+    // waits for this grid before it touches the activations.
+    grid_dep_launch();
+    grid_dep_wait();  // the previous grid in the stream may still be writing x or reading ext
     ActDst o;
     o.act = ext + p.ext_codes;
     o.pitch = p.K;
@@ -353,7 +356,7 @@ __global__ void __launch_bounds__(kDmmaThreads, 1) qmm_dmma_kernel(const DmmaPar
         fence_mbar_init();
     }
     __syncthreads();
-    grid_dep_launch();  // a K-split reduction launched after this grid may be scheduled
+    grid_dep_launch();  // the next grid (a K-split reduction, the next call) may be scheduled
 
     if (warp == kDmmaWarps) {
         // ------------------------------ producer ------------------------------
@@ -400,9 +403,12 @@ __global__ void __launch_bounds__(kDmmaThreads, 1) qmm_dmma_kernel(const DmmaPar
         for (int grp = grp0; grp < p.ntiles && ok; grp += p.per_slice) {
             for (int ch = 0; ch < nch && ok; ++ch, ++g) {
                 const int slot = (int)(g % S);
-                if (g == S && !act_done) {  // the first stages are in flight: now the activations
-                    fetch_act();
-                    act_done = true;
+                if (g == S) {  // the first stages are in flight: wait for the previous grid
+                    grid_dep_wait();
+                    if (!act_done) {  // and fetch the prepared activations
+                        fetch_act();
+                        act_done = true;
+                    }
                 }
                 if (g >= S) {
                     int okl = 1;
@@ -448,6 +454,9 @@ __global__ void __launch_bounds__(kDmmaThreads, 1) qmm_dmma_kernel(const DmmaPar
     if (warp == kDmmaWarps + 1) {
         // ------------------------------ reducer ------------------------------
         if (EPI != E_Y) return;
+        // a programmatically launched grid may be resident long before its
+        // activations exist: start the bounded waits only once they can come
+        grid_dep_wait();
         int tc = 0;
         for (int grp = grp0; grp < p.ntiles; grp += p.per_slice, ++tc) {
             if (!mbar_wait(smem_u32(rfull), (uint32_t)(tc & 1), flags, p.err)) break;
@@ -472,6 +481,7 @@ __global__ void __launch_bounds__(kDmmaThreads, 1) qmm_dmma_kernel(const DmmaPar
 
     // ------------------------------ consumers ------------------------------
     if (p.ext) {
+        grid_dep_wait();  // as the reducer: bounded waits start once the activations can come
         mbar_wait(smem_u32(abar), 0u, flags, p.err);
     } else {
         ActDst o;
@@ -481,6 +491,7 @@ __global__ void __launch_bounds__(kDmmaThreads, 1) qmm_dmma_kernel(const DmmaPar
         o.sstride = p.sstride;
         o.aux = smem + p.off_aux;
         o.xplanes = p.xplanes;
+        grid_dep_wait();  // x may be the previous grid's output
         if (prep_per_warp<WT, AM>())
             prep_items<WT, AM>(p.x, p.M, p.K, su0, sunits, o, warp, kDmmaWarps, lane);
         else

@@ -13,22 +13,9 @@ cudaError_t go(const DmmaPlan& pl, int smem_max, cudaStream_t s) {
     auto* k = qmm_dmma_kernel<WT, AM, NB, EPI>;
     cudaError_t e = ensure_smem(k, smem_max, g_smem_done[WT == T_Q4_0 ? 0 : 1][AM][NB == 4 ? 2 : NB - 1][EPI]);
     if (e != cudaSuccess) return e;
-    if (!pl.p.ext) {
-        k<<<pl.grid, kDmmaThreads, pl.smem, s>>>(pl.p);
-        return cudaGetLastError();
-    }
-    // after the preparing kernel: programmatic dependent launch
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)pl.grid);
-    cfg.blockDim = dim3(kDmmaThreads);
-    cfg.dynamicSmemBytes = pl.smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k, pl.p);
+    // programmatic dependent launch: the first weight stages stream while the
+    // previous grid (the preparing kernel, or the last call) finishes
+    return launch_pdl(k, (unsigned)pl.grid, kDmmaThreads, pl.smem, s, pl.p);
 }
 
 template <int WT>

@@ -124,6 +124,7 @@ __global__ void __launch_bounds__((kGemvWarps + 1) * 32, 1) qmm_gemv_kernel(cons
         fence_mbar_init();
     }
     __syncthreads();
+    grid_dep_launch();  // the next call's first grid may be scheduled (it waits for this one)
 
     if (warp == kGemvWarps) {
         // ------------------------------ producer ------------------------------
@@ -131,6 +132,9 @@ __global__ void __launch_bounds__((kGemvWarps + 1) * 32, 1) qmm_gemv_kernel(cons
         long long g = 0;
         for (int grp = blockIdx.x; grp < p.ngroups; grp += gridDim.x, ++g) {
             const int slot = (int)(g % S);
+            // launched programmatically, the first stages stream while the
+            // previous grid finishes; the bounded waits start after it
+            if (g == S) grid_dep_wait();
             if (g >= S && !mbar_wait(smem_u32(&bars[S + slot]), (uint32_t)(((g / S) - 1) & 1), flags, p.err)) break;
             uint8_t* st = smem + p.off_stage + (long long)slot * p.stage_bytes;
             const long long s0 = (long long)grp * p.tr * p.rb;
@@ -152,6 +156,7 @@ __global__ void __launch_bounds__((kGemvWarps + 1) * 32, 1) qmm_gemv_kernel(cons
     }
 
     // ------------------------------ consumers ------------------------------
+    grid_dep_wait();  // x may be the previous grid's output
     gemv_prepare<WT, MT>(p, smem, tid);
     consumer_sync<kGemvWarps>();
 

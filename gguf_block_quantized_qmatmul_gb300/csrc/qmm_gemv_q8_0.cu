@@ -11,8 +11,7 @@ cudaError_t go(const GemvPlan& pl, int smem_max, cudaStream_t s, unsigned long l
     auto* k = qmm_gemv_kernel<T_Q8_0, MT, EPI>;
     cudaError_t e = ensure_smem(k, smem_max, done);
     if (e != cudaSuccess) return e;
-    k<<<pl.grid, (kGemvWarps + 1) * 32, pl.smem, s>>>(pl.p);
-    return cudaGetLastError();
+    return launch_pdl(k, (unsigned)pl.grid, (kGemvWarps + 1) * 32, pl.smem, s, pl.p);
 }
 
 template <int EPI>

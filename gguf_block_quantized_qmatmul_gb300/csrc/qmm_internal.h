@@ -71,4 +71,27 @@ inline cudaError_t ensure_smem(F* kernel, int smem_max, unsigned long long& done
     return e;
 }
 
+// Launch with programmatic stream serialization: the grid may be scheduled
+// once the previous grid in the stream has triggered (griddepcontrol
+// .launch_dependents) instead of once it has completed.  Every kernel
+// launched this way executes griddepcontrol.wait before it reads what an
+// earlier grid writes, writes what an earlier grid reads, or starts a
+// bounded wait that needs such data; only constant inputs (the weights) are
+// read before it.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), unsigned grid, unsigned block, size_t smem, cudaStream_t s,
+                              Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 }  // namespace qmm

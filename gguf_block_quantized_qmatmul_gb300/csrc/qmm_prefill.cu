@@ -69,17 +69,7 @@ cudaError_t tc_go(const TcPlan& pl, const void* wq, const float* x, void* ws, fl
     auto* k = qmm_tc_kernel<WT>;
     e = ensure_smem(k, smem_max, g_tc_smem_done[WT == T_Q8_0 ? 0 : WT == T_Q4_K ? 1 : WT == T_Q4_0 ? 2 : 3]);
     if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)pl.grid);
-    cfg.blockDim = dim3(kTcThreads);
-    cfg.dynamicSmemBytes = pl.smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k, tw, tah, tal, p);
+    return launch_pdl(k, (unsigned)pl.grid, kTcThreads, pl.smem, s, tw, tah, tal, p);
 }
 
 }  // namespace

@@ -344,7 +344,8 @@ inline unsigned grid_for(long long n, int block) { return (unsigned)((n + block 
 
 // y[i] = sum over K slices s = 0..ks-1 of partial[s][i], in slice order.
 __global__ void splitk_reduce_kernel(const float* __restrict__ partial, long long n, int ks, float* __restrict__ y) {
-    grid_dep_wait();  // launched while the split kernel runs: wait for its partial sums
+    grid_dep_launch();  // the next call's preparing grid may be scheduled (it waits for this one)
+    grid_dep_wait();    // launched while the split kernel runs: wait for its partial sums
     const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= n) return;
     float v = 0.0f;
@@ -356,16 +357,7 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ partial, long lon
 
 cudaError_t launch_splitk_reduce(const float* partial, long long n, int ks, float* y, cudaStream_t s) {
     // programmatic dependent launch: scheduled while the split kernel still runs
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid_for(n, 256));
-    cfg.blockDim = dim3(256);
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, splitk_reduce_kernel, partial, n, ks, y);
+    return launch_pdl(splitk_reduce_kernel, (unsigned)grid_for(n, 256), 256, 0, s, partial, n, ks, y);
 }
 
 cudaError_t launch_quantize(int type, const float* x, long long rows, long long K, void* out, cudaStream_t s) {

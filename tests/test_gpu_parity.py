@@ -285,6 +285,45 @@ def test_launch_counts(qmm):
     assert qmm.matmul_launches("q6_k", "f32_act", 256, 4096, 4096) == 1
 
 
+CHAIN_SHAPES = {"q8_0": [(8192, 8192), (576, 8192), (8192, 576), (8192, 8192)],
+                "q4_k": [(8192, 8192), (512, 8192), (8192, 512), (8192, 8192)]}
+
+
+@pytest.mark.parametrize("M", [1, 4])
+@pytest.mark.parametrize("mode", ["int8_act", "f32_act"])
+@pytest.mark.parametrize("wtype", ["q8_0", "q4_k"])
+def test_chained_calls_wait_for_the_previous_output(qmm, orc, wtype, mode, M):
+    """Each call's x is the previous call's y, with no host synchronisation
+    between calls.  The decode grids are launched programmatically and stream
+    weights before the previous grid has finished; every output must still be
+    the oracle's product of the weights with the previous (complete) output.
+    The output buffers start as NaN, so a read of an unfinished output shows."""
+    shapes = CHAIN_SHAPES[wtype] * 2
+    wqs = {}
+    for N, K in set(shapes):
+        wqs[(N, K)] = orc.quantize(wtype, qmm_synth.weights(N, K, seed=N + 3 * K) * np.float32(50.0 / np.sqrt(K)))
+    wq_dev = {k: dev(v) for k, v in wqs.items()}
+    x0 = dev(qmm_synth.activations(M, shapes[0][1], seed=5))
+    ys = [torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda") for N, _ in shapes]
+    wss = [torch.empty(max(qmm.matmul_workspace(wtype, mode, M, N, K), 1), dtype=torch.uint8, device="cuda")
+           for N, K in shapes]
+    launches = [qmm.matmul_launches(wtype, mode, M, N, K) for N, K in shapes]
+    torch.cuda.synchronize()
+    x = x0
+    for (N, K), y, ws in zip(shapes, ys, wss):
+        qmm.matmul(wq_dev[(N, K)], x, wtype, mode, N=N, out=y, workspace=ws)
+        x = y
+    outs = [host(y) for y in ys]
+    xin = host(x0)
+    for i, ((N, K), y) in enumerate(zip(shapes, outs)):
+        y_orc, T = orc.matmul(wtype, mode, wqs[(N, K)], xin)
+        assert_within_bound(y, y_orc, T, f"{wtype} {mode} M{M} call {i} N{N} K{K}")
+        xin = y
+    check_device_error(qmm)
+    if not (wtype == "q8_0" and mode == "int8_act" and M == 1):  # that form runs the one-launch GEMV
+        assert max(launches) >= 2  # the chain includes a preparing kernel or a K-split reduction
+
+
 def test_error_statuses_on_device(qmm, orc):
     wq = dev(orc.quantize("q8_0", qmm_synth.weights(100, 8192)))
     x = dev(qmm_synth.activations(8, 8192))
