@@ -1,4 +1,4 @@
-// qmm_dmma.cuh -- decode matmul (M <= 8 activation rows) on warp tensor cores
+// qmm_dmma.cuh -- decode matmul (M <= 16 activation rows) on warp tensor cores
 // with 16-row weight tiles.
 //
 // Serves both forms of "同一个 GGUF，CPU 和 Metal 生成的文字不一样" section 出处
@@ -7,7 +7,7 @@
 // weights dequantized in-kernel).
 //
 // The MMA's A operand holds 16 weight rows, its B operand the activations:
-//   int8_act: B column c = activation row c (M <= 8); mma.m16n8k32 takes the
+//   int8_act: B column c of column set s = activation row 8 s + c; mma.m16n8k32 takes the
 //     raw Q8_0 codes, or the Q4_K nibbles (low as 0..15, high as 16 n), as A
 //     with no conversion.  Q8_0: y += f(d_w) f(d_a) isum per block.  Q4_K: S_sc
 //     accumulates sc_j * isum_j exactly in int32; S_m = sum_j m_j bsum_j is one
@@ -16,7 +16,7 @@
 //   f32_act: each weight unit (Q8_0 block, Q4_K super-block) of each
 //     activation row is scaled by its own power of two 2^s and split into two
 //     exact f16 pieces, x 2^s = hi + lo; B column 2r holds hi of row r and
-//     column 2r+1 its lo (a second column set serves rows 4..7).  Weight codes
+//     column 2r+1 its lo (further column sets serve rows 4..15).  Weight codes
 //     become exact f16: Q8_0 q; Q4_K sc_j * q (<= 945), the 6-bit factor
 //     folded into the conversion, so the 16 MMAs of a super-block chain in one
 //     accumulator.  The min term f(dmin) sum_j m_j X_j (X_j = the sub-block's
@@ -33,7 +33,10 @@
 // for small weight matrices (one launch), or once per call by
 // dmma_prep_kernel for large ones, whose output every CTA fetches with a few
 // bulk copies after its first weight stages are in flight (programmatic
-// dependent launch).  K is split across CTAs only when the activation rows of
+// dependent launch).  Every grid is launched programmatically: it streams its
+// first weight stages while the previous grid in the stream finishes, and
+// waits for that grid (griddepcontrol.wait) before it touches the activations
+// or starts a bounded wait.  K is split across CTAs only when the activation rows of
 // the whole K range do not fit in shared memory; the slices' partial sums then
 // go to the workspace and a second small kernel adds them in slice order.
 #pragma once
