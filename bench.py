@@ -462,8 +462,14 @@ def run_ours(args):
     torch.cuda.synchronize()
     barrier(world)
 
-    # per-call events inside the timed region (all launches go to `stream`)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)] for _ in range(args.steps)]
+    # The timed region: exactly K steps.  Consecutive calls of one (type, form, M) group
+    # (its 8 rotated buffers) run back to back with nothing recorded between them, so
+    # each call's grids are scheduled while the previous call finishes (programmatic
+    # dependent launch), as in a model's step; an event after each group (on the
+    # launching stream) attributes its time to the one kernel the group runs.
+    groups = [calls[i:i + BUFFERS] for i in range(0, len(calls), BUFFERS)]
+    assert all(len({(M, t, mode) for (M, t, mode, _) in g}) == 1 for g in groups)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(groups) + 1)] for _ in range(args.steps)]
     clocks = Clocks(local)
     clocks.start()
     start = torch.cuda.Event(enable_timing=True)
@@ -473,9 +479,10 @@ def run_ours(args):
     start.record(stream)
     for s in range(args.steps):
         ev[s][0].record(stream)
-        for i, c in enumerate(calls):
-            call(*c)
-            ev[s][i + 1].record(stream)
+        for gi, g in enumerate(groups):
+            for c in g:
+                call(*c)
+            ev[s][gi + 1].record(stream)
     stop.record(stream)
     torch.cuda.synchronize()
     ck = clocks.stop()
@@ -484,18 +491,19 @@ def run_ours(args):
     bytes_per_step = sum(wbytes[t] for (_, t, _, _) in calls)
     value = world * bytes_per_step * args.steps / (elapsed_ms / 1e3) / 1e9
 
-    # per-call durations -> per-kernel roofline and breakdown
+    # group durations -> per-kernel roofline and breakdown
     per = {}
     kern = {}  # kernel -> [algorithmic bytes, ms, launches]
     for s in range(args.steps):
-        for i, (M, t, mode, b) in enumerate(calls):
-            d = ev[s][i].elapsed_time(ev[s][i + 1])
-            ab = wbytes[t] + M * K_DEC * 4 + M * N_DEC * 4
+        for gi, g in enumerate(groups):
+            M, t, mode, _ = g[0]
+            d = ev[s][gi].elapsed_time(ev[s][gi + 1])
+            ab = len(g) * (wbytes[t] + M * K_DEC * 4 + M * N_DEC * 4)
             k = kern.setdefault(kernel_of(t, mode, M), [0.0, 0.0, 0])
             k[0] += ab
             k[1] += d
-            k[2] += 1
-            per.setdefault((t, mode, M), []).append((wbytes[t], d))
+            k[2] += len(g)
+            per.setdefault((t, mode, M), []).append((len(g) * wbytes[t], d))
     sweep = {f"{t}/{mode}/M{M}": round(sum(b for b, _ in v) / (sum(d for _, d in v) / 1e3) / 1e9, 1)
              for (t, mode, M), v in sorted(per.items())}
     dom = max(kern, key=lambda k: kern[k][1])
@@ -604,7 +612,9 @@ def run_ours(args):
                              "frac": round(achieved / hbm_peak, 4), "traffic": traffic,
                              "kernel": dom, "peak_source": f"{peak_src} hbm_gbs",
                              "alg_bytes": "weights + x f32 + y f32 per call; a call's duration includes its "
-                                          "activation-preparing launch"},
+                                          "activation-preparing launch",
+                             "durations": "CUDA events in the timed region after each group of 8 calls "
+                                          "of one type, form and M (one kernel per group)"},
                 "kernels": kernels,
                 "dequantize_all": dequant_all,
                 "cpu_baseline": cpu,
