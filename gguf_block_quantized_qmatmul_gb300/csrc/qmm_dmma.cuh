@@ -915,8 +915,8 @@ struct DmmaPlan {
 };
 
 // Weight matrices at least this large prepare the activations once per call
-// (a second, small launch); smaller ones, bound by launch latency, prepare
-// them inside the single decode launch.
+// (a second, small launch) when the batch has more than a few rows; smaller
+// ones, bound by launch latency, prepare them inside the single decode launch.
 constexpr long long kDmmaExtMinBytes = 32ll << 20;
 
 // The planner first looks for a chunk size that leaves this many stages.
@@ -1034,7 +1034,11 @@ inline bool plan_dmma(int wt, int am, long long M, long long N, long long K, int
     p.per_slice = per;
     pl.grid = per * p.kslices;
     pl.ext_bytes = 0;
-    if (ext_ok && p.total_bytes >= kDmmaExtMinBytes) {
+    // Large weights with more than a few activation rows: prepare the activations once per
+    // call in their own launch.  Up to 2 rows (4 for 32-value blocks) every CTA prepares its
+    // own slice from x (a few KB, hot in L2): measured faster on 28672 x 8192, since the
+    // separate launch would sit between the previous call's grid and this one's consumers.
+    if (ext_ok && p.total_bytes >= kDmmaExtMinBytes && M > (is_b32(wt) ? 4 : 2)) {
         auto r256 = [](long long v) { return (v + 255) / 256 * 256; };
         p.ext_codes = 0;
         long long off = r256(am == A_INT8 ? M * K : 2 * M * K * 2);

@@ -272,7 +272,9 @@ def test_launch_counts(qmm):
     preparation + decode kernel + optional K-split reduction)."""
     assert qmm.matmul_launches("q8_0", "int8_act", 1, 100, 8192) == 1     # per-thread GEMV
     assert qmm.matmul_launches("q8_0", "f32_act", 1, 100, 8192) == 1      # small: prepared in-kernel
-    assert qmm.matmul_launches("q8_0", "f32_act", 1, 28672, 8192) == 2    # large: preparing kernel first
+    assert qmm.matmul_launches("q8_0", "f32_act", 1, 28672, 8192) == 1    # large, M <= 4: each CTA prepares its slice
+    assert qmm.matmul_launches("q4_k", "f32_act", 4, 28672, 8192) == 2    # large, M > 2: preparing kernel first
+    assert qmm.matmul_launches("q4_k", "int8_act", 2, 28672, 8192) == 1
     assert qmm.matmul_launches("q4_k", "int8_act", 8, 28672, 8192) == 2
     assert qmm.matmul_launches("q8_0", "f32_act", 8, 28672, 8192) == 3    # K split: reduction after
     assert qmm.matmul_launches("q8_0", "int8_act", 256, 4096, 4096) == 2  # prefill: operand + GEMM
@@ -289,7 +291,7 @@ CHAIN_SHAPES = {"q8_0": [(8192, 8192), (576, 8192), (8192, 576), (8192, 8192)],
                 "q4_k": [(8192, 8192), (512, 8192), (8192, 512), (8192, 8192)]}
 
 
-@pytest.mark.parametrize("M", [1, 4])
+@pytest.mark.parametrize("M", [1, 5])
 @pytest.mark.parametrize("mode", ["int8_act", "f32_act"])
 @pytest.mark.parametrize("wtype", ["q8_0", "q4_k"])
 def test_chained_calls_wait_for_the_previous_output(qmm, orc, wtype, mode, M):
@@ -320,8 +322,8 @@ def test_chained_calls_wait_for_the_previous_output(qmm, orc, wtype, mode, M):
         assert_within_bound(y, y_orc, T, f"{wtype} {mode} M{M} call {i} N{N} K{K}")
         xin = y
     check_device_error(qmm)
-    if not (wtype == "q8_0" and mode == "int8_act" and M == 1):  # that form runs the one-launch GEMV
-        assert max(launches) >= 2  # the chain includes a preparing kernel or a K-split reduction
+    if M > 4:  # the 8192 x 8192 calls prepare their activations in a launch of their own
+        assert max(launches) >= 2
 
 
 def test_error_statuses_on_device(qmm, orc):
