@@ -32,9 +32,10 @@ template <int WT, int AM>
 cudaError_t prep(const DmmaPlan& pl, void* ext, cudaStream_t s) {
     const DmmaParams& p = pl.p;
     long long blocks;
-    if (AM == A_F32) blocks = p.M;                                            // a block per row
-    else if (WT == T_Q8_0) blocks = ((long long)p.M * p.units + kPrepThreads - 1) / kPrepThreads;  // a thread per 32-block
-    else blocks = ((long long)p.M * p.units + kPrepThreads / 32 - 1) / (kPrepThreads / 32);       // a warp per super-block
+    constexpr int warps = kPrepThreads / 32;
+    if (AM == A_F32 && WT == T_Q8_0) blocks = ((long long)p.M * ((p.units + 7) / 8) + warps - 1) / warps;  // a warp per 8 blocks
+    else if (WT == T_Q8_0) blocks = ((long long)p.M * p.units + kPrepThreads - 1) / kPrepThreads;        // a thread per 32-block
+    else blocks = ((long long)p.M * p.units + warps - 1) / warps;                                         // a warp per super-block
     if (blocks > 1024) blocks = 1024;
     // programmatic dependent launch: scheduled while the previous grid in the
     // stream (normally the last call's decode grid) still runs; the kernel
