@@ -289,30 +289,29 @@ def test_launch_counts(qmm):
 
 CHAIN_SHAPES = {"q8_0": [(8192, 8192), (576, 8192), (8192, 576), (8192, 8192)],
                 "q4_k": [(8192, 8192), (512, 8192), (8192, 512), (8192, 8192)]}
+PREFILL_CHAIN_SHAPES = [(1024, 1024), (768, 1024), (1024, 768), (1024, 1024)]
 
 
-@pytest.mark.parametrize("M", [1, 5])
-@pytest.mark.parametrize("mode", ["int8_act", "f32_act"])
-@pytest.mark.parametrize("wtype", ["q8_0", "q4_k"])
-def test_chained_calls_wait_for_the_previous_output(qmm, orc, wtype, mode, M):
+def run_chain(qmm, orc, wtype, mode, M, shapes):
     """Each call's x is the previous call's y, with no host synchronisation
-    between calls.  The decode grids are launched programmatically and stream
-    weights before the previous grid has finished; every output must still be
-    the oracle's product of the weights with the previous (complete) output.
-    The output buffers start as NaN, so a read of an unfinished output shows."""
-    shapes = CHAIN_SHAPES[wtype] * 2
+    between calls and one workspace shared by all of them.  Grids are launched
+    programmatically and read weights before the previous grid has finished;
+    every output must still be the oracle's product of the weights with the
+    previous (complete) output.  The outputs start as NaN, so a read of an
+    unfinished output shows; so does a workspace overwritten too early."""
+    shapes = shapes * 2
     wqs = {}
     for N, K in set(shapes):
         wqs[(N, K)] = orc.quantize(wtype, qmm_synth.weights(N, K, seed=N + 3 * K) * np.float32(50.0 / np.sqrt(K)))
     wq_dev = {k: dev(v) for k, v in wqs.items()}
     x0 = dev(qmm_synth.activations(M, shapes[0][1], seed=5))
     ys = [torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda") for N, _ in shapes]
-    wss = [torch.empty(max(qmm.matmul_workspace(wtype, mode, M, N, K), 1), dtype=torch.uint8, device="cuda")
-           for N, K in shapes]
+    ws = torch.empty(max(max(qmm.matmul_workspace(wtype, mode, M, N, K) for N, K in shapes), 16), dtype=torch.uint8,
+                     device="cuda")
     launches = [qmm.matmul_launches(wtype, mode, M, N, K) for N, K in shapes]
     torch.cuda.synchronize()
     x = x0
-    for (N, K), y, ws in zip(shapes, ys, wss):
+    for (N, K), y in zip(shapes, ys):
         qmm.matmul(wq_dev[(N, K)], x, wtype, mode, N=N, out=y, workspace=ws)
         x = y
     outs = [host(y) for y in ys]
@@ -322,8 +321,26 @@ def test_chained_calls_wait_for_the_previous_output(qmm, orc, wtype, mode, M):
         assert_within_bound(y, y_orc, T, f"{wtype} {mode} M{M} call {i} N{N} K{K}")
         xin = y
     check_device_error(qmm)
+    return launches
+
+
+@pytest.mark.parametrize("M", [1, 5])
+@pytest.mark.parametrize("mode", ["int8_act", "f32_act"])
+@pytest.mark.parametrize("wtype", ["q8_0", "q4_k"])
+def test_chained_calls_wait_for_the_previous_output(qmm, orc, wtype, mode, M):
+    launches = run_chain(qmm, orc, wtype, mode, M, CHAIN_SHAPES[wtype])
     if M > 4:  # the 8192 x 8192 calls prepare their activations in a launch of their own
         assert max(launches) >= 2
+
+
+@pytest.mark.parametrize("M", [37, 300])
+@pytest.mark.parametrize("mode", ["int8_act", "f32_act"])
+@pytest.mark.parametrize("wtype", ["q8_0", "q4_k"])
+def test_chained_prefill_calls_wait_for_the_previous_output(qmm, orc, wtype, mode, M):
+    """The same chain on the tcgen05 GEMM, whose preparing grid reads the
+    weights' row scales before the previous GEMM has finished."""
+    launches = run_chain(qmm, orc, wtype, mode, M, PREFILL_CHAIN_SHAPES)
+    assert min(launches) == 2  # operand preparation + GEMM
 
 
 def test_error_statuses_on_device(qmm, orc):
