@@ -2,7 +2,7 @@
 //
 // Built and run by tests/test_plans.py on the CPU (no GPU is touched: only the
 // inline host planners of the kernel headers are called).  For a grid of
-// shapes it checks that every plan the decode, GEMV and tcgen05 planners
+// shapes it checks that every plan the decode, GEMV, streaming and tcgen05 planners
 // return fits the device limits it was planned for and keeps the layout rules
 // its kernel relies on: shared-memory regions in order and inside the
 // allocation, at least the ring depth the kernel assumes, one CTA per SM, K
@@ -125,6 +125,33 @@ int check_tc(int wt, long long M, long long N, long long K) {
 #undef CASE
     return 1;
 }
+
+int check_stream(int wt, int am, int epi, long long M, long long N, long long K) {
+    StreamPlan pl;
+    if (!plan_stream(wt, am, epi, M, N, K, kSms, kSmem, pl)) return 0;
+    const StreamParams& p = pl.p;
+    const int ub = unit_bytes(wt);
+#define CASE "stream %s am%d epi%d M%lld N%lld K%lld", tname(wt), am, epi, M, N, K
+    CHECK(pl.smem <= (size_t)kSmem, CASE);
+    CHECK(p.stages >= 2 && p.stages <= 8, CASE);
+    CHECK(p.off_flags >= 128 && p.off_flags < p.off_codes && p.off_codes <= p.off_scale && p.off_scale <= p.off_aux &&
+              p.off_aux <= p.off_rs && p.off_rs <= p.off_red && p.off_red < p.off_stage,
+          CASE);
+    CHECK((size_t)p.off_stage + (size_t)p.stages * kTileRows * p.row_stride <= pl.smem, CASE);
+    CHECK(p.row_stride >= p.ups * ub + 32 && p.row_stride % 128 == 16, CASE);
+    CHECK(p.kslices >= 1 && (long long)(p.kslices - 1) * p.slice_units < p.units &&
+              (long long)p.kslices * p.slice_units >= p.units,
+          CASE);
+    CHECK(p.ups >= 1 && p.ups <= p.slice_units, CASE);
+    CHECK((long long)p.mr * p.mchunks >= M && p.pairs == p.kslices * p.mchunks, CASE);
+    CHECK(pl.grid == p.pairs * p.per_pair && p.per_pair >= 1 && p.per_pair <= p.ntiles, CASE);
+    CHECK(pl.workspace == ((epi == E_Y && p.kslices > 1)
+                               ? (size_t)p.kslices * M * N * 4 + (size_t)p.mchunks * p.ntiles * 4 + 256
+                               : 0),
+          CASE);
+#undef CASE
+    return 1;
+}
 }  // namespace
 
 int main() {
@@ -154,6 +181,17 @@ int main() {
                 for (long long K : {256, 1024, 4096, 14336})
                     plans += check_tc(wt, M, N, K);
     }
+    for (int wt : types)
+        for (int am : {A_INT8, A_F32})
+            for (int epi : {E_Y, E_SUMS}) {
+                if (epi == E_SUMS && am == A_F32) continue;  // block sums are an int8_act hook
+                for (long long M : {1, 9, 17, 37, 64, 100, 300, 1024})
+                    for (long long N : {1, 33, 576, 4096, 14336})
+                        for (long long K : {32, 576, 1536, 4096, 14336}) {
+                            if (K % (is_b32(wt) ? 32 : 256)) continue;
+                            plans += check_stream(wt, am, epi, M, N, K);
+                        }
+            }
     // the shapes the benchmark and the tests depend on must have plans
     DmmaPlan dp;
     for (int wt : types)
