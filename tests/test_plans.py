@@ -1,8 +1,9 @@
 """The launch planners' invariants, on the CPU: tests/plan_invariants.cu calls
 the inline host planners of the kernel headers (decode warp-MMA kernel, dp4a
-GEMV, streaming warp-MMA kernel, tcgen05 GEMM) over a grid of shapes and checks every plan against the
-device limits it was made for (GB300: 152 SMs, 227 KB of shared memory per
-block) and the layout rules its kernel relies on.  No GPU is touched."""
+GEMV, streaming warp-MMA kernel, tcgen05 GEMM) over a grid of shapes and
+checks every plan against the device limits it was made for (GB300: 152 SMs,
+227 KB of shared memory per block) and the layout rules its kernel relies on.
+No GPU is touched."""
 import os
 import subprocess
 
