@@ -26,8 +26,9 @@
  *    are programmatic dependent launches: when the previous kernel in the
  *    stream is one of this library's, they may start while it finishes and
  *    read the quantized weights early, but they wait for it to complete
- *    before they read x, write y or touch the workspace.  (A kernel of the
- *    caller's always completes first, so it may write the weights.)
+ *    before they read x, write y or touch the workspace.  A caller's kernel
+ *    that does not itself trigger dependents early (griddepcontrol
+ *    .launch_dependents) completes first, so it may write the weights.
  *  - Matrices are row-major.  W is [N, K] (N output rows, K input channels,
  *    the GGUF / Linear convention), x is [M, K], y = x . W^T is [M, N].
  *    Blocks run along K inside a row; a quantized matrix is N rows of
