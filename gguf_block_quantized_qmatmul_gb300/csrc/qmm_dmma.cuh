@@ -256,9 +256,8 @@ __device__ __forceinline__ void prep_items(const float* x, int M, int K, int u0,
     }
 }
 
-// Small blocks: beside a running decode CTA (96 registers x 576 threads) an SM
-// has room for a 128-thread block, so the preparing grid is resident across
-// many SMs before the previous grid ends and starts the moment it does.
+// Small blocks spread the preparation over many SMs as soon as the previous
+// grid's CTAs leave them (measured faster than 1024-thread blocks).
 constexpr int kPrepThreads = 128;
 
 // Once per call, for large weight matrices: the whole K range into ext.
