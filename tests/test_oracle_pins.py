@@ -696,3 +696,102 @@ def test_x0_block_sums_equal_brute_force(orc, t, off, K):
     a = np.stack([py_decode_q8_0(xq[m], K)[1] for m in range(M)]).astype(np.int64).reshape(M, K // 32, 32)
     ref = np.einsum("nbi,mbi->mnb", ci, a)
     assert np.array_equal(orc.block_sums(t, wq, xq, M, N, K), ref.astype(np.int32))
+
+
+# ---------------------------------------------------------------------------
+# The CPU form's float combine, pinned exactly: y equals the float64 dot of
+# the exactly dequantized weight rows and activation rows, both read from
+# the bytes by the Python readers above (not by the oracle's own unpacking)
+# ---------------------------------------------------------------------------
+
+def py_decode_x0(row: np.ndarray, K: int, t: str):
+    """Q4_0 / Q5_0 block: f16 d, (Q5_0) a little-endian 32-bit word whose bit
+    i is bit 4 of code i, then 16 bytes with code j in the low nibble of byte
+    j and code j + 16 in the high nibble.  Returns f(d) and the signed codes
+    (code - 8 for Q4_0, code - 16 for Q5_0)."""
+    bb, off = (18, 8) if t == "q4_0" else (22, 16)
+    blocks = row.reshape(K // 32, bb)
+    d = py_f16(blocks[:, 0].astype(np.uint16) | (blocks[:, 1].astype(np.uint16) << 8))
+    nib = blocks[:, bb - 16:].astype(np.int64)
+    q = np.concatenate([nib & 0xF, nib >> 4], axis=1)
+    if t == "q5_0":
+        qh = (blocks[:, 2].astype(np.int64) | (blocks[:, 3].astype(np.int64) << 8)
+              | (blocks[:, 4].astype(np.int64) << 16) | (blocks[:, 5].astype(np.int64) << 24))
+        q |= ((qh[:, None] >> np.arange(32)[None, :]) & 1) << 4
+    return d, q - off
+
+
+def _py_dequant_f64(t: str, wq: np.ndarray, K: int) -> np.ndarray:
+    """Dequantized weights in float64 from the Python readers: f(d) q for the
+    32-value types, f(d) sc_j q - f(dmin) m_j for Q4_K (no f32 rounding
+    anywhere: every product is exact in float64)."""
+    out = np.zeros((wq.shape[0], K))
+    for n in range(wq.shape[0]):
+        if t == "q8_0":
+            d, q = py_decode_q8_0(wq[n], K)
+            out[n] = (d[:, None].astype(np.float64) * q).ravel()
+        elif t in ("q4_0", "q5_0"):
+            d, q = py_decode_x0(wq[n], K, t)
+            out[n] = (d[:, None].astype(np.float64) * q).ravel()
+        else:
+            D, Dm, sc, mn, q = py_decode_q4_k(wq[n], K)
+            e = D[:, None].astype(np.float64) * sc            # [nsb, 8]
+            o = Dm[:, None].astype(np.float64) * mn
+            out[n] = (np.repeat(e, 32, axis=1) * q - np.repeat(o, 32, axis=1)).ravel()
+    return out
+
+
+def _py_act_f64(atype: str, xq: np.ndarray, K: int) -> np.ndarray:
+    """Dequantized activation rows d_a q_a in float64 (Q8_0: f16 d; Q8K: f32 d)."""
+    out = np.zeros((xq.shape[0], K))
+    for m in range(xq.shape[0]):
+        if atype == "q8_0":
+            d, q = py_decode_q8_0(xq[m], K)
+        else:
+            d, q, _ = py_decode_q8_k(xq[m], K)
+        out[m] = (d[:, None].astype(np.float64) * q).ravel()
+    return out
+
+
+@pytest.mark.parametrize("wtype,K", [("q8_0", 576), ("q4_0", 576), ("q5_0", 576), ("q4_k", 1536),
+                                     ("q8_0", 1536), ("q4_k", 512)])
+def test_int8_act_is_the_dequantized_dot(orc, wtype, K):
+    """The CPU form's float combine equals, to float64 rounding, the dot of
+    the exactly dequantized weights with the exactly dequantized activation
+    codes.  A misplaced scale, a dropped min term, a wrong sub-block index,
+    or f(d) S rounded through f32 (a relative error near 6e-8) fails the
+    1e-12 bound; adversarial rows are in both operands."""
+    w = np.concatenate([qmm_synth.weights(40, K, seed=31), qmm_synth.special_block_rows(K)])
+    x = np.concatenate([qmm_synth.activations(3, K, seed=32), qmm_synth.special_block_rows(K)[1:6]])
+    wq = orc.quantize(wtype, w)
+    atype = "q8_k" if wtype == "q4_k" else "q8_0"
+    xq = orc.quantize(atype, x)
+    y, T = orc.matmul(wtype, "int8_act", wq, x)
+    W = _py_dequant_f64(wtype, wq, K)
+    X = _py_act_f64(atype, xq, K)
+    ref = X @ W.T
+    scale = np.abs(X) @ np.abs(W).T
+    assert np.all(np.abs(y - ref) <= 1e-12 * scale + 1e-300)
+    # T is the sum of |scaled block terms|: at least |y|, and at most the sum of
+    # |element products| (for Q4_K with the scale and min parts taken apart)
+    assert (np.abs(y) <= T * (1 + 1e-12)).all()
+    if wtype == "q4_k":
+        parts = np.zeros_like(W)
+        for n in range(wq.shape[0]):
+            D, Dm, sc, mn, q = py_decode_q4_k(wq[n], K)
+            e = np.repeat(D[:, None].astype(np.float64) * sc, 32, axis=1)
+            o = np.repeat(Dm[:, None].astype(np.float64) * mn, 32, axis=1)
+            parts[n] = (np.abs(e * q) + o).ravel()
+        scale = np.abs(X) @ parts.T
+    assert (T <= scale * (1 + 1e-12) + 1e-300).all()
+
+
+@pytest.mark.parametrize("t", ["q4_0", "q5_0"])
+def test_x0_layout_decode_matches_python_reader(orc, t):
+    """The oracle's dequantization of Q4_0 / Q5_0 bytes equals the Python
+    reader's f(d) (code - off): a swapped nibble order or a misread fifth
+    bit fails."""
+    K = 576
+    w = np.concatenate([qmm_synth.weights(32, K, seed=33), qmm_synth.special_block_rows(K)])
+    wq = orc.quantize(t, w)
+    assert np.array_equal(orc.dequantize(t, wq, K).astype(np.float64), _py_dequant_f64(t, wq, K))
