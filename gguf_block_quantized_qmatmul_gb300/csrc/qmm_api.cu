@@ -80,13 +80,12 @@ size_t workspace_for(const StreamPlan& pl) {
 // The kernel a matmul call dispatches to and its plan.  Planning searches
 // chunk sizes and K splits, so decisions are cached per host thread by
 // (device, type, form, epilogue, M, N, K).
-enum Kind { KIND_NONE, KIND_GEMV, KIND_DMMA, KIND_TC, KIND_PREFILL, KIND_STREAM };
+enum Kind { KIND_NONE, KIND_GEMV, KIND_DMMA, KIND_TC, KIND_STREAM };
 struct Dispatch {
     Kind kind = KIND_NONE;
     GemvPlan gp;
     DmmaPlan dp;
     TcPlan tp;
-    PrefillPlan fp;
     StreamPlan sp;
     size_t workspace = 0;
     int launches = 0;
@@ -123,10 +122,6 @@ void plan_dispatch(int wt, int am, int epi, long long M, long long N, long long 
         d.kind = KIND_TC;
         d.workspace = d.tp.workspace;
         d.launches = 2;  // operand preparation, GEMM
-    } else if (epi == E_Y && plan_prefill(wt, am, M, N, K, sms, smem, d.fp)) {  // prefill: warp-MMA GEMM
-        d.kind = KIND_PREFILL;
-        d.workspace = d.fp.workspace;
-        d.launches = 2;  // activation operand, GEMM
     } else if (plan_stream(wt, am, epi, M, N, K, sms, smem, d.sp)) {
         d.kind = KIND_STREAM;
         d.workspace = epi == E_Y ? workspace_for(d.sp) : 0;
@@ -204,13 +199,6 @@ qmm_status stream_call(qmm_type wtype, int am, int epi, const void* wq, const fl
         TcPlan tp = d.tp;
         tp.p.err = err;
         return launch_tc(wt, am, tp, wq, x, ws, y, smem, s) == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
-    }
-    if (d.kind == KIND_PREFILL) {
-        PrefillPlan fp = d.fp;
-        fp.p.y = y;
-        fp.p.err = err;
-        if (!ws || ws_bytes < fp.workspace) return QMM_ERR_WORKSPACE;
-        return launch_prefill(am, fp, wq, x, ws, smem, s) == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
     }
     if (d.kind != KIND_STREAM) return QMM_ERR_SHAPE;
     StreamPlan pl = d.sp;

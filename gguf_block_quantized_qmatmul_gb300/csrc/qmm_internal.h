@@ -5,7 +5,6 @@
 
 #include "qmm_dmma.cuh"
 #include "qmm_gemv.cuh"
-#include "qmm_prefill.cuh"
 #include "qmm_tc.cuh"
 #include "qmm_stream.cuh"
 
@@ -27,8 +26,6 @@ cudaError_t launch_dmma_q6_k(int am, int epi, const DmmaPlan& plan, int smem_max
 cudaError_t launch_dmma_prep(int wt, int am, const DmmaPlan& plan, void* ext, cudaStream_t s);
 cudaError_t launch_tc(int wt, int am, const TcPlan& plan, const void* wq, const float* x, void* ws, float* y, int smem_max,
                       cudaStream_t s);
-cudaError_t launch_prefill(int am, const PrefillPlan& plan, const void* wq, const float* x, void* ws, int smem_max,
-                           cudaStream_t s);
 
 // many independent small matmuls in one launch (qmm_batch.cu)
 constexpr int kBatchMax = 256;  // items per launch (the launch parameters carry the table)

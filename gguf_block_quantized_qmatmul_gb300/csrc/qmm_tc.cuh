@@ -44,9 +44,17 @@
 #include <cuda.h>
 
 #include "qmm_device.cuh"
-#include "qmm_prefill.cuh"
 
 namespace qmm {
+
+// load one TMA box (2-D) into shared memory, completing on an mbarrier
+__device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            dst),
+        "l"(map), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
 
 constexpr int kTcBW = 128;      // weight rows per tile (MMA M, the TMEM lanes)
 constexpr int kTcBXMax = 256;   // activation rows per tile, at most (MMA N)

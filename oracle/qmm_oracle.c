@@ -25,8 +25,7 @@
  *  6-bit sub-block scales and mins, 128 bytes of 4-bit codes; f32 d, int8
  *  codes, 16 int16 sums of 16 codes) follow the public GGUF layout.
  *
- * Readings where the pages are silent (listed with the others in the design
- * notes): Q4_0, Q5_0 and Q6_K use the public GGUF block layouts and the
+ * Readings where the pages are silent: Q4_0, Q5_0 and Q6_K use the public GGUF block layouts and the
  * signed-max quantizers written below; rounding of codes is round-half-away-from-zero (C roundf); codes of
  * Q8_0/Q8K use the f32 scale d and the reciprocal 1/d; Q8K is symmetric
  * (+-127); Q4_K uses the closed-form min/max quantizer written below; the

@@ -6,7 +6,9 @@ products): it only draws f32 weights and activations with the shapes and value
 distributions of the workloads, so that both the CUDA path and the CPU oracle
 receive the same host buffers.
 
-Distributions (a reading of the workloads; the design notes list it):
+Distributions (the workloads name only "N(0, 0.02), 1% of columns x8" for
+weights and "N(0, 1), 4 outlier channels x20" for prefill activations; this
+is the plain reading of those phrases):
   * weights W [N, K] ~ N(0, 0.02^2) drawn in float64 and rounded to float32;
     round(0.01 * K) input columns (k indices), chosen by a seeded permutation,
     are multiplied by 8 ("1% of columns x8 outliers");
