@@ -36,9 +36,12 @@ __device__ __forceinline__ void q8_scale(float amax, float& d, float& id) {
     id = d != 0.0f ? __fdiv_rn(1.0f, d) : 0.0f;
 }
 
-// nearest integer (ties away from zero) of x * id, clamped to [-127, 127]
+// nearest integer (ties away from zero) of x * id, clamped to [-127, 127];
+// 0 where the product is NaN (0 * inf: a zero in a block so small that the
+// f32 reciprocal of its scale overflows; x / d = 0 there)
 __device__ __forceinline__ int q8_code(float x, float id) {
     float r = roundf(__fmul_rn(x, id));
+    r = r == r ? r : 0.0f;
     r = fminf(fmaxf(r, -127.0f), 127.0f);
     return (int)r;
 }
@@ -121,17 +124,46 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Bounded wait on an mbarrier phase.  Gives up after ~2^31 SM clocks (about
-// a second), or at once when another warp of the block already gave up; on
-// giving up it raises the device error word and the block-wide abort flag.
+// Spin limit of a bounded wait in SM clocks: 2^31 (about a second), unless
+// the word after the device error word holds a smaller log2 (a test hook of
+// the host library lowers it so that an injected stall ends in milliseconds).
+__device__ __forceinline__ long long wait_limit(const unsigned* err) {
+    const unsigned lg = *reinterpret_cast<const volatile unsigned*>(err + 1);
+    return 1ll << (lg == 0u || lg > 31u ? 31u : lg);
+}
+
+// Bounded wait on an mbarrier phase.  Gives up after wait_limit() SM clocks,
+// or at once when another warp of the block already gave up; on giving up it
+// raises the device error word and the block-wide abort flag.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                           unsigned* err) {
     if (mbar_try(bar, parity)) return true;
-    long long t0 = clock64();
+    const long long lim = wait_limit(err);
+    const long long t0 = clock64();
     while (true) {
         if (mbar_try(bar, parity)) return true;
         if (*abort_flag) return false;
-        if (clock64() - t0 > (1ll << 31)) {
+        if (clock64() - t0 > lim) {
+            atomicOr(err, ERR_TIMEOUT);
+            *abort_flag = 1;
+            return false;
+        }
+    }
+}
+
+// Bounded wait for a phase whose arrivals were certainly issued (a copy or an
+// MMA commit of this block), ignoring the abort flag: a producer calls it for
+// each of its copies still in flight before the block exits, so that even on
+// the abort path nothing is still writing the block's shared or tensor memory
+// when it is released.
+__device__ __forceinline__ bool mbar_drain(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                           unsigned* err) {
+    if (mbar_try(bar, parity)) return true;
+    const long long lim = wait_limit(err);
+    const long long t0 = clock64();
+    while (true) {
+        if (mbar_try(bar, parity)) return true;
+        if (clock64() - t0 > lim) {
             atomicOr(err, ERR_TIMEOUT);
             *abort_flag = 1;
             return false;

@@ -161,8 +161,11 @@ __global__ void quant_x_0_kernel(const float* __restrict__ x, long long nblocks,
     const float id = d != 0.0f ? __fdiv_rn(1.0f, d) : 0.0f;
     int c[32];
 #pragma unroll
-    for (int k = 0; k < 32; ++k)
-        c[k] = (int)fminf(fmaxf(__fadd_rn(roundf(__fmul_rn(v[k], id)), (float)OFF), 0.0f), (float)(2 * OFF - 1));
+    for (int k = 0; k < 32; ++k) {
+        float t = roundf(__fmul_rn(v[k], id));
+        t = t == t ? t : 0.0f;  // 0 * inf (a zero where 1/d overflows): x / d = 0
+        c[k] = (int)fminf(fmaxf(__fadd_rn(t, (float)OFF), 0.0f), (float)(2 * OFF - 1));
+    }
     uint16_t* o = reinterpret_cast<uint16_t*>(out + i * BYTES);  // 2-byte aligned block
     o[0] = (uint16_t)f2h(d);
     int q0 = 1;

@@ -196,6 +196,7 @@ static void q8_0_block(const float* x, uint8_t* out) {
     for (int i = 0; i < 32; ++i) {
         float v = x[i] * id;
         float r = roundf(v);
+        if (r != r) r = 0.0f;  /* 0 * inf: a zero in a block whose reciprocal overflows; x/d = 0 */
         if (r > 127.0f) r = 127.0f;
         if (r < -127.0f) r = -127.0f;
         out[2 + i] = (uint8_t)(int8_t)(int)r;
@@ -223,6 +224,7 @@ static void q8_k_block(const float* x, uint8_t* out) {
     int8_t q[256];
     for (int i = 0; i < 256; ++i) {
         float r = roundf(x[i] * id);
+        if (r != r) r = 0.0f;  /* 0 * inf: a zero in a block whose reciprocal overflows; x/d = 0 */
         if (r > 127.0f) r = 127.0f;
         if (r < -127.0f) r = -127.0f;
         q[i] = (int8_t)(int)r;
@@ -268,7 +270,9 @@ static void x_0_block(const float* x, int off, uint8_t* out) {
     put_u16(out, orc_f32_to_f16(d));
     int c[32];
     for (int i = 0; i < 32; ++i) {
-        float r = roundf(x[i] * id) + (float)off;
+        float t = roundf(x[i] * id);
+        if (t != t) t = 0.0f;  /* 0 * inf: a zero in a block whose reciprocal overflows; x/d = 0 */
+        float r = t + (float)off;
         if (r < 0.0f) r = 0.0f;
         if (r > (float)(2 * off - 1)) r = (float)(2 * off - 1);
         c[i] = (int)r;

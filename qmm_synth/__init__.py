@@ -69,7 +69,9 @@ def smollm2_linears():
 def special_block_rows(K: int, seed: int = 7) -> np.ndarray:
     """A small set of adversarial rows used by edge-case tests: zeros, constants,
     one-hot values, ties at +-0.5 code steps, all-negative and all-positive
-    blocks, tiny and huge magnitudes, +-127 and random integer blocks."""
+    blocks, tiny and huge magnitudes, +-127 and random integer blocks, and
+    values near the bottom of the f32 range (normal and subnormal, where the
+    f32 reciprocal of a block scale overflows) mixed with zeros."""
     r = _rng(seed)
     rows = [np.zeros(K), np.full(K, 0.75), np.full(K, -3.0)]
     oh = np.zeros(K); oh[r.integers(K)] = 1.5; rows.append(oh)
@@ -86,4 +88,6 @@ def special_block_rows(K: int, seed: int = 7) -> np.ndarray:
     ints = r.integers(-127, 128, K).astype(np.float64)
     ints[::32] = 127.0
     rows.append(ints)
+    rows.append(r.standard_normal(K) * 1e-30)
+    rows.append(np.where(r.random(K) < 0.5, 0.0, r.standard_normal(K) * 1e-38))
     return np.asarray(rows, dtype=np.float32)

@@ -185,8 +185,12 @@ def test_q8_0_scale_rule_and_codes(orc):
         nz = amax > 0
         ext = np.abs(codes[nz][np.arange(nz.sum()), np.abs(blocks[nz]).argmax(axis=1)])
         assert (ext == 127).all()
-        ratio = blocks[nz].astype(np.float64) / d[nz, None].astype(np.float64)
-        assert (np.abs(codes[nz] - ratio) <= 0.5 + 1e-4).all()
+        # blocks whose f32 reciprocal 1/d overflows (amax below ~3.7e-37) leave the
+        # nearest-integer property: their codes are pinned by the overflow test below
+        with np.errstate(divide="ignore", over="ignore"):
+            fin = nz & np.isfinite(np.float32(1.0) / d)
+        ratio = blocks[fin].astype(np.float64) / d[fin, None].astype(np.float64)
+        assert (np.abs(codes[fin] - ratio) <= 0.5 + 1e-4).all()
         assert (codes[~nz] == 0).all()
 
 
@@ -211,7 +215,11 @@ def test_q8_k_fields(orc):
         assert np.array_equal(d, np.abs(blocks).max(axis=1) / np.float32(127.0))
         assert np.array_equal(bs, codes.reshape(-1, 16, 16).sum(axis=2))
         ok = d > 0
-        assert (np.abs(codes[ok] - blocks[ok].astype(np.float64) / d[ok, None]) <= 0.5 + 1e-4).all()
+        # where the f32 reciprocal 1/d overflows, codes leave the nearest-integer
+        # property (pinned by the overflow test below)
+        with np.errstate(divide="ignore", over="ignore"):
+            fin = ok & np.isfinite(np.float32(1.0) / d)
+        assert (np.abs(codes[fin] - blocks[fin].astype(np.float64) / d[fin, None]) <= 0.5 + 1e-4).all()
         assert (codes[~ok] == 0).all()
 
 
@@ -243,7 +251,9 @@ def test_round_trip_bounds(orc):
     w = orc.dequantize("q8_k", q, K)
     b = x.reshape(-1, 256).astype(np.float64)
     amax = np.abs(b).max(axis=1, keepdims=True)
-    assert (np.abs(b - w.reshape(-1, 256)) <= amax / 254.0 + 2.0 ** -20 * amax).all()
+    with np.errstate(divide="ignore", over="ignore"):  # blocks whose f32 1/d overflows: the overflow test
+        fin = np.isfinite(np.float32(1.0) / (amax.astype(np.float32) / np.float32(127.0)))[:, 0]
+    assert (np.abs(b - w.reshape(-1, 256))[fin] <= (amax / 254.0 + 2.0 ** -20 * amax)[fin]).all()
     # Q4_K
     q = orc.quantize("q4_k", x)
     w = orc.dequantize("q4_k", q, K).astype(np.float64)
@@ -795,3 +805,31 @@ def test_x0_layout_decode_matches_python_reader(orc, t):
     w = np.concatenate([qmm_synth.weights(32, K, seed=33), qmm_synth.special_block_rows(K)])
     wq = orc.quantize(t, w)
     assert np.array_equal(orc.dequantize(t, wq, K).astype(np.float64), _py_dequant_f64(t, wq, K))
+
+
+@pytest.mark.parametrize("t", ["q8_0", "q8_k", "q4_0", "q5_0"])
+def test_zero_in_a_block_whose_reciprocal_overflows_gets_code_zero(orc, t):
+    """Codes are round(x * (1/d)) with the f32 reciprocal.  For a block whose
+    largest magnitude is near the bottom of the f32 range, 1/d overflows to
+    infinity: nonzero values then take the extreme codes, and a zero value
+    takes code 0 (x / d = 0), not the NaN of 0 * inf."""
+    K = 256
+    x = np.zeros((1, K), np.float32)
+    x[0, 3], x[0, 5], x[0, 40] = 1e-38, -5e-39, 2e-39
+    q = orc.quantize(t, x)
+    if t == "q8_0":
+        codes = np.concatenate([py_decode_q8_0(q[0], K)[1][b] for b in range(K // 32)])
+        zero, pos, neg = 0, 127, -127
+    elif t == "q8_k":
+        codes = py_decode_q8_k(q[0], K)[1].ravel()
+        zero, pos, neg = 0, 127, -127
+    else:
+        codes = py_decode_x0(q[0], K, t)[1].ravel()
+        off = 8 if t == "q4_0" else 16
+        # d = m / -off: the extreme value m = 1e-38 takes code -off, the opposite sign the top code
+        zero, pos, neg = 0, -off, off - 1
+    assert codes[3] == pos and codes[5] == neg
+    nz = np.zeros(K, bool)
+    nz[[3, 5, 40]] = True
+    blk0 = np.arange(K) < 32
+    assert (codes[~nz & blk0] == zero).all()
