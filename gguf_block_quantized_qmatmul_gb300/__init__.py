@@ -34,8 +34,9 @@ STATUS = {0: "QMM_OK", 1: "QMM_ERR_NULL", 2: "QMM_ERR_SHAPE", 3: "QMM_ERR_TYPE",
 # every symbol declared in include/qmm.h
 EXPORTS = ["qmm_block_values", "qmm_block_bytes", "qmm_row_bytes", "qmm_quantize_weights", "qmm_quantize_act",
            "qmm_dequantize", "qmm_matmul_workspace", "qmm_matmul_launches", "qmm_matmul", "qmm_matmul_static_workspace",
-           "qmm_block_sums", "qmm_matmul_batch",
+           "qmm_block_sums", "qmm_matmul_batch", "qmm_test_inject", "qmm_test_set_wait_limit",
            "qmm_last_device_error", "qmm_status_string"]
+INJECT = {"off": 0, "launch_failure": 1, "stall": 2}
 
 
 class QmmError(RuntimeError):
@@ -62,6 +63,8 @@ def _load() -> ctypes.CDLL:
     lib.qmm_matmul.argtypes, lib.qmm_matmul.restype = [i32, i32, p, p, p, i64, i64, i64, p, sz, p], i32
     lib.qmm_block_sums.argtypes, lib.qmm_block_sums.restype = [i32, p, p, i64, i64, i64, p, p], i32
     lib.qmm_matmul_batch.argtypes, lib.qmm_matmul_batch.restype = [i32, i32, p, i64, p], i32
+    lib.qmm_test_inject.argtypes, lib.qmm_test_inject.restype = [i32, i32, i32], i32
+    lib.qmm_test_set_wait_limit.argtypes, lib.qmm_test_set_wait_limit.restype = [i32], i32
     lib.qmm_last_device_error.argtypes, lib.qmm_last_device_error.restype = [], i32
     lib.qmm_status_string.argtypes, lib.qmm_status_string.restype = [i32], ctypes.c_char_p
     return lib
@@ -211,3 +214,17 @@ def matmul_batch(items, wtype, mode, stream=None):
 
 def last_device_error() -> int:
     return int(_lib().qmm_last_device_error())
+
+
+def test_inject(kind: str, count: int = 1, arg: int = 0) -> None:
+    """Failure-test hook: arm an injected failure ("launch_failure": the next
+    `count` matmul calls return QMM_ERR_CUDA without touching the device;
+    "stall": the next decode-kernel launch withholds its first block's weight
+    stages from stage `arg` on, so a bounded wait times out; "off")."""
+    _check(_lib().qmm_test_inject(INJECT[kind], count, arg), "qmm_test_inject")
+
+
+def test_set_wait_limit(log2_clocks: int) -> None:
+    """Failure-test hook: spin limit of the device's bounded waits, 2^log2
+    SM clocks (0 restores the default of about one second)."""
+    _check(_lib().qmm_test_set_wait_limit(log2_clocks), "qmm_test_set_wait_limit")

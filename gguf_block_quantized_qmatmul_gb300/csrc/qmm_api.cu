@@ -1,6 +1,7 @@
 // qmm_api.cu -- the C ABI (include/qmm.h): argument checks, planning, launches.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 
@@ -11,34 +12,61 @@ using namespace qmm;
 
 namespace {
 
-__device__ unsigned g_qmm_err = 0;  // device error word (timeouts of bounded waits)
+// Device error word [0] (timeouts of bounded waits) and, in [1], the log2 of
+// the bounded waits' spin limit (0: the default of 2^31 SM clocks; lowered
+// only by qmm_test_set_wait_limit).
+__device__ unsigned g_qmm_err[2] = {0u, 0u};
 
 constexpr int kMaxDev = 64;
-unsigned* g_err_ptr[kMaxDev];
-int g_sm_count[kMaxDev];
-int g_smem_optin[kMaxDev];
+struct DeviceInfo {
+    std::atomic<unsigned*> err{nullptr};  // published last (release) once the sizes below are stored
+    std::atomic<int> sm_count{0};
+    std::atomic<int> smem_optin{0};
+};
+DeviceInfo g_dev[kMaxDev];
 
 // Per-device constants: error-word address, SM count, opt-in shared memory.
+// Host threads may race on a device's first call: each computes the same
+// values, and every field is atomic.
 cudaError_t device_info(unsigned** err, int* sms, int* smem, int* device = nullptr) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
-    if (!g_err_ptr[dev]) {
+    DeviceInfo& di = g_dev[dev];
+    unsigned* ep = di.err.load(std::memory_order_acquire);
+    int n = 0, s = 0;
+    if (ep) {
+        n = di.sm_count.load(std::memory_order_relaxed);
+        s = di.smem_optin.load(std::memory_order_relaxed);
+    } else {
         void* p = nullptr;
         if ((e = cudaGetSymbolAddress(&p, g_qmm_err)) != cudaSuccess) return e;
-        int n = 0, s = 0;
         if ((e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
         if ((e = cudaDeviceGetAttribute(&s, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess) return e;
-        g_sm_count[dev] = n;
-        g_smem_optin[dev] = s;
-        g_err_ptr[dev] = static_cast<unsigned*>(p);
+        ep = static_cast<unsigned*>(p);
+        di.sm_count.store(n, std::memory_order_relaxed);
+        di.smem_optin.store(s, std::memory_order_relaxed);
+        di.err.store(ep, std::memory_order_release);
     }
-    if (err) *err = g_err_ptr[dev];
-    if (sms) *sms = g_sm_count[dev];
-    if (smem) *smem = g_smem_optin[dev];
+    if (err) *err = ep;
+    if (sms) *sms = n;
+    if (smem) *smem = s;
     if (device) *device = dev;
     return cudaSuccess;
+}
+
+// Failure-test injection (qmm_test_inject): counts of calls still to fail.
+std::atomic<int> g_inject_launch_failures{0};
+std::atomic<int> g_inject_stalls{0};
+std::atomic<int> g_inject_stall_stage{0};
+
+// Takes one pending injection of a kind, if any.
+bool take_injection(std::atomic<int>& pending) {
+    int v = pending.load(std::memory_order_relaxed);
+    while (v > 0)
+        if (pending.compare_exchange_weak(v, v - 1, std::memory_order_relaxed)) return true;
+    return false;
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
@@ -158,6 +186,7 @@ const Dispatch& get_dispatch(int dev, int wt, int am, int epi, long long M, long
 
 qmm_status stream_call(qmm_type wtype, int am, int epi, const void* wq, const float* x, float* y, int32_t* sums,
                        int64_t M, int64_t N, int64_t K, void* ws, size_t ws_bytes, qmm_stream_t stream) {
+    if (take_injection(g_inject_launch_failures)) return QMM_ERR_CUDA;  // test hook: no CUDA call made
     unsigned* err = nullptr;
     int sms = 0, smem = 0, dev = 0;
     if (device_info(&err, &sms, &smem, &dev) != cudaSuccess) return QMM_ERR_CUDA;
@@ -181,6 +210,7 @@ qmm_status stream_call(qmm_type wtype, int am, int epi, const void* wq, const fl
         dp.p.y = y;
         dp.p.sums = sums;
         dp.p.err = err;
+        dp.p.stall_stage = take_injection(g_inject_stalls) ? g_inject_stall_stage.load(std::memory_order_relaxed) + 1 : 0;
         const bool split = epi == E_Y && dp.p.kslices > 1;
         if (split || dp.ext_bytes) {
             if (!ws || ws_bytes < dp.workspace) return QMM_ERR_WORKSPACE;
@@ -411,6 +441,32 @@ qmm_status qmm_block_sums(qmm_type wtype, const void* wq, const float* x, int64_
     if (!wq || !x || !out) return QMM_ERR_NULL;
     if (!aligned(wq, 16) || !aligned(x, 16) || !aligned(out, 4)) return QMM_ERR_ALIGN;
     return stream_call(wtype, A_INT8, E_SUMS, wq, x, nullptr, out, M, N, K, nullptr, 0, stream);
+}
+
+qmm_status qmm_test_inject(qmm_inject_kind kind, int count, int arg) {
+    if (count < 0 || arg < 0) return QMM_ERR_SHAPE;
+    switch (kind) {
+        case QMM_INJECT_OFF:
+            g_inject_launch_failures.store(0);
+            g_inject_stalls.store(0);
+            return QMM_OK;
+        case QMM_INJECT_LAUNCH_FAILURE:
+            g_inject_launch_failures.store(count);
+            return QMM_OK;
+        case QMM_INJECT_STALL:
+            g_inject_stall_stage.store(arg);
+            g_inject_stalls.store(count);
+            return QMM_OK;
+        default:
+            return QMM_ERR_TYPE;
+    }
+}
+
+qmm_status qmm_test_set_wait_limit(int log2_clocks) {
+    if (log2_clocks != 0 && (log2_clocks < 16 || log2_clocks > 31)) return QMM_ERR_SHAPE;
+    const unsigned v = (unsigned)log2_clocks;
+    if (cudaMemcpyToSymbol(g_qmm_err, &v, sizeof(v), sizeof(unsigned)) != cudaSuccess) return QMM_ERR_CUDA;
+    return QMM_OK;
 }
 
 qmm_status qmm_last_device_error(void) {

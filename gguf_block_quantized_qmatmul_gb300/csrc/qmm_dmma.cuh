@@ -77,6 +77,11 @@ struct DmmaParams {
     // ([2M][K] in MMA k order), scales [unit][sstride], aux [unit][...].
     const uint8_t* ext;
     long long ext_codes, ext_scale, ext_aux;
+    // Failure test hook (0 = off): when s > 0, block 0's producer issues no
+    // weight stage from stage s - 1 on, so that the consumers' bounded wait
+    // for that stage runs out (QMM_ERR_TIMEOUT) and the block takes its abort
+    // path.  Set only by the library's test hook, never by a plan.
+    int stall_stage;
 };
 
 // position p (0..31) of a 32-value group in the MMA k order -> value index
@@ -421,6 +426,10 @@ __global__ void __launch_bounds__(kDmmaThreads, 1) qmm_dmma_kernel(const DmmaPar
                     ok = __shfl_sync(0xffffffffu, okl, 0) != 0;
                     if (!ok) break;
                 }
+                if (p.stall_stage > 0 && blockIdx.x == 0 && g == p.stall_stage - 1) {
+                    ok = false;  // injected stall: nothing from this stage on is issued
+                    break;
+                }
                 const int cu0 = su0 + ch * p.ups;
                 const int cnu = min(p.ups, su0 + sunits - cu0);
                 uint8_t* st = smem + p.off_stage + (long long)slot * p.stage_bytes;
@@ -451,8 +460,8 @@ __global__ void __launch_bounds__(kDmmaThreads, 1) qmm_dmma_kernel(const DmmaPar
         if (!act_done) fetch_act();
         if (lane == 0) {
             const long long first = g > S ? g - S : 0;
-            for (long long q = first; q < g; ++q) mbar_wait(smem_u32(&bars[q % S]), (uint32_t)((q / S) & 1), flags, p.err);
-            if (p.ext) mbar_wait(smem_u32(abar), 0u, flags, p.err);
+            for (long long q = first; q < g; ++q) mbar_drain(smem_u32(&bars[q % S]), (uint32_t)((q / S) & 1), flags, p.err);
+            if (p.ext) mbar_drain(smem_u32(abar), 0u, flags, p.err);
         }
         return;
     }

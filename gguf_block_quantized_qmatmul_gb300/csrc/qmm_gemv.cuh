@@ -151,7 +151,7 @@ __global__ void __launch_bounds__((kGemvWarps + 1) * 32, 1) qmm_gemv_kernel(cons
             if (b > a) bulk_g2s(smem_u32(st), p.wq + a, (uint32_t)(b - a), fb);
         }
         const long long first = g > S ? g - S : 0;
-        for (long long q = first; q < g; ++q) mbar_wait(smem_u32(&bars[q % S]), (uint32_t)((q / S) & 1), flags, p.err);
+        for (long long q = first; q < g; ++q) mbar_drain(smem_u32(&bars[q % S]), (uint32_t)((q / S) & 1), flags, p.err);
         return;
     }
 

@@ -9,6 +9,8 @@
 // instead of from the caller.
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "../../include/qmm.h"
 
 namespace {
@@ -17,19 +19,21 @@ namespace {
 static __device__ __align__(256) unsigned char g_static_workspace[QMM_STATIC_WORKSPACE_BYTES];
 
 constexpr int kMaxDev = 64;
-void* g_static_ws_addr[kMaxDev];  // device address of the array, per device
+std::atomic<void*> g_static_ws_addr[kMaxDev];  // device address of the array, per device
 
 // Set-up, once per device, with that device current: in host code the array's
-// name is only a stand-in, so the device address has to be looked up.
+// name is only a stand-in, so the device address has to be looked up.  Host
+// threads racing on a device's first call look up the same address; the
+// cache is atomic.
 qmm_status static_workspace_address(void** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return QMM_ERR_CUDA;
-    if (!g_static_ws_addr[dev]) {
-        void* p = nullptr;
+    void* p = g_static_ws_addr[dev].load(std::memory_order_acquire);
+    if (!p) {
         if (cudaGetSymbolAddress(&p, g_static_workspace) != cudaSuccess || !p) return QMM_ERR_CUDA;
-        g_static_ws_addr[dev] = p;
+        g_static_ws_addr[dev].store(p, std::memory_order_release);
     }
-    *out = g_static_ws_addr[dev];
+    *out = p;
     return QMM_OK;
 }
 
@@ -44,7 +48,8 @@ extern "C" qmm_status qmm_matmul_static_workspace(qmm_type wtype, qmm_act_mode m
     const qmm_status st = static_workspace_address(&ws);
     if (st != QMM_OK) return st;
     // qmm_matmul clears on `stream` the part of the workspace that must start
-    // at zero (the arrival counters of a K split in the prefill kernel) before
-    // its launch; partial sums are overwritten and need no clearing.
+    // at zero (the K-split arrival counters of the streaming and tcgen05
+    // kernels) before its launch; partial sums are overwritten and need no
+    // clearing.
     return qmm_matmul(wtype, mode, wq, x, y, M, N, K, ws, (size_t)QMM_STATIC_WORKSPACE_BYTES, stream);
 }

@@ -563,7 +563,7 @@ __global__ void __launch_bounds__((consumer_warps(WT, AM, NT) + 1) * 32, 1)
         // wait for the copies still in flight into this block's stages
         if (lane == 0) {
             const long long first = g > S ? g - S : 0;
-            for (long long q = first; q < g; ++q) mbar_wait(smem_u32(&bars[q % S]), (uint32_t)((q / S) & 1), flags, p.err);
+            for (long long q = first; q < g; ++q) mbar_drain(smem_u32(&bars[q % S]), (uint32_t)((q / S) & 1), flags, p.err);
         }
         return;
     }

@@ -17,8 +17,9 @@
  *
  * Conventions for every entry point:
  *  - Pointers are DEVICE pointers owned by the caller unless stated.  The
- *    library allocates nothing.  It keeps one 4-byte device error word per
- *    device (see qmm_last_device_error).
+ *    library allocates nothing.  It keeps two 4-byte device words per
+ *    device: the error word (see qmm_last_device_error) and the spin limit
+ *    of its bounded waits (see qmm_test_set_wait_limit).
  *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
  *    default stream).  Argument errors are returned synchronously, before
  *    anything is launched.  QMM_ERR_CUDA reports a launch error.
@@ -228,12 +229,35 @@ qmm_status qmm_matmul_batch(qmm_type wtype, qmm_act_mode mode, const qmm_matmul_
      that device current); make that first call before any stream capture.
    - Every call shares the one array and it keeps the last call's contents:
      each call clears on `stream` whatever part must start at zero (the
-     arrival counters of a K split in the prefill kernel), but calls that
-     overlap on the GPU (other streams, other host threads) race on it.
+     K-split arrival counters of the streaming and tcgen05 kernels), but
+     calls that overlap on the GPU (other streams, other host threads) race
+     on it.
    Other arguments and errors as qmm_matmul. */
 #define QMM_STATIC_WORKSPACE_BYTES (8u << 20)
 qmm_status qmm_matmul_static_workspace(qmm_type wtype, qmm_act_mode mode, const void* wq, const float* x, float* y,
                                        int64_t M, int64_t N, int64_t K, qmm_stream_t stream);
+
+/* Failure-test hooks.  (The pages have no counterpart: these exist so that
+   the library's failure paths can be exercised without faulting a GPU.)
+   qmm_test_inject arms an injected failure, consumed by the next `count`
+   calls that reach it; QMM_INJECT_OFF disarms every kind.
+   - QMM_INJECT_LAUNCH_FAILURE: qmm_matmul / qmm_block_sums return
+     QMM_ERR_CUDA at once, as if the launch had failed, without any CUDA call
+     (the outputs are not touched).
+   - QMM_INJECT_STALL: the next decode-kernel launch (qmm_dmma_kernel, the
+     M <= 16 warp-MMA path) issues no weight stage from stage `arg` on in its
+     first block, so that block's consumers wait in vain: their bounded wait
+     gives up, the block drains the copies it did issue and exits, and
+     qmm_last_device_error then reports QMM_ERR_TIMEOUT.  The call's output
+     is undefined; later calls are unaffected.
+   qmm_test_set_wait_limit sets the bounded waits' spin limit on the current
+   device to 2^log2_clocks SM clocks (16..31; 0 restores the default 2^31,
+   about one second), so that an injected stall ends in milliseconds.  It
+   writes device memory synchronously.  Errors: SHAPE (argument out of
+   range), TYPE (unknown kind), CUDA. */
+typedef enum { QMM_INJECT_OFF = 0, QMM_INJECT_LAUNCH_FAILURE = 1, QMM_INJECT_STALL = 2 } qmm_inject_kind;
+qmm_status qmm_test_inject(qmm_inject_kind kind, int count, int arg);
+qmm_status qmm_test_set_wait_limit(int log2_clocks);
 
 /* Reads and clears the current device's error word (synchronizes that
    device).  QMM_ERR_TIMEOUT if a device-side wait of an earlier launch gave

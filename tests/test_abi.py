@@ -133,3 +133,19 @@ def test_product_package_never_imports_the_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
                 txt = open(os.path.join(dirpath, f), encoding="utf-8").read()
                 assert "import oracle" not in txt and "from oracle" not in txt and "qmm_oracle" not in txt, f
+
+
+def test_injected_launch_failure_needs_no_device(qmm):
+    """The failure-test hook: an armed launch failure makes the next call
+    return QMM_ERR_CUDA before any CUDA call (this host has no GPU, so any
+    CUDA call would fail differently or hang nothing), and arguments of the
+    hooks themselves are checked on the host."""
+    L = _lib(qmm)
+    assert L.qmm_test_inject(1, 2, 0) == 0
+    for _ in range(2):   # valid, aligned arguments: only the injection stops the call
+        assert L.qmm_matmul(qmm.QMM_Q8_0, 0, 16, 16, 16, 1, 1, 256, None, 0, None) == 6
+    assert L.qmm_test_inject(0, 0, 0) == 0
+    assert L.qmm_test_inject(9, 1, 0) == 3            # unknown kind
+    assert L.qmm_test_inject(1, -1, 0) == 2           # negative count
+    assert L.qmm_test_set_wait_limit(5) == 2          # below 2^16 clocks
+    assert L.qmm_test_set_wait_limit(40) == 2
