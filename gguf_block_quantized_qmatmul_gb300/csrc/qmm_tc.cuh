@@ -13,8 +13,9 @@
 // rows and weight rows separately, into [2^14, 2^15) at the row maximum) and
 // split into two f16 pieces, v = hi + lo (exact for the 18-19 significant
 // bits of f(d) q, 2^-22 relative otherwise); the product takes three MMAs,
-// hi.hi + hi.lo + lo.hi (the dropped lo.lo is below 2^-22 relative), all into
-// one f32 accumulator, and the epilogue multiplies by 2^-(s_row + s_col).
+// hi.hi + hi.lo + lo.hi (the dropped lo.lo is below 2^-22 relative), into an
+// f32 accumulator restarted every kchunk raw stages (see kTcChunkInt8), and the
+// epilogue multiplies by 2^-(s_row + s_col) and adds the chunks.
 //
 // One persistent CTA per SM over work units: an output tile of 128 weight
 // rows x bx activation rows (bx <= 256, a multiple of 16, the MMA's N) and
@@ -30,9 +31,10 @@
 //             current one, so a ready stage costs no stall;
 //   epilogue  8 warps, a TMEM lane quarter (32 weight rows) and half of the
 //             accumulator columns each: tcgen05.ld, scale, y stores coalesced
-//             along N; with K split, unscaled partial tiles in the workspace,
-//             and the unit that completes a tile sums its ks partials in
-//             slice order (deterministic) and writes y;
+//             along N (later chunks of the unit: added into y); with
+//             K split, unscaled partial tiles in the workspace, and the unit
+//             that completes a tile sums its ks partials in slice order
+//             (deterministic) and writes y;
 //   converter 8 warps in two groups (even and odd stages): each thread one
 //             weight row's 32 values of a stage, read from the raw stage with
 //             conflict-free 16-byte loads, dequantized, split into hi and lo,
@@ -69,6 +71,20 @@ constexpr int kTcThreads = (2 + kTcEpiWarps + kTcConvWarps) * 32;
 constexpr int kTcTmemCols = 512;
 constexpr int kTcWCol0 = 256;   // weight pieces: stage s at 256 + 32 s (hi 16 columns, lo 16 columns)
 constexpr int kTcMaxSplit = 16;
+// Accumulation chunks.  The tensor core's f32 accumulation truncates: its
+// error grows with the number of MMAs chained into one accumulator and leans
+// toward zero.  Over a whole 4096-K unit (768 f16 MMAs of three passes) the
+// CPU form's worst output reached the parity bound at 14336 x 4096, M = 1024
+// (that bound is taken over block terms, which cancel less than element
+// products; the Metal form's bound, over element products, kept a 4x
+// margin).  So a unit restarts its accumulator every `kchunk` raw stages and
+// the epilogue adds the chunks' results into y in f32 with round-to-nearest;
+// the worst error falls about as the chunk length does.  With two
+// accumulators (bx <= 128) the epilogue drains one chunk while the MMAs fill
+// the other: 1024 K.  With one, the MMAs wait for each drain: 2048 K for the
+// CPU form, 4096 K for the Metal form.  (Tiles of at most 192 rows, which
+// would leave room for two accumulators, measured 35 % slower at M = 1024.)
+constexpr int kTcChunkDouble = 4, kTcChunkInt8 = 8, kTcChunkF32 = 16;
 
 struct TcParams {
     float* y;
@@ -80,6 +96,7 @@ struct TcParams {
     int M, N, K;
     int bx;             // activation rows per tile (MMA N)
     int nacc;           // accumulators: 2 when bx <= 128
+    int kchunk;         // raw stages per accumulation chunk
     int mtiles, ntiles, tiles;
     int ks, units;      // K slices; work units = tiles x ks
     int nrs;            // raw stages in K
@@ -467,28 +484,29 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             // let every copy this thread issued land before the CTA can exit
             for (long long q = (g > kTcS ? g - kTcS : 0); q < g; ++q)
-                mbar_wait(smem_u32(&full[q % kTcS]), (uint32_t)((q / kTcS) & 1), flags, p.err);
+                mbar_drain(smem_u32(&full[q % kTcS]), (uint32_t)((q / kTcS) & 1), flags, p.err);
             for (long long q = (ri > p.nraw ? ri - p.nraw : 0); q < ri; ++q)
-                mbar_wait(smem_u32(&r_full[q % p.nraw]), (uint32_t)((q / p.nraw) & 1), flags, p.err);
+                mbar_drain(smem_u32(&r_full[q % p.nraw]), (uint32_t)((q / p.nraw) & 1), flags, p.err);
         }
     } else if (warp == 1) {
         // ------------------------------ MMA issuer ------------------------------
         if (lane == 0) {
             const uint32_t idesc = tc_idesc(p.bx);
             long long g = 0;
-            int uc = 0;
+            int cc = 0;  // accumulation chunks issued
             bool ok = true;
             uint32_t ready = 0;  // the next stage's barrier, tested ahead
-            for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x, ++uc) {
-                const int ab = p.nacc == 2 ? (uc & 1) : 0;
-                const int use = p.nacc == 2 ? (uc >> 1) : uc;
+            for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
+              int r0, r1;
+              tc_slice(p, u / p.tiles, r0, r1);
+              for (int c0 = r0; c0 < r1 && ok; c0 += p.kchunk, ++cc) {
+                const int ab = p.nacc == 2 ? (cc & 1) : 0;
+                const int use = p.nacc == 2 ? (cc >> 1) : cc;
                 if (use > 0) ok = mbar_wait(smem_u32(&acc_empty[ab]), (uint32_t)((use - 1) & 1), flags, p.err);
                 if (!ok) break;
                 tc_fence_after();
                 const uint32_t dt = tmem + (uint32_t)(ab * 128);
-                int r0, r1;
-                tc_slice(p, u / p.tiles, r0, r1);
-                const int nst = (r1 - r0) * kTcSub;
+                const int nst = ((c0 + p.kchunk < r1 ? c0 + p.kchunk : r1) - c0) * kTcSub;
                 for (int i = 0; i < nst; ++i, ++g) {
                     const int s = (int)(g % kTcS);
                     const uint32_t nxt = mbar_test(smem_u32(&full[(g + 1) % kTcS]), (uint32_t)(((g + 1) / kTcS) & 1));
@@ -510,9 +528,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 if (!ok) break;
                 tc_commit(smem_u32(&acc_full[ab]));
+              }
             }
             // the last commits must land before TMEM is released
-            if (g > 0) mbar_wait(smem_u32(&empty[(g - 1) % kTcS]), (uint32_t)(((g - 1) / kTcS) & 1), flags, p.err);
+            if (g > 0) mbar_drain(smem_u32(&empty[(g - 1) % kTcS]), (uint32_t)(((g - 1) / kTcS) & 1), flags, p.err);
         }
     } else if (warp < 2 + kTcEpiWarps) {
         // ------------------------------ epilogue ------------------------------
@@ -521,10 +540,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int half = ew >> 2;      // accumulator columns: 16-column chunks half, half + 2, ...
         const uint32_t tq = (uint32_t)(32 * q) << 16;
         const int nch = p.bx / 16;
-        int uc = 0, fix = 0;
-        for (int u = blockIdx.x; u < p.units; u += gridDim.x, ++uc) {
-            const int ab = p.nacc == 2 ? (uc & 1) : 0;
-            const int use = p.nacc == 2 ? (uc >> 1) : uc;
+        int cc = 0, fix = 0;  // accumulation chunks read; split-K fix-ups
+        bool ok = true;
+        for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
             const int tile = u % p.tiles, split = u / p.tiles;
             const int m0 = (tile % p.mtiles) * p.bx, n0 = (tile / p.mtiles) * kTcBW;
             const int n = n0 + 32 * q + lane;
@@ -542,32 +560,60 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     asc[j] = mr < p.bx && m < p.M ? __ldg(p.ais + m) : 0.0f;
                 }
             }
-            if (!mbar_wait(smem_u32(&acc_full[ab]), (uint32_t)(use & 1), flags, p.err)) break;
-            tc_fence_after();
-            __syncwarp();
             float* dst = p.ks == 1 ? p.y : p.part + (size_t)split * p.M * p.N;
-            const uint32_t acol = tmem + tq + (uint32_t)(ab * 128);
-            uint32_t r[16];
-            if (half < nch) tc_ld16(acol + 16 * half, r);
-            for (int c = half, k = 0; c < nch; c += 2, ++k) {
-                tc_wait_ld();
-                float v[16];
+            int r0, r1;
+            tc_slice(p, split, r0, r1);
+            // the unit's accumulation chunks: the first stores its (scaled) result,
+            // later ones add theirs to it (this thread wrote those elements itself)
+            for (int c0 = r0; c0 < r1; c0 += p.kchunk, ++cc) {
+                const bool first = c0 == r0;
+                const int ab = p.nacc == 2 ? (cc & 1) : 0;
+                const int use = p.nacc == 2 ? (cc >> 1) : cc;
+                if (!(ok = mbar_wait(smem_u32(&acc_full[ab]), (uint32_t)(use & 1), flags, p.err))) break;
+                tc_fence_after();
+                __syncwarp();
+                const uint32_t acol = tmem + tq + (uint32_t)(ab * 128);
+                uint32_t r[16];
+                if (half < nch) tc_ld16(acol + 16 * half, r);
+                for (int c = half, k = 0; c < nch; c += 2, ++k) {
+                    tc_wait_ld();
+                    float v[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-                if (c + 2 < nch) tc_ld16(acol + 16 * (c + 2), r);  // the next chunk's load overlaps the stores
-                const int mb = m0 + 16 * c;
-                if (nok && !flags[0]) {
-                    float* yr = dst + (size_t)mb * p.N + n;
-                    const float* ak = asc + 16 * k;
+                    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+                    if (c + 2 < nch) tc_ld16(acol + 16 * (c + 2), r);  // the next 16 columns' load overlaps the stores
+                    const int mb = m0 + 16 * c;
+                    if (nok && !flags[0]) {
+                        float* yr = dst + (size_t)mb * p.N + n;
+                        const float* ak = asc + 16 * k;
 #pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        if (mb + i < p.M) yr[(size_t)i * p.N] = p.ks == 1 ? v[i] * wsn * ak[i] : v[i];
+                        for (int i = 0; i < 16; ++i) v[i] = p.ks == 1 ? v[i] * wsn * ak[i] : v[i];
+                        if (first) {
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                if (mb + i < p.M) yr[(size_t)i * p.N] = v[i];
+                        } else {  // later chunks add to what this thread stored (four loads in flight:
+                                  // 18 warps leave 96 registers a thread)
+                            float* yp = yr;
+#pragma unroll
+                            for (int h = 0; h < 16; h += 4) {
+                                float o[4];
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) o[i] = mb + h + i < p.M ? yp[(size_t)i * p.N] : 0.0f;
+#pragma unroll
+                                for (int i = 0; i < 4; ++i)
+                                    if (mb + h + i < p.M) yp[(size_t)i * p.N] = o[i] + v[h + i];
+                                yp += (size_t)4 * p.N;
+                            }
+                        }
+                    }
                 }
+                __syncwarp();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&acc_empty[ab]));
             }
+            if (!ok) break;
             __syncwarp();  // the scale area is rewritten for the next unit
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&acc_empty[ab]));
             if (p.ks > 1) {
                 // the unit that completes the tile sums its ks partials in slice order
                 __threadfence();
@@ -766,9 +812,10 @@ struct TcPlan {
 // N; a unit adds its accumulator hand-off (the epilogue's drain of a single
 // accumulator stalls the MMAs); a split tile's last unit also sums the ks
 // partial tiles, at ~24 B a cycle through L2.
-inline double tc_unit_cycles(int bx, int nacc, int ks, int nr, bool last) {
+inline double tc_unit_cycles(int bx, int nacc, int kchunk, int ks, int nr, bool last) {
     const double stage = bx * 3.5 > 560.0 ? bx * 3.5 : 560.0;
-    double c = nr * kTcSub * stage + (nacc == 1 ? 6000.0 : 1500.0);
+    const int chunks = (nr + kchunk - 1) / kchunk;  // one accumulator: the MMAs wait for each chunk's drain
+    double c = nr * kTcSub * stage + (nacc == 1 ? 6000.0 * chunks : 1500.0);
     if (ks > 1 && last) c += ks * bx * (kTcBW * 4.0 / 24.0);
     return c;
 }
@@ -783,6 +830,7 @@ inline bool plan_tc(int wt, int am, long long M, long long N, long long K, int s
     p.mtiles = (int)((M + kTcBXMax - 1) / kTcBXMax);
     p.bx = round_up((int)((M + p.mtiles - 1) / p.mtiles), 16);
     p.nacc = p.bx <= 128 ? 2 : 1;
+    p.kchunk = p.nacc == 2 ? kTcChunkDouble : am == A_INT8 ? kTcChunkInt8 : kTcChunkF32;
     p.ntiles = (int)((N + kTcBW - 1) / kTcBW);
     p.tiles = p.mtiles * p.ntiles;
     p.nrs = (int)(K / kTcRK);
@@ -811,7 +859,7 @@ inline bool plan_tc(int wt, int am, long long M, long long N, long long K, int s
             for (long long u = c; u < units; u += grid) {
                 const int split = (int)(u / p.tiles);
                 const int nr = (split + 1) * p.nrs / ks - split * p.nrs / ks;
-                t += tc_unit_cycles(p.bx, p.nacc, ks, nr, split == ks - 1);
+                t += tc_unit_cycles(p.bx, p.nacc, p.kchunk, ks, nr, split == ks - 1);
             }
             if (t > worst) worst = t;
         }
@@ -834,7 +882,6 @@ inline bool plan_tc(int wt, int am, long long M, long long N, long long K, int s
     pl.ws_part = pl.ws_wis + r256((size_t)N * 4);
     pl.ws_cnt = pl.ws_part + (p.ks > 1 ? r256((size_t)p.ks * M * N * 4) : 0);
     pl.workspace = pl.ws_cnt + (p.ks > 1 ? r256((size_t)p.tiles * 4) : 0);
-    (void)am;
     out = pl;
     return true;
 }

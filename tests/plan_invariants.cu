@@ -115,6 +115,8 @@ int check_tc(int wt, long long M, long long N, long long K) {
     CHECK(p.bx % 16 == 0 && p.bx >= 16 && p.bx <= kTcBXMax && (long long)p.bx * p.mtiles >= M, CASE);
     // TMEM: the accumulators plus four stages of 32 weight-piece columns fit the 512 columns
     CHECK((p.nacc == 2 ? 2 * 128 : 256) + kTcS * 32 <= kTcTmemCols && p.nacc == (p.bx <= 128 ? 2 : 1), CASE);
+    // accumulation chunks: 1024 K with two accumulators; 2048 K (CPU form) or 4096 K (Metal form) with one
+    CHECK(p.kchunk == (p.nacc == 2 ? 4 : 8), CASE);
     CHECK(p.ntiles == (int)((N + kTcBW - 1) / kTcBW) && p.tiles == p.mtiles * p.ntiles, CASE);
     CHECK(p.ks >= 1 && p.ks <= p.nrs && p.units == p.tiles * p.ks, CASE);
     CHECK(pl.grid == (p.units < kSms ? p.units : kSms), CASE);
