@@ -44,6 +44,33 @@ def check_device_error(qmm):
     assert qmm.last_device_error() == 0
 
 
+# Canaries: outputs are views into a larger buffer whose guard words before
+# and after hold a NaN bit pattern; a write outside the output shows.  The
+# output itself starts as that NaN, so an element left unwritten fails too.
+CANARY = 0x7FBADBAD
+GUARD = 64  # 4-byte words on each side
+
+
+def guarded_out(M, N):
+    buf = torch.full((M * N + 2 * GUARD,), CANARY, dtype=torch.int32, device="cuda")
+    return buf, buf[GUARD:GUARD + M * N].view(torch.float32).view(M, N)
+
+
+def check_guards(buf, what=""):
+    b = host(buf)
+    assert (b[:GUARD] == CANARY).all() and (b[-GUARD:] == CANARY).all(), f"{what}: write outside the output"
+
+
+def matmul_checked(qmm, wq, x, wtype, mode, N, **kw):
+    """qmm.matmul into a guarded output; returns y on the host."""
+    M = x.shape[0]
+    buf, y = guarded_out(M, N)
+    qmm.matmul(wq, x, wtype, mode, N=N, out=y, **kw)
+    out = host(y).copy()
+    check_guards(buf, f"{wtype} {mode} M{M} N{N}")
+    return out
+
+
 # ---------------------------------------------------------------------------
 # quantizers and dequantization: bit-exact
 # ---------------------------------------------------------------------------
@@ -163,7 +190,7 @@ def test_matmul_within_bound(qmm, orc, wtype, M, N, K, mode):
     w = qmm_synth.weights(N, K, seed=N * 7 + K)
     x = qmm_synth.activations(M, K, seed=M + 11, outlier_channels=4 if M >= 16 else 0)
     wq = orc.quantize(wtype, w)
-    y = host(qmm.matmul(dev(wq), dev(x), wtype, mode, N=N))
+    y = matmul_checked(qmm, dev(wq), dev(x), wtype, mode, N)
     y_orc, T = orc.matmul(wtype, mode, wq, x)
     assert_within_bound(y, y_orc, T, f"{wtype} {mode} M{M} N{N} K{K}")
     check_device_error(qmm)
@@ -181,6 +208,126 @@ def test_prefill_special_rows(qmm, orc, wtype, K, mode):
     y = host(qmm.matmul(dev(wq), dev(x), wtype, mode, N=w.shape[0]))
     y_orc, T = orc.matmul(wtype, mode, wq, x)
     assert_within_bound(y, y_orc, T, f"{wtype} {mode} special rows")
+    check_device_error(qmm)
+
+
+# ---------------------------------------------------------------------------
+# adversarial rows (zeros, constants, one-hot, rounding ties, all-negative and
+# all-positive blocks, magnitudes from the bottom of the f32 range to 3e3,
+# +-127 and integer blocks) in both operands, through every matmul kernel
+# ---------------------------------------------------------------------------
+
+def edge_operands(wtype, K, M, n_plain=20, seed=0):
+    """Weights: plain rows followed by the adversarial rows.  Activations: M
+    rows cycling through the adversarial rows from a per-M offset (plain rows
+    fill in past them)."""
+    sp = qmm_synth.special_block_rows(K)
+    w = np.concatenate([qmm_synth.weights(n_plain, K, seed=seed + 1), sp])
+    plain = qmm_synth.activations(max(M, 1), K, seed=seed + 2)
+    x = np.stack([sp[(5 * m + M) % len(sp)] if m < len(sp) else plain[m] for m in range(M)]).astype(np.float32)
+    return w, x
+
+
+DECODE_EDGE = [(t, M) for t in ("q8_0", "q4_k", "q4_0", "q5_0", "q6_k") for M in (2, 4, 8, 16)]
+
+
+@pytest.mark.parametrize("mode", ["int8_act", "f32_act"])
+@pytest.mark.parametrize("wtype,M", DECODE_EDGE)
+def test_decode_kernel_edge_rows(qmm, orc, wtype, M, mode):
+    """The 16-row warp-MMA decode kernel (activations prepared in the launch):
+    every weight type, 2..16 activation rows, both forms, adversarial rows in
+    both operands; outputs guarded by canaries."""
+    K = 1536
+    w, x = edge_operands(wtype, K, M)
+    wq = orc.quantize(wtype, w)
+    y = matmul_checked(qmm, dev(wq), dev(x), wtype, mode, w.shape[0])
+    y_orc, T = orc.matmul(wtype, mode, wq, x)
+    assert_within_bound(y, y_orc, T, f"{wtype} {mode} M{M} edge rows")
+    check_device_error(qmm)
+
+
+@pytest.mark.parametrize("mode", ["int8_act", "f32_act"])
+@pytest.mark.parametrize("wtype", ["q8_0", "q4_k", "q4_0", "q5_0", "q6_k"])
+def test_single_row_edge_rows(qmm, orc, wtype, mode):
+    """M = 1 (the dp4a GEMV for Q8_0 int8_act, the warp-MMA decode kernel
+    otherwise): each adversarial row alone as the activation."""
+    K = 1536
+    sp = qmm_synth.special_block_rows(K)
+    w = np.concatenate([qmm_synth.weights(20, K, seed=9), sp])
+    wq = orc.quantize(wtype, w)
+    wq_d = dev(wq)
+    for i in range(len(sp)):
+        x = sp[i:i + 1]
+        y = matmul_checked(qmm, wq_d, dev(x), wtype, mode, w.shape[0])
+        y_orc, T = orc.matmul(wtype, mode, wq, x)
+        assert_within_bound(y, y_orc, T, f"{wtype} {mode} adversarial row {i}")
+    check_device_error(qmm)
+
+
+@pytest.mark.parametrize("mode", ["int8_act", "f32_act"])
+@pytest.mark.parametrize("wtype,N,M", [("q8_0", 4100, 8), ("q8_0", 4100, 16), ("q4_k", 8192, 4), ("q4_k", 8192, 8),
+                                       ("q6_k", 5000, 8)])
+def test_prepared_activations_edge_rows(qmm, orc, wtype, N, M, mode):
+    """Weights over 32 MB with more than a few rows: the activations are
+    prepared once by their own launch, then fetched by every decode block;
+    adversarial rows in both operands (the weights' last rows)."""
+    K = 8192
+    w, x = edge_operands(wtype, K, M, n_plain=N - len(qmm_synth.special_block_rows(K)), seed=40)
+    assert qmm.matmul_launches(wtype, mode, M, N, K) >= 2
+    wq = orc.quantize(wtype, w)
+    y = matmul_checked(qmm, dev(wq), dev(x), wtype, mode, N)
+    y_orc, T = orc.matmul(wtype, mode, wq, x)
+    assert_within_bound(y, y_orc, T, f"{wtype} {mode} M{M} N{N} prepared activations, edge rows")
+    check_device_error(qmm)
+
+
+@pytest.mark.parametrize("mode", ["int8_act", "f32_act"])
+@pytest.mark.parametrize("wtype,M,K", [("q6_k", 37, 1536), ("q6_k", 37, 8192), ("q8_0", 37, 576), ("q5_0", 37, 576),
+                                       ("q4_0", 20, 576)])
+def test_streaming_kernel_edge_rows(qmm, orc, wtype, M, K, mode):
+    """The streaming warp-MMA kernel (all Q6_K prefill; 32-value blocks with
+    K % 256 != 0 above 16 rows), with and without a K split: adversarial rows
+    in both operands."""
+    w, x = edge_operands(wtype, K, M, n_plain=50, seed=60)
+    wq = orc.quantize(wtype, w)
+    y = matmul_checked(qmm, dev(wq), dev(x), wtype, mode, w.shape[0])
+    y_orc, T = orc.matmul(wtype, mode, wq, x)
+    assert_within_bound(y, y_orc, T, f"{wtype} {mode} M{M} K{K} streaming, edge rows")
+    check_device_error(qmm)
+
+
+@pytest.mark.parametrize("wtype,M,K", [("q8_0", 1, 576), ("q8_0", 8, 1536), ("q4_k", 8, 1536), ("q4_0", 4, 576),
+                                       ("q5_0", 16, 576), ("q6_k", 8, 1536), ("q6_k", 37, 1536), ("q8_0", 37, 576),
+                                       ("q4_k", 37, 1536)])
+def test_block_sums_edge_rows_bit_exact(qmm, orc, wtype, M, K):
+    """Integer block sums with adversarial rows in both operands: bit-exact
+    (decode kernel, GEMV and streaming kernel)."""
+    w, x = edge_operands(wtype, K, M, n_plain=20, seed=80)
+    wq = orc.quantize(wtype, w)
+    N = w.shape[0]
+    s = host(qmm.block_sums(dev(wq), dev(x), wtype, N=N))
+    xq = orc.quantize("q8_k" if wtype in ("q4_k", "q6_k") else "q8_0", x)
+    assert np.array_equal(s, orc.block_sums(wtype, wq, xq, M, N, K))
+    check_device_error(qmm)
+
+
+@pytest.mark.parametrize("mode", ["int8_act", "f32_act"])
+@pytest.mark.parametrize("wtype", ["q8_0", "q4_0", "q5_0"])
+def test_matmul_batch_edge_rows(qmm, orc, wtype, mode):
+    """qmm_matmul_batch with adversarial rows in the weights and activation
+    rows of its items (M = 1..8, K = 576 and 1536); guarded outputs."""
+    items, refs, guards = [], [], []
+    for i, (M, K) in enumerate([(1, 576), (2, 576), (8, 1536), (4, 1536), (1, 1536), (8, 576)]):
+        w, x = edge_operands(wtype, K, M, n_plain=7 + i, seed=100 + i)
+        wq = orc.quantize(wtype, w)
+        buf, y = guarded_out(M, w.shape[0])
+        items.append((dev(wq), dev(x), y))
+        refs.append(orc.matmul(wtype, mode, wq, x))
+        guards.append(buf)
+    qmm.matmul_batch(items, wtype, mode)
+    for (wq, x, y), (y_orc, T), buf in zip(items, refs, guards):
+        assert_within_bound(host(y), y_orc, T, f"batch {wtype} {mode} edge rows M{x.shape[0]}")
+        check_guards(buf, "batch item")
     check_device_error(qmm)
 
 
@@ -362,29 +509,34 @@ def test_error_statuses_on_device(qmm, orc):
 
 
 # ---------------------------------------------------------------------------
-# full-size workloads, in the launch configuration the benchmark times,
-# checked on sampled output rows
+# full-size workloads, in the launch configuration the benchmark times:
+# every output element against the oracle (run on all host cores)
 # ---------------------------------------------------------------------------
 
-FULL = [("q4_k", 28672, 8192, 8), ("q8_0", 28672, 8192, 8), ("q6_k", 28672, 8192, 8), ("q8_0", 14336, 4096, 1024),
-        ("q4_k", 14336, 4096, 1024), ("q8_0", 14336, 4096, 256), ("q4_k", 4096, 4096, 256),
-        ("q8_0", 4096, 4096, 16), ("q8_0", 49152, 576, 1), ("q5_0", 14336, 4096, 256), ("q5_0", 49152, 576, 1)]
+FULL = [("q4_k", 28672, 8192, 8), ("q8_0", 28672, 8192, 8), ("q6_k", 28672, 8192, 8),  # decode kernel
+        ("q8_0", 28672, 8192, 1),                                                       # dp4a GEMV (int8_act)
+        ("q4_k", 28672, 8192, 1),
+        ("q8_0", 14336, 4096, 1024), ("q4_k", 14336, 4096, 1024),                       # tcgen05 GEMM
+        ("q8_0", 14336, 4096, 256), ("q4_k", 4096, 4096, 256), ("q5_0", 14336, 4096, 256),
+        ("q4_k", 14336, 4096, 37), ("q8_0", 14336, 4096, 64),
+        ("q6_k", 14336, 4096, 256),                                                     # streaming kernel
+        ("q8_0", 4096, 4096, 16), ("q8_0", 49152, 576, 1), ("q5_0", 49152, 576, 1)]
 
 
+@pytest.mark.slow
 @pytest.mark.parametrize("wtype,N,K,M", FULL)
-def test_full_size_sampled_rows(qmm, orc, wtype, N, K, M):
+def test_full_size_full_outputs(qmm, orc, wtype, N, K, M):
     g = torch.Generator(device="cuda").manual_seed(0)
     w = torch.randn((N, K), generator=g, device="cuda") * 0.02
     wq = qmm.quantize_weights(w, wtype)
     del w
     x_np = qmm_synth.activations(M, K, outlier_channels=4 if M >= 16 else 0)
     x = dev(x_np)
-    rows = np.unique(np.concatenate([np.arange(16), np.random.default_rng(0).choice(N, 48, replace=False), [N - 1]]))
-    wq_rows = host(wq)[rows]
+    wq_h = host(wq)
     for mode in ("int8_act", "f32_act"):
-        y = host(qmm.matmul(wq, x, wtype, mode, N=N))
-        y_orc, T = orc.matmul(wtype, mode, wq_rows, x_np)
-        assert_within_bound(y[:, rows], y_orc, T, f"{wtype} {mode} N{N} K{K} M{M}")
+        y = matmul_checked(qmm, wq, x, wtype, mode, N)
+        y_orc, T = orc.matmul(wtype, mode, wq_h, x_np)
+        assert_within_bound(y, y_orc, T, f"{wtype} {mode} N{N} K{K} M{M}")
     check_device_error(qmm)
 
 
@@ -464,10 +616,9 @@ def test_matmul_batch_many_items_empty_items_and_largest_rows(qmm, orc, mode):
 
 
 def test_matmul_batch_smollm2_step_matches_single_calls(qmm, orc):
-    """The 211 linears of the SmolLM2-135M-shaped decode step in one batch
-    (two launches of <= 256 items would also do): every output equals the
-    single-call result within the bound, checked against the oracle on a few
-    items, and the batch writes every row."""
+    """The 211 linears of the SmolLM2-135M-shaped decode step in one batch:
+    every output element of every item against the oracle (outputs NaN-filled
+    before each form, so an unwritten row fails)."""
     lins = qmm_synth.smollm2_linears()
     xs = {K: dev(qmm_synth.activations(1, K, seed=K)) for K in (576, 1536)}
     items = []
@@ -475,11 +626,12 @@ def test_matmul_batch_smollm2_step_matches_single_calls(qmm, orc):
         g = torch.Generator(device="cuda").manual_seed(1000 + i)
         w = torch.randn((N, K), generator=g, device="cuda") * 0.02
         items.append((qmm.quantize_weights(w, "q8_0"), xs[K], torch.full((1, N), float("nan"), device="cuda")))
+    hosts = [(host(wq), host(x)) for wq, x, _ in items]
     for mode in ("int8_act", "f32_act"):
+        for _, _, y in items:
+            y.fill_(float("nan"))
         qmm.matmul_batch(items, "q8_0", mode)
-        for i in (0, 1, 6, 100, len(items) - 1):
-            wq, x, y = items[i]
-            y_orc, T = orc.matmul("q8_0", mode, host(wq), host(x))
+        for i, ((wq_h, x_h), (_, _, y)) in enumerate(zip(hosts, items)):
+            y_orc, T = orc.matmul("q8_0", mode, wq_h, x_h)
             assert_within_bound(host(y), y_orc, T, f"smollm2 item {i} {mode}")
-        assert all(bool(torch.isfinite(y).all()) for _, _, y in items)
     check_device_error(qmm)

@@ -3,10 +3,11 @@
 Callers such as a host engine that owns every device allocation, or a
 latency-critical loop that must not touch the allocator, cannot hand
 qmm_matmul a workspace.  This entry point uses the library's own device array
-instead.  Here it is called through the C ABI and compared with qmm_matmul
-(whose workspace the test allocates), on two calls in a row, with the same
-bound the parity tests use; a shape whose workspace exceeds the array must be
-refused before any launch.  This file is collected last on purpose.
+instead.  Here it is called through the C ABI and compared with the CPU oracle
+and with qmm_matmul (whose workspace the test allocates), on two calls in a
+row, with the same bound the parity tests use, on each kernel that can need a
+workspace; a shape whose workspace exceeds the array must be refused before
+any launch.  This file is collected last on purpose.
 """
 import ctypes
 
@@ -38,25 +39,37 @@ def _entry(q):
     return f
 
 
-def test_static_workspace_matches_qmm_matmul(qmm, orc):
+# Shapes whose workspace the entry point takes from its own array: the decode
+# kernel with K split (partial sums only), the tcgen05 GEMM with K split (its
+# arrival counters must start at zero on every call) and the streaming kernel
+# with K split (the same, cleared by a memset on the stream).
+STATIC_CASES = [("q8_0", "f32_act", 8, 100, 8192), ("q8_0", "int8_act", 64, 300, 4096),
+                ("q4_k", "f32_act", 37, 256, 2048), ("q6_k", "int8_act", 37, 64, 4096),
+                ("q6_k", "f32_act", 37, 64, 4096)]
+
+
+@pytest.mark.parametrize("wtype,mode,M,N,K", STATIC_CASES)
+def test_static_workspace_matches_qmm_matmul(qmm, orc, wtype, mode, M, N, K):
     f = _entry(qmm)
-    wtype, mode, M, N, K = "q8_0", "f32_act", 8, 100, 8192
     need = qmm.matmul_workspace(wtype, mode, M, N, K)
-    assert 0 < need <= 8 << 20        # this shape splits K, so a workspace is really used
+    assert 0 < need <= 8 << 20        # a workspace is really used, and it fits the array
     wq_h = orc.quantize(wtype, qmm_synth.weights(N, K, seed=21))
     wq = torch.from_numpy(wq_h).cuda()
     stream = torch.cuda.current_stream().cuda_stream
     for call in range(2):             # two calls in a row: the array keeps the last call's contents
-        x_h = qmm_synth.activations(M, K, seed=30 + call)
+        x_h = qmm_synth.activations(M, K, seed=30 + call, outlier_channels=4 if M >= 16 else 0)
         x = torch.from_numpy(x_h).cuda()
         y_ref = qmm.matmul(wq, x, wtype, mode, N=N)
         y = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
         st = f(qmm.TYPES[wtype], qmm.MODES[mode], wq.data_ptr(), x.data_ptr(), y.data_ptr(), M, N, K, stream)
         assert st == 0, qmm._lib().qmm_status_string(st)
         torch.cuda.synchronize()
-        _, T = orc.matmul(wtype, mode, wq_h, x_h)
-        err = np.abs(y.cpu().numpy().astype(np.float64) - y_ref.cpu().numpy())
-        assert np.all(err <= 1e-5 * T + 1e-6)
+        y_orc, T = orc.matmul(wtype, mode, wq_h, x_h)
+        bound = 1e-5 * T + 1e-6
+        got = y.cpu().numpy().astype(np.float64)
+        # against the oracle, and against qmm_matmul with a caller's workspace
+        assert np.all(np.abs(got - y_orc) <= bound)
+        assert np.all(np.abs(got - y_ref.cpu().numpy()) <= bound)
     assert qmm.last_device_error() == 0
 
 
