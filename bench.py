@@ -431,6 +431,133 @@ def dequant_all_case(q, torch, stream, wq, t, N, K, Ms=(16, 256, 1024)):
     return res
 
 
+PREFILL_SHAPES = ((4096, 4096), (14336, 4096))
+PREFILL_MS = (16, 37, 64, 256, 1024)
+PREFILL_HEADLINE = "q8_0/int8_act/M1024/14336x4096"
+
+
+def prefill_section(q, torch, stream, hbm_peak, bf16_peak):
+    """Config 4: the Llama-shaped prefill GEMMs (4096 x 4096 and 14336 x 4096
+    weights; Q8_0, Q4_K, and Q6_K as a next type; M = 16, 37, 64, 256, 1024;
+    both forms).  Each point runs calls back to back over distinct quantized
+    weight buffers that together exceed twice the L2 (so every call streams
+    its weights from HBM), timed with CUDA events over the whole run.
+    Reported per point: algorithmic TOPS = 2 M N K / t and its fraction of
+    the measured bf16 tensor peak (the GEMM runs f16 tcgen05 MMAs, which run
+    at the bf16 rate); weight GB/s and its fraction of the measured HBM
+    bandwidth; the roofline time max(2 M N K / peak, bytes / HBM) with bytes =
+    weights + x + y, and roofline_frac = roofline time / measured time.  The
+    tcgen05 GEMM's three f16 passes are reported beside it as tensor_TFLOPs.
+    Returns (points, the dequantize-all comparison)."""
+    l2 = getattr(torch.cuda.get_device_properties(0), "L2_cache_size", 0) or 129 * 1024 * 1024
+    points, deq = {}, {}
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    K = 4096
+    cols = torch.from_numpy(qmm_synth.outlier_columns(K)).cuda()
+    for t in ("q8_0", "q4_k", "q6_k"):
+        for N, _ in PREFILL_SHAPES:
+            wbytes = N * q.row_bytes(t, K)
+            nbuf = max(3, -(-2 * l2 // wbytes) + 1)
+            bufs = []
+            for b in range(nbuf):
+                g = torch.Generator(device="cuda").manual_seed(7000 + b)
+                w = torch.randn((N, K), generator=g, device="cuda") * 0.02
+                w[:, cols] *= 8.0
+                bufs.append(q.quantize_weights(w, t))
+                del w
+            modes = MODES if t != "q6_k" else MODES
+            Ms = PREFILL_MS if t != "q6_k" else (37, 256, 1024)
+            for mode in modes:
+                for M in Ms:
+                    x = torch.from_numpy(qmm_synth.activations(M, K, outlier_channels=4)).cuda()
+                    y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+                    wsp = torch.empty(max(q.matmul_workspace(t, mode, M, N, K), 16), dtype=torch.uint8, device="cuda")
+                    for i in range(3):
+                        q.matmul(bufs[i % nbuf], x, t, mode, N=N, out=y, workspace=wsp)
+                    reps = max(2 * nbuf, 12)
+                    torch.cuda.synchronize()
+                    ev0.record(stream)
+                    for i in range(reps):
+                        q.matmul(bufs[i % nbuf], x, t, mode, N=N, out=y, workspace=wsp)
+                    ev1.record(stream)
+                    torch.cuda.synchronize()
+                    sec = ev0.elapsed_time(ev1) / reps / 1e3
+                    ops = 2.0 * M * N * K
+                    nbytes = wbytes + 4.0 * M * K + 4.0 * M * N
+                    roof = max(ops / (bf16_peak * 1e12), nbytes / (hbm_peak * 1e9))
+                    pt = {"us": round(sec * 1e6, 2), "TOPS": round(ops / sec / 1e12, 1),
+                          "frac_of_bf16_peak": round(ops / sec / 1e12 / bf16_peak, 4),
+                          "weight_GBps": round(wbytes / sec / 1e9, 1),
+                          "frac_of_hbm": round(nbytes / sec / 1e9 / hbm_peak, 4),
+                          "bound": "tensor" if ops / (bf16_peak * 1e12) > nbytes / (hbm_peak * 1e9) else "hbm",
+                          "roofline_us": round(roof * 1e6, 2), "roofline_frac": round(roof / sec, 4),
+                          "buffers": nbuf, "launches_per_call": q.matmul_launches(t, mode, M, N, K)}
+                    if M > 16 and t != "q6_k":  # the tcgen05 GEMM: three f16 passes
+                        pt["tensor_TFLOPs"] = round(3 * ops / sec / 1e12, 1)
+                    points[f"{t}/{mode}/M{M}/{N}x{K}"] = pt
+            if t == "q8_0":
+                deq[f"{N}x{K}"] = dequant_all_case(q, torch, stream, bufs[0], t, N, K)
+            del bufs
+            torch.cuda.empty_cache()
+    return points, deq
+
+
+def oracle_configs():
+    """The oracle timed on the host cores beside the GPU configurations:
+    configs 1 and 2 on one thread (single calls), the SmolLM2-135M-shaped step
+    and the prefill shapes on all cores (the prefill on a sample of weight
+    rows, scaled to TOPS).  Inputs are synthetic, quantized by the oracle."""
+    import oracle
+    out = {"cores_all": None, "configs": {}}
+    res = out["configs"]
+
+    def timed(fn, min_s=0.2):
+        n, t0 = 0, time.perf_counter()
+        while True:
+            fn()
+            n += 1
+            el = time.perf_counter() - t0
+            if el >= min_s:
+                return el / n
+
+    oracle.set_num_threads(1)
+    try:
+        for t, N, K, Ms in (("q8_0", 576, 576, (1,)), ("q4_k", 576, 1536, (1, 2, 4, 8))):
+            wq = oracle.quantize(t, qmm_synth.weights(N, K))
+            for M in Ms:
+                x = qmm_synth.activations(M, K)
+                for mode in MODES:
+                    s = timed(lambda: oracle.matmul(t, mode, wq, x))
+                    res[f"{t} {N}x{K} M{M} {mode}"] = {"us_per_call": round(s * 1e6, 1), "threads": 1}
+    finally:
+        oracle.set_num_threads(0)
+    out["cores_all"] = oracle.num_threads()
+    lins = qmm_synth.smollm2_linears()
+    wqs = [(oracle.quantize("q8_0", qmm_synth.weights(N, K, seed=1000 + i)), K) for i, (_, N, K) in enumerate(lins)]
+    xs = {K: qmm_synth.activations(1, K, seed=K) for K in (576, 1536)}
+    for mode in MODES:
+        t0 = time.perf_counter()
+        for wq, K in wqs:
+            oracle.matmul("q8_0", mode, wq, xs[K])
+        s = time.perf_counter() - t0
+        res[f"smollm2_step_211_matmuls q8_0 M1 {mode}"] = {"ms_per_step": round(s * 1e3, 2),
+                                                            "threads": out["cores_all"]}
+    rows = 512
+    K = 4096
+    for t in ("q8_0", "q4_k"):
+        wq = oracle.quantize(t, qmm_synth.weights(rows, K, seed=7))
+        for mode in MODES:
+            for M in PREFILL_MS:
+                x = qmm_synth.activations(M, K, outlier_channels=4)
+                t0 = time.perf_counter()
+                oracle.matmul(t, mode, wq, x)
+                s = time.perf_counter() - t0
+                res[f"{t}/{mode}/M{M}/prefill K{K}"] = {
+                    "TOPS": round(2.0 * M * rows * K / s / 1e12, 4), "sample": f"{rows} weight rows",
+                    "threads": out["cores_all"]}
+    return out
+
+
 def run_ours(args):
     import torch
 
@@ -549,43 +676,16 @@ def run_ours(args):
     e2e_s = allmax(world, time.perf_counter() - t0)
     e2e = world * bytes_per_step * args.steps / e2e_s / 1e9
 
-    # prefill (Llama-shaped, both forms): TOPS = 2 M N K / time. The tensor cores run
-    # three f16 passes (hi.hi, hi.lo, lo.hi) of that product, so the tensor work is
-    # 3 x 2 M N K; its rate is compared with the measured dense bf16 peak (f16 runs
-    # at the bf16 rate).
-    prefill = {}
-    dequant_all = {}
+    # prefill (config 4, Llama-shaped, both forms) on weights rotated through buffers
+    # that together exceed 2 x L2, with the algorithmic roofline per point
+    prefill, prefill_points, dequant_all = {}, {}, {}
     if not args.no_prefill:
-        for t in TYPES:
-            for N in (4096, 14336):
-                g = torch.Generator(device="cuda").manual_seed(7)
-                w = torch.randn((N, 4096), generator=g, device="cuda") * 0.02
-                wq = q.quantize_weights(w, t)
-                del w
-                for M, mode in [(m, f) for f in ("int8_act", "f32_act") for m in (16, 37, 64, 256, 1024)]:
-                    x = torch.from_numpy(qmm_synth.activations(M, 4096, outlier_channels=4)).cuda()
-                    y = torch.empty((M, N), dtype=torch.float32, device="cuda")
-                    need = q.matmul_workspace(t, mode, M, N, 4096)
-                    wsp = torch.empty(max(need, 16), dtype=torch.uint8, device="cuda")
-                    for _ in range(3):
-                        q.matmul(wq, x, t, mode, N=N, out=y, workspace=wsp)
-                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                    reps = 10
-                    e0.record(stream)
-                    for _ in range(reps):
-                        q.matmul(wq, x, t, mode, N=N, out=y, workspace=wsp)
-                    e1.record(stream)
-                    torch.cuda.synchronize()
-                    ms = e0.elapsed_time(e1) / reps
-                    tops = 2.0 * M * N * 4096 / (ms / 1e3) / 1e12
-                    prefill[f"{t}/{mode}/M{M}/{N}x4096"] = {
-                        "ms": round(ms, 4), "TOPS": round(tops, 1),
-                        "tensor_TFLOPs": round(3 * tops, 1),
-                        "tensor_frac_of_bf16_peak": round(3 * tops / bf16_peak, 4),
-                        "weight_GBps": round(wq.numel() / (ms / 1e3) / 1e9, 1)}
-                if t == "q8_0":
-                    dequant_all[f"{N}x4096"] = dequant_all_case(q, torch, stream, wq, t, N, 4096)
-                del wq
+        prefill_points, dequant_all = prefill_section(q, torch, stream, hbm_peak, bf16_peak)
+        head = prefill_points.get(PREFILL_HEADLINE)
+        if head:
+            prefill = {"point": PREFILL_HEADLINE, "TOPS": head["TOPS"], "frac_of_bf16_peak": head["frac_of_bf16_peak"],
+                       "roofline_frac": head["roofline_frac"], "peak_TFLOPs": bf16_peak,
+                       "l2": "weights rotated over distinct buffers totalling > 2 x L2"}
 
     small = small_configs(q, torch, stream) if not args.no_small else {}
     nxt = next_types(q, torch, stream) if not args.no_small else {}
@@ -600,6 +700,8 @@ def run_ours(args):
         b, s = oracle_sample(rows, wq_h, xs_h)
         cpu = {"value": b / s / 1e9, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
                "sample": f"{rows} of {N_DEC} rows of one buffer per type, all M and both forms ({s:.1f} s)"}
+
+    oracle_cfg = oracle_configs() if (rank == 0 and world == 1 and not args.no_cpu) else None
 
     if rank == 0:
         line = {"metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -621,7 +723,8 @@ def run_ours(args):
                 "e2e": {"value": round(e2e, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                         "d2h_bytes_per_step": d2h},
                 "gpu_launches": launches * args.steps,
-                "clocks": ck, "sweep_GBps": sweep, "prefill": prefill, "small_configs": small, "next_types": nxt}
+                "clocks": ck, "sweep_GBps": sweep, "prefill": prefill, "prefill_points": prefill_points,
+                "small_configs": small, "next_types": nxt, "oracle_configs": oracle_cfg}
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

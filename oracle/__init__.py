@@ -71,6 +71,7 @@ def _load():
             lib.orc_matmul_int8_act.argtypes = [ctypes.c_int, p, p, i64, i64, i64, p, p]
             lib.orc_matmul_f32_act.argtypes = [ctypes.c_int, p, p, i64, i64, i64, p, p]
             lib.orc_num_threads.restype = ctypes.c_int
+            lib.orc_set_num_threads.argtypes = [ctypes.c_int]
             _lib = lib
     return _lib
 
@@ -104,6 +105,12 @@ def row_bytes(t, K: int) -> int:
 
 def num_threads() -> int:
     return int(_load().orc_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """Threads of the oracle's parallel loops (n <= 0: all available); the
+    results do not depend on it."""
+    _load().orc_set_num_threads(int(n))
 
 
 def f32_to_f16_bits(x) -> np.ndarray:

@@ -747,3 +747,14 @@ int orc_num_threads(void) {
     return 1;
 #endif
 }
+
+/* Threads used by the parallel loops from now on (n <= 0: all available).
+   Each output element's summation order is fixed, so results do not depend
+   on it; the benchmark times the single-threaded configurations with 1. */
+void orc_set_num_threads(int n) {
+#ifdef _OPENMP
+    omp_set_num_threads(n > 0 ? n : omp_get_num_procs());
+#else
+    (void)n;
+#endif
+}
