@@ -434,6 +434,20 @@ def dequant_all_case(q, torch, stream, wq, t, N, K, Ms=(16, 256, 1024)):
 PREFILL_SHAPES = ((4096, 4096), (14336, 4096))
 PREFILL_MS = (16, 37, 64, 256, 1024)
 PREFILL_HEADLINE = "q8_0/int8_act/M1024/14336x4096"
+PREFILL_HEADLINE_F32 = "q8_0/f32_act/M1024/14336x4096"
+WARP_MMA_F16_PEAK = 605.0  # TFLOP/s, legacy warp-level f16 MMA on this GPU (register-only probe)
+
+
+def prefill_kernel(t: str, mode: str, M: int) -> str:
+    """The kernel qmm_matmul runs for a prefill shape with K % 256 = 0 (the
+    library's dispatch): the Metal form on the tcgen05 GEMM; the CPU form,
+    whose bound needs exact integer block sums, on the warp-MMA prefill GEMM
+    (Q8_0) or the streaming warp-MMA kernel; up to 16 rows, the decode kernel."""
+    if M <= 16:
+        return "qmm_dmma_kernel"
+    if mode == "f32_act":
+        return "qmm_tc_kernel"
+    return "qmm_prefill_kernel" if t == "q8_0" else "qmm_stream_kernel"
 
 
 def prefill_section(q, torch, stream, hbm_peak, bf16_peak):
@@ -442,12 +456,13 @@ def prefill_section(q, torch, stream, hbm_peak, bf16_peak):
     both forms).  Each point runs calls back to back over distinct quantized
     weight buffers that together exceed twice the L2 (so every call streams
     its weights from HBM), timed with CUDA events over the whole run.
-    Reported per point: algorithmic TOPS = 2 M N K / t and its fraction of
-    the measured bf16 tensor peak (the GEMM runs f16 tcgen05 MMAs, which run
-    at the bf16 rate); weight GB/s and its fraction of the measured HBM
-    bandwidth; the roofline time max(2 M N K / peak, bytes / HBM) with bytes =
-    weights + x + y, and roofline_frac = roofline time / measured time.  The
-    tcgen05 GEMM's three f16 passes are reported beside it as tensor_TFLOPs.
+    Reported per point: the kernel; algorithmic TOPS = 2 M N K / t and its
+    fraction of the measured bf16 tensor peak (tcgen05 f16 MMAs run at the
+    bf16 rate) and, for the warp-MMA kernels, of the legacy warp-level f16
+    MMA's rate; weight GB/s and its fraction of the measured HBM bandwidth;
+    the roofline time max(2 M N K / peak, bytes / HBM) with bytes = weights +
+    x + y, and roofline_frac = roofline time / measured time.  The tcgen05
+    GEMM's three f16 passes are reported beside it as tensor_TFLOPs.
     Returns (points, the dequantize-all comparison)."""
     l2 = getattr(torch.cuda.get_device_properties(0), "L2_cache_size", 0) or 129 * 1024 * 1024
     points, deq = {}, {}
@@ -465,9 +480,8 @@ def prefill_section(q, torch, stream, hbm_peak, bf16_peak):
                 w[:, cols] *= 8.0
                 bufs.append(q.quantize_weights(w, t))
                 del w
-            modes = MODES if t != "q6_k" else MODES
             Ms = PREFILL_MS if t != "q6_k" else (37, 256, 1024)
-            for mode in modes:
+            for mode in MODES:
                 for M in Ms:
                     x = torch.from_numpy(qmm_synth.activations(M, K, outlier_channels=4)).cuda()
                     y = torch.empty((M, N), dtype=torch.float32, device="cuda")
@@ -485,15 +499,18 @@ def prefill_section(q, torch, stream, hbm_peak, bf16_peak):
                     ops = 2.0 * M * N * K
                     nbytes = wbytes + 4.0 * M * K + 4.0 * M * N
                     roof = max(ops / (bf16_peak * 1e12), nbytes / (hbm_peak * 1e9))
-                    pt = {"us": round(sec * 1e6, 2), "TOPS": round(ops / sec / 1e12, 1),
+                    kern = prefill_kernel(t, mode, M)
+                    pt = {"kernel": kern, "us": round(sec * 1e6, 2), "TOPS": round(ops / sec / 1e12, 1),
                           "frac_of_bf16_peak": round(ops / sec / 1e12 / bf16_peak, 4),
                           "weight_GBps": round(wbytes / sec / 1e9, 1),
                           "frac_of_hbm": round(nbytes / sec / 1e9 / hbm_peak, 4),
                           "bound": "tensor" if ops / (bf16_peak * 1e12) > nbytes / (hbm_peak * 1e9) else "hbm",
                           "roofline_us": round(roof * 1e6, 2), "roofline_frac": round(roof / sec, 4),
                           "buffers": nbuf, "launches_per_call": q.matmul_launches(t, mode, M, N, K)}
-                    if M > 16 and t != "q6_k":  # the tcgen05 GEMM: three f16 passes
+                    if kern == "qmm_tc_kernel":  # three f16 passes
                         pt["tensor_TFLOPs"] = round(3 * ops / sec / 1e12, 1)
+                    else:
+                        pt["frac_of_warp_mma_f16_peak"] = round(ops / sec / 1e12 / WARP_MMA_F16_PEAK, 4)
                     points[f"{t}/{mode}/M{M}/{N}x{K}"] = pt
             if t == "q8_0":
                 deq[f"{N}x{K}"] = dequant_all_case(q, torch, stream, bufs[0], t, N, K)
@@ -682,9 +699,14 @@ def run_ours(args):
     if not args.no_prefill:
         prefill_points, dequant_all = prefill_section(q, torch, stream, hbm_peak, bf16_peak)
         head = prefill_points.get(PREFILL_HEADLINE)
+        hf = prefill_points.get(PREFILL_HEADLINE_F32)
         if head:
-            prefill = {"point": PREFILL_HEADLINE, "TOPS": head["TOPS"], "frac_of_bf16_peak": head["frac_of_bf16_peak"],
+            prefill = {"point": PREFILL_HEADLINE, "kernel": head["kernel"], "TOPS": head["TOPS"],
+                       "frac_of_bf16_peak": head["frac_of_bf16_peak"],
+                       "frac_of_warp_mma_f16_peak": head.get("frac_of_warp_mma_f16_peak"),
                        "roofline_frac": head["roofline_frac"], "peak_TFLOPs": bf16_peak,
+                       "f32_act_point": PREFILL_HEADLINE_F32, "f32_act_TOPS": hf["TOPS"] if hf else None,
+                       "f32_act_frac_of_bf16_peak": hf["frac_of_bf16_peak"] if hf else None,
                        "l2": "weights rotated over distinct buffers totalling > 2 x L2"}
 
     small = small_configs(q, torch, stream) if not args.no_small else {}

@@ -108,12 +108,13 @@ size_t workspace_for(const StreamPlan& pl) {
 // The kernel a matmul call dispatches to and its plan.  Planning searches
 // chunk sizes and K splits, so decisions are cached per host thread by
 // (device, type, form, epilogue, M, N, K).
-enum Kind { KIND_NONE, KIND_GEMV, KIND_DMMA, KIND_TC, KIND_STREAM };
+enum Kind { KIND_NONE, KIND_GEMV, KIND_DMMA, KIND_TC, KIND_PREFILL, KIND_STREAM };
 struct Dispatch {
     Kind kind = KIND_NONE;
     GemvPlan gp;
     DmmaPlan dp;
     TcPlan tp;
+    PrefillPlan fp;
     StreamPlan sp;
     size_t workspace = 0;
     int launches = 0;
@@ -122,13 +123,14 @@ struct Dispatch {
 void plan_dispatch(int wt, int am, int epi, long long M, long long N, long long K, int sms, int smem, Dispatch& d) {
     d = Dispatch();
     if (wt == T_Q4_0 || wt == T_Q5_0 || wt == T_Q6_K) {
-        // up to 16 rows on 16-row warp-MMA tiles; Q4_0 / Q5_0 prefill on the tcgen05 GEMM
-        // where K allows; everything else (Q6_K prefill among it) on the streaming kernel
+        // up to 16 rows on 16-row warp-MMA tiles; Metal-form prefill on the tcgen05 GEMM
+        // where K allows (K % 256 = 0); the rest (the CPU form's exact block sums
+        // above 16 rows among it) on the streaming kernel
         if (M <= kDmmaMaxM && plan_dmma(wt, am, M, N, K, sms, smem, d.dp, epi == E_Y)) {
             d.kind = KIND_DMMA;
             d.workspace = d.dp.workspace;
             d.launches = 1 + (d.dp.ext_bytes ? 1 : 0) + (epi == E_Y && d.dp.p.kslices > 1 ? 1 : 0);
-        } else if (wt != T_Q6_K && epi == E_Y && M > kDecodeMaxM && plan_tc(wt, am, M, N, K, sms, smem, d.tp)) {
+        } else if (epi == E_Y && am == A_F32 && M > kDecodeMaxM && plan_tc(wt, M, N, K, sms, smem, d.tp)) {
             d.kind = KIND_TC;
             d.workspace = d.tp.workspace;
             d.launches = 2;  // operand preparation, GEMM
@@ -146,10 +148,14 @@ void plan_dispatch(int wt, int am, int epi, long long M, long long N, long long 
         d.kind = KIND_DMMA;
         d.workspace = d.dp.workspace;
         d.launches = 1 + (d.dp.ext_bytes ? 1 : 0) + (epi == E_Y && d.dp.p.kslices > 1 ? 1 : 0);
-    } else if (epi == E_Y && plan_tc(wt, am, M, N, K, sms, smem, d.tp)) {  // prefill: tcgen05 GEMM
+    } else if (epi == E_Y && am == A_F32 && plan_tc(wt, M, N, K, sms, smem, d.tp)) {  // Metal-form prefill: tcgen05 GEMM
         d.kind = KIND_TC;
         d.workspace = d.tp.workspace;
         d.launches = 2;  // operand preparation, GEMM
+    } else if (epi == E_Y && am == A_INT8 && plan_prefill(wt, M, N, K, sms, smem, d.fp)) {  // CPU-form prefill (Q8_0): exact block sums
+        d.kind = KIND_PREFILL;
+        d.workspace = d.fp.workspace;
+        d.launches = 2;  // activation codes, GEMM
     } else if (plan_stream(wt, am, epi, M, N, K, sms, smem, d.sp)) {
         d.kind = KIND_STREAM;
         d.workspace = epi == E_Y ? workspace_for(d.sp) : 0;
@@ -228,7 +234,13 @@ qmm_status stream_call(qmm_type wtype, int am, int epi, const void* wq, const fl
         if (!ws || ws_bytes < d.tp.workspace) return QMM_ERR_WORKSPACE;
         TcPlan tp = d.tp;
         tp.p.err = err;
-        return launch_tc(wt, am, tp, wq, x, ws, y, smem, s) == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
+        return launch_tc(wt, tp, wq, x, ws, y, smem, s) == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
+    }
+    if (d.kind == KIND_PREFILL) {
+        if (!ws || ws_bytes < d.fp.workspace) return QMM_ERR_WORKSPACE;
+        PrefillPlan fp = d.fp;
+        fp.p.err = err;
+        return launch_prefill(fp, wq, x, ws, y, smem, s) == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
     }
     if (d.kind != KIND_STREAM) return QMM_ERR_SHAPE;
     StreamPlan pl = d.sp;

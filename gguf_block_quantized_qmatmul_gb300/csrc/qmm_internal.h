@@ -5,6 +5,7 @@
 
 #include "qmm_dmma.cuh"
 #include "qmm_gemv.cuh"
+#include "qmm_prefill.cuh"
 #include "qmm_tc.cuh"
 #include "qmm_stream.cuh"
 
@@ -24,8 +25,14 @@ cudaError_t launch_dmma(int wt, int am, int epi, const DmmaPlan& plan, int smem_
 cudaError_t launch_dmma_x_0(int wt, int am, int epi, const DmmaPlan& plan, int smem_max, cudaStream_t s);
 cudaError_t launch_dmma_q6_k(int am, int epi, const DmmaPlan& plan, int smem_max, cudaStream_t s);
 cudaError_t launch_dmma_prep(int wt, int am, const DmmaPlan& plan, void* ext, cudaStream_t s);
-cudaError_t launch_tc(int wt, int am, const TcPlan& plan, const void* wq, const float* x, void* ws, float* y, int smem_max,
+cudaError_t launch_tc(int wt, const TcPlan& plan, const void* wq, const float* x, void* ws, float* y, int smem_max,
                       cudaStream_t s);
+cudaError_t launch_prefill(const PrefillPlan& plan, const void* wq, const float* x, void* ws, float* y, int smem_max,
+                           cudaStream_t s);
+// A 2-D tensor map (rows of `inner` elements, `row_bytes` apart) with a box
+// of box_inner x box_outer elements; false when the driver refuses it.
+bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, unsigned long long inner, unsigned long long outer,
+              unsigned long long row_bytes, unsigned box_inner, unsigned box_outer, CUtensorMapSwizzle swz);
 
 // many independent small matmuls in one launch (qmm_batch.cu)
 constexpr int kBatchMax = 256;  // items per launch (the launch parameters carry the table)

@@ -1,29 +1,31 @@
-// qmm_tc.cuh -- prefill GEMM (M > 8 activation rows) on the 5th-generation
-// tensor cores: tcgen05.mma with the accumulator in tensor memory.
+// qmm_tc.cuh -- the Metal form's prefill GEMM (f32_act, M > 16 activation
+// rows) on the 5th-generation tensor cores: tcgen05.mma with the accumulator
+// in tensor memory.
 //
-// Both QMatMul forms ("同一个 GGUF，CPU 和 Metal 生成的文字不一样" section 出处)
-// are the exact sum y = sum_k a_k w_k of dequantized operands:
-//   int8_act: a = f(d_a) q_a, the row-quantized activations (Q8_0 or Q8K);
-//             sum_k a_k w_k equals the CPU form's sum_b f(d_w) f(d_a) isum_b
-//             (both are the same real number; only rounding order differs);
-//   f32_act:  a = x.
-//   w = f(d) q (Q8_0) or (f(d) sc) q - f(dmin) m (Q4_K), one f32 rounding.
-// tcgen05 has no integer kind on sm_103a and its f16 kind carries 11 bits per
-// operand, so every operand is scaled by a power of two per row (activation
-// rows and weight rows separately, into [2^14, 2^15) at the row maximum) and
-// split into two f16 pieces, v = hi + lo (exact for the 18-19 significant
-// bits of f(d) q, 2^-22 relative otherwise); the product takes three MMAs,
-// hi.hi + hi.lo + lo.hi (the dropped lo.lo is below 2^-22 relative), into an
-// f32 accumulator restarted every kchunk raw stages (see kTcChunkInt8), and the
-// epilogue multiplies by 2^-(s_row + s_col) and adds the chunks.
+// "同一个 GGUF，CPU 和 Metal 生成的文字不一样" section 出处: the Metal form
+// multiplies f32 activations by weights dequantized in the kernel,
+//   y = sum_k x_k w_k, w = f(d) q (Q8_0), (f(d) sc) q - f(dmin) m (Q4_K),
+//   f(d) (code - off) (Q4_0, Q5_0) or (f(d) sc) code (Q6_K).
+// Its parity bound is taken over the element products x_k w_k, which an f32
+// accumulation meets.  (The CPU form's bound is taken over block terms, which
+// can cancel far more; it runs on kernels that form exact integer block
+// sums.)  tcgen05 has no integer kind on sm_103a and its f16 kind carries 11
+// bits per operand, so every operand is scaled by a power of two per row
+// (activation rows and weight rows separately, into [2^14, 2^15) at the row
+// maximum) and split into two f16 pieces, v = hi + lo (2^-22 relative); the
+// product takes three MMAs, hi.hi + hi.lo + lo.hi (the dropped lo.lo is below
+// 2^-22 relative), into an f32 accumulator restarted every kchunk raw stages
+// (see kTcChunk1), and the epilogue multiplies by 2^-(s_row + s_col) and adds
+// the chunks.
 //
 // One persistent CTA per SM over work units: an output tile of 128 weight
 // rows x bx activation rows (bx <= 256, a multiple of 16, the MMA's N) and
 // one of ks slices of K.  18 warps:
-//   producer  TMA: raw weight rows (2-D box, 128 rows x 272 B = 8 Q8_0 blocks,
-//             or 144 B = 1 Q4_K super-block, per 256 K; up to six stages in
-//             flight) and the activation pieces (bx rows x 32 f16, 64-byte
-//             swizzle, hi and lo, per 32 K);
+//   producer  TMA: raw weight rows (2-D box of 128 rows per 256 K: 272 B = 8
+//             Q8_0 blocks, 144 B = 1 Q4_K super-block or 8 Q4_0 blocks, 176 B
+//             = 8 Q5_0 blocks, or a 240-byte slot holding 1 Q6_K super-block;
+//             up to six stages in flight) and the activation pieces (bx rows
+//             x 32 f16, 64-byte swizzle, hi and lo, per 32 K);
 //   MMA       one thread: per 32-K stage six tcgen05.mma (M 128, N bx, K 16:
 //             hi.hi, hi.lo, lo.hi, two K steps each) with the weights as the A
 //             operand in tensor memory and the activation piece from shared
@@ -43,20 +45,9 @@
 // four stages x 32 columns of weight pieces at column 256.
 #pragma once
 
-#include <cuda.h>
-
 #include "qmm_device.cuh"
 
 namespace qmm {
-
-// load one TMA box (2-D) into shared memory, completing on an mbarrier
-__device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-            dst),
-        "l"(map), "r"(x), "r"(y), "r"(bar)
-        : "memory");
-}
 
 constexpr int kTcBW = 128;      // weight rows per tile (MMA M, the TMEM lanes)
 constexpr int kTcBXMax = 256;   // activation rows per tile, at most (MMA N)
@@ -73,18 +64,15 @@ constexpr int kTcWCol0 = 256;   // weight pieces: stage s at 256 + 32 s (hi 16 c
 constexpr int kTcMaxSplit = 16;
 // Accumulation chunks.  The tensor core's f32 accumulation truncates: its
 // error grows with the number of MMAs chained into one accumulator and leans
-// toward zero.  Over a whole 4096-K unit (768 f16 MMAs of three passes) the
-// CPU form's worst output reached the parity bound at 14336 x 4096, M = 1024
-// (that bound is taken over block terms, which cancel less than element
-// products; the Metal form's bound, over element products, kept a 4x
-// margin).  So a unit restarts its accumulator every `kchunk` raw stages and
-// the epilogue adds the chunks' results into y in f32 with round-to-nearest;
-// the worst error falls about as the chunk length does.  With two
-// accumulators (bx <= 128) the epilogue drains one chunk while the MMAs fill
-// the other: 1024 K.  With one, the MMAs wait for each drain: 2048 K for the
-// CPU form, 4096 K for the Metal form.  (Tiles of at most 192 rows, which
-// would leave room for two accumulators, measured 35 % slower at M = 1024.)
-constexpr int kTcChunkDouble = 4, kTcChunkInt8 = 8, kTcChunkF32 = 16;
+// toward zero (measured: at 14336 x 4096, M = 1024, 768 chained MMAs put the
+// worst output at 0.23 of the bound, 0.07 when the chains were eight times
+// shorter).  A unit restarts its accumulator every `kchunk` raw stages and
+// the epilogue adds the chunks' results into y in f32 with round-to-nearest.
+// With two accumulators (bx <= 128) the epilogue drains one chunk while the
+// MMAs fill the other: 1024 K.  With one, the MMAs wait for each drain: 4096 K.
+// (Tiles of at most 192 rows, which would leave room for two accumulators,
+// measured 35 % slower at M = 1024.)
+constexpr int kTcChunk2 = 4, kTcChunk1 = 16;
 
 struct TcParams {
     float* y;
@@ -284,6 +272,45 @@ __device__ __forceinline__ void tc_conv_x_0(const uint8_t* row, float wsc, uint3
     }
 }
 
+// Q6_K stage J (0..7) of a super-block repacked into a 240-byte slot at sbk
+// (16-byte aligned; the preparation launch copies each 210-byte super-block
+// there: ql[128], qh[64], 16 int8 group scales, f16 d).  Value l of the stage
+// is value 32 J + l of the super-block: its low four bits are nibble
+// (J % 4) / 2 of ql[64 (J / 4) + 32 (J % 2) + l], its high two bits are bits
+// 2 (J % 4).. of qh[32 (J / 4) + l], the code is those six bits - 32, and its
+// group is 2 J + l / 16.  w 2^s = (f(d) 2^s sc) code, exact in f32 (18 + 6
+// bits), split as f16(v) + f16(v - f16(v)).
+template <int J>
+__device__ __forceinline__ void tc_conv_q6_k(const uint8_t* sbk, float wsc, uint32_t h[16], uint32_t l[16]) {
+    constexpr int H = J >> 2, Q = J & 3;
+    const uint4 a0 = *reinterpret_cast<const uint4*>(sbk + 64 * H + 32 * (Q & 1));
+    const uint4 a1 = *reinterpret_cast<const uint4*>(sbk + 64 * H + 32 * (Q & 1) + 16);
+    const uint4 b0 = *reinterpret_cast<const uint4*>(sbk + 128 + 32 * H);
+    const uint4 b1 = *reinterpret_cast<const uint4*>(sbk + 128 + 32 * H + 16);
+    const uint4 sc = *reinterpret_cast<const uint4*>(sbk + 192);
+    const uint4 dd = *reinterpret_cast<const uint4*>(sbk + 208);
+    const uint32_t scw = (J < 2 ? sc.x : J < 4 ? sc.y : J < 6 ? sc.z : sc.w) >> (16 * (J & 1));  // sc_2J, sc_2J+1
+    const float fd = h2f(dd.x) * wsc;
+    const float e0 = fd * (float)(int8_t)(scw & 0xFFu), e1 = fd * (float)(int8_t)((scw >> 8) & 0xFFu);
+    const uint32_t qa[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+    const uint32_t qb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t c = ((qa[i] >> (4 * (Q >> 1))) & 0x0F0F0F0Fu) | (((qb[i] >> (2 * Q)) & 0x03030303u) << 4);
+        const float e = i < 4 ? e0 : e1;
+#pragma unroll
+        for (int p = 0; p < 2; ++p) {
+            const float v0 = e * (float)((int)((c >> (16 * p)) & 63u) - 32);
+            const float v1 = e * (float)((int)((c >> (16 * p + 8)) & 63u) - 32);
+            const __half2 hi = __floats2half2_rn(v0, v1);
+            const float2 hf = __half22float2(hi);
+            const __half2 lo = __floats2half2_rn(v0 - hf.x, v1 - hf.y);
+            h[2 * i + p] = *reinterpret_cast<const uint32_t*>(&hi);
+            l[2 * i + p] = *reinterpret_cast<const uint32_t*>(&lo);
+        }
+    }
+}
+
 // K slice `split` of ks: raw stages [r0, r1)
 __device__ __forceinline__ void tc_slice(const TcParams& p, int split, int& r0, int& r1) {
     r0 = split * p.nrs / p.ks;
@@ -315,6 +342,11 @@ __device__ __forceinline__ bool tc_convert_raw(const uint8_t* rrow, float wsc, l
             else if (u == 1) tc_conv_x_0<WT, G + 2>(rrow, wsc, h, l);
             else if (u == 2) tc_conv_x_0<WT, G + 4>(rrow, wsc, h, l);
             else tc_conv_x_0<WT, G + 6>(rrow, wsc, h, l);
+        } else if (WT == T_Q6_K) {
+            if (u == 0) tc_conv_q6_k<G>(rrow, wsc, h, l);
+            else if (u == 1) tc_conv_q6_k<G + 2>(rrow, wsc, h, l);
+            else if (u == 2) tc_conv_q6_k<G + 4>(rrow, wsc, h, l);
+            else tc_conv_q6_k<G + 6>(rrow, wsc, h, l);
         } else {
             if (u == 0) tc_conv_q4_k<G>(rrow, wsc, h, l);
             else if (u == 1) tc_conv_q4_k<G + 2>(rrow, wsc, h, l);
@@ -690,10 +722,15 @@ __device__ __forceinline__ float tc_row_iscale(float amax) {
 }
 
 // blocks [0, M): activation rows; blocks [M, M + ceil(N / 8)): 8 weight rows each (a warp per row)
-template <int WT, int AM>
+// Q6_K: every 210-byte super-block is also copied into a 240-byte slot of w6
+// (rows of K / 256 slots), which the GEMM's tensor map reads: 210-byte blocks
+// cannot start every copy on the 16-byte boundary a TMA copy needs.
+constexpr int kTcQ6Slot = 240;
+template <int WT>
 __global__ void __launch_bounds__(kTcPrepThreads) tc_prep_kernel(const float* __restrict__ x, const uint8_t* __restrict__ wq,
                                                                  int M, int N, int K, __half* ahi, __half* alo,
-                                                                 float* ais, float* wis, unsigned* cnt, int ncnt) {
+                                                                 float* ais, float* wis, unsigned* cnt, int ncnt,
+                                                                 uint8_t* __restrict__ w6) {
     grid_dep_launch();
     __shared__ float red[kTcPrepThreads / 32];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -714,7 +751,6 @@ __global__ void __launch_bounds__(kTcPrepThreads) tc_prep_kernel(const float* __
         amax = red[0];
 #pragma unroll
         for (int i = 1; i < kTcPrepThreads / 32; ++i) amax = fmaxf(amax, red[i]);
-        // int8: |f(d_a) q| <= amax (1 + 2^-11), still below 2^15 after scaling
         const float is = tc_row_iscale(amax);
         const float sc = __frcp_rn(is);
         if (tid == 0) ais[m] = is;
@@ -735,25 +771,8 @@ __global__ void __launch_bounds__(kTcPrepThreads) tc_prep_kernel(const float* __
                 v[4 * i + 2] = t.z;
                 v[4 * i + 3] = t.w;
             }
-            if (AM == A_F32) {
 #pragma unroll
-                for (int i = 0; i < 16; ++i) v[i] = __fmul_rn(v[i], sc);
-            } else {
-                float bm = 0.0f;
-#pragma unroll
-                for (int i = 0; i < 16; ++i) bm = fmaxf(bm, fabsf(v[i]));
-                bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 1));  // Q8_0: the block's other half
-                if (!is_b32(WT)) {                                       // Q8K: sixteen threads
-                    bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 2));
-                    bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
-                    bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 8));
-                }
-                float d, id;
-                q8_scale(bm, d, id);
-                const float ds = (is_b32(WT) ? h2f(f2h(d)) : d) * sc;  // f(d_a) 2^s (Q8_0 keeps d as f16)
-#pragma unroll
-                for (int i = 0; i < 16; ++i) v[i] = is_b32(WT) ? ds * (float)q8_code(v[i], id) : __fmul_rn(d * (float)q8_code(v[i], id), sc);
-            }
+            for (int i = 0; i < 16; ++i) v[i] = __fmul_rn(v[i], sc);
             if (on) {
                 uint32_t hw[8], lw[8];
 #pragma unroll
@@ -783,6 +802,23 @@ __global__ void __launch_bounds__(kTcPrepThreads) tc_prep_kernel(const float* __
             constexpr float CM = WT == T_Q8_0 ? 127.0f : WT == T_Q5_0 ? 16.0f : 8.0f;
             const uint8_t* row = wq + n * (long long)(K / 32) * BB;
             for (int b = lane; b < K / 32; b += 32) bmax = fmaxf(bmax, fabsf(h2f(*reinterpret_cast<const uint16_t*>(row + b * BB))) * CM);
+        } else if (WT == T_Q6_K) {
+            // |w| <= |f(d)| max_j |sc_j| 32; the row's super-blocks to their slots (2-byte words)
+            const int nsb = K / 256;
+            const uint8_t* row = wq + n * (long long)nsb * 210;
+            for (int b = lane; b < nsb; b += 32) {
+                const uint8_t* sb = row + b * 210;
+                int scm = 0;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) scm = max(scm, abs((int)(int8_t)__ldg(sb + 192 + j)));
+                bmax = fmaxf(bmax, fabsf(h2f(__ldg(reinterpret_cast<const unsigned short*>(sb + 208)))) * (float)scm * 32.0f);
+            }
+            const uint16_t* src = reinterpret_cast<const uint16_t*>(row);
+            uint16_t* dst = reinterpret_cast<uint16_t*>(w6 + n * (long long)nsb * kTcQ6Slot);
+            for (int i = lane; i < nsb * 105; i += 32) {
+                const int b = i / 105, hw = i - 105 * b;
+                dst[b * (kTcQ6Slot / 2) + hw] = __ldg(src + i);
+            }
         } else {
             const uint8_t* row = wq + n * (long long)(K / 256) * 144;
             for (int b = lane; b < K / 256; b += 32) {
@@ -803,7 +839,7 @@ struct TcPlan {
     TcParams p;
     int grid;
     size_t smem;
-    size_t ws_ahi, ws_alo, ws_ais, ws_wis, ws_part, ws_cnt, workspace;
+    size_t ws_ahi, ws_alo, ws_ais, ws_wis, ws_part, ws_cnt, ws_w6, workspace;
 };
 
 // Modelled SM cycles of one work unit of `nr` raw stages (fitted to GB300
@@ -820,7 +856,7 @@ inline double tc_unit_cycles(int bx, int nacc, int kchunk, int ks, int nr, bool 
     return c;
 }
 
-inline bool plan_tc(int wt, int am, long long M, long long N, long long K, int sm_count, int smem_max, TcPlan& out) {
+inline bool plan_tc(int wt, long long M, long long N, long long K, int sm_count, int smem_max, TcPlan& out) {
     if (K % kTcRK != 0 || M < 9 || K > (1 << 26) || M > (1 << 24) || N > (1 << 24)) return false;
     TcPlan pl{};
     TcParams& p = pl.p;
@@ -830,11 +866,11 @@ inline bool plan_tc(int wt, int am, long long M, long long N, long long K, int s
     p.mtiles = (int)((M + kTcBXMax - 1) / kTcBXMax);
     p.bx = round_up((int)((M + p.mtiles - 1) / p.mtiles), 16);
     p.nacc = p.bx <= 128 ? 2 : 1;
-    p.kchunk = p.nacc == 2 ? kTcChunkDouble : am == A_INT8 ? kTcChunkInt8 : kTcChunkF32;
+    p.kchunk = p.nacc == 2 ? kTcChunk2 : kTcChunk1;
     p.ntiles = (int)((N + kTcBW - 1) / kTcBW);
     p.tiles = p.mtiles * p.ntiles;
     p.nrs = (int)(K / kTcRK);
-    p.raw_row = wt == T_Q8_0 ? kTcRK / 32 * 34 : wt == T_Q5_0 ? kTcRK / 32 * 22 : 144;  // Q4_K, Q4_0: 144
+    p.raw_row = wt == T_Q8_0 ? kTcRK / 32 * 34 : wt == T_Q5_0 ? kTcRK / 32 * 22 : wt == T_Q6_K ? kTcQ6Slot : 144;  // Q4_K, Q4_0: 144
     p.raw_stage = round_up(kTcBW * p.raw_row, 1024);
     p.piece = p.bx * 64;
     p.off_raw = kTcS * 2 * p.piece;  // activation pieces; weight pieces live in TMEM
@@ -881,7 +917,8 @@ inline bool plan_tc(int wt, int am, long long M, long long N, long long K, int s
     pl.ws_wis = pl.ws_ais + r256((size_t)M * 4);
     pl.ws_part = pl.ws_wis + r256((size_t)N * 4);
     pl.ws_cnt = pl.ws_part + (p.ks > 1 ? r256((size_t)p.ks * M * N * 4) : 0);
-    pl.workspace = pl.ws_cnt + (p.ks > 1 ? r256((size_t)p.tiles * 4) : 0);
+    pl.ws_w6 = pl.ws_cnt + (p.ks > 1 ? r256((size_t)p.tiles * 4) : 0);
+    pl.workspace = pl.ws_w6 + (wt == T_Q6_K ? r256((size_t)N * (K / 256) * kTcQ6Slot) : 0);
     out = pl;
     return true;
 }

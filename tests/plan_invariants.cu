@@ -104,7 +104,7 @@ int check_gemv(int wt, long long M, long long N, long long K) {
 
 int check_tc(int wt, long long M, long long N, long long K) {
     TcPlan pl;
-    if (!plan_tc(wt, A_INT8, M, N, K, kSms, kSmem, pl)) return 0;
+    if (!plan_tc(wt, M, N, K, kSms, kSmem, pl)) return 0;
     const TcParams& p = pl.p;
 #define CASE "tc %s M%lld N%lld K%lld", tname(wt), M, N, K
     CHECK(pl.smem <= (size_t)kSmem, CASE);
@@ -115,8 +115,8 @@ int check_tc(int wt, long long M, long long N, long long K) {
     CHECK(p.bx % 16 == 0 && p.bx >= 16 && p.bx <= kTcBXMax && (long long)p.bx * p.mtiles >= M, CASE);
     // TMEM: the accumulators plus four stages of 32 weight-piece columns fit the 512 columns
     CHECK((p.nacc == 2 ? 2 * 128 : 256) + kTcS * 32 <= kTcTmemCols && p.nacc == (p.bx <= 128 ? 2 : 1), CASE);
-    // accumulation chunks: 1024 K with two accumulators; 2048 K (CPU form) or 4096 K (Metal form) with one
-    CHECK(p.kchunk == (p.nacc == 2 ? 4 : 8), CASE);
+    // accumulation chunks: 1024 K with two accumulators, 4096 K with one
+    CHECK(p.kchunk == (p.nacc == 2 ? 4 : 16), CASE);
     CHECK(p.ntiles == (int)((N + kTcBW - 1) / kTcBW) && p.tiles == p.mtiles * p.ntiles, CASE);
     CHECK(p.ks >= 1 && p.ks <= p.nrs && p.units == p.tiles * p.ks, CASE);
     CHECK(pl.grid == (p.units < kSms ? p.units : kSms), CASE);
@@ -124,6 +124,27 @@ int check_tc(int wt, long long M, long long N, long long K) {
               pl.ws_part >= pl.ws_wis + N * 4 && pl.workspace >= pl.ws_cnt,
           CASE);
     if (p.ks > 1) CHECK(pl.ws_cnt >= pl.ws_part + (size_t)p.ks * M * N * 4 && pl.workspace >= pl.ws_cnt + p.tiles * 4, CASE);
+    // Q6_K: the super-blocks repacked into 240-byte slots (16-byte aligned rows for the tensor map)
+    if (wt == T_Q6_K)
+        CHECK(p.raw_row == kTcQ6Slot && pl.ws_w6 >= pl.ws_cnt && pl.ws_w6 % 256 == 0 &&
+                  pl.workspace >= pl.ws_w6 + (size_t)N * (K / 256) * kTcQ6Slot && (K / 256 * kTcQ6Slot) % 16 == 0,
+              CASE);
+#undef CASE
+    return 1;
+}
+
+int check_prefill(long long M, long long N, long long K) {
+    PrefillPlan pl;
+    if (!plan_prefill(T_Q8_0, M, N, K, kSms, kSmem, pl)) return 0;
+    const PrefillParams& p = pl.p;
+#define CASE "prefill M%lld N%lld K%lld", M, N, K
+    CHECK(pl.smem <= (size_t)kSmem && p.stages >= 2 && p.stages <= 4, CASE);
+    CHECK(p.off_a % 1024 == 0 && p.off_s == p.off_a + 4 * p.bm * 128 && p.stage_bytes % 1024 == 0 &&
+              p.stage_bytes >= p.off_s + p.bm * 32,
+          CASE);
+    CHECK(p.kchunks * kPfKC == K && (long long)p.n_mt * p.bm >= M && (long long)p.n_nt * kPfBN >= N, CASE);
+    CHECK(pl.grid >= 1 && pl.grid <= kSms && pl.ws_s == (size_t)M * K * 2 && pl.workspace >= pl.ws_s + (size_t)M * (K / 32) * 4,
+          CASE);
 #undef CASE
     return 1;
 }
@@ -177,11 +198,12 @@ int main() {
                     plans += check_gemv(wt, M, N, K);
                 }
     for (int wt : types) {
-        if (wt == T_Q6_K) continue;  // Q6_K prefill runs the streaming kernel
         for (long long M : {17, 37, 64, 255, 256, 300, 1024, 4097})
             for (long long N : {128, 300, 4096, 14336})
-                for (long long K : {256, 1024, 4096, 14336})
+                for (long long K : {256, 1024, 4096, 14336}) {
                     plans += check_tc(wt, M, N, K);
+                    if (wt == T_Q8_0) plans += check_prefill(M, N, K);
+                }
     }
     for (int wt : types)
         for (int am : {A_INT8, A_F32})
@@ -201,8 +223,12 @@ int main() {
             for (long long M : {1, 2, 4, 8, 16})
                 CHECK(plan_dmma(wt, am, M, 28672, 8192, kSms, kSmem, dp, true), "no decode plan for %s am%d M%lld", tname(wt), am, M);
     TcPlan tp;
+    PrefillPlan fp;
     for (long long M : {37, 64, 256, 1024})
-        CHECK(plan_tc(T_Q8_0, A_INT8, M, 14336, 4096, kSms, kSmem, tp), "no tcgen05 plan for M%lld", M);
+        for (int wt : types) {
+            CHECK(plan_tc(wt, M, 14336, 4096, kSms, kSmem, tp), "no tcgen05 plan for %s M%lld", tname(wt), M);
+            if (wt == T_Q8_0) CHECK(plan_prefill(wt, M, 14336, 4096, kSms, kSmem, fp), "no exact prefill plan for M%lld", M);
+        }
     std::printf("%s %d plans\n", g_bad ? "FAILED" : "ok", plans);
     return g_bad ? 1 : 0;
 }

@@ -282,11 +282,12 @@ def test_prepared_activations_edge_rows(qmm, orc, wtype, N, M, mode):
 
 
 @pytest.mark.parametrize("mode", ["int8_act", "f32_act"])
-@pytest.mark.parametrize("wtype,M,K", [("q6_k", 37, 1536), ("q6_k", 37, 8192), ("q8_0", 37, 576), ("q5_0", 37, 576),
-                                       ("q4_0", 20, 576)])
-def test_streaming_kernel_edge_rows(qmm, orc, wtype, M, K, mode):
-    """The streaming warp-MMA kernel (all Q6_K prefill; 32-value blocks with
-    K % 256 != 0 above 16 rows), with and without a K split: adversarial rows
+@pytest.mark.parametrize("wtype,M,K", [("q8_0", 37, 576), ("q5_0", 37, 576), ("q4_0", 20, 576), ("q8_0", 300, 96),
+                                       ("q6_k", 37, 1536), ("q6_k", 37, 8192), ("q6_k", 300, 512)])
+def test_prefill_kernels_edge_rows(qmm, orc, wtype, M, K, mode):
+    """Prefill above 16 rows: the streaming warp-MMA kernel (32-value blocks
+    with K % 256 != 0) and the tcgen05 GEMM on Q6_K (super-blocks repacked
+    into 16-byte aligned slots), with and without a K split: adversarial rows
     in both operands."""
     w, x = edge_operands(wtype, K, M, n_plain=50, seed=60)
     wq = orc.quantize(wtype, w)
@@ -424,14 +425,17 @@ def test_launch_counts(qmm):
     assert qmm.matmul_launches("q4_k", "int8_act", 2, 28672, 8192) == 1
     assert qmm.matmul_launches("q4_k", "int8_act", 8, 28672, 8192) == 2
     assert qmm.matmul_launches("q8_0", "f32_act", 8, 28672, 8192) == 3    # K split: reduction after
-    assert qmm.matmul_launches("q8_0", "int8_act", 256, 4096, 4096) == 2  # prefill: operand + GEMM
+    assert qmm.matmul_launches("q8_0", "int8_act", 256, 4096, 4096) == 2  # exact prefill: activation codes + GEMM
+    assert qmm.matmul_launches("q8_0", "f32_act", 256, 4096, 4096) == 2   # tcgen05: operand pieces + GEMM
+    assert qmm.matmul_launches("q4_k", "int8_act", 256, 4096, 4096) == 1  # exact block sums: the streaming kernel
     assert qmm.matmul_launches("q8_0", "int8_act", 1, 100, 100) == 0      # K not a multiple of 32
     assert qmm.matmul_launches("q5_0", "int8_act", 1, 576, 576) == 1      # Q4_0 / Q5_0 decode: the MMA kernel
     assert qmm.matmul_launches("q4_0", "f32_act", 8, 28672, 8192) == 3    # large: preparing kernel, K split
     assert qmm.matmul_launches("q4_0", "f32_act", 64, 4096, 4096) == 2     # prefill, K % 256 = 0: tcgen05
     assert qmm.matmul_launches("q5_0", "int8_act", 64, 576, 576) == 1     # K = 576: the streaming kernel
     assert qmm.matmul_launches("q6_k", "int8_act", 1, 576, 1536) == 1     # Q6_K decode: the MMA kernel
-    assert qmm.matmul_launches("q6_k", "f32_act", 256, 4096, 4096) == 1
+    assert qmm.matmul_launches("q6_k", "f32_act", 256, 4096, 4096) == 2   # Q6_K prefill: tcgen05 (repack + GEMM)
+    assert qmm.matmul_launches("q5_0", "f32_act", 256, 576, 576) == 1     # K % 256 != 0: the streaming kernel
 
 
 CHAIN_SHAPES = {"q8_0": [(8192, 8192), (576, 8192), (8192, 576), (8192, 8192)],
@@ -484,10 +488,13 @@ def test_chained_calls_wait_for_the_previous_output(qmm, orc, wtype, mode, M):
 @pytest.mark.parametrize("mode", ["int8_act", "f32_act"])
 @pytest.mark.parametrize("wtype", ["q8_0", "q4_k"])
 def test_chained_prefill_calls_wait_for_the_previous_output(qmm, orc, wtype, mode, M):
-    """The same chain on the tcgen05 GEMM, whose preparing grid reads the
-    weights' row scales before the previous GEMM has finished."""
+    """The same chain on the prefill kernels: the tcgen05 GEMM (f32_act),
+    whose preparing grid reads the weights' row scales before the previous
+    GEMM has finished, the exact Q8_0 prefill GEMM and the streaming kernel
+    (int8_act)."""
     launches = run_chain(qmm, orc, wtype, mode, M, PREFILL_CHAIN_SHAPES)
-    assert min(launches) == 2  # operand preparation + GEMM
+    # operand preparation + GEMM, except the single-launch streaming kernel (Q4_K int8_act)
+    assert min(launches) == (1 if (wtype, mode) == ("q4_k", "int8_act") else 2)
 
 
 def test_error_statuses_on_device(qmm, orc):
@@ -519,7 +526,8 @@ FULL = [("q4_k", 28672, 8192, 8), ("q8_0", 28672, 8192, 8), ("q6_k", 28672, 8192
         ("q8_0", 14336, 4096, 1024), ("q4_k", 14336, 4096, 1024),                       # tcgen05 GEMM
         ("q8_0", 14336, 4096, 256), ("q4_k", 4096, 4096, 256), ("q5_0", 14336, 4096, 256),
         ("q4_k", 14336, 4096, 37), ("q8_0", 14336, 4096, 64),
-        ("q6_k", 14336, 4096, 256),                                                     # streaming kernel
+        ("q6_k", 14336, 4096, 256), ("q6_k", 4096, 4096, 1024),                        # tcgen05, Q6_K repacked
+        ("q5_0", 49152, 576, 64),                                                       # streaming kernel (K % 256 != 0)
         ("q8_0", 4096, 4096, 16), ("q8_0", 49152, 576, 1), ("q5_0", 49152, 576, 1)]
 
 

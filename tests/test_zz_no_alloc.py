@@ -41,11 +41,12 @@ def _entry(q):
 
 # Shapes whose workspace the entry point takes from its own array: the decode
 # kernel with K split (partial sums only), the tcgen05 GEMM with K split (its
-# arrival counters must start at zero on every call) and the streaming kernel
-# with K split (the same, cleared by a memset on the stream).
-STATIC_CASES = [("q8_0", "f32_act", 8, 100, 8192), ("q8_0", "int8_act", 64, 300, 4096),
-                ("q4_k", "f32_act", 37, 256, 2048), ("q6_k", "int8_act", 37, 64, 4096),
-                ("q6_k", "f32_act", 37, 64, 4096)]
+# arrival counters must start at zero on every call; Q6_K also repacks its
+# weights there), the exact Q8_0 prefill GEMM (activation codes) and the
+# streaming kernel with K split (arrival counters cleared by a memset).
+STATIC_CASES = [("q8_0", "f32_act", 8, 100, 8192), ("q8_0", "f32_act", 64, 300, 4096),
+                ("q4_k", "f32_act", 37, 256, 2048), ("q6_k", "f32_act", 37, 64, 4096),
+                ("q8_0", "int8_act", 64, 300, 4096), ("q6_k", "int8_act", 37, 64, 4096)]
 
 
 @pytest.mark.parametrize("wtype,mode,M,N,K", STATIC_CASES)
