@@ -301,7 +301,8 @@ def small_configs(q, torch, stream):
     the L2 flushed before every step (a 2 x L2 buffer written, then read back
     so that no dirty line of it is written back inside the timed step):
     eagerly and replayed from a CUDA graph (211 launches), and as one
-    qmm_matmul_batch call."""
+    qmm_matmul_batch call; then the same step with the weight types of the
+    model's Q4_K_M file as one qmm_matmul_batch_typed call."""
     out = {}
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
 
@@ -390,6 +391,49 @@ def small_configs(q, torch, stream):
             ms = tot / (reps + 3)
             res[name] = {"ms_per_step": round(ms, 4), "weight_GBps": round(step_bytes / (ms * 1e6), 1), "launches": 1}
     out["smollm2_step_weight_bytes"] = step_bytes
+    # the same step with the weight types of the model's Q4_K_M file (Q5_0, Q8_0,
+    # Q4_K, Q6_K): 211 qmm_matmul calls replayed from a graph, and one
+    # qmm_matmul_batch_typed launch (direct and from a graph)
+    tl = qmm_synth.smollm2_q4_k_m_linears()
+    twq = []
+    for i, (_, N, K, t) in enumerate(tl):
+        g = torch.Generator(device="cuda").manual_seed(2000 + i)
+        twq.append((t, q.quantize_weights(torch.randn((N, K), generator=g, device="cuda") * 0.02, t), N, K))
+    tbytes = sum(w.numel() for _, w, _, _ in twq)
+    tys = [torch.empty((1, N), dtype=torch.float32, device="cuda") for _, _, N, _ in twq]
+    for mode in MODES:
+        def tstep():
+            for (t, w, N, K), y in zip(twq, tys):
+                q.matmul(w, xs[K], t, mode, N=N, out=y)
+        tstep()
+        torch.cuda.synchronize()
+        tgraph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(tgraph):
+            tstep()
+        tb = q.MatmulBatchTyped([(t, w, xs[K], y) for (t, w, N, K), y in zip(twq, tys)], mode)
+        tb.run()
+        torch.cuda.synchronize()
+        tbgraph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(tbgraph):
+            tb.run()
+        torch.cuda.synchronize()
+        res = {}
+        for name, fn in (("graph", tgraph.replay), ("batched", tb.run), ("batched_graph", tbgraph.replay)):
+            tot = 0.0
+            reps = 20
+            for _ in range(reps + 3):
+                flush_l2()
+                ev0.record(stream)
+                fn()
+                ev1.record(stream)
+                torch.cuda.synchronize()
+                tot += ev0.elapsed_time(ev1)
+            ms = tot / (reps + 3)
+            res[name] = {"ms_per_step": round(ms, 4), "weight_GBps": round(tbytes / (ms * 1e6), 1),
+                         "launches": 1 if name.startswith("batched") else len(twq)}
+        out[f"smollm2_step_211_matmuls q4_k_m M1 {mode} (L2 flushed)"] = res
+    out["smollm2_q4_k_m_step_weight_bytes"] = tbytes
+    assert q.last_device_error() == 0
     return out
 
 
@@ -559,6 +603,15 @@ def oracle_configs():
         s = time.perf_counter() - t0
         res[f"smollm2_step_211_matmuls q8_0 M1 {mode}"] = {"ms_per_step": round(s * 1e3, 2),
                                                             "threads": out["cores_all"]}
+    tl = qmm_synth.smollm2_q4_k_m_linears()
+    twq = [(t, oracle.quantize(t, qmm_synth.weights(N, K, seed=2000 + i)), K) for i, (_, N, K, t) in enumerate(tl)]
+    for mode in MODES:
+        t0 = time.perf_counter()
+        for t, wq, K in twq:
+            oracle.matmul(t, mode, wq, xs[K])
+        s = time.perf_counter() - t0
+        res[f"smollm2_step_211_matmuls q4_k_m M1 {mode}"] = {"ms_per_step": round(s * 1e3, 2),
+                                                              "threads": out["cores_all"]}
     rows = 512
     K = 4096
     for t in ("q8_0", "q4_k"):
@@ -760,6 +813,21 @@ def run_profile_case(spec: str, launches: int):
     import torch
 
     import gguf_block_quantized_qmatmul_gb300 as q
+    if spec.startswith("q4_k_m_batch:"):
+        _, mode = spec.split(":")
+        items = []
+        xs = {K: torch.from_numpy(qmm_synth.activations(1, K)).cuda() for K in (576, 1536)}
+        for i, (_, N, K, t) in enumerate(qmm_synth.smollm2_q4_k_m_linears()):
+            g = torch.Generator(device="cuda").manual_seed(2000 + i)
+            w = q.quantize_weights(torch.randn((N, K), generator=g, device="cuda") * 0.02, t)
+            items.append((t, w, xs[K], torch.empty((1, N), dtype=torch.float32, device="cuda")))
+        batch = q.MatmulBatchTyped(items, mode)
+        for _ in range(launches):
+            batch.run()
+        torch.cuda.synchronize()
+        assert q.last_device_error() == 0
+        print(f"profile case {spec}: {launches} launches ok")
+        return
     if spec.startswith("smollm2_batch:"):
         _, wtype, mode = spec.split(":")
         wqs = []
@@ -802,7 +870,7 @@ def main():
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-small", action="store_true")
-    ap.add_argument("--profile", default=None, help="wtype:mode:M:N:K or smollm2_batch:wtype:mode -- run a few launches for ncu and exit")
+    ap.add_argument("--profile", default=None, help="wtype:mode:M:N:K, smollm2_batch:wtype:mode or q4_k_m_batch:mode -- run a few launches for ncu and exit")
     ap.add_argument("--launches", type=int, default=4)
     args = ap.parse_args()
     if args.profile:

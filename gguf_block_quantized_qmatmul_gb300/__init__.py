@@ -13,6 +13,7 @@ Entry points mirror the C ABI names:
   matmul(wq, x, wtype, mode)      y = x . W^T, mode "int8_act" or "f32_act"
   block_sums(wq, x, wtype)        exact per-block integer sums of the int8_act form
   matmul_batch(items, wtype, mode)  many independent small matmuls in one launch
+  matmul_batch_typed(items, mode)   the same, each item with its own weight type
 """
 from __future__ import annotations
 
@@ -34,7 +35,7 @@ STATUS = {0: "QMM_OK", 1: "QMM_ERR_NULL", 2: "QMM_ERR_SHAPE", 3: "QMM_ERR_TYPE",
 # every symbol declared in include/qmm.h
 EXPORTS = ["qmm_block_values", "qmm_block_bytes", "qmm_row_bytes", "qmm_quantize_weights", "qmm_quantize_act",
            "qmm_dequantize", "qmm_matmul_workspace", "qmm_matmul_launches", "qmm_matmul", "qmm_matmul_static_workspace",
-           "qmm_block_sums", "qmm_matmul_batch", "qmm_test_inject", "qmm_test_set_wait_limit",
+           "qmm_block_sums", "qmm_matmul_batch", "qmm_matmul_batch_typed", "qmm_test_inject", "qmm_test_set_wait_limit",
            "qmm_last_device_error", "qmm_status_string"]
 INJECT = {"off": 0, "launch_failure": 1, "stall": 2}
 
@@ -63,6 +64,7 @@ def _load() -> ctypes.CDLL:
     lib.qmm_matmul.argtypes, lib.qmm_matmul.restype = [i32, i32, p, p, p, i64, i64, i64, p, sz, p], i32
     lib.qmm_block_sums.argtypes, lib.qmm_block_sums.restype = [i32, p, p, i64, i64, i64, p, p], i32
     lib.qmm_matmul_batch.argtypes, lib.qmm_matmul_batch.restype = [i32, i32, p, i64, p], i32
+    lib.qmm_matmul_batch_typed.argtypes, lib.qmm_matmul_batch_typed.restype = [i32, p, i64, p], i32
     lib.qmm_test_inject.argtypes, lib.qmm_test_inject.restype = [i32, i32, i32], i32
     lib.qmm_test_set_wait_limit.argtypes, lib.qmm_test_set_wait_limit.restype = [i32], i32
     lib.qmm_last_device_error.argtypes, lib.qmm_last_device_error.restype = [], i32
@@ -210,6 +212,38 @@ def matmul_batch(items, wtype, mode, stream=None):
     b = MatmulBatch(items, wtype, mode)
     b.run(stream)
     return [y for _, _, y in b.items]
+
+
+class TypedMatmulDesc(ctypes.Structure):
+    """qmm_matmul_typed_desc: one item of qmm_matmul_batch_typed."""
+    _fields_ = [("wtype", ctypes.c_int), ("wq", ctypes.c_void_p), ("x", ctypes.c_void_p), ("y", ctypes.c_void_p),
+                ("M", ctypes.c_int64), ("N", ctypes.c_int64), ("K", ctypes.c_int64)]
+
+
+class MatmulBatchTyped:
+    """A descriptor table for qmm_matmul_batch_typed, built once: items are
+    (wtype, wq, x, y), each with its own weight type (a decode step of a
+    mixed-type file); run() launches it (one launch per 256 items)."""
+
+    def __init__(self, items, mode):
+        self.items = list(items)  # keeps the tensors alive
+        self.mode = _m(mode)
+        self.descs = (TypedMatmulDesc * max(len(self.items), 1))()
+        for i, (t, wq, x, y) in enumerate(self.items):
+            M, K = x.shape
+            self.descs[i] = TypedMatmulDesc(_t(t), _ptr(wq), _ptr(x), _ptr(y), M, y.shape[1], K)
+        self.ptr = ctypes.cast(self.descs, ctypes.c_void_p)
+
+    def run(self, stream=None):
+        _check(_lib().qmm_matmul_batch_typed(self.mode, self.ptr, len(self.items), _stream(stream)),
+               "qmm_matmul_batch_typed")
+
+
+def matmul_batch_typed(items, mode, stream=None):
+    """One-off qmm_matmul_batch_typed over (wtype, wq, x, y) items; returns the ys."""
+    b = MatmulBatchTyped(items, mode)
+    b.run(stream)
+    return [y for _, _, _, y in b.items]
 
 
 def last_device_error() -> int:

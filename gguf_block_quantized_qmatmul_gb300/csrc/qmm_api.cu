@@ -388,20 +388,28 @@ qmm_status qmm_matmul(qmm_type wtype, qmm_act_mode mode, const void* wq, const f
                        workspace_bytes, stream);
 }
 
-qmm_status qmm_matmul_batch(qmm_type wtype, qmm_act_mode mode, const qmm_matmul_desc* items, int64_t count,
-                            qmm_stream_t stream) {
-    if (wtype != QMM_Q8_0 && wtype != QMM_Q4_0 && wtype != QMM_Q5_0) return QMM_ERR_TYPE;
+extern "C++" {
+namespace {
+
+// Both batch entry points: item i is get(i), a qmm_matmul_typed_desc.  Every
+// item is checked before anything is launched; then one launch per kBatchMax
+// live items, with the kernel of their one weight type when they share a
+// 32-value type, else the kernel whose items carry their own types.
+template <typename Get>
+qmm_status batch_run(qmm_act_mode mode, int64_t count, bool have_items, Get get, qmm_stream_t stream) {
     if (mode != QMM_INT8_ACT && mode != QMM_F32_ACT) return QMM_ERR_TYPE;
     if (count < 0) return QMM_ERR_SHAPE;
     if (count == 0) return QMM_OK;
-    if (!items) return QMM_ERR_NULL;
+    if (!have_items) return QMM_ERR_NULL;
     int64_t live = 0;
-    for (int64_t i = 0; i < count; ++i) {  // every item is checked before anything is launched
-        const qmm_matmul_desc& d = items[i];
+    for (int64_t i = 0; i < count; ++i) {
+        const qmm_matmul_typed_desc d = get(i);
+        if (!weight_type(d.wtype)) return QMM_ERR_TYPE;
         if (d.M < 0 || d.N < 0 || d.K < 0 || d.N > INT32_MAX) return QMM_ERR_SHAPE;
         if (d.M == 0 || d.N == 0) continue;
         ++live;
-        if (d.K == 0 || d.K % 32 != 0 || d.M > QMM_BATCH_MAX_M || d.M * d.K > QMM_BATCH_MAX_MK) return QMM_ERR_SHAPE;
+        if (d.K == 0 || d.K % qmm_block_values(d.wtype) != 0 || d.M > QMM_BATCH_MAX_M || d.M * d.K > QMM_BATCH_MAX_MK)
+            return QMM_ERR_SHAPE;
         if (!d.wq || !d.x || !d.y) return QMM_ERR_NULL;
         if (!aligned(d.wq, 16) || !aligned(d.x, 16) || !aligned(d.y, 4)) return QMM_ERR_ALIGN;
     }
@@ -409,20 +417,20 @@ qmm_status qmm_matmul_batch(qmm_type wtype, qmm_act_mode mode, const qmm_matmul_
     unsigned* err = nullptr;
     int sms = 0, smem = 0;
     if (device_info(&err, &sms, &smem) != cudaSuccess) return QMM_ERR_CUDA;
-    const int wt = internal_type(wtype);
-    const int bb = (int)qmm_block_bytes(wtype);
+    const int am = mode == QMM_INT8_ACT ? A_INT8 : A_F32;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    BatchParams p;  // ~10 KB: the item table travels in the launch parameters
+    BatchParams p;  // ~16 KB: the item table travels in the launch parameters
     int64_t i = 0;
     while (i < count) {
         p.count = 0;
         p.total = 0;
-        p.max_mk = 0;
+        p.act_bytes = 0;
         p.err = err;
-        int max_m = 1;
+        int max_m = 1, kind = -1;
         for (; i < count && p.count < kBatchMax; ++i) {
-            const qmm_matmul_desc& d = items[i];
+            const qmm_matmul_typed_desc d = get(i);
             if (d.M == 0 || d.N == 0) continue;
+            const int wt = internal_type(d.wtype);
             BatchItem& it = p.it[p.count++];
             it.wq = static_cast<const uint8_t*>(d.wq);
             it.x = d.x;
@@ -430,16 +438,37 @@ qmm_status qmm_matmul_batch(qmm_type wtype, qmm_act_mode mode, const qmm_matmul_
             it.M = (int)d.M;
             it.N = (int)d.N;
             it.K = (int)d.K;
+            it.wt = wt;
             it.lpr = it.bpl = it.tr = 0;
             it.byte0 = p.total;
-            p.total += d.N * (d.K / 32) * bb;
-            if (d.M * d.K > p.max_mk) p.max_mk = (int)(d.M * d.K);
+            p.total += d.N * (int64_t)qmm_row_bytes(d.wtype, d.K);
+            const int64_t ab = d.M * (d.K / unit_vals(wt)) * batch_act_unit(wt, am);
+            if (ab > p.act_bytes) p.act_bytes = (int)ab;
             if (d.M > max_m) max_m = (int)d.M;
+            kind = kind == -1 || kind == wt ? wt : T_MIX;
         }
         if (p.count == 0) break;
-        if (launch_batch(wt, mode == QMM_INT8_ACT ? A_INT8 : A_F32, p, max_m, sms, smem, s) != cudaSuccess) return QMM_ERR_CUDA;
+        if (!is_b32(kind)) kind = T_MIX;
+        if (launch_batch(kind, am, p, max_m, sms, smem, s) != cudaSuccess) return QMM_ERR_CUDA;
     }
     return QMM_OK;
+}
+
+}  // namespace
+}  // extern "C++"
+
+qmm_status qmm_matmul_batch(qmm_type wtype, qmm_act_mode mode, const qmm_matmul_desc* items, int64_t count,
+                            qmm_stream_t stream) {
+    if (!weight_type(wtype)) return QMM_ERR_TYPE;
+    return batch_run(mode, count, items != nullptr, [&](int64_t i) {
+        const qmm_matmul_desc& d = items[i];
+        return qmm_matmul_typed_desc{wtype, d.wq, d.x, d.y, d.M, d.N, d.K};
+    }, stream);
+}
+
+qmm_status qmm_matmul_batch_typed(qmm_act_mode mode, const qmm_matmul_typed_desc* items, int64_t count,
+                                  qmm_stream_t stream) {
+    return batch_run(mode, count, items != nullptr, [&](int64_t i) { return items[i]; }, stream);
 }
 
 qmm_status qmm_block_sums(qmm_type wtype, const void* wq, const float* x, int64_t M, int64_t N, int64_t K,

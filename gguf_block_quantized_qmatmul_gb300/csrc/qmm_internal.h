@@ -34,28 +34,6 @@ cudaError_t launch_prefill(const PrefillPlan& plan, const void* wq, const float*
 bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, unsigned long long inner, unsigned long long outer,
               unsigned long long row_bytes, unsigned box_inner, unsigned box_outer, CUtensorMapSwizzle swz);
 
-// many independent small matmuls in one launch (qmm_batch.cu)
-constexpr int kBatchMax = 256;  // items per launch (the launch parameters carry the table)
-struct BatchItem {
-    const uint8_t* wq;
-    const float* x;
-    float* y;
-    long long byte0;  // the item's first weight byte in the launch's byte order
-    int M, N, K;
-    int lpr, bpl, tr;  // lanes per row, blocks per lane, rows per stage (set by the launcher)
-};
-struct BatchParams {
-    BatchItem it[kBatchMax];
-    long long total;  // weight bytes of all items
-    unsigned* err;    // the device error word (bounded waits)
-    int count;
-    int max_mk;       // the largest M x K (shared-memory activation codes)
-    int slot_bytes;   // bytes of one weight stage slot (set by the launcher)
-    int stages;       // slots in the ring, 2..16 (set by the launcher)
-};
-cudaError_t launch_batch(int wt, int am, const BatchParams& p, int max_m, int sm_count, int smem_max, cudaStream_t s);
-void plan_batch_item(int nb, int bb, int am, int mt, int& lpr, int& bpl, int& tr);
-
 // largest activation batch served by the per-thread dp4a GEMV (int8_act,
 // Q8_0 weights only); larger decode batches, Q4_K weights and every f32_act
 // decode batch up to 8 use the 16-row-tile tensor-core kernel
@@ -99,3 +77,6 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), unsigned grid, unsigned 
 }
 
 }  // namespace qmm
+
+// many independent small matmuls in one launch (uses ensure_smem above)
+#include "qmm_batch.cuh"

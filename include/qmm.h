@@ -200,18 +200,39 @@ typedef struct {
    issued one by one are bound by launch latency rather than by their weight
    bytes.  Each item computes exactly what qmm_matmul(wtype, mode, ...) computes
    for it ("同一个 GGUF…" section 出处: int8_act quantizes each activation row
-   to Q8_0 and forms exact int32 block dots; f32_act multiplies f32
-   activations by the dequantized weights in f32), within the same bound.
-   wtype: QMM_Q8_0, QMM_Q4_0 or QMM_Q5_0 (32-value blocks; one type and one
-   form for the whole batch).  items: host array of `count` descriptors, read
-   during the call (the launch carries a copy), so the call can be captured
-   in a CUDA graph.  Items with M = 0 or N = 0 are skipped.  Items may share
-   x; their y must not overlap.  Needs no workspace.
-   Errors: TYPE; SHAPE (negative sizes, K % 32, M > QMM_BATCH_MAX_M or
-   M * K > QMM_BATCH_MAX_MK); NULL; ALIGN; CUDA.  Nothing is launched when
-   any item is invalid. */
+   to Q8_0, or to Q8K for Q4_K and Q6_K weights, and forms exact int32 block
+   dots; f32_act multiplies f32 activations by the dequantized weights in f32),
+   within the same bound.
+   wtype: any weight type (QMM_Q8_0, QMM_Q4_0, QMM_Q5_0, QMM_Q4_K, QMM_Q6_K),
+   one type and one form for the whole batch (qmm_matmul_batch_typed mixes
+   types).  items: host array of `count` descriptors, read during the call
+   (the launch carries a copy), so the call can be captured in a CUDA graph.
+   Items with M = 0 or N = 0 are skipped.  Items may share x; their y must not
+   overlap.  Needs no workspace.
+   Errors: TYPE; SHAPE (negative sizes, K not a multiple of the block size,
+   M > QMM_BATCH_MAX_M or M * K > QMM_BATCH_MAX_MK); NULL; ALIGN; CUDA.
+   Nothing is launched when any item is invalid. */
 qmm_status qmm_matmul_batch(qmm_type wtype, qmm_act_mode mode, const qmm_matmul_desc* items, int64_t count,
                             qmm_stream_t stream);
+
+/* One item of qmm_matmul_batch_typed: a qmm_matmul_desc with its own weight type. */
+typedef struct {
+    qmm_type wtype;   /* QMM_Q8_0, QMM_Q4_0, QMM_Q5_0, QMM_Q4_K or QMM_Q6_K        */
+    const void* wq;   /* weight blocks, N * qmm_row_bytes(wtype, K) bytes, 16-byte aligned */
+    const float* x;   /* activations [M, K] f32, 16-byte aligned                         */
+    float* y;         /* output [M, N] f32, 4-byte aligned                                */
+    int64_t M, N, K;
+} qmm_matmul_typed_desc;
+
+/* qmm_matmul_batch for items of different weight types in one launch: a whole
+   decode step of a mixed-type file, such as the Q4_K_M files the "GGUF 文件"
+   page describes (Q5_0 and Q8_0 matrices where the row length is not a
+   multiple of 256, Q4_K and Q6_K elsewhere).  Each item computes exactly what
+   qmm_matmul(item.wtype, mode, ...) computes for it, within the same bound;
+   mode is one form for the whole batch.  Same contract and errors as
+   qmm_matmul_batch (TYPE also for an item's invalid wtype). */
+qmm_status qmm_matmul_batch_typed(qmm_act_mode mode, const qmm_matmul_typed_desc* items, int64_t count,
+                                  qmm_stream_t stream);
 
 /* qmm_matmul for callers that cannot allocate device memory.
    (The pages have no counterpart: this is an addition of this library.)

@@ -66,6 +66,28 @@ def smollm2_linears():
     return out
 
 
+def smollm2_q4_k_m_linears():
+    """(name, N, K, wtype) of the same 211 linears with the weight types of a
+    Q4_K_M file of this model, as the "GGUF 文件" page lists that file's
+    tensors: a row of 576 values cannot hold 256-value super-blocks, so those
+    matrices are Q5_0, except attn_v in 14 of the 30 layers (Q8_0); ffn_down
+    (rows of 1536) is Q6_K in 14 layers and Q4_K in the other 16; the tied
+    output head is the Q8_0 token embedding.  The page does not say which 14
+    layers: the even layers 0, 2, ..., 26 here (the step's types, shapes and
+    bytes do not depend on the choice)."""
+    out = []
+    for name, N, K in smollm2_linears():
+        if name == "lm_head":
+            t = "q8_0"
+        else:
+            layer = int(name.split(".")[1])
+            more = layer % 2 == 0 and layer < 28
+            t = ("q6_k" if more else "q4_k") if name.endswith("ffn_down") else \
+                ("q8_0" if more else "q5_0") if name.endswith("attn_v") else "q5_0"
+        out.append((name, N, K, t))
+    return out
+
+
 def special_block_rows(K: int, seed: int = 7) -> np.ndarray:
     """A small set of adversarial rows used by edge-case tests: zeros, constants,
     one-hot values, ties at +-0.5 code steps, all-negative and all-positive

@@ -107,8 +107,10 @@ def test_batch_argument_errors_return_before_launch(qmm):
         arr = (D * max(len(items), 1))(*items)
         return L.qmm_matmul_batch(wtype, mode, ctypes.cast(arr, ctypes.c_void_p), len(items), None)
 
-    assert call(qmm.QMM_Q4_K, 0, [ok]) == 3                  # 32-value block types only
-    assert call(qmm.QMM_Q6_K, 0, [ok]) == 3
+    assert call(qmm.QMM_Q8_K, 0, [ok]) == 3                  # weight types only
+    assert call(qmm.QMM_F32, 0, [ok]) == 3
+    assert call(qmm.QMM_Q4_K, 0, [ok]) == 2                  # K % 256
+    assert call(qmm.QMM_Q6_K, 1, [ok, D(16, 16, 16, 1, 8, 700)]) == 2     # K % 256
     assert call(qmm.QMM_Q8_0, 5, [ok]) == 3
     assert call(qmm.QMM_Q8_0, 0, [ok, D(16, 16, 16, 9, 8, 64)]) == 2      # M > QMM_BATCH_MAX_M
     assert call(qmm.QMM_Q8_0, 0, [ok, D(16, 16, 16, 2, 8, 16384)]) == 2   # M * K > QMM_BATCH_MAX_MK
@@ -118,6 +120,27 @@ def test_batch_argument_errors_return_before_launch(qmm):
     assert call(qmm.QMM_Q8_0, 0, [D(None, None, None, 0, 8, 64)]) == 0   # empty items are skipped
     assert L.qmm_matmul_batch(qmm.QMM_Q8_0, 0, None, 0, None) == 0
     assert L.qmm_matmul_batch(qmm.QMM_Q8_0, 0, None, 3, None) == 1
+
+
+def test_typed_batch_argument_errors_return_before_launch(qmm):
+    L = _lib(qmm)
+    D = qmm.TypedMatmulDesc
+    ok = D(qmm.QMM_Q8_0, 16, 16, 16, 1, 8, 64)
+
+    def call(mode, items):
+        arr = (D * max(len(items), 1))(*items)
+        return L.qmm_matmul_batch_typed(mode, ctypes.cast(arr, ctypes.c_void_p), len(items), None)
+
+    assert call(5, [ok]) == 3
+    assert call(0, [ok, D(qmm.QMM_Q8_K, 16, 16, 16, 1, 8, 256)]) == 3      # an item's type
+    assert call(0, [ok, D(qmm.QMM_Q4_K, 16, 16, 16, 1, 8, 64)]) == 2       # K % 256 for Q4_K
+    assert call(1, [ok, D(qmm.QMM_Q6_K, 16, 16, 16, 9, 8, 256)]) == 2      # M > QMM_BATCH_MAX_M
+    assert call(0, [ok, D(qmm.QMM_Q4_K, 16, 16, 16, 2, 8, 8448 + 8192)]) == 2  # M * K > QMM_BATCH_MAX_MK
+    assert call(0, [ok, D(qmm.QMM_Q5_0, None, 16, 16, 1, 8, 64)]) == 1
+    assert call(0, [ok, D(qmm.QMM_Q6_K, 24, 16, 16, 1, 8, 256)]) == 4
+    assert call(0, [D(qmm.QMM_Q4_K, None, None, None, 0, 8, 256)]) == 0  # empty items are skipped
+    assert L.qmm_matmul_batch_typed(0, None, 0, None) == 0
+    assert L.qmm_matmul_batch_typed(0, None, 2, None) == 1
 
 
 def test_binding_raises_on_error_status(qmm):

@@ -313,12 +313,13 @@ def test_block_sums_edge_rows_bit_exact(qmm, orc, wtype, M, K):
 
 
 @pytest.mark.parametrize("mode", ["int8_act", "f32_act"])
-@pytest.mark.parametrize("wtype", ["q8_0", "q4_0", "q5_0"])
+@pytest.mark.parametrize("wtype", ["q8_0", "q4_0", "q5_0", "q4_k", "q6_k"])
 def test_matmul_batch_edge_rows(qmm, orc, wtype, mode):
     """qmm_matmul_batch with adversarial rows in the weights and activation
-    rows of its items (M = 1..8, K = 576 and 1536); guarded outputs."""
+    rows of its items (M = 1..8, K = 576 or 256 and 1536); guarded outputs."""
     items, refs, guards = [], [], []
-    for i, (M, K) in enumerate([(1, 576), (2, 576), (8, 1536), (4, 1536), (1, 1536), (8, 576)]):
+    k0 = 256 if wtype in ("q4_k", "q6_k") else 576
+    for i, (M, K) in enumerate([(1, k0), (2, k0), (8, 1536), (4, 1536), (1, 1536), (8, k0)]):
         w, x = edge_operands(wtype, K, M, n_plain=7 + i, seed=100 + i)
         wq = orc.quantize(wtype, w)
         buf, y = guarded_out(M, w.shape[0])
@@ -574,13 +575,17 @@ def test_weights_beyond_2gb_use_64_bit_offsets(qmm, orc, M):
     check_device_error(qmm)
 
 
-@pytest.mark.parametrize("wtype", ["q8_0", "q4_0", "q5_0"])
+@pytest.mark.parametrize("wtype", ["q8_0", "q4_0", "q5_0", "q4_k", "q6_k"])
 @pytest.mark.parametrize("mode", ["int8_act", "f32_act"])
 def test_matmul_batch_items_within_bound(qmm, orc, wtype, mode):
     """qmm_matmul_batch: items of different N, K and M (<= 8), some sharing
     one x, each within the bound of its own oracle product."""
-    shapes = [(1, 576, 576), (1, 192, 576), (1, 1536, 576), (1, 576, 1536), (4, 100, 2048), (8, 33, 64),
-              (2, 4097, 256), (3, 1, 32), (1, 576, 576)]
+    if wtype in ("q4_k", "q6_k"):
+        shapes = [(1, 576, 1536), (1, 192, 512), (1, 1536, 256), (1, 576, 14336), (4, 100, 2048), (8, 33, 256),
+                  (2, 4097, 256), (3, 1, 768), (1, 576, 1536), (2, 300, 8192)]
+    else:
+        shapes = [(1, 576, 576), (1, 192, 576), (1, 1536, 576), (1, 576, 1536), (4, 100, 2048), (8, 33, 64),
+                  (2, 4097, 256), (3, 1, 32), (1, 576, 576)]
     items, ref = [], []
     xs = {}
     for i, (M, N, K) in enumerate(shapes):
@@ -642,4 +647,92 @@ def test_matmul_batch_smollm2_step_matches_single_calls(qmm, orc):
         for i, ((wq_h, x_h), (_, _, y)) in enumerate(zip(hosts, items)):
             y_orc, T = orc.matmul("q8_0", mode, wq_h, x_h)
             assert_within_bound(host(y), y_orc, T, f"smollm2 item {i} {mode}")
+    check_device_error(qmm)
+
+
+def test_matmul_batch_typed_q4_k_m_step(qmm, orc):
+    """The 211 linears of a SmolLM2-135M decode step with the weight types of
+    its Q4_K_M file (Q5_0, Q8_0, Q4_K, Q6_K) in one qmm_matmul_batch_typed
+    launch: every output element of every item against the oracle, both forms
+    (outputs NaN-filled before each form, so an unwritten row fails)."""
+    lins = qmm_synth.smollm2_q4_k_m_linears()
+    xs = {K: qmm_synth.activations(1, K, seed=K) for K in (576, 1536)}
+    xd = {K: dev(x) for K, x in xs.items()}
+    items, hosts = [], []
+    for i, (_, N, K, t) in enumerate(lins):
+        g = torch.Generator(device="cuda").manual_seed(2000 + i)
+        w = torch.randn((N, K), generator=g, device="cuda") * 0.02
+        wq = qmm.quantize_weights(w, t)
+        items.append((t, wq, xd[K], torch.full((1, N), float("nan"), device="cuda")))
+        hosts.append(host(wq))
+    for mode in ("int8_act", "f32_act"):
+        for *_, y in items:
+            y.fill_(float("nan"))
+        qmm.matmul_batch_typed(items, mode)
+        for i, ((t, _, x, y), wq_h) in enumerate(zip(items, hosts)):
+            y_orc, T = orc.matmul(t, mode, wq_h, xs[x.shape[1]])
+            assert_within_bound(host(y), y_orc, T, f"q4_k_m item {i} {t} {mode}")
+    check_device_error(qmm)
+
+
+@pytest.mark.parametrize("mode", ["int8_act", "f32_act"])
+def test_matmul_batch_typed_mixed_items(qmm, orc, mode):
+    """qmm_matmul_batch_typed with every weight type interleaved: items of
+    M = 1..8 that share one x across types (the staged activations change
+    form between Q8_0 and Q8K for the same x), adversarial rows, ragged N,
+    guarded outputs; 300 items (two launches) with empty items among them."""
+    types = ["q8_0", "q4_k", "q5_0", "q6_k", "q4_0"]
+    xs = {}
+    for M, K in ((1, 1536), (3, 512), (8, 2048), (2, 256), (1, 8192)):
+        _, x = edge_operands("q8_0", K, M, n_plain=1, seed=M * 7 + K)
+        xs[(M, K)] = x
+    keys = list(xs)
+    items, refs, guards = [], [], []
+    for i in range(300):
+        t = types[i % 5]
+        M, K = keys[(i // 5 + i) % len(keys)]
+        if i % 97 == 40:  # an empty item
+            items.append((t, torch.empty(16, dtype=torch.uint8, device="cuda"), dev(xs[(M, K)]),
+                          torch.empty((M, 0), device="cuda")))
+            refs.append(None), guards.append(None)
+            continue
+        N = 5 + (i * 37) % 60
+        w, _ = edge_operands(t, K, 1, n_plain=N, seed=500 + i)
+        wq = orc.quantize(t, w)
+        buf, y = guarded_out(M, w.shape[0])
+        items.append((t, dev(wq), dev(xs[(M, K)]), y))
+        refs.append(orc.matmul(t, mode, wq, xs[(M, K)]))
+        guards.append(buf)
+    qmm.matmul_batch_typed(items, mode)
+    for (t, _, x, y), r, buf in zip(items, refs, guards):
+        if r is None:
+            continue
+        assert_within_bound(host(y), r[0], r[1], f"typed batch {t} {mode} M{x.shape[0]} K{x.shape[1]}")
+        check_guards(buf, "typed batch item")
+    check_device_error(qmm)
+
+
+SB_CANCEL = [(t, M, K) for t in ("q4_k", "q6_k") for (M, K) in ((1, 512), (2, 512), (8, 512), (1, 4096),
+                                                                 (4, 4096), (16, 512), (37, 4096), (256, 4096))]
+
+
+@pytest.mark.parametrize("wtype,M,K", SB_CANCEL)
+def test_int8_superblock_sums_are_whole(qmm, orc, wtype, M, K):
+    """int8_act on super-blocks whose exact sum is 0 while its four 64-value
+    pieces are large and unequal (tests/superblock_cancel.py): T = 0, so every
+    output must be within 1e-6 of 0, which only whole int32 super-block sums
+    reach (per-piece f32 terms leave residues near 0.5).  Decode, streaming
+    and prefill paths through qmm_matmul, and the batch kernel for M <= 8."""
+    import superblock_cancel as sc
+    N = 70
+    wq = sc.weights(wtype, N, K)
+    x = sc.activations(M, K)
+    y_orc, T = orc.matmul(wtype, "int8_act", wq, x)
+    y = matmul_checked(qmm, dev(wq), dev(x), wtype, "int8_act", N)
+    assert_within_bound(y, y_orc, T, f"{wtype} M{M} K{K} zero-sum super-blocks")
+    if M <= 8 and M * K <= 16384:
+        buf, yb = guarded_out(M, N)
+        qmm.matmul_batch([(dev(wq), dev(x), yb)], wtype, "int8_act")
+        assert_within_bound(host(yb), y_orc, T, f"batch {wtype} M{M} K{K} zero-sum super-blocks")
+        check_guards(buf, "batch zero-sum item")
     check_device_error(qmm)

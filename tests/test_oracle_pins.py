@@ -833,3 +833,26 @@ def test_zero_in_a_block_whose_reciprocal_overflows_gets_code_zero(orc, t):
     nz[[3, 5, 40]] = True
     blk0 = np.arange(K) < 32
     assert (codes[~nz & blk0] == zero).all()
+
+
+@pytest.mark.parametrize("wtype", ["q4_k", "q6_k"])
+def test_superblock_cancellation_fixture(orc, wtype):
+    """The zero-sum super-block operands (tests/superblock_cancel.py) decode as
+    built: every weight f(d) sc code, every Q8K activation code one of the
+    piece codes; the exact int8_act result is 0 with T = 0 (closed form: the
+    piece codes sum to 0 and every weight of a row is the same), while each
+    64-value piece's integer sum is not."""
+    import superblock_cancel as sc
+    N, M, K = 5, 3, 512
+    wq = sc.weights(wtype, N, K)
+    x = sc.activations(M, K)
+    w = orc.dequantize(wtype, wq, K)
+    for n in range(N):
+        assert np.all(w[n] == np.float32(sc.weight_value(wtype, n)))
+    xq = orc.quantize("q8_k", x).reshape(M, K // 256, 292)
+    codes = xq[:, :, 4:260].view(np.int8).reshape(M, K).astype(np.int64)
+    assert np.array_equal(codes, np.tile(np.repeat(np.array(sc.PIECE_CODES), 64), (M, K // 256)))
+    y, T = orc.matmul(wtype, "int8_act", wq, x)
+    assert np.all(y == 0.0) and np.all(T == 0.0)
+    piece = codes.reshape(M, -1, 4, 64).sum(axis=-1)
+    assert np.all(np.abs(piece) >= 100 * 64)
