@@ -13,16 +13,18 @@ cudaError_t go(int am, BatchParams& p, int mt, int grid, int smem_max, cudaStrea
                         : batch_go_mt<WT, A_F32>(p, mt, grid, smem_max, s);
 }
 
-// issue cost of one unit relative to a 32-value block: a super-block holds
-// eight blocks' values, and its 6-bit scales, mins and codes cost a little more
-// to unpack
-int unit_work(int wt) { return is_sb(wt) ? 9 : 1; }
+// issue cost of one unit relative to a 32-value block: a 64-value piece of a
+// super-block holds two blocks' values, and its 6-bit scales, mins and codes
+// (and, for int8_act, the quad's exchanges) cost a little more
+int unit_work(int wt) { return is_sb(wt) ? 3 : 1; }
 
 }  // namespace
 
-void plan_batch_item(int wt, int nu, int am, int mt, int& lpr, int& bpl, int& tr) {
+void plan_batch_item(int wt, int nu, long long rb, int am, int mt, int& lpr, int& bpl, int& tr) {
     // Lanes per row (lpr) and units per lane (bpl = ceil(nu / lpr)) for a row of
-    // nu units of type wt, and rows per stage (tr).  A warp holds 32 / lpr lane groups of R
+    // nu units of type wt (rb bytes), and rows per stage (tr).  int8_act on
+    // super-blocks wants lane groups of a multiple of 4 lanes (a super-block's
+    // four pieces on one quad of lanes).  A warp holds 32 / lpr lane groups of R
     // rows each; a stage is one pass of the 16 consumer warps over its rows, at
     // most kBatchStageCap bytes.  The cost of a pass is about 30 issue slots per
     // 32 values and row a lane takes, 12 per 32 values for the shared
@@ -30,13 +32,14 @@ void plan_batch_item(int wt, int nu, int am, int mt, int& lpr, int& bpl, int& tr
     // with the least cost per row wins.
     const int R = batch_rows_per_group(wt, am, mt);
     const int work = unit_work(wt);
-    const long long rb = (long long)nu * unit_bytes(wt);
+    const bool quads = is_sb(wt) && am == A_INT8;
     const long long cap = std::max<long long>(1, (kBatchStageCap - 32) / rb);
     double best = 1e300;
     lpr = 32, bpl = (nu + 31) / 32, tr = (int)std::min<long long>(kBatchWarps, cap);
     for (int l = 1; l <= 32; ++l) {
+        if (quads && l % 4 != 0) continue;
         const int b = (nu + l - 1) / l;
-        if ((nu + b - 1) / b != l) continue;  // the same bpl with fewer lanes
+        if (!quads && (nu + b - 1) / b != l) continue;  // the same bpl with fewer lanes
         const long long t = std::min<long long>((long long)kBatchWarps * (32 / l) * R, cap);
         int levels = 0;
         while ((1 << levels) < l) ++levels;
@@ -52,13 +55,13 @@ cudaError_t launch_batch(int wt, int am, const BatchParams& p0, int max_m, int s
     int last_k = -1, last_wt = -1, lpr = 0, bpl = 0, tr = 0;  // consecutive items of one type and K share a plan
     for (int i = 0; i < p.count; ++i) {
         BatchItem& it = p.it[i];
-        const int ub = unit_bytes(it.wt), nu = it.K / unit_vals(it.wt);
+        const long long rb = (long long)(it.K / unit_vals(it.wt)) * unit_bytes(it.wt);
         if (it.K != last_k || it.wt != last_wt) {
-            plan_batch_item(it.wt, nu, am, mt, lpr, bpl, tr);
+            plan_batch_item(it.wt, batch_units(it.wt, it.K), rb, am, mt, lpr, bpl, tr);
             last_k = it.K, last_wt = it.wt;
         }
         it.lpr = lpr, it.bpl = bpl, it.tr = tr;
-        stage = std::max(stage, (long long)it.tr * nu * ub);
+        stage = std::max(stage, (long long)it.tr * rb);
         rows += it.N;
     }
     // a slot holds a stage's rows plus the 16-byte alignment slack and the

@@ -15,7 +15,7 @@
 //                   S_m = sum_j m_j bsum_j (bsum_j: sub-block j's activation codes);
 //             Q6_K: y += d_a f(d) S, S = sum_g sc_g isum_g over 16 groups of 16;
 //             each super-block's S_sc, S_m and S are whole int32 sums before
-//             the one conversion to f32 (one lane takes the whole super-block);
+//             the one conversion to f32 (its four pieces' lanes add them exactly);
 //   f32_act:  y += f32 products of the dequantized weight and x: f(d) sum(q x)
 //             per 32-value block, e_j sum(q x) - o_j sum(x) per Q4_K
 //             sub-block (e_j = f(d) sc_j, o_j = f(dmin) m_j), f(d) sc_g
@@ -32,7 +32,8 @@
 // the Q4_K sub-block sums of x), then take each stage's rows in lane groups:
 // lpr lanes per group, up to two rows per group sharing the activation loads,
 // lane gl taking units gl, gl + lpr, ... of its rows (a unit: one 32-value
-// block or one super-block); the group sums its lanes with a shuffle tree.
+// block or one 64-value piece of a super-block); the group sums its lanes with
+// a shuffle tree.
 // lpr, the units per lane and the rows per stage are planned per item on the
 // host.
 #pragma once
@@ -71,10 +72,22 @@ struct BatchParams {
 // Shared-memory bytes of one staged activation unit (row m, unit b):
 //   Q8_0 codes (int8_act, 32-value types): 32 codes, the f16-rounded scale as f32 at 32;
 //   f32 (f32_act, 32-value types): 32 floats (+16 bytes of padding);
-//   Q8K (int8_act, super-block types): 256 codes, 8 int32 sub-block code sums at 256, f32 d at 288;
-//   f32 (f32_act, super-block types): 256 floats, 8 f32 sub-block sums of x at 1024.
+//   Q8K (int8_act, super-block types): 8 slots of 48 bytes, each 32 codes; the
+//     8 int32 code sums of the 32-value sub-blocks at 384, f32 d at 416;
+//   f32 (f32_act, super-block types): 8 slots of 144 bytes, each 32 floats; the
+//     8 f32 sums of x of the sub-blocks at 1152.
+// A super-block's 32-value quarters go to slots in the order its pieces read
+// them: piece c reads slots 2c and 2c + 1 (Q4_K: sub-blocks 2c, 2c + 1, in
+// order; Q6_K: quarters p and p + 2 of half hh, c = 2 hh + p).  Slot and unit
+// strides are odd numbers of 16-byte granules, so that the eight lanes of a
+// quarter-warp (two quads on consecutive super-blocks) read eight distinct
+// granules of the 128-byte bank row.
 __host__ __device__ constexpr int batch_act_unit(int wt, int am) {
-    return is_sb(wt) ? (am == A_INT8 ? 304 : 1056) : (am == A_INT8 ? 48 : 144);
+    return is_sb(wt) ? (am == A_INT8 ? 432 : 1200) : (am == A_INT8 ? 48 : 144);
+}
+// the staged slot of 32-value quarter q (value / 32) of a super-block of type wt
+__host__ __device__ constexpr int batch_slot(int wt, int q) {
+    return wt == T_Q6_K ? (q & 4) | ((q & 1) << 1) | ((q >> 1) & 1) : q;
 }
 // weight rows a lane group works on at once (they share the activation loads)
 __host__ __device__ constexpr int batch_rows_per_group(int wt, int am, int mt) {
@@ -83,8 +96,8 @@ __host__ __device__ constexpr int batch_rows_per_group(int wt, int am, int mt) {
 
 cudaError_t launch_batch(int wt, int am, const BatchParams& p, int max_m, int sm_count, int smem_max, cudaStream_t s);
 cudaError_t launch_batch_mix(int am, BatchParams& p, int mt, int grid, int smem_max, cudaStream_t s);
-// lpr, bpl and tr for a row of nu units of weight type wt
-void plan_batch_item(int wt, int nu, int am, int mt, int& lpr, int& bpl, int& tr);
+// lpr, bpl and tr for a row of nu units of weight type wt, rb bytes
+void plan_batch_item(int wt, int nu, long long rb, int am, int mt, int& lpr, int& bpl, int& tr);
 
 namespace {
 
@@ -261,219 +274,202 @@ __device__ __forceinline__ void block_dot(const uint8_t* s, const int (&wo)[R], 
     }
 }
 
-// The same for one Q4_K super-block (144 bytes at the 16-byte aligned offset
-// wo[h]: f16 d, f16 dmin, 12 bytes of 6-bit scales and mins, 128 bytes of
-// nibbles: sub-block 2c in the low nibbles of bytes 32c..32c+31, 2c + 1 in the
-// high nibbles).  Taken as four 64-value pieces c; int8_act keeps S_sc and
-// S_m in int32 over all four.
+// Super-block types are taken in 64-value pieces: piece c of a Q4_K
+// super-block is sub-blocks 2c, 2c + 1; piece i of a Q6_K super-block is
+// quarters p and p + 2 of half hh (i = 2 hh + p), which share their ql and
+// qh bytes.  The four pieces of a super-block sit on four consecutive lanes
+// (lane groups of a multiple of 4 lanes).  int8_act sums each piece in int32
+// and adds the four with two exchanges inside the quad, so that the whole
+// super-block sum is converted to f32 once (by the lane of piece 0); f32_act
+// adds each piece's f32 terms where it is.
+
+// The int32 sum of the four lanes of a quad (lanes 4k..4k+3), on every lane.
+__device__ __forceinline__ int quad_sum(int v) {
+    v += __shfl_xor_sync(0xffffffffu, v, 1);
+    return v + __shfl_xor_sync(0xffffffffu, v, 2);
+}
+
+// acc[h][m] += piece c of the Q4_K super-block of weight row h (144 bytes at
+// the 16-byte aligned offset wo[h]: f16 d, f16 dmin, 12 bytes of 6-bit scales
+// and mins, 128 bytes of nibbles: sub-block 2c in the low nibbles of bytes
+// 32c..32c+31, 2c + 1 in the high nibbles), where v[h].  ao: the offset of the
+// activation super-block for row 0.
+//   int8_act: S_sc = sum_j sc_j isum_j, S_m = sum_j m_j bsum_j over the whole
+//             super-block, y += d_a (f(d) S_sc - f(dmin) S_m);
+//   f32_act:  y += e_j sum(q x) - o_j sum(x), e_j = f(d) sc_j, o_j = f(dmin) m_j.
 template <int AM, int MT, int R>
-__device__ __forceinline__ void q4k_unit_dot(const uint8_t* s, const int (&wo)[R], int ao, int astep, int M,
-                                             const bool (&v)[R], float (&acc)[R][MT]) {
-    uint4 hw[R];
+__device__ __forceinline__ void q4k_piece_dot(const uint8_t* s, const int (&wo)[R], int c, int ao, int astep, int M,
+                                              const bool (&v)[R], float (&acc)[R][MT]) {
+    // the 6-bit scale and min of sub-blocks 2c, 2c + 1: j < 4 in the low 6 bits
+    // of bytes j (scales) and 4 + j (mins); j >= 4 in the nibbles of byte 8 + j - 4
+    // with the high 2 bits in bits 6-7 of bytes j - 4 and j
+    const uint32_t sh = 16u * (uint32_t)(c & 1);  // byte (2c) & 3 of the word, times 8
+    const bool low = c < 2;
+    uint32_t lo[R][8], hi[R][8];
+    int sc0[R], sc1[R], mn0[R], mn1[R];
     float fd[R], fm[R];
 #pragma unroll
     for (int h = 0; h < R; ++h) {
-        hw[h] = ld128(s + wo[h]);
-        fd[h] = h2f(hw[h].x);
-        fm[h] = h2f(hw[h].x >> 16);
+        const uint4 hw = ld128(s + wo[h]);  // d | dmin, scale bytes 0-3, 4-7, 8-11
+        fd[h] = h2f(hw.x);
+        fm[h] = h2f(hw.x >> 16);
+        const uint32_t a0 = hw.y >> sh, a1 = hw.z >> sh, a2 = hw.w >> sh;
+        const int ls0 = (int)(a0 & 63u), ls1 = (int)((a0 >> 8) & 63u);
+        const int lm0 = (int)(a1 & 63u), lm1 = (int)((a1 >> 8) & 63u);
+        const int hs0 = (int)((a2 & 15u) | ((a0 >> 2) & 48u)), hs1 = (int)(((a2 >> 8) & 15u) | ((a0 >> 10) & 48u));
+        const int hm0 = (int)(((a2 >> 4) & 15u) | ((a1 >> 2) & 48u)), hm1 = (int)(((a2 >> 12) & 15u) | ((a1 >> 10) & 48u));
+        sc0[h] = low ? ls0 : hs0, sc1[h] = low ? ls1 : hs1;
+        mn0[h] = low ? lm0 : hm0, mn1[h] = low ? lm1 : hm1;
+        const uint4 qa = ld128(s + wo[h] + 16 + 32 * c), qb = ld128(s + wo[h] + 32 + 32 * c);
+        const uint32_t qq[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            lo[h][k] = qq[k] & 0x0F0F0F0Fu;
+            hi[h][k] = (qq[k] >> 4) & 0x0F0F0F0Fu;
+        }
     }
-    int ssc[R][MT], smn[R][MT];
     if (AM == A_INT8) {
 #pragma unroll
-        for (int h = 0; h < R; ++h)
+        for (int m = 0; m < MT; ++m) {
+            if (m >= M) break;
+            const uint8_t* a = s + ao + m * astep;
+            const uint4 a0 = ld128(a + 96 * c), a1 = ld128(a + 96 * c + 16);        // slot 2c: sub-block 2c
+            const uint4 a2 = ld128(a + 96 * c + 48), a3 = ld128(a + 96 * c + 64);   // slot 2c + 1
+            const uint2 bs = ld64(a + 384 + 8 * c);
+            const float da = *reinterpret_cast<const float*>(a + 416);
 #pragma unroll
-            for (int m = 0; m < MT; ++m) ssc[h][m] = 0, smn[h][m] = 0;
-    }
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        uint32_t lo[R][8], hi[R][8];  // (f32_act: lo holds the packed bytes, split at use)
-        int sc0[R], sc1[R], mn0[R], mn1[R];
+            for (int h = 0; h < R; ++h) {
+                int s0 = dp4a(lo[h][0], a0.x, 0), s1 = dp4a(hi[h][0], a2.x, 0);
+                s0 = dp4a(lo[h][1], a0.y, s0), s1 = dp4a(hi[h][1], a2.y, s1);
+                s0 = dp4a(lo[h][2], a0.z, s0), s1 = dp4a(hi[h][2], a2.z, s1);
+                s0 = dp4a(lo[h][3], a0.w, s0), s1 = dp4a(hi[h][3], a2.w, s1);
+                s0 = dp4a(lo[h][4], a1.x, s0), s1 = dp4a(hi[h][4], a3.x, s1);
+                s0 = dp4a(lo[h][5], a1.y, s0), s1 = dp4a(hi[h][5], a3.y, s1);
+                s0 = dp4a(lo[h][6], a1.z, s0), s1 = dp4a(hi[h][6], a3.z, s1);
+                s0 = dp4a(lo[h][7], a1.w, s0), s1 = dp4a(hi[h][7], a3.w, s1);
+                const int ssc = quad_sum(sc0[h] * s0 + sc1[h] * s1);
+                const int smn = quad_sum(mn0[h] * (int)bs.x + mn1[h] * (int)bs.y);
+                const float t = da * (fd[h] * (float)ssc - fm[h] * (float)smn);
+                acc[h][m] = v[h] && c == 0 ? acc[h][m] + t : acc[h][m];
+            }
+        }
+    } else {
 #pragma unroll
         for (int h = 0; h < R; ++h) {
-            const uint4 qa = ld128(s + wo[h] + 16 + 32 * c), qb = ld128(s + wo[h] + 32 + 32 * c);
-            const uint32_t qq[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                lo[h][k] = AM == A_INT8 ? qq[k] & 0x0F0F0F0Fu : qq[k];
-                if (AM == A_INT8) hi[h][k] = (qq[k] >> 4) & 0x0F0F0F0Fu;
-            }
-            sc0[h] = q4k_sc(hw[h].y, hw[h].w, 2 * c);
-            sc1[h] = q4k_sc(hw[h].y, hw[h].w, 2 * c + 1);
-            mn0[h] = q4k_mn(hw[h].z, hw[h].w, 2 * c);
-            mn1[h] = q4k_mn(hw[h].z, hw[h].w, 2 * c + 1);
-        }
-        if (AM == A_INT8) {
+            // e_j and o_j are exact f32 products (11-bit by 6-bit)
+            const float e0 = fd[h] * (float)sc0[h], e1 = fd[h] * (float)sc1[h];
+            const float o0 = fm[h] * (float)mn0[h], o1 = fm[h] * (float)mn1[h];
+            float sl[MT], sh2[MT];
+            dot_u8_f32_rows<8, 0, MT>(lo[h], s + ao + 288 * c, astep, M, sl);         // slot 2c
+            dot_u8_f32_rows<8, 0, MT>(hi[h], s + ao + 288 * c + 144, astep, M, sh2);  // slot 2c + 1
 #pragma unroll
             for (int m = 0; m < MT; ++m) {
                 if (m >= M) break;
-                const uint8_t* a = s + ao + m * astep;
-                const uint4 a0 = ld128(a + 64 * c), a1 = ld128(a + 64 * c + 16);
-                const uint4 a2 = ld128(a + 64 * c + 32), a3 = ld128(a + 64 * c + 48);
-                const uint2 bs = ld64(a + 256 + 8 * c);
-#pragma unroll
-                for (int h = 0; h < R; ++h) {
-                    int s0 = dp4a(lo[h][0], a0.x, 0), s1 = dp4a(hi[h][0], a2.x, 0);
-                    s0 = dp4a(lo[h][1], a0.y, s0), s1 = dp4a(hi[h][1], a2.y, s1);
-                    s0 = dp4a(lo[h][2], a0.z, s0), s1 = dp4a(hi[h][2], a2.z, s1);
-                    s0 = dp4a(lo[h][3], a0.w, s0), s1 = dp4a(hi[h][3], a2.w, s1);
-                    s0 = dp4a(lo[h][4], a1.x, s0), s1 = dp4a(hi[h][4], a3.x, s1);
-                    s0 = dp4a(lo[h][5], a1.y, s0), s1 = dp4a(hi[h][5], a3.y, s1);
-                    s0 = dp4a(lo[h][6], a1.z, s0), s1 = dp4a(hi[h][6], a3.z, s1);
-                    s0 = dp4a(lo[h][7], a1.w, s0), s1 = dp4a(hi[h][7], a3.w, s1);
-                    ssc[h][m] += sc0[h] * s0 + sc1[h] * s1;
-                    smn[h][m] += mn0[h] * (int)bs.x + mn1[h] * (int)bs.y;
-                }
-            }
-        } else {
-#pragma unroll
-            for (int h = 0; h < R; ++h) {
-                // e_j and o_j are exact f32 products (11-bit by 6-bit)
-                const float e0 = fd[h] * (float)sc0[h], e1 = fd[h] * (float)sc1[h];
-                const float o0 = fm[h] * (float)mn0[h], o1 = fm[h] * (float)mn1[h];
-                uint32_t nib[8];
-                float sq[MT];
-#pragma unroll
-                for (int k = 0; k < 8; ++k) nib[k] = lo[h][k] & 0x0F0F0F0Fu;
-                dot_u8_f32_rows<8, 0, MT>(nib, s + ao + 256 * c, astep, M, sq);
-#pragma unroll
-                for (int m = 0; m < MT; ++m) {
-                    if (m >= M) break;
-                    const float X = *reinterpret_cast<const float*>(s + ao + m * astep + 1024 + 8 * c);
-                    acc[h][m] = v[h] ? acc[h][m] + (e0 * sq[m] - o0 * X) : acc[h][m];
-                }
-#pragma unroll
-                for (int k = 0; k < 8; ++k) nib[k] = (lo[h][k] >> 4) & 0x0F0F0F0Fu;
-                dot_u8_f32_rows<8, 0, MT>(nib, s + ao + 256 * c + 128, astep, M, sq);
-#pragma unroll
-                for (int m = 0; m < MT; ++m) {
-                    if (m >= M) break;
-                    const float X = *reinterpret_cast<const float*>(s + ao + m * astep + 1028 + 8 * c);
-                    acc[h][m] = v[h] ? acc[h][m] + (e1 * sq[m] - o1 * X) : acc[h][m];
-                }
-            }
-        }
-    }
-    if (AM == A_INT8) {
-#pragma unroll
-        for (int m = 0; m < MT; ++m) {
-            if (m >= M) break;
-            const float da = *reinterpret_cast<const float*>(s + ao + m * astep + 288);
-#pragma unroll
-            for (int h = 0; h < R; ++h) {
-                const float t = da * (fd[h] * (float)ssc[h][m] - fm[h] * (float)smn[h][m]);
+                const float2 X = *reinterpret_cast<const float2*>(s + ao + m * astep + 1152 + 8 * c);
+                const float t = (e0 * sl[m] - o0 * X.x) + (e1 * sh2[m] - o1 * X.y);
                 acc[h][m] = v[h] ? acc[h][m] + t : acc[h][m];
             }
         }
     }
 }
 
-// The same for one Q6_K super-block (210 bytes at the even offset wo[h]: ql
-// 0-127, qh 128-191, 16 int8 group scales 192-207, f16 d 208).  Value i =
-// 128 hh + 32 q + l takes the low 4 bits from nibble q / 2 of ql byte
-// 64 hh + 32 (q % 2) + l and the high 2 bits from bits 2q, 2q + 1 of qh byte
-// 32 hh + l; the code is the 6 bits less 32.  Taken as four 64-value pieces
-// (hh, p): quarters p and p + 2 of half hh share their ql and qh bytes.
-// int8_act keeps S in int32 over all four.
+// acc[h][m] += piece i of the Q6_K super-block of weight row h (210 bytes at
+// the even offset wo[h]: ql 0-127, qh 128-191, 16 int8 group scales 192-207,
+// f16 d 208), where v[h].  Value 128 hh + 32 q + l takes the low 4 bits from
+// nibble q / 2 of ql byte 64 hh + 32 (q % 2) + l and the high 2 bits from bits
+// 2q, 2q + 1 of qh byte 32 hh + l; the code is the 6 bits less 32.
+//   int8_act: S = sum_g sc_g isum_g over the whole super-block, y += d_a f(d) S;
+//   f32_act:  y += f(d) sc_g sum(q x) per group of 16.
 template <int AM, int MT, int R>
-__device__ __forceinline__ void q6k_unit_dot(const uint8_t* s, const int (&wo)[R], int ao, int astep, int M,
-                                             const bool (&v)[R], float (&acc)[R][MT]) {
+__device__ __forceinline__ void q6k_piece_dot(const uint8_t* s, const int (&wo)[R], int i, int ao, int astep, int M,
+                                              const bool (&v)[R], float (&acc)[R][MT]) {
+    const int hh = i >> 1, p = i & 1;
+    const int g0 = 8 * hh + 2 * p;  // groups g0, g0 + 1 (quarter p) and g0 + 4, g0 + 5 (quarter p + 2)
+    const uint32_t ush = 4u - 2u * (uint32_t)p, dsh = 2u * (uint32_t)p;
+    // ca: quarter p, cb: quarter p + 2; the 6-bit fields as unsigned bytes, less 32 for int8_act
+    uint32_t ca[R][8], cb[R][8];
+    int sc[R][4];
     float fd[R];
 #pragma unroll
-    for (int h = 0; h < R; ++h) fd[h] = h2f(*reinterpret_cast<const uint16_t*>(s + wo[h] + 208));
-    int S[R][MT];
-    if (AM == A_INT8) {
+    for (int h = 0; h < R; ++h) {
+        uint32_t ql[8], qh[8];
+        ld_words<8>(s, wo[h] + 64 * hh + 32 * p, ql);
+        ld_words<8>(s, wo[h] + 128 + 32 * hh, qh);
 #pragma unroll
-        for (int h = 0; h < R; ++h)
-#pragma unroll
-            for (int m = 0; m < MT; ++m) S[h][m] = 0;
-    }
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-        uint32_t qh[R][8];
-#pragma unroll
-        for (int h = 0; h < R; ++h) ld_words<8>(s, wo[h] + 128 + 32 * hh, qh[h]);
-#pragma unroll
-        for (int p = 0; p < 2; ++p) {
-            // ca: quarter p (groups g0, g0 + 1), cb: quarter p + 2 (groups g0 + 4,
-            // g0 + 5); the 6-bit fields as unsigned bytes, less 32 for int8_act
-            uint32_t ca[R][8], cb[R][8];
-            int sc[R][4];
-            const int g0 = 8 * hh + 2 * p;
-#pragma unroll
-            for (int h = 0; h < R; ++h) {
-                uint32_t ql[8];
-                ld_words<8>(s, wo[h] + 64 * hh + 32 * p, ql);
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    ca[h][k] = (ql[k] & 0x0F0F0F0Fu) | ((qh[h][k] << (4 - 2 * p)) & 0x30303030u);
-                    cb[h][k] = ((ql[k] >> 4) & 0x0F0F0F0Fu) | ((qh[h][k] >> (2 * p)) & 0x30303030u);
-                    if (AM == A_INT8) ca[h][k] = __vsub4(ca[h][k], 0x20202020u), cb[h][k] = __vsub4(cb[h][k], 0x20202020u);
-                }
-                // the group scales g0, g0 + 1 and g0 + 4, g0 + 5: two aligned 16-bit loads
-                const uint32_t s01 = *reinterpret_cast<const uint16_t*>(s + wo[h] + 192 + g0);
-                const uint32_t s45 = *reinterpret_cast<const uint16_t*>(s + wo[h] + 196 + g0);
-                sc[h][0] = (int)(s01 << 24) >> 24, sc[h][1] = (int)(s01 << 16) >> 24;
-                sc[h][2] = (int)(s45 << 24) >> 24, sc[h][3] = (int)(s45 << 16) >> 24;
-            }
-            if (AM == A_INT8) {
-#pragma unroll
-                for (int m = 0; m < MT; ++m) {
-                    if (m >= M) break;
-                    const uint8_t* a = s + ao + m * astep + 128 * hh + 32 * p;  // quarter p's first code
-                    const uint4 a0 = ld128(a), a1 = ld128(a + 16), a2 = ld128(a + 64), a3 = ld128(a + 80);
-#pragma unroll
-                    for (int h = 0; h < R; ++h) {
-                        const uint32_t* sa = ca[h];
-                        const uint32_t* sb = cb[h];
-                        int i0 = dp4a(sa[0], a0.x, 0), i1 = dp4a(sa[4], a1.x, 0);
-                        int i2 = dp4a(sb[0], a2.x, 0), i3 = dp4a(sb[4], a3.x, 0);
-                        i0 = dp4a(sa[1], a0.y, i0), i1 = dp4a(sa[5], a1.y, i1), i2 = dp4a(sb[1], a2.y, i2), i3 = dp4a(sb[5], a3.y, i3);
-                        i0 = dp4a(sa[2], a0.z, i0), i1 = dp4a(sa[6], a1.z, i1), i2 = dp4a(sb[2], a2.z, i2), i3 = dp4a(sb[6], a3.z, i3);
-                        i0 = dp4a(sa[3], a0.w, i0), i1 = dp4a(sa[7], a1.w, i1), i2 = dp4a(sb[3], a2.w, i2), i3 = dp4a(sb[7], a3.w, i3);
-                        S[h][m] += sc[h][0] * i0 + sc[h][1] * i1 + sc[h][2] * i2 + sc[h][3] * i3;
-                    }
-                }
-            } else {
-                const uint8_t* xa = s + ao + 4 * (128 * hh + 32 * p);  // quarter p's first value
-#pragma unroll
-                for (int h = 0; h < R; ++h) {
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        // group i: 16 values; f(d) sc_g is an exact f32 product (11-bit by 7-bit)
-                        float sq[MT];
-                        dot_u8_f32_rows<4, 32, MT>((i < 2 ? ca[h] : cb[h]) + 4 * (i & 1), xa + 256 * (i >> 1) + 64 * (i & 1),
-                                                   astep, M, sq);
-                        const float e = fd[h] * (float)sc[h][i];
-#pragma unroll
-                        for (int m = 0; m < MT; ++m) {
-                            if (m >= M) break;
-                            acc[h][m] = v[h] ? fmaf(e, sq[m], acc[h][m]) : acc[h][m];
-                        }
-                    }
-                }
-            }
+        for (int k = 0; k < 8; ++k) {
+            ca[h][k] = (ql[k] & 0x0F0F0F0Fu) | ((qh[k] << ush) & 0x30303030u);
+            cb[h][k] = ((ql[k] >> 4) & 0x0F0F0F0Fu) | ((qh[k] >> dsh) & 0x30303030u);
+            if (AM == A_INT8) ca[h][k] = __vsub4(ca[h][k], 0x20202020u), cb[h][k] = __vsub4(cb[h][k], 0x20202020u);
         }
+        // the four group scales: two aligned 16-bit loads
+        const uint32_t s01 = *reinterpret_cast<const uint16_t*>(s + wo[h] + 192 + g0);
+        const uint32_t s45 = *reinterpret_cast<const uint16_t*>(s + wo[h] + 196 + g0);
+        sc[h][0] = (int)(s01 << 24) >> 24, sc[h][1] = (int)(s01 << 16) >> 24;
+        sc[h][2] = (int)(s45 << 24) >> 24, sc[h][3] = (int)(s45 << 16) >> 24;
+        fd[h] = h2f(*reinterpret_cast<const uint16_t*>(s + wo[h] + 208));
     }
     if (AM == A_INT8) {
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
             if (m >= M) break;
-            const float da = *reinterpret_cast<const float*>(s + ao + m * astep + 288);
+            const uint8_t* a = s + ao + m * astep;
+            const float da = *reinterpret_cast<const float*>(a + 416);
+            a += 96 * i;  // slot 2i: quarter p; slot 2i + 1: quarter p + 2
+            const uint4 a0 = ld128(a), a1 = ld128(a + 16), a2 = ld128(a + 48), a3 = ld128(a + 64);
 #pragma unroll
             for (int h = 0; h < R; ++h) {
-                const float t = da * fd[h] * (float)S[h][m];
-                acc[h][m] = v[h] ? acc[h][m] + t : acc[h][m];
+                const uint32_t* qa = ca[h];
+                const uint32_t* qb = cb[h];
+                int i0 = dp4a(qa[0], a0.x, 0), i1 = dp4a(qa[4], a1.x, 0);
+                int i2 = dp4a(qb[0], a2.x, 0), i3 = dp4a(qb[4], a3.x, 0);
+                i0 = dp4a(qa[1], a0.y, i0), i1 = dp4a(qa[5], a1.y, i1), i2 = dp4a(qb[1], a2.y, i2), i3 = dp4a(qb[5], a3.y, i3);
+                i0 = dp4a(qa[2], a0.z, i0), i1 = dp4a(qa[6], a1.z, i1), i2 = dp4a(qb[2], a2.z, i2), i3 = dp4a(qb[6], a3.z, i3);
+                i0 = dp4a(qa[3], a0.w, i0), i1 = dp4a(qa[7], a1.w, i1), i2 = dp4a(qb[3], a2.w, i2), i3 = dp4a(qb[7], a3.w, i3);
+                const int S = quad_sum(sc[h][0] * i0 + sc[h][1] * i1 + sc[h][2] * i2 + sc[h][3] * i3);
+                const float t = da * fd[h] * (float)S;
+                acc[h][m] = v[h] && i == 0 ? acc[h][m] + t : acc[h][m];
+            }
+        }
+    } else {
+        const uint8_t* xa = s + ao + 288 * i;  // slot 2i: quarter p; slot 2i + 1: quarter p + 2
+#pragma unroll
+        for (int h = 0; h < R; ++h) {
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                // group g of the piece: 16 values; f(d) sc_g is an exact f32 product (11-bit by 7-bit)
+                float sq[MT];
+                dot_u8_f32_rows<4, 32, MT>((g < 2 ? ca[h] : cb[h]) + 4 * (g & 1), xa + 144 * (g >> 1) + 64 * (g & 1),
+                                           astep, M, sq);
+                const float e = fd[h] * (float)sc[h][g];
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    if (m >= M) break;
+                    acc[h][m] = v[h] ? fmaf(e, sq[m], acc[h][m]) : acc[h][m];
+                }
             }
         }
     }
 }
 
+// Weight units per row: 32-value blocks, or 64-value pieces of super-blocks.
+__host__ __device__ constexpr int batch_units(int wt, int K) { return is_sb(wt) ? K / 64 : K / 32; }
+
+// The contribution of unit b (b < nb) of the R rows at wrow[h] to acc.
 template <int WT, int AM, int MT, int R>
-__device__ __forceinline__ void unit_dot(const uint8_t* s, const int (&wo)[R], int ao, int astep, int M,
+__device__ __forceinline__ void unit_dot(const uint8_t* s, const int (&wrow)[R], int b, int acts, int astep, int M,
                                          const bool (&v)[R], float (&acc)[R][MT]) {
-    if (WT == T_Q4_K) q4k_unit_dot<AM, MT, R>(s, wo, ao, astep, M, v, acc);
-    else if (WT == T_Q6_K) q6k_unit_dot<AM, MT, R>(s, wo, ao, astep, M, v, acc);
-    else block_dot<WT, AM, MT, R>(s, wo, ao, astep, M, v, acc);
+    constexpr int BB = unit_bytes(WT), ES = batch_act_unit(WT, AM);
+    int wo[R];
+    if (is_sb(WT)) {
+#pragma unroll
+        for (int h = 0; h < R; ++h) wo[h] = wrow[h] + (b >> 2) * BB;
+        if (WT == T_Q4_K) q4k_piece_dot<AM, MT, R>(s, wo, b & 3, acts + (b >> 2) * ES, astep, M, v, acc);
+        else q6k_piece_dot<AM, MT, R>(s, wo, b & 3, acts + (b >> 2) * ES, astep, M, v, acc);
+    } else {
+#pragma unroll
+        for (int h = 0; h < R; ++h) wo[h] = wrow[h] + b * BB;
+        block_dot<WT, AM, MT, R>(s, wo, acts + b * ES, astep, M, v, acc);
+    }
 }
 
 // The first item whose weight bytes reach past lo (items are in byte order).
@@ -503,11 +499,12 @@ __device__ __forceinline__ long long batch_row_bytes(int wt, int K) {
 }
 
 // The item's activation rows into shared memory at o, unit (m, b) at
-// (m * nu + b) * batch_act_unit (the consumer warps; rows are contiguous).
+// (m * nu + b) * batch_act_unit, in the layout of weight type wt (the consumer
+// warps; rows are contiguous).
 template <int AM>
-__device__ __forceinline__ void stage_acts(const BatchItem& it, bool sb, uint8_t* o, int tid, int warp, int lane) {
+__device__ __forceinline__ void stage_acts(const BatchItem& it, int wt, uint8_t* o, int tid, int warp, int lane) {
     const int M = it.M;
-    if (!sb) {
+    if (!is_sb(wt)) {
         if (AM == A_INT8) {
             for (int blk = tid; blk < M * (it.K / 32); blk += kBatchWarps * 32) {
                 uint32_t c[8];
@@ -526,7 +523,8 @@ __device__ __forceinline__ void stage_acts(const BatchItem& it, bool sb, uint8_t
         return;
     }
     // super-block types: one warp per 256 values, lane l taking values 8l..8l+7
-    // (sub-block l / 4)
+    // (sub-block l / 4), stored in the slot order of weight type wt
+    const int slot = batch_slot(wt, lane >> 2), part = lane & 3;
     for (int u = warp; u < M * (it.K / 256); u += kBatchWarps) {
         const float4* src = reinterpret_cast<const float4*>(it.x + 256ll * u + 8 * lane);
         const float4 v0 = __ldg(src), v1 = __ldg(src + 1);
@@ -541,19 +539,19 @@ __device__ __forceinline__ void stage_acts(const BatchItem& it, bool sb, uint8_t
             q8_scale(amax, d, id);
             const uint32_t w0 = pack4(q8_code(v0.x, id), q8_code(v0.y, id), q8_code(v0.z, id), q8_code(v0.w, id));
             const uint32_t w1 = pack4(q8_code(v1.x, id), q8_code(v1.y, id), q8_code(v1.z, id), q8_code(v1.w, id));
-            *reinterpret_cast<uint2*>(dst + 8 * lane) = make_uint2(w0, w1);
+            *reinterpret_cast<uint2*>(dst + 48 * slot + 8 * part) = make_uint2(w0, w1);
             int sum = bsum4(w0) + bsum4(w1);
             sum += __shfl_xor_sync(0xffffffffu, sum, 1);
             sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-            if ((lane & 3) == 0) *reinterpret_cast<int*>(dst + 256 + lane) = sum;
-            if (lane == 0) *reinterpret_cast<float*>(dst + 288) = d;
+            if (part == 0) *reinterpret_cast<int*>(dst + 384 + lane) = sum;  // sub-block lane / 4
+            if (lane == 0) *reinterpret_cast<float*>(dst + 416) = d;
         } else {
-            *reinterpret_cast<float4*>(dst + 32 * lane) = v0;
-            *reinterpret_cast<float4*>(dst + 32 * lane + 16) = v1;
+            *reinterpret_cast<float4*>(dst + 144 * slot + 32 * part) = v0;
+            *reinterpret_cast<float4*>(dst + 144 * slot + 32 * part + 16) = v1;
             float sum = ((v0.x + v0.y) + (v0.z + v0.w)) + ((v1.x + v1.y) + (v1.z + v1.w));
             sum += __shfl_xor_sync(0xffffffffu, sum, 1);
             sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-            if ((lane & 3) == 0) *reinterpret_cast<float*>(dst + 1024 + lane) = sum;
+            if (part == 0) *reinterpret_cast<float*>(dst + 1152 + lane) = sum;
         }
     }
 }
@@ -563,17 +561,16 @@ template <int WT, int AM, int MT>
 __device__ __forceinline__ void batch_piece(const BatchParams& p, const BatchItem& it, long long r0, long long r1,
                                             uint8_t* smem, int acts, uint64_t* bars, volatile int* flags, int& slot,
                                             uint32_t& phase, int warp, int lane) {
-    constexpr int BB = unit_bytes(WT);
     constexpr int ES = batch_act_unit(WT, AM);
     constexpr int R = batch_rows_per_group(WT, AM, MT);
     const int S = p.stages;
-    const int nb = it.K / unit_vals(WT), M = it.M, rb = nb * BB;
+    const int nb = batch_units(WT, it.K), M = it.M, rb = (int)batch_row_bytes(WT, it.K);
     // lanes in groups of lpr, R weight rows per group: lane gl of a group takes the
     // rows' units gl, gl + lpr, ... (bpl of them), and the group sums its lanes.
     // A warp holds rpw groups; its rows are j0 + grp + h * rpw.
     const int lpr = it.lpr, bpl = it.bpl, tr = it.tr, rpw = 32 / lpr;
     const int grp = lane / lpr, gl = lane - grp * lpr;
-    const int astep = nb * ES;
+    const int astep = it.K / unit_vals(WT) * ES;
     for (long long r = r0; r < r1; r += tr) {
         const bool ok = mbar_wait(smem_u32(&bars[slot]), phase, flags, p.err);
         const int rows = (int)(r + tr < r1 ? tr : r1 - r);
@@ -594,12 +591,10 @@ __device__ __forceinline__ void batch_piece(const BatchParams& p, const BatchIte
                 for (int m = 0; m < MT; ++m) acc[h][m] = 0.0f;
             for (int q = 0; q < bpl; ++q) {
                 const int b = gl + q * lpr;
-                const int cb = b < nb ? b : 0;
                 bool v[R];
-                int wo[R];
 #pragma unroll
-                for (int h = 0; h < R; ++h) v[h] = jv[h] && b < nb, wo[h] = wrow[h] + cb * BB;
-                unit_dot<WT, AM, MT, R>(smem, wo, acts + cb * ES, astep, M, v, acc);
+                for (int h = 0; h < R; ++h) v[h] = jv[h] && b < nb;
+                unit_dot<WT, AM, MT, R>(smem, wrow, b < nb ? b : 0, acts, astep, M, v, acc);
             }
             // the group's sums: a tree over offsets below lpr, lanes past the group masked
 #pragma unroll
@@ -691,19 +686,19 @@ __global__ void __launch_bounds__((kBatchWarps + 1) * 32, 1) qmm_batch_kernel(co
     int slot = 0;
     uint32_t phase = 0;
     const float* prep_x = nullptr;  // the activations now in shared memory
-    int prep_m = 0, prep_k = 0, prep_sb = 0;
+    int prep_m = 0, prep_k = 0, prep_layout = -1;
     for (int i = batch_first_item(p, lo); i < p.count && p.it[i].byte0 < hi; ++i) {
         const BatchItem& it = p.it[i];
         const int wt = WT == T_MIX ? it.wt : WT;
         long long r0, r1;
         batch_rows(it, batch_row_bytes(wt, it.K), lo, hi, r0, r1);
         if (r0 >= r1) continue;
-        const int sb = is_sb(wt) ? 1 : 0;
-        if (it.x != prep_x || it.M != prep_m || it.K != prep_k || sb != prep_sb) {
+        const int layout = is_sb(wt) ? wt : 0;  // Q8_0 blocks, or Q8K in a type's slot order
+        if (it.x != prep_x || it.M != prep_m || it.K != prep_k || layout != prep_layout) {
             consumer_sync<kBatchWarps>();  // the previous activations are no longer read
-            stage_acts<AM>(it, sb, smem + acts, tid, warp, lane);
+            stage_acts<AM>(it, wt, smem + acts, tid, warp, lane);
             consumer_sync<kBatchWarps>();
-            prep_x = it.x, prep_m = it.M, prep_k = it.K, prep_sb = sb;
+            prep_x = it.x, prep_m = it.M, prep_k = it.K, prep_layout = layout;
         }
         if (WT != T_MIX) {
             batch_piece<WT, AM, MT>(p, it, r0, r1, smem, acts, bars, flags, slot, phase, warp, lane);
