@@ -108,12 +108,13 @@ size_t workspace_for(const StreamPlan& pl) {
 // The kernel a matmul call dispatches to and its plan.  Planning searches
 // chunk sizes and K splits, so decisions are cached per host thread by
 // (device, type, form, epilogue, M, N, K).
-enum Kind { KIND_NONE, KIND_GEMV, KIND_DMMA, KIND_TC, KIND_PREFILL, KIND_STREAM };
+enum Kind { KIND_NONE, KIND_GEMV, KIND_DMMA, KIND_TC, KIND_TCX, KIND_PREFILL, KIND_STREAM };
 struct Dispatch {
     Kind kind = KIND_NONE;
     GemvPlan gp;
     DmmaPlan dp;
     TcPlan tp;
+    TcxPlan xp;
     PrefillPlan fp;
     StreamPlan sp;
     size_t workspace = 0;
@@ -152,6 +153,10 @@ void plan_dispatch(int wt, int am, int epi, long long M, long long N, long long 
         d.kind = KIND_TC;
         d.workspace = d.tp.workspace;
         d.launches = 2;  // operand preparation, GEMM
+    } else if (epi == E_Y && am == A_INT8 && plan_tcx(wt, M, N, K, sms, smem, d.xp)) {  // CPU-form prefill (Q8_0): exact block sums on tcgen05
+        d.kind = KIND_TCX;
+        d.workspace = d.xp.workspace;
+        d.launches = 2;  // activation codes, GEMM
     } else if (epi == E_Y && am == A_INT8 && plan_prefill(wt, M, N, K, sms, smem, d.fp)) {  // CPU-form prefill (Q8_0): exact block sums
         d.kind = KIND_PREFILL;
         d.workspace = d.fp.workspace;
@@ -235,6 +240,12 @@ qmm_status stream_call(qmm_type wtype, int am, int epi, const void* wq, const fl
         TcPlan tp = d.tp;
         tp.p.err = err;
         return launch_tc(wt, tp, wq, x, ws, y, smem, s) == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
+    }
+    if (d.kind == KIND_TCX) {
+        if (!ws || ws_bytes < d.xp.workspace) return QMM_ERR_WORKSPACE;
+        TcxPlan xp = d.xp;
+        xp.p.err = err;
+        return launch_tcx(xp, wq, x, ws, y, smem, s) == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
     }
     if (d.kind == KIND_PREFILL) {
         if (!ws || ws_bytes < d.fp.workspace) return QMM_ERR_WORKSPACE;
@@ -440,8 +451,9 @@ qmm_status batch_run(qmm_act_mode mode, int64_t count, bool have_items, Get get,
             it.K = (int)d.K;
             it.wt = wt;
             it.lpr = it.bpl = it.tr = 0;
-            it.byte0 = p.total;
-            p.total += d.N * (int64_t)qmm_row_bytes(d.wtype, d.K);
+            it.cpr = batch_row_cost(wt, am, (int)d.K);
+            it.c0 = p.total;
+            p.total += d.N * (int64_t)it.cpr;
             const int64_t ab = d.M * (d.K / unit_vals(wt)) * batch_act_unit(wt, am);
             if (ab > p.act_bytes) p.act_bytes = (int)ab;
             if (d.M > max_m) max_m = (int)d.M;

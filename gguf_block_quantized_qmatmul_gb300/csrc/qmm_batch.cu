@@ -20,6 +20,22 @@ int unit_work(int wt) { return is_sb(wt) ? 3 : 1; }
 
 }  // namespace
 
+int batch_row_cost(int wt, int am, int K) {
+    // time of 32 values at saturation, in units of about 10 fs (batches of one
+    // type, M = 1, K = 1536 and 4096): the 32-value types with Q8_0 activations
+    // and Q8_0 weights are bound by bytes, Q5_0 and Q4_0 by unpacking, so their
+    // rows cost alike per value although their bytes differ by 1.5-1.9x
+    int w;
+    switch (wt) {
+        case T_Q8_0: w = am == A_INT8 ? 28 : 36; break;
+        case T_Q5_0: w = am == A_INT8 ? 29 : 34; break;
+        case T_Q4_0: w = am == A_INT8 ? 22 : 29; break;
+        case T_Q4_K: w = am == A_INT8 ? 21 : 30; break;
+        default: w = am == A_INT8 ? 30 : 37; break;  // Q6_K
+    }
+    return K / 32 * w;
+}
+
 void plan_batch_item(int wt, int nu, long long rb, int am, int mt, int& lpr, int& bpl, int& tr) {
     // Lanes per row (lpr) and units per lane (bpl = ceil(nu / lpr)) for a row of
     // nu units of type wt (rb bytes), and rows per stage (tr).  int8_act on

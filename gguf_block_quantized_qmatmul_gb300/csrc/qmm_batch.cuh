@@ -21,9 +21,11 @@
 //             sub-block (e_j = f(d) sc_j, o_j = f(dmin) m_j), f(d) sc_g
 //             sum(q x) per Q6_K group.
 //
-// The weight bytes of all items are one virtual stream; CTA c (one per SM)
-// takes the rows whose first byte falls in its 1/G share of it, item by item
-// (a "piece": consecutive rows of one item, contiguous bytes).  A producer
+// The rows of all items are one virtual stream, each row weighted by its
+// cost (its values times a per-type, per-form cost of 32 values measured at
+// saturation); CTA c (one per SM) takes the rows whose first position falls in
+// its 1/G share of the total, item by item (a "piece": consecutive rows of one
+// item, contiguous bytes).  A producer
 // lane streams each piece in stages of whole rows, one 1-D bulk copy per
 // stage, into a ring of shared-memory slots (the copy engine pays a fixed cost
 // per contiguous segment, so stages are large).  16 consumer warps stage the
@@ -54,14 +56,15 @@ struct BatchItem {
     const uint8_t* wq;
     const float* x;
     float* y;
-    long long byte0;  // the item's first weight byte in the launch's byte order
+    long long c0;     // the item's first position in the launch's cost order
+    int cpr;          // the cost of one of its rows (batch_row_cost)
     int M, N, K;
     int wt;            // weight type (T_Q8_0, T_Q4_0, T_Q5_0, T_Q4_K, T_Q6_K)
     int lpr, bpl, tr;  // lanes per row, units per lane, rows per stage (set by the launcher)
 };
 struct BatchParams {
     BatchItem it[kBatchMax];
-    long long total;  // weight bytes of all items
+    long long total;  // the cost of all items
     unsigned* err;    // the device error word (bounded waits)
     int count;
     int act_bytes;    // the most shared-memory bytes one item's staged activations take
@@ -95,6 +98,11 @@ __host__ __device__ constexpr int batch_rows_per_group(int wt, int am, int mt) {
 }
 
 cudaError_t launch_batch(int wt, int am, const BatchParams& p, int max_m, int sm_count, int smem_max, cudaStream_t s);
+// The cost of one weight row of K values of type wt in form am: the CTAs take
+// equal shares of the launch's total cost, so that types that are cheap in
+// bytes but dear in unpacking (Q5_0, Q4_0) do not leave the CTAs holding
+// bandwidth-bound rows (Q8_0) idle.
+int batch_row_cost(int wt, int am, int K);
 cudaError_t launch_batch_mix(int am, BatchParams& p, int mt, int grid, int smem_max, cudaStream_t s);
 // lpr, bpl and tr for a row of nu units of weight type wt, rb bytes
 void plan_batch_item(int wt, int nu, long long rb, int am, int mt, int& lpr, int& bpl, int& tr);
@@ -472,24 +480,23 @@ __device__ __forceinline__ void unit_dot(const uint8_t* s, const int (&wrow)[R],
     }
 }
 
-// The first item whose weight bytes reach past lo (items are in byte order).
+// The first item whose cost reaches past lo (items are in cost order).
 __device__ __forceinline__ int batch_first_item(const BatchParams& p, long long lo) {
     int a = 0, b = p.count;  // invariant: items before a end at or before lo
     while (a < b) {
         const int m = (a + b) >> 1;
-        const long long end = m + 1 < p.count ? p.it[m + 1].byte0 : p.total;
+        const long long end = m + 1 < p.count ? p.it[m + 1].c0 : p.total;
         if (end <= lo) a = m + 1;
         else b = m;
     }
     return a;
 }
 
-// The rows of item it whose first weight byte lies in [lo, hi): [r0, r1).
-__device__ __forceinline__ void batch_rows(const BatchItem& it, long long rb, long long lo, long long hi, long long& r0,
-                                           long long& r1) {
-    const long long b0 = it.byte0;
-    r0 = lo > b0 ? (lo - b0 + rb - 1) / rb : 0;
-    r1 = hi > b0 ? (hi - b0 + rb - 1) / rb : 0;
+// The rows of item it whose first cost position lies in [lo, hi): [r0, r1).
+__device__ __forceinline__ void batch_rows(const BatchItem& it, long long lo, long long hi, long long& r0, long long& r1) {
+    const long long c0 = it.c0, rc = it.cpr;
+    r0 = lo > c0 ? (lo - c0 + rc - 1) / rc : 0;
+    r1 = hi > c0 ? (hi - c0 + rc - 1) / rc : 0;
     if (r1 > it.N) r1 = it.N;
     if (r0 > r1) r0 = r1;
 }
@@ -653,11 +660,11 @@ __global__ void __launch_bounds__((kBatchWarps + 1) * 32, 1) qmm_batch_kernel(co
         long long g = 0;
         int slot = 0, round = 0;
         bool ok = true;
-        for (int i = batch_first_item(p, lo); i < p.count && p.it[i].byte0 < hi && ok; ++i) {
+        for (int i = batch_first_item(p, lo); i < p.count && p.it[i].c0 < hi && ok; ++i) {
             const BatchItem& it = p.it[i];
             const long long rb = batch_row_bytes(WT == T_MIX ? it.wt : WT, it.K);
             long long r0, r1;
-            batch_rows(it, rb, lo, hi, r0, r1);
+            batch_rows(it, lo, hi, r0, r1);
             const int tr = it.tr;
             const long long end = (long long)it.N * rb;  // the item's buffer
             for (long long r = r0; r < r1 && ok; r += tr, ++g) {
@@ -687,11 +694,11 @@ __global__ void __launch_bounds__((kBatchWarps + 1) * 32, 1) qmm_batch_kernel(co
     uint32_t phase = 0;
     const float* prep_x = nullptr;  // the activations now in shared memory
     int prep_m = 0, prep_k = 0, prep_layout = -1;
-    for (int i = batch_first_item(p, lo); i < p.count && p.it[i].byte0 < hi; ++i) {
+    for (int i = batch_first_item(p, lo); i < p.count && p.it[i].c0 < hi; ++i) {
         const BatchItem& it = p.it[i];
         const int wt = WT == T_MIX ? it.wt : WT;
         long long r0, r1;
-        batch_rows(it, batch_row_bytes(wt, it.K), lo, hi, r0, r1);
+        batch_rows(it, lo, hi, r0, r1);
         if (r0 >= r1) continue;
         const int layout = is_sb(wt) ? wt : 0;  // Q8_0 blocks, or Q8K in a type's slot order
         if (it.x != prep_x || it.M != prep_m || it.K != prep_k || layout != prep_layout) {

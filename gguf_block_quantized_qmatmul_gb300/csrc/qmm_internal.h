@@ -7,6 +7,7 @@
 #include "qmm_gemv.cuh"
 #include "qmm_prefill.cuh"
 #include "qmm_tc.cuh"
+#include "qmm_tcx.cuh"
 #include "qmm_stream.cuh"
 
 namespace qmm {
@@ -27,6 +28,7 @@ cudaError_t launch_dmma_q6_k(int am, int epi, const DmmaPlan& plan, int smem_max
 cudaError_t launch_dmma_prep(int wt, int am, const DmmaPlan& plan, void* ext, cudaStream_t s);
 cudaError_t launch_tc(int wt, const TcPlan& plan, const void* wq, const float* x, void* ws, float* y, int smem_max,
                       cudaStream_t s);
+cudaError_t launch_tcx(const TcxPlan& plan, const void* wq, const float* x, void* ws, float* y, int smem_max, cudaStream_t s);
 cudaError_t launch_prefill(const PrefillPlan& plan, const void* wq, const float* x, void* ws, float* y, int smem_max,
                            cudaStream_t s);
 // A 2-D tensor map (rows of `inner` elements, `row_bytes` apart) with a box

@@ -149,6 +149,26 @@ int check_prefill(long long M, long long N, long long K) {
     return 1;
 }
 
+int check_tcx(long long M, long long N, long long K) {
+    TcxPlan pl;
+    if (!plan_tcx(T_Q8_0, M, N, K, kSms, kSmem, pl)) return 0;
+    const TcxParams& p = pl.p;
+#define CASE "tcx M%lld N%lld K%lld", M, N, K
+    CHECK(pl.smem <= (size_t)kSmem && p.nraw >= 3 && p.nraw <= kTxRawMax, CASE);
+    CHECK(p.off_raw == kTxS * kTxStage && p.off_raw % 1024 == 0 && kTxRawSlot % 1024 == 0 &&
+              p.off_bar == p.off_raw + p.nraw * kTxRawSlot && (size_t)p.off_bar + 512 + 1024 <= pl.smem,
+          CASE);
+    CHECK(p.nrs * 256 == K && (long long)p.mtiles * kTxX >= M && (long long)p.ntiles * kTxW >= N &&
+              p.units == p.mtiles * p.ntiles,
+          CASE);
+    CHECK(pl.grid >= 1 && pl.grid <= kSms && pl.grid <= p.units && pl.mp % 4 == 0 && pl.mp >= M, CASE);
+    CHECK(pl.ws_scales >= (size_t)M * K * 2 && pl.ws_scales % 256 == 0 &&
+              pl.workspace >= pl.ws_scales + (size_t)(K / 32) * pl.mp * 4,
+          CASE);
+#undef CASE
+    return 1;
+}
+
 int check_stream(int wt, int am, int epi, long long M, long long N, long long K) {
     StreamPlan pl;
     if (!plan_stream(wt, am, epi, M, N, K, kSms, kSmem, pl)) return 0;
@@ -202,7 +222,7 @@ int main() {
             for (long long N : {128, 300, 4096, 14336})
                 for (long long K : {256, 1024, 4096, 14336}) {
                     plans += check_tc(wt, M, N, K);
-                    if (wt == T_Q8_0) plans += check_prefill(M, N, K);
+                    if (wt == T_Q8_0) plans += check_prefill(M, N, K) + check_tcx(M, N, K);
                 }
     }
     for (int wt : types)
