@@ -108,14 +108,13 @@ size_t workspace_for(const StreamPlan& pl) {
 // The kernel a matmul call dispatches to and its plan.  Planning searches
 // chunk sizes and K splits, so decisions are cached per host thread by
 // (device, type, form, epilogue, M, N, K).
-enum Kind { KIND_NONE, KIND_GEMV, KIND_DMMA, KIND_TC, KIND_TCX, KIND_PREFILL, KIND_STREAM };
+enum Kind { KIND_NONE, KIND_GEMV, KIND_DMMA, KIND_TC, KIND_TCX, KIND_STREAM };
 struct Dispatch {
     Kind kind = KIND_NONE;
     GemvPlan gp;
     DmmaPlan dp;
     TcPlan tp;
     TcxPlan xp;
-    PrefillPlan fp;
     StreamPlan sp;
     size_t workspace = 0;
     int launches = 0;
@@ -156,10 +155,6 @@ void plan_dispatch(int wt, int am, int epi, long long M, long long N, long long 
     } else if (epi == E_Y && am == A_INT8 && plan_tcx(wt, M, N, K, sms, smem, d.xp)) {  // CPU-form prefill (Q8_0): exact block sums on tcgen05
         d.kind = KIND_TCX;
         d.workspace = d.xp.workspace;
-        d.launches = 2;  // activation codes, GEMM
-    } else if (epi == E_Y && am == A_INT8 && plan_prefill(wt, M, N, K, sms, smem, d.fp)) {  // CPU-form prefill (Q8_0): exact block sums
-        d.kind = KIND_PREFILL;
-        d.workspace = d.fp.workspace;
         d.launches = 2;  // activation codes, GEMM
     } else if (plan_stream(wt, am, epi, M, N, K, sms, smem, d.sp)) {
         d.kind = KIND_STREAM;
@@ -246,12 +241,6 @@ qmm_status stream_call(qmm_type wtype, int am, int epi, const void* wq, const fl
         TcxPlan xp = d.xp;
         xp.p.err = err;
         return launch_tcx(xp, wq, x, ws, y, smem, s) == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
-    }
-    if (d.kind == KIND_PREFILL) {
-        if (!ws || ws_bytes < d.fp.workspace) return QMM_ERR_WORKSPACE;
-        PrefillPlan fp = d.fp;
-        fp.p.err = err;
-        return launch_prefill(fp, wq, x, ws, y, smem, s) == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
     }
     if (d.kind != KIND_STREAM) return QMM_ERR_SHAPE;
     StreamPlan pl = d.sp;

@@ -133,22 +133,6 @@ int check_tc(int wt, long long M, long long N, long long K) {
     return 1;
 }
 
-int check_prefill(long long M, long long N, long long K) {
-    PrefillPlan pl;
-    if (!plan_prefill(T_Q8_0, M, N, K, kSms, kSmem, pl)) return 0;
-    const PrefillParams& p = pl.p;
-#define CASE "prefill M%lld N%lld K%lld", M, N, K
-    CHECK(pl.smem <= (size_t)kSmem && p.stages >= 2 && p.stages <= 4, CASE);
-    CHECK(p.off_a % 1024 == 0 && p.off_s == p.off_a + 4 * p.bm * 128 && p.stage_bytes % 1024 == 0 &&
-              p.stage_bytes >= p.off_s + p.bm * 32,
-          CASE);
-    CHECK(p.kchunks * kPfKC == K && (long long)p.n_mt * p.bm >= M && (long long)p.n_nt * kPfBN >= N, CASE);
-    CHECK(pl.grid >= 1 && pl.grid <= kSms && pl.ws_s == (size_t)M * K * 2 && pl.workspace >= pl.ws_s + (size_t)M * (K / 32) * 4,
-          CASE);
-#undef CASE
-    return 1;
-}
-
 int check_tcx(long long M, long long N, long long K) {
     TcxPlan pl;
     if (!plan_tcx(T_Q8_0, M, N, K, kSms, kSmem, pl)) return 0;
@@ -222,7 +206,7 @@ int main() {
             for (long long N : {128, 300, 4096, 14336})
                 for (long long K : {256, 1024, 4096, 14336}) {
                     plans += check_tc(wt, M, N, K);
-                    if (wt == T_Q8_0) plans += check_prefill(M, N, K) + check_tcx(M, N, K);
+                    if (wt == T_Q8_0) plans += check_tcx(M, N, K);
                 }
     }
     for (int wt : types)
@@ -243,11 +227,11 @@ int main() {
             for (long long M : {1, 2, 4, 8, 16})
                 CHECK(plan_dmma(wt, am, M, 28672, 8192, kSms, kSmem, dp, true), "no decode plan for %s am%d M%lld", tname(wt), am, M);
     TcPlan tp;
-    PrefillPlan fp;
+    TcxPlan xp;
     for (long long M : {37, 64, 256, 1024})
         for (int wt : types) {
             CHECK(plan_tc(wt, M, 14336, 4096, kSms, kSmem, tp), "no tcgen05 plan for %s M%lld", tname(wt), M);
-            if (wt == T_Q8_0) CHECK(plan_prefill(wt, M, 14336, 4096, kSms, kSmem, fp), "no exact prefill plan for M%lld", M);
+            if (wt == T_Q8_0) CHECK(plan_tcx(wt, M, 14336, 4096, kSms, kSmem, xp), "no exact prefill plan for M%lld", M);
         }
     std::printf("%s %d plans\n", g_bad ? "FAILED" : "ok", plans);
     return g_bad ? 1 : 0;
