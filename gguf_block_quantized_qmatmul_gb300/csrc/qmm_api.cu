@@ -152,7 +152,7 @@ void plan_dispatch(int wt, int am, int epi, long long M, long long N, long long 
         d.kind = KIND_TC;
         d.workspace = d.tp.workspace;
         d.launches = 2;  // operand preparation, GEMM
-    } else if (epi == E_Y && am == A_INT8 && plan_tcx(wt, M, N, K, sms, smem, d.xp)) {  // CPU-form prefill (Q8_0): exact block sums on tcgen05
+    } else if (epi == E_Y && am == A_INT8 && plan_tcx(wt, M, N, K, sms, smem, d.xp)) {  // CPU-form prefill (Q8_0, Q4_K): exact block sums on tcgen05
         d.kind = KIND_TCX;
         d.workspace = d.xp.workspace;
         d.launches = 2;  // activation codes, GEMM
@@ -240,7 +240,7 @@ qmm_status stream_call(qmm_type wtype, int am, int epi, const void* wq, const fl
         if (!ws || ws_bytes < d.xp.workspace) return QMM_ERR_WORKSPACE;
         TcxPlan xp = d.xp;
         xp.p.err = err;
-        return launch_tcx(xp, wq, x, ws, y, smem, s) == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
+        return launch_tcx(wt, xp, wq, x, ws, y, smem, s) == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
     }
     if (d.kind != KIND_STREAM) return QMM_ERR_SHAPE;
     StreamPlan pl = d.sp;

@@ -5,36 +5,51 @@
 namespace qmm {
 
 namespace {
-unsigned long long g_tcx_smem_done;
-}
+unsigned long long g_tcx_smem_done[2];
 
-cudaError_t launch_tcx(const TcxPlan& pl, const void* wq, const float* x, void* ws, float* y, int smem_max, cudaStream_t s) {
+template <int WT>
+cudaError_t tcx_go(const TcxPlan& pl, const void* wq, const float* x, void* ws, float* y, int smem_max, cudaStream_t s) {
+    using R = TxRaw<WT>;
     const TcxParams& p0 = pl.p;
     uint8_t* wsb = static_cast<uint8_t*>(ws);
     __half* codes = reinterpret_cast<__half*>(wsb + pl.ws_codes);
     float* scales = reinterpret_cast<float*>(wsb + pl.ws_scales);
-    // 1. the activation operand: f16 codes [M][K], f(d_a) block-major [K / 32][mp]
-    const long long items = (long long)p0.M * (p0.K / 32);
-    tcx_act_kernel<T_Q8_0><<<(unsigned)((items + 255) / 256), 256, 0, s>>>(x, p0.M, p0.K, pl.mp, codes, scales);
+    __half* bsums = reinterpret_cast<__half*>(wsb + pl.ws_bsums);
+    // 1. the activation operand: f16 codes [M][K], scales block-major, (Q4_K) sums of 16 codes
+    const long long items = WT == T_Q8_0 ? (long long)p0.M * (p0.K / 32) : (long long)p0.M * (p0.K / 256) * 32;
+    tcx_act_kernel<WT><<<(unsigned)((items + 255) / 256), 256, 0, s>>>(x, p0.M, p0.K, pl.mp, codes, scales, bsums);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    // 2. tensor maps: raw weight rows as uint16 (128 rows x 272 B); activation codes,
-    //    32 K x 128 rows, 64-byte swizzle; activation scales, 128 rows x 8 blocks
-    CUtensorMap tw, ta, ts;
-    const unsigned long long rb = (unsigned long long)p0.K / 32 * 34;
-    if (!make_map(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT16, wq, rb / 2, p0.N, rb, kTxRaw / 2, kTxW, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !make_map(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, codes, p0.K, p0.M, (unsigned long long)p0.K * 2, 32, kTxX,
-                  CU_TENSOR_MAP_SWIZZLE_64B) ||
-        !make_map(&ts, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, scales, pl.mp, p0.K / 32, (unsigned long long)pl.mp * 4, kTxX, 8,
-                  CU_TENSOR_MAP_SWIZZLE_NONE))
-        return cudaErrorInvalidValue;
+    // 2. tensor maps: raw weight rows as uint16 (128 rows x 256 K); activation codes, 32 K x
+    //    128 rows, 64-byte swizzle; activation scales; (Q4_K) the sums of 16 codes, 16 x 128
+    //    rows, 32-byte swizzle
+    CUtensorMap tw, ta, ts, tb;
+    const unsigned long long rb = (unsigned long long)p0.K / 256 * R::row;
+    const unsigned long long nsc = WT == T_Q8_0 ? p0.K / 32 : p0.K / 256;
+    bool ok = make_map(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT16, wq, rb / 2, p0.N, rb, R::row / 2, kTxW, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+              make_map(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, codes, p0.K, p0.M, (unsigned long long)p0.K * 2, 32, kTxX,
+                       CU_TENSOR_MAP_SWIZZLE_64B) &&
+              make_map(&ts, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, scales, pl.mp, nsc, (unsigned long long)pl.mp * 4, kTxX,
+                       WT == T_Q8_0 ? 8 : 1, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (WT == T_Q4_K)
+        ok = ok && make_map(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, bsums, p0.K / 16, p0.M, (unsigned long long)p0.K / 8, 16,
+                            kTxX, CU_TENSOR_MAP_SWIZZLE_32B);
+    else
+        tb = ts;  // unused
+    if (!ok) return cudaErrorInvalidValue;
     TcxParams p = p0;
     p.y = y;
     // 3. the GEMM, a programmatic dependent of the preparation
-    auto* k = qmm_tcx_kernel<T_Q8_0>;
-    e = ensure_smem(k, smem_max, g_tcx_smem_done);
+    auto* k = qmm_tcx_kernel<WT>;
+    e = ensure_smem(k, smem_max, g_tcx_smem_done[WT == T_Q8_0 ? 0 : 1]);
     if (e != cudaSuccess) return e;
-    return launch_pdl(k, (unsigned)pl.grid, kTxThreads, pl.smem, s, tw, ta, ts, p);
+    return launch_pdl(k, (unsigned)pl.grid, kTxThreads, pl.smem, s, tw, ta, ts, tb, p);
+}
+}  // namespace
+
+cudaError_t launch_tcx(int wt, const TcxPlan& pl, const void* wq, const float* x, void* ws, float* y, int smem_max,
+                       cudaStream_t s) {
+    return wt == T_Q8_0 ? tcx_go<T_Q8_0>(pl, wq, x, ws, y, smem_max, s) : tcx_go<T_Q4_K>(pl, wq, x, ws, y, smem_max, s);
 }
 
 }  // namespace qmm

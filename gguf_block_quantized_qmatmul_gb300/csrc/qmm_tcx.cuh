@@ -42,14 +42,31 @@ constexpr int kTxX = 128;         // activation rows per tile (MMA N)
 constexpr int kTxS = 4;           // block stages: weight codes + activation codes in shared memory
 constexpr int kTxAcc = 4;         // TMEM accumulators of kTxX columns
 constexpr int kTxTmemCols = kTxAcc * kTxX;
-constexpr int kTxRaw = 272;       // raw bytes per weight row per raw stage (8 Q8_0 blocks)
 constexpr int kTxRawMax = 6;
 constexpr int kTxEpiWarps = 16;
 constexpr int kTxConvWarps = 4;
 constexpr int kTxThreads = (2 + kTxEpiWarps + kTxConvWarps) * 32;
-constexpr int kTxStage = 2 * kTxW * 64;                 // A (weights) then B (activations): 8 KB each
-constexpr int kTxScaleOff = kTxW * kTxRaw;              // activation scales inside a raw slot
-constexpr int kTxRawSlot = (kTxScaleOff + 8 * kTxX * 4 + 1023) / 1024 * 1024;
+constexpr int kTxStage = 2 * kTxW * 64;  // A (weights) then B (activations): 8 KB each
+
+// A raw stage holds 256 K of the tile's 128 weight rows and what the fold
+// needs of the tile's 128 activation rows:
+//   Q8_0: rows of 272 B (8 blocks); f(d_a) of the 8 blocks, [8][128] f32;
+//   Q4_K: rows of 144 B (1 super-block); d_a, [128] f32; the min term's
+//         activation operand (16 sums of 16 codes per row, f16, 32-byte
+//         swizzle) and its weight operand (m_j twice each, written by the
+//         converters).
+template <int WT>
+struct TxRaw {
+    static constexpr int row = WT == T_Q8_0 ? 272 : 144;
+    static constexpr int scales = kTxW * row;                                      // f(d_a)
+    static constexpr int bsum = WT == T_Q8_0 ? 0 : scales + 1024;                  // Q4_K: [128][16] f16
+    static constexpr int amin = WT == T_Q8_0 ? 0 : bsum + kTxX * 32;              // Q4_K: [128][16] f16
+    static constexpr int slot = WT == T_Q8_0 ? (scales + 8 * kTxX * 4 + 1023) / 1024 * 1024 : amin + kTxW * 32;
+    static constexpr int tx = WT == T_Q8_0 ? kTxW * row + 8 * kTxX * 4 : kTxW * row + kTxX * 4 + kTxX * 32;
+    // accumulators (drain units) per raw stage: Q8_0 one per block; Q4_K S_sc and S_m
+    static constexpr int drains = WT == T_Q8_0 ? 8 : 2;
+};
+static_assert(TxRaw<T_Q8_0>::slot % 1024 == 0 && TxRaw<T_Q4_K>::slot % 1024 == 0, "1 KB aligned raw slots");
 
 struct TcxParams {
     float* y;
@@ -68,6 +85,12 @@ __device__ __forceinline__ void tcx_mma(uint32_t tmem, uint64_t da, uint64_t db,
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem),
         "l"(da), "l"(db), "r"(idesc), "r"(accumulate)
         : "memory");
+}
+
+// shared-memory matrix descriptor: K-major, 32-byte swizzle (rows of 16 f16), 8-row atoms 256 B apart
+__device__ __forceinline__ uint64_t tcx_sdesc32(uint32_t addr) {
+    return (uint64_t)((addr >> 4) & 0x3FFF) | ((uint64_t)1 << 16) | ((uint64_t)(256 >> 4) << 32) | ((uint64_t)1 << 46) |
+           ((uint64_t)6 << 61);
 }
 
 // signed codes of a word (4 bytes) as two exact f16 pairs: bytes 0, 1 and 2, 3
@@ -101,26 +124,51 @@ __device__ __forceinline__ void tcx_conv_q8_0(const uint8_t* row, uint32_t h[16]
     }
 }
 
+// Q4_K sub-block J (0..7) of the super-block at sbk (16-byte aligned) as 16
+// words of exact f16 pairs sc_J q (at most 63 x 15 = 945): its codes are
+// nibble J % 2 of bytes 16 + 32 (J / 2) .. + 31
+template <int J>
+__device__ __forceinline__ void tcx_conv_q4_k(const uint8_t* sbk, uint32_t h[16]) {
+    const uint4 hd = *reinterpret_cast<const uint4*>(sbk);
+    const float sc = (float)q4k_sc(hd.y, hd.w, J);
+    const __half2 sc2 = __half2half2(__float2half_rn(sc));  // exact
+    const __half2 k1024 = __half2half2(__ushort_as_half(0x6400));
+    const uint4 q0 = *reinterpret_cast<const uint4*>(sbk + 16 + 32 * (J >> 1));
+    const uint4 q1 = *reinterpret_cast<const uint4*>(sbk + 32 + 32 * (J >> 1));
+    const uint32_t qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t nb = (qw[i] >> (4 * (J & 1))) & 0x0F0F0F0Fu;  // values 4i..4i+3
+        uint32_t a = __byte_perm(nb, 0x64646464u, 0x5140u), b = __byte_perm(nb, 0x64646464u, 0x5342u);  // 1024 + q
+        const __half2 ha = __hmul2(__hsub2(*reinterpret_cast<__half2*>(&a), k1024), sc2);
+        const __half2 hb = __hmul2(__hsub2(*reinterpret_cast<__half2*>(&b), k1024), sc2);
+        h[2 * i] = *reinterpret_cast<const uint32_t*>(&ha);
+        h[2 * i + 1] = *reinterpret_cast<const uint32_t*>(&hb);
+    }
+}
+
 // f(d) of Q8_0 block j of the raw row at `row` (2-byte aligned)
 __device__ __forceinline__ float tcx_block_scale(const uint8_t* row, int j) {
     return h2f(*reinterpret_cast<const uint16_t*>(row + 34 * j));
 }
 
-template <int WT>  // T_Q8_0
+template <int WT>  // T_Q8_0 or T_Q4_K
 __global__ void __launch_bounds__(kTxThreads, 1)
     qmm_tcx_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUtensorMap ta,
-                   const __grid_constant__ CUtensorMap ts, const TcxParams p) {
+                   const __grid_constant__ CUtensorMap ts, const __grid_constant__ CUtensorMap tb, const TcxParams p) {
+    using R = TxRaw<WT>;
     extern __shared__ __align__(1024) uint8_t smraw[];
     uint8_t* sm = smraw + ((1024 - (smem_u32(smraw) & 1023)) & 1023);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + p.off_bar);
     uint64_t* full = bars;                       // [kTxS] activation codes landed and weight codes converted
     uint64_t* empty = full + kTxS;               // [kTxS] stage consumed by the MMAs (commit)
-    uint64_t* r_full = empty + kTxS;             // [kTxRawMax] raw weight rows and scales landed (TMA)
+    uint64_t* r_full = empty + kTxS;             // [kTxRawMax] raw stage landed (TMA)
     uint64_t* r_empty = r_full + kTxRawMax;      // [kTxRawMax] raw stage converted and folded
-    uint64_t* acc_full = r_empty + kTxRawMax;    // [kTxAcc] block sums complete (commit)
-    uint64_t* acc_empty = acc_full + kTxAcc;     // [kTxAcc] block sums drained (epilogue)
-    static_assert((2 * kTxS + 2 * kTxRawMax + 2 * kTxAcc) * 8 <= 448, "mbarriers overlap the TMEM slot");
+    uint64_t* min_ready = r_empty + kTxRawMax;   // [kTxRawMax] Q4_K: the min term's weight operand written
+    uint64_t* acc_full = min_ready + kTxRawMax;  // [kTxAcc] accumulator complete (commit)
+    uint64_t* acc_empty = acc_full + kTxAcc;     // [kTxAcc] accumulator drained (epilogue)
+    static_assert((2 * kTxS + 3 * kTxRawMax + 2 * kTxAcc) * 8 <= 448, "mbarriers overlap the TMEM slot");
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + p.off_bar + 448);
     volatile int* flags = reinterpret_cast<volatile int*>(sm + p.off_bar + 480);  // [0] abort
     if (tid == 0) {
@@ -131,6 +179,7 @@ __global__ void __launch_bounds__(kTxThreads, 1)
         for (int i = 0; i < kTxRawMax; ++i) {
             mbar_init(smem_u32(&r_full[i]), 1);
             mbar_init(smem_u32(&r_empty[i]), kTxConvWarps + kTxEpiWarps);
+            mbar_init(smem_u32(&min_ready[i]), kTxConvWarps);
         }
         for (int i = 0; i < kTxAcc; ++i) {
             mbar_init(smem_u32(&acc_full[i]), 1);
@@ -153,8 +202,7 @@ __global__ void __launch_bounds__(kTxThreads, 1)
 
     auto wstage = [&](int s) { return sm + s * kTxStage; };               // A: weight codes
     auto xstage = [&](int s) { return sm + s * kTxStage + kTxW * 64; };   // B: activation codes
-    auto raw = [&](int s) { return sm + p.off_raw + s * kTxRawSlot; };
-    const int nb = p.nrs * 8;  // blocks per unit
+    auto raw = [&](int s) { return sm + p.off_raw + s * R::slot; };
     // unit u: weight tile u / mtiles (rows n0..n0+127), activation tile u % mtiles (rows m0..m0+127)
 
     if (warp == 0) {
@@ -174,9 +222,15 @@ __global__ void __launch_bounds__(kTxThreads, 1)
                         if (ri >= p.nraw) ok = mbar_wait(smem_u32(&r_empty[rs]), (uint32_t)(((ri / p.nraw) - 1) & 1), flags, p.err);
                         if (!ok) break;
                         const int in0 = (iu / p.mtiles) * kTxW, im0 = (iu % p.mtiles) * kTxX;
-                        mbar_arrive_tx(smem_u32(&r_full[rs]), (uint32_t)(kTxW * kTxRaw + 8 * kTxX * 4));
-                        tma_2d(smem_u32(raw(rs)), &tw, ir * (kTxRaw / 2), in0, smem_u32(&r_full[rs]));
-                        tma_2d(smem_u32(raw(rs) + kTxScaleOff), &ts, im0, 8 * ir, smem_u32(&r_full[rs]));
+                        const uint32_t fb = smem_u32(&r_full[rs]);
+                        mbar_arrive_tx(fb, (uint32_t)R::tx);
+                        tma_2d(smem_u32(raw(rs)), &tw, ir * (R::row / 2), in0, fb);
+                        if (WT == T_Q8_0) {
+                            tma_2d(smem_u32(raw(rs) + R::scales), &ts, im0, 8 * ir, fb);
+                        } else {
+                            tma_2d(smem_u32(raw(rs) + R::scales), &ts, im0, ir, fb);
+                            tma_2d(smem_u32(raw(rs) + R::bsum), &tb, 16 * ir, im0, fb);
+                        }
                         ++ri;
                         if (++ir >= p.nrs) ir = 0, iu += gridDim.x;
                     }
@@ -199,29 +253,53 @@ __global__ void __launch_bounds__(kTxThreads, 1)
         // ------------------------------ MMA issuer ------------------------------
         if (lane == 0) {
             const uint32_t idesc = tc_idesc(kTxX);
-            long long g = 0;
+            long long g = 0, du = 0, rg = 0;  // blocks; drain units; raw stages
             bool ok = true;
             uint32_t ready = 0;  // the next stage's barrier, tested ahead
+            auto acc_take = [&](long long d) {  // accumulator d % kTxAcc, once the epilogue drained its last use
+                if (d >= kTxAcc) ok = mbar_wait(smem_u32(&acc_empty[d % kTxAcc]), (uint32_t)(((d / kTxAcc) - 1) & 1), flags, p.err);
+                return (uint32_t)((d % kTxAcc) * kTxX);
+            };
             for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
-                for (int b = 0; b < nb && ok; ++b, ++g) {
-                    const int s = (int)(g % kTxS), ab = (int)(g % kTxAcc);
-                    if (g >= kTxAcc) ok = mbar_wait(smem_u32(&acc_empty[ab]), (uint32_t)(((g / kTxAcc) - 1) & 1), flags, p.err);
-                    if (!ok) break;
-                    const uint32_t nxt = mbar_test(smem_u32(&full[(g + 1) % kTxS]), (uint32_t)(((g + 1) / kTxS) & 1));
-                    if (!ready) ok = mbar_wait(smem_u32(&full[s]), (uint32_t)((g / kTxS) & 1), flags, p.err);
-                    if (!ok) break;
-                    tc_fence_after();
-                    const uint32_t wa = smem_u32(wstage(s)), xb = smem_u32(xstage(s));
-                    const uint32_t dt = tmem + (uint32_t)(ab * kTxX);
+                for (int r = 0; r < p.nrs && ok; ++r, ++rg) {
+                    uint32_t dcol = 0;
+                    if (WT == T_Q4_K) dcol = acc_take(du);  // S_sc of the super-block
+                    for (int j = 0; j < 8 && ok; ++j, ++g) {
+                        const int s = (int)(g % kTxS);
+                        if (WT == T_Q8_0) dcol = acc_take(du + j);
+                        if (!ok) break;
+                        const uint32_t nxt = mbar_test(smem_u32(&full[(g + 1) % kTxS]), (uint32_t)(((g + 1) / kTxS) & 1));
+                        if (!ready) ok = mbar_wait(smem_u32(&full[s]), (uint32_t)((g / kTxS) & 1), flags, p.err);
+                        if (!ok) break;
+                        tc_fence_after();
+                        const uint32_t wa = smem_u32(wstage(s)), xb = smem_u32(xstage(s));
 #pragma unroll
-                    for (int kk = 0; kk < 2; ++kk) tcx_mma(dt, tc_sdesc(wa + 32 * kk), tc_sdesc(xb + 32 * kk), idesc, kk);
-                    tc_commit(smem_u32(&empty[s]));
-                    tc_commit(smem_u32(&acc_full[ab]));
-                    ready = nxt;
+                        for (int kk = 0; kk < 2; ++kk)
+                            tcx_mma(tmem + dcol, tc_sdesc(wa + 32 * kk), tc_sdesc(xb + 32 * kk), idesc,
+                                    WT == T_Q8_0 ? (uint32_t)kk : (uint32_t)(j | kk));
+                        tc_commit(smem_u32(&empty[s]));
+                        if (WT == T_Q8_0) tc_commit(smem_u32(&acc_full[(du + j) % kTxAcc]));
+                        ready = nxt;
+                    }
+                    if (!ok) break;
+                    if (WT == T_Q4_K) {
+                        tc_commit(smem_u32(&acc_full[du % kTxAcc]));
+                        // S_m = sum_j m_j bsum_j: one K 16 MMA over the 16 sums of 16 codes
+                        const uint32_t mcol = acc_take(du + 1);
+                        const int rs = (int)(rg % p.nraw);
+                        if (ok) ok = mbar_wait(smem_u32(&min_ready[rs]), (uint32_t)((rg / p.nraw) & 1), flags, p.err);
+                        if (!ok) break;
+                        tc_fence_after();
+                        tcx_mma(tmem + mcol, tcx_sdesc32(smem_u32(raw(rs) + R::amin)), tcx_sdesc32(smem_u32(raw(rs) + R::bsum)),
+                                idesc, 0u);
+                        tc_commit(smem_u32(&acc_full[(du + 1) % kTxAcc]));
+                    }
+                    du += R::drains;
                 }
             }
             // the last commits must land before TMEM is released
             if (g > 0) mbar_drain(smem_u32(&empty[(g - 1) % kTxS]), (uint32_t)(((g - 1) / kTxS) & 1), flags, p.err);
+            if (du > 0) mbar_drain(smem_u32(&acc_full[(du - 1) % kTxAcc]), (uint32_t)(((du - 1) / kTxAcc) & 1), flags, p.err);
         }
     } else if (warp < 2 + kTxEpiWarps) {
         // ------------------------------ epilogue ------------------------------
@@ -230,8 +308,17 @@ __global__ void __launch_bounds__(kTxThreads, 1)
         const int cq = ew >> 2;   // accumulator columns 32cq..32cq+31: activation rows of the tile
         const uint32_t tq = (uint32_t)(32 * q) << 16;
         const int nl = 32 * q + lane;  // this thread's weight row in the tile
-        long long g = 0, rg = 0;
+        long long du = 0, rg = 0;
         bool ok = true;
+        auto acc_wait = [&](long long d) {
+            ok = mbar_wait(smem_u32(&acc_full[d % kTxAcc]), (uint32_t)((d / kTxAcc) & 1), flags, p.err);
+            return tmem + tq + (uint32_t)((d % kTxAcc) * kTxX + 32 * cq);
+        };
+        auto acc_release = [&](long long d) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&acc_empty[d % kTxAcc]));
+        };
         for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
             const int m0 = (u % p.mtiles) * kTxX, n0 = (u / p.mtiles) * kTxW;
             unsigned long long acc[16];  // running sums of activation rows 32cq + 2i, 2i + 1
@@ -239,33 +326,64 @@ __global__ void __launch_bounds__(kTxThreads, 1)
             for (int i = 0; i < 16; ++i) acc[i] = 0ull;
             for (int r = 0; r < p.nrs && ok; ++r, ++rg) {
                 const int rs = (int)(rg % p.nraw);
-                const uint8_t* wrow = raw(rs) + nl * kTxRaw;
-                const float* asc = reinterpret_cast<const float*>(raw(rs) + kTxScaleOff) + 32 * cq;
-                for (int j = 0; j < 8; ++j, ++g) {
-                    const int ab = (int)(g % kTxAcc);
-                    if (!(ok = mbar_wait(smem_u32(&acc_full[ab]), (uint32_t)((g / kTxAcc) & 1), flags, p.err))) break;
+                const uint8_t* wrow = raw(rs) + nl * R::row;
+                const float* asc = reinterpret_cast<const float*>(raw(rs) + R::scales) + 32 * cq;
+                if (WT == T_Q8_0) {
+                    for (int j = 0; j < 8; ++j, ++du) {
+                        const uint32_t acol = acc_wait(du);
+                        if (!ok) break;
+                        tc_fence_after();
+                        __syncwarp();
+                        uint32_t v0[16], v1[16];
+                        tc_ld16(acol, v0);
+                        tc_ld16(acol + 16, v1);
+                        tc_wait_ld();
+                        acc_release(du);
+                        // fold: y += isum f(d_w) f(d_a)
+                        const float dw = tcx_block_scale(wrow, j);
+                        const unsigned long long dw2 = f2pack(dw, dw);
+                        const float* aj = asc + j * kTxX;
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) {
+                            const float4 a4 = *reinterpret_cast<const float4*>(aj + 4 * c);
+                            const uint32_t* v = c < 4 ? v0 + 4 * c : v1 + 4 * (c - 4);
+                            const unsigned long long s01 = mul2(f2pack(a4.x, a4.y), dw2), s23 = mul2(f2pack(a4.z, a4.w), dw2);
+                            acc[2 * c] = fma2(f2pack(__uint_as_float(v[0]), __uint_as_float(v[1])), s01, acc[2 * c]);
+                            acc[2 * c + 1] = fma2(f2pack(__uint_as_float(v[2]), __uint_as_float(v[3])), s23, acc[2 * c + 1]);
+                        }
+                    }
+                } else {
+                    // y += d_a (f(d) S_sc - f(dmin) S_m): S_sc and S_m exact integers in f32
+                    const uint32_t ca = acc_wait(du);
+                    const uint32_t cm = ok ? acc_wait(du + 1) : 0u;
+                    if (!ok) break;
                     tc_fence_after();
                     __syncwarp();
-                    const uint32_t acol = tmem + tq + (uint32_t)(ab * kTxX + 32 * cq);
-                    uint32_t v0[16], v1[16];
-                    tc_ld16(acol, v0);
-                    tc_ld16(acol + 16, v1);
-                    tc_wait_ld();
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(smem_u32(&acc_empty[ab]));
-                    // fold: y += isum f(d_w) f(d_a)
-                    const float dw = tcx_block_scale(wrow, j);
-                    const unsigned long long dw2 = f2pack(dw, dw);
-                    const float* aj = asc + j * kTxX;
+                    const uint32_t dd = *reinterpret_cast<const uint32_t*>(wrow);  // f16 d, f16 dmin
+                    const unsigned long long fd2 = f2pack(h2f(dd), h2f(dd)), fm2 = f2pack(-h2f(dd >> 16), -h2f(dd >> 16));
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        const float4 a4 = *reinterpret_cast<const float4*>(aj + 4 * c);
-                        const uint32_t* v = c < 4 ? v0 + 4 * c : v1 + 4 * (c - 4);
-                        const unsigned long long s01 = mul2(f2pack(a4.x, a4.y), dw2), s23 = mul2(f2pack(a4.z, a4.w), dw2);
-                        acc[2 * c] = fma2(f2pack(__uint_as_float(v[0]), __uint_as_float(v[1])), s01, acc[2 * c]);
-                        acc[2 * c + 1] = fma2(f2pack(__uint_as_float(v[2]), __uint_as_float(v[3])), s23, acc[2 * c + 1]);
+                    for (int h = 0; h < 2; ++h) {
+                        uint32_t vs[16], vm[16];
+                        tc_ld16(ca + 16 * h, vs);
+                        tc_ld16(cm + 16 * h, vm);
+                        tc_wait_ld();
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            const float4 a4 = *reinterpret_cast<const float4*>(asc + 16 * h + 4 * c);
+#pragma unroll
+                            for (int e = 0; e < 2; ++e) {
+                                const int i = 4 * c + 2 * e;
+                                const unsigned long long t =
+                                    fma2(f2pack(__uint_as_float(vs[i]), __uint_as_float(vs[i + 1])), fd2,
+                                         mul2(f2pack(__uint_as_float(vm[i]), __uint_as_float(vm[i + 1])), fm2));
+                                const unsigned long long a2 = e ? f2pack(a4.z, a4.w) : f2pack(a4.x, a4.y);
+                                acc[8 * h + 2 * c + e] = fma2(t, a2, acc[8 * h + 2 * c + e]);
+                            }
+                        }
                     }
+                    acc_release(du);
+                    acc_release(du + 1);
+                    du += 2;
                 }
                 if (!ok) break;
                 __syncwarp();
@@ -293,20 +411,50 @@ __global__ void __launch_bounds__(kTxThreads, 1)
             for (int rr = 0; rr < p.nrs && ok; ++rr, ++rg) {
                 const int rs = (int)(rg % p.nraw);
                 if (!(ok = mbar_wait(smem_u32(&r_full[rs]), (uint32_t)((rg / p.nraw) & 1), flags, p.err))) break;
-                const uint8_t* wrow = raw(rs) + r * kTxRaw;
+                const uint8_t* wrow = raw(rs) + r * R::row;
+                if (WT == T_Q4_K) {
+                    // the min term's weight operand: m_j twice each, 16 f16 = two 16-byte
+                    // chunks in the 32-byte swizzled K-major layout
+                    const uint4 hd = *reinterpret_cast<const uint4*>(wrow);
+                    uint32_t mw[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const __half mh = __float2half_rn((float)q4k_mn(hd.z, hd.w, j));  // exact
+                        const __half2 m2 = __halves2half2(mh, mh);
+                        mw[j] = *reinterpret_cast<const uint32_t*>(&m2);
+                    }
+                    uint8_t* am = raw(rs) + R::amin + (r >> 3) * 256 + (r & 7) * 32;
+                    const int s32 = (r >> 2) & 1;
+                    *reinterpret_cast<uint4*>(am + ((0 ^ s32) << 4)) = make_uint4(mw[0], mw[1], mw[2], mw[3]);
+                    *reinterpret_cast<uint4*>(am + ((1 ^ s32) << 4)) = make_uint4(mw[4], mw[5], mw[6], mw[7]);
+                    fence_proxy_async();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&min_ready[rs]));
+                }
 #pragma unroll
                 for (int j = 0; j < 8; ++j, ++g) {
                     const int s = (int)(g % kTxS);
                     if (g >= kTxS && !(ok = mbar_wait(smem_u32(&empty[s]), (uint32_t)(((g / kTxS) - 1) & 1), flags, p.err))) break;
                     uint32_t h[16];
-                    if (j == 0) tcx_conv_q8_0<0>(wrow, h);
-                    else if (j == 1) tcx_conv_q8_0<1>(wrow, h);
-                    else if (j == 2) tcx_conv_q8_0<2>(wrow, h);
-                    else if (j == 3) tcx_conv_q8_0<3>(wrow, h);
-                    else if (j == 4) tcx_conv_q8_0<4>(wrow, h);
-                    else if (j == 5) tcx_conv_q8_0<5>(wrow, h);
-                    else if (j == 6) tcx_conv_q8_0<6>(wrow, h);
-                    else tcx_conv_q8_0<7>(wrow, h);
+                    if (WT == T_Q8_0) {
+                        if (j == 0) tcx_conv_q8_0<0>(wrow, h);
+                        else if (j == 1) tcx_conv_q8_0<1>(wrow, h);
+                        else if (j == 2) tcx_conv_q8_0<2>(wrow, h);
+                        else if (j == 3) tcx_conv_q8_0<3>(wrow, h);
+                        else if (j == 4) tcx_conv_q8_0<4>(wrow, h);
+                        else if (j == 5) tcx_conv_q8_0<5>(wrow, h);
+                        else if (j == 6) tcx_conv_q8_0<6>(wrow, h);
+                        else tcx_conv_q8_0<7>(wrow, h);
+                    } else {
+                        if (j == 0) tcx_conv_q4_k<0>(wrow, h);
+                        else if (j == 1) tcx_conv_q4_k<1>(wrow, h);
+                        else if (j == 2) tcx_conv_q4_k<2>(wrow, h);
+                        else if (j == 3) tcx_conv_q4_k<3>(wrow, h);
+                        else if (j == 4) tcx_conv_q4_k<4>(wrow, h);
+                        else if (j == 5) tcx_conv_q4_k<5>(wrow, h);
+                        else if (j == 6) tcx_conv_q4_k<6>(wrow, h);
+                        else tcx_conv_q4_k<7>(wrow, h);
+                    }
                     uint8_t* a = wstage(s) + rbase;
 #pragma unroll
                     for (int c = 0; c < 4; ++c)
@@ -329,27 +477,57 @@ __global__ void __launch_bounds__(kTxThreads, 1)
     }
 }
 
-// The activation operand, written once per call: one thread per (row m,
-// 32-block b) quantizes the block to Q8_0 and writes its codes as f16 to
+// The activation operand, written once per call.  Q8_0: one thread per
+// (row m, 32-block b) quantizes the block to Q8_0, writes its codes as f16 to
 // codes[m][K] and the f16-rounded scale f(d_a) block-major to scales[b][mp].
-template <int WT>  // T_Q8_0
+// Q4_K: one warp per (row m, super-block b), lane l taking values 8l..8l+7,
+// quantizes it to Q8K (f32 d = amax / 127 over the 256 values), writes the
+// codes as f16, d to scales[b][mp] and the 16 sums of 16 codes (at most
+// 2032 in magnitude, exact in f16) to bsums[m][K / 16].
+template <int WT>
 __global__ void tcx_act_kernel(const float* __restrict__ x, int M, int K, int mp, __half* __restrict__ codes,
-                               float* __restrict__ scales) {
+                               float* __restrict__ scales, __half* __restrict__ bsums) {
     grid_dep_launch();
-    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    const int nb = K / 32;
-    if (i >= (long long)M * nb) return;
-    const int m = (int)(i / nb), b = (int)(i - (long long)m * nb);
-    uint32_t c[8];
-    float d;
-    quant_q8_0_32(x + (long long)m * K + 32 * b, c, d);
-    uint32_t h[16];
+    if (WT == T_Q8_0) {
+        const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+        const int nb = K / 32;
+        if (i >= (long long)M * nb) return;
+        const int m = (int)(i / nb), b = (int)(i - (long long)m * nb);
+        uint32_t c[8];
+        float d;
+        quant_q8_0_32(x + (long long)m * K + 32 * b, c, d);
+        uint32_t h[16];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) tcx_codes(c[k], h[2 * k], h[2 * k + 1]);
-    uint4* o = reinterpret_cast<uint4*>(codes + (long long)m * K + 32 * b);
+        for (int k = 0; k < 8; ++k) tcx_codes(c[k], h[2 * k], h[2 * k + 1]);
+        uint4* o = reinterpret_cast<uint4*>(codes + (long long)m * K + 32 * b);
 #pragma unroll
-    for (int k = 0; k < 4; ++k) o[k] = make_uint4(h[4 * k], h[4 * k + 1], h[4 * k + 2], h[4 * k + 3]);
-    scales[(long long)b * mp + m] = h2f(f2h(d));
+        for (int k = 0; k < 4; ++k) o[k] = make_uint4(h[4 * k], h[4 * k + 1], h[4 * k + 2], h[4 * k + 3]);
+        scales[(long long)b * mp + m] = h2f(f2h(d));
+    } else {
+        const long long w = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+        const int lane = threadIdx.x & 31;
+        const int nsb = K / 256;
+        if (w >= (long long)M * nsb) return;  // whole warps leave together
+        const int m = (int)(w / nsb), b = (int)(w - (long long)m * nsb);
+        const float4* src = reinterpret_cast<const float4*>(x + (long long)m * K + 256 * b + 8 * lane);
+        const float4 v0 = __ldg(src), v1 = __ldg(src + 1);
+        float amax = fmaxf(fmaxf(fmaxf(fabsf(v0.x), fabsf(v0.y)), fmaxf(fabsf(v0.z), fabsf(v0.w))),
+                           fmaxf(fmaxf(fabsf(v1.x), fabsf(v1.y)), fmaxf(fabsf(v1.z), fabsf(v1.w))));
+#pragma unroll
+        for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        float d, id;
+        q8_scale(amax, d, id);
+        const uint32_t w0 = pack4(q8_code(v0.x, id), q8_code(v0.y, id), q8_code(v0.z, id), q8_code(v0.w, id));
+        const uint32_t w1 = pack4(q8_code(v1.x, id), q8_code(v1.y, id), q8_code(v1.z, id), q8_code(v1.w, id));
+        uint32_t h[4];
+        tcx_codes(w0, h[0], h[1]);
+        tcx_codes(w1, h[2], h[3]);
+        *reinterpret_cast<uint4*>(codes + (long long)m * K + 256 * b + 8 * lane) = make_uint4(h[0], h[1], h[2], h[3]);
+        const int s8 = bsum4(w0) + bsum4(w1);
+        const int s16 = s8 + __shfl_xor_sync(0xffffffffu, s8, 1);  // lanes 2i, 2i + 1: codes 16i..16i+15
+        if ((lane & 1) == 0) bsums[(long long)m * (K / 16) + 16 * b + (lane >> 1)] = __float2half_rn((float)s16);
+        if (lane == 0) scales[(long long)b * mp + m] = d;
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -360,11 +538,14 @@ struct TcxPlan {
     int grid;
     size_t smem;
     int mp;  // activation scale rows: M rounded up to 4 (16-byte rows for the tensor map)
-    size_t ws_codes, ws_scales, workspace;
+    size_t ws_codes, ws_scales, ws_bsums, workspace;
 };
 
+inline int tcx_raw_slot(int wt) { return wt == T_Q8_0 ? TxRaw<T_Q8_0>::slot : TxRaw<T_Q4_K>::slot; }
+
 inline bool plan_tcx(int wt, long long M, long long N, long long K, int sm_count, int smem_max, TcxPlan& out) {
-    if (wt != T_Q8_0 || K % 256 != 0 || M < 17 || K > (1 << 26) || M > (1 << 24) || N > (1 << 24)) return false;
+    if ((wt != T_Q8_0 && wt != T_Q4_K) || K % 256 != 0 || M < 17 || K > (1 << 26) || M > (1 << 24) || N > (1 << 24))
+        return false;
     TcxPlan pl{};
     TcxParams& p = pl.p;
     p.M = (int)M;
@@ -376,17 +557,19 @@ inline bool plan_tcx(int wt, long long M, long long N, long long K, int sm_count
     p.nrs = (int)(K / 256);
     p.off_raw = kTxS * kTxStage;
     const int fixed = 512 + 1024;  // barriers, TMEM slot, flags; alignment slack
-    p.nraw = (smem_max - p.off_raw - fixed) / kTxRawSlot;
+    p.nraw = (smem_max - p.off_raw - fixed) / tcx_raw_slot(wt);
     if (p.nraw > kTxRawMax) p.nraw = kTxRawMax;
     if (p.nraw < 3) return false;  // the epilogue holds a raw stage while the converters fill the next
-    p.off_bar = p.off_raw + p.nraw * kTxRawSlot;
+    p.off_bar = p.off_raw + p.nraw * tcx_raw_slot(wt);
     pl.smem = (size_t)p.off_bar + fixed;
     pl.grid = p.units < sm_count ? p.units : sm_count;
     pl.mp = (int)((M + 3) / 4 * 4);
     auto r256 = [](size_t v) { return (v + 255) / 256 * 256; };
     pl.ws_codes = 0;
     pl.ws_scales = r256((size_t)M * K * 2);
-    pl.workspace = pl.ws_scales + r256((size_t)(K / 32) * pl.mp * 4);
+    const size_t per = wt == T_Q8_0 ? 32 : 256;  // values per activation scale
+    pl.ws_bsums = pl.ws_scales + r256((size_t)(K / per) * pl.mp * 4);
+    pl.workspace = pl.ws_bsums + (wt == T_Q4_K ? r256((size_t)M * (K / 16) * 2) : 0);
     out = pl;
     return true;
 }

@@ -428,7 +428,8 @@ def test_launch_counts(qmm):
     assert qmm.matmul_launches("q8_0", "f32_act", 8, 28672, 8192) == 3    # K split: reduction after
     assert qmm.matmul_launches("q8_0", "int8_act", 256, 4096, 4096) == 2  # exact prefill: activation codes + GEMM
     assert qmm.matmul_launches("q8_0", "f32_act", 256, 4096, 4096) == 2   # tcgen05: operand pieces + GEMM
-    assert qmm.matmul_launches("q4_k", "int8_act", 256, 4096, 4096) == 1  # exact block sums: the streaming kernel
+    assert qmm.matmul_launches("q4_k", "int8_act", 256, 4096, 4096) == 2  # exact tcgen05: activation codes + GEMM
+    assert qmm.matmul_launches("q6_k", "int8_act", 256, 4096, 4096) == 1  # exact block sums: the streaming kernel
     assert qmm.matmul_launches("q8_0", "int8_act", 1, 100, 100) == 0      # K not a multiple of 32
     assert qmm.matmul_launches("q5_0", "int8_act", 1, 576, 576) == 1      # Q4_0 / Q5_0 decode: the MMA kernel
     assert qmm.matmul_launches("q4_0", "f32_act", 8, 28672, 8192) == 3    # large: preparing kernel, K split
@@ -495,7 +496,7 @@ def test_chained_prefill_calls_wait_for_the_previous_output(qmm, orc, wtype, mod
     (int8_act)."""
     launches = run_chain(qmm, orc, wtype, mode, M, PREFILL_CHAIN_SHAPES)
     # operand preparation + GEMM, except the single-launch streaming kernel (Q4_K int8_act)
-    assert min(launches) == (1 if (wtype, mode) == ("q4_k", "int8_act") else 2)
+    assert min(launches) == 2
 
 
 def test_error_statuses_on_device(qmm, orc):
