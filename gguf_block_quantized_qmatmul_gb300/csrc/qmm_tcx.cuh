@@ -39,7 +39,7 @@ namespace qmm {
 
 constexpr int kTxW = 128;         // weight rows per tile (MMA M)
 constexpr int kTxX = 128;         // activation rows per tile (MMA N)
-constexpr int kTxS = 4;           // block stages: weight codes + activation codes in shared memory
+constexpr int kTxSMax = 8;        // block stages (weight codes + activation codes in shared memory), at most
 constexpr int kTxAcc = 4;         // TMEM accumulators of kTxX columns
 constexpr int kTxTmemCols = kTxAcc * kTxX;
 constexpr int kTxRawMax = 6;
@@ -65,6 +65,9 @@ struct TxRaw {
     static constexpr int tx = WT == T_Q8_0 ? kTxW * row + 8 * kTxX * 4 : kTxW * row + kTxX * 4 + kTxX * 32;
     // accumulators (drain units) per raw stage: Q8_0 one per block; Q4_K S_sc and S_m
     static constexpr int drains = WT == T_Q8_0 ? 8 : 2;
+    // block stages: Q4_K's smaller raw slots leave room for eight, which its
+    // lighter fold needs to keep the activation boxes' L2 latency covered
+    static constexpr int stages = WT == T_Q8_0 ? 4 : 8;
 };
 static_assert(TxRaw<T_Q8_0>::slot % 1024 == 0 && TxRaw<T_Q4_K>::slot % 1024 == 0, "1 KB aligned raw slots");
 
@@ -131,8 +134,8 @@ template <int J>
 __device__ __forceinline__ void tcx_conv_q4_k(const uint8_t* sbk, uint32_t h[16]) {
     const uint4 hd = *reinterpret_cast<const uint4*>(sbk);
     const float sc = (float)q4k_sc(hd.y, hd.w, J);
-    const __half2 sc2 = __half2half2(__float2half_rn(sc));  // exact
-    const __half2 k1024 = __half2half2(__ushort_as_half(0x6400));
+    const __half2 sc2 = __half2half2(__float2half_rn(sc));              // exact
+    const __half2 nsc = __half2half2(__float2half_rn(-1024.0f * sc));  // exact: 1024 times a 6-bit integer
     const uint4 q0 = *reinterpret_cast<const uint4*>(sbk + 16 + 32 * (J >> 1));
     const uint4 q1 = *reinterpret_cast<const uint4*>(sbk + 32 + 32 * (J >> 1));
     const uint32_t qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
@@ -140,8 +143,9 @@ __device__ __forceinline__ void tcx_conv_q4_k(const uint8_t* sbk, uint32_t h[16]
     for (int i = 0; i < 8; ++i) {
         const uint32_t nb = (qw[i] >> (4 * (J & 1))) & 0x0F0F0F0Fu;  // values 4i..4i+3
         uint32_t a = __byte_perm(nb, 0x64646464u, 0x5140u), b = __byte_perm(nb, 0x64646464u, 0x5342u);  // 1024 + q
-        const __half2 ha = __hmul2(__hsub2(*reinterpret_cast<__half2*>(&a), k1024), sc2);
-        const __half2 hb = __hmul2(__hsub2(*reinterpret_cast<__half2*>(&b), k1024), sc2);
+        // (1024 + q) sc - 1024 sc with one rounding: the exact q sc (at most 945)
+        const __half2 ha = __hfma2(*reinterpret_cast<__half2*>(&a), sc2, nsc);
+        const __half2 hb = __hfma2(*reinterpret_cast<__half2*>(&b), sc2, nsc);
         h[2 * i] = *reinterpret_cast<const uint32_t*>(&ha);
         h[2 * i + 1] = *reinterpret_cast<const uint32_t*>(&hb);
     }
@@ -161,6 +165,7 @@ __global__ void __launch_bounds__(kTxThreads, 1)
     uint8_t* sm = smraw + ((1024 - (smem_u32(smraw) & 1023)) & 1023);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + p.off_bar);
+    constexpr int kTxS = R::stages;
     uint64_t* full = bars;                       // [kTxS] activation codes landed and weight codes converted
     uint64_t* empty = full + kTxS;               // [kTxS] stage consumed by the MMAs (commit)
     uint64_t* r_full = empty + kTxS;             // [kTxRawMax] raw stage landed (TMA)
@@ -168,7 +173,7 @@ __global__ void __launch_bounds__(kTxThreads, 1)
     uint64_t* min_ready = r_empty + kTxRawMax;   // [kTxRawMax] Q4_K: the min term's weight operand written
     uint64_t* acc_full = min_ready + kTxRawMax;  // [kTxAcc] accumulator complete (commit)
     uint64_t* acc_empty = acc_full + kTxAcc;     // [kTxAcc] accumulator drained (epilogue)
-    static_assert((2 * kTxS + 3 * kTxRawMax + 2 * kTxAcc) * 8 <= 448, "mbarriers overlap the TMEM slot");
+    static_assert((2 * kTxSMax + 3 * kTxRawMax + 2 * kTxAcc) * 8 <= 448, "mbarriers overlap the TMEM slot");
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + p.off_bar + 448);
     volatile int* flags = reinterpret_cast<volatile int*>(sm + p.off_bar + 480);  // [0] abort
     if (tid == 0) {
@@ -405,7 +410,7 @@ __global__ void __launch_bounds__(kTxThreads, 1)
         const int r = 32 * (warp - 2 - kTxEpiWarps) + lane;  // weight row of the tile
         // this row's four 16-byte chunks in the 64-byte swizzled K-major layout
         const int rbase = (r >> 3) * 512 + (r & 7) * 64, sw = (r >> 1) & 3;
-        long long g = 0, rg = 0;
+        long long rg = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
             for (int rr = 0; rr < p.nrs && ok; ++rr, ++rg) {
@@ -432,7 +437,8 @@ __global__ void __launch_bounds__(kTxThreads, 1)
                     if (lane == 0) mbar_arrive(smem_u32(&min_ready[rs]));
                 }
 #pragma unroll
-                for (int j = 0; j < 8; ++j, ++g) {
+                for (int j = 0; j < 8; ++j) {
+                    const long long g = rg * 8 + j;
                     const int s = (int)(g % kTxS);
                     if (g >= kTxS && !(ok = mbar_wait(smem_u32(&empty[s]), (uint32_t)(((g / kTxS) - 1) & 1), flags, p.err))) break;
                     uint32_t h[16];
@@ -542,6 +548,7 @@ struct TcxPlan {
 };
 
 inline int tcx_raw_slot(int wt) { return wt == T_Q8_0 ? TxRaw<T_Q8_0>::slot : TxRaw<T_Q4_K>::slot; }
+inline int tcx_stages(int wt) { return wt == T_Q8_0 ? TxRaw<T_Q8_0>::stages : TxRaw<T_Q4_K>::stages; }
 
 inline bool plan_tcx(int wt, long long M, long long N, long long K, int sm_count, int smem_max, TcxPlan& out) {
     if ((wt != T_Q8_0 && wt != T_Q4_K) || K % 256 != 0 || M < 17 || K > (1 << 26) || M > (1 << 24) || N > (1 << 24))
@@ -555,7 +562,7 @@ inline bool plan_tcx(int wt, long long M, long long N, long long K, int sm_count
     p.ntiles = (int)((N + kTxW - 1) / kTxW);
     p.units = p.mtiles * p.ntiles;
     p.nrs = (int)(K / 256);
-    p.off_raw = kTxS * kTxStage;
+    p.off_raw = tcx_stages(wt) * kTxStage;
     const int fixed = 512 + 1024;  // barriers, TMEM slot, flags; alignment slack
     p.nraw = (smem_max - p.off_raw - fixed) / tcx_raw_slot(wt);
     if (p.nraw > kTxRawMax) p.nraw = kTxRawMax;
