@@ -485,14 +485,13 @@ WARP_MMA_F16_PEAK = 605.0  # TFLOP/s, legacy warp-level f16 MMA on this GPU (reg
 def prefill_kernel(t: str, mode: str, M: int) -> str:
     """The kernel qmm_matmul runs for a prefill shape with K % 256 = 0 (the
     library's dispatch): the Metal form on the tcgen05 GEMM; the CPU form,
-    whose bound needs exact integer block sums, on the exact tcgen05 GEMM
-    (Q8_0, Q4_K) or the streaming warp-MMA kernel (Q6_K); up to 16 rows, the
-    decode kernel."""
+    whose bound needs exact integer block sums, on the exact tcgen05 GEMM;
+    up to 16 rows, the decode kernel."""
     if M <= 16:
         return "qmm_dmma_kernel"
     if mode == "f32_act":
         return "qmm_tc_kernel"
-    return "qmm_tcx_kernel" if t in ("q8_0", "q4_k") else "qmm_stream_kernel"
+    return "qmm_tcx_kernel"
 
 
 def prefill_section(q, torch, stream, hbm_peak, bf16_peak):

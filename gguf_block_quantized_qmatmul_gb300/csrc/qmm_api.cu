@@ -123,9 +123,9 @@ struct Dispatch {
 void plan_dispatch(int wt, int am, int epi, long long M, long long N, long long K, int sms, int smem, Dispatch& d) {
     d = Dispatch();
     if (wt == T_Q4_0 || wt == T_Q5_0 || wt == T_Q6_K) {
-        // up to 16 rows on 16-row warp-MMA tiles; Metal-form prefill on the tcgen05 GEMM
-        // where K allows (K % 256 = 0); the rest (the CPU form's exact block sums
-        // above 16 rows among it) on the streaming kernel
+        // up to 16 rows on 16-row warp-MMA tiles; prefill on the tcgen05 GEMMs where K
+        // allows (K % 256 = 0: the Metal form, and Q6_K's CPU form with exact sums); the
+        // rest on the streaming kernel
         if (M <= kDmmaMaxM && plan_dmma(wt, am, M, N, K, sms, smem, d.dp, epi == E_Y)) {
             d.kind = KIND_DMMA;
             d.workspace = d.dp.workspace;
@@ -134,6 +134,10 @@ void plan_dispatch(int wt, int am, int epi, long long M, long long N, long long 
             d.kind = KIND_TC;
             d.workspace = d.tp.workspace;
             d.launches = 2;  // operand preparation, GEMM
+        } else if (epi == E_Y && am == A_INT8 && M > kDecodeMaxM && plan_tcx(wt, M, N, K, sms, smem, d.xp)) {
+            d.kind = KIND_TCX;  // Q6_K's CPU-form prefill: exact sums on tcgen05
+            d.workspace = d.xp.workspace;
+            d.launches = 3;  // activation codes, repacked weights, GEMM
         } else if (plan_stream(wt, am, epi, M, N, K, sms, smem, d.sp)) {
             d.kind = KIND_STREAM;
             d.workspace = epi == E_Y ? workspace_for(d.sp) : 0;
@@ -152,10 +156,10 @@ void plan_dispatch(int wt, int am, int epi, long long M, long long N, long long 
         d.kind = KIND_TC;
         d.workspace = d.tp.workspace;
         d.launches = 2;  // operand preparation, GEMM
-    } else if (epi == E_Y && am == A_INT8 && plan_tcx(wt, M, N, K, sms, smem, d.xp)) {  // CPU-form prefill (Q8_0, Q4_K): exact block sums on tcgen05
+    } else if (epi == E_Y && am == A_INT8 && plan_tcx(wt, M, N, K, sms, smem, d.xp)) {  // CPU-form prefill (Q8_0, Q4_K, Q6_K): exact sums on tcgen05
         d.kind = KIND_TCX;
         d.workspace = d.xp.workspace;
-        d.launches = 2;  // activation codes, GEMM
+        d.launches = wt == T_Q6_K ? 3 : 2;  // activation codes, (Q6_K) repacked weights, GEMM
     } else if (plan_stream(wt, am, epi, M, N, K, sms, smem, d.sp)) {
         d.kind = KIND_STREAM;
         d.workspace = epi == E_Y ? workspace_for(d.sp) : 0;

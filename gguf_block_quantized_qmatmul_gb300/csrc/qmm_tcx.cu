@@ -5,7 +5,7 @@
 namespace qmm {
 
 namespace {
-unsigned long long g_tcx_smem_done[2];
+unsigned long long g_tcx_smem_done[3];
 
 template <int WT>
 cudaError_t tcx_go(const TcxPlan& pl, const void* wq, const float* x, void* ws, float* y, int smem_max, cudaStream_t s) {
@@ -15,18 +15,26 @@ cudaError_t tcx_go(const TcxPlan& pl, const void* wq, const float* x, void* ws, 
     __half* codes = reinterpret_cast<__half*>(wsb + pl.ws_codes);
     float* scales = reinterpret_cast<float*>(wsb + pl.ws_scales);
     __half* bsums = reinterpret_cast<__half*>(wsb + pl.ws_bsums);
+    uint8_t* w6 = wsb + pl.ws_w6;  // Q6_K: super-blocks in 240-byte slots
     // 1. the activation operand: f16 codes [M][K], scales block-major, (Q4_K) sums of 16 codes
     const long long items = WT == T_Q8_0 ? (long long)p0.M * (p0.K / 32) : (long long)p0.M * (p0.K / 256) * 32;
     tcx_act_kernel<WT><<<(unsigned)((items + 255) / 256), 256, 0, s>>>(x, p0.M, p0.K, pl.mp, codes, scales, bsums);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    if (WT == T_Q6_K) {
+        tcx_q6_repack_kernel<T_Q6_K><<<(unsigned)(((long long)p0.N * 32 + 255) / 256), 256, 0, s>>>(static_cast<const uint8_t*>(wq),
+                                                                                        p0.N, p0.K, w6);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
     // 2. tensor maps: raw weight rows as uint16 (128 rows x 256 K); activation codes, 32 K x
     //    128 rows, 64-byte swizzle; activation scales; (Q4_K) the sums of 16 codes, 16 x 128
     //    rows, 32-byte swizzle
     CUtensorMap tw, ta, ts, tb;
     const unsigned long long rb = (unsigned long long)p0.K / 256 * R::row;
     const unsigned long long nsc = WT == T_Q8_0 ? p0.K / 32 : p0.K / 256;
-    bool ok = make_map(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT16, wq, rb / 2, p0.N, rb, R::row / 2, kTxW, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+    const void* wsrc = WT == T_Q6_K ? static_cast<const void*>(w6) : wq;
+    bool ok = make_map(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT16, wsrc, rb / 2, p0.N, rb, R::row / 2, kTxW, CU_TENSOR_MAP_SWIZZLE_NONE) &&
               make_map(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, codes, p0.K, p0.M, (unsigned long long)p0.K * 2, 32, kTxX,
                        CU_TENSOR_MAP_SWIZZLE_64B) &&
               make_map(&ts, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, scales, pl.mp, nsc, (unsigned long long)pl.mp * 4, kTxX,
@@ -41,7 +49,7 @@ cudaError_t tcx_go(const TcxPlan& pl, const void* wq, const float* x, void* ws, 
     p.y = y;
     // 3. the GEMM, a programmatic dependent of the preparation
     auto* k = qmm_tcx_kernel<WT>;
-    e = ensure_smem(k, smem_max, g_tcx_smem_done[WT == T_Q8_0 ? 0 : 1]);
+    e = ensure_smem(k, smem_max, g_tcx_smem_done[WT == T_Q8_0 ? 0 : WT == T_Q4_K ? 1 : 2]);
     if (e != cudaSuccess) return e;
     return launch_pdl(k, (unsigned)pl.grid, kTxThreads, pl.smem, s, tw, ta, ts, tb, p);
 }
@@ -49,7 +57,11 @@ cudaError_t tcx_go(const TcxPlan& pl, const void* wq, const float* x, void* ws, 
 
 cudaError_t launch_tcx(int wt, const TcxPlan& pl, const void* wq, const float* x, void* ws, float* y, int smem_max,
                        cudaStream_t s) {
-    return wt == T_Q8_0 ? tcx_go<T_Q8_0>(pl, wq, x, ws, y, smem_max, s) : tcx_go<T_Q4_K>(pl, wq, x, ws, y, smem_max, s);
+    switch (wt) {
+        case T_Q8_0: return tcx_go<T_Q8_0>(pl, wq, x, ws, y, smem_max, s);
+        case T_Q4_K: return tcx_go<T_Q4_K>(pl, wq, x, ws, y, smem_max, s);
+        default: return tcx_go<T_Q6_K>(pl, wq, x, ws, y, smem_max, s);
+    }
 }
 
 }  // namespace qmm

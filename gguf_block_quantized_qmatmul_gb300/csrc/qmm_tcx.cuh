@@ -1,32 +1,46 @@
 // qmm_tcx.cuh -- the CPU form's prefill GEMM (int8_act, M > 16 activation
-// rows) on the 5th-generation tensor cores with exact per-block sums.
+// rows; Q8_0, Q4_K and Q6_K weights) on the 5th-generation tensor cores with
+// exact per-block sums.
 //
 // "同一个 GGUF，CPU 和 Metal 生成的文字不一样" section 出处: the CPU form
-// quantizes every activation row to Q8_0 and multiplies it block by block as
-// an integer dot product,
-//   y = sum_b f(d_w) f(d_a) isum_b,   isum_b = sum over the block's 32 values
-//   of the weight code times the activation code.
-// Its parity bound is taken over the block terms, so every isum_b must be
-// formed exactly.  sm_103a's tcgen05 has no integer kind, but every code
-// (|q| <= 127) is exact in f16 and every sum of at most 32 products of two
-// codes (< 2^19) is exact in the f32 accumulator: an MMA group of one block
-// with a restarted accumulator yields isum_b exactly.  The fold, y += isum_b
-// f(d_w) f(d_a), is then one scale product and one FMA per output element
-// per block, in packed f32x2 arithmetic on the drained accumulator.
+// quantizes every activation row (Q8_0, or Q8K for K-quant weights) and
+// multiplies it block by block as an integer dot product,
+//   Q8_0: y = sum_b f(d_w) f(d_a) isum_b;
+//   Q4_K: y = sum_s d_a (f(d) S_sc - f(dmin) S_m);   Q6_K: y = sum_s d_a f(d) S.
+// Its parity bound is taken over the block (super-block) terms, so every
+// isum_b, S_sc, S_m and S must be formed whole before it is scaled.
+// sm_103a's tcgen05 has no integer kind, but integer codes are exact f16
+// operands and integer partial sums below 2^24 are exact in the f32
+// accumulator, so an MMA group with a restarted accumulator yields them:
+//   Q8_0: one group per 32-value block (isum_b < 2^19);
+//   Q4_K: one group per super-block on codes sc_j q (<= 945): S_sc (past
+//         2^24 only for adversarial blocks, whose rounding stays inside the
+//         bound); S_m as one more K 16 MMA of the m_j against the 16 sums of
+//         16 activation codes;
+//   Q6_K: its int8 group scales times codes reach 4064, not exact in f16, so
+//         each scale is split sc_g = 16 a_g + b_g and the super-block takes
+//         two groups, S_a on a_g q (|.| <= 256) and S_b on b_g q (<= 480),
+//         each exact (< 2^24); S = 16 S_a + S_b.
+// The fold, y += (block sum) x scales, is one scale product and one FMA per
+// output element per block (Q8_0) or per super-block (Q4_K, Q6_K), in packed
+// f32x2 arithmetic on the drained accumulators.
 //
 // One persistent CTA per SM over work units: an output tile of 128 weight
 // rows (MMA M, the TMEM lanes) x 128 activation rows (MMA N), all of K.
 // 22 warps:
-//   producer   TMA: raw weight rows (2-D box of 128 rows x 272 B = 8 Q8_0
-//              blocks) with the 8 blocks' activation scales ([8][128] f32,
-//              prepared block-major) into a raw ring; per block the
+//   producer   TMA: raw weight rows (2-D box of 128 rows x 256 K: 272 B of
+//              Q8_0, 144 B of Q4_K, a 240-byte slot of Q6_K) with that
+//              stretch's activation scales (prepared block-major) and, for
+//              Q4_K, the sums of 16 codes, into a raw ring; per block the
 //              activation codes (128 rows x 32 f16, 64-byte swizzle);
-//   MMA        one thread: per block two tcgen05.mma (K 16) from shared
-//              memory into one of four TMEM accumulators, restarted;
+//   MMA        one thread: per block two (Q6_K: four) tcgen05.mma (K 16)
+//              from shared memory into TMEM accumulators (four of 128
+//              columns in a ring), restarted per block or super-block;
 //   epilogue   16 warps, a TMEM lane quarter (32 weight rows) and 32 of the
-//              128 accumulator columns each: drain the block's sums, fold
-//              them with f(d_w) (read from the raw stage) and f(d_a), keep
-//              the tile's running sums in registers, store y at the end;
+//              128 accumulator columns each: drain the sums, fold them with
+//              the weight scales (read from the raw stage) and the
+//              activation scales, keep the tile's running sums in
+//              registers, store y at the end;
 //   converter  4 warps, one weight row per thread: the block's 32 codes to
 //              exact f16, written to shared memory in the MMA's 64-byte
 //              swizzled K-major layout.
@@ -46,7 +60,6 @@ constexpr int kTxRawMax = 6;
 constexpr int kTxEpiWarps = 16;
 constexpr int kTxConvWarps = 4;
 constexpr int kTxThreads = (2 + kTxEpiWarps + kTxConvWarps) * 32;
-constexpr int kTxStage = 2 * kTxW * 64;  // A (weights) then B (activations): 8 KB each
 
 // A raw stage holds 256 K of the tile's 128 weight rows and what the fold
 // needs of the tile's 128 activation rows:
@@ -54,22 +67,35 @@ constexpr int kTxStage = 2 * kTxW * 64;  // A (weights) then B (activations): 8 
 //   Q4_K: rows of 144 B (1 super-block); d_a, [128] f32; the min term's
 //         activation operand (16 sums of 16 codes per row, f16, 32-byte
 //         swizzle) and its weight operand (m_j twice each, written by the
-//         converters).
+//         converters);
+//   Q6_K: rows of 240 B (1 super-block repacked into a 16-byte aligned slot);
+//         d_a, [128] f32.
+// A block stage holds the block's weight codes (Q6_K: two tiles, a_g q and
+// b_g q, for the group scales split as sc_g = 16 a_g + b_g) and the 128
+// activation rows' codes.
 template <int WT>
 struct TxRaw {
-    static constexpr int row = WT == T_Q8_0 ? 272 : 144;
+    static constexpr int row = WT == T_Q8_0 ? 272 : WT == T_Q4_K ? 144 : 240;
     static constexpr int scales = kTxW * row;                                      // f(d_a)
-    static constexpr int bsum = WT == T_Q8_0 ? 0 : scales + 1024;                  // Q4_K: [128][16] f16
-    static constexpr int amin = WT == T_Q8_0 ? 0 : bsum + kTxX * 32;              // Q4_K: [128][16] f16
-    static constexpr int slot = WT == T_Q8_0 ? (scales + 8 * kTxX * 4 + 1023) / 1024 * 1024 : amin + kTxW * 32;
-    static constexpr int tx = WT == T_Q8_0 ? kTxW * row + 8 * kTxX * 4 : kTxW * row + kTxX * 4 + kTxX * 32;
-    // accumulators (drain units) per raw stage: Q8_0 one per block; Q4_K S_sc and S_m
+    static constexpr int bsum = WT == T_Q4_K ? scales + 1024 : 0;                  // Q4_K: [128][16] f16
+    static constexpr int amin = WT == T_Q4_K ? bsum + kTxX * 32 : 0;              // Q4_K: [128][16] f16
+    static constexpr int slot = WT == T_Q8_0 ? (scales + 8 * kTxX * 4 + 1023) / 1024 * 1024
+                                : WT == T_Q4_K ? amin + kTxW * 32
+                                               : (scales + kTxX * 4 + 1023) / 1024 * 1024;
+    static constexpr int tx = WT == T_Q8_0   ? kTxW * row + 8 * kTxX * 4
+                              : WT == T_Q4_K ? kTxW * row + kTxX * 4 + kTxX * 32
+                                             : kTxW * row + kTxX * 4;
+    // accumulators (drain units) per raw stage: Q8_0 one per block; Q4_K S_sc
+    // and S_m; Q6_K S_a and S_b (S = 16 S_a + S_b)
     static constexpr int drains = WT == T_Q8_0 ? 8 : 2;
     // block stages: Q4_K's smaller raw slots leave room for eight, which its
     // lighter fold needs to keep the activation boxes' L2 latency covered
-    static constexpr int stages = WT == T_Q8_0 ? 4 : 8;
+    static constexpr int stages = WT == T_Q4_K ? 8 : 4;
+    static constexpr int wtiles = WT == T_Q6_K ? 2 : 1;        // weight-code tiles per block stage
+    static constexpr int stage = (wtiles + 1) * kTxW * 64;      // bytes of a block stage
 };
-static_assert(TxRaw<T_Q8_0>::slot % 1024 == 0 && TxRaw<T_Q4_K>::slot % 1024 == 0, "1 KB aligned raw slots");
+static_assert(TxRaw<T_Q8_0>::slot % 1024 == 0 && TxRaw<T_Q4_K>::slot % 1024 == 0 && TxRaw<T_Q6_K>::slot % 1024 == 0,
+              "1 KB aligned raw slots");
 
 struct TcxParams {
     float* y;
@@ -151,12 +177,51 @@ __device__ __forceinline__ void tcx_conv_q4_k(const uint8_t* sbk, uint32_t h[16]
     }
 }
 
+// Q6_K stage J (0..7) of a super-block in its 240-byte slot at sbk (16-byte
+// aligned: ql[128], qh[64], 16 int8 group scales, f16 d): values 32 J + l, l <
+// 32, in groups 2 J (l < 16) and 2 J + 1.  Value 128 H + 32 Q + l (H = J / 4,
+// Q = J % 4) takes its low 4 bits from nibble Q / 2 of ql[64 H + 32 (Q % 2) +
+// l] and its high 2 bits from bits 2 Q, 2 Q + 1 of qh[32 H + l]; the code is
+// the 6 bits less 32.  With sc_g = 16 a_g + b_g (a_g = sc_g >> 4 in [-8, 7],
+// b_g = sc_g & 15), ha holds a_g code (|.| <= 256) and hb b_g code (<= 480),
+// both exact f16: (1024 + u) t - 1056 t rounds once, to the exact (u - 32) t.
+template <int J>
+__device__ __forceinline__ void tcx_conv_q6_k(const uint8_t* sbk, uint32_t ha[16], uint32_t hb[16]) {
+    constexpr int H = J >> 2, Q = J & 3;
+    const uint4 l0 = *reinterpret_cast<const uint4*>(sbk + 64 * H + 32 * (Q & 1));
+    const uint4 l1 = *reinterpret_cast<const uint4*>(sbk + 64 * H + 32 * (Q & 1) + 16);
+    const uint4 h0 = *reinterpret_cast<const uint4*>(sbk + 128 + 32 * H);
+    const uint4 h1 = *reinterpret_cast<const uint4*>(sbk + 128 + 32 * H + 16);
+    const uint32_t scw = *reinterpret_cast<const uint32_t*>(sbk + 192 + 4 * (J >> 1)) >> (16 * (J & 1));  // sc_2J, sc_2J+1
+    const uint32_t ql[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
+    const uint32_t qh[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {  // group 2 J + e: words 4 e .. 4 e + 3
+        const int sc = (int)(int8_t)((scw >> (8 * e)) & 0xFFu);
+        const float a = (float)(sc >> 4), b = (float)(sc & 15);
+        const __half2 a2 = __half2half2(__float2half_rn(a)), na = __half2half2(__float2half_rn(-1056.0f * a));
+        const __half2 b2 = __half2half2(__float2half_rn(b)), nb = __half2half2(__float2half_rn(-1056.0f * b));
+#pragma unroll
+        for (int i = 4 * e; i < 4 * e + 4; ++i) {
+            const uint32_t u = ((ql[i] >> (4 * (Q >> 1))) & 0x0F0F0F0Fu) | (((qh[i] >> (2 * Q)) & 0x03030303u) << 4);
+            uint32_t p = __byte_perm(u, 0x64646464u, 0x5140u), q = __byte_perm(u, 0x64646464u, 0x5342u);  // 1024 + u
+            const __half2 xp = *reinterpret_cast<__half2*>(&p), xq = *reinterpret_cast<__half2*>(&q);
+            const __half2 pa = __hfma2(xp, a2, na), qa = __hfma2(xq, a2, na);
+            const __half2 pb = __hfma2(xp, b2, nb), qb = __hfma2(xq, b2, nb);
+            ha[2 * i] = *reinterpret_cast<const uint32_t*>(&pa);
+            ha[2 * i + 1] = *reinterpret_cast<const uint32_t*>(&qa);
+            hb[2 * i] = *reinterpret_cast<const uint32_t*>(&pb);
+            hb[2 * i + 1] = *reinterpret_cast<const uint32_t*>(&qb);
+        }
+    }
+}
+
 // f(d) of Q8_0 block j of the raw row at `row` (2-byte aligned)
 __device__ __forceinline__ float tcx_block_scale(const uint8_t* row, int j) {
     return h2f(*reinterpret_cast<const uint16_t*>(row + 34 * j));
 }
 
-template <int WT>  // T_Q8_0 or T_Q4_K
+template <int WT>  // T_Q8_0, T_Q4_K or T_Q6_K
 __global__ void __launch_bounds__(kTxThreads, 1)
     qmm_tcx_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUtensorMap ta,
                    const __grid_constant__ CUtensorMap ts, const __grid_constant__ CUtensorMap tb, const TcxParams p) {
@@ -205,8 +270,8 @@ __global__ void __launch_bounds__(kTxThreads, 1)
     const uint32_t tmem = *tslot;
     grid_dep_wait();  // the activation-preparing grid has completed
 
-    auto wstage = [&](int s) { return sm + s * kTxStage; };               // A: weight codes
-    auto xstage = [&](int s) { return sm + s * kTxStage + kTxW * 64; };   // B: activation codes
+    auto wstage = [&](int s) { return sm + s * R::stage; };                           // A: weight codes (Q6_K: a q, then b q)
+    auto xstage = [&](int s) { return sm + s * R::stage + R::wtiles * kTxW * 64; };   // B: activation codes
     auto raw = [&](int s) { return sm + p.off_raw + s * R::slot; };
     // unit u: weight tile u / mtiles (rows n0..n0+127), activation tile u % mtiles (rows m0..m0+127)
 
@@ -234,7 +299,7 @@ __global__ void __launch_bounds__(kTxThreads, 1)
                             tma_2d(smem_u32(raw(rs) + R::scales), &ts, im0, 8 * ir, fb);
                         } else {
                             tma_2d(smem_u32(raw(rs) + R::scales), &ts, im0, ir, fb);
-                            tma_2d(smem_u32(raw(rs) + R::bsum), &tb, 16 * ir, im0, fb);
+                            if (WT == T_Q4_K) tma_2d(smem_u32(raw(rs) + R::bsum), &tb, 16 * ir, im0, fb);
                         }
                         ++ri;
                         if (++ir >= p.nrs) ir = 0, iu += gridDim.x;
@@ -267,8 +332,9 @@ __global__ void __launch_bounds__(kTxThreads, 1)
             };
             for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
                 for (int r = 0; r < p.nrs && ok; ++r, ++rg) {
-                    uint32_t dcol = 0;
-                    if (WT == T_Q4_K) dcol = acc_take(du);  // S_sc of the super-block
+                    uint32_t dcol = 0, dcol2 = 0;
+                    if (WT != T_Q8_0) dcol = acc_take(du);                // S_sc (Q4_K), S_a (Q6_K)
+                    if (WT == T_Q6_K && ok) dcol2 = acc_take(du + 1);    // S_b
                     for (int j = 0; j < 8 && ok; ++j, ++g) {
                         const int s = (int)(g % kTxS);
                         if (WT == T_Q8_0) dcol = acc_take(du + j);
@@ -282,11 +348,21 @@ __global__ void __launch_bounds__(kTxThreads, 1)
                         for (int kk = 0; kk < 2; ++kk)
                             tcx_mma(tmem + dcol, tc_sdesc(wa + 32 * kk), tc_sdesc(xb + 32 * kk), idesc,
                                     WT == T_Q8_0 ? (uint32_t)kk : (uint32_t)(j | kk));
+                        if (WT == T_Q6_K) {
+#pragma unroll
+                            for (int kk = 0; kk < 2; ++kk)
+                                tcx_mma(tmem + dcol2, tc_sdesc(wa + kTxW * 64 + 32 * kk), tc_sdesc(xb + 32 * kk), idesc,
+                                        (uint32_t)(j | kk));
+                        }
                         tc_commit(smem_u32(&empty[s]));
                         if (WT == T_Q8_0) tc_commit(smem_u32(&acc_full[(du + j) % kTxAcc]));
                         ready = nxt;
                     }
                     if (!ok) break;
+                    if (WT == T_Q6_K) {
+                        tc_commit(smem_u32(&acc_full[du % kTxAcc]));
+                        tc_commit(smem_u32(&acc_full[(du + 1) % kTxAcc]));
+                    }
                     if (WT == T_Q4_K) {
                         tc_commit(smem_u32(&acc_full[du % kTxAcc]));
                         // S_m = sum_j m_j bsum_j: one K 16 MMA over the 16 sums of 16 codes
@@ -357,6 +433,38 @@ __global__ void __launch_bounds__(kTxThreads, 1)
                             acc[2 * c + 1] = fma2(f2pack(__uint_as_float(v[2]), __uint_as_float(v[3])), s23, acc[2 * c + 1]);
                         }
                     }
+                } else if (WT == T_Q6_K) {
+                    // y += d_a f(d) S with S = 16 S_a + S_b (S_a, S_b exact integers in f32;
+                    // 16 S_a exact, the sum rounded once, relative to |S|)
+                    const uint32_t ca = acc_wait(du);
+                    const uint32_t cb = ok ? acc_wait(du + 1) : 0u;
+                    if (!ok) break;
+                    tc_fence_after();
+                    __syncwarp();
+                    const float fd = h2f(*reinterpret_cast<const uint16_t*>(wrow + 208));
+                    const unsigned long long fd2 = f2pack(fd, fd), k16 = f2pack(16.0f, 16.0f);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        uint32_t va[16], vb[16];
+                        tc_ld16(ca + 16 * h, va);
+                        tc_ld16(cb + 16 * h, vb);
+                        tc_wait_ld();
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            const float4 a4 = *reinterpret_cast<const float4*>(asc + 16 * h + 4 * c);
+#pragma unroll
+                            for (int e = 0; e < 2; ++e) {
+                                const int i = 4 * c + 2 * e;
+                                const unsigned long long t = fma2(f2pack(__uint_as_float(va[i]), __uint_as_float(va[i + 1])), k16,
+                                                                  f2pack(__uint_as_float(vb[i]), __uint_as_float(vb[i + 1])));
+                                const unsigned long long sc2 = mul2(e ? f2pack(a4.z, a4.w) : f2pack(a4.x, a4.y), fd2);
+                                acc[8 * h + 2 * c + e] = fma2(t, sc2, acc[8 * h + 2 * c + e]);
+                            }
+                        }
+                    }
+                    acc_release(du);
+                    acc_release(du + 1);
+                    du += 2;
                 } else {
                     // y += d_a (f(d) S_sc - f(dmin) S_m): S_sc and S_m exact integers in f32
                     const uint32_t ca = acc_wait(du);
@@ -442,7 +550,21 @@ __global__ void __launch_bounds__(kTxThreads, 1)
                     const int s = (int)(g % kTxS);
                     if (g >= kTxS && !(ok = mbar_wait(smem_u32(&empty[s]), (uint32_t)(((g / kTxS) - 1) & 1), flags, p.err))) break;
                     uint32_t h[16];
-                    if (WT == T_Q8_0) {
+                    if (WT == T_Q6_K) {
+                        uint32_t h2[16];
+                        if (j == 0) tcx_conv_q6_k<0>(wrow, h, h2);
+                        else if (j == 1) tcx_conv_q6_k<1>(wrow, h, h2);
+                        else if (j == 2) tcx_conv_q6_k<2>(wrow, h, h2);
+                        else if (j == 3) tcx_conv_q6_k<3>(wrow, h, h2);
+                        else if (j == 4) tcx_conv_q6_k<4>(wrow, h, h2);
+                        else if (j == 5) tcx_conv_q6_k<5>(wrow, h, h2);
+                        else if (j == 6) tcx_conv_q6_k<6>(wrow, h, h2);
+                        else tcx_conv_q6_k<7>(wrow, h, h2);
+                        uint8_t* a2 = wstage(s) + kTxW * 64 + rbase;
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+                            *reinterpret_cast<uint4*>(a2 + ((c ^ sw) << 4)) = make_uint4(h2[4 * c], h2[4 * c + 1], h2[4 * c + 2], h2[4 * c + 3]);
+                    } else if (WT == T_Q8_0) {
                         if (j == 0) tcx_conv_q8_0<0>(wrow, h);
                         else if (j == 1) tcx_conv_q8_0<1>(wrow, h);
                         else if (j == 2) tcx_conv_q8_0<2>(wrow, h);
@@ -536,6 +658,24 @@ __global__ void tcx_act_kernel(const float* __restrict__ x, int M, int K, int mp
     }
 }
 
+// Q6_K: every 210-byte super-block copied into a 240-byte slot (rows of K / 256
+// slots), 16-byte aligned for the GEMM's tensor map; one warp per weight row,
+// 2-byte words
+template <int WT>  // T_Q6_K
+__global__ void tcx_q6_repack_kernel(const uint8_t* __restrict__ wq, int N, int K, uint8_t* __restrict__ w6) {
+    grid_dep_launch();
+    const long long n = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (n >= N) return;
+    const int nsb = K / 256;
+    const uint16_t* src = reinterpret_cast<const uint16_t*>(wq + n * (long long)nsb * 210);
+    uint16_t* dst = reinterpret_cast<uint16_t*>(w6 + n * (long long)nsb * TxRaw<T_Q6_K>::row);
+    for (int i = lane; i < nsb * 105; i += 32) {
+        const int b = i / 105, hw = i - 105 * b;
+        dst[b * (TxRaw<T_Q6_K>::row / 2) + hw] = __ldg(src + i);
+    }
+}
+
 // ---------------------------------------------------------------------------
 // host-side plan
 // ---------------------------------------------------------------------------
@@ -544,14 +684,22 @@ struct TcxPlan {
     int grid;
     size_t smem;
     int mp;  // activation scale rows: M rounded up to 4 (16-byte rows for the tensor map)
-    size_t ws_codes, ws_scales, ws_bsums, workspace;
+    size_t ws_codes, ws_scales, ws_bsums, ws_w6, workspace;
 };
 
-inline int tcx_raw_slot(int wt) { return wt == T_Q8_0 ? TxRaw<T_Q8_0>::slot : TxRaw<T_Q4_K>::slot; }
-inline int tcx_stages(int wt) { return wt == T_Q8_0 ? TxRaw<T_Q8_0>::stages : TxRaw<T_Q4_K>::stages; }
+inline int tcx_raw_slot(int wt) {
+    return wt == T_Q8_0 ? TxRaw<T_Q8_0>::slot : wt == T_Q4_K ? TxRaw<T_Q4_K>::slot : TxRaw<T_Q6_K>::slot;
+}
+inline int tcx_stages(int wt) {
+    return wt == T_Q8_0 ? TxRaw<T_Q8_0>::stages : wt == T_Q4_K ? TxRaw<T_Q4_K>::stages : TxRaw<T_Q6_K>::stages;
+}
+inline int tcx_stage_bytes(int wt) {
+    return wt == T_Q8_0 ? TxRaw<T_Q8_0>::stage : wt == T_Q4_K ? TxRaw<T_Q4_K>::stage : TxRaw<T_Q6_K>::stage;
+}
 
 inline bool plan_tcx(int wt, long long M, long long N, long long K, int sm_count, int smem_max, TcxPlan& out) {
-    if ((wt != T_Q8_0 && wt != T_Q4_K) || K % 256 != 0 || M < 17 || K > (1 << 26) || M > (1 << 24) || N > (1 << 24))
+    if ((wt != T_Q8_0 && wt != T_Q4_K && wt != T_Q6_K) || K % 256 != 0 || M < 17 || K > (1 << 26) || M > (1 << 24) ||
+        N > (1 << 24))
         return false;
     TcxPlan pl{};
     TcxParams& p = pl.p;
@@ -562,7 +710,7 @@ inline bool plan_tcx(int wt, long long M, long long N, long long K, int sm_count
     p.ntiles = (int)((N + kTxW - 1) / kTxW);
     p.units = p.mtiles * p.ntiles;
     p.nrs = (int)(K / 256);
-    p.off_raw = tcx_stages(wt) * kTxStage;
+    p.off_raw = tcx_stages(wt) * tcx_stage_bytes(wt);
     const int fixed = 512 + 1024;  // barriers, TMEM slot, flags; alignment slack
     p.nraw = (smem_max - p.off_raw - fixed) / tcx_raw_slot(wt);
     if (p.nraw > kTxRawMax) p.nraw = kTxRawMax;
@@ -576,7 +724,8 @@ inline bool plan_tcx(int wt, long long M, long long N, long long K, int sm_count
     pl.ws_scales = r256((size_t)M * K * 2);
     const size_t per = wt == T_Q8_0 ? 32 : 256;  // values per activation scale
     pl.ws_bsums = pl.ws_scales + r256((size_t)(K / per) * pl.mp * 4);
-    pl.workspace = pl.ws_bsums + (wt == T_Q4_K ? r256((size_t)M * (K / 16) * 2) : 0);
+    pl.ws_w6 = pl.ws_bsums + (wt != T_Q8_0 ? r256((size_t)M * (K / 16) * 2) : 0);
+    pl.workspace = pl.ws_w6 + (wt == T_Q6_K ? r256((size_t)N * (K / 256) * TxRaw<T_Q6_K>::row) : 0);
     out = pl;
     return true;
 }

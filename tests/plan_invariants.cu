@@ -139,7 +139,7 @@ int check_tcx(int wt, long long M, long long N, long long K) {
     const TcxParams& p = pl.p;
 #define CASE "tcx %s M%lld N%lld K%lld", tname(wt), M, N, K
     CHECK(pl.smem <= (size_t)kSmem && p.nraw >= 3 && p.nraw <= kTxRawMax, CASE);
-    CHECK(p.off_raw == tcx_stages(wt) * kTxStage && p.off_raw % 1024 == 0 && tcx_raw_slot(wt) % 1024 == 0 &&
+    CHECK(p.off_raw == tcx_stages(wt) * tcx_stage_bytes(wt) && p.off_raw % 1024 == 0 && tcx_raw_slot(wt) % 1024 == 0 &&
               p.off_bar == p.off_raw + p.nraw * tcx_raw_slot(wt) && (size_t)p.off_bar + 512 + 1024 <= pl.smem,
           CASE);
     CHECK(p.nrs * 256 == K && (long long)p.mtiles * kTxX >= M && (long long)p.ntiles * kTxW >= N &&
@@ -148,7 +148,8 @@ int check_tcx(int wt, long long M, long long N, long long K) {
     CHECK(pl.grid >= 1 && pl.grid <= kSms && pl.grid <= p.units && pl.mp % 4 == 0 && pl.mp >= M, CASE);
     CHECK(pl.ws_scales >= (size_t)M * K * 2 && pl.ws_scales % 256 == 0 && pl.ws_bsums % 256 == 0 &&
               pl.ws_bsums >= pl.ws_scales + (size_t)(K / (wt == T_Q8_0 ? 32 : 256)) * pl.mp * 4 &&
-              pl.workspace >= pl.ws_bsums + (wt == T_Q4_K ? (size_t)M * (K / 16) * 2 : 0),
+              pl.ws_w6 % 256 == 0 && pl.ws_w6 >= pl.ws_bsums + (wt != T_Q8_0 ? (size_t)M * (K / 16) * 2 : 0) &&
+              pl.workspace >= pl.ws_w6 + (wt == T_Q6_K ? (size_t)N * (K / 256) * 240 : 0),
           CASE);
 #undef CASE
     return 1;
@@ -207,7 +208,7 @@ int main() {
             for (long long N : {128, 300, 4096, 14336})
                 for (long long K : {256, 1024, 4096, 14336}) {
                     plans += check_tc(wt, M, N, K);
-                    if (wt == T_Q8_0 || wt == T_Q4_K) plans += check_tcx(wt, M, N, K);
+                    if (wt == T_Q8_0 || wt == T_Q4_K || wt == T_Q6_K) plans += check_tcx(wt, M, N, K);
                 }
     }
     for (int wt : types)
@@ -232,7 +233,7 @@ int main() {
     for (long long M : {37, 64, 256, 1024})
         for (int wt : types) {
             CHECK(plan_tc(wt, M, 14336, 4096, kSms, kSmem, tp), "no tcgen05 plan for %s M%lld", tname(wt), M);
-            if (wt == T_Q8_0 || wt == T_Q4_K)
+            if (wt == T_Q8_0 || wt == T_Q4_K || wt == T_Q6_K)
                 CHECK(plan_tcx(wt, M, 14336, 4096, kSms, kSmem, xp), "no exact prefill plan for %s M%lld", tname(wt), M);
         }
     std::printf("%s %d plans\n", g_bad ? "FAILED" : "ok", plans);
