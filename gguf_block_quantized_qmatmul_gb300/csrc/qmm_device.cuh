@@ -133,23 +133,40 @@ __device__ __forceinline__ long long wait_limit(const unsigned* err) {
     return 1ll << (lg == 0u || lg > 31u ? 31u : lg);
 }
 
-// Bounded wait on an mbarrier phase.  Gives up after wait_limit() SM clocks,
-// or at once when another warp of the block already gave up; on giving up it
-// raises the device error word and the block-wide abort flag.
+// The limit is read from global memory only once a wait has lasted 2^15
+// clocks (below every limit the hook allows), so no handoff between a block's
+// roles waits for an L2 round trip.
+constexpr long long kWaitLimitCheck = 1ll << 15;
+
+// The spinning part of a bounded wait, out of line: inlined at every wait of
+// a many-role kernel it made up much of the code those roles' loops fetch.
+// `drain` ignores the abort flag.  Gives up after wait_limit() SM clocks (or,
+// unless `drain`, at once when another warp of the block already gave up),
+// raising the device error word and the block-wide abort flag.
+static __device__ __noinline__ bool mbar_spin(uint32_t bar, uint32_t parity, volatile int* abort_flag, unsigned* err,
+                                              bool drain) {
+    const long long t0 = clock64();
+    long long lim = 0;
+    while (true) {
+        if (mbar_try(bar, parity)) return true;
+        if (!drain && *abort_flag) return false;
+        const long long dt = clock64() - t0;
+        if (dt > kWaitLimitCheck) {
+            if (lim == 0) lim = wait_limit(err);
+            if (dt > lim) {
+                atomicOr(err, ERR_TIMEOUT);
+                *abort_flag = 1;
+                return false;
+            }
+        }
+    }
+}
+
+// Bounded wait on an mbarrier phase: a first test inline, then mbar_spin.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                           unsigned* err) {
     if (mbar_try(bar, parity)) return true;
-    const long long lim = wait_limit(err);
-    const long long t0 = clock64();
-    while (true) {
-        if (mbar_try(bar, parity)) return true;
-        if (*abort_flag) return false;
-        if (clock64() - t0 > lim) {
-            atomicOr(err, ERR_TIMEOUT);
-            *abort_flag = 1;
-            return false;
-        }
-    }
+    return mbar_spin(bar, parity, abort_flag, err, false);
 }
 
 // Bounded wait for a phase whose arrivals were certainly issued (a copy or an
@@ -160,16 +177,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
 __device__ __forceinline__ bool mbar_drain(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                            unsigned* err) {
     if (mbar_try(bar, parity)) return true;
-    const long long lim = wait_limit(err);
-    const long long t0 = clock64();
-    while (true) {
-        if (mbar_try(bar, parity)) return true;
-        if (clock64() - t0 > lim) {
-            atomicOr(err, ERR_TIMEOUT);
-            *abort_flag = 1;
-            return false;
-        }
-    }
+    return mbar_spin(bar, parity, abort_flag, err, true);
 }
 
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {

@@ -5,9 +5,9 @@
 namespace qmm {
 
 namespace {
-unsigned long long g_tcx_smem_done[3];
+unsigned long long g_tcx_smem_done[6];
 
-template <int WT>
+template <int WT, int NX>
 cudaError_t tcx_go(const TcxPlan& pl, const void* wq, const float* x, void* ws, float* y, int smem_max, cudaStream_t s) {
     using R = TxRaw<WT>;
     const TcxParams& p0 = pl.p;
@@ -16,9 +16,12 @@ cudaError_t tcx_go(const TcxPlan& pl, const void* wq, const float* x, void* ws, 
     float* scales = reinterpret_cast<float*>(wsb + pl.ws_scales);
     __half* bsums = reinterpret_cast<__half*>(wsb + pl.ws_bsums);
     uint8_t* w6 = wsb + pl.ws_w6;  // Q6_K: super-blocks in 240-byte slots
-    // 1. the activation operand: f16 codes [M][K], scales block-major, (Q4_K) sums of 16 codes
+    unsigned* cnt = reinterpret_cast<unsigned*>(wsb + pl.ws_cnt);
+    // 1. the activation operand: f16 codes [M][K], scales block-major, (Q4_K) sums of 16 codes;
+    //    the split-K arrival counters zeroed
     const long long items = WT == T_Q8_0 ? (long long)p0.M * (p0.K / 32) : (long long)p0.M * (p0.K / 256) * 32;
-    tcx_act_kernel<WT><<<(unsigned)((items + 255) / 256), 256, 0, s>>>(x, p0.M, p0.K, pl.mp, codes, scales, bsums);
+    tcx_act_kernel<WT><<<(unsigned)((items + 255) / 256), 256, 0, s>>>(x, p0.M, p0.K, pl.mp, codes, scales, bsums, cnt,
+                                                                      p0.ks > 1 ? p0.tiles : 0);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (WT == T_Q6_K) {
@@ -28,28 +31,30 @@ cudaError_t tcx_go(const TcxPlan& pl, const void* wq, const float* x, void* ws, 
         if (e != cudaSuccess) return e;
     }
     // 2. tensor maps: raw weight rows as uint16 (128 rows x 256 K); activation codes, 32 K x
-    //    128 rows, 64-byte swizzle; activation scales; (Q4_K) the sums of 16 codes, 16 x 128
+    //    NX rows, 64-byte swizzle; activation scales; (Q4_K) the sums of 16 codes, 16 x NX
     //    rows, 32-byte swizzle
     CUtensorMap tw, ta, ts, tb;
     const unsigned long long rb = (unsigned long long)p0.K / 256 * R::row;
     const unsigned long long nsc = WT == T_Q8_0 ? p0.K / 32 : p0.K / 256;
     const void* wsrc = WT == T_Q6_K ? static_cast<const void*>(w6) : wq;
     bool ok = make_map(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT16, wsrc, rb / 2, p0.N, rb, R::row / 2, kTxW, CU_TENSOR_MAP_SWIZZLE_NONE) &&
-              make_map(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, codes, p0.K, p0.M, (unsigned long long)p0.K * 2, 32, kTxX,
+              make_map(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, codes, p0.K, p0.M, (unsigned long long)p0.K * 2, 32, NX,
                        CU_TENSOR_MAP_SWIZZLE_64B) &&
-              make_map(&ts, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, scales, pl.mp, nsc, (unsigned long long)pl.mp * 4, kTxX,
+              make_map(&ts, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, scales, pl.mp, nsc, (unsigned long long)pl.mp * 4, NX,
                        WT == T_Q8_0 ? 8 : 1, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (WT == T_Q4_K)
         ok = ok && make_map(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, bsums, p0.K / 16, p0.M, (unsigned long long)p0.K / 8, 16,
-                            kTxX, CU_TENSOR_MAP_SWIZZLE_32B);
+                            NX, CU_TENSOR_MAP_SWIZZLE_32B);
     else
         tb = ts;  // unused
     if (!ok) return cudaErrorInvalidValue;
     TcxParams p = p0;
     p.y = y;
+    p.part = reinterpret_cast<float*>(wsb + pl.ws_part);
+    p.cnt = cnt;
     // 3. the GEMM, a programmatic dependent of the preparation
-    auto* k = qmm_tcx_kernel<WT>;
-    e = ensure_smem(k, smem_max, g_tcx_smem_done[WT == T_Q8_0 ? 0 : WT == T_Q4_K ? 1 : 2]);
+    auto* k = qmm_tcx_kernel<WT, NX>;
+    e = ensure_smem(k, smem_max, g_tcx_smem_done[(WT == T_Q8_0 ? 0 : WT == T_Q4_K ? 1 : 2) + (NX == 64 ? 3 : 0)]);
     if (e != cudaSuccess) return e;
     return launch_pdl(k, (unsigned)pl.grid, kTxThreads, pl.smem, s, tw, ta, ts, tb, p);
 }
@@ -57,10 +62,11 @@ cudaError_t tcx_go(const TcxPlan& pl, const void* wq, const float* x, void* ws, 
 
 cudaError_t launch_tcx(int wt, const TcxPlan& pl, const void* wq, const float* x, void* ws, float* y, int smem_max,
                        cudaStream_t s) {
+    const bool n64 = pl.nx == 64;
     switch (wt) {
-        case T_Q8_0: return tcx_go<T_Q8_0>(pl, wq, x, ws, y, smem_max, s);
-        case T_Q4_K: return tcx_go<T_Q4_K>(pl, wq, x, ws, y, smem_max, s);
-        default: return tcx_go<T_Q6_K>(pl, wq, x, ws, y, smem_max, s);
+        case T_Q8_0: return n64 ? tcx_go<T_Q8_0, 64>(pl, wq, x, ws, y, smem_max, s) : tcx_go<T_Q8_0, 128>(pl, wq, x, ws, y, smem_max, s);
+        case T_Q4_K: return n64 ? tcx_go<T_Q4_K, 64>(pl, wq, x, ws, y, smem_max, s) : tcx_go<T_Q4_K, 128>(pl, wq, x, ws, y, smem_max, s);
+        default: return n64 ? tcx_go<T_Q6_K, 64>(pl, wq, x, ws, y, smem_max, s) : tcx_go<T_Q6_K, 128>(pl, wq, x, ws, y, smem_max, s);
     }
 }
 

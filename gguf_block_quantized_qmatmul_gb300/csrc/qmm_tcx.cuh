@@ -52,11 +52,12 @@
 namespace qmm {
 
 constexpr int kTxW = 128;         // weight rows per tile (MMA M)
-constexpr int kTxX = 128;         // activation rows per tile (MMA N)
+constexpr int kTxX = 128;         // activation rows per tile (MMA N), at most: 64 or 128
 constexpr int kTxSMax = 8;        // block stages (weight codes + activation codes in shared memory), at most
-constexpr int kTxAcc = 4;         // TMEM accumulators of kTxX columns
-constexpr int kTxTmemCols = kTxAcc * kTxX;
+constexpr int kTxTmemCols = 512;  // a ring of 512 / NX accumulators of NX columns
+constexpr int kTxAccMax = kTxTmemCols / 64;
 constexpr int kTxRawMax = 6;
+constexpr int kTxMaxSplit = 16;   // K slices of a tile, at most
 constexpr int kTxEpiWarps = 16;
 constexpr int kTxConvWarps = 4;
 constexpr int kTxThreads = (2 + kTxEpiWarps + kTxConvWarps) * 32;
@@ -82,9 +83,10 @@ struct TxRaw {
     static constexpr int slot = WT == T_Q8_0 ? (scales + 8 * kTxX * 4 + 1023) / 1024 * 1024
                                 : WT == T_Q4_K ? amin + kTxW * 32
                                                : (scales + kTxX * 4 + 1023) / 1024 * 1024;
-    static constexpr int tx = WT == T_Q8_0   ? kTxW * row + 8 * kTxX * 4
-                              : WT == T_Q4_K ? kTxW * row + kTxX * 4 + kTxX * 32
-                                             : kTxW * row + kTxX * 4;
+    // bytes a raw stage's copies bring, for tiles of nx activation rows
+    __host__ __device__ static constexpr int tx(int nx) {
+        return WT == T_Q8_0 ? kTxW * row + 8 * nx * 4 : WT == T_Q4_K ? kTxW * row + nx * 4 + nx * 32 : kTxW * row + nx * 4;
+    }
     // accumulators (drain units) per raw stage: Q8_0 one per block; Q4_K S_sc
     // and S_m; Q6_K S_a and S_b (S = 16 S_a + S_b)
     static constexpr int drains = WT == T_Q8_0 ? 8 : 2;
@@ -100,12 +102,24 @@ static_assert(TxRaw<T_Q8_0>::slot % 1024 == 0 && TxRaw<T_Q4_K>::slot % 1024 == 0
 struct TcxParams {
     float* y;
     unsigned* err;
+    float* part;    // partial tiles [ks][M][N] when K is split
+    unsigned* cnt;  // per-tile arrival counters when K is split (zeroed by the activation launch)
     int M, N, K;
-    int mtiles, ntiles, units;
-    int nrs;       // raw stages in K (K / 256)
-    int nraw;      // raw slots in shared memory
+    int mtiles, ntiles, tiles;
+    int ks, units;  // K slices; work units = tiles x ks
+    int nrs;        // raw stages in K (K / 256)
+    int nraw;       // raw slots in shared memory
     int off_raw, off_bar;
 };
+
+// work unit u: tile u % tiles (weight rows n0 = (tile / mtiles) 128.., activation
+// rows m0 = (tile % mtiles) NX..), K slice u / tiles: raw stages [r0, r1)
+__device__ __forceinline__ void tcx_slice(const TcxParams& p, int u, int& tile, int& r0, int& r1) {
+    tile = u % p.tiles;
+    const int split = u / p.tiles;
+    r0 = split * p.nrs / p.ks;
+    r1 = (split + 1) * p.nrs / p.ks;
+}
 
 // D (TMEM) += A (shared memory) x B (shared memory)^T
 __device__ __forceinline__ void tcx_mma(uint32_t tmem, uint64_t da, uint64_t db, uint32_t idesc, uint32_t accumulate) {
@@ -114,6 +128,13 @@ __device__ __forceinline__ void tcx_mma(uint32_t tmem, uint64_t da, uint64_t db,
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem),
         "l"(da), "l"(db), "r"(idesc), "r"(accumulate)
         : "memory");
+}
+
+// 8 f32 columns of this warp's TMEM lane quarter (the wait is separate)
+__device__ __forceinline__ void tcx_ld8(uint32_t taddr, uint32_t r[8]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
 }
 
 // shared-memory matrix descriptor: K-major, 32-byte swizzle (rows of 16 f16), 8-row atoms 256 B apart
@@ -221,11 +242,31 @@ __device__ __forceinline__ float tcx_block_scale(const uint8_t* row, int j) {
     return h2f(*reinterpret_cast<const uint16_t*>(row + 34 * j));
 }
 
-template <int WT>  // T_Q8_0, T_Q4_K or T_Q6_K
+// K split: y of a tile (rows m0.., n0..) as the sum of its ks partial tiles in
+// slice order, by the tile's last unit; thread t of the 16 epilogue warps
+// takes column n0 + t % 128 and every fourth row from t / 128 (stores
+// coalesced along N)
+template <int NX>
+__device__ __forceinline__ void tcx_fixup(const TcxParams& p, int t, int m0, int n0) {
+    const int n = n0 + (t & (kTxW - 1));
+    if (n >= p.N) return;
+    const size_t slice = (size_t)p.M * p.N;
+    for (int mr = t >> 7; mr < NX && m0 + mr < p.M; mr += kTxEpiWarps * 32 / kTxW) {
+        const float* src = p.part + (size_t)(m0 + mr) * p.N + n;
+        float sum = __ldcg(src);
+        for (int k = 1; k < p.ks; ++k) sum += __ldcg(src + k * slice);
+        p.y[(size_t)(m0 + mr) * p.N + n] = sum;
+    }
+}
+
+template <int WT, int NX>  // T_Q8_0, T_Q4_K or T_Q6_K; tiles of NX = 64 or 128 activation rows
 __global__ void __launch_bounds__(kTxThreads, 1)
     qmm_tcx_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUtensorMap ta,
                    const __grid_constant__ CUtensorMap ts, const __grid_constant__ CUtensorMap tb, const TcxParams p) {
     using R = TxRaw<WT>;
+    static_assert(NX == 64 || NX == 128, "tile widths");
+    constexpr int kAcc = kTxTmemCols / NX;  // TMEM accumulators
+    constexpr int CW = NX / 4;              // accumulator columns an epilogue warp drains
     extern __shared__ __align__(1024) uint8_t smraw[];
     uint8_t* sm = smraw + ((1024 - (smem_u32(smraw) & 1023)) & 1023);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -236,11 +277,13 @@ __global__ void __launch_bounds__(kTxThreads, 1)
     uint64_t* r_full = empty + kTxS;             // [kTxRawMax] raw stage landed (TMA)
     uint64_t* r_empty = r_full + kTxRawMax;      // [kTxRawMax] raw stage converted and folded
     uint64_t* min_ready = r_empty + kTxRawMax;   // [kTxRawMax] Q4_K: the min term's weight operand written
-    uint64_t* acc_full = min_ready + kTxRawMax;  // [kTxAcc] accumulator complete (commit)
-    uint64_t* acc_empty = acc_full + kTxAcc;     // [kTxAcc] accumulator drained (epilogue)
-    static_assert((2 * kTxSMax + 3 * kTxRawMax + 2 * kTxAcc) * 8 <= 448, "mbarriers overlap the TMEM slot");
+    uint64_t* acc_full = min_ready + kTxRawMax;  // [kAcc] accumulator complete (commit)
+    uint64_t* acc_empty = acc_full + kAcc;       // [kAcc] accumulator drained (epilogue)
+    uint64_t* epi_done = acc_empty + kAcc;       // K split: the unit's partial tile stored (epilogue warps)
+    uint64_t* fix_ready = epi_done + 1;          // K split: whether this CTA completes the tile is known
+    static_assert((2 * kTxSMax + 3 * kTxRawMax + 2 * kTxAccMax + 2) * 8 <= 448, "mbarriers overlap the TMEM slot");
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + p.off_bar + 448);
-    volatile int* flags = reinterpret_cast<volatile int*>(sm + p.off_bar + 480);  // [0] abort
+    volatile int* flags = reinterpret_cast<volatile int*>(sm + p.off_bar + 480);  // [0] abort, [1] tile owner
     if (tid == 0) {
         for (int i = 0; i < kTxS; ++i) {
             mbar_init(smem_u32(&full[i]), 1 + kTxConvWarps);
@@ -251,11 +294,14 @@ __global__ void __launch_bounds__(kTxThreads, 1)
             mbar_init(smem_u32(&r_empty[i]), kTxConvWarps + kTxEpiWarps);
             mbar_init(smem_u32(&min_ready[i]), kTxConvWarps);
         }
-        for (int i = 0; i < kTxAcc; ++i) {
+        for (int i = 0; i < kAcc; ++i) {
             mbar_init(smem_u32(&acc_full[i]), 1);
             mbar_init(smem_u32(&acc_empty[i]), kTxEpiWarps);
         }
+        mbar_init(smem_u32(epi_done), kTxEpiWarps);
+        mbar_init(smem_u32(fix_ready), 1);
         flags[0] = 0;
+        flags[1] = 0;
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -273,17 +319,19 @@ __global__ void __launch_bounds__(kTxThreads, 1)
     auto wstage = [&](int s) { return sm + s * R::stage; };                           // A: weight codes (Q6_K: a q, then b q)
     auto xstage = [&](int s) { return sm + s * R::stage + R::wtiles * kTxW * 64; };   // B: activation codes
     auto raw = [&](int s) { return sm + p.off_raw + s * R::slot; };
-    // unit u: weight tile u / mtiles (rows n0..n0+127), activation tile u % mtiles (rows m0..m0+127)
 
     if (warp == 0) {
         // ------------------------------ producer ------------------------------
         if (lane == 0) {
             long long g = 0, ri = 0, rc = 0;  // blocks issued; raw stages issued; raw stages whose blocks are issued
-            int iu = blockIdx.x, ir = 0;      // raw-issue cursor: unit, raw stage
+            int iu = blockIdx.x, ir = 0, ir1 = 0, itile = 0;  // raw-issue cursor: unit, raw stage, its slice's end, tile
+            if (iu < p.units) tcx_slice(p, iu, itile, ir, ir1);
             bool ok = true;
             for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
-                const int m0 = (u % p.mtiles) * kTxX;
-                for (int r = 0; r < p.nrs && ok; ++r, ++rc) {
+                int tile, r0, r1;
+                tcx_slice(p, u, tile, r0, r1);
+                const int m0 = (tile % p.mtiles) * NX;
+                for (int r = r0; r < r1 && ok; ++r, ++rc) {
                     // raw stages up to nraw - 2 ahead, across units: the slot a new stage
                     // reuses is then two stages old, one the epilogue has finished folding
                     // (waiting on a younger one would hold back this stage's activations)
@@ -291,9 +339,9 @@ __global__ void __launch_bounds__(kTxThreads, 1)
                         const int rs = (int)(ri % p.nraw);
                         if (ri >= p.nraw) ok = mbar_wait(smem_u32(&r_empty[rs]), (uint32_t)(((ri / p.nraw) - 1) & 1), flags, p.err);
                         if (!ok) break;
-                        const int in0 = (iu / p.mtiles) * kTxW, im0 = (iu % p.mtiles) * kTxX;
+                        const int in0 = (itile / p.mtiles) * kTxW, im0 = (itile % p.mtiles) * NX;
                         const uint32_t fb = smem_u32(&r_full[rs]);
-                        mbar_arrive_tx(fb, (uint32_t)R::tx);
+                        mbar_arrive_tx(fb, (uint32_t)R::tx(NX));
                         tma_2d(smem_u32(raw(rs)), &tw, ir * (R::row / 2), in0, fb);
                         if (WT == T_Q8_0) {
                             tma_2d(smem_u32(raw(rs) + R::scales), &ts, im0, 8 * ir, fb);
@@ -302,13 +350,16 @@ __global__ void __launch_bounds__(kTxThreads, 1)
                             if (WT == T_Q4_K) tma_2d(smem_u32(raw(rs) + R::bsum), &tb, 16 * ir, im0, fb);
                         }
                         ++ri;
-                        if (++ir >= p.nrs) ir = 0, iu += gridDim.x;
+                        if (++ir >= ir1) {
+                            iu += gridDim.x;
+                            if (iu < p.units) tcx_slice(p, iu, itile, ir, ir1);
+                        }
                     }
                     for (int j = 0; j < 8 && ok; ++j, ++g) {
                         const int s = (int)(g % kTxS);
                         if (g >= kTxS) ok = mbar_wait(smem_u32(&empty[s]), (uint32_t)(((g / kTxS) - 1) & 1), flags, p.err);
                         if (!ok) break;
-                        mbar_arrive_tx(smem_u32(&full[s]), (uint32_t)(kTxX * 64));
+                        mbar_arrive_tx(smem_u32(&full[s]), (uint32_t)(NX * 64));
                         tma_2d(smem_u32(xstage(s)), &ta, (r * 8 + j) * 32, m0, smem_u32(&full[s]));
                     }
                 }
@@ -322,16 +373,19 @@ __global__ void __launch_bounds__(kTxThreads, 1)
     } else if (warp == 1) {
         // ------------------------------ MMA issuer ------------------------------
         if (lane == 0) {
-            const uint32_t idesc = tc_idesc(kTxX);
-            long long g = 0, du = 0, rg = 0;  // blocks; drain units; raw stages
+            const uint32_t idesc = tc_idesc(NX);
+            long long g = 0, rg = 0;  // blocks; raw stages
+            uint32_t du = 0;          // drain units (a launch drains far fewer than 2^32)
             bool ok = true;
             uint32_t ready = 0;  // the next stage's barrier, tested ahead
-            auto acc_take = [&](long long d) {  // accumulator d % kTxAcc, once the epilogue drained its last use
-                if (d >= kTxAcc) ok = mbar_wait(smem_u32(&acc_empty[d % kTxAcc]), (uint32_t)(((d / kTxAcc) - 1) & 1), flags, p.err);
-                return (uint32_t)((d % kTxAcc) * kTxX);
+            auto acc_take = [&](uint32_t d) {  // accumulator d % kAcc, once the epilogue drained its last use
+                if (d >= kAcc) ok = mbar_wait(smem_u32(&acc_empty[d % kAcc]), (uint32_t)(((d / kAcc) - 1) & 1), flags, p.err);
+                return (uint32_t)((d % kAcc) * NX);
             };
             for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
-                for (int r = 0; r < p.nrs && ok; ++r, ++rg) {
+                int tile, r0, r1;
+                tcx_slice(p, u, tile, r0, r1);
+                for (int r = r0; r < r1 && ok; ++r, ++rg) {
                     uint32_t dcol = 0, dcol2 = 0;
                     if (WT != T_Q8_0) dcol = acc_take(du);                // S_sc (Q4_K), S_a (Q6_K)
                     if (WT == T_Q6_K && ok) dcol2 = acc_take(du + 1);    // S_b
@@ -355,16 +409,16 @@ __global__ void __launch_bounds__(kTxThreads, 1)
                                         (uint32_t)(j | kk));
                         }
                         tc_commit(smem_u32(&empty[s]));
-                        if (WT == T_Q8_0) tc_commit(smem_u32(&acc_full[(du + j) % kTxAcc]));
+                        if (WT == T_Q8_0) tc_commit(smem_u32(&acc_full[(du + j) % kAcc]));
                         ready = nxt;
                     }
                     if (!ok) break;
                     if (WT == T_Q6_K) {
-                        tc_commit(smem_u32(&acc_full[du % kTxAcc]));
-                        tc_commit(smem_u32(&acc_full[(du + 1) % kTxAcc]));
+                        tc_commit(smem_u32(&acc_full[du % kAcc]));
+                        tc_commit(smem_u32(&acc_full[(du + 1) % kAcc]));
                     }
                     if (WT == T_Q4_K) {
-                        tc_commit(smem_u32(&acc_full[du % kTxAcc]));
+                        tc_commit(smem_u32(&acc_full[du % kAcc]));
                         // S_m = sum_j m_j bsum_j: one K 16 MMA over the 16 sums of 16 codes
                         const uint32_t mcol = acc_take(du + 1);
                         const int rs = (int)(rg % p.nraw);
@@ -373,61 +427,67 @@ __global__ void __launch_bounds__(kTxThreads, 1)
                         tc_fence_after();
                         tcx_mma(tmem + mcol, tcx_sdesc32(smem_u32(raw(rs) + R::amin)), tcx_sdesc32(smem_u32(raw(rs) + R::bsum)),
                                 idesc, 0u);
-                        tc_commit(smem_u32(&acc_full[(du + 1) % kTxAcc]));
+                        tc_commit(smem_u32(&acc_full[(du + 1) % kAcc]));
                     }
                     du += R::drains;
                 }
             }
             // the last commits must land before TMEM is released
             if (g > 0) mbar_drain(smem_u32(&empty[(g - 1) % kTxS]), (uint32_t)(((g - 1) / kTxS) & 1), flags, p.err);
-            if (du > 0) mbar_drain(smem_u32(&acc_full[(du - 1) % kTxAcc]), (uint32_t)(((du - 1) / kTxAcc) & 1), flags, p.err);
+            if (du > 0) mbar_drain(smem_u32(&acc_full[(du - 1) % kAcc]), (uint32_t)(((du - 1) / kAcc) & 1), flags, p.err);
         }
     } else if (warp < 2 + kTxEpiWarps) {
         // ------------------------------ epilogue ------------------------------
         const int ew = warp - 2;
         const int q = warp & 3;   // TMEM lane quarter: weight rows 32q..32q+31 of the tile
-        const int cq = ew >> 2;   // accumulator columns 32cq..32cq+31: activation rows of the tile
+        const int cq = ew >> 2;   // accumulator columns CW cq..CW cq + CW - 1: activation rows of the tile
         const uint32_t tq = (uint32_t)(32 * q) << 16;
         const int nl = 32 * q + lane;  // this thread's weight row in the tile
-        long long du = 0, rg = 0;
+        // drain units: a launch drains far fewer than 2^32 accumulators
+        uint32_t du = 0;
+        long long rg = 0;
         bool ok = true;
-        auto acc_wait = [&](long long d) {
-            ok = mbar_wait(smem_u32(&acc_full[d % kTxAcc]), (uint32_t)((d / kTxAcc) & 1), flags, p.err);
-            return tmem + tq + (uint32_t)((d % kTxAcc) * kTxX + 32 * cq);
+        auto acc_wait = [&](uint32_t d) {
+            ok = mbar_wait(smem_u32(&acc_full[d % kAcc]), (uint32_t)((d / kAcc) & 1), flags, p.err);
+            return tmem + tq + (uint32_t)((d % kAcc) * NX + CW * cq);
         };
-        auto acc_release = [&](long long d) {
+        auto acc_release = [&](uint32_t d) {
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&acc_empty[d % kTxAcc]));
+            if (lane == 0) mbar_arrive(smem_u32(&acc_empty[d % kAcc]));
         };
         for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
-            const int m0 = (u % p.mtiles) * kTxX, n0 = (u / p.mtiles) * kTxW;
-            unsigned long long acc[16];  // running sums of activation rows 32cq + 2i, 2i + 1
+            int r0, r1;
+            {
+                int tile_;
+                tcx_slice(p, u, tile_, r0, r1);
+            }
+            unsigned long long acc[CW / 2];  // running sums of activation rows CW cq + 2i, 2i + 1
 #pragma unroll
-            for (int i = 0; i < 16; ++i) acc[i] = 0ull;
-            for (int r = 0; r < p.nrs && ok; ++r, ++rg) {
+            for (int i = 0; i < CW / 2; ++i) acc[i] = 0ull;
+            for (int r = r0; r < r1 && ok; ++r, ++rg) {
                 const int rs = (int)(rg % p.nraw);
                 const uint8_t* wrow = raw(rs) + nl * R::row;
-                const float* asc = reinterpret_cast<const float*>(raw(rs) + R::scales) + 32 * cq;
+                const float* asc = reinterpret_cast<const float*>(raw(rs) + R::scales) + CW * cq;
                 if (WT == T_Q8_0) {
                     for (int j = 0; j < 8; ++j, ++du) {
                         const uint32_t acol = acc_wait(du);
                         if (!ok) break;
                         tc_fence_after();
                         __syncwarp();
-                        uint32_t v0[16], v1[16];
-                        tc_ld16(acol, v0);
-                        tc_ld16(acol + 16, v1);
+                        uint32_t vv[CW];
+#pragma unroll
+                        for (int h = 0; h < CW / 16; ++h) tc_ld16(acol + 16 * h, vv + 16 * h);
                         tc_wait_ld();
                         acc_release(du);
                         // fold: y += isum f(d_w) f(d_a)
                         const float dw = tcx_block_scale(wrow, j);
                         const unsigned long long dw2 = f2pack(dw, dw);
-                        const float* aj = asc + j * kTxX;
+                        const float* aj = asc + j * NX;
 #pragma unroll
-                        for (int c = 0; c < 8; ++c) {
+                        for (int c = 0; c < CW / 4; ++c) {
                             const float4 a4 = *reinterpret_cast<const float4*>(aj + 4 * c);
-                            const uint32_t* v = c < 4 ? v0 + 4 * c : v1 + 4 * (c - 4);
+                            const uint32_t* v = vv + 4 * c;
                             const unsigned long long s01 = mul2(f2pack(a4.x, a4.y), dw2), s23 = mul2(f2pack(a4.z, a4.w), dw2);
                             acc[2 * c] = fma2(f2pack(__uint_as_float(v[0]), __uint_as_float(v[1])), s01, acc[2 * c]);
                             acc[2 * c + 1] = fma2(f2pack(__uint_as_float(v[2]), __uint_as_float(v[3])), s23, acc[2 * c + 1]);
@@ -444,21 +504,21 @@ __global__ void __launch_bounds__(kTxThreads, 1)
                     const float fd = h2f(*reinterpret_cast<const uint16_t*>(wrow + 208));
                     const unsigned long long fd2 = f2pack(fd, fd), k16 = f2pack(16.0f, 16.0f);
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        uint32_t va[16], vb[16];
-                        tc_ld16(ca + 16 * h, va);
-                        tc_ld16(cb + 16 * h, vb);
+                    for (int h = 0; h < CW / 8; ++h) {  // 8 columns at a time: the running sums hold 2 CW registers
+                        uint32_t va[8], vb[8];
+                        tcx_ld8(ca + 8 * h, va);
+                        tcx_ld8(cb + 8 * h, vb);
                         tc_wait_ld();
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            const float4 a4 = *reinterpret_cast<const float4*>(asc + 16 * h + 4 * c);
+                        for (int c = 0; c < 2; ++c) {
+                            const float4 a4 = *reinterpret_cast<const float4*>(asc + 8 * h + 4 * c);
 #pragma unroll
                             for (int e = 0; e < 2; ++e) {
                                 const int i = 4 * c + 2 * e;
                                 const unsigned long long t = fma2(f2pack(__uint_as_float(va[i]), __uint_as_float(va[i + 1])), k16,
                                                                   f2pack(__uint_as_float(vb[i]), __uint_as_float(vb[i + 1])));
                                 const unsigned long long sc2 = mul2(e ? f2pack(a4.z, a4.w) : f2pack(a4.x, a4.y), fd2);
-                                acc[8 * h + 2 * c + e] = fma2(t, sc2, acc[8 * h + 2 * c + e]);
+                                acc[4 * h + 2 * c + e] = fma2(t, sc2, acc[4 * h + 2 * c + e]);
                             }
                         }
                     }
@@ -475,14 +535,14 @@ __global__ void __launch_bounds__(kTxThreads, 1)
                     const uint32_t dd = *reinterpret_cast<const uint32_t*>(wrow);  // f16 d, f16 dmin
                     const unsigned long long fd2 = f2pack(h2f(dd), h2f(dd)), fm2 = f2pack(-h2f(dd >> 16), -h2f(dd >> 16));
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        uint32_t vs[16], vm[16];
-                        tc_ld16(ca + 16 * h, vs);
-                        tc_ld16(cm + 16 * h, vm);
+                    for (int h = 0; h < CW / 8; ++h) {  // 8 columns at a time: the running sums hold 2 CW registers
+                        uint32_t vs[8], vm[8];
+                        tcx_ld8(ca + 8 * h, vs);
+                        tcx_ld8(cm + 8 * h, vm);
                         tc_wait_ld();
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            const float4 a4 = *reinterpret_cast<const float4*>(asc + 16 * h + 4 * c);
+                        for (int c = 0; c < 2; ++c) {
+                            const float4 a4 = *reinterpret_cast<const float4*>(asc + 8 * h + 4 * c);
 #pragma unroll
                             for (int e = 0; e < 2; ++e) {
                                 const int i = 4 * c + 2 * e;
@@ -490,7 +550,7 @@ __global__ void __launch_bounds__(kTxThreads, 1)
                                     fma2(f2pack(__uint_as_float(vs[i]), __uint_as_float(vs[i + 1])), fd2,
                                          mul2(f2pack(__uint_as_float(vm[i]), __uint_as_float(vm[i + 1])), fm2));
                                 const unsigned long long a2 = e ? f2pack(a4.z, a4.w) : f2pack(a4.x, a4.y);
-                                acc[8 * h + 2 * c + e] = fma2(t, a2, acc[8 * h + 2 * c + e]);
+                                acc[4 * h + 2 * c + e] = fma2(t, a2, acc[4 * h + 2 * c + e]);
                             }
                         }
                     }
@@ -503,13 +563,37 @@ __global__ void __launch_bounds__(kTxThreads, 1)
                 if (lane == 0) mbar_arrive(smem_u32(&r_empty[rs]));  // this warp no longer reads the raw stage
             }
             if (!ok || flags[0]) break;
+            const int tile = u % p.tiles;
+            const int m0 = (tile % p.mtiles) * NX, n0 = (tile / p.mtiles) * kTxW;
             const int n = n0 + nl;
+            float* dst = p.ks == 1 ? p.y : p.part + (size_t)(u / p.tiles) * p.M * p.N;
             if (n < p.N) {
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int m = m0 + 32 * cq + 2 * i;
-                    if (m < p.M) p.y[(size_t)m * p.N + n] = f2lo(acc[i]);
-                    if (m + 1 < p.M) p.y[(size_t)(m + 1) * p.N + n] = f2hi(acc[i]);
+                for (int i = 0; i < CW / 2; ++i) {
+                    const int m = m0 + CW * cq + 2 * i;
+                    if (m < p.M) dst[(size_t)m * p.N + n] = f2lo(acc[i]);
+                    if (m + 1 < p.M) dst[(size_t)(m + 1) * p.N + n] = f2hi(acc[i]);
+                }
+            }
+            if (p.ks > 1) {
+                // the unit that completes the tile sums its ks partials in slice order
+                const uint32_t fix = (uint32_t)(((u - (int)blockIdx.x) / (int)gridDim.x) & 1);  // this CTA's unit count
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(epi_done));
+                if (ew == 0 && lane == 0) {
+                    int owner = 0;
+                    if (mbar_wait(smem_u32(epi_done), fix, flags, p.err)) {
+                        __threadfence();
+                        owner = atomicAdd(p.cnt + tile, 1u) == (unsigned)(p.ks - 1);
+                    }
+                    flags[1] = owner;
+                    mbar_arrive(smem_u32(fix_ready));
+                }
+                if (!(ok = mbar_wait(smem_u32(fix_ready), fix, flags, p.err))) break;
+                if (flags[1]) {
+                    __threadfence();
+                    tcx_fixup<NX>(p, ew * 32 + lane, m0, n0);
                 }
             }
         }
@@ -521,7 +605,9 @@ __global__ void __launch_bounds__(kTxThreads, 1)
         long long rg = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
-            for (int rr = 0; rr < p.nrs && ok; ++rr, ++rg) {
+            int tile, r0, r1;
+            tcx_slice(p, u, tile, r0, r1);
+            for (int rr = r0; rr < r1 && ok; ++rr, ++rg) {
                 const int rs = (int)(rg % p.nraw);
                 if (!(ok = mbar_wait(smem_u32(&r_full[rs]), (uint32_t)((rg / p.nraw) & 1), flags, p.err))) break;
                 const uint8_t* wrow = raw(rs) + r * R::row;
@@ -611,11 +697,14 @@ __global__ void __launch_bounds__(kTxThreads, 1)
 // Q4_K: one warp per (row m, super-block b), lane l taking values 8l..8l+7,
 // quantizes it to Q8K (f32 d = amax / 127 over the 256 values), writes the
 // codes as f16, d to scales[b][mp] and the 16 sums of 16 codes (at most
-// 2032 in magnitude, exact in f16) to bsums[m][K / 16].
+// 2032 in magnitude, exact in f16) to bsums[m][K / 16].  It also zeroes the
+// GEMM's ncnt split-K arrival counters.
 template <int WT>
 __global__ void tcx_act_kernel(const float* __restrict__ x, int M, int K, int mp, __half* __restrict__ codes,
-                               float* __restrict__ scales, __half* __restrict__ bsums) {
+                               float* __restrict__ scales, __half* __restrict__ bsums, unsigned* __restrict__ cnt, int ncnt) {
     grid_dep_launch();
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < ncnt; i += (long long)gridDim.x * blockDim.x)
+        cnt[i] = 0u;
     if (WT == T_Q8_0) {
         const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
         const int nb = K / 32;
@@ -681,10 +770,11 @@ __global__ void tcx_q6_repack_kernel(const uint8_t* __restrict__ wq, int N, int 
 // ---------------------------------------------------------------------------
 struct TcxPlan {
     TcxParams p;
+    int nx;  // activation rows per tile: 64 or 128
     int grid;
     size_t smem;
     int mp;  // activation scale rows: M rounded up to 4 (16-byte rows for the tensor map)
-    size_t ws_codes, ws_scales, ws_bsums, ws_w6, workspace;
+    size_t ws_codes, ws_scales, ws_bsums, ws_w6, ws_part, ws_cnt, workspace;
 };
 
 inline int tcx_raw_slot(int wt) {
@@ -706,10 +796,33 @@ inline bool plan_tcx(int wt, long long M, long long N, long long K, int sm_count
     p.M = (int)M;
     p.N = (int)N;
     p.K = (int)K;
-    p.mtiles = (int)((M + kTxX - 1) / kTxX);
+    // 64-row tiles when they hold all activation rows: half the fold and the
+    // accumulator drains of a 128-row tile
+    pl.nx = M <= 64 ? 64 : kTxX;
+    p.mtiles = (int)((M + pl.nx - 1) / pl.nx);
     p.ntiles = (int)((N + kTxW - 1) / kTxW);
-    p.units = p.mtiles * p.ntiles;
+    if ((long long)p.mtiles * p.ntiles * kTxMaxSplit > INT32_MAX) return false;
+    p.tiles = p.mtiles * p.ntiles;
     p.nrs = (int)(K / 256);
+    // K slices: with few tiles, the smallest ks whose busiest CTA (units dealt
+    // round-robin, one CTA per SM) carries the fewest raw stages, counting a
+    // unit's start and, for a split tile's last unit, its sum of ks partials
+    // as about half a stage each
+    {
+        double best = 0.0;
+        int best_ks = 1;
+        const int kmax = p.nrs < kTxMaxSplit ? p.nrs : kTxMaxSplit;
+        for (int ks = 1; ks <= kmax; ++ks) {
+            const long long units = (long long)p.tiles * ks;
+            const long long grid = units < sm_count ? units : sm_count;
+            const long long per = (units + grid - 1) / grid;  // units of the busiest CTA
+            const double stages = (double)p.nrs / ks + 0.5 + (ks > 1 ? 0.5 * ks / 4.0 : 0.0);
+            const double worst = per * stages;
+            if (ks == 1 || worst < best * 0.98) best = worst, best_ks = ks;
+        }
+        p.ks = best_ks;
+    }
+    p.units = p.tiles * p.ks;
     p.off_raw = tcx_stages(wt) * tcx_stage_bytes(wt);
     const int fixed = 512 + 1024;  // barriers, TMEM slot, flags; alignment slack
     p.nraw = (smem_max - p.off_raw - fixed) / tcx_raw_slot(wt);
@@ -725,7 +838,9 @@ inline bool plan_tcx(int wt, long long M, long long N, long long K, int sm_count
     const size_t per = wt == T_Q8_0 ? 32 : 256;  // values per activation scale
     pl.ws_bsums = pl.ws_scales + r256((size_t)(K / per) * pl.mp * 4);
     pl.ws_w6 = pl.ws_bsums + (wt != T_Q8_0 ? r256((size_t)M * (K / 16) * 2) : 0);
-    pl.workspace = pl.ws_w6 + (wt == T_Q6_K ? r256((size_t)N * (K / 256) * TxRaw<T_Q6_K>::row) : 0);
+    pl.ws_part = pl.ws_w6 + (wt == T_Q6_K ? r256((size_t)N * (K / 256) * TxRaw<T_Q6_K>::row) : 0);
+    pl.ws_cnt = pl.ws_part + (p.ks > 1 ? r256((size_t)p.ks * M * N * 4) : 0);
+    pl.workspace = pl.ws_cnt + (p.ks > 1 ? r256((size_t)p.tiles * 4) : 0);
     out = pl;
     return true;
 }

@@ -142,14 +142,23 @@ int check_tcx(int wt, long long M, long long N, long long K) {
     CHECK(p.off_raw == tcx_stages(wt) * tcx_stage_bytes(wt) && p.off_raw % 1024 == 0 && tcx_raw_slot(wt) % 1024 == 0 &&
               p.off_bar == p.off_raw + p.nraw * tcx_raw_slot(wt) && (size_t)p.off_bar + 512 + 1024 <= pl.smem,
           CASE);
-    CHECK(p.nrs * 256 == K && (long long)p.mtiles * kTxX >= M && (long long)p.ntiles * kTxW >= N &&
-              p.units == p.mtiles * p.ntiles,
+    CHECK((pl.nx == 64 || pl.nx == kTxX) && (pl.nx == 64) == (M <= 64), CASE);
+    CHECK(p.nrs * 256 == K && (long long)p.mtiles * pl.nx >= M && (long long)(p.mtiles - 1) * pl.nx < M &&
+              (long long)p.ntiles * kTxW >= N && p.tiles == p.mtiles * p.ntiles,
           CASE);
+    // every K slice holds at least one raw stage, and the slices tile K
+    CHECK(p.ks >= 1 && p.ks <= kTxMaxSplit && p.ks <= p.nrs && p.units == p.tiles * p.ks, CASE);
+    for (int sp = 0; sp < p.ks; ++sp) {
+        const int r0 = sp * p.nrs / p.ks, r1 = (sp + 1) * p.nrs / p.ks;
+        CHECK(r1 > r0 && (sp > 0 || r0 == 0) && (sp < p.ks - 1 || r1 == p.nrs), CASE);
+    }
     CHECK(pl.grid >= 1 && pl.grid <= kSms && pl.grid <= p.units && pl.mp % 4 == 0 && pl.mp >= M, CASE);
     CHECK(pl.ws_scales >= (size_t)M * K * 2 && pl.ws_scales % 256 == 0 && pl.ws_bsums % 256 == 0 &&
               pl.ws_bsums >= pl.ws_scales + (size_t)(K / (wt == T_Q8_0 ? 32 : 256)) * pl.mp * 4 &&
               pl.ws_w6 % 256 == 0 && pl.ws_w6 >= pl.ws_bsums + (wt != T_Q8_0 ? (size_t)M * (K / 16) * 2 : 0) &&
-              pl.workspace >= pl.ws_w6 + (wt == T_Q6_K ? (size_t)N * (K / 256) * 240 : 0),
+              pl.ws_part % 256 == 0 && pl.ws_part >= pl.ws_w6 + (wt == T_Q6_K ? (size_t)N * (K / 256) * 240 : 0) &&
+              pl.ws_cnt % 256 == 0 && pl.ws_cnt >= pl.ws_part + (p.ks > 1 ? (size_t)p.ks * M * N * 4 : 0) &&
+              pl.workspace >= pl.ws_cnt + (p.ks > 1 ? (size_t)p.tiles * 4 : 0),
           CASE);
 #undef CASE
     return 1;
