@@ -90,11 +90,12 @@ struct TxRaw {
     // accumulators (drain units) per raw stage: Q8_0 one per block; Q4_K S_sc
     // and S_m; Q6_K S_a and S_b (S = 16 S_a + S_b)
     static constexpr int drains = WT == T_Q8_0 ? 8 : 2;
-    // block stages: Q4_K's smaller raw slots leave room for eight, which its
-    // lighter fold needs to keep the activation boxes' L2 latency covered
-    static constexpr int stages = WT == T_Q4_K ? 8 : 4;
-    static constexpr int wtiles = WT == T_Q6_K ? 2 : 1;        // weight-code tiles per block stage
-    static constexpr int stage = (wtiles + 1) * kTxW * 64;      // bytes of a block stage
+    static constexpr int wtiles = WT == T_Q6_K ? 2 : 1;  // weight-code tiles per block stage
+    // bytes of a block stage for tiles of nx activation rows (a multiple of 4 KB)
+    __host__ __device__ static constexpr int stage(int nx) { return wtiles * kTxW * 64 + nx * 64; }
+    // block stages: Q4_K's smaller raw slots leave room for eight, the others
+    // take four (more measured no faster at 64 or 128 activation rows)
+    __host__ __device__ static constexpr int stages(int) { return WT == T_Q4_K ? 8 : 4; }
 };
 static_assert(TxRaw<T_Q8_0>::slot % 1024 == 0 && TxRaw<T_Q4_K>::slot % 1024 == 0 && TxRaw<T_Q6_K>::slot % 1024 == 0,
               "1 KB aligned raw slots");
@@ -271,7 +272,8 @@ __global__ void __launch_bounds__(kTxThreads, 1)
     uint8_t* sm = smraw + ((1024 - (smem_u32(smraw) & 1023)) & 1023);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + p.off_bar);
-    constexpr int kTxS = R::stages;
+    constexpr int kTxS = R::stages(NX);
+    static_assert(kTxS <= kTxSMax, "block stages");
     uint64_t* full = bars;                       // [kTxS] activation codes landed and weight codes converted
     uint64_t* empty = full + kTxS;               // [kTxS] stage consumed by the MMAs (commit)
     uint64_t* r_full = empty + kTxS;             // [kTxRawMax] raw stage landed (TMA)
@@ -316,8 +318,8 @@ __global__ void __launch_bounds__(kTxThreads, 1)
     const uint32_t tmem = *tslot;
     grid_dep_wait();  // the activation-preparing grid has completed
 
-    auto wstage = [&](int s) { return sm + s * R::stage; };                           // A: weight codes (Q6_K: a q, then b q)
-    auto xstage = [&](int s) { return sm + s * R::stage + R::wtiles * kTxW * 64; };   // B: activation codes
+    auto wstage = [&](int s) { return sm + s * R::stage(NX); };                           // A: weight codes (Q6_K: a q, then b q)
+    auto xstage = [&](int s) { return sm + s * R::stage(NX) + R::wtiles * kTxW * 64; };   // B: activation codes
     auto raw = [&](int s) { return sm + p.off_raw + s * R::slot; };
 
     if (warp == 0) {
@@ -780,11 +782,11 @@ struct TcxPlan {
 inline int tcx_raw_slot(int wt) {
     return wt == T_Q8_0 ? TxRaw<T_Q8_0>::slot : wt == T_Q4_K ? TxRaw<T_Q4_K>::slot : TxRaw<T_Q6_K>::slot;
 }
-inline int tcx_stages(int wt) {
-    return wt == T_Q8_0 ? TxRaw<T_Q8_0>::stages : wt == T_Q4_K ? TxRaw<T_Q4_K>::stages : TxRaw<T_Q6_K>::stages;
+inline int tcx_stages(int wt, int nx) {
+    return wt == T_Q8_0 ? TxRaw<T_Q8_0>::stages(nx) : wt == T_Q4_K ? TxRaw<T_Q4_K>::stages(nx) : TxRaw<T_Q6_K>::stages(nx);
 }
-inline int tcx_stage_bytes(int wt) {
-    return wt == T_Q8_0 ? TxRaw<T_Q8_0>::stage : wt == T_Q4_K ? TxRaw<T_Q4_K>::stage : TxRaw<T_Q6_K>::stage;
+inline int tcx_stage_bytes(int wt, int nx) {
+    return wt == T_Q8_0 ? TxRaw<T_Q8_0>::stage(nx) : wt == T_Q4_K ? TxRaw<T_Q4_K>::stage(nx) : TxRaw<T_Q6_K>::stage(nx);
 }
 
 inline bool plan_tcx(int wt, long long M, long long N, long long K, int sm_count, int smem_max, TcxPlan& out) {
@@ -823,7 +825,7 @@ inline bool plan_tcx(int wt, long long M, long long N, long long K, int sm_count
         p.ks = best_ks;
     }
     p.units = p.tiles * p.ks;
-    p.off_raw = tcx_stages(wt) * tcx_stage_bytes(wt);
+    p.off_raw = tcx_stages(wt, pl.nx) * tcx_stage_bytes(wt, pl.nx);
     const int fixed = 512 + 1024;  // barriers, TMEM slot, flags; alignment slack
     p.nraw = (smem_max - p.off_raw - fixed) / tcx_raw_slot(wt);
     if (p.nraw > kTxRawMax) p.nraw = kTxRawMax;

@@ -139,7 +139,7 @@ int check_tcx(int wt, long long M, long long N, long long K) {
     const TcxParams& p = pl.p;
 #define CASE "tcx %s M%lld N%lld K%lld", tname(wt), M, N, K
     CHECK(pl.smem <= (size_t)kSmem && p.nraw >= 3 && p.nraw <= kTxRawMax, CASE);
-    CHECK(p.off_raw == tcx_stages(wt) * tcx_stage_bytes(wt) && p.off_raw % 1024 == 0 && tcx_raw_slot(wt) % 1024 == 0 &&
+    CHECK(p.off_raw == tcx_stages(wt, pl.nx) * tcx_stage_bytes(wt, pl.nx) && p.off_raw % 1024 == 0 && tcx_raw_slot(wt) % 1024 == 0 &&
               p.off_bar == p.off_raw + p.nraw * tcx_raw_slot(wt) && (size_t)p.off_bar + 512 + 1024 <= pl.smem,
           CASE);
     CHECK((pl.nx == 64 || pl.nx == kTxX) && (pl.nx == 64) == (M <= 64), CASE);
