@@ -30,16 +30,16 @@ cudaError_t tcx_go(const TcxPlan& pl, const void* wq, const float* x, void* ws, 
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    // 2. tensor maps: raw weight rows as uint16 (128 rows x 256 K); activation codes, 32 K x
-    //    NX rows, 64-byte swizzle; activation scales; (Q4_K) the sums of 16 codes, 16 x NX
+    // 2. tensor maps: raw weight rows as uint16 (128 rows x 256 K); activation codes, 64 K x
+    //    NX rows, 128-byte swizzle; activation scales; (Q4_K) the sums of 16 codes, 16 x NX
     //    rows, 32-byte swizzle
     CUtensorMap tw, ta, ts, tb;
     const unsigned long long rb = (unsigned long long)p0.K / 256 * R::row;
     const unsigned long long nsc = WT == T_Q8_0 ? p0.K / 32 : p0.K / 256;
     const void* wsrc = WT == T_Q6_K ? static_cast<const void*>(w6) : wq;
     bool ok = make_map(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT16, wsrc, rb / 2, p0.N, rb, R::row / 2, kTxW, CU_TENSOR_MAP_SWIZZLE_NONE) &&
-              make_map(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, codes, p0.K, p0.M, (unsigned long long)p0.K * 2, 32, NX,
-                       CU_TENSOR_MAP_SWIZZLE_64B) &&
+              make_map(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, codes, p0.K, p0.M, (unsigned long long)p0.K * 2, 64, NX,
+                       CU_TENSOR_MAP_SWIZZLE_128B) &&
               make_map(&ts, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, scales, pl.mp, nsc, (unsigned long long)pl.mp * 4, NX,
                        WT == T_Q8_0 ? 8 : 1, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (WT == T_Q4_K)

@@ -26,23 +26,25 @@
 // f32x2 arithmetic on the drained accumulators.
 //
 // One persistent CTA per SM over work units: an output tile of 128 weight
-// rows (MMA M, the TMEM lanes) x 128 activation rows (MMA N), all of K.
-// 22 warps:
+// rows (MMA M, the TMEM lanes) x NX = 64 or 128 activation rows (MMA N), over
+// all of K or, with few tiles, one of ks K slices.  Block stages hold two
+// 32-value blocks (64 K: 128-byte swizzled rows), so every handoff between
+// roles covers two blocks.  22 warps:
 //   producer   TMA: raw weight rows (2-D box of 128 rows x 256 K: 272 B of
 //              Q8_0, 144 B of Q4_K, a 240-byte slot of Q6_K) with that
 //              stretch's activation scales (prepared block-major) and, for
-//              Q4_K, the sums of 16 codes, into a raw ring; per block the
-//              activation codes (128 rows x 32 f16, 64-byte swizzle);
+//              Q4_K, the sums of 16 codes, into a raw ring; per block stage
+//              the activation codes (NX rows x 64 f16, 128-byte swizzle);
 //   MMA        one thread: per block two (Q6_K: four) tcgen05.mma (K 16)
-//              from shared memory into TMEM accumulators (four of 128
-//              columns in a ring), restarted per block or super-block;
-//   epilogue   16 warps, a TMEM lane quarter (32 weight rows) and 32 of the
-//              128 accumulator columns each: drain the sums, fold them with
-//              the weight scales (read from the raw stage) and the
-//              activation scales, keep the tile's running sums in
-//              registers, store y at the end;
-//   converter  4 warps, one weight row per thread: the block's 32 codes to
-//              exact f16, written to shared memory in the MMA's 64-byte
+//              from shared memory into TMEM accumulators (a ring of 512
+//              columns), restarted per block or super-block;
+//   epilogue   16 warps, a TMEM lane quarter (32 weight rows) and NX / 4
+//              accumulator columns each: drain the sums, fold them with the
+//              weight scales (read from the raw stage) and the activation
+//              scales, keep the tile's running sums in registers, store y
+//              (or a partial tile) at the end;
+//   converter  4 warps, one weight row per thread: each block's 32 codes to
+//              exact f16, written to shared memory in the MMA's 128-byte
 //              swizzled K-major layout.
 // A raw stage is released when its blocks are converted and folded.
 #pragma once
@@ -91,11 +93,11 @@ struct TxRaw {
     // and S_m; Q6_K S_a and S_b (S = 16 S_a + S_b)
     static constexpr int drains = WT == T_Q8_0 ? 8 : 2;
     static constexpr int wtiles = WT == T_Q6_K ? 2 : 1;  // weight-code tiles per block stage
-    // bytes of a block stage for tiles of nx activation rows (a multiple of 4 KB)
-    __host__ __device__ static constexpr int stage(int nx) { return wtiles * kTxW * 64 + nx * 64; }
-    // block stages: Q4_K's smaller raw slots leave room for eight, the others
-    // take four (more measured no faster at 64 or 128 activation rows)
-    __host__ __device__ static constexpr int stages(int) { return WT == T_Q4_K ? 8 : 4; }
+    // bytes of a block stage (two 32-value blocks: 128-byte rows) for tiles of
+    // nx activation rows (a multiple of 8 KB)
+    __host__ __device__ static constexpr int stage(int nx) { return wtiles * kTxW * 128 + nx * 128; }
+    // block stages: Q4_K's smaller raw slots leave room for four, the others take two
+    __host__ __device__ static constexpr int stages(int) { return WT == T_Q4_K ? 4 : 2; }
 };
 static_assert(TxRaw<T_Q8_0>::slot % 1024 == 0 && TxRaw<T_Q4_K>::slot % 1024 == 0 && TxRaw<T_Q6_K>::slot % 1024 == 0,
               "1 KB aligned raw slots");
@@ -136,6 +138,12 @@ __device__ __forceinline__ void tcx_ld8(uint32_t taddr, uint32_t r[8]) {
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
                  : "r"(taddr));
+}
+
+// shared-memory matrix descriptor: K-major, 128-byte swizzle (rows of 64 f16), 8-row atoms 1 KB apart
+__device__ __forceinline__ uint64_t tcx_sdesc128(uint32_t addr) {
+    return (uint64_t)((addr >> 4) & 0x3FFF) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) |
+           ((uint64_t)2 << 61);
 }
 
 // shared-memory matrix descriptor: K-major, 32-byte swizzle (rows of 16 f16), 8-row atoms 256 B apart
@@ -318,8 +326,8 @@ __global__ void __launch_bounds__(kTxThreads, 1)
     const uint32_t tmem = *tslot;
     grid_dep_wait();  // the activation-preparing grid has completed
 
-    auto wstage = [&](int s) { return sm + s * R::stage(NX); };                           // A: weight codes (Q6_K: a q, then b q)
-    auto xstage = [&](int s) { return sm + s * R::stage(NX) + R::wtiles * kTxW * 64; };   // B: activation codes
+    auto wstage = [&](int s) { return sm + s * R::stage(NX); };                            // A: weight codes (Q6_K: a q, then b q)
+    auto xstage = [&](int s) { return sm + s * R::stage(NX) + R::wtiles * kTxW * 128; };   // B: activation codes
     auto raw = [&](int s) { return sm + p.off_raw + s * R::slot; };
 
     if (warp == 0) {
@@ -357,12 +365,12 @@ __global__ void __launch_bounds__(kTxThreads, 1)
                             if (iu < p.units) tcx_slice(p, iu, itile, ir, ir1);
                         }
                     }
-                    for (int j = 0; j < 8 && ok; ++j, ++g) {
+                    for (int j = 0; j < 4 && ok; ++j, ++g) {  // block stages: blocks 2 j, 2 j + 1
                         const int s = (int)(g % kTxS);
                         if (g >= kTxS) ok = mbar_wait(smem_u32(&empty[s]), (uint32_t)(((g / kTxS) - 1) & 1), flags, p.err);
                         if (!ok) break;
-                        mbar_arrive_tx(smem_u32(&full[s]), (uint32_t)(NX * 64));
-                        tma_2d(smem_u32(xstage(s)), &ta, (r * 8 + j) * 32, m0, smem_u32(&full[s]));
+                        mbar_arrive_tx(smem_u32(&full[s]), (uint32_t)(NX * 128));
+                        tma_2d(smem_u32(xstage(s)), &ta, (r * 8 + 2 * j) * 32, m0, smem_u32(&full[s]));
                     }
                 }
             }
@@ -391,27 +399,34 @@ __global__ void __launch_bounds__(kTxThreads, 1)
                     uint32_t dcol = 0, dcol2 = 0;
                     if (WT != T_Q8_0) dcol = acc_take(du);                // S_sc (Q4_K), S_a (Q6_K)
                     if (WT == T_Q6_K && ok) dcol2 = acc_take(du + 1);    // S_b
-                    for (int j = 0; j < 8 && ok; ++j, ++g) {
+                    for (int j = 0; j < 4 && ok; ++j, ++g) {  // block stages: blocks 2 j, 2 j + 1
                         const int s = (int)(g % kTxS);
-                        if (WT == T_Q8_0) dcol = acc_take(du + j);
+                        uint32_t dcolb = 0;  // Q8_0: the second block's accumulator
+                        if (WT == T_Q8_0) {
+                            dcol = acc_take(du + 2 * j);
+                            if (ok) dcolb = acc_take(du + 2 * j + 1);
+                        }
                         if (!ok) break;
                         const uint32_t nxt = mbar_test(smem_u32(&full[(g + 1) % kTxS]), (uint32_t)(((g + 1) / kTxS) & 1));
                         if (!ready) ok = mbar_wait(smem_u32(&full[s]), (uint32_t)((g / kTxS) & 1), flags, p.err);
                         if (!ok) break;
                         tc_fence_after();
                         const uint32_t wa = smem_u32(wstage(s)), xb = smem_u32(xstage(s));
+                        // K = 16 steps ks = 0..3 at 32 bytes each along the 128-byte swizzled rows
 #pragma unroll
-                        for (int kk = 0; kk < 2; ++kk)
-                            tcx_mma(tmem + dcol, tc_sdesc(wa + 32 * kk), tc_sdesc(xb + 32 * kk), idesc,
-                                    WT == T_Q8_0 ? (uint32_t)kk : (uint32_t)(j | kk));
-                        if (WT == T_Q6_K) {
-#pragma unroll
-                            for (int kk = 0; kk < 2; ++kk)
-                                tcx_mma(tmem + dcol2, tc_sdesc(wa + kTxW * 64 + 32 * kk), tc_sdesc(xb + 32 * kk), idesc,
-                                        (uint32_t)(j | kk));
+                        for (int ks = 0; ks < 4; ++ks) {
+                            const uint32_t col = WT == T_Q8_0 && ks >= 2 ? dcolb : dcol;
+                            const uint32_t accu = WT == T_Q8_0 ? (uint32_t)(ks & 1) : (uint32_t)(j | ks);
+                            tcx_mma(tmem + col, tcx_sdesc128(wa + 32 * ks), tcx_sdesc128(xb + 32 * ks), idesc, accu);
+                            if (WT == T_Q6_K)
+                                tcx_mma(tmem + dcol2, tcx_sdesc128(wa + kTxW * 128 + 32 * ks), tcx_sdesc128(xb + 32 * ks), idesc,
+                                        accu);
                         }
                         tc_commit(smem_u32(&empty[s]));
-                        if (WT == T_Q8_0) tc_commit(smem_u32(&acc_full[(du + j) % kAcc]));
+                        if (WT == T_Q8_0) {
+                            tc_commit(smem_u32(&acc_full[(du + 2 * j) % kAcc]));
+                            tc_commit(smem_u32(&acc_full[(du + 2 * j + 1) % kAcc]));
+                        }
                         ready = nxt;
                     }
                     if (!ok) break;
@@ -602,8 +617,8 @@ __global__ void __launch_bounds__(kTxThreads, 1)
     } else {
         // ------------------------------ converters ------------------------------
         const int r = 32 * (warp - 2 - kTxEpiWarps) + lane;  // weight row of the tile
-        // this row's four 16-byte chunks in the 64-byte swizzled K-major layout
-        const int rbase = (r >> 3) * 512 + (r & 7) * 64, sw = (r >> 1) & 3;
+        // this row's eight 16-byte chunks (four per block) in the 128-byte swizzled K-major layout
+        const int rbase = (r >> 3) * 1024 + (r & 7) * 128, sw = r & 7;
         long long rg = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
@@ -634,9 +649,12 @@ __global__ void __launch_bounds__(kTxThreads, 1)
                 }
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    const long long g = rg * 8 + j;
+                    const long long g = rg * 4 + (j >> 1);  // block stage of blocks 2 (j / 2), 2 (j / 2) + 1
                     const int s = (int)(g % kTxS);
-                    if (g >= kTxS && !(ok = mbar_wait(smem_u32(&empty[s]), (uint32_t)(((g / kTxS) - 1) & 1), flags, p.err))) break;
+                    const int c0 = 4 * (j & 1);            // the block's first chunk in the 128-byte row
+                    if ((j & 1) == 0 && g >= kTxS &&
+                        !(ok = mbar_wait(smem_u32(&empty[s]), (uint32_t)(((g / kTxS) - 1) & 1), flags, p.err)))
+                        break;
                     uint32_t h[16];
                     if (WT == T_Q6_K) {
                         uint32_t h2[16];
@@ -648,10 +666,11 @@ __global__ void __launch_bounds__(kTxThreads, 1)
                         else if (j == 5) tcx_conv_q6_k<5>(wrow, h, h2);
                         else if (j == 6) tcx_conv_q6_k<6>(wrow, h, h2);
                         else tcx_conv_q6_k<7>(wrow, h, h2);
-                        uint8_t* a2 = wstage(s) + kTxW * 64 + rbase;
+                        uint8_t* a2 = wstage(s) + kTxW * 128 + rbase;
 #pragma unroll
                         for (int c = 0; c < 4; ++c)
-                            *reinterpret_cast<uint4*>(a2 + ((c ^ sw) << 4)) = make_uint4(h2[4 * c], h2[4 * c + 1], h2[4 * c + 2], h2[4 * c + 3]);
+                            *reinterpret_cast<uint4*>(a2 + (((c0 + c) ^ sw) << 4)) =
+                                make_uint4(h2[4 * c], h2[4 * c + 1], h2[4 * c + 2], h2[4 * c + 3]);
                     } else if (WT == T_Q8_0) {
                         if (j == 0) tcx_conv_q8_0<0>(wrow, h);
                         else if (j == 1) tcx_conv_q8_0<1>(wrow, h);
@@ -674,10 +693,12 @@ __global__ void __launch_bounds__(kTxThreads, 1)
                     uint8_t* a = wstage(s) + rbase;
 #pragma unroll
                     for (int c = 0; c < 4; ++c)
-                        *reinterpret_cast<uint4*>(a + ((c ^ sw) << 4)) = make_uint4(h[4 * c], h[4 * c + 1], h[4 * c + 2], h[4 * c + 3]);
-                    fence_proxy_async();  // the generic-proxy stores, before the tensor core reads them
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(smem_u32(&full[s]));
+                        *reinterpret_cast<uint4*>(a + (((c0 + c) ^ sw) << 4)) = make_uint4(h[4 * c], h[4 * c + 1], h[4 * c + 2], h[4 * c + 3]);
+                    if (j & 1) {
+                        fence_proxy_async();  // the generic-proxy stores, before the tensor core reads them
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(smem_u32(&full[s]));
+                    }
                 }
                 if (!ok) break;
                 __syncwarp();
