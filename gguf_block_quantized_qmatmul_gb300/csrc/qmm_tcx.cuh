@@ -93,11 +93,16 @@ struct TxRaw {
     // and S_m; Q6_K S_a and S_b (S = 16 S_a + S_b)
     static constexpr int drains = WT == T_Q8_0 ? 8 : 2;
     static constexpr int wtiles = WT == T_Q6_K ? 2 : 1;  // weight-code tiles per block stage
-    // bytes of a block stage (two 32-value blocks: 128-byte rows) for tiles of
-    // nx activation rows (a multiple of 8 KB)
-    __host__ __device__ static constexpr int stage(int nx) { return wtiles * kTxW * 128 + nx * 128; }
-    // block stages: Q4_K's smaller raw slots leave room for four, the others take two
-    __host__ __device__ static constexpr int stages(int) { return WT == T_Q4_K ? 4 : 2; }
+    // 32-value blocks per block stage (2 or 4): every handoff between the
+    // roles covers that many blocks.  A stage holds bps / 2 "atoms" of 64 K,
+    // each 128-byte swizzled rows: a weight tile of 128 rows and an
+    // activation tile of nx rows per atom.
+    __host__ __device__ static constexpr int bps(int nx) { return WT == T_Q4_K || (WT == T_Q8_0 && nx == 64) ? 4 : 2; }
+    __host__ __device__ static constexpr int atoms(int nx) { return bps(nx) / 2; }
+    __host__ __device__ static constexpr int wtile(int nx) { return atoms(nx) * kTxW * 128; }  // bytes of a weight tile
+    __host__ __device__ static constexpr int stage(int nx) { return wtiles * wtile(nx) + atoms(nx) * nx * 128; }
+    // block stages (a multiple of 8 KB each)
+    __host__ __device__ static constexpr int stages(int nx) { return WT == T_Q4_K && bps(nx) == 2 ? 4 : 2; }
 };
 static_assert(TxRaw<T_Q8_0>::slot % 1024 == 0 && TxRaw<T_Q4_K>::slot % 1024 == 0 && TxRaw<T_Q6_K>::slot % 1024 == 0,
               "1 KB aligned raw slots");
@@ -327,7 +332,9 @@ __global__ void __launch_bounds__(kTxThreads, 1)
     grid_dep_wait();  // the activation-preparing grid has completed
 
     auto wstage = [&](int s) { return sm + s * R::stage(NX); };                            // A: weight codes (Q6_K: a q, then b q)
-    auto xstage = [&](int s) { return sm + s * R::stage(NX) + R::wtiles * kTxW * 128; };   // B: activation codes
+    auto xstage = [&](int s) { return sm + s * R::stage(NX) + R::wtiles * R::wtile(NX); };  // B: activation codes
+    constexpr int kBps = R::bps(NX);        // blocks per block stage
+    constexpr int kSpr = 8 / kBps;          // block stages per raw stage
     auto raw = [&](int s) { return sm + p.off_raw + s * R::slot; };
 
     if (warp == 0) {
@@ -365,12 +372,15 @@ __global__ void __launch_bounds__(kTxThreads, 1)
                             if (iu < p.units) tcx_slice(p, iu, itile, ir, ir1);
                         }
                     }
-                    for (int j = 0; j < 4 && ok; ++j, ++g) {  // block stages: blocks 2 j, 2 j + 1
+                    for (int j = 0; j < kSpr && ok; ++j, ++g) {  // block stages: blocks kBps j ..
                         const int s = (int)(g % kTxS);
                         if (g >= kTxS) ok = mbar_wait(smem_u32(&empty[s]), (uint32_t)(((g / kTxS) - 1) & 1), flags, p.err);
                         if (!ok) break;
-                        mbar_arrive_tx(smem_u32(&full[s]), (uint32_t)(NX * 128));
-                        tma_2d(smem_u32(xstage(s)), &ta, (r * 8 + 2 * j) * 32, m0, smem_u32(&full[s]));
+                        mbar_arrive_tx(smem_u32(&full[s]), (uint32_t)(NX * 64 * kBps));
+#pragma unroll
+                        for (int a = 0; a < kBps / 2; ++a)  // one box of 64 K per atom
+                            tma_2d(smem_u32(xstage(s) + a * NX * 128), &ta, (r * 8 + kBps * j + 2 * a) * 32, m0,
+                                   smem_u32(&full[s]));
                     }
                 }
             }
@@ -399,12 +409,13 @@ __global__ void __launch_bounds__(kTxThreads, 1)
                     uint32_t dcol = 0, dcol2 = 0;
                     if (WT != T_Q8_0) dcol = acc_take(du);                // S_sc (Q4_K), S_a (Q6_K)
                     if (WT == T_Q6_K && ok) dcol2 = acc_take(du + 1);    // S_b
-                    for (int j = 0; j < 4 && ok; ++j, ++g) {  // block stages: blocks 2 j, 2 j + 1
+                    for (int j = 0; j < kSpr && ok; ++j, ++g) {  // block stages: blocks kBps j ..
                         const int s = (int)(g % kTxS);
-                        uint32_t dcolb = 0;  // Q8_0: the second block's accumulator
+                        uint32_t dq[kBps];  // Q8_0: the accumulator of each block of the stage
                         if (WT == T_Q8_0) {
-                            dcol = acc_take(du + 2 * j);
-                            if (ok) dcolb = acc_take(du + 2 * j + 1);
+#pragma unroll
+                            for (int b = 0; b < kBps; ++b)
+                                if (ok) dq[b] = acc_take(du + kBps * j + b);
                         }
                         if (!ok) break;
                         const uint32_t nxt = mbar_test(smem_u32(&full[(g + 1) % kTxS]), (uint32_t)(((g + 1) / kTxS) & 1));
@@ -412,20 +423,21 @@ __global__ void __launch_bounds__(kTxThreads, 1)
                         if (!ok) break;
                         tc_fence_after();
                         const uint32_t wa = smem_u32(wstage(s)), xb = smem_u32(xstage(s));
-                        // K = 16 steps ks = 0..3 at 32 bytes each along the 128-byte swizzled rows
+                        // K = 16 steps ks: atom ks / 4, 32 bytes each along its 128-byte swizzled rows
 #pragma unroll
-                        for (int ks = 0; ks < 4; ++ks) {
-                            const uint32_t col = WT == T_Q8_0 && ks >= 2 ? dcolb : dcol;
+                        for (int ks = 0; ks < 2 * kBps; ++ks) {
+                            const uint32_t col = WT == T_Q8_0 ? dq[ks >> 1] : dcol;
                             const uint32_t accu = WT == T_Q8_0 ? (uint32_t)(ks & 1) : (uint32_t)(j | ks);
-                            tcx_mma(tmem + col, tcx_sdesc128(wa + 32 * ks), tcx_sdesc128(xb + 32 * ks), idesc, accu);
+                            const uint32_t wk = wa + (ks >> 2) * kTxW * 128 + 32 * (ks & 3);
+                            const uint32_t xk = xb + (ks >> 2) * NX * 128 + 32 * (ks & 3);
+                            tcx_mma(tmem + col, tcx_sdesc128(wk), tcx_sdesc128(xk), idesc, accu);
                             if (WT == T_Q6_K)
-                                tcx_mma(tmem + dcol2, tcx_sdesc128(wa + kTxW * 128 + 32 * ks), tcx_sdesc128(xb + 32 * ks), idesc,
-                                        accu);
+                                tcx_mma(tmem + dcol2, tcx_sdesc128(wk + R::wtile(NX)), tcx_sdesc128(xk), idesc, accu);
                         }
                         tc_commit(smem_u32(&empty[s]));
                         if (WT == T_Q8_0) {
-                            tc_commit(smem_u32(&acc_full[(du + 2 * j) % kAcc]));
-                            tc_commit(smem_u32(&acc_full[(du + 2 * j + 1) % kAcc]));
+#pragma unroll
+                            for (int b = 0; b < kBps; ++b) tc_commit(smem_u32(&acc_full[(du + kBps * j + b) % kAcc]));
                         }
                         ready = nxt;
                     }
@@ -649,10 +661,12 @@ __global__ void __launch_bounds__(kTxThreads, 1)
                 }
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    const long long g = rg * 4 + (j >> 1);  // block stage of blocks 2 (j / 2), 2 (j / 2) + 1
+                    const long long g = rg * kSpr + j / kBps;  // the block's stage
                     const int s = (int)(g % kTxS);
-                    const int c0 = 4 * (j & 1);            // the block's first chunk in the 128-byte row
-                    if ((j & 1) == 0 && g >= kTxS &&
+                    const int b = j % kBps;                       // its place in the stage
+                    const int c0 = 4 * (b & 1);                   // its first chunk in the atom's 128-byte row
+                    const int ab = (b >> 1) * kTxW * 128;         // its atom
+                    if (b == 0 && g >= kTxS &&
                         !(ok = mbar_wait(smem_u32(&empty[s]), (uint32_t)(((g / kTxS) - 1) & 1), flags, p.err)))
                         break;
                     uint32_t h[16];
@@ -666,7 +680,7 @@ __global__ void __launch_bounds__(kTxThreads, 1)
                         else if (j == 5) tcx_conv_q6_k<5>(wrow, h, h2);
                         else if (j == 6) tcx_conv_q6_k<6>(wrow, h, h2);
                         else tcx_conv_q6_k<7>(wrow, h, h2);
-                        uint8_t* a2 = wstage(s) + kTxW * 128 + rbase;
+                        uint8_t* a2 = wstage(s) + R::wtile(NX) + ab + rbase;
 #pragma unroll
                         for (int c = 0; c < 4; ++c)
                             *reinterpret_cast<uint4*>(a2 + (((c0 + c) ^ sw) << 4)) =
@@ -690,11 +704,11 @@ __global__ void __launch_bounds__(kTxThreads, 1)
                         else if (j == 6) tcx_conv_q4_k<6>(wrow, h);
                         else tcx_conv_q4_k<7>(wrow, h);
                     }
-                    uint8_t* a = wstage(s) + rbase;
+                    uint8_t* a = wstage(s) + ab + rbase;
 #pragma unroll
                     for (int c = 0; c < 4; ++c)
                         *reinterpret_cast<uint4*>(a + (((c0 + c) ^ sw) << 4)) = make_uint4(h[4 * c], h[4 * c + 1], h[4 * c + 2], h[4 * c + 3]);
-                    if (j & 1) {
+                    if (b == kBps - 1) {
                         fence_proxy_async();  // the generic-proxy stores, before the tensor core reads them
                         __syncwarp();
                         if (lane == 0) mbar_arrive(smem_u32(&full[s]));
