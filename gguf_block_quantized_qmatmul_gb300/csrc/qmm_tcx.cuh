@@ -259,17 +259,30 @@ __device__ __forceinline__ float tcx_block_scale(const uint8_t* row, int j) {
 // K split: y of a tile (rows m0.., n0..) as the sum of its ks partial tiles in
 // slice order, by the tile's last unit; thread t of the 16 epilogue warps
 // takes column n0 + t % 128 and every fourth row from t / 128 (stores
-// coalesced along N)
+// coalesced along N), four rows' loads of a slice in flight at a time
 template <int NX>
-__device__ __forceinline__ void tcx_fixup(const TcxParams& p, int t, int m0, int n0) {
+__device__ __forceinline__ void tcx_fixup(const float* __restrict__ part, float* __restrict__ y, int M, int N, int ks,
+                                          int t, int m0, int n0) {
     const int n = n0 + (t & (kTxW - 1));
-    if (n >= p.N) return;
-    const size_t slice = (size_t)p.M * p.N;
-    for (int mr = t >> 7; mr < NX && m0 + mr < p.M; mr += kTxEpiWarps * 32 / kTxW) {
-        const float* src = p.part + (size_t)(m0 + mr) * p.N + n;
-        float sum = __ldcg(src);
-        for (int k = 1; k < p.ks; ++k) sum += __ldcg(src + k * slice);
-        p.y[(size_t)(m0 + mr) * p.N + n] = sum;
+    if (n >= N) return;
+    const int r0 = t >> 7;
+    const size_t slice = (size_t)M * N;
+    for (int c = 0; c < NX / 4; c += 4) {
+        float sum[4];
+        for (int k = 0; k < ks; ++k) {
+            const float* src = part + k * slice + n;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int m = m0 + r0 + 4 * (c + i);
+                const float v = m < M ? __ldcg(src + (size_t)m * N) : 0.0f;
+                sum[i] = k == 0 ? v : sum[i] + v;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int m = m0 + r0 + 4 * (c + i);
+            if (m < M) y[(size_t)m * N + n] = sum[i];
+        }
     }
 }
 
@@ -622,7 +635,7 @@ __global__ void __launch_bounds__(kTxThreads, 1)
                 if (!(ok = mbar_wait(smem_u32(fix_ready), fix, flags, p.err))) break;
                 if (flags[1]) {
                     __threadfence();
-                    tcx_fixup<NX>(p, ew * 32 + lane, m0, n0);
+                    tcx_fixup<NX>(p.part, p.y, p.M, p.N, p.ks, ew * 32 + lane, m0, n0);
                 }
             }
         }
@@ -843,8 +856,10 @@ inline bool plan_tcx(int wt, long long M, long long N, long long K, int sm_count
     p.nrs = (int)(K / 256);
     // K slices: with few tiles, the smallest ks whose busiest CTA (units dealt
     // round-robin, one CTA per SM) carries the fewest raw stages, counting a
-    // unit's start and, for a split tile's last unit, its sum of ks partials
-    // as about half a stage each
+    // unit's start as half a stage and a split unit's partial tile, arrival
+    // and share of the sum of partials as three (measured: the 112 and 224
+    // tiles of 14336 weight rows at M <= 64 and M = 256 run fastest unsplit,
+    // the 32 and 64 of 4096 rows fastest in 4 and 2 slices)
     {
         double best = 0.0;
         int best_ks = 1;
@@ -853,7 +868,7 @@ inline bool plan_tcx(int wt, long long M, long long N, long long K, int sm_count
             const long long units = (long long)p.tiles * ks;
             const long long grid = units < sm_count ? units : sm_count;
             const long long per = (units + grid - 1) / grid;  // units of the busiest CTA
-            const double stages = (double)p.nrs / ks + 0.5 + (ks > 1 ? 0.5 * ks / 4.0 : 0.0);
+            const double stages = (double)p.nrs / ks + (ks > 1 ? 3.0 : 0.5);
             const double worst = per * stages;
             if (ks == 1 || worst < best * 0.98) best = worst, best_ks = ks;
         }
