@@ -1,6 +1,8 @@
 // qmm_tcx.cuh -- the CPU form's prefill GEMM (int8_act, M > 16 activation
 // rows; Q8_0, Q4_K and Q6_K weights) on the 5th-generation tensor cores with
-// exact per-block sums.
+// exact per-block sums; the same GEMM of exact weight codes also serves the
+// Metal form (f32_act) for Q4_K up to 64 rows, with each activation row split
+// into two f16 pieces (see TxRaw).
 //
 // "同一个 GGUF，CPU 和 Metal 生成的文字不一样" section 出处: the CPU form
 // quantizes every activation row (Q8_0, or Q8K for K-quant weights) and
@@ -76,18 +78,27 @@ constexpr int kTxThreads = (2 + kTxEpiWarps + kTxConvWarps) * 32;
 // A block stage holds the block's weight codes (Q6_K: two tiles, a_g q and
 // b_g q, for the group scales split as sc_g = 16 a_g + b_g) and the 128
 // activation rows' codes.
-template <int WT>
+// The f32_act form (Q4_K only, AM = A_F32) takes the same weight codes and
+// each activation row scaled by a power of two and split into two f16 pieces,
+// x 2^s = hi + lo: two MMAs per K step into one accumulator, and the min
+// term's sums of 16 values in two pieces as well; the fold needs no
+// activation scale per super-block (2^-s is applied at the store).
+template <int WT, int AM = A_INT8>
 struct TxRaw {
+    static_assert(AM == A_INT8 || WT == T_Q4_K, "the f32_act form: Q4_K");
+    static constexpr int pieces = AM == A_F32 ? 2 : 1;                             // activation pieces
     static constexpr int row = WT == T_Q8_0 ? 272 : WT == T_Q4_K ? 144 : 240;
-    static constexpr int scales = kTxW * row;                                      // f(d_a)
-    static constexpr int bsum = WT == T_Q4_K ? scales + 1024 : 0;                  // Q4_K: [128][16] f16
-    static constexpr int amin = WT == T_Q4_K ? bsum + kTxX * 32 : 0;              // Q4_K: [128][16] f16
+    static constexpr int scales = kTxW * row;                                      // f(d_a) (int8_act)
+    static constexpr int bsum = WT == T_Q4_K ? scales + 1024 : 0;                  // Q4_K: pieces x [128][16] f16
+    static constexpr int amin = WT == T_Q4_K ? bsum + pieces * kTxX * 32 : 0;     // Q4_K: [128][16] f16
     static constexpr int slot = WT == T_Q8_0 ? (scales + 8 * kTxX * 4 + 1023) / 1024 * 1024
                                 : WT == T_Q4_K ? amin + kTxW * 32
                                                : (scales + kTxX * 4 + 1023) / 1024 * 1024;
     // bytes a raw stage's copies bring, for tiles of nx activation rows
     __host__ __device__ static constexpr int tx(int nx) {
-        return WT == T_Q8_0 ? kTxW * row + 8 * nx * 4 : WT == T_Q4_K ? kTxW * row + nx * 4 + nx * 32 : kTxW * row + nx * 4;
+        return WT == T_Q8_0   ? kTxW * row + 8 * nx * 4
+               : WT == T_Q4_K ? kTxW * row + (AM == A_F32 ? 0 : nx * 4) + pieces * nx * 32
+                              : kTxW * row + nx * 4;
     }
     // accumulators (drain units) per raw stage: Q8_0 one per block; Q4_K S_sc
     // and S_m; Q6_K S_a and S_b (S = 16 S_a + S_b)
@@ -97,19 +108,24 @@ struct TxRaw {
     // roles covers that many blocks.  A stage holds bps / 2 "atoms" of 64 K,
     // each 128-byte swizzled rows: a weight tile of 128 rows and an
     // activation tile of nx rows per atom.
-    __host__ __device__ static constexpr int bps(int nx) { return WT == T_Q4_K || (WT == T_Q8_0 && nx == 64) ? 4 : 2; }
+    __host__ __device__ static constexpr int bps(int nx) {
+        return AM == A_F32 ? (nx == 64 ? 4 : 2) : WT == T_Q4_K || (WT == T_Q8_0 && nx == 64) ? 4 : 2;
+    }
     __host__ __device__ static constexpr int atoms(int nx) { return bps(nx) / 2; }
     __host__ __device__ static constexpr int wtile(int nx) { return atoms(nx) * kTxW * 128; }  // bytes of a weight tile
-    __host__ __device__ static constexpr int stage(int nx) { return wtiles * wtile(nx) + atoms(nx) * nx * 128; }
+    // activation tiles: piece p of atom a at p atoms(nx) + a
+    __host__ __device__ static constexpr int stage(int nx) { return wtiles * wtile(nx) + pieces * atoms(nx) * nx * 128; }
     // block stages (a multiple of 8 KB each)
-    __host__ __device__ static constexpr int stages(int nx) { return WT == T_Q4_K && bps(nx) == 2 ? 4 : 2; }
+    __host__ __device__ static constexpr int stages(int nx) { return AM == A_INT8 && WT == T_Q4_K && bps(nx) == 2 ? 4 : 2; }
 };
-static_assert(TxRaw<T_Q8_0>::slot % 1024 == 0 && TxRaw<T_Q4_K>::slot % 1024 == 0 && TxRaw<T_Q6_K>::slot % 1024 == 0,
+static_assert(TxRaw<T_Q8_0>::slot % 1024 == 0 && TxRaw<T_Q4_K>::slot % 1024 == 0 && TxRaw<T_Q6_K>::slot % 1024 == 0 &&
+                  TxRaw<T_Q4_K, A_F32>::slot % 1024 == 0,
               "1 KB aligned raw slots");
 
 struct TcxParams {
     float* y;
     unsigned* err;
+    const float* ais;  // f32_act: 2^-s per activation row
     float* part;    // partial tiles [ks][M][N] when K is split
     unsigned* cnt;  // per-tile arrival counters when K is split (zeroed by the activation launch)
     int M, N, K;
@@ -286,11 +302,15 @@ __device__ __forceinline__ void tcx_fixup(const float* __restrict__ part, float*
     }
 }
 
-template <int WT, int NX>  // T_Q8_0, T_Q4_K or T_Q6_K; tiles of NX = 64 or 128 activation rows
+// tensor maps: tw raw weight rows; ta activation codes (f32_act: the hi pieces); ts
+// int8_act: activation scales, f32_act: the lo pieces; tb Q4_K: sums of 16 codes
+// (f32_act: hi sums, then lo sums, along each row)
+template <int WT, int NX, int AM>  // T_Q8_0, T_Q4_K or T_Q6_K; tiles of NX = 64 or 128 activation rows; A_INT8 or A_F32
 __global__ void __launch_bounds__(kTxThreads, 1)
     qmm_tcx_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUtensorMap ta,
                    const __grid_constant__ CUtensorMap ts, const __grid_constant__ CUtensorMap tb, const TcxParams p) {
-    using R = TxRaw<WT>;
+    using R = TxRaw<WT, AM>;
+    constexpr bool kF32 = AM == A_F32;
     static_assert(NX == 64 || NX == 128, "tile widths");
     constexpr int kAcc = kTxTmemCols / NX;  // TMEM accumulators
     constexpr int CW = NX / 4;              // accumulator columns an epilogue warp drains
@@ -373,7 +393,10 @@ __global__ void __launch_bounds__(kTxThreads, 1)
                         const uint32_t fb = smem_u32(&r_full[rs]);
                         mbar_arrive_tx(fb, (uint32_t)R::tx(NX));
                         tma_2d(smem_u32(raw(rs)), &tw, ir * (R::row / 2), in0, fb);
-                        if (WT == T_Q8_0) {
+                        if (kF32) {
+                            tma_2d(smem_u32(raw(rs) + R::bsum), &tb, 16 * ir, im0, fb);
+                            tma_2d(smem_u32(raw(rs) + R::bsum + kTxX * 32), &tb, p.K / 16 + 16 * ir, im0, fb);
+                        } else if (WT == T_Q8_0) {
                             tma_2d(smem_u32(raw(rs) + R::scales), &ts, im0, 8 * ir, fb);
                         } else {
                             tma_2d(smem_u32(raw(rs) + R::scales), &ts, im0, ir, fb);
@@ -389,11 +412,15 @@ __global__ void __launch_bounds__(kTxThreads, 1)
                         const int s = (int)(g % kTxS);
                         if (g >= kTxS) ok = mbar_wait(smem_u32(&empty[s]), (uint32_t)(((g / kTxS) - 1) & 1), flags, p.err);
                         if (!ok) break;
-                        mbar_arrive_tx(smem_u32(&full[s]), (uint32_t)(NX * 64 * kBps));
+                        mbar_arrive_tx(smem_u32(&full[s]), (uint32_t)(R::pieces * NX * 64 * kBps));
 #pragma unroll
-                        for (int a = 0; a < kBps / 2; ++a)  // one box of 64 K per atom
+                        for (int a = 0; a < kBps / 2; ++a) {  // one box of 64 K per atom (and piece)
                             tma_2d(smem_u32(xstage(s) + a * NX * 128), &ta, (r * 8 + kBps * j + 2 * a) * 32, m0,
                                    smem_u32(&full[s]));
+                            if (kF32)
+                                tma_2d(smem_u32(xstage(s) + (kBps / 2 + a) * NX * 128), &ts, (r * 8 + kBps * j + 2 * a) * 32, m0,
+                                       smem_u32(&full[s]));
+                        }
                     }
                 }
             }
@@ -444,6 +471,8 @@ __global__ void __launch_bounds__(kTxThreads, 1)
                             const uint32_t wk = wa + (ks >> 2) * kTxW * 128 + 32 * (ks & 3);
                             const uint32_t xk = xb + (ks >> 2) * NX * 128 + 32 * (ks & 3);
                             tcx_mma(tmem + col, tcx_sdesc128(wk), tcx_sdesc128(xk), idesc, accu);
+                            if (kF32)  // the lo piece into the same accumulator
+                                tcx_mma(tmem + col, tcx_sdesc128(wk), tcx_sdesc128(xk + (kBps / 2) * NX * 128), idesc, 1u);
                             if (WT == T_Q6_K)
                                 tcx_mma(tmem + dcol2, tcx_sdesc128(wk + R::wtile(NX)), tcx_sdesc128(xk), idesc, accu);
                         }
@@ -469,6 +498,9 @@ __global__ void __launch_bounds__(kTxThreads, 1)
                         tc_fence_after();
                         tcx_mma(tmem + mcol, tcx_sdesc32(smem_u32(raw(rs) + R::amin)), tcx_sdesc32(smem_u32(raw(rs) + R::bsum)),
                                 idesc, 0u);
+                        if (kF32)
+                            tcx_mma(tmem + mcol, tcx_sdesc32(smem_u32(raw(rs) + R::amin)),
+                                    tcx_sdesc32(smem_u32(raw(rs) + R::bsum + kTxX * 32)), idesc, 1u);
                         tc_commit(smem_u32(&acc_full[(du + 1) % kAcc]));
                     }
                     du += R::drains;
@@ -575,7 +607,9 @@ __global__ void __launch_bounds__(kTxThreads, 1)
                     tc_fence_after();
                     __syncwarp();
                     const uint32_t dd = *reinterpret_cast<const uint32_t*>(wrow);  // f16 d, f16 dmin
-                    const unsigned long long fd2 = f2pack(h2f(dd), h2f(dd)), fm2 = f2pack(-h2f(dd >> 16), -h2f(dd >> 16));
+                    // f32_act: the min operand holds the sums of 16 over 16 (they fit f16), so f(dmin) 16
+                    const float fm = -h2f(dd >> 16) * (kF32 ? 16.0f : 1.0f);
+                    const unsigned long long fd2 = f2pack(h2f(dd), h2f(dd)), fm2 = f2pack(fm, fm);
 #pragma unroll
                     for (int h = 0; h < CW / 8; ++h) {  // 8 columns at a time: the running sums hold 2 CW registers
                         uint32_t vs[8], vm[8];
@@ -584,15 +618,26 @@ __global__ void __launch_bounds__(kTxThreads, 1)
                         tc_wait_ld();
 #pragma unroll
                         for (int c = 0; c < 2; ++c) {
-                            const float4 a4 = *reinterpret_cast<const float4*>(asc + 8 * h + 4 * c);
+                            if constexpr (kF32) {
+                                // y 2^s += f(d) S_sc - f(dmin) S_m (sums of x 2^s, 2^-s applied at the store)
 #pragma unroll
-                            for (int e = 0; e < 2; ++e) {
-                                const int i = 4 * c + 2 * e;
-                                const unsigned long long t =
-                                    fma2(f2pack(__uint_as_float(vs[i]), __uint_as_float(vs[i + 1])), fd2,
-                                         mul2(f2pack(__uint_as_float(vm[i]), __uint_as_float(vm[i + 1])), fm2));
-                                const unsigned long long a2 = e ? f2pack(a4.z, a4.w) : f2pack(a4.x, a4.y);
-                                acc[4 * h + 2 * c + e] = fma2(t, a2, acc[4 * h + 2 * c + e]);
+                                for (int e = 0; e < 2; ++e) {
+                                    const int i = 4 * c + 2 * e;
+                                    unsigned long long& a = acc[4 * h + 2 * c + e];
+                                    a = fma2(f2pack(__uint_as_float(vs[i]), __uint_as_float(vs[i + 1])), fd2, a);
+                                    a = fma2(f2pack(__uint_as_float(vm[i]), __uint_as_float(vm[i + 1])), fm2, a);
+                                }
+                            } else {
+                                const float4 a4 = *reinterpret_cast<const float4*>(asc + 8 * h + 4 * c);
+#pragma unroll
+                                for (int e = 0; e < 2; ++e) {
+                                    const int i = 4 * c + 2 * e;
+                                    const unsigned long long t =
+                                        fma2(f2pack(__uint_as_float(vs[i]), __uint_as_float(vs[i + 1])), fd2,
+                                             mul2(f2pack(__uint_as_float(vm[i]), __uint_as_float(vm[i + 1])), fm2));
+                                    const unsigned long long a2 = e ? f2pack(a4.z, a4.w) : f2pack(a4.x, a4.y);
+                                    acc[4 * h + 2 * c + e] = fma2(t, a2, acc[4 * h + 2 * c + e]);
+                                }
                             }
                         }
                     }
@@ -613,8 +658,8 @@ __global__ void __launch_bounds__(kTxThreads, 1)
 #pragma unroll
                 for (int i = 0; i < CW / 2; ++i) {
                     const int m = m0 + CW * cq + 2 * i;
-                    if (m < p.M) dst[(size_t)m * p.N + n] = f2lo(acc[i]);
-                    if (m + 1 < p.M) dst[(size_t)(m + 1) * p.N + n] = f2hi(acc[i]);
+                    if (m < p.M) dst[(size_t)m * p.N + n] = kF32 ? f2lo(acc[i]) * __ldg(p.ais + m) : f2lo(acc[i]);
+                    if (m + 1 < p.M) dst[(size_t)(m + 1) * p.N + n] = kF32 ? f2hi(acc[i]) * __ldg(p.ais + m + 1) : f2hi(acc[i]);
                 }
             }
             if (p.ks > 1) {
@@ -797,6 +842,79 @@ __global__ void tcx_act_kernel(const float* __restrict__ x, int M, int K, int mp
     }
 }
 
+// The f32_act operand (Q4_K), written once per call: one 256-thread block per
+// activation row m finds the row's largest magnitude, takes 2^s with
+// max |x| 2^s in [2^14, 2^15) and splits every value exactly into two f16
+// pieces, x 2^s = hi + lo (hi[m][K], lo[m][K]); each 16 values' sum of x 2^s,
+// over 16 (at most 2^15, so it fits f16), is split the same way into
+// bsums[m][K / 16 + j] after the hi sums bsums[m][j]; ais[m] = 2^-s.  It also
+// zeroes the GEMM's ncnt split-K arrival counters.
+template <int WT>  // T_Q4_K
+__global__ void tcx_act_f32_kernel(const float* __restrict__ x, int M, int K, __half* __restrict__ hi, __half* __restrict__ lo,
+                                   __half* __restrict__ bsums, float* __restrict__ ais, unsigned* __restrict__ cnt, int ncnt) {
+    grid_dep_launch();
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < ncnt; i += (long long)gridDim.x * blockDim.x)
+        cnt[i] = 0u;
+    __shared__ float red[32];
+    const int m = blockIdx.x, tid = threadIdx.x;
+    if (m >= M) return;
+    const float* xr = x + (long long)m * K;
+    float amax = 0.0f;
+    for (int k = 4 * tid; k < K; k += 4 * blockDim.x) {
+        const float4 v = __ldg(reinterpret_cast<const float4*>(xr + k));
+        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    if ((tid & 31) == 0) red[tid >> 5] = amax;
+    __syncthreads();
+    if (tid < 32) {
+        float a = tid < (int)(blockDim.x >> 5) ? red[tid] : 0.0f;
+#pragma unroll
+        for (int o = 16; o; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+        if (tid == 0) red[0] = a;
+    }
+    __syncthreads();
+    const float is = tc_row_iscale(red[0]);
+    const float sc = __frcp_rn(is);  // 2^s, exact
+    if (tid == 0) ais[m] = is;
+    __half* hr = hi + (long long)m * K;
+    __half* lr = lo + (long long)m * K;
+    __half* br = bsums + (long long)m * (K / 8);
+    for (int g = tid; g < K / 16; g += blockDim.x) {  // 16 values per thread
+        const float4* src = reinterpret_cast<const float4*>(xr + 16 * g);
+        uint32_t hw[8], lw[8];
+        float sum = 0.0f;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float4 v4 = __ldg(src + q);
+            const float v[4] = {v4.x * sc, v4.y * sc, v4.z * sc, v4.w * sc};
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const __half2 h2 = __floats2half2_rn(v[2 * e], v[2 * e + 1]);
+                const float2 hf = __half22float2(h2);
+                const __half2 l2 = __floats2half2_rn(v[2 * e] - hf.x, v[2 * e + 1] - hf.y);
+                hw[2 * q + e] = *reinterpret_cast<const uint32_t*>(&h2);
+                lw[2 * q + e] = *reinterpret_cast<const uint32_t*>(&l2);
+            }
+            sum += v[0];
+            sum += v[1];
+            sum += v[2];
+            sum += v[3];
+        }
+        uint4* ho = reinterpret_cast<uint4*>(hr + 16 * g);
+        uint4* lo4 = reinterpret_cast<uint4*>(lr + 16 * g);
+        ho[0] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        ho[1] = make_uint4(hw[4], hw[5], hw[6], hw[7]);
+        lo4[0] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        lo4[1] = make_uint4(lw[4], lw[5], lw[6], lw[7]);
+        const float s16 = sum * 0.0625f;  // exact
+        const __half sh = __float2half_rn(s16);
+        br[g] = sh;
+        br[K / 16 + g] = __float2half_rn(s16 - __half2float(sh));
+    }
+}
+
 // Q6_K: every 210-byte super-block copied into a 240-byte slot (rows of K / 256
 // slots), 16-byte aligned for the GEMM's tensor map; one warp per weight row,
 // 2-byte words
@@ -820,28 +938,38 @@ __global__ void tcx_q6_repack_kernel(const uint8_t* __restrict__ wq, int N, int 
 // ---------------------------------------------------------------------------
 struct TcxPlan {
     TcxParams p;
+    int am;  // A_INT8 (exact block sums) or A_F32 (Q4_K: two activation pieces)
     int nx;  // activation rows per tile: 64 or 128
     int grid;
     size_t smem;
     int mp;  // activation scale rows: M rounded up to 4 (16-byte rows for the tensor map)
-    size_t ws_codes, ws_scales, ws_bsums, ws_w6, ws_part, ws_cnt, workspace;
+    // workspace: activation codes (f32_act: the hi pieces), int8_act scales or f32_act lo
+    // pieces, Q4_K sums of 16, f32_act 2^-s per row, Q6_K repacked weights, split-K partials
+    // and counters
+    size_t ws_codes, ws_scales, ws_bsums, ws_ais, ws_w6, ws_part, ws_cnt, workspace;
 };
 
-inline int tcx_raw_slot(int wt) {
-    return wt == T_Q8_0 ? TxRaw<T_Q8_0>::slot : wt == T_Q4_K ? TxRaw<T_Q4_K>::slot : TxRaw<T_Q6_K>::slot;
+inline int tcx_raw_slot(int wt, int am) {
+    return am == A_F32 ? TxRaw<T_Q4_K, A_F32>::slot
+                       : wt == T_Q8_0 ? TxRaw<T_Q8_0>::slot : wt == T_Q4_K ? TxRaw<T_Q4_K>::slot : TxRaw<T_Q6_K>::slot;
 }
-inline int tcx_stages(int wt, int nx) {
-    return wt == T_Q8_0 ? TxRaw<T_Q8_0>::stages(nx) : wt == T_Q4_K ? TxRaw<T_Q4_K>::stages(nx) : TxRaw<T_Q6_K>::stages(nx);
+inline int tcx_stages(int wt, int am, int nx) {
+    return am == A_F32 ? TxRaw<T_Q4_K, A_F32>::stages(nx)
+                       : wt == T_Q8_0 ? TxRaw<T_Q8_0>::stages(nx)
+                                      : wt == T_Q4_K ? TxRaw<T_Q4_K>::stages(nx) : TxRaw<T_Q6_K>::stages(nx);
 }
-inline int tcx_stage_bytes(int wt, int nx) {
-    return wt == T_Q8_0 ? TxRaw<T_Q8_0>::stage(nx) : wt == T_Q4_K ? TxRaw<T_Q4_K>::stage(nx) : TxRaw<T_Q6_K>::stage(nx);
+inline int tcx_stage_bytes(int wt, int am, int nx) {
+    return am == A_F32 ? TxRaw<T_Q4_K, A_F32>::stage(nx)
+                       : wt == T_Q8_0 ? TxRaw<T_Q8_0>::stage(nx)
+                                      : wt == T_Q4_K ? TxRaw<T_Q4_K>::stage(nx) : TxRaw<T_Q6_K>::stage(nx);
 }
 
-inline bool plan_tcx(int wt, long long M, long long N, long long K, int sm_count, int smem_max, TcxPlan& out) {
-    if ((wt != T_Q8_0 && wt != T_Q4_K && wt != T_Q6_K) || K % 256 != 0 || M < 17 || K > (1 << 26) || M > (1 << 24) ||
-        N > (1 << 24))
+inline bool plan_tcx(int wt, int am, long long M, long long N, long long K, int sm_count, int smem_max, TcxPlan& out) {
+    if ((wt != T_Q8_0 && wt != T_Q4_K && wt != T_Q6_K) || (am == A_F32 && wt != T_Q4_K) || K % 256 != 0 || M < 17 ||
+        K > (1 << 26) || M > (1 << 24) || N > (1 << 24))
         return false;
     TcxPlan pl{};
+    pl.am = am;
     TcxParams& p = pl.p;
     p.M = (int)M;
     p.N = (int)N;
@@ -875,12 +1003,12 @@ inline bool plan_tcx(int wt, long long M, long long N, long long K, int sm_count
         p.ks = best_ks;
     }
     p.units = p.tiles * p.ks;
-    p.off_raw = tcx_stages(wt, pl.nx) * tcx_stage_bytes(wt, pl.nx);
+    p.off_raw = tcx_stages(wt, am, pl.nx) * tcx_stage_bytes(wt, am, pl.nx);
     const int fixed = 512 + 1024;  // barriers, TMEM slot, flags; alignment slack
-    p.nraw = (smem_max - p.off_raw - fixed) / tcx_raw_slot(wt);
+    p.nraw = (smem_max - p.off_raw - fixed) / tcx_raw_slot(wt, am);
     if (p.nraw > kTxRawMax) p.nraw = kTxRawMax;
     if (p.nraw < 3) return false;  // the epilogue holds a raw stage while the converters fill the next
-    p.off_bar = p.off_raw + p.nraw * tcx_raw_slot(wt);
+    p.off_bar = p.off_raw + p.nraw * tcx_raw_slot(wt, am);
     pl.smem = (size_t)p.off_bar + fixed;
     pl.grid = p.units < sm_count ? p.units : sm_count;
     pl.mp = (int)((M + 3) / 4 * 4);
@@ -888,8 +1016,9 @@ inline bool plan_tcx(int wt, long long M, long long N, long long K, int sm_count
     pl.ws_codes = 0;
     pl.ws_scales = r256((size_t)M * K * 2);
     const size_t per = wt == T_Q8_0 ? 32 : 256;  // values per activation scale
-    pl.ws_bsums = pl.ws_scales + r256((size_t)(K / per) * pl.mp * 4);
-    pl.ws_w6 = pl.ws_bsums + (wt != T_Q8_0 ? r256((size_t)M * (K / 16) * 2) : 0);
+    pl.ws_bsums = pl.ws_scales + (am == A_F32 ? r256((size_t)M * K * 2) : r256((size_t)(K / per) * pl.mp * 4));
+    pl.ws_ais = pl.ws_bsums + (wt != T_Q8_0 ? r256((size_t)M * (K / 16) * 2 * (am == A_F32 ? 2 : 1)) : 0);
+    pl.ws_w6 = pl.ws_ais + (am == A_F32 ? r256((size_t)M * 4) : 0);
     pl.ws_part = pl.ws_w6 + (wt == T_Q6_K ? r256((size_t)N * (K / 256) * TxRaw<T_Q6_K>::row) : 0);
     pl.ws_cnt = pl.ws_part + (p.ks > 1 ? r256((size_t)p.ks * M * N * 4) : 0);
     pl.workspace = pl.ws_cnt + (p.ks > 1 ? r256((size_t)p.tiles * 4) : 0);

@@ -133,14 +133,14 @@ int check_tc(int wt, long long M, long long N, long long K) {
     return 1;
 }
 
-int check_tcx(int wt, long long M, long long N, long long K) {
+int check_tcx(int wt, int am, long long M, long long N, long long K) {
     TcxPlan pl;
-    if (!plan_tcx(wt, M, N, K, kSms, kSmem, pl)) return 0;
+    if (!plan_tcx(wt, am, M, N, K, kSms, kSmem, pl)) return 0;
     const TcxParams& p = pl.p;
 #define CASE "tcx %s M%lld N%lld K%lld", tname(wt), M, N, K
     CHECK(pl.smem <= (size_t)kSmem && p.nraw >= 3 && p.nraw <= kTxRawMax, CASE);
-    CHECK(p.off_raw == tcx_stages(wt, pl.nx) * tcx_stage_bytes(wt, pl.nx) && p.off_raw % 1024 == 0 && tcx_raw_slot(wt) % 1024 == 0 &&
-              p.off_bar == p.off_raw + p.nraw * tcx_raw_slot(wt) && (size_t)p.off_bar + 512 + 1024 <= pl.smem,
+    CHECK(p.off_raw == tcx_stages(wt, am, pl.nx) * tcx_stage_bytes(wt, am, pl.nx) && p.off_raw % 1024 == 0 && tcx_raw_slot(wt, am) % 1024 == 0 &&
+              p.off_bar == p.off_raw + p.nraw * tcx_raw_slot(wt, am) && (size_t)p.off_bar + 512 + 1024 <= pl.smem,
           CASE);
     CHECK((pl.nx == 64 || pl.nx == kTxX) && (pl.nx == 64) == (M <= 64), CASE);
     CHECK(p.nrs * 256 == K && (long long)p.mtiles * pl.nx >= M && (long long)(p.mtiles - 1) * pl.nx < M &&
@@ -153,9 +153,12 @@ int check_tcx(int wt, long long M, long long N, long long K) {
         CHECK(r1 > r0 && (sp > 0 || r0 == 0) && (sp < p.ks - 1 || r1 == p.nrs), CASE);
     }
     CHECK(pl.grid >= 1 && pl.grid <= kSms && pl.grid <= p.units && pl.mp % 4 == 0 && pl.mp >= M, CASE);
+    CHECK(pl.am == am && (am == A_INT8 || wt == T_Q4_K), CASE);
     CHECK(pl.ws_scales >= (size_t)M * K * 2 && pl.ws_scales % 256 == 0 && pl.ws_bsums % 256 == 0 &&
-              pl.ws_bsums >= pl.ws_scales + (size_t)(K / (wt == T_Q8_0 ? 32 : 256)) * pl.mp * 4 &&
-              pl.ws_w6 % 256 == 0 && pl.ws_w6 >= pl.ws_bsums + (wt != T_Q8_0 ? (size_t)M * (K / 16) * 2 : 0) &&
+              pl.ws_bsums >= pl.ws_scales + (am == A_F32 ? (size_t)M * K * 2 : (size_t)(K / (wt == T_Q8_0 ? 32 : 256)) * pl.mp * 4) &&
+              pl.ws_ais % 256 == 0 &&
+              pl.ws_ais >= pl.ws_bsums + (wt != T_Q8_0 ? (size_t)M * (K / 16) * 2 * (am == A_F32 ? 2 : 1) : 0) &&
+              pl.ws_w6 % 256 == 0 && pl.ws_w6 >= pl.ws_ais + (am == A_F32 ? (size_t)M * 4 : 0) &&
               pl.ws_part % 256 == 0 && pl.ws_part >= pl.ws_w6 + (wt == T_Q6_K ? (size_t)N * (K / 256) * 240 : 0) &&
               pl.ws_cnt % 256 == 0 && pl.ws_cnt >= pl.ws_part + (p.ks > 1 ? (size_t)p.ks * M * N * 4 : 0) &&
               pl.workspace >= pl.ws_cnt + (p.ks > 1 ? (size_t)p.tiles * 4 : 0),
@@ -217,7 +220,8 @@ int main() {
             for (long long N : {128, 300, 4096, 14336})
                 for (long long K : {256, 1024, 4096, 14336}) {
                     plans += check_tc(wt, M, N, K);
-                    if (wt == T_Q8_0 || wt == T_Q4_K || wt == T_Q6_K) plans += check_tcx(wt, M, N, K);
+                    if (wt == T_Q8_0 || wt == T_Q4_K || wt == T_Q6_K) plans += check_tcx(wt, A_INT8, M, N, K);
+                    if (wt == T_Q4_K) plans += check_tcx(wt, A_F32, M, N, K);
                 }
     }
     for (int wt : types)
@@ -243,7 +247,9 @@ int main() {
         for (int wt : types) {
             CHECK(plan_tc(wt, M, 14336, 4096, kSms, kSmem, tp), "no tcgen05 plan for %s M%lld", tname(wt), M);
             if (wt == T_Q8_0 || wt == T_Q4_K || wt == T_Q6_K)
-                CHECK(plan_tcx(wt, M, 14336, 4096, kSms, kSmem, xp), "no exact prefill plan for %s M%lld", tname(wt), M);
+                CHECK(plan_tcx(wt, A_INT8, M, 14336, 4096, kSms, kSmem, xp), "no exact prefill plan for %s M%lld", tname(wt), M);
+            if (wt == T_Q4_K)
+                CHECK(plan_tcx(wt, A_F32, M, 14336, 4096, kSms, kSmem, xp), "no f32_act code-GEMM plan for M%lld", M);
         }
     std::printf("%s %d plans\n", g_bad ? "FAILED" : "ok", plans);
     return g_bad ? 1 : 0;

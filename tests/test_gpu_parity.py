@@ -333,7 +333,7 @@ def test_matmul_batch_edge_rows(qmm, orc, wtype, mode):
     check_device_error(qmm)
 
 
-@pytest.mark.parametrize("wtype,M,N,K", [("q8_0", 64, 300, 4096), ("q4_k", 256, 200, 2048)])
+@pytest.mark.parametrize("wtype,M,N,K", [("q8_0", 64, 300, 4096), ("q4_k", 256, 200, 2048), ("q4_k", 37, 200, 2048)])
 def test_prefill_split_k_is_deterministic(qmm, orc, wtype, M, N, K):
     """Few output tiles split K across CTAs; the tile's last unit sums the
     partial tiles in slice order, so repeated calls agree bit for bit."""
@@ -429,6 +429,7 @@ def test_launch_counts(qmm):
     assert qmm.matmul_launches("q8_0", "int8_act", 256, 4096, 4096) == 2  # exact prefill: activation codes + GEMM
     assert qmm.matmul_launches("q8_0", "f32_act", 256, 4096, 4096) == 2   # tcgen05: operand pieces + GEMM
     assert qmm.matmul_launches("q4_k", "int8_act", 256, 4096, 4096) == 2  # exact tcgen05: activation codes + GEMM
+    assert qmm.matmul_launches("q4_k", "f32_act", 64, 4096, 4096) == 2    # code GEMM: activation pieces + GEMM
     assert qmm.matmul_launches("q6_k", "int8_act", 256, 4096, 4096) == 3  # exact tcgen05: codes, repack, GEMM
     assert qmm.matmul_launches("q6_k", "int8_act", 16, 4096, 4096) == 1   # up to 16 rows: the decode kernel
     assert qmm.matmul_launches("q8_0", "int8_act", 1, 100, 100) == 0      # K not a multiple of 32
