@@ -152,12 +152,13 @@ void plan_dispatch(int wt, int am, int epi, long long M, long long N, long long 
         d.kind = KIND_DMMA;
         d.workspace = d.dp.workspace;
         d.launches = 1 + (d.dp.ext_bytes ? 1 : 0) + (epi == E_Y && d.dp.p.kslices > 1 ? 1 : 0);
-    } else if (epi == E_Y && am == A_F32 && wt == T_Q4_K && M <= 64 && plan_tcx(wt, A_F32, M, N, K, sms, smem, d.xp)) {
-        // Metal-form prefill of Q4_K up to 64 rows: exact f16 codes times two activation pieces
-        // (tcgen05; 1.3-1.6x the three-pass GEMM there, slower from 256 rows on)
+    } else if (epi == E_Y && am == A_F32 && M <= 64 && plan_tcx(wt, A_F32, M, N, K, sms, smem, d.xp)) {
+        // Metal-form prefill up to 64 rows (Q8_0, Q4_K, Q6_K): exact f16 weight codes times two
+        // activation pieces on tcgen05 (Q4_K 1.3-1.6x the three-pass GEMM there, Q8_0 1.1x,
+        // Q6_K even; the three passes are faster from 256 rows on)
         d.kind = KIND_TCX;
         d.workspace = d.xp.workspace;
-        d.launches = 2;  // activation pieces, GEMM
+        d.launches = wt == T_Q6_K ? 3 : 2;  // activation pieces, (Q6_K) repacked weights, GEMM
     } else if (epi == E_Y && am == A_F32 && plan_tc(wt, M, N, K, sms, smem, d.tp)) {  // Metal-form prefill: tcgen05 GEMM
         d.kind = KIND_TC;
         d.workspace = d.tp.workspace;

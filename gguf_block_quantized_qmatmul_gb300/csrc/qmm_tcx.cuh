@@ -1,8 +1,8 @@
 // qmm_tcx.cuh -- the CPU form's prefill GEMM (int8_act, M > 16 activation
 // rows; Q8_0, Q4_K and Q6_K weights) on the 5th-generation tensor cores with
 // exact per-block sums; the same GEMM of exact weight codes also serves the
-// Metal form (f32_act) for Q4_K up to 64 rows, with each activation row split
-// into two f16 pieces (see TxRaw).
+// Metal form (f32_act) up to 64 rows, with each activation row split into two
+// f16 pieces (see TxRaw).
 //
 // "同一个 GGUF，CPU 和 Metal 生成的文字不一样" section 出处: the CPU form
 // quantizes every activation row (Q8_0, or Q8K for K-quant weights) and
@@ -78,14 +78,13 @@ constexpr int kTxThreads = (2 + kTxEpiWarps + kTxConvWarps) * 32;
 // A block stage holds the block's weight codes (Q6_K: two tiles, a_g q and
 // b_g q, for the group scales split as sc_g = 16 a_g + b_g) and the 128
 // activation rows' codes.
-// The f32_act form (Q4_K only, AM = A_F32) takes the same weight codes and
-// each activation row scaled by a power of two and split into two f16 pieces,
-// x 2^s = hi + lo: two MMAs per K step into one accumulator, and the min
-// term's sums of 16 values in two pieces as well; the fold needs no
-// activation scale per super-block (2^-s is applied at the store).
+// The f32_act form (AM = A_F32) takes the same weight codes and each
+// activation row scaled by a power of two and split into two f16 pieces,
+// x 2^s = hi + lo: two MMAs per K step into one accumulator (Q4_K: the min
+// term's sums of 16 values in two pieces as well); the fold needs no
+// activation scale (2^-s is applied at the store).
 template <int WT, int AM = A_INT8>
 struct TxRaw {
-    static_assert(AM == A_INT8 || WT == T_Q4_K, "the f32_act form: Q4_K");
     static constexpr int pieces = AM == A_F32 ? 2 : 1;                             // activation pieces
     static constexpr int row = WT == T_Q8_0 ? 272 : WT == T_Q4_K ? 144 : 240;
     static constexpr int scales = kTxW * row;                                      // f(d_a) (int8_act)
@@ -96,8 +95,9 @@ struct TxRaw {
                                                : (scales + kTxX * 4 + 1023) / 1024 * 1024;
     // bytes a raw stage's copies bring, for tiles of nx activation rows
     __host__ __device__ static constexpr int tx(int nx) {
-        return WT == T_Q8_0   ? kTxW * row + 8 * nx * 4
-               : WT == T_Q4_K ? kTxW * row + (AM == A_F32 ? 0 : nx * 4) + pieces * nx * 32
+        return AM == A_F32    ? kTxW * row + (WT == T_Q4_K ? pieces * nx * 32 : 0)
+               : WT == T_Q8_0 ? kTxW * row + 8 * nx * 4
+               : WT == T_Q4_K ? kTxW * row + nx * 4 + nx * 32
                               : kTxW * row + nx * 4;
     }
     // accumulators (drain units) per raw stage: Q8_0 one per block; Q4_K S_sc
@@ -109,7 +109,7 @@ struct TxRaw {
     // each 128-byte swizzled rows: a weight tile of 128 rows and an
     // activation tile of nx rows per atom.
     __host__ __device__ static constexpr int bps(int nx) {
-        return AM == A_F32 ? (nx == 64 ? 4 : 2) : WT == T_Q4_K || (WT == T_Q8_0 && nx == 64) ? 4 : 2;
+        return AM == A_F32 ? (WT == T_Q4_K && nx == 64 ? 4 : 2) : WT == T_Q4_K || (WT == T_Q8_0 && nx == 64) ? 4 : 2;
     }
     __host__ __device__ static constexpr int atoms(int nx) { return bps(nx) / 2; }
     __host__ __device__ static constexpr int wtile(int nx) { return atoms(nx) * kTxW * 128; }  // bytes of a weight tile
@@ -119,7 +119,8 @@ struct TxRaw {
     __host__ __device__ static constexpr int stages(int nx) { return AM == A_INT8 && WT == T_Q4_K && bps(nx) == 2 ? 4 : 2; }
 };
 static_assert(TxRaw<T_Q8_0>::slot % 1024 == 0 && TxRaw<T_Q4_K>::slot % 1024 == 0 && TxRaw<T_Q6_K>::slot % 1024 == 0 &&
-                  TxRaw<T_Q4_K, A_F32>::slot % 1024 == 0,
+                  TxRaw<T_Q8_0, A_F32>::slot % 1024 == 0 && TxRaw<T_Q4_K, A_F32>::slot % 1024 == 0 &&
+                  TxRaw<T_Q6_K, A_F32>::slot % 1024 == 0,
               "1 KB aligned raw slots");
 
 struct TcxParams {
@@ -394,8 +395,10 @@ __global__ void __launch_bounds__(kTxThreads, 1)
                         mbar_arrive_tx(fb, (uint32_t)R::tx(NX));
                         tma_2d(smem_u32(raw(rs)), &tw, ir * (R::row / 2), in0, fb);
                         if (kF32) {
-                            tma_2d(smem_u32(raw(rs) + R::bsum), &tb, 16 * ir, im0, fb);
-                            tma_2d(smem_u32(raw(rs) + R::bsum + kTxX * 32), &tb, p.K / 16 + 16 * ir, im0, fb);
+                            if (WT == T_Q4_K) {
+                                tma_2d(smem_u32(raw(rs) + R::bsum), &tb, 16 * ir, im0, fb);
+                                tma_2d(smem_u32(raw(rs) + R::bsum + kTxX * 32), &tb, p.K / 16 + 16 * ir, im0, fb);
+                            }
                         } else if (WT == T_Q8_0) {
                             tma_2d(smem_u32(raw(rs) + R::scales), &ts, im0, 8 * ir, fb);
                         } else {
@@ -473,8 +476,12 @@ __global__ void __launch_bounds__(kTxThreads, 1)
                             tcx_mma(tmem + col, tcx_sdesc128(wk), tcx_sdesc128(xk), idesc, accu);
                             if (kF32)  // the lo piece into the same accumulator
                                 tcx_mma(tmem + col, tcx_sdesc128(wk), tcx_sdesc128(xk + (kBps / 2) * NX * 128), idesc, 1u);
-                            if (WT == T_Q6_K)
+                            if (WT == T_Q6_K) {
                                 tcx_mma(tmem + dcol2, tcx_sdesc128(wk + R::wtile(NX)), tcx_sdesc128(xk), idesc, accu);
+                                if (kF32)
+                                    tcx_mma(tmem + dcol2, tcx_sdesc128(wk + R::wtile(NX)),
+                                            tcx_sdesc128(xk + (kBps / 2) * NX * 128), idesc, 1u);
+                            }
                         }
                         tc_commit(smem_u32(&empty[s]));
                         if (WT == T_Q8_0) {
@@ -560,11 +567,16 @@ __global__ void __launch_bounds__(kTxThreads, 1)
                         const float* aj = asc + j * NX;
 #pragma unroll
                         for (int c = 0; c < CW / 4; ++c) {
-                            const float4 a4 = *reinterpret_cast<const float4*>(aj + 4 * c);
                             const uint32_t* v = vv + 4 * c;
-                            const unsigned long long s01 = mul2(f2pack(a4.x, a4.y), dw2), s23 = mul2(f2pack(a4.z, a4.w), dw2);
-                            acc[2 * c] = fma2(f2pack(__uint_as_float(v[0]), __uint_as_float(v[1])), s01, acc[2 * c]);
-                            acc[2 * c + 1] = fma2(f2pack(__uint_as_float(v[2]), __uint_as_float(v[3])), s23, acc[2 * c + 1]);
+                            if constexpr (kF32) {  // y 2^s += S f(d_w) (sums of x 2^s)
+                                acc[2 * c] = fma2(f2pack(__uint_as_float(v[0]), __uint_as_float(v[1])), dw2, acc[2 * c]);
+                                acc[2 * c + 1] = fma2(f2pack(__uint_as_float(v[2]), __uint_as_float(v[3])), dw2, acc[2 * c + 1]);
+                            } else {
+                                const float4 a4 = *reinterpret_cast<const float4*>(aj + 4 * c);
+                                const unsigned long long s01 = mul2(f2pack(a4.x, a4.y), dw2), s23 = mul2(f2pack(a4.z, a4.w), dw2);
+                                acc[2 * c] = fma2(f2pack(__uint_as_float(v[0]), __uint_as_float(v[1])), s01, acc[2 * c]);
+                                acc[2 * c + 1] = fma2(f2pack(__uint_as_float(v[2]), __uint_as_float(v[3])), s23, acc[2 * c + 1]);
+                            }
                         }
                     }
                 } else if (WT == T_Q6_K) {
@@ -585,13 +597,14 @@ __global__ void __launch_bounds__(kTxThreads, 1)
                         tc_wait_ld();
 #pragma unroll
                         for (int c = 0; c < 2; ++c) {
-                            const float4 a4 = *reinterpret_cast<const float4*>(asc + 8 * h + 4 * c);
+                            const float4 a4 = kF32 ? make_float4(1.0f, 1.0f, 1.0f, 1.0f)  // f32_act: 2^-s at the store
+                                                   : *reinterpret_cast<const float4*>(asc + 8 * h + 4 * c);
 #pragma unroll
                             for (int e = 0; e < 2; ++e) {
                                 const int i = 4 * c + 2 * e;
                                 const unsigned long long t = fma2(f2pack(__uint_as_float(va[i]), __uint_as_float(va[i + 1])), k16,
                                                                   f2pack(__uint_as_float(vb[i]), __uint_as_float(vb[i + 1])));
-                                const unsigned long long sc2 = mul2(e ? f2pack(a4.z, a4.w) : f2pack(a4.x, a4.y), fd2);
+                                const unsigned long long sc2 = kF32 ? fd2 : mul2(e ? f2pack(a4.z, a4.w) : f2pack(a4.x, a4.y), fd2);
                                 acc[4 * h + 2 * c + e] = fma2(t, sc2, acc[4 * h + 2 * c + e]);
                             }
                         }
@@ -842,14 +855,14 @@ __global__ void tcx_act_kernel(const float* __restrict__ x, int M, int K, int mp
     }
 }
 
-// The f32_act operand (Q4_K), written once per call: one 256-thread block per
+// The f32_act operand, written once per call: one 256-thread block per
 // activation row m finds the row's largest magnitude, takes 2^s with
 // max |x| 2^s in [2^14, 2^15) and splits every value exactly into two f16
-// pieces, x 2^s = hi + lo (hi[m][K], lo[m][K]); each 16 values' sum of x 2^s,
-// over 16 (at most 2^15, so it fits f16), is split the same way into
+// pieces, x 2^s = hi + lo (hi[m][K], lo[m][K]); for Q4_K each 16 values' sum
+// of x 2^s, over 16 (at most 2^15, so it fits f16), is split the same way into
 // bsums[m][K / 16 + j] after the hi sums bsums[m][j]; ais[m] = 2^-s.  It also
 // zeroes the GEMM's ncnt split-K arrival counters.
-template <int WT>  // T_Q4_K
+template <int WT>
 __global__ void tcx_act_f32_kernel(const float* __restrict__ x, int M, int K, __half* __restrict__ hi, __half* __restrict__ lo,
                                    __half* __restrict__ bsums, float* __restrict__ ais, unsigned* __restrict__ cnt, int ncnt) {
     grid_dep_launch();
@@ -908,10 +921,12 @@ __global__ void tcx_act_f32_kernel(const float* __restrict__ x, int M, int K, __
         ho[1] = make_uint4(hw[4], hw[5], hw[6], hw[7]);
         lo4[0] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
         lo4[1] = make_uint4(lw[4], lw[5], lw[6], lw[7]);
-        const float s16 = sum * 0.0625f;  // exact
-        const __half sh = __float2half_rn(s16);
-        br[g] = sh;
-        br[K / 16 + g] = __float2half_rn(s16 - __half2float(sh));
+        if (WT == T_Q4_K) {
+            const float s16 = sum * 0.0625f;  // exact
+            const __half sh = __float2half_rn(s16);
+            br[g] = sh;
+            br[K / 16 + g] = __float2half_rn(s16 - __half2float(sh));
+        }
     }
 }
 
@@ -938,7 +953,7 @@ __global__ void tcx_q6_repack_kernel(const uint8_t* __restrict__ wq, int N, int 
 // ---------------------------------------------------------------------------
 struct TcxPlan {
     TcxParams p;
-    int am;  // A_INT8 (exact block sums) or A_F32 (Q4_K: two activation pieces)
+    int am;  // A_INT8 (exact block sums) or A_F32 (two activation pieces)
     int nx;  // activation rows per tile: 64 or 128
     int grid;
     size_t smem;
@@ -949,23 +964,26 @@ struct TcxPlan {
     size_t ws_codes, ws_scales, ws_bsums, ws_ais, ws_w6, ws_part, ws_cnt, workspace;
 };
 
-inline int tcx_raw_slot(int wt, int am) {
-    return am == A_F32 ? TxRaw<T_Q4_K, A_F32>::slot
-                       : wt == T_Q8_0 ? TxRaw<T_Q8_0>::slot : wt == T_Q4_K ? TxRaw<T_Q4_K>::slot : TxRaw<T_Q6_K>::slot;
+template <int AM>
+inline int tcx_raw_slot_am(int wt) {
+    return wt == T_Q8_0 ? TxRaw<T_Q8_0, AM>::slot : wt == T_Q4_K ? TxRaw<T_Q4_K, AM>::slot : TxRaw<T_Q6_K, AM>::slot;
 }
-inline int tcx_stages(int wt, int am, int nx) {
-    return am == A_F32 ? TxRaw<T_Q4_K, A_F32>::stages(nx)
-                       : wt == T_Q8_0 ? TxRaw<T_Q8_0>::stages(nx)
-                                      : wt == T_Q4_K ? TxRaw<T_Q4_K>::stages(nx) : TxRaw<T_Q6_K>::stages(nx);
+template <int AM>
+inline int tcx_stages_am(int wt, int nx) {
+    return wt == T_Q8_0 ? TxRaw<T_Q8_0, AM>::stages(nx) : wt == T_Q4_K ? TxRaw<T_Q4_K, AM>::stages(nx) : TxRaw<T_Q6_K, AM>::stages(nx);
 }
+template <int AM>
+inline int tcx_stage_bytes_am(int wt, int nx) {
+    return wt == T_Q8_0 ? TxRaw<T_Q8_0, AM>::stage(nx) : wt == T_Q4_K ? TxRaw<T_Q4_K, AM>::stage(nx) : TxRaw<T_Q6_K, AM>::stage(nx);
+}
+inline int tcx_raw_slot(int wt, int am) { return am == A_F32 ? tcx_raw_slot_am<A_F32>(wt) : tcx_raw_slot_am<A_INT8>(wt); }
+inline int tcx_stages(int wt, int am, int nx) { return am == A_F32 ? tcx_stages_am<A_F32>(wt, nx) : tcx_stages_am<A_INT8>(wt, nx); }
 inline int tcx_stage_bytes(int wt, int am, int nx) {
-    return am == A_F32 ? TxRaw<T_Q4_K, A_F32>::stage(nx)
-                       : wt == T_Q8_0 ? TxRaw<T_Q8_0>::stage(nx)
-                                      : wt == T_Q4_K ? TxRaw<T_Q4_K>::stage(nx) : TxRaw<T_Q6_K>::stage(nx);
+    return am == A_F32 ? tcx_stage_bytes_am<A_F32>(wt, nx) : tcx_stage_bytes_am<A_INT8>(wt, nx);
 }
 
 inline bool plan_tcx(int wt, int am, long long M, long long N, long long K, int sm_count, int smem_max, TcxPlan& out) {
-    if ((wt != T_Q8_0 && wt != T_Q4_K && wt != T_Q6_K) || (am == A_F32 && wt != T_Q4_K) || K % 256 != 0 || M < 17 ||
+    if ((wt != T_Q8_0 && wt != T_Q4_K && wt != T_Q6_K) || K % 256 != 0 || M < 17 ||
         K > (1 << 26) || M > (1 << 24) || N > (1 << 24))
         return false;
     TcxPlan pl{};
@@ -1017,7 +1035,7 @@ inline bool plan_tcx(int wt, int am, long long M, long long N, long long K, int 
     pl.ws_scales = r256((size_t)M * K * 2);
     const size_t per = wt == T_Q8_0 ? 32 : 256;  // values per activation scale
     pl.ws_bsums = pl.ws_scales + (am == A_F32 ? r256((size_t)M * K * 2) : r256((size_t)(K / per) * pl.mp * 4));
-    pl.ws_ais = pl.ws_bsums + (wt != T_Q8_0 ? r256((size_t)M * (K / 16) * 2 * (am == A_F32 ? 2 : 1)) : 0);
+    pl.ws_ais = pl.ws_bsums + (wt == T_Q4_K || (wt == T_Q6_K && am == A_INT8) ? r256((size_t)M * (K / 16) * 2 * (am == A_F32 ? 2 : 1)) : 0);
     pl.ws_w6 = pl.ws_ais + (am == A_F32 ? r256((size_t)M * 4) : 0);
     pl.ws_part = pl.ws_w6 + (wt == T_Q6_K ? r256((size_t)N * (K / 256) * TxRaw<T_Q6_K>::row) : 0);
     pl.ws_cnt = pl.ws_part + (p.ks > 1 ? r256((size_t)p.ks * M * N * 4) : 0);

@@ -153,11 +153,11 @@ int check_tcx(int wt, int am, long long M, long long N, long long K) {
         CHECK(r1 > r0 && (sp > 0 || r0 == 0) && (sp < p.ks - 1 || r1 == p.nrs), CASE);
     }
     CHECK(pl.grid >= 1 && pl.grid <= kSms && pl.grid <= p.units && pl.mp % 4 == 0 && pl.mp >= M, CASE);
-    CHECK(pl.am == am && (am == A_INT8 || wt == T_Q4_K), CASE);
+    CHECK(pl.am == am, CASE);
     CHECK(pl.ws_scales >= (size_t)M * K * 2 && pl.ws_scales % 256 == 0 && pl.ws_bsums % 256 == 0 &&
               pl.ws_bsums >= pl.ws_scales + (am == A_F32 ? (size_t)M * K * 2 : (size_t)(K / (wt == T_Q8_0 ? 32 : 256)) * pl.mp * 4) &&
               pl.ws_ais % 256 == 0 &&
-              pl.ws_ais >= pl.ws_bsums + (wt != T_Q8_0 ? (size_t)M * (K / 16) * 2 * (am == A_F32 ? 2 : 1) : 0) &&
+              pl.ws_ais >= pl.ws_bsums + (wt == T_Q4_K || (wt == T_Q6_K && am == A_INT8) ? (size_t)M * (K / 16) * 2 * (am == A_F32 ? 2 : 1) : 0) &&
               pl.ws_w6 % 256 == 0 && pl.ws_w6 >= pl.ws_ais + (am == A_F32 ? (size_t)M * 4 : 0) &&
               pl.ws_part % 256 == 0 && pl.ws_part >= pl.ws_w6 + (wt == T_Q6_K ? (size_t)N * (K / 256) * 240 : 0) &&
               pl.ws_cnt % 256 == 0 && pl.ws_cnt >= pl.ws_part + (p.ks > 1 ? (size_t)p.ks * M * N * 4 : 0) &&
@@ -221,7 +221,7 @@ int main() {
                 for (long long K : {256, 1024, 4096, 14336}) {
                     plans += check_tc(wt, M, N, K);
                     if (wt == T_Q8_0 || wt == T_Q4_K || wt == T_Q6_K) plans += check_tcx(wt, A_INT8, M, N, K);
-                    if (wt == T_Q4_K) plans += check_tcx(wt, A_F32, M, N, K);
+                    if (wt == T_Q8_0 || wt == T_Q4_K || wt == T_Q6_K) plans += check_tcx(wt, A_F32, M, N, K);
                 }
     }
     for (int wt : types)
