@@ -484,11 +484,10 @@ WARP_MMA_F16_PEAK = 605.0  # TFLOP/s, legacy warp-level f16 MMA on this GPU (reg
 
 def prefill_kernel(t: str, mode: str, M: int) -> str:
     """The kernel qmm_matmul runs for a prefill shape with K % 256 = 0 (the
-    library's dispatch): the Metal form on the three-pass tcgen05 GEMM (up
-    to 64 rows of Q8_0, Q4_K, Q6_K: on the code GEMM, with two activation
-    pieces); the CPU
-    form, whose bound needs exact integer block sums, on the exact tcgen05
-    GEMM; up to 16 rows, the decode kernel."""
+    library's dispatch): the Metal form on the three-pass tcgen05 GEMM, up to
+    64 rows on the exact-code GEMM with two activation pieces; the CPU form,
+    whose bound needs exact integer block sums, on the exact tcgen05 GEMM; up
+    to 16 rows, the decode kernel."""
     if M <= 16:
         return "qmm_dmma_kernel"
     if mode == "f32_act" and M > 64:
