@@ -38,7 +38,7 @@ cudaError_t tc_go(const TcPlan& pl, const void* wq, const float* x, void* ws, fl
                                                               alo, ais, wis, cnt, p0.ks > 1 ? p0.tiles : 0, w6);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    // 2. tensor maps: raw weight rows as uint16; activation pieces, 32 K x bx rows, 64-byte swizzle
+    // 2. tensor maps: raw weight rows as uint16; activation pieces, 64 K x bx rows, 128-byte swizzle
     CUtensorMap tw, tah, tal;
     const unsigned long long rb = WT == T_Q4_K   ? (unsigned long long)p0.K / 256 * 144
                                   : WT == T_Q6_K ? (unsigned long long)p0.K / 256 * kTcQ6Slot
@@ -46,9 +46,9 @@ cudaError_t tc_go(const TcPlan& pl, const void* wq, const float* x, void* ws, fl
     const void* wsrc = WT == T_Q6_K ? static_cast<const void*>(w6) : wq;
     if (!make_map(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT16, wsrc, rb / 2, p0.N, rb, p0.raw_row / 2, kTcBW, CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !make_map(&tah, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, ahi, p0.K, p0.M, (unsigned long long)p0.K * 2, kTcBK, p0.bx,
-                  CU_TENSOR_MAP_SWIZZLE_64B) ||
+                  CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(&tal, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, alo, p0.K, p0.M, (unsigned long long)p0.K * 2, kTcBK, p0.bx,
-                  CU_TENSOR_MAP_SWIZZLE_64B))
+                  CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     TcParams p = p0;
     p.y = y;

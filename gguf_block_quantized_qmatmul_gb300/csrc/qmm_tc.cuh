@@ -25,9 +25,10 @@
 //             Q8_0 blocks, 144 B = 1 Q4_K super-block or 8 Q4_0 blocks, 176 B
 //             = 8 Q5_0 blocks, or a 240-byte slot holding 1 Q6_K super-block;
 //             up to six stages in flight) and the activation pieces (bx rows
-//             x 32 f16, 64-byte swizzle, hi and lo, per 32 K);
-//   MMA       one thread: per 32-K stage six tcgen05.mma (M 128, N bx, K 16:
-//             hi.hi, hi.lo, lo.hi, two K steps each) with the weights as the A
+//             x 64 f16, 128-byte swizzle, hi and lo, per 64 K: two 32-value
+//             blocks per stage, so each handoff between roles covers two);
+//   MMA       one thread: per 64-K stage twelve tcgen05.mma (M 128, N bx, K 16:
+//             hi.hi, hi.lo, lo.hi, four K steps each) with the weights as the A
 //             operand in tensor memory and the activation piece from shared
 //             memory; it tests the next stage's barrier before issuing the
 //             current one, so a ready stage costs no stall;
@@ -38,11 +39,11 @@
 //             that completes a tile sums its ks partials in slice order
 //             (deterministic) and writes y;
 //   converter 8 warps in two groups (even and odd stages): each thread one
-//             weight row's 32 values of a stage, read from the raw stage with
+//             weight row's 64 values of a stage, read from the raw stage with
 //             conflict-free 16-byte loads, dequantized, split into hi and lo,
 //             written straight into tensor memory (tcgen05.st).
 // TMEM: accumulators (two of 128 columns when bx <= 128, else one of 256) and
-// four stages x 32 columns of weight pieces at column 256.
+// two stages x 64 columns of weight pieces at column 256.
 #pragma once
 
 #include "qmm_device.cuh"
@@ -51,16 +52,16 @@ namespace qmm {
 
 constexpr int kTcBW = 128;      // weight rows per tile (MMA M, the TMEM lanes)
 constexpr int kTcBXMax = 256;   // activation rows per tile, at most (MMA N)
-constexpr int kTcBK = 32;       // K per stage
+constexpr int kTcBK = 64;       // K per stage: two 32-value blocks, 128-byte swizzled activation rows
 constexpr int kTcRK = 256;      // K per raw weight stage
 constexpr int kTcSub = kTcRK / kTcBK;  // stages per raw stage
-constexpr int kTcS = 4;         // stages: activation pieces in shared memory, weight pieces in TMEM
+constexpr int kTcS = 2;         // stages: activation pieces in shared memory, weight pieces in TMEM
 constexpr int kTcRSMax = 6;     // raw weight stages, at most
 constexpr int kTcConvWarps = 8;
 constexpr int kTcEpiWarps = 8;
 constexpr int kTcThreads = (2 + kTcEpiWarps + kTcConvWarps) * 32;
 constexpr int kTcTmemCols = 512;
-constexpr int kTcWCol0 = 256;   // weight pieces: stage s at 256 + 32 s (hi 16 columns, lo 16 columns)
+constexpr int kTcWCol0 = 256;   // weight pieces: stage s at 256 + 64 s (hi 32 columns, lo 32 columns)
 constexpr int kTcMaxSplit = 16;
 // Accumulation chunks.  The tensor core's f32 accumulation truncates: its
 // error grows with the number of MMAs chained into one accumulator and leans
@@ -95,10 +96,10 @@ struct TcParams {
     int off_raw, off_bar;
 };
 
-// shared-memory matrix descriptor: K-major, 64-byte swizzle, 8-row atoms 512 B apart
-__device__ __forceinline__ uint64_t tc_sdesc(uint32_t addr) {
-    return (uint64_t)((addr >> 4) & 0x3FFF) | ((uint64_t)1 << 16) | ((uint64_t)(512 >> 4) << 32) | ((uint64_t)1 << 46) |
-           ((uint64_t)4 << 61);
+// shared-memory matrix descriptor: K-major, 128-byte swizzle (rows of 64 f16), 8-row atoms 1 KB apart
+__device__ __forceinline__ uint64_t tc_sdesc128(uint32_t addr) {
+    return (uint64_t)((addr >> 4) & 0x3FFF) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) |
+           ((uint64_t)2 << 61);
 }
 // instruction descriptor: f32 accumulator, f16 A and B, both K-major, M = 128, N = bx
 __device__ __forceinline__ uint32_t tc_idesc(int bx) {
@@ -317,45 +318,41 @@ __device__ __forceinline__ void tc_slice(const TcParams& p, int split, int& r0, 
     r1 = (split + 1) * p.nrs / p.ks;
 }
 
-// one converter warp's share of a raw stage: stages G, G + 2, G + 4, G + 6 of
-// the eight it feeds (G = the warp's group); g0 = the global index of the
-// raw stage's first stage
+// one 32-value block J (0..7) of a raw stage: hi and lo pieces
+template <int WT, int J>
+__device__ __forceinline__ void tc_conv_block(const uint8_t* rrow, float wsc, uint32_t h[16], uint32_t l[16]) {
+    if (WT == T_Q8_0) tc_conv_q8_0<J>(rrow, wsc, h, l);
+    else if (WT == T_Q4_0 || WT == T_Q5_0) tc_conv_x_0<WT, J>(rrow, wsc, h, l);
+    else if (WT == T_Q6_K) tc_conv_q6_k<J>(rrow, wsc, h, l);
+    else tc_conv_q4_k<J>(rrow, wsc, h, l);
+}
+
+// one converter warp's share of a raw stage: stages G and G + 2 of the four
+// it feeds (G = the warp's group; stage j holds blocks 2 j and 2 j + 1, their
+// hi pieces in 32 TMEM columns, then their lo pieces); g0 = the global index
+// of the raw stage's first stage
 template <int WT, int G>
 __device__ __forceinline__ bool tc_convert_raw(const uint8_t* rrow, float wsc, long long g0, uint32_t tq, uint32_t tmem,
                                                uint64_t* full, uint64_t* empty, volatile int* flags, unsigned* err,
                                                int lane) {
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < 2; ++u) {
         const int j = 2 * u + G;
         const long long g = g0 + j;
         const int s = (int)(g % kTcS);
         if (g >= kTcS && !mbar_wait(smem_u32(&empty[s]), (uint32_t)(((g / kTcS) - 1) & 1), flags, err)) return false;
         tc_fence_after();
-        uint32_t h[16], l[16];
-        if (WT == T_Q8_0) {
-            if (u == 0) tc_conv_q8_0<G>(rrow, wsc, h, l);
-            else if (u == 1) tc_conv_q8_0<G + 2>(rrow, wsc, h, l);
-            else if (u == 2) tc_conv_q8_0<G + 4>(rrow, wsc, h, l);
-            else tc_conv_q8_0<G + 6>(rrow, wsc, h, l);
-        } else if (WT == T_Q4_0 || WT == T_Q5_0) {
-            if (u == 0) tc_conv_x_0<WT, G>(rrow, wsc, h, l);
-            else if (u == 1) tc_conv_x_0<WT, G + 2>(rrow, wsc, h, l);
-            else if (u == 2) tc_conv_x_0<WT, G + 4>(rrow, wsc, h, l);
-            else tc_conv_x_0<WT, G + 6>(rrow, wsc, h, l);
-        } else if (WT == T_Q6_K) {
-            if (u == 0) tc_conv_q6_k<G>(rrow, wsc, h, l);
-            else if (u == 1) tc_conv_q6_k<G + 2>(rrow, wsc, h, l);
-            else if (u == 2) tc_conv_q6_k<G + 4>(rrow, wsc, h, l);
-            else tc_conv_q6_k<G + 6>(rrow, wsc, h, l);
-        } else {
-            if (u == 0) tc_conv_q4_k<G>(rrow, wsc, h, l);
-            else if (u == 1) tc_conv_q4_k<G + 2>(rrow, wsc, h, l);
-            else if (u == 2) tc_conv_q4_k<G + 4>(rrow, wsc, h, l);
-            else tc_conv_q4_k<G + 6>(rrow, wsc, h, l);
+        const uint32_t col = tmem + tq + (uint32_t)(kTcWCol0 + 64 * s);
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+            uint32_t h[16], l[16];
+            if (u == 0 && b == 0) tc_conv_block<WT, 2 * G>(rrow, wsc, h, l);
+            else if (u == 0) tc_conv_block<WT, 2 * G + 1>(rrow, wsc, h, l);
+            else if (b == 0) tc_conv_block<WT, 2 * G + 4>(rrow, wsc, h, l);
+            else tc_conv_block<WT, 2 * G + 5>(rrow, wsc, h, l);
+            tc_st16(col + 16 * b, h);
+            tc_st16(col + 32 + 16 * b, l);
         }
-        const uint32_t col = tmem + tq + (uint32_t)(kTcWCol0 + 32 * s);
-        tc_st16(col, h);
-        tc_st16(col + 16, l);
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         tc_fence_before();
         __syncwarp();
@@ -546,14 +543,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     if (!ok) break;
                     tc_fence_after();
                     const uint32_t xhi = smem_u32(stage(s)), xlo = xhi + (uint32_t)p.piece;
-                    const uint32_t whi = tmem + (uint32_t)(kTcWCol0 + 32 * s), wlo = whi + 16;
+                    const uint32_t whi = tmem + (uint32_t)(kTcWCol0 + 64 * s), wlo = whi + 32;
 #pragma unroll
                     for (int pass = 0; pass < 3; ++pass) {
                         // w_hi x_hi, w_hi x_lo, w_lo x_hi
                         const uint32_t wa = pass == 2 ? wlo : whi, xb = pass == 1 ? xlo : xhi;
 #pragma unroll
                         for (int kk = 0; kk < kTcBK / 16; ++kk)
-                            tc_mma(dt, wa + 8 * kk, tc_sdesc(xb + 32 * kk), idesc, (i | pass | kk) != 0 ? 1u : 0u);
+                            tc_mma(dt, wa + 8 * kk, tc_sdesc128(xb + 32 * kk), idesc, (i | pass | kk) != 0 ? 1u : 0u);
                     }
                     tc_commit(smem_u32(&empty[s]));
                     ready = nxt;
@@ -843,13 +840,13 @@ struct TcPlan {
 };
 
 // Modelled SM cycles of one work unit of `nr` raw stages (fitted to GB300
-// timings): a stage costs six M 128 x N bx x K 16 MMAs at ~3.5 cycles per
-// activation row, with a floor of ~560 cycles for the issuing thread at small
-// N; a unit adds its accumulator hand-off (the epilogue's drain of a single
+// timings): a 64-K stage costs twelve M 128 x N bx x K 16 MMAs at ~7 cycles
+// per activation row, with a floor of ~800 cycles for the issuing thread at
+// small N; a unit adds its accumulator hand-off (the epilogue's drain of a single
 // accumulator stalls the MMAs); a split tile's last unit also sums the ks
 // partial tiles, at ~24 B a cycle through L2.
 inline double tc_unit_cycles(int bx, int nacc, int kchunk, int ks, int nr, bool last) {
-    const double stage = bx * 3.5 > 560.0 ? bx * 3.5 : 560.0;
+    const double stage = bx * 7.0 > 800.0 ? bx * 7.0 : 800.0;
     const int chunks = (nr + kchunk - 1) / kchunk;  // one accumulator: the MMAs wait for each chunk's drain
     double c = nr * kTcSub * stage + (nacc == 1 ? 6000.0 * chunks : 1500.0);
     if (ks > 1 && last) c += ks * bx * (kTcBW * 4.0 / 24.0);
@@ -872,7 +869,7 @@ inline bool plan_tc(int wt, long long M, long long N, long long K, int sm_count,
     p.nrs = (int)(K / kTcRK);
     p.raw_row = wt == T_Q8_0 ? kTcRK / 32 * 34 : wt == T_Q5_0 ? kTcRK / 32 * 22 : wt == T_Q6_K ? kTcQ6Slot : 144;  // Q4_K, Q4_0: 144
     p.raw_stage = round_up(kTcBW * p.raw_row, 1024);
-    p.piece = p.bx * 64;
+    p.piece = p.bx * 128;
     p.off_raw = kTcS * 2 * p.piece;  // activation pieces; weight pieces live in TMEM
     const int fixed = 512 + kTcEpiWarps * kTcBXMax / 2 * 4 + 1024;  // barriers, TMEM slot, flags; epilogue scales; alignment slack
     p.nraw = (smem_max - p.off_raw - fixed) / p.raw_stage;

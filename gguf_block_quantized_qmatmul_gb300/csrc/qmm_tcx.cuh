@@ -162,12 +162,6 @@ __device__ __forceinline__ void tcx_ld8(uint32_t taddr, uint32_t r[8]) {
                  : "r"(taddr));
 }
 
-// shared-memory matrix descriptor: K-major, 128-byte swizzle (rows of 64 f16), 8-row atoms 1 KB apart
-__device__ __forceinline__ uint64_t tcx_sdesc128(uint32_t addr) {
-    return (uint64_t)((addr >> 4) & 0x3FFF) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) |
-           ((uint64_t)2 << 61);
-}
-
 // shared-memory matrix descriptor: K-major, 32-byte swizzle (rows of 16 f16), 8-row atoms 256 B apart
 __device__ __forceinline__ uint64_t tcx_sdesc32(uint32_t addr) {
     return (uint64_t)((addr >> 4) & 0x3FFF) | ((uint64_t)1 << 16) | ((uint64_t)(256 >> 4) << 32) | ((uint64_t)1 << 46) |
@@ -473,14 +467,14 @@ __global__ void __launch_bounds__(kTxThreads, 1)
                             const uint32_t accu = WT == T_Q8_0 ? (uint32_t)(ks & 1) : (uint32_t)(j | ks);
                             const uint32_t wk = wa + (ks >> 2) * kTxW * 128 + 32 * (ks & 3);
                             const uint32_t xk = xb + (ks >> 2) * NX * 128 + 32 * (ks & 3);
-                            tcx_mma(tmem + col, tcx_sdesc128(wk), tcx_sdesc128(xk), idesc, accu);
+                            tcx_mma(tmem + col, tc_sdesc128(wk), tc_sdesc128(xk), idesc, accu);
                             if (kF32)  // the lo piece into the same accumulator
-                                tcx_mma(tmem + col, tcx_sdesc128(wk), tcx_sdesc128(xk + (kBps / 2) * NX * 128), idesc, 1u);
+                                tcx_mma(tmem + col, tc_sdesc128(wk), tc_sdesc128(xk + (kBps / 2) * NX * 128), idesc, 1u);
                             if (WT == T_Q6_K) {
-                                tcx_mma(tmem + dcol2, tcx_sdesc128(wk + R::wtile(NX)), tcx_sdesc128(xk), idesc, accu);
+                                tcx_mma(tmem + dcol2, tc_sdesc128(wk + R::wtile(NX)), tc_sdesc128(xk), idesc, accu);
                                 if (kF32)
-                                    tcx_mma(tmem + dcol2, tcx_sdesc128(wk + R::wtile(NX)),
-                                            tcx_sdesc128(xk + (kBps / 2) * NX * 128), idesc, 1u);
+                                    tcx_mma(tmem + dcol2, tc_sdesc128(wk + R::wtile(NX)),
+                                            tc_sdesc128(xk + (kBps / 2) * NX * 128), idesc, 1u);
                             }
                         }
                         tc_commit(smem_u32(&empty[s]));

@@ -114,7 +114,7 @@ int check_tc(int wt, long long M, long long N, long long K) {
     // the MMA's N: a multiple of 16 up to 256 that covers M in mtiles tiles
     CHECK(p.bx % 16 == 0 && p.bx >= 16 && p.bx <= kTcBXMax && (long long)p.bx * p.mtiles >= M, CASE);
     // TMEM: the accumulators plus four stages of 32 weight-piece columns fit the 512 columns
-    CHECK((p.nacc == 2 ? 2 * 128 : 256) + kTcS * 32 <= kTcTmemCols && p.nacc == (p.bx <= 128 ? 2 : 1), CASE);
+    CHECK((p.nacc == 2 ? 2 * 128 : 256) + kTcS * 64 <= kTcTmemCols && p.nacc == (p.bx <= 128 ? 2 : 1), CASE);
     // accumulation chunks: 1024 K with two accumulators, 4096 K with one
     CHECK(p.kchunk == (p.nacc == 2 ? 4 : 16), CASE);
     CHECK(p.ntiles == (int)((N + kTcBW - 1) / kTcBW) && p.tiles == p.mtiles * p.ntiles, CASE);
