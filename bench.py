@@ -479,6 +479,7 @@ PREFILL_SHAPES = ((4096, 4096), (14336, 4096))
 PREFILL_MS = (16, 37, 64, 256, 1024)
 PREFILL_HEADLINE = "q8_0/int8_act/M1024/14336x4096"
 PREFILL_HEADLINE_F32 = "q8_0/f32_act/M1024/14336x4096"
+PREFILL_HEADLINE_Q4_K = "q4_k/int8_act/M1024/14336x4096"
 WARP_MMA_F16_PEAK = 605.0  # TFLOP/s, legacy warp-level f16 MMA on this GPU (register-only probe)
 
 
@@ -762,6 +763,10 @@ def run_ours(args):
                        "f32_act_point": PREFILL_HEADLINE_F32, "f32_act_TOPS": hf["TOPS"] if hf else None,
                        "f32_act_frac_of_bf16_peak": hf["frac_of_bf16_peak"] if hf else None,
                        "l2": "weights rotated over distinct buffers totalling > 2 x L2"}
+            hk = prefill_points.get(PREFILL_HEADLINE_Q4_K)
+            if hk:  # the same int8_act GEMM on the other headline weight type
+                prefill.update({"q4_k_point": PREFILL_HEADLINE_Q4_K, "q4_k_TOPS": hk["TOPS"],
+                                "q4_k_frac_of_bf16_peak": hk["frac_of_bf16_peak"]})
 
     small = small_configs(q, torch, stream) if not args.no_small else {}
     nxt = next_types(q, torch, stream) if not args.no_small else {}
