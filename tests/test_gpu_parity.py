@@ -531,6 +531,7 @@ FULL = [("q4_k", 28672, 8192, 8), ("q8_0", 28672, 8192, 8), ("q6_k", 28672, 8192
         ("q8_0", 14336, 4096, 256), ("q4_k", 4096, 4096, 256), ("q5_0", 14336, 4096, 256),
         ("q4_k", 14336, 4096, 37), ("q8_0", 14336, 4096, 64),
         ("q6_k", 14336, 4096, 256), ("q6_k", 4096, 4096, 1024),                        # tcgen05, Q6_K repacked
+        ("q6_k", 14336, 4096, 37),                                                      # exact / code GEMM, 64-row tiles
         ("q5_0", 49152, 576, 64),                                                       # streaming kernel (K % 256 != 0)
         ("q8_0", 4096, 4096, 16), ("q8_0", 49152, 576, 1), ("q5_0", 49152, 576, 1)]
 
