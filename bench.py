@@ -491,15 +491,15 @@ def prefill_kernel(t: str, mode: str, M: int) -> str:
     to 16 rows, the decode kernel."""
     if M <= 16:
         return "qmm_dmma_kernel"
-    if mode == "f32_act" and M > 64:
+    if mode == "f32_act" and (M > 64 or t in ("q4_0", "q5_0")):
         return "qmm_tc_kernel"
     return "qmm_tcx_kernel"
 
 
 def prefill_section(q, torch, stream, hbm_peak, bf16_peak):
     """Config 4: the Llama-shaped prefill GEMMs (4096 x 4096 and 14336 x 4096
-    weights; Q8_0, Q4_K, and Q6_K as a next type; M = 16, 37, 64, 256, 1024;
-    both forms).  Each point runs calls back to back over distinct quantized
+    weights; Q8_0, Q4_K at M = 16, 37, 64, 256, 1024, and Q6_K and Q5_0 as
+    next types at M = 37, 256, 1024; both forms).  Each point runs calls back to back over distinct quantized
     weight buffers that together exceed twice the L2 (so every call streams
     its weights from HBM), timed with CUDA events over the whole run.
     Reported per point: the kernel; algorithmic TOPS = 2 M N K / t and its
@@ -515,7 +515,7 @@ def prefill_section(q, torch, stream, hbm_peak, bf16_peak):
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     K = 4096
     cols = torch.from_numpy(qmm_synth.outlier_columns(K)).cuda()
-    for t in ("q8_0", "q4_k", "q6_k"):
+    for t in ("q8_0", "q4_k", "q6_k", "q5_0"):
         for N, _ in PREFILL_SHAPES:
             wbytes = N * q.row_bytes(t, K)
             nbuf = max(3, -(-2 * l2 // wbytes) + 1)
@@ -526,7 +526,7 @@ def prefill_section(q, torch, stream, hbm_peak, bf16_peak):
                 w[:, cols] *= 8.0
                 bufs.append(q.quantize_weights(w, t))
                 del w
-            Ms = PREFILL_MS if t != "q6_k" else (37, 256, 1024)
+            Ms = PREFILL_MS if t in ("q8_0", "q4_k") else (37, 256, 1024)
             for mode in MODES:
                 for M in Ms:
                     x = torch.from_numpy(qmm_synth.activations(M, K, outlier_channels=4)).cuda()

@@ -122,29 +122,9 @@ struct Dispatch {
 
 void plan_dispatch(int wt, int am, int epi, long long M, long long N, long long K, int sms, int smem, Dispatch& d) {
     d = Dispatch();
-    if (wt == T_Q4_0 || wt == T_Q5_0 || wt == T_Q6_K) {
-        // up to 16 rows on 16-row warp-MMA tiles; prefill on the tcgen05 GEMMs where K
-        // allows (K % 256 = 0: the Metal form, and Q6_K's CPU form with exact sums); the
-        // rest on the streaming kernel
-        if (M <= kDmmaMaxM && plan_dmma(wt, am, M, N, K, sms, smem, d.dp, epi == E_Y)) {
-            d.kind = KIND_DMMA;
-            d.workspace = d.dp.workspace;
-            d.launches = 1 + (d.dp.ext_bytes ? 1 : 0) + (epi == E_Y && d.dp.p.kslices > 1 ? 1 : 0);
-        } else if (epi == E_Y && am == A_F32 && M > kDecodeMaxM && plan_tc(wt, M, N, K, sms, smem, d.tp)) {
-            d.kind = KIND_TC;
-            d.workspace = d.tp.workspace;
-            d.launches = 2;  // operand preparation, GEMM
-        } else if (epi == E_Y && am == A_INT8 && M > kDecodeMaxM && plan_tcx(wt, A_INT8, M, N, K, sms, smem, d.xp)) {
-            d.kind = KIND_TCX;  // Q6_K's CPU-form prefill: exact sums on tcgen05
-            d.workspace = d.xp.workspace;
-            d.launches = 3;  // activation codes, repacked weights, GEMM
-        } else if (plan_stream(wt, am, epi, M, N, K, sms, smem, d.sp)) {
-            d.kind = KIND_STREAM;
-            d.workspace = epi == E_Y ? workspace_for(d.sp) : 0;
-            d.launches = 1;
-        }
-        return;
-    }
+    // Q4_0, Q5_0, Q6_K above 16 rows go to the GEMMs only (K % 256 = 0), else to the streaming kernel
+    const bool gemm_rows = M > kDecodeMaxM || wt == T_Q8_0 || wt == T_Q4_K;
+    const bool code_f32 = wt == T_Q8_0 || wt == T_Q4_K || wt == T_Q6_K;  // the code GEMM's f32_act types
     if (am == A_INT8 && wt == T_Q8_0 && M <= kGemvMaxM && plan_gemv(wt, M, N, K, sms, smem, d.gp)) {  // decode: whole-row weight stream
         d.kind = KIND_GEMV;
         d.launches = 1;
@@ -152,18 +132,19 @@ void plan_dispatch(int wt, int am, int epi, long long M, long long N, long long 
         d.kind = KIND_DMMA;
         d.workspace = d.dp.workspace;
         d.launches = 1 + (d.dp.ext_bytes ? 1 : 0) + (epi == E_Y && d.dp.p.kslices > 1 ? 1 : 0);
-    } else if (epi == E_Y && am == A_F32 && M <= 64 && plan_tcx(wt, A_F32, M, N, K, sms, smem, d.xp)) {
-        // Metal-form prefill up to 64 rows (Q8_0, Q4_K, Q6_K): exact f16 weight codes times two
-        // activation pieces on tcgen05 (Q4_K 1.3-1.6x the three-pass GEMM there, Q8_0 1.1x,
-        // Q6_K even; the three passes are faster from 256 rows on)
+    } else if (epi == E_Y && am == A_F32 && code_f32 && M <= 64 && plan_tcx(wt, A_F32, M, N, K, sms, smem, d.xp)) {
+        // Metal-form prefill up to 64 rows: exact f16 weight codes times two activation pieces on
+        // tcgen05 (Q4_K 1.3-1.6x the three-pass GEMM there, Q8_0 1.1x; the three passes are
+        // faster from 256 rows on)
         d.kind = KIND_TCX;
         d.workspace = d.xp.workspace;
         d.launches = wt == T_Q6_K ? 3 : 2;  // activation pieces, (Q6_K) repacked weights, GEMM
-    } else if (epi == E_Y && am == A_F32 && plan_tc(wt, M, N, K, sms, smem, d.tp)) {  // Metal-form prefill: tcgen05 GEMM
+    } else if (epi == E_Y && am == A_F32 && gemm_rows && plan_tc(wt, M, N, K, sms, smem, d.tp)) {  // Metal-form prefill: tcgen05 GEMM
         d.kind = KIND_TC;
         d.workspace = d.tp.workspace;
         d.launches = 2;  // operand preparation, GEMM
-    } else if (epi == E_Y && am == A_INT8 && plan_tcx(wt, A_INT8, M, N, K, sms, smem, d.xp)) {  // CPU-form prefill (Q8_0, Q4_K, Q6_K): exact sums on tcgen05
+    } else if (epi == E_Y && am == A_INT8 && gemm_rows && plan_tcx(wt, A_INT8, M, N, K, sms, smem, d.xp)) {
+        // CPU-form prefill: exact integer block sums on tcgen05
         d.kind = KIND_TCX;
         d.workspace = d.xp.workspace;
         d.launches = wt == T_Q6_K ? 3 : 2;  // activation codes, (Q6_K) repacked weights, GEMM

@@ -5,7 +5,13 @@
 namespace qmm {
 
 namespace {
-unsigned long long g_tcx_smem_done[12];
+unsigned long long g_tcx_smem_done[16];
+
+// the index of a (form, type, tile width) instance in g_tcx_smem_done
+constexpr int tcx_instance(int am, int wt, int nx) {
+    return (am == A_F32 ? 10 : 0) + 2 * (wt == T_Q8_0 ? 0 : wt == T_Q4_K ? 1 : wt == T_Q6_K ? 2 : wt == T_Q4_0 ? 3 : 4) +
+           (nx == 64 ? 1 : 0);
+}
 
 // the f32_act form: pieces of the activations, (Q6_K) repacked weights, then the GEMM
 template <int WT, int NX>
@@ -50,7 +56,7 @@ cudaError_t tcx_go_f32(const TcxPlan& pl, const void* wq, const float* x, void* 
     p.part = reinterpret_cast<float*>(wsb + pl.ws_part);
     p.cnt = cnt;
     auto* k = qmm_tcx_kernel<WT, NX, A_F32>;
-    e = ensure_smem(k, smem_max, g_tcx_smem_done[6 + 2 * (WT == T_Q8_0 ? 0 : WT == T_Q4_K ? 1 : 2) + (NX == 64 ? 1 : 0)]);
+    e = ensure_smem(k, smem_max, g_tcx_smem_done[tcx_instance(A_F32, WT, NX)]);
     if (e != cudaSuccess) return e;
     return launch_pdl(k, (unsigned)pl.grid, kTxThreads, pl.smem, s, tw, ta, ts, tb, p);
 }
@@ -67,7 +73,8 @@ cudaError_t tcx_go(const TcxPlan& pl, const void* wq, const float* x, void* ws, 
     unsigned* cnt = reinterpret_cast<unsigned*>(wsb + pl.ws_cnt);
     // 1. the activation operand: f16 codes [M][K], scales block-major, (Q4_K) sums of 16 codes;
     //    the split-K arrival counters zeroed
-    const long long items = WT == T_Q8_0 ? (long long)p0.M * (p0.K / 32) : (long long)p0.M * (p0.K / 256) * 32;
+    constexpr bool b32 = R::b32;
+    const long long items = b32 ? (long long)p0.M * (p0.K / 32) : (long long)p0.M * (p0.K / 256) * 32;
     tcx_act_kernel<WT><<<(unsigned)((items + 255) / 256), 256, 0, s>>>(x, p0.M, p0.K, pl.mp, codes, scales, bsums, cnt,
                                                                       p0.ks > 1 ? p0.tiles : 0);
     cudaError_t e = cudaGetLastError();
@@ -83,13 +90,13 @@ cudaError_t tcx_go(const TcxPlan& pl, const void* wq, const float* x, void* ws, 
     //    rows, 32-byte swizzle
     CUtensorMap tw, ta, ts, tb;
     const unsigned long long rb = (unsigned long long)p0.K / 256 * R::row;
-    const unsigned long long nsc = WT == T_Q8_0 ? p0.K / 32 : p0.K / 256;
+    const unsigned long long nsc = b32 ? p0.K / 32 : p0.K / 256;
     const void* wsrc = WT == T_Q6_K ? static_cast<const void*>(w6) : wq;
     bool ok = make_map(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT16, wsrc, rb / 2, p0.N, rb, R::row / 2, kTxW, CU_TENSOR_MAP_SWIZZLE_NONE) &&
               make_map(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, codes, p0.K, p0.M, (unsigned long long)p0.K * 2, 64, NX,
                        CU_TENSOR_MAP_SWIZZLE_128B) &&
               make_map(&ts, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, scales, pl.mp, nsc, (unsigned long long)pl.mp * 4, NX,
-                       WT == T_Q8_0 ? 8 : 1, CU_TENSOR_MAP_SWIZZLE_NONE);
+                       b32 ? 8 : 1, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (WT == T_Q4_K)
         ok = ok && make_map(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, bsums, p0.K / 16, p0.M, (unsigned long long)p0.K / 8, 16,
                             NX, CU_TENSOR_MAP_SWIZZLE_32B);
@@ -102,7 +109,7 @@ cudaError_t tcx_go(const TcxPlan& pl, const void* wq, const float* x, void* ws, 
     p.cnt = cnt;
     // 3. the GEMM, a programmatic dependent of the preparation
     auto* k = qmm_tcx_kernel<WT, NX, A_INT8>;
-    e = ensure_smem(k, smem_max, g_tcx_smem_done[(WT == T_Q8_0 ? 0 : WT == T_Q4_K ? 1 : 2) + (NX == 64 ? 3 : 0)]);
+    e = ensure_smem(k, smem_max, g_tcx_smem_done[tcx_instance(A_INT8, WT, NX)]);
     if (e != cudaSuccess) return e;
     return launch_pdl(k, (unsigned)pl.grid, kTxThreads, pl.smem, s, tw, ta, ts, tb, p);
 }
@@ -121,6 +128,8 @@ cudaError_t launch_tcx(int wt, const TcxPlan& pl, const void* wq, const float* x
     switch (wt) {
         case T_Q8_0: return n64 ? tcx_go<T_Q8_0, 64>(pl, wq, x, ws, y, smem_max, s) : tcx_go<T_Q8_0, 128>(pl, wq, x, ws, y, smem_max, s);
         case T_Q4_K: return n64 ? tcx_go<T_Q4_K, 64>(pl, wq, x, ws, y, smem_max, s) : tcx_go<T_Q4_K, 128>(pl, wq, x, ws, y, smem_max, s);
+        case T_Q4_0: return n64 ? tcx_go<T_Q4_0, 64>(pl, wq, x, ws, y, smem_max, s) : tcx_go<T_Q4_0, 128>(pl, wq, x, ws, y, smem_max, s);
+        case T_Q5_0: return n64 ? tcx_go<T_Q5_0, 64>(pl, wq, x, ws, y, smem_max, s) : tcx_go<T_Q5_0, 128>(pl, wq, x, ws, y, smem_max, s);
         default: return n64 ? tcx_go<T_Q6_K, 64>(pl, wq, x, ws, y, smem_max, s) : tcx_go<T_Q6_K, 128>(pl, wq, x, ws, y, smem_max, s);
     }
 }

@@ -85,31 +85,33 @@ constexpr int kTxThreads = (2 + kTxEpiWarps + kTxConvWarps) * 32;
 // activation scale (2^-s is applied at the store).
 template <int WT, int AM = A_INT8>
 struct TxRaw {
+    static constexpr bool b32 = WT == T_Q8_0 || WT == T_Q4_0 || WT == T_Q5_0;      // 32-value blocks, Q8_0 activations
+    static constexpr int bb = WT == T_Q8_0 ? 34 : WT == T_Q5_0 ? 22 : 18;           // bytes per 32-value block
     static constexpr int pieces = AM == A_F32 ? 2 : 1;                             // activation pieces
-    static constexpr int row = WT == T_Q8_0 ? 272 : WT == T_Q4_K ? 144 : 240;
+    static constexpr int row = b32 ? 8 * bb : WT == T_Q4_K ? 144 : 240;
     static constexpr int scales = kTxW * row;                                      // f(d_a) (int8_act)
     static constexpr int bsum = WT == T_Q4_K ? scales + 1024 : 0;                  // Q4_K: pieces x [128][16] f16
     static constexpr int amin = WT == T_Q4_K ? bsum + pieces * kTxX * 32 : 0;     // Q4_K: [128][16] f16
-    static constexpr int slot = WT == T_Q8_0 ? (scales + 8 * kTxX * 4 + 1023) / 1024 * 1024
+    static constexpr int slot = b32 ? (scales + 8 * kTxX * 4 + 1023) / 1024 * 1024
                                 : WT == T_Q4_K ? amin + kTxW * 32
                                                : (scales + kTxX * 4 + 1023) / 1024 * 1024;
     // bytes a raw stage's copies bring, for tiles of nx activation rows
     __host__ __device__ static constexpr int tx(int nx) {
         return AM == A_F32    ? kTxW * row + (WT == T_Q4_K ? pieces * nx * 32 : 0)
-               : WT == T_Q8_0 ? kTxW * row + 8 * nx * 4
+               : b32 ? kTxW * row + 8 * nx * 4
                : WT == T_Q4_K ? kTxW * row + nx * 4 + nx * 32
                               : kTxW * row + nx * 4;
     }
     // accumulators (drain units) per raw stage: Q8_0 one per block; Q4_K S_sc
     // and S_m; Q6_K S_a and S_b (S = 16 S_a + S_b)
-    static constexpr int drains = WT == T_Q8_0 ? 8 : 2;
+    static constexpr int drains = b32 ? 8 : 2;
     static constexpr int wtiles = WT == T_Q6_K ? 2 : 1;  // weight-code tiles per block stage
     // 32-value blocks per block stage (2 or 4): every handoff between the
     // roles covers that many blocks.  A stage holds bps / 2 "atoms" of 64 K,
     // each 128-byte swizzled rows: a weight tile of 128 rows and an
     // activation tile of nx rows per atom.
     __host__ __device__ static constexpr int bps(int nx) {
-        return AM == A_F32 ? (WT == T_Q4_K && nx == 64 ? 4 : 2) : WT == T_Q4_K || (WT == T_Q8_0 && nx == 64) ? 4 : 2;
+        return AM == A_F32 ? (WT == T_Q4_K && nx == 64 ? 4 : 2) : WT == T_Q4_K || (b32 && nx == 64) ? 4 : 2;
     }
     __host__ __device__ static constexpr int atoms(int nx) { return bps(nx) / 2; }
     __host__ __device__ static constexpr int wtile(int nx) { return atoms(nx) * kTxW * 128; }  // bytes of a weight tile
@@ -120,7 +122,8 @@ struct TxRaw {
 };
 static_assert(TxRaw<T_Q8_0>::slot % 1024 == 0 && TxRaw<T_Q4_K>::slot % 1024 == 0 && TxRaw<T_Q6_K>::slot % 1024 == 0 &&
                   TxRaw<T_Q8_0, A_F32>::slot % 1024 == 0 && TxRaw<T_Q4_K, A_F32>::slot % 1024 == 0 &&
-                  TxRaw<T_Q6_K, A_F32>::slot % 1024 == 0,
+                  TxRaw<T_Q6_K, A_F32>::slot % 1024 == 0 && TxRaw<T_Q4_0>::slot % 1024 == 0 &&
+                  TxRaw<T_Q5_0>::slot % 1024 == 0,
               "1 KB aligned raw slots");
 
 struct TcxParams {
@@ -168,14 +171,18 @@ __device__ __forceinline__ uint64_t tcx_sdesc32(uint32_t addr) {
            ((uint64_t)6 << 61);
 }
 
-// signed codes of a word (4 bytes) as two exact f16 pairs: bytes 0, 1 and 2, 3
-__device__ __forceinline__ void tcx_codes(uint32_t word, uint32_t& p01, uint32_t& p23) {
-    const uint32_t u = word ^ 0x80808080u;  // code + 128
+// codes biased by 128 (4 bytes of code + 128) as two exact f16 pairs: bytes 0, 1 and 2, 3
+__device__ __forceinline__ void tcx_codes_biased(uint32_t u, uint32_t& p01, uint32_t& p23) {
     uint32_t a = __byte_perm(u, 0x64646464u, 0x5140u), b = __byte_perm(u, 0x64646464u, 0x5342u);  // f16 1024 + (code + 128)
     const __half2 off = __half2half2(__ushort_as_half(0x6480));                                    // 1152
     const __half2 ha = __hsub2(*reinterpret_cast<__half2*>(&a), off), hb = __hsub2(*reinterpret_cast<__half2*>(&b), off);
     p01 = *reinterpret_cast<const uint32_t*>(&ha);
     p23 = *reinterpret_cast<const uint32_t*>(&hb);
+}
+
+// signed codes of a word (4 bytes) as two exact f16 pairs: bytes 0, 1 and 2, 3
+__device__ __forceinline__ void tcx_codes(uint32_t word, uint32_t& p01, uint32_t& p23) {
+    tcx_codes_biased(word ^ 0x80808080u, p01, p23);
 }
 
 // Q8_0 block J (0..7) of a 272-byte raw row (16-byte aligned) as 16 words of
@@ -262,9 +269,65 @@ __device__ __forceinline__ void tcx_conv_q6_k(const uint8_t* sbk, uint32_t ha[16
     }
 }
 
-// f(d) of Q8_0 block j of the raw row at `row` (2-byte aligned)
+// Q4_0 / Q5_0 block J (0..7) of a raw row (144 / 176 bytes, 16-byte aligned)
+// as 16 words of exact f16 code pairs, code - 8 (Q4_0) or code - 16 (Q5_0):
+// the 4-bit fields (value j in the low nibble of byte j, value j + 16 in its
+// high nibble) plus, for Q5_0, bit 4 from the block's word of fifth bits
+template <int WT, int J>
+__device__ __forceinline__ void tcx_conv_x_0(const uint8_t* row, uint32_t h[16]) {
+    constexpr int BB = WT == T_Q5_0 ? 22 : 18;  // bytes per block
+    constexpr int QS = WT == T_Q5_0 ? 6 : 2;    // offset of the 16 nibble bytes
+    constexpr int A = (BB * J) & ~15, O = BB * J - A;
+    constexpr int NC = (O + BB + 15) / 16;      // 16-byte chunks covering the block
+    uint32_t w[12];
+#pragma unroll
+    for (int c = 0; c < 3; ++c) {
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (c < NC) v = *reinterpret_cast<const uint4*>(row + A + 16 * c);
+        w[4 * c] = v.x;
+        w[4 * c + 1] = v.y;
+        w[4 * c + 2] = v.z;
+        w[4 * c + 3] = v.w;
+    }
+    constexpr int QW = (O + QS) / 4, QSH = 8 * ((O + QS) % 4);
+    static_assert(QW + 4 + (QSH != 0 ? 1 : 0) <= 12, "the chunks hold the block");
+    uint32_t q[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        if constexpr (QSH != 0) q[i] = __funnelshift_r(w[QW + i], w[QW + i + 1], QSH);
+        else q[i] = w[QW + i];
+    }
+    uint32_t hb = 0;
+    if constexpr (WT == T_Q5_0) {
+        constexpr int HW = (O + 2) / 4, HSH = 8 * ((O + 2) % 4);
+        if constexpr (HSH != 0) hb = __funnelshift_r(w[HW], w[HW + 1], HSH);
+        else hb = w[HW];
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        // values 4k..4k+3: low nibbles of word k (k < 4) or high nibbles of word k - 4
+        uint32_t word = k < 4 ? (q[k & 3] & 0x0F0F0F0Fu) : ((q[k & 3] >> 4) & 0x0F0F0F0Fu);
+        if constexpr (WT == T_Q5_0) {
+            word |= ((((hb >> (4 * k)) & 0xFu) * 0x00204081u) & 0x01010101u) << 4;  // bit 4 of each byte
+            word += 0x70707070u;  // code - 16 + 128
+        } else {
+            word += 0x78787878u;  // code - 8 + 128
+        }
+        tcx_codes_biased(word, h[2 * k], h[2 * k + 1]);
+    }
+}
+
+// a 32-value block type's block J as exact f16 codes
+template <int WT, int J>
+__device__ __forceinline__ void tcx_conv_b32(const uint8_t* row, uint32_t h[16]) {
+    if constexpr (WT == T_Q8_0) tcx_conv_q8_0<J>(row, h);
+    else tcx_conv_x_0<WT, J>(row, h);
+}
+
+// f(d) of 32-value block j (BB bytes each, d first) of the raw row at `row`
+template <int BB>
 __device__ __forceinline__ float tcx_block_scale(const uint8_t* row, int j) {
-    return h2f(*reinterpret_cast<const uint16_t*>(row + 34 * j));
+    return h2f(*reinterpret_cast<const uint16_t*>(row + BB * j));
 }
 
 // K split: y of a tile (rows m0.., n0..) as the sum of its ks partial tiles in
@@ -300,12 +363,13 @@ __device__ __forceinline__ void tcx_fixup(const float* __restrict__ part, float*
 // tensor maps: tw raw weight rows; ta activation codes (f32_act: the hi pieces); ts
 // int8_act: activation scales, f32_act: the lo pieces; tb Q4_K: sums of 16 codes
 // (f32_act: hi sums, then lo sums, along each row)
-template <int WT, int NX, int AM>  // T_Q8_0, T_Q4_K or T_Q6_K; tiles of NX = 64 or 128 activation rows; A_INT8 or A_F32
+template <int WT, int NX, int AM>  // T_Q8_0, T_Q4_0, T_Q5_0 (int8_act), T_Q4_K or T_Q6_K; tiles of NX = 64 or 128 rows; A_INT8 or A_F32
 __global__ void __launch_bounds__(kTxThreads, 1)
     qmm_tcx_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUtensorMap ta,
                    const __grid_constant__ CUtensorMap ts, const __grid_constant__ CUtensorMap tb, const TcxParams p) {
     using R = TxRaw<WT, AM>;
     constexpr bool kF32 = AM == A_F32;
+    constexpr bool kB32 = R::b32;  // Q8_0, Q4_0, Q5_0: a fold per 32-value block
     static_assert(NX == 64 || NX == 128, "tile widths");
     constexpr int kAcc = kTxTmemCols / NX;  // TMEM accumulators
     constexpr int CW = NX / 4;              // accumulator columns an epilogue warp drains
@@ -393,7 +457,7 @@ __global__ void __launch_bounds__(kTxThreads, 1)
                                 tma_2d(smem_u32(raw(rs) + R::bsum), &tb, 16 * ir, im0, fb);
                                 tma_2d(smem_u32(raw(rs) + R::bsum + kTxX * 32), &tb, p.K / 16 + 16 * ir, im0, fb);
                             }
-                        } else if (WT == T_Q8_0) {
+                        } else if (kB32) {
                             tma_2d(smem_u32(raw(rs) + R::scales), &ts, im0, 8 * ir, fb);
                         } else {
                             tma_2d(smem_u32(raw(rs) + R::scales), &ts, im0, ir, fb);
@@ -444,12 +508,12 @@ __global__ void __launch_bounds__(kTxThreads, 1)
                 tcx_slice(p, u, tile, r0, r1);
                 for (int r = r0; r < r1 && ok; ++r, ++rg) {
                     uint32_t dcol = 0, dcol2 = 0;
-                    if (WT != T_Q8_0) dcol = acc_take(du);                // S_sc (Q4_K), S_a (Q6_K)
+                    if (!kB32) dcol = acc_take(du);                       // S_sc (Q4_K), S_a (Q6_K)
                     if (WT == T_Q6_K && ok) dcol2 = acc_take(du + 1);    // S_b
                     for (int j = 0; j < kSpr && ok; ++j, ++g) {  // block stages: blocks kBps j ..
                         const int s = (int)(g % kTxS);
                         uint32_t dq[kBps];  // Q8_0: the accumulator of each block of the stage
-                        if (WT == T_Q8_0) {
+                        if (kB32) {
 #pragma unroll
                             for (int b = 0; b < kBps; ++b)
                                 if (ok) dq[b] = acc_take(du + kBps * j + b);
@@ -463,8 +527,8 @@ __global__ void __launch_bounds__(kTxThreads, 1)
                         // K = 16 steps ks: atom ks / 4, 32 bytes each along its 128-byte swizzled rows
 #pragma unroll
                         for (int ks = 0; ks < 2 * kBps; ++ks) {
-                            const uint32_t col = WT == T_Q8_0 ? dq[ks >> 1] : dcol;
-                            const uint32_t accu = WT == T_Q8_0 ? (uint32_t)(ks & 1) : (uint32_t)(j | ks);
+                            const uint32_t col = kB32 ? dq[ks >> 1] : dcol;
+                            const uint32_t accu = kB32 ? (uint32_t)(ks & 1) : (uint32_t)(j | ks);
                             const uint32_t wk = wa + (ks >> 2) * kTxW * 128 + 32 * (ks & 3);
                             const uint32_t xk = xb + (ks >> 2) * NX * 128 + 32 * (ks & 3);
                             tcx_mma(tmem + col, tc_sdesc128(wk), tc_sdesc128(xk), idesc, accu);
@@ -478,7 +542,7 @@ __global__ void __launch_bounds__(kTxThreads, 1)
                             }
                         }
                         tc_commit(smem_u32(&empty[s]));
-                        if (WT == T_Q8_0) {
+                        if (kB32) {
 #pragma unroll
                             for (int b = 0; b < kBps; ++b) tc_commit(smem_u32(&acc_full[(du + kBps * j + b) % kAcc]));
                         }
@@ -544,7 +608,7 @@ __global__ void __launch_bounds__(kTxThreads, 1)
                 const int rs = (int)(rg % p.nraw);
                 const uint8_t* wrow = raw(rs) + nl * R::row;
                 const float* asc = reinterpret_cast<const float*>(raw(rs) + R::scales) + CW * cq;
-                if (WT == T_Q8_0) {
+                if (kB32) {
                     for (int j = 0; j < 8; ++j, ++du) {
                         const uint32_t acol = acc_wait(du);
                         if (!ok) break;
@@ -556,7 +620,7 @@ __global__ void __launch_bounds__(kTxThreads, 1)
                         tc_wait_ld();
                         acc_release(du);
                         // fold: y += isum f(d_w) f(d_a)
-                        const float dw = tcx_block_scale(wrow, j);
+                        const float dw = tcx_block_scale<R::bb>(wrow, j);
                         const unsigned long long dw2 = f2pack(dw, dw);
                         const float* aj = asc + j * NX;
 #pragma unroll
@@ -750,15 +814,15 @@ __global__ void __launch_bounds__(kTxThreads, 1)
                         for (int c = 0; c < 4; ++c)
                             *reinterpret_cast<uint4*>(a2 + (((c0 + c) ^ sw) << 4)) =
                                 make_uint4(h2[4 * c], h2[4 * c + 1], h2[4 * c + 2], h2[4 * c + 3]);
-                    } else if (WT == T_Q8_0) {
-                        if (j == 0) tcx_conv_q8_0<0>(wrow, h);
-                        else if (j == 1) tcx_conv_q8_0<1>(wrow, h);
-                        else if (j == 2) tcx_conv_q8_0<2>(wrow, h);
-                        else if (j == 3) tcx_conv_q8_0<3>(wrow, h);
-                        else if (j == 4) tcx_conv_q8_0<4>(wrow, h);
-                        else if (j == 5) tcx_conv_q8_0<5>(wrow, h);
-                        else if (j == 6) tcx_conv_q8_0<6>(wrow, h);
-                        else tcx_conv_q8_0<7>(wrow, h);
+                    } else if (kB32) {
+                        if (j == 0) tcx_conv_b32<WT, 0>(wrow, h);
+                        else if (j == 1) tcx_conv_b32<WT, 1>(wrow, h);
+                        else if (j == 2) tcx_conv_b32<WT, 2>(wrow, h);
+                        else if (j == 3) tcx_conv_b32<WT, 3>(wrow, h);
+                        else if (j == 4) tcx_conv_b32<WT, 4>(wrow, h);
+                        else if (j == 5) tcx_conv_b32<WT, 5>(wrow, h);
+                        else if (j == 6) tcx_conv_b32<WT, 6>(wrow, h);
+                        else tcx_conv_b32<WT, 7>(wrow, h);
                     } else {
                         if (j == 0) tcx_conv_q4_k<0>(wrow, h);
                         else if (j == 1) tcx_conv_q4_k<1>(wrow, h);
@@ -807,7 +871,7 @@ __global__ void tcx_act_kernel(const float* __restrict__ x, int M, int K, int mp
     grid_dep_launch();
     for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < ncnt; i += (long long)gridDim.x * blockDim.x)
         cnt[i] = 0u;
-    if (WT == T_Q8_0) {
+    if (WT == T_Q8_0 || WT == T_Q4_0 || WT == T_Q5_0) {  // Q8_0 activations
         const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
         const int nb = K / 32;
         if (i >= (long long)M * nb) return;
@@ -960,15 +1024,33 @@ struct TcxPlan {
 
 template <int AM>
 inline int tcx_raw_slot_am(int wt) {
-    return wt == T_Q8_0 ? TxRaw<T_Q8_0, AM>::slot : wt == T_Q4_K ? TxRaw<T_Q4_K, AM>::slot : TxRaw<T_Q6_K, AM>::slot;
+    switch (wt) {
+        case T_Q8_0: return TxRaw<T_Q8_0, AM>::slot;
+        case T_Q4_0: return TxRaw<T_Q4_0, AM>::slot;
+        case T_Q5_0: return TxRaw<T_Q5_0, AM>::slot;
+        case T_Q4_K: return TxRaw<T_Q4_K, AM>::slot;
+        default: return TxRaw<T_Q6_K, AM>::slot;
+    }
 }
 template <int AM>
 inline int tcx_stages_am(int wt, int nx) {
-    return wt == T_Q8_0 ? TxRaw<T_Q8_0, AM>::stages(nx) : wt == T_Q4_K ? TxRaw<T_Q4_K, AM>::stages(nx) : TxRaw<T_Q6_K, AM>::stages(nx);
+    switch (wt) {
+        case T_Q8_0: return TxRaw<T_Q8_0, AM>::stages(nx);
+        case T_Q4_0: return TxRaw<T_Q4_0, AM>::stages(nx);
+        case T_Q5_0: return TxRaw<T_Q5_0, AM>::stages(nx);
+        case T_Q4_K: return TxRaw<T_Q4_K, AM>::stages(nx);
+        default: return TxRaw<T_Q6_K, AM>::stages(nx);
+    }
 }
 template <int AM>
 inline int tcx_stage_bytes_am(int wt, int nx) {
-    return wt == T_Q8_0 ? TxRaw<T_Q8_0, AM>::stage(nx) : wt == T_Q4_K ? TxRaw<T_Q4_K, AM>::stage(nx) : TxRaw<T_Q6_K, AM>::stage(nx);
+    switch (wt) {
+        case T_Q8_0: return TxRaw<T_Q8_0, AM>::stage(nx);
+        case T_Q4_0: return TxRaw<T_Q4_0, AM>::stage(nx);
+        case T_Q5_0: return TxRaw<T_Q5_0, AM>::stage(nx);
+        case T_Q4_K: return TxRaw<T_Q4_K, AM>::stage(nx);
+        default: return TxRaw<T_Q6_K, AM>::stage(nx);
+    }
 }
 inline int tcx_raw_slot(int wt, int am) { return am == A_F32 ? tcx_raw_slot_am<A_F32>(wt) : tcx_raw_slot_am<A_INT8>(wt); }
 inline int tcx_stages(int wt, int am, int nx) { return am == A_F32 ? tcx_stages_am<A_F32>(wt, nx) : tcx_stages_am<A_INT8>(wt, nx); }
@@ -977,7 +1059,9 @@ inline int tcx_stage_bytes(int wt, int am, int nx) {
 }
 
 inline bool plan_tcx(int wt, int am, long long M, long long N, long long K, int sm_count, int smem_max, TcxPlan& out) {
-    if ((wt != T_Q8_0 && wt != T_Q4_K && wt != T_Q6_K) || K % 256 != 0 || M < 17 ||
+    // int8_act: Q8_0, Q4_0, Q5_0, Q4_K, Q6_K; f32_act: Q8_0, Q4_K, Q6_K
+    const bool b32 = wt == T_Q8_0 || wt == T_Q4_0 || wt == T_Q5_0;
+    if ((!b32 && wt != T_Q4_K && wt != T_Q6_K) || (am == A_F32 && (wt == T_Q4_0 || wt == T_Q5_0)) || K % 256 != 0 || M < 17 ||
         K > (1 << 26) || M > (1 << 24) || N > (1 << 24))
         return false;
     TcxPlan pl{};
@@ -1027,7 +1111,7 @@ inline bool plan_tcx(int wt, int am, long long M, long long N, long long K, int 
     auto r256 = [](size_t v) { return (v + 255) / 256 * 256; };
     pl.ws_codes = 0;
     pl.ws_scales = r256((size_t)M * K * 2);
-    const size_t per = wt == T_Q8_0 ? 32 : 256;  // values per activation scale
+    const size_t per = b32 ? 32 : 256;  // values per activation scale
     pl.ws_bsums = pl.ws_scales + (am == A_F32 ? r256((size_t)M * K * 2) : r256((size_t)(K / per) * pl.mp * 4));
     pl.ws_ais = pl.ws_bsums + (wt == T_Q4_K || (wt == T_Q6_K && am == A_INT8) ? r256((size_t)M * (K / 16) * 2 * (am == A_F32 ? 2 : 1)) : 0);
     pl.ws_w6 = pl.ws_ais + (am == A_F32 ? r256((size_t)M * 4) : 0);

@@ -220,7 +220,7 @@ int main() {
             for (long long N : {128, 300, 4096, 14336})
                 for (long long K : {256, 1024, 4096, 14336}) {
                     plans += check_tc(wt, M, N, K);
-                    if (wt == T_Q8_0 || wt == T_Q4_K || wt == T_Q6_K) plans += check_tcx(wt, A_INT8, M, N, K);
+                    plans += check_tcx(wt, A_INT8, M, N, K);
                     if (wt == T_Q8_0 || wt == T_Q4_K || wt == T_Q6_K) plans += check_tcx(wt, A_F32, M, N, K);
                 }
     }
@@ -246,8 +246,7 @@ int main() {
     for (long long M : {37, 64, 256, 1024})
         for (int wt : types) {
             CHECK(plan_tc(wt, M, 14336, 4096, kSms, kSmem, tp), "no tcgen05 plan for %s M%lld", tname(wt), M);
-            if (wt == T_Q8_0 || wt == T_Q4_K || wt == T_Q6_K)
-                CHECK(plan_tcx(wt, A_INT8, M, 14336, 4096, kSms, kSmem, xp), "no exact prefill plan for %s M%lld", tname(wt), M);
+            CHECK(plan_tcx(wt, A_INT8, M, 14336, 4096, kSms, kSmem, xp), "no exact prefill plan for %s M%lld", tname(wt), M);
             if (wt == T_Q4_K)
                 CHECK(plan_tcx(wt, A_F32, M, 14336, 4096, kSms, kSmem, xp), "no f32_act code-GEMM plan for M%lld", M);
         }

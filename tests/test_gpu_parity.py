@@ -430,6 +430,8 @@ def test_launch_counts(qmm):
     assert qmm.matmul_launches("q8_0", "f32_act", 256, 4096, 4096) == 2   # tcgen05: operand pieces + GEMM
     assert qmm.matmul_launches("q4_k", "int8_act", 256, 4096, 4096) == 2  # exact tcgen05: activation codes + GEMM
     assert qmm.matmul_launches("q4_k", "f32_act", 64, 4096, 4096) == 2    # code GEMM: activation pieces + GEMM
+    assert qmm.matmul_launches("q6_k", "f32_act", 64, 4096, 4096) == 3    # code GEMM: pieces, repack, GEMM
+    assert qmm.matmul_launches("q5_0", "int8_act", 64, 4096, 4096) == 2   # exact tcgen05: activation codes + GEMM
     assert qmm.matmul_launches("q6_k", "int8_act", 256, 4096, 4096) == 3  # exact tcgen05: codes, repack, GEMM
     assert qmm.matmul_launches("q6_k", "int8_act", 16, 4096, 4096) == 1   # up to 16 rows: the decode kernel
     assert qmm.matmul_launches("q8_0", "int8_act", 1, 100, 100) == 0      # K not a multiple of 32
