@@ -149,7 +149,8 @@ size_t qmm_matmul_workspace(qmm_type wtype, qmm_act_mode mode, int64_t M, int64_
 /* Number of kernel launches one qmm_matmul call makes for this shape on the
    current device (decode: an activation-preparing kernel for large weight
    matrices, the decode kernel, a K-split reduction; prefill: the activation
-   operand and the GEMM).  0 for an invalid shape or type.  Launches nothing.
+   operand, for Q6_K its weights repacked to 16-byte aligned slots, and the
+   GEMM).  0 for an invalid shape or type.  Launches nothing.
    (A diagnostic of this library; the pages have no counterpart.) */
 int qmm_matmul_launches(qmm_type wtype, qmm_act_mode mode, int64_t M, int64_t N, int64_t K);
 
