@@ -16,7 +16,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libqmm.so")
 ROOT = os.path.dirname(HERE)
-UNITS = ["qmm_api", "qmm_quant", "qmm_stream_q8_0", "qmm_stream_q4_k", "qmm_stream_x_0", "qmm_stream_q6_k", "qmm_gemv_q8_0", "qmm_gemv_q4_k", "qmm_dmma", "qmm_dmma_x_0", "qmm_dmma_q6_k", "qmm_tc", "qmm_tcx", "qmm_static_ws", "qmm_batch", "qmm_batch_mix"]
+UNITS = ["qmm_api", "qmm_quant", "qmm_stream_q8_0", "qmm_stream_q4_k", "qmm_stream_x_0", "qmm_stream_q6_k", "qmm_gemv_q8_0", "qmm_gemv_q4_k", "qmm_dmma", "qmm_dmma_x_0", "qmm_dmma_q6_k", "qmm_tc", "qmm_tcx", "qmm_tcx_f32", "qmm_static_ws", "qmm_batch", "qmm_batch_mix"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v"]
 

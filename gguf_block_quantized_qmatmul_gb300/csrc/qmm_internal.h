@@ -28,6 +28,8 @@ cudaError_t launch_dmma_prep(int wt, int am, const DmmaPlan& plan, void* ext, cu
 cudaError_t launch_tc(int wt, const TcPlan& plan, const void* wq, const float* x, void* ws, float* y, int smem_max,
                       cudaStream_t s);
 cudaError_t launch_tcx(int wt, const TcxPlan& plan, const void* wq, const float* x, void* ws, float* y, int smem_max, cudaStream_t s);
+cudaError_t launch_tcx_f32(int wt, const TcxPlan& plan, const void* wq, const float* x, void* ws, float* y, int smem_max,
+                           cudaStream_t s);
 // A 2-D tensor map (rows of `inner` elements, `row_bytes` apart) with a box
 // of box_inner x box_outer elements; false when the driver refuses it.
 bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, unsigned long long inner, unsigned long long outer,
