@@ -427,6 +427,13 @@ __global__ void __launch_bounds__(kTxThreads, 1)
     auto xstage = [&](int s) { return sm + s * R::stage(NX) + R::wtiles * R::wtile(NX); };  // B: activation codes
     constexpr int kBps = R::bps(NX);        // blocks per block stage
     constexpr int kSpr = 8 / kBps;          // block stages per raw stage
+    // 32-value types at 64-row tiles: the accumulators of two consecutive blocks are
+    // one drain group, handed over with one commit and one release (barriers
+    // 0 .. kGrp - 1), and the epilogue loads both before one wait; 128-row tiles,
+    // with half as many accumulators and twice the columns, hand each over alone
+    constexpr int kG = kB32 && NX == 64 ? 2 : 1;
+    constexpr int kGrp = kAcc / kG;
+    static_assert(kBps % kG == 0 && kAcc % kG == 0, "accumulator groups");
     auto raw = [&](int s) { return sm + p.off_raw + s * R::slot; };
 
     if (warp == 0) {
@@ -513,10 +520,15 @@ __global__ void __launch_bounds__(kTxThreads, 1)
                     for (int j = 0; j < kSpr && ok; ++j, ++g) {  // block stages: blocks kBps j ..
                         const int s = (int)(g % kTxS);
                         uint32_t dq[kBps];  // Q8_0: the accumulator of each block of the stage
+                        const uint32_t d0 = du + kBps * j;  // the stage's first accumulator (a group start)
                         if (kB32) {
 #pragma unroll
-                            for (int b = 0; b < kBps; ++b)
-                                if (ok) dq[b] = acc_take(du + kBps * j + b);
+                            for (int b = 0; b < kBps; b += kG)
+                                if (ok && d0 + b >= kAcc)
+                                    ok = mbar_wait(smem_u32(&acc_empty[((d0 + b) / kG) % kGrp]),
+                                                   (uint32_t)((((d0 + b) / kAcc) - 1) & 1), flags, p.err);
+#pragma unroll
+                            for (int b = 0; b < kBps; ++b) dq[b] = (uint32_t)(((d0 + b) % kAcc) * NX);
                         }
                         if (!ok) break;
                         const uint32_t nxt = mbar_test(smem_u32(&full[(g + 1) % kTxS]), (uint32_t)(((g + 1) / kTxS) & 1));
@@ -544,7 +556,7 @@ __global__ void __launch_bounds__(kTxThreads, 1)
                         tc_commit(smem_u32(&empty[s]));
                         if (kB32) {
 #pragma unroll
-                            for (int b = 0; b < kBps; ++b) tc_commit(smem_u32(&acc_full[(du + kBps * j + b) % kAcc]));
+                            for (int b = 0; b < kBps; b += kG) tc_commit(smem_u32(&acc_full[((d0 + b) / kG) % kGrp]));
                         }
                         ready = nxt;
                     }
@@ -573,7 +585,9 @@ __global__ void __launch_bounds__(kTxThreads, 1)
             }
             // the last commits must land before TMEM is released
             if (g > 0) mbar_drain(smem_u32(&empty[(g - 1) % kTxS]), (uint32_t)(((g - 1) / kTxS) & 1), flags, p.err);
-            if (du > 0) mbar_drain(smem_u32(&acc_full[(du - 1) % kAcc]), (uint32_t)(((du - 1) / kAcc) & 1), flags, p.err);
+            if (du > 0)
+                mbar_drain(smem_u32(&acc_full[((du - 1) / kG) % kGrp]),
+                           (uint32_t)(((du - 1) / kAcc) & 1), flags, p.err);
         }
     } else if (warp < 2 + kTxEpiWarps) {
         // ------------------------------ epilogue ------------------------------
@@ -609,31 +623,40 @@ __global__ void __launch_bounds__(kTxThreads, 1)
                 const uint8_t* wrow = raw(rs) + nl * R::row;
                 const float* asc = reinterpret_cast<const float*>(raw(rs) + R::scales) + CW * cq;
                 if (kB32) {
-                    for (int j = 0; j < 8; ++j, ++du) {
-                        const uint32_t acol = acc_wait(du);
+                    for (int j = 0; j < 8; j += kG, du += kG) {  // a drain group: blocks j .. j + kG - 1
+                        ok = mbar_wait(smem_u32(&acc_full[(du / kG) % kGrp]), (uint32_t)((du / kAcc) & 1), flags, p.err);
                         if (!ok) break;
                         tc_fence_after();
                         __syncwarp();
-                        uint32_t vv[CW];
+                        uint32_t vv[kG][CW];
 #pragma unroll
-                        for (int h = 0; h < CW / 16; ++h) tc_ld16(acol + 16 * h, vv + 16 * h);
+                        for (int b = 0; b < kG; ++b) {
+                            const uint32_t acol = tmem + tq + (uint32_t)(((du + b) % kAcc) * NX + CW * cq);
+#pragma unroll
+                            for (int h = 0; h < CW / 16; ++h) tc_ld16(acol + 16 * h, vv[b] + 16 * h);
+                        }
                         tc_wait_ld();
-                        acc_release(du);
-                        // fold: y += isum f(d_w) f(d_a)
-                        const float dw = tcx_block_scale<R::bb>(wrow, j);
-                        const unsigned long long dw2 = f2pack(dw, dw);
-                        const float* aj = asc + j * NX;
+                        tc_fence_before();  // the group's accumulators go back to the MMAs
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(smem_u32(&acc_empty[(du / kG) % kGrp]));
 #pragma unroll
-                        for (int c = 0; c < CW / 4; ++c) {
-                            const uint32_t* v = vv + 4 * c;
-                            if constexpr (kF32) {  // y 2^s += S f(d_w) (sums of x 2^s)
-                                acc[2 * c] = fma2(f2pack(__uint_as_float(v[0]), __uint_as_float(v[1])), dw2, acc[2 * c]);
-                                acc[2 * c + 1] = fma2(f2pack(__uint_as_float(v[2]), __uint_as_float(v[3])), dw2, acc[2 * c + 1]);
-                            } else {
-                                const float4 a4 = *reinterpret_cast<const float4*>(aj + 4 * c);
-                                const unsigned long long s01 = mul2(f2pack(a4.x, a4.y), dw2), s23 = mul2(f2pack(a4.z, a4.w), dw2);
-                                acc[2 * c] = fma2(f2pack(__uint_as_float(v[0]), __uint_as_float(v[1])), s01, acc[2 * c]);
-                                acc[2 * c + 1] = fma2(f2pack(__uint_as_float(v[2]), __uint_as_float(v[3])), s23, acc[2 * c + 1]);
+                        for (int b = 0; b < kG; ++b) {
+                            // fold: y += isum f(d_w) f(d_a)
+                            const float dw = tcx_block_scale<R::bb>(wrow, j + b);
+                            const unsigned long long dw2 = f2pack(dw, dw);
+                            const float* aj = asc + (j + b) * NX;
+#pragma unroll
+                            for (int c = 0; c < CW / 4; ++c) {
+                                const uint32_t* v = vv[b] + 4 * c;
+                                if constexpr (kF32) {  // y 2^s += S f(d_w) (sums of x 2^s)
+                                    acc[2 * c] = fma2(f2pack(__uint_as_float(v[0]), __uint_as_float(v[1])), dw2, acc[2 * c]);
+                                    acc[2 * c + 1] = fma2(f2pack(__uint_as_float(v[2]), __uint_as_float(v[3])), dw2, acc[2 * c + 1]);
+                                } else {
+                                    const float4 a4 = *reinterpret_cast<const float4*>(aj + 4 * c);
+                                    const unsigned long long s01 = mul2(f2pack(a4.x, a4.y), dw2), s23 = mul2(f2pack(a4.z, a4.w), dw2);
+                                    acc[2 * c] = fma2(f2pack(__uint_as_float(v[0]), __uint_as_float(v[1])), s01, acc[2 * c]);
+                                    acc[2 * c + 1] = fma2(f2pack(__uint_as_float(v[2]), __uint_as_float(v[3])), s23, acc[2 * c + 1]);
+                                }
                             }
                         }
                     }
