@@ -427,11 +427,13 @@ __global__ void __launch_bounds__(kTxThreads, 1)
     auto xstage = [&](int s) { return sm + s * R::stage(NX) + R::wtiles * R::wtile(NX); };  // B: activation codes
     constexpr int kBps = R::bps(NX);        // blocks per block stage
     constexpr int kSpr = 8 / kBps;          // block stages per raw stage
-    // 32-value types at 64-row tiles: the accumulators of two consecutive blocks are
-    // one drain group, handed over with one commit and one release (barriers
-    // 0 .. kGrp - 1), and the epilogue loads both before one wait; 128-row tiles,
-    // with half as many accumulators and twice the columns, hand each over alone
-    constexpr int kG = kB32 && NX == 64 ? 2 : 1;
+    // Drain groups: accumulators handed from the MMAs to the epilogue with one
+    // commit and returned with one release (barriers 0 .. kGrp - 1).  A super-block's
+    // two (Q4_K S_sc and S_m, Q6_K S_a and S_b) are one group; so are two
+    // consecutive 32-value blocks at 64-row tiles, whose epilogue loads both before
+    // one wait; 128-row tiles, with half as many accumulators and twice the columns,
+    // hand each 32-value block over alone.
+    constexpr int kG = kB32 && NX == 128 ? 1 : 2;
     constexpr int kGrp = kAcc / kG;
     static_assert(kBps % kG == 0 && kAcc % kG == 0, "accumulator groups");
     auto raw = [&](int s) { return sm + p.off_raw + s * R::slot; };
@@ -506,17 +508,15 @@ __global__ void __launch_bounds__(kTxThreads, 1)
             uint32_t du = 0;          // drain units (a launch drains far fewer than 2^32)
             bool ok = true;
             uint32_t ready = 0;  // the next stage's barrier, tested ahead
-            auto acc_take = [&](uint32_t d) {  // accumulator d % kAcc, once the epilogue drained its last use
-                if (d >= kAcc) ok = mbar_wait(smem_u32(&acc_empty[d % kAcc]), (uint32_t)(((d / kAcc) - 1) & 1), flags, p.err);
-                return (uint32_t)((d % kAcc) * NX);
-            };
             for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
                 int tile, r0, r1;
                 tcx_slice(p, u, tile, r0, r1);
                 for (int r = r0; r < r1 && ok; ++r, ++rg) {
-                    uint32_t dcol = 0, dcol2 = 0;
-                    if (!kB32) dcol = acc_take(du);                       // S_sc (Q4_K), S_a (Q6_K)
-                    if (WT == T_Q6_K && ok) dcol2 = acc_take(du + 1);    // S_b
+                    // super-blocks: S_sc and S_m (Q4_K), S_a and S_b (Q6_K), once the epilogue
+                    // drained the group's last use
+                    const uint32_t dcol = (uint32_t)((du % kAcc) * NX), dcol2 = (uint32_t)(((du + 1) % kAcc) * NX);
+                    if (!kB32 && du >= kAcc)
+                        ok = mbar_wait(smem_u32(&acc_empty[(du / kG) % kGrp]), (uint32_t)(((du / kAcc) - 1) & 1), flags, p.err);
                     for (int j = 0; j < kSpr && ok; ++j, ++g) {  // block stages: blocks kBps j ..
                         const int s = (int)(g % kTxS);
                         uint32_t dq[kBps];  // Q8_0: the accumulator of each block of the stage
@@ -561,14 +561,10 @@ __global__ void __launch_bounds__(kTxThreads, 1)
                         ready = nxt;
                     }
                     if (!ok) break;
-                    if (WT == T_Q6_K) {
-                        tc_commit(smem_u32(&acc_full[du % kAcc]));
-                        tc_commit(smem_u32(&acc_full[(du + 1) % kAcc]));
-                    }
+                    if (WT == T_Q6_K) tc_commit(smem_u32(&acc_full[(du / kG) % kGrp]));
                     if (WT == T_Q4_K) {
-                        tc_commit(smem_u32(&acc_full[du % kAcc]));
                         // S_m = sum_j m_j bsum_j: one K 16 MMA over the 16 sums of 16 codes
-                        const uint32_t mcol = acc_take(du + 1);
+                        const uint32_t mcol = dcol2;
                         const int rs = (int)(rg % p.nraw);
                         if (ok) ok = mbar_wait(smem_u32(&min_ready[rs]), (uint32_t)((rg / p.nraw) & 1), flags, p.err);
                         if (!ok) break;
@@ -578,7 +574,7 @@ __global__ void __launch_bounds__(kTxThreads, 1)
                         if (kF32)
                             tcx_mma(tmem + mcol, tcx_sdesc32(smem_u32(raw(rs) + R::amin)),
                                     tcx_sdesc32(smem_u32(raw(rs) + R::bsum + kTxX * 32)), idesc, 1u);
-                        tc_commit(smem_u32(&acc_full[(du + 1) % kAcc]));
+                        tc_commit(smem_u32(&acc_full[(du / kG) % kGrp]));
                     }
                     du += R::drains;
                 }
@@ -600,15 +596,19 @@ __global__ void __launch_bounds__(kTxThreads, 1)
         uint32_t du = 0;
         long long rg = 0;
         bool ok = true;
-        auto acc_wait = [&](uint32_t d) {
-            ok = mbar_wait(smem_u32(&acc_full[d % kAcc]), (uint32_t)((d / kAcc) & 1), flags, p.err);
+        // a super-block's group: wait for it, then the columns of its two accumulators
+        auto grp_wait = [&](uint32_t d) {
+            ok = mbar_wait(smem_u32(&acc_full[(d / kG) % kGrp]), (uint32_t)((d / kAcc) & 1), flags, p.err);
             return tmem + tq + (uint32_t)((d % kAcc) * NX + CW * cq);
         };
-        auto acc_release = [&](uint32_t d) {
+        auto grp_release = [&](uint32_t d) {  // after the group's last TMEM load completed
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&acc_empty[d % kAcc]));
+            if (lane == 0) mbar_arrive(smem_u32(&acc_empty[(d / kG) % kGrp]));
         };
+        // 8-column pieces a super-block's drain loads per TMEM round trip: all of them
+        // at 64-row tiles, one at a time at 128 (the running sums hold 2 CW registers)
+        constexpr int kH = NX == 64 ? CW / 8 : 1;
         for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
             int r0, r1;
             {
@@ -663,21 +663,30 @@ __global__ void __launch_bounds__(kTxThreads, 1)
                 } else if (WT == T_Q6_K) {
                     // y += d_a f(d) S with S = 16 S_a + S_b (S_a, S_b exact integers in f32;
                     // 16 S_a exact, the sum rounded once, relative to |S|)
-                    const uint32_t ca = acc_wait(du);
-                    const uint32_t cb = ok ? acc_wait(du + 1) : 0u;
+                    const uint32_t ca = grp_wait(du);
+                    const uint32_t cb = ca + NX;  // the group's second accumulator (du is even)
                     if (!ok) break;
                     tc_fence_after();
                     __syncwarp();
                     const float fd = h2f(*reinterpret_cast<const uint16_t*>(wrow + 208));
                     const unsigned long long fd2 = f2pack(fd, fd), k16 = f2pack(16.0f, 16.0f);
 #pragma unroll
-                    for (int h = 0; h < CW / 8; ++h) {  // 8 columns at a time: the running sums hold 2 CW registers
-                        uint32_t va[8], vb[8];
-                        tcx_ld8(ca + 8 * h, va);
-                        tcx_ld8(cb + 8 * h, vb);
+                    for (int h0 = 0; h0 < CW / 8; h0 += kH) {
+                        uint32_t vA[kH][8], vB[kH][8];
+#pragma unroll
+                        for (int hh = 0; hh < kH; ++hh) {
+                            tcx_ld8(ca + 8 * (h0 + hh), vA[hh]);
+                            tcx_ld8(cb + 8 * (h0 + hh), vB[hh]);
+                        }
                         tc_wait_ld();
+                        if (h0 + kH >= CW / 8) grp_release(du);
+#pragma unroll
+                        for (int hh = 0; hh < kH; ++hh)
 #pragma unroll
                         for (int c = 0; c < 2; ++c) {
+                            const int h = h0 + hh;
+                            const uint32_t* va = vA[hh];
+                            const uint32_t* vb = vB[hh];
                             const float4 a4 = kF32 ? make_float4(1.0f, 1.0f, 1.0f, 1.0f)  // f32_act: 2^-s at the store
                                                    : *reinterpret_cast<const float4*>(asc + 8 * h + 4 * c);
 #pragma unroll
@@ -690,13 +699,11 @@ __global__ void __launch_bounds__(kTxThreads, 1)
                             }
                         }
                     }
-                    acc_release(du);
-                    acc_release(du + 1);
                     du += 2;
                 } else {
                     // y += d_a (f(d) S_sc - f(dmin) S_m): S_sc and S_m exact integers in f32
-                    const uint32_t ca = acc_wait(du);
-                    const uint32_t cm = ok ? acc_wait(du + 1) : 0u;
+                    const uint32_t ca = grp_wait(du);
+                    const uint32_t cm = ca + NX;  // the group's second accumulator (du is even)
                     if (!ok) break;
                     tc_fence_after();
                     __syncwarp();
@@ -705,13 +712,22 @@ __global__ void __launch_bounds__(kTxThreads, 1)
                     const float fm = -h2f(dd >> 16) * (kF32 ? 16.0f : 1.0f);
                     const unsigned long long fd2 = f2pack(h2f(dd), h2f(dd)), fm2 = f2pack(fm, fm);
 #pragma unroll
-                    for (int h = 0; h < CW / 8; ++h) {  // 8 columns at a time: the running sums hold 2 CW registers
-                        uint32_t vs[8], vm[8];
-                        tcx_ld8(ca + 8 * h, vs);
-                        tcx_ld8(cm + 8 * h, vm);
+                    for (int h0 = 0; h0 < CW / 8; h0 += kH) {
+                        uint32_t vS[kH][8], vM[kH][8];
+#pragma unroll
+                        for (int hh = 0; hh < kH; ++hh) {
+                            tcx_ld8(ca + 8 * (h0 + hh), vS[hh]);
+                            tcx_ld8(cm + 8 * (h0 + hh), vM[hh]);
+                        }
                         tc_wait_ld();
+                        if (h0 + kH >= CW / 8) grp_release(du);
+#pragma unroll
+                        for (int hh = 0; hh < kH; ++hh)
 #pragma unroll
                         for (int c = 0; c < 2; ++c) {
+                            const int h = h0 + hh;
+                            const uint32_t* vs = vS[hh];
+                            const uint32_t* vm = vM[hh];
                             if constexpr (kF32) {
                                 // y 2^s += f(d) S_sc - f(dmin) S_m (sums of x 2^s, 2^-s applied at the store)
 #pragma unroll
@@ -735,8 +751,6 @@ __global__ void __launch_bounds__(kTxThreads, 1)
                             }
                         }
                     }
-                    acc_release(du);
-                    acc_release(du + 1);
                     du += 2;
                 }
                 if (!ok) break;
