@@ -346,6 +346,24 @@ def test_prefill_split_k_is_deterministic(qmm, orc, wtype, M, N, K):
     check_device_error(qmm)
 
 
+@pytest.mark.parametrize("wtype,M,N,K", [("q8_0", 40, 25600, 512), ("q4_k", 40, 25600, 512), ("q6_k", 40, 25600, 512),
+                                        ("q5_0", 40, 25600, 512), ("q8_0", 200, 12800, 512), ("q4_k", 200, 12800, 512)])
+def test_prefill_ctas_take_several_tiles(qmm, orc, wtype, M, N, K):
+    """More output tiles than SMs (200 tiles of 128 weight rows): the
+    persistent tcgen05 CTAs take several tiles each, so the accumulator and
+    stage rings (and their barrier phases) carry over from one tile to the
+    next, at 64- and 128-row activation tiles, in both forms."""
+    w = qmm_synth.weights(N, K, seed=5)
+    x_np = qmm_synth.activations(M, K, seed=6, outlier_channels=4)
+    wq_h = orc.quantize(wtype, w)
+    wq, x = dev(wq_h), dev(x_np)
+    for mode in ("int8_act", "f32_act"):
+        y = matmul_checked(qmm, wq, x, wtype, mode, N)
+        y_orc, T = orc.matmul(wtype, mode, wq_h, x_np)
+        assert_within_bound(y, y_orc, T, f"{wtype} {mode} M{M} N{N} K{K}")
+    check_device_error(qmm)
+
+
 def test_gap_ordering(qmm, orc):
     """The CPU form's distance to the dequantized-f32 product is far larger
     than the Metal form's (the activation-quantization error; the pages put
