@@ -429,11 +429,12 @@ __global__ void __launch_bounds__(kTxThreads, 1)
     constexpr int kSpr = 8 / kBps;          // block stages per raw stage
     // Drain groups: accumulators handed from the MMAs to the epilogue with one
     // commit and returned with one release (barriers 0 .. kGrp - 1).  A super-block's
-    // two (Q4_K S_sc and S_m, Q6_K S_a and S_b) are one group; so are two
-    // consecutive 32-value blocks at 64-row tiles, whose epilogue loads both before
-    // one wait; 128-row tiles, with half as many accumulators and twice the columns,
-    // hand each 32-value block over alone.
-    constexpr int kG = kB32 && NX == 128 ? 1 : 2;
+    // two (Q4_K S_sc and S_m, Q6_K S_a and S_b) are one group; so are a block
+    // stage's 32-value blocks at 64-row tiles (two or four), whose epilogue loads
+    // two of them before each wait; 128-row tiles, with half as many accumulators
+    // and twice the columns, hand each 32-value block over alone.
+    constexpr int kG = kB32 ? (NX == 128 ? 1 : kBps) : 2;
+    constexpr int kL = kB32 && NX == 128 ? 1 : 2;  // 32-value blocks per TMEM load round trip
     constexpr int kGrp = kAcc / kG;
     static_assert(kBps % kG == 0 && kAcc % kG == 0, "accumulator groups");
     auto raw = [&](int s) { return sm + p.off_raw + s * R::slot; };
@@ -628,23 +629,27 @@ __global__ void __launch_bounds__(kTxThreads, 1)
                         if (!ok) break;
                         tc_fence_after();
                         __syncwarp();
-                        uint32_t vv[kG][CW];
 #pragma unroll
-                        for (int b = 0; b < kG; ++b) {
-                            const uint32_t acol = tmem + tq + (uint32_t)(((du + b) % kAcc) * NX + CW * cq);
+                        for (int l0 = 0; l0 < kG; l0 += kL) {  // kL blocks per TMEM load round trip
+                        uint32_t vv[kL][CW];
+#pragma unroll
+                        for (int b = 0; b < kL; ++b) {
+                            const uint32_t acol = tmem + tq + (uint32_t)(((du + l0 + b) % kAcc) * NX + CW * cq);
 #pragma unroll
                             for (int h = 0; h < CW / 16; ++h) tc_ld16(acol + 16 * h, vv[b] + 16 * h);
                         }
                         tc_wait_ld();
-                        tc_fence_before();  // the group's accumulators go back to the MMAs
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(smem_u32(&acc_empty[(du / kG) % kGrp]));
+                        if (l0 + kL >= kG) {
+                            tc_fence_before();  // the group's accumulators go back to the MMAs
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(smem_u32(&acc_empty[(du / kG) % kGrp]));
+                        }
 #pragma unroll
-                        for (int b = 0; b < kG; ++b) {
+                        for (int b = 0; b < kL; ++b) {
                             // fold: y += isum f(d_w) f(d_a)
-                            const float dw = tcx_block_scale<R::bb>(wrow, j + b);
+                            const float dw = tcx_block_scale<R::bb>(wrow, j + l0 + b);
                             const unsigned long long dw2 = f2pack(dw, dw);
-                            const float* aj = asc + (j + b) * NX;
+                            const float* aj = asc + (j + l0 + b) * NX;
 #pragma unroll
                             for (int c = 0; c < CW / 4; ++c) {
                                 const uint32_t* v = vv[b] + 4 * c;
@@ -658,6 +663,7 @@ __global__ void __launch_bounds__(kTxThreads, 1)
                                     acc[2 * c + 1] = fma2(f2pack(__uint_as_float(v[2]), __uint_as_float(v[3])), s23, acc[2 * c + 1]);
                                 }
                             }
+                        }
                         }
                     }
                 } else if (WT == T_Q6_K) {
