@@ -505,6 +505,10 @@ __global__ void __launch_bounds__(kTxThreads, 1)
         // ------------------------------ MMA issuer ------------------------------
         if (lane == 0) {
             const uint32_t idesc = tc_idesc(NX);
+            // shared-memory descriptors of stage 0's weight and activation tiles, split in
+            // their 32-bit halves; the high half is the same for every 128-byte-swizzled tile
+            const uint64_t d0w = tc_sdesc128(smem_u32(wstage(0))), d0x = tc_sdesc128(smem_u32(xstage(0)));
+            const uint32_t wlo0 = (uint32_t)d0w, xlo0 = (uint32_t)d0x, dhi = (uint32_t)(d0w >> 32);
             long long g = 0, rg = 0;  // blocks; raw stages
             uint32_t du = 0;          // drain units (a launch drains far fewer than 2^32)
             bool ok = true;
@@ -536,22 +540,24 @@ __global__ void __launch_bounds__(kTxThreads, 1)
                         if (!ready) ok = mbar_wait(smem_u32(&full[s]), (uint32_t)((g / kTxS) & 1), flags, p.err);
                         if (!ok) break;
                         tc_fence_after();
-                        const uint32_t wa = smem_u32(wstage(s)), xb = smem_u32(xstage(s));
+                        // the stage's descriptors: the base's, plus the byte offset / 16 in the
+                        // start-address field (no carry: shared addresses are below 2^18)
+                        const uint32_t wlo = wlo0 + (uint32_t)s * (R::stage(NX) >> 4), xlo = xlo0 + (uint32_t)s * (R::stage(NX) >> 4);
+                        auto desc = [&](uint32_t lo, uint32_t off) { return ((uint64_t)dhi << 32) | (lo + (off >> 4)); };
                         // K = 16 steps ks: atom ks / 4, 32 bytes each along its 128-byte swizzled rows
 #pragma unroll
                         for (int ks = 0; ks < 2 * kBps; ++ks) {
                             const uint32_t col = kB32 ? dq[ks >> 1] : dcol;
                             const uint32_t accu = kB32 ? (uint32_t)(ks & 1) : (uint32_t)(j | ks);
-                            const uint32_t wk = wa + (ks >> 2) * kTxW * 128 + 32 * (ks & 3);
-                            const uint32_t xk = xb + (ks >> 2) * NX * 128 + 32 * (ks & 3);
-                            tcx_mma(tmem + col, tc_sdesc128(wk), tc_sdesc128(xk), idesc, accu);
+                            const uint32_t wk = (ks >> 2) * kTxW * 128 + 32 * (ks & 3);
+                            const uint32_t xk = (ks >> 2) * NX * 128 + 32 * (ks & 3);
+                            tcx_mma(tmem + col, desc(wlo, wk), desc(xlo, xk), idesc, accu);
                             if (kF32)  // the lo piece into the same accumulator
-                                tcx_mma(tmem + col, tc_sdesc128(wk), tc_sdesc128(xk + (kBps / 2) * NX * 128), idesc, 1u);
+                                tcx_mma(tmem + col, desc(wlo, wk), desc(xlo, xk + (kBps / 2) * NX * 128), idesc, 1u);
                             if (WT == T_Q6_K) {
-                                tcx_mma(tmem + dcol2, tc_sdesc128(wk + R::wtile(NX)), tc_sdesc128(xk), idesc, accu);
+                                tcx_mma(tmem + dcol2, desc(wlo, wk + R::wtile(NX)), desc(xlo, xk), idesc, accu);
                                 if (kF32)
-                                    tcx_mma(tmem + dcol2, tc_sdesc128(wk + R::wtile(NX)),
-                                            tc_sdesc128(xk + (kBps / 2) * NX * 128), idesc, 1u);
+                                    tcx_mma(tmem + dcol2, desc(wlo, wk + R::wtile(NX)), desc(xlo, xk + (kBps / 2) * NX * 128), idesc, 1u);
                             }
                         }
                         tc_commit(smem_u32(&empty[s]));
