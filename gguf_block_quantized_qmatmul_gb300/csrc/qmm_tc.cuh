@@ -521,6 +521,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // ------------------------------ MMA issuer ------------------------------
         if (lane == 0) {
             const uint32_t idesc = tc_idesc(p.bx);
+            // stage 0's hi-piece descriptor in its 32-bit halves: a stage's and a K step's
+            // offsets / 16 add to the start-address field (shared addresses are below 2^18)
+            const uint64_t d0 = tc_sdesc128(smem_u32(stage(0)));
+            const uint32_t lo0 = (uint32_t)d0, dhi = (uint32_t)(d0 >> 32);
             long long g = 0;
             int cc = 0;  // accumulation chunks issued
             bool ok = true;
@@ -542,7 +546,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     if (!ready) ok = mbar_wait(smem_u32(&full[s]), (uint32_t)((g / kTcS) & 1), flags, p.err);
                     if (!ok) break;
                     tc_fence_after();
-                    const uint32_t xhi = smem_u32(stage(s)), xlo = xhi + (uint32_t)p.piece;
+                    const uint32_t xhi = lo0 + (uint32_t)((s * 2 * p.piece) >> 4), xlo = xhi + (uint32_t)(p.piece >> 4);
                     const uint32_t whi = tmem + (uint32_t)(kTcWCol0 + 64 * s), wlo = whi + 32;
 #pragma unroll
                     for (int pass = 0; pass < 3; ++pass) {
@@ -550,7 +554,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         const uint32_t wa = pass == 2 ? wlo : whi, xb = pass == 1 ? xlo : xhi;
 #pragma unroll
                         for (int kk = 0; kk < kTcBK / 16; ++kk)
-                            tc_mma(dt, wa + 8 * kk, tc_sdesc128(xb + 32 * kk), idesc, (i | pass | kk) != 0 ? 1u : 0u);
+                            tc_mma(dt, wa + 8 * kk, ((uint64_t)dhi << 32) | (xb + 2 * kk), idesc, (i | pass | kk) != 0 ? 1u : 0u);
                     }
                     tc_commit(smem_u32(&empty[s]));
                     ready = nxt;
