@@ -637,39 +637,39 @@ __global__ void __launch_bounds__(kTxThreads, 1)
                         __syncwarp();
 #pragma unroll
                         for (int l0 = 0; l0 < kG; l0 += kL) {  // kL blocks per TMEM load round trip
-                        uint32_t vv[kL][CW];
+                            uint32_t vv[kL][CW];
 #pragma unroll
-                        for (int b = 0; b < kL; ++b) {
-                            const uint32_t acol = tmem + tq + (uint32_t)(((du + l0 + b) % kAcc) * NX + CW * cq);
+                            for (int b = 0; b < kL; ++b) {
+                                const uint32_t acol = tmem + tq + (uint32_t)(((du + l0 + b) % kAcc) * NX + CW * cq);
 #pragma unroll
-                            for (int h = 0; h < CW / 16; ++h) tc_ld16(acol + 16 * h, vv[b] + 16 * h);
-                        }
-                        tc_wait_ld();
-                        if (l0 + kL >= kG) {
-                            tc_fence_before();  // the group's accumulators go back to the MMAs
-                            __syncwarp();
-                            if (lane == 0) mbar_arrive(smem_u32(&acc_empty[(du / kG) % kGrp]));
-                        }
+                                for (int h = 0; h < CW / 16; ++h) tc_ld16(acol + 16 * h, vv[b] + 16 * h);
+                            }
+                            tc_wait_ld();
+                            if (l0 + kL >= kG) {
+                                tc_fence_before();  // the group's accumulators go back to the MMAs
+                                __syncwarp();
+                                if (lane == 0) mbar_arrive(smem_u32(&acc_empty[(du / kG) % kGrp]));
+                            }
 #pragma unroll
-                        for (int b = 0; b < kL; ++b) {
-                            // fold: y += isum f(d_w) f(d_a)
-                            const float dw = tcx_block_scale<R::bb>(wrow, j + l0 + b);
-                            const unsigned long long dw2 = f2pack(dw, dw);
-                            const float* aj = asc + (j + l0 + b) * NX;
+                            for (int b = 0; b < kL; ++b) {
+                                // fold: y += isum f(d_w) f(d_a)
+                                const float dw = tcx_block_scale<R::bb>(wrow, j + l0 + b);
+                                const unsigned long long dw2 = f2pack(dw, dw);
+                                const float* aj = asc + (j + l0 + b) * NX;
 #pragma unroll
-                            for (int c = 0; c < CW / 4; ++c) {
-                                const uint32_t* v = vv[b] + 4 * c;
-                                if constexpr (kF32) {  // y 2^s += S f(d_w) (sums of x 2^s)
-                                    acc[2 * c] = fma2(f2pack(__uint_as_float(v[0]), __uint_as_float(v[1])), dw2, acc[2 * c]);
-                                    acc[2 * c + 1] = fma2(f2pack(__uint_as_float(v[2]), __uint_as_float(v[3])), dw2, acc[2 * c + 1]);
-                                } else {
-                                    const float4 a4 = *reinterpret_cast<const float4*>(aj + 4 * c);
-                                    const unsigned long long s01 = mul2(f2pack(a4.x, a4.y), dw2), s23 = mul2(f2pack(a4.z, a4.w), dw2);
-                                    acc[2 * c] = fma2(f2pack(__uint_as_float(v[0]), __uint_as_float(v[1])), s01, acc[2 * c]);
-                                    acc[2 * c + 1] = fma2(f2pack(__uint_as_float(v[2]), __uint_as_float(v[3])), s23, acc[2 * c + 1]);
+                                for (int c = 0; c < CW / 4; ++c) {
+                                    const uint32_t* v = vv[b] + 4 * c;
+                                    if constexpr (kF32) {  // y 2^s += S f(d_w) (sums of x 2^s)
+                                        acc[2 * c] = fma2(f2pack(__uint_as_float(v[0]), __uint_as_float(v[1])), dw2, acc[2 * c]);
+                                        acc[2 * c + 1] = fma2(f2pack(__uint_as_float(v[2]), __uint_as_float(v[3])), dw2, acc[2 * c + 1]);
+                                    } else {
+                                        const float4 a4 = *reinterpret_cast<const float4*>(aj + 4 * c);
+                                        const unsigned long long s01 = mul2(f2pack(a4.x, a4.y), dw2), s23 = mul2(f2pack(a4.z, a4.w), dw2);
+                                        acc[2 * c] = fma2(f2pack(__uint_as_float(v[0]), __uint_as_float(v[1])), s01, acc[2 * c]);
+                                        acc[2 * c + 1] = fma2(f2pack(__uint_as_float(v[2]), __uint_as_float(v[3])), s23, acc[2 * c + 1]);
+                                    }
                                 }
                             }
-                        }
                         }
                     }
                 } else if (WT == T_Q6_K) {
